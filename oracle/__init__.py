@@ -1,0 +1,200 @@
+"""CPU oracle for the paired 3D RoPE of the LTX-2.5 diffusion decoder.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline / reference leg of ``bench.py`` import this package. The product
+library (``rope_rope3d_apply_gb300``) never imports it and shares no code with
+it; the two meet only through the seeded inputs of the ``synthetic`` package.
+
+The arithmetic lives in ``rope3d_oracle.c`` (plain C, built with
+``-ffp-contract=off``); this module compiles it with gcc and wraps it with
+ctypes over numpy arrays. What each function follows is cited in the C file:
+sglang PR #35698 review ("fused LTX-2.5 decoder 3D RoPE"), sections
+"实现拆解" (steps 1 and 2) and "关键源码片段" (the rotate_pair arithmetic, the
+kernel's index decode and the wrapper's preflight).
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, exact-rational rounding, a float64 complex brute force,
+high-precision table values, invariants and planted-mistake checks).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rope3d_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "librope3d_oracle.so")
+
+# Flags: no contraction into fused multiply-add, no fast-math, IEEE defaults.
+CFLAGS = ["-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(out_path: str = _LIB_PATH, extra_flags: list[str] | None = None) -> str:
+    """Compile the oracle with gcc; returns the path of the shared library."""
+    os.makedirs(os.path.dirname(out_path), exist_ok=True)
+    tmp = out_path + f".tmp{os.getpid()}"
+    cmd = ["gcc", *CFLAGS, *(extra_flags or []), _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out_path)
+    return out_path
+
+
+def _declare(lib):
+    i64, f32p = ctypes.c_int64, ctypes.c_void_p
+    vp = ctypes.c_void_p
+    lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_f32.restype = ctypes.c_float
+    lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_axis_table.argtypes = [i64, i64, ctypes.c_double, f32p, f32p]
+    lib.oracle_axis_table.restype = ctypes.c_int
+    lib.oracle_rotate_pair_f32.argtypes = [ctypes.c_float] * 4 + [vp, vp]
+    lib.oracle_rotate_pair_f32.restype = None
+    full = [vp, vp] + [i64] * 6 + [vp] + [vp] * 6
+    lib.oracle_rope3d_bf16.argtypes = full
+    lib.oracle_rope3d_bf16.restype = ctypes.c_int
+    lib.oracle_rope3d_f32.argtypes = full
+    lib.oracle_rope3d_f32.restype = ctypes.c_int
+    at = [vp, vp, i64, vp] + [i64] * 6 + [vp] + [vp] * 6
+    lib.oracle_rope3d_bf16_at.argtypes = at
+    lib.oracle_rope3d_bf16_at.restype = ctypes.c_int
+    lib.oracle_rope3d_f32_at.argtypes = at
+    lib.oracle_rope3d_f32_at.restype = ctypes.c_int
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the oracle library. ``path`` loads a
+    separately built copy, e.g. one compiled with a planted mistake."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH) or (
+                os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+            ):
+                build()
+            _lib = _declare(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _split_arr(split) -> np.ndarray:
+    s = np.asarray(split, dtype=np.int32)
+    if s.shape != (3,):
+        raise ValueError("split must have three entries (d_T, d_H, d_W)")
+    return np.ascontiguousarray(s)
+
+
+# ---------------------------------------------------------------------------
+# scalar conversions
+# ---------------------------------------------------------------------------
+
+def bf16_to_f32(bits: int, lib=None) -> float:
+    return (lib or load()).oracle_bf16_to_f32(int(bits))
+
+
+def f32_to_bf16(value: float, lib=None) -> int:
+    return int((lib or load()).oracle_f32_to_bf16(float(np.float32(value))))
+
+
+def rotate_pair(even: float, odd: float, c: float, s: float, lib=None):
+    """One pair in the eager order; returns float32 (y_even, y_odd)."""
+    y = np.zeros(2, dtype=np.float32)
+    (lib or load()).oracle_rotate_pair_f32(
+        float(np.float32(even)), float(np.float32(odd)),
+        float(np.float32(c)), float(np.float32(s)),
+        _ptr(y), _ptr(y) + 4)
+    return y[0], y[1]
+
+
+# ---------------------------------------------------------------------------
+# tables
+# ---------------------------------------------------------------------------
+
+def axis_table(length: int, dim: int, base: float = 10000.0, lib=None):
+    """(cos, sin) float32 arrays of shape [length, dim // 2]."""
+    c = np.empty((length, dim // 2), dtype=np.float32)
+    s = np.empty((length, dim // 2), dtype=np.float32)
+    rc = (lib or load()).oracle_axis_table(length, dim, float(base), _ptr(c), _ptr(s))
+    if rc != 0:
+        raise ValueError(f"oracle_axis_table rejected length={length} dim={dim} base={base}")
+    return c, s
+
+
+def tables(T: int, H: int, W: int, split, base: float = 10000.0, lib=None):
+    """((cos_t, sin_t), (cos_h, sin_h), (cos_w, sin_w))."""
+    return tuple(axis_table(n, d, base, lib) for n, d in zip((T, H, W), split))
+
+
+def _table_args(tabs):
+    flat = []
+    for c, s in tabs:
+        flat += [np.ascontiguousarray(c, dtype=np.float32),
+                 np.ascontiguousarray(s, dtype=np.float32)]
+    return flat
+
+
+# ---------------------------------------------------------------------------
+# the rotation
+# ---------------------------------------------------------------------------
+
+def rope3d(x: np.ndarray, shape, split, tabs, lib=None) -> np.ndarray:
+    """Full oracle pass.
+
+    x: uint16 (bf16 bit patterns) or float32 array with B*T*H*W*heads*head_dim
+    elements in [B, T, H, W, heads, head_dim] order. shape = (B, T, H, W,
+    heads, head_dim). Returns an array of the same dtype and shape as x.
+    """
+    lib = lib or load()
+    B, T, H, W, heads, head_dim = (int(v) for v in shape)
+    x = np.ascontiguousarray(x)
+    if x.size != B * T * H * W * heads * head_dim:
+        raise ValueError("x does not match shape")
+    y = np.empty_like(x)
+    sp = _split_arr(split)
+    tb = _table_args(tabs)
+    if x.dtype == np.uint16:
+        fn = lib.oracle_rope3d_bf16
+    elif x.dtype == np.float32:
+        fn = lib.oracle_rope3d_f32
+    else:
+        raise TypeError("x must be uint16 (bf16 bits) or float32")
+    rc = fn(_ptr(x), _ptr(y), B, T, H, W, heads, head_dim, _ptr(sp), *[_ptr(t) for t in tb])
+    if rc != 0:
+        raise ValueError(f"oracle rejected shape={shape} split={tuple(split)}")
+    return y
+
+
+def rope3d_at(x: np.ndarray, indices: np.ndarray, shape, split, tabs, lib=None) -> np.ndarray:
+    """Output elements at the given flat indices, computed one at a time."""
+    lib = lib or load()
+    B, T, H, W, heads, head_dim = (int(v) for v in shape)
+    x = np.ascontiguousarray(x).reshape(-1)
+    idx = np.ascontiguousarray(indices, dtype=np.int64)
+    out = np.empty(idx.size, dtype=x.dtype)
+    sp = _split_arr(split)
+    tb = _table_args(tabs)
+    if x.dtype == np.uint16:
+        fn = lib.oracle_rope3d_bf16_at
+    elif x.dtype == np.float32:
+        fn = lib.oracle_rope3d_f32_at
+    else:
+        raise TypeError("x must be uint16 (bf16 bits) or float32")
+    rc = fn(_ptr(x), _ptr(idx), idx.size, _ptr(out), B, T, H, W, heads, head_dim,
+            _ptr(sp), *[_ptr(t) for t in tb])
+    if rc != 0:
+        raise ValueError("oracle rejected the sample request")
+    return out
