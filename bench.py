@@ -1,0 +1,427 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused paired 3D RoPE (Q and K) on GB300.
+
+One step is one rotation of Q and K (one rope3d_apply_pair call, one kernel
+launch) over the largest single-GPU workload: B=2, T=24, H=96, W=96
+(221,184 tokens per batch), 24 heads, head_dim 128, split (32, 48, 48),
+base 10000, bf16 values N(0, 1) from seed 4. Each step moves 10.87 GB
+(read Q and K, write Q_out and K_out, read the tables once): far more than
+the 129 MB L2, so no flush is needed between steps.
+
+Metric: achieved HBM GB/s from algorithmic bytes (and the fraction of the
+measured peak), plus tokens*heads per second. Printed as one JSON line.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
+
+--impl reference times the CPU oracle (single thread, as it stands) on a
+bounded sample of the same workload: each step rotates Q and K of the first
+frame(s) of batch 0.
+Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
+rotation needs no exchange): the value is all ranks' bytes over the slowest
+rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+METRIC = "fused 3D RoPE Q+K: achieved HBM GB/s and % of GB300 peak; bit-exact vs oracle"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = [
+    os.path.join(ROOT, "rope_rope3d_apply_gb300", "csrc", "rope3d_kernels.cu"),
+    os.path.join(ROOT, "rope_rope3d_apply_gb300", "csrc", "rope3d_internal.h"),
+]
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "rope3d_vec16_bf16_large.md")
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="large", choices=sorted(synthetic.WORKLOADS))
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle baseline sample")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def workload_config(w: synthetic.Workload) -> dict:
+    return {
+        "workload": (f"{w.name}: B={w.B}, T={w.T}, H={w.H}, W={w.W} (N={w.N}), heads={w.heads}, "
+                     f"head_dim={w.head_dim}, split={tuple(w.split)}, base={w.base:g}, "
+                     f"{w.dtype} N(0,{w.sigma:g}) seed {w.seed}"),
+        "B": w.B, "T": w.T, "H": w.H, "W": w.W, "heads": w.heads, "head_dim": w.head_dim,
+        "split": list(w.split), "io_dtype": w.dtype,
+        "bytes_per_step": w.bytes_per_call,
+        "token_heads_per_step": w.token_heads,
+        "l2": ("no flush: each step reads and writes %.2f GB, far more than the 129 MB L2"
+               % (w.bytes_per_call / 1e9)) if w.bytes_per_call > 1 << 30 else
+              "inputs smaller than L2: numbers include L2 reuse",
+    }
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch(w: synthetic.Workload):
+    """DRAM bytes per launch from the committed ncu summary, when it was taken
+    on the current kernel source; otherwise None."""
+    try:
+        text = open(TRAFFIC_SUMMARY).read()
+    except OSError:
+        return None
+    src = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    per_byte = re.search(r"dram_bytes_per_algorithmic_byte:\s*([0-9.]+)", text)
+    if not src or not per_byte or src.group(1) != kernel_source_hash():
+        return None
+    return int(float(per_byte.group(1)) * w.bytes_per_call)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.samples = []  # (time, sm_mhz, max_mhz, reasons)
+        self._proc = None
+        self._thread = None
+
+    def start(self):
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self._proc = None
+            return
+        self._thread = threading.Thread(target=self._read, daemon=True)
+        self._thread.start()
+
+    def _read(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self._proc.stdout:
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            reasons = [n for n, v in zip(names, parts[5:9]) if v.lower().startswith("active")]
+            self.samples.append((time.time(), sm, mx, reasons))
+
+    def stop(self):
+        if self._proc:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+        if self._thread:
+            self._thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        used = inside
+        if not used and self.samples:
+            # the timed region was shorter than the sampling period: nearest sample
+            mid = 0.5 * (t0 + t1)
+            used = [min(self.samples, key=lambda s: abs(s[0] - mid))]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({r for s in used for r in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in used),
+                "sm_max_mhz": max(s[2] for s in used), "reasons": reasons,
+                "samples": len(used), "samples_in_window": len(inside)}
+
+
+def launches_per_call(w: synthetic.Workload, kernel: int) -> int:
+    """Kernel launches of one call: one per 2^30 work units (16-byte vectors or
+    pairs), whole rows per launch."""
+    per_unit = (16 // w.elem_bytes) if kernel == 1 else 2
+    units_per_row = w.heads * w.head_dim // per_unit
+    rows_per_launch = max(1, (1 << 30) // units_per_row)
+    rows = w.B * w.N
+    return -(-rows // rows_per_launch)
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The slowest rank's time (a no-op on one process)."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def smi_gpu_id(local: int) -> str:
+    """nvidia-smi --id for CUDA device `local` (by PCI bus id when known)."""
+    try:
+        import torch
+
+        p = torch.cuda.get_device_properties(local)
+        return "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v for v in vis.split(",") if v.strip()]
+        return ids[local] if local < len(ids) else str(local)
+
+
+def oracle_sample_step(w: synthetic.Workload, frames: int, rows: int, cache: dict):
+    """One oracle pass over Q and K of a leading sub-grid of batch 0: the first
+    `rows` rows (h) of frame 0 when frames == 1, else the first `frames` whole
+    frames. Those tokens use the same table rows as in the full workload, so
+    the sub-grid is the same computation as that part of the workload.
+    Returns the algorithmic bytes of the pass."""
+    import oracle
+
+    key = (frames, rows)
+    if key not in cache:
+        shape = (1, frames, rows, w.W, w.heads, w.head_dim)
+        n = int(np.prod(shape))
+        q = synthetic.normal(n, w.sigma, w.seed, 0, w.dtype)
+        k = synthetic.normal(n, w.sigma, w.seed, 1, w.dtype)
+        tabs = oracle.tables(frames, rows, w.W, w.split, w.base)
+        cache[key] = (shape, q, k, tabs)
+    shape, q, k, tabs = cache[key]
+    oracle.rope3d(q, shape, w.split, tabs)
+    oracle.rope3d(k, shape, w.split, tabs)
+    return 4 * q.size * w.elem_bytes + sum(8 * n * (d // 2) for n, d in zip(shape[1:4], w.split))
+
+
+def cpu_baseline(w: synthetic.Workload, seconds: float) -> dict:
+    """The oracle as it stands, single-threaded, on the first frames of batch 0."""
+    cache = {}
+    t0 = time.perf_counter()
+    oracle_sample_step(w, 1, w.H, cache)  # one frame first, to size the sample
+    one = time.perf_counter() - t0
+    frames = int(max(1, min(w.T, seconds / max(one, 1e-3))))
+    cache.clear()
+    t0 = time.perf_counter()
+    moved = oracle_sample_step(w, frames, w.H, cache)
+    dt = time.perf_counter() - t0
+    return {"value": moved / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": (f"frames 0..{frames - 1} of batch 0 ({frames * w.H * w.W} tokens x {w.heads} heads, "
+                       f"Q and K, {moved / 1e9:.3f} GB algorithmic) in {dt:.2f} s, one thread")}
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+
+def run_reference(args, w):
+    """The oracle timed on the host cores; each step a bounded sample (leading
+    rows of frame 0 of batch 0) sized so that warm-up and timed steps together
+    take about two minutes."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    cache = {}
+    oracle_sample_step(w, 1, 1, cache)  # inputs drawn once, outside the estimate
+    t0 = time.perf_counter()
+    oracle_sample_step(w, 1, 1, cache)
+    per_row = time.perf_counter() - t0
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(w.H, budget / max(per_row, 1e-6))))
+    for _ in range(max(args.warmup, 0)):
+        oracle_sample_step(w, 1, rows, cache)
+    t0 = time.perf_counter()
+    moved = 0
+    for _ in range(args.steps):
+        moved += oracle_sample_step(w, 1, rows, cache)
+    dt = time.perf_counter() - t0
+    value = moved / dt / 1e9
+    sample = (f"each step: rows h=0..{rows - 1} of frame 0 of batch 0 ({rows * w.W} tokens x "
+              f"{w.heads} heads, Q and K), oracle single thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, w):
+    import torch
+
+    import rope_rope3d_apply_gb300 as r
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    r.load_library()
+
+    # inputs: pinned host buffers (also the end-to-end inputs), then device copies
+    np_dt = np.uint16 if w.dtype == "bf16" else np.float32
+    t_dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    shp = (w.B, w.N, w.heads, w.head_dim)
+    host = [torch.empty(w.numel * w.elem_bytes, dtype=torch.uint8).pin_memory() for _ in range(4)]
+    hq, hk, hqo, hko = (h.numpy().view(np_dt).reshape(shp) for h in host)
+    synthetic.qk(w, hq.reshape(-1), hk.reshape(-1))
+    q = host[0].to(dev).view(t_dtype).view(shp)
+    k = host[1].to(dev).view(t_dtype).view(shp)
+    qo = torch.empty_like(q)
+    ko = torch.empty_like(k)
+    tabs = r.rope3d_build_tables(w.T, w.H, w.W, w.split, w.base)
+    stream = torch.cuda.current_stream(dev)
+
+    # warm-up (the first call also runs the library's bit-exact gate)
+    for _ in range(max(args.warmup, 3)):
+        r.rope3d_apply_pair(q, k, tabs, qo, ko, stream=stream)
+    torch.cuda.synchronize(dev)
+    dt_code = r.BF16 if w.dtype == "bf16" else r.F32
+    verdict = r.rope3d_gate_verdict(w.B, w.T, w.H, w.W, w.heads, w.head_dim, w.split, w.base, dt_code)
+    launch = r.rope3d_last_launch()
+    launches_per_step = launches_per_call(w, launch["kernel"])
+
+    # timed region: exactly K steps, per-launch events on the launching stream
+    clocks = ClockSampler(smi_gpu_id(local))
+    clocks.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        r.rope3d_apply_pair(q, k, tabs, qo, ko, stream=stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    total_ms = starts[0].elapsed_time(ends[-1])
+    per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    time.sleep(0.25)
+    clocks.stop()
+    clk = clocks.summary(t_wall0, t_wall1)
+
+    total_ms = max_over_ranks(total_ms, dist, dev)
+
+    bytes_step = w.bytes_per_call
+    value = world * args.steps * bytes_step / (total_ms / 1e3) / 1e9
+    kernel_ms = statistics.fmean(per_launch)
+    achieved = bytes_step / (kernel_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+
+    # end to end through the host-buffer entry point (copies inside the timed region)
+    e2e = None
+    if not args.no_e2e:
+        r.rope3d_apply_pair_host(hq, hk, hqo, hko, tabs)  # warm-up: staging allocation
+        if dist:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            r.rope3d_apply_pair_host(hq, hk, hqo, hko, tabs)
+        e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
+        e2e = {"value": world * args.e2e_steps * bytes_step / e2e_s / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": 2 * w.numel * w.elem_bytes,
+               "d2h_bytes_per_step": 2 * w.numel * w.elem_bytes,
+               "steps": args.e2e_steps, "api": "rope3d_apply_pair_host (pinned host buffers)"}
+        r.rope3d_release_scratch()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": dict(workload_config(w), parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
+            "token_heads_per_s": world * args.steps * w.token_heads / (total_ms / 1e3),
+            "pct_of_peak_hbm": 100.0 * achieved / peak,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic_per_launch(w),
+                         "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
+                         "kernel_ms": kernel_ms},
+            "clocks": clk,
+            "gpu_launches": args.steps * launches_per_step,
+            "kernel": {"variant": {1: "vec16", 2: "pair"}.get(launch["kernel"], "?"),
+                       "grid": launch["grid"], "block": launch["block"]},
+            "gate_verdict": {0: "unseen", 1: "verified", 2: "refused"}[verdict],
+            "e2e": e2e,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    tabs.close()
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    w = synthetic.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,277 @@
+/*
+ * rope3d.h -- C ABI of the fused paired 3D rotary position embedding (RoPE)
+ * for GB300 (sm_103a).
+ *
+ * What it computes (sglang PR #35698 review, "fused LTX-2.5 decoder 3D RoPE",
+ * prhub.com.cn; sections "实现拆解" steps 1-4 and "关键源码片段"): before each
+ * attention block of the LTX-2.5 diffusion video decoder, Q and K of shape
+ * [B, T*H*W, heads, head_dim] (tokens row-major over the (T, H, W) grid) are
+ * rotated pair by pair. head_dim is split into three chunks
+ * split = (d_T, d_H, d_W); the chunk of axis X uses that axis's fp32 table
+ * (cos_X, sin_X) of shape [L_X, d_X/2] at the row given by the token's grid
+ * coordinate on X. Inside a chunk, pair j is channels (2j, 2j+1):
+ *     y_even = RN(RN(even*cos) - RN(odd*sin))
+ *     y_odd  = RN(RN(even*sin) + RN(odd*cos))
+ * in float32, four separately rounded products and no fused multiply-add,
+ * then a round-to-nearest-even cast back to the input dtype. Q and K share the
+ * table lookups and are rotated in one kernel launch.
+ *
+ * Threading: every function may be called from any host thread; the table
+ * cache and the verification gate are protected by one mutex.
+ * Errors: every int-returning function returns ROPE3D_OK (0) or a negative
+ * ROPE3D_ERR_* code; rope3d_status_string() names it. Nothing is written to
+ * any output when a call fails its checks. No call ever falls back to a CPU
+ * computation of the result.
+ */
+#ifndef ROPE3D_H
+#define ROPE3D_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ROPE3D_ABI_VERSION 1
+
+/* ---- status codes ------------------------------------------------------ */
+#define ROPE3D_OK            0
+#define ROPE3D_ERR_NULL     -1  /* a required pointer is NULL                     */
+#define ROPE3D_ERR_SHAPE    -2  /* a size <= 0, head_dim != d_T+d_H+d_W, a chunk
+                                   odd or <= 0, or a size beyond the limits below  */
+#define ROPE3D_ERR_DTYPE    -3  /* dtype is not ROPE3D_BF16 or ROPE3D_F32         */
+#define ROPE3D_ERR_ALIGN    -4  /* a Q/K/output pointer is not 4-byte aligned     */
+#define ROPE3D_ERR_ALIAS    -5  /* an output overlaps an input or the other output */
+#define ROPE3D_ERR_DEVICE   -6  /* a pointer is not memory of the expected kind on
+                                   the current device (see each function)          */
+#define ROPE3D_ERR_PARITY   -7  /* the verification gate found a mismatch for this
+                                   configuration; it stays refused until
+                                   rope3d_gate_reset()                            */
+#define ROPE3D_ERR_CUDA     -8  /* a CUDA runtime call or kernel launch failed    */
+#define ROPE3D_ERR_TABLES   -9  /* the table handle does not match (T, H, W, split) */
+#define ROPE3D_ERR_NOMEM   -10  /* a device or host allocation failed             */
+#define ROPE3D_ERR_ARG     -11  /* another argument is out of range               */
+
+/* ---- element types ----------------------------------------------------- */
+#define ROPE3D_BF16 0   /* bfloat16 in and out                                */
+#define ROPE3D_F32  1   /* float32 in and out (same steps, identity cast)     */
+
+/* ---- limits -------------------------------------------------------------- */
+#define ROPE3D_MAX_HEAD_DIM 4096   /* head_dim above this -> ROPE3D_ERR_SHAPE  */
+#define ROPE3D_TABLE_CACHE_CAP 16  /* FIFO table cache size ("实现拆解" step 1) */
+
+typedef struct rope3d_tables rope3d_tables;  /* opaque, refcounted */
+
+/*
+ * rope3d_build_tables -- the per-axis cos/sin tables of one (T, H, W) grid,
+ * through the table cache ("实现拆解" step 1: _axis_tables(length, dim) and
+ * _tables(); a module-level cache keyed on the grid, the split and the base,
+ * capped at 16 entries with first-in-first-out eviction, shared by every
+ * attention block).
+ *
+ * Table values: table X has [L_X][d_X/2] entries (L = T, H, W); entry
+ * (p, j) is cos / sin of p * base^(-2j/d_X), evaluated in double precision
+ * with the host C library and rounded once to float. (The pages give the
+ * shape and inputs of the table, not its formula; this is standard per-axis
+ * RoPE.)
+ *
+ *   T, H, W   grid extents, each in [1, 2^31)
+ *   split     (d_T, d_H, d_W), each even and > 0; the sum is head_dim
+ *   base      RoPE base, finite and > 0 (the decoder uses 10000)
+ *   stream    cudaStream_t (NULL = legacy default stream) on which the upload
+ *             of a newly built entry is ordered; later use on other streams is
+ *             safe because the call waits for that upload before returning
+ *   out       receives a handle that the caller owns one reference to
+ *
+ * A cache hit returns the existing entry (and does not refresh its age). When
+ * a 17th entry is inserted the oldest is unlinked from the cache; its memory
+ * is freed when its last reference is released, so handles stay valid.
+ * Device memory: one buffer per entry, allocated by the library.
+ * Errors: NULL, SHAPE, ARG (bad base), NOMEM, CUDA.
+ */
+int rope3d_build_tables(int64_t T, int64_t H, int64_t W, const int32_t split[3],
+                        double base, void *stream, rope3d_tables **out);
+
+/* Drop one reference. Returns ERR_NULL for NULL. */
+int rope3d_release_tables(rope3d_tables *tables);
+
+/* Add one reference (for callers that share a handle). */
+int rope3d_retain_tables(rope3d_tables *tables);
+
+/*
+ * rope3d_apply_pair -- rotate Q and K on the GPU in one kernel launch
+ * ("实现拆解" steps 3-4: fused_ltx25_decoder_rope writes Q_out and K_out in a
+ * single launch, after the preflight can_use_ltx25_decoder_rope and the
+ * first-seen bit-exact gate).
+ *
+ *   q, k          device pointers, [B, T, H, W, heads, head_dim] contiguous
+ *                 (the same memory as [B, T*H*W, heads, head_dim]), elements
+ *                 of type dtype, 4-byte aligned, on the current device
+ *   q_out, k_out  device pointers of the same shape and type, owned by the
+ *                 caller; each must overlap neither input nor the other output
+ *                 (q and k may overlap each other: they are only read)
+ *   tables        a handle from rope3d_build_tables for the same T, H, W and
+ *                 split
+ *   dtype         ROPE3D_BF16 or ROPE3D_F32
+ *   stream        cudaStream_t the kernel is launched on (NULL = default)
+ *
+ * The call is asynchronous on `stream`, except the first call for each
+ * configuration (dtype, B, T, H, W, heads, head_dim, split, base) while the
+ * gate is on (the default): that call waits for the kernel, copies Q, K and
+ * the outputs back to the host, recomputes the result on the CPU in the
+ * eager order and compares every element (equal bits; or both NaN). A match
+ * marks the configuration verified; a mismatch marks it refused and returns
+ * ROPE3D_ERR_PARITY now and on every later call (no fallback; the outputs of
+ * the refused call hold the kernel's result). So make the first call of a
+ * configuration outside CUDA graph capture, or turn the gate off.
+ *
+ * 16-byte-aligned pointers with head_dim and every chunk a multiple of 8 (bf16)
+ * or 4 (fp32) elements take the 16-byte vector kernel; any other valid input
+ * takes the per-pair kernel with the same arithmetic.
+ * Errors: NULL, SHAPE, DTYPE, ALIGN, ALIAS, DEVICE (a pointer that is not
+ * device or managed memory of the current device), TABLES, PARITY, CUDA.
+ */
+int rope3d_apply_pair(const void *q, const void *k, void *q_out, void *k_out,
+                      const rope3d_tables *tables,
+                      int64_t B, int64_t T, int64_t H, int64_t W,
+                      int64_t heads, int64_t head_dim, const int32_t split[3],
+                      int32_t dtype, void *stream);
+
+/*
+ * rope3d_apply_pair_host -- the same rotation for HOST buffers: the library
+ * streams Q and K to the GPU in token chunks, rotates each chunk with the same
+ * kernel, and streams Q_out and K_out back, overlapping the two copy
+ * directions with the kernel. Returns when the outputs are in host memory.
+ *
+ *   q, k, q_out, k_out  host pointers with the layout of rope3d_apply_pair;
+ *                       pinned (page-locked) memory gives full copy speed,
+ *                       pageable memory works but copies synchronously
+ *   other arguments     as for rope3d_apply_pair; `stream` orders the work
+ *                       after earlier work on it
+ *
+ * Scratch: device staging buffers owned by the library (allocated on first
+ * use, reused and grown as needed, freed by rope3d_release_scratch()).
+ * The gate applies as in rope3d_apply_pair, on the host buffers.
+ * Errors: as rope3d_apply_pair; DEVICE when a pointer is device memory;
+ * NOMEM when the staging buffers cannot be allocated.
+ */
+int rope3d_apply_pair_host(const void *q, const void *k, void *q_out, void *k_out,
+                           const rope3d_tables *tables,
+                           int64_t B, int64_t T, int64_t H, int64_t W,
+                           int64_t heads, int64_t head_dim, const int32_t split[3],
+                           int32_t dtype, void *stream);
+
+/* Free the staging buffers of rope3d_apply_pair_host (waits for the device). */
+int rope3d_release_scratch(void);
+
+/*
+ * rope3d_preflight -- the argument checks of rope3d_apply_pair without a
+ * launch ("关键源码片段", can_use_ltx25_decoder_rope: sizes > 0,
+ * head_dim == sum(split), every chunk even and > 0, 4-byte pointer alignment,
+ * table shapes (T, d_T/2), (H, d_H/2), (W, d_W/2); plus the overlap check).
+ * check_device = 0 skips the device-memory query, so the host-only checks can
+ * run without a GPU. Returns the status rope3d_apply_pair would return before
+ * launching.
+ */
+int rope3d_preflight(const void *q, const void *k, const void *q_out, const void *k_out,
+                     const rope3d_tables *tables,
+                     int64_t B, int64_t T, int64_t H, int64_t W,
+                     int64_t heads, int64_t head_dim, const int32_t split[3],
+                     int32_t dtype, int32_t check_device);
+
+/*
+ * rope3d_axis_table_host -- the host table builder alone: fills cos_out and
+ * sin_out (each [length][dim/2] floats, caller-owned host memory) with the
+ * values described under rope3d_build_tables. No GPU needed.
+ * Errors: NULL, SHAPE (length <= 0, dim <= 0 or odd), ARG (base).
+ */
+int rope3d_axis_table_host(int64_t length, int64_t dim, double base,
+                           float *cos_out, float *sin_out);
+
+/*
+ * rope3d_tables_info -- the key of a handle: dims = (T, H, W), split, base.
+ * Any output pointer may be NULL.
+ */
+int rope3d_tables_info(const rope3d_tables *tables, int64_t dims[3],
+                       int32_t split[3], double *base);
+
+/*
+ * rope3d_tables_read -- copy axis `axis` (0 = T, 1 = H, 2 = W) of a handle
+ * into caller-owned host arrays of [L_X][d_X/2] floats. from_device = 0 reads
+ * the library's host copy; 1 reads back the device copy the kernel uses.
+ * Errors: NULL, ARG (axis), CUDA.
+ */
+int rope3d_tables_read(const rope3d_tables *tables, int32_t axis, int32_t from_device,
+                       float *cos_out, float *sin_out);
+
+/* ---- table cache --------------------------------------------------------- */
+/* Counters since the last rope3d_cache_clear(); any pointer may be NULL. */
+int rope3d_cache_stats(int64_t *entries, int64_t *hits, int64_t *misses,
+                       int64_t *evictions);
+/* Unlink every entry (held handles stay valid) and zero the counters. */
+int rope3d_cache_clear(void);
+
+/* ---- verification gate ("实现拆解" step 4: BitExactFusionGate) ------------ */
+#define ROPE3D_GATE_OFF   0  /* never verify                                   */
+#define ROPE3D_GATE_FIRST 1  /* verify the first call of each configuration    */
+int rope3d_gate_set_mode(int32_t mode);
+int rope3d_gate_get_mode(void);
+/* Forget every verdict. */
+int rope3d_gate_reset(void);
+/*
+ * Verdict for a configuration: 0 = not seen yet, 1 = verified, 2 = refused.
+ * Returns the verdict (>= 0) or a negative error code.
+ */
+int rope3d_gate_verdict(int64_t B, int64_t T, int64_t H, int64_t W, int64_t heads,
+                        int64_t head_dim, const int32_t split[3], double base,
+                        int32_t dtype);
+/*
+ * Test hook for the gate's failure path: the next `count` verifications flip
+ * one bit of the host copy of the kernel's output before comparing, so they
+ * must refuse. Never touches device memory.
+ */
+int rope3d_testing_corrupt_gate(int32_t count);
+
+/* ---- introspection ------------------------------------------------------- */
+/*
+ * Which kernel the last successful rope3d_apply_pair / _host launch used on
+ * this thread: 1 = 16-byte vector kernel, 2 = per-pair kernel, 0 = none yet.
+ * grid and block receive the launch shape of the last kernel (may be NULL).
+ */
+int rope3d_last_launch(int32_t *grid, int32_t *block);
+
+/* Name of a status code (static storage). */
+const char *rope3d_status_string(int status);
+
+/* ROPE3D_ABI_VERSION of the built library. */
+int rope3d_abi_version(void);
+
+/*
+ * Host-side check of the integer division used by the kernels' index decode:
+ * returns n / d computed with the precomputed multiplier the kernels use
+ * (valid for 1 <= d < 2^31 and 0 <= n < 2^31), or -1 for arguments out of range.
+ */
+int64_t rope3d_testing_fastdiv(int64_t n, int64_t d);
+
+/*
+ * Test hook: 1 makes the table cache keep its tables in host memory instead
+ * of device memory, so the cache logic can be exercised without a GPU; the
+ * GPU entry points then refuse those handles with ROPE3D_ERR_DEVICE. Only
+ * allowed while the cache is empty. 0 restores device memory.
+ */
+int rope3d_testing_host_tables(int32_t on);
+
+/*
+ * Test hook: cap the work units (16-byte vectors or pairs) of one kernel
+ * launch at n, so that small inputs exercise the split into several launches
+ * that very large inputs take (rows never straddle two launches; a row larger
+ * than n gets a launch of its own). 0 restores the default cap of 2^30.
+ * Errors: ARG for n < 0 or n > 2^30.
+ */
+int rope3d_testing_max_units_per_launch(int64_t n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ROPE3D_H */

@@ -1,0 +1,346 @@
+"""Python binding of the fused paired 3D RoPE library (``include/rope3d.h``).
+
+Argument marshalling only: every step of the rotation runs in the CUDA
+kernels of ``_build/librope3d.so``; this module turns tensors into pointers,
+sizes and a stream and turns status codes into exceptions. PyTorch is used for
+nothing but device memory and streams. When the library has not been built,
+loading raises: there is no other code path.
+
+The operation (sglang PR #35698 review, "fused LTX-2.5 decoder 3D RoPE",
+sections "实现拆解" and "关键源码片段"): Q and K of shape
+[B, T*H*W, heads, head_dim] are rotated pair by pair, T, H and W each using
+their own chunk of head_dim and their own fp32 cos/sin table, in the eager
+float32 order, in one kernel launch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "Rope3dError", "Tables", "load_library", "rope3d_build_tables", "rope3d_apply_pair",
+    "rope3d_apply_pair_host", "rope3d_preflight", "rope3d_axis_table_host",
+    "rope3d_tables_read", "rope3d_cache_stats", "rope3d_cache_clear", "rope3d_gate_set_mode",
+    "rope3d_gate_get_mode", "rope3d_gate_reset", "rope3d_gate_verdict",
+    "rope3d_testing_corrupt_gate", "rope3d_last_launch", "rope3d_status_string",
+    "rope3d_release_scratch", "rope3d_testing_fastdiv", "rope3d_testing_host_tables",
+    "rope3d_testing_max_units_per_launch",
+    "STATUS", "BF16", "F32", "GATE_OFF", "GATE_FIRST", "LIB_PATH",
+]
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "librope3d.so")
+
+BF16, F32 = 0, 1
+GATE_OFF, GATE_FIRST = 0, 1
+STATUS = {
+    0: "OK", -1: "ERR_NULL", -2: "ERR_SHAPE", -3: "ERR_DTYPE", -4: "ERR_ALIGN",
+    -5: "ERR_ALIAS", -6: "ERR_DEVICE", -7: "ERR_PARITY", -8: "ERR_CUDA", -9: "ERR_TABLES",
+    -10: "ERR_NOMEM", -11: "ERR_ARG",
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Rope3dError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+        msg = rope3d_status_string(status) if _lib is not None else self.name
+        super().__init__(f"{what}: {msg}" if what else msg)
+
+
+def _declare(lib):
+    c = ctypes
+    i64, i32, vp, dbl = c.c_int64, c.c_int32, c.c_void_p, c.c_double
+    sig = {
+        "rope3d_build_tables": ([i64, i64, i64, vp, dbl, vp, vp], c.c_int),
+        "rope3d_release_tables": ([vp], c.c_int),
+        "rope3d_retain_tables": ([vp], c.c_int),
+        "rope3d_apply_pair": ([vp, vp, vp, vp, vp] + [i64] * 6 + [vp, i32, vp], c.c_int),
+        "rope3d_apply_pair_host": ([vp, vp, vp, vp, vp] + [i64] * 6 + [vp, i32, vp], c.c_int),
+        "rope3d_release_scratch": ([], c.c_int),
+        "rope3d_preflight": ([vp, vp, vp, vp, vp] + [i64] * 6 + [vp, i32, i32], c.c_int),
+        "rope3d_axis_table_host": ([i64, i64, dbl, vp, vp], c.c_int),
+        "rope3d_tables_info": ([vp, vp, vp, vp], c.c_int),
+        "rope3d_tables_read": ([vp, i32, i32, vp, vp], c.c_int),
+        "rope3d_cache_stats": ([vp, vp, vp, vp], c.c_int),
+        "rope3d_cache_clear": ([], c.c_int),
+        "rope3d_gate_set_mode": ([i32], c.c_int),
+        "rope3d_gate_get_mode": ([], c.c_int),
+        "rope3d_gate_reset": ([], c.c_int),
+        "rope3d_gate_verdict": ([i64] * 6 + [vp, dbl, i32], c.c_int),
+        "rope3d_testing_corrupt_gate": ([i32], c.c_int),
+        "rope3d_last_launch": ([vp, vp], c.c_int),
+        "rope3d_status_string": ([c.c_int], c.c_char_p),
+        "rope3d_abi_version": ([], c.c_int),
+        "rope3d_testing_fastdiv": ([i64, i64], i64),
+        "rope3d_testing_host_tables": ([i32], c.c_int),
+        "rope3d_testing_max_units_per_launch": ([i64], c.c_int),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+def load_library(path: str | None = None):
+    """Load the built library (fails loudly when it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise ImportError(
+                    f"{p} is missing: build the CUDA library first "
+                    "(python -m rope_rope3d_apply_gb300.build)")
+            _lib = _declare(ctypes.CDLL(p))
+    return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise Rope3dError(rc, what)
+
+
+def _split(split):
+    if len(split) != 3:
+        raise ValueError("split must have three entries (d_T, d_H, d_W)")
+    return (ctypes.c_int32 * 3)(*[int(v) for v in split])
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    if hasattr(x, "ctypes"):
+        return int(x.ctypes.data)
+    raise TypeError(f"cannot take a pointer of {type(x)!r}")
+
+
+def _stream(stream, like=None) -> int:
+    if stream is None:
+        if like is not None and getattr(like, "is_cuda", False):
+            import torch
+
+            return int(torch.cuda.current_stream(like.device).cuda_stream)
+        return 0
+    if hasattr(stream, "cuda_stream"):
+        return int(stream.cuda_stream)
+    return int(stream)
+
+
+def _dtype_code(x) -> int:
+    dt = str(getattr(x, "dtype", ""))
+    if dt in ("torch.bfloat16", "uint16"):
+        return BF16
+    if dt in ("torch.float32", "float32"):
+        return F32
+    raise TypeError(f"unsupported dtype {dt} (bfloat16 or float32)")
+
+
+def _contiguous(x) -> bool:
+    if hasattr(x, "is_contiguous"):
+        return bool(x.is_contiguous())
+    if hasattr(x, "flags"):
+        return bool(x.flags["C_CONTIGUOUS"])
+    return True
+
+
+class Tables:
+    """One reference to a cached table set; released by close() or on
+    garbage collection."""
+
+    def __init__(self, handle: int):
+        self.handle = handle
+        dims = (ctypes.c_int64 * 3)()
+        split = (ctypes.c_int32 * 3)()
+        base = ctypes.c_double()
+        _check(load_library().rope3d_tables_info(handle, dims, split, ctypes.byref(base)),
+               "rope3d_tables_info")
+        self.T, self.H, self.W = (int(v) for v in dims)
+        self.split = tuple(int(v) for v in split)
+        self.base = float(base.value)
+
+    def close(self):
+        if self.handle:
+            load_library().rope3d_release_tables(self.handle)
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+def rope3d_build_tables(T: int, H: int, W: int, split, base: float = 10000.0,
+                        stream=None) -> Tables:
+    out = ctypes.c_void_p()
+    _check(load_library().rope3d_build_tables(int(T), int(H), int(W), _split(split),
+                                              float(base), _stream(stream),
+                                              ctypes.byref(out)), "rope3d_build_tables")
+    return Tables(out.value)
+
+
+def _geometry(q, tables: Tables):
+    """(B, heads, head_dim) of q laid out as [B, T*H*W, heads, head_dim] or
+    [B, T, H, W, heads, head_dim]."""
+    shape = tuple(int(v) for v in q.shape)
+    N = tables.T * tables.H * tables.W
+    if len(shape) == 6:
+        if shape[1:4] != (tables.T, tables.H, tables.W):
+            raise ValueError(f"q grid {shape[1:4]} != tables grid {(tables.T, tables.H, tables.W)}")
+        return shape[0], shape[4], shape[5]
+    if len(shape) == 4:
+        if shape[1] != N:
+            raise ValueError(f"q has {shape[1]} tokens, the tables' grid has {N}")
+        return shape[0], shape[2], shape[3]
+    raise ValueError("q must be [B, T*H*W, heads, head_dim] or [B, T, H, W, heads, head_dim]")
+
+
+def _marshal(q, k, q_out, k_out, tables: Tables):
+    for name, t in (("q", q), ("k", k), ("q_out", q_out), ("k_out", k_out)):
+        if not _contiguous(t):
+            raise ValueError(f"{name} must be contiguous")
+        if tuple(t.shape) != tuple(q.shape):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, q has {tuple(q.shape)}")
+    B, heads, head_dim = _geometry(q, tables)
+    dt = _dtype_code(q)
+    for t in (k, q_out, k_out):
+        if _dtype_code(t) != dt:
+            raise TypeError("q, k, q_out and k_out must have one dtype")
+    return B, heads, head_dim, dt
+
+
+def rope3d_apply_pair(q, k, tables: Tables, q_out=None, k_out=None, stream=None):
+    """Rotate device tensors q and k; returns (q_out, k_out). Outputs are
+    allocated with torch.empty_like when not given."""
+    if q_out is None or k_out is None:
+        import torch
+
+        q_out = torch.empty_like(q) if q_out is None else q_out
+        k_out = torch.empty_like(k) if k_out is None else k_out
+    B, heads, head_dim, dt = _marshal(q, k, q_out, k_out, tables)
+    rc = load_library().rope3d_apply_pair(
+        _ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), tables.handle, B, tables.T, tables.H,
+        tables.W, heads, head_dim, _split(tables.split), dt, _stream(stream, q))
+    _check(rc, "rope3d_apply_pair")
+    return q_out, k_out
+
+
+def rope3d_apply_pair_host(q, k, q_out, k_out, tables: Tables, stream=None):
+    """Rotate host buffers (torch CPU tensors, ideally pinned, or numpy arrays;
+    bf16 may be given as uint16 bit patterns). Returns when the outputs are in
+    host memory."""
+    B, heads, head_dim, dt = _marshal(q, k, q_out, k_out, tables)
+    rc = load_library().rope3d_apply_pair_host(
+        _ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), tables.handle, B, tables.T, tables.H,
+        tables.W, heads, head_dim, _split(tables.split), dt, _stream(stream))
+    _check(rc, "rope3d_apply_pair_host")
+    return q_out, k_out
+
+
+def rope3d_preflight(q, k, q_out, k_out, tables, B, T, H, W, heads, head_dim, split, dtype,
+                     check_device=True) -> int:
+    """Status that rope3d_apply_pair would return before launching (no launch)."""
+    handle = tables.handle if isinstance(tables, Tables) else (tables or 0)
+    return load_library().rope3d_preflight(
+        _ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), handle, int(B), int(T), int(H), int(W),
+        int(heads), int(head_dim), _split(split) if split is not None else None, int(dtype),
+        1 if check_device else 0)
+
+
+def rope3d_axis_table_host(length: int, dim: int, base: float = 10000.0):
+    import numpy as np
+
+    c = np.empty((length, dim // 2), np.float32)
+    s = np.empty((length, dim // 2), np.float32)
+    _check(load_library().rope3d_axis_table_host(int(length), int(dim), float(base),
+                                                 _ptr(c), _ptr(s)), "rope3d_axis_table_host")
+    return c, s
+
+
+def rope3d_tables_read(tables: Tables, axis: int, from_device: bool = False):
+    import numpy as np
+
+    L = (tables.T, tables.H, tables.W)[axis]
+    d = tables.split[axis]
+    c = np.empty((L, d // 2), np.float32)
+    s = np.empty((L, d // 2), np.float32)
+    _check(load_library().rope3d_tables_read(tables.handle, int(axis), 1 if from_device else 0,
+                                             _ptr(c), _ptr(s)), "rope3d_tables_read")
+    return c, s
+
+
+def rope3d_cache_stats() -> dict:
+    v = [ctypes.c_int64() for _ in range(4)]
+    _check(load_library().rope3d_cache_stats(*[ctypes.byref(x) for x in v]), "rope3d_cache_stats")
+    return dict(zip(("entries", "hits", "misses", "evictions"), (x.value for x in v)))
+
+
+def rope3d_cache_clear():
+    _check(load_library().rope3d_cache_clear(), "rope3d_cache_clear")
+
+
+def rope3d_gate_set_mode(mode: int):
+    _check(load_library().rope3d_gate_set_mode(int(mode)), "rope3d_gate_set_mode")
+
+
+def rope3d_gate_get_mode() -> int:
+    return int(load_library().rope3d_gate_get_mode())
+
+
+def rope3d_gate_reset():
+    _check(load_library().rope3d_gate_reset(), "rope3d_gate_reset")
+
+
+def rope3d_gate_verdict(B, T, H, W, heads, head_dim, split, base, dtype) -> int:
+    r = load_library().rope3d_gate_verdict(int(B), int(T), int(H), int(W), int(heads),
+                                           int(head_dim), _split(split), float(base), int(dtype))
+    if r < 0:
+        raise Rope3dError(r, "rope3d_gate_verdict")
+    return r
+
+
+def rope3d_testing_corrupt_gate(count: int):
+    _check(load_library().rope3d_testing_corrupt_gate(int(count)), "rope3d_testing_corrupt_gate")
+
+
+def rope3d_testing_host_tables(on: bool):
+    _check(load_library().rope3d_testing_host_tables(1 if on else 0), "rope3d_testing_host_tables")
+
+
+def rope3d_testing_fastdiv(n: int, d: int) -> int:
+    return int(load_library().rope3d_testing_fastdiv(int(n), int(d)))
+
+
+def rope3d_testing_max_units_per_launch(n: int):
+    _check(load_library().rope3d_testing_max_units_per_launch(int(n)),
+           "rope3d_testing_max_units_per_launch")
+
+
+def rope3d_last_launch():
+    g, b = ctypes.c_int32(), ctypes.c_int32()
+    kernel = load_library().rope3d_last_launch(ctypes.byref(g), ctypes.byref(b))
+    return {"kernel": int(kernel), "grid": g.value, "block": b.value}
+
+
+def rope3d_release_scratch():
+    _check(load_library().rope3d_release_scratch(), "rope3d_release_scratch")
+
+
+def rope3d_status_string(status: int) -> str:
+    return load_library().rope3d_status_string(int(status)).decode()

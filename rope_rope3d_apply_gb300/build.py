@@ -1,0 +1,93 @@
+"""Build step of the rope3d library: compiles the CUDA kernels for sm_103a and
+the host C ABI, and links them into ``_build/librope3d.so`` inside this
+package (in-tree, so the same file is what the tests and the benchmark load).
+
+    python -m rope_rope3d_apply_gb300.build
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(HERE, "csrc")
+BUILD = os.path.join(HERE, "_build")
+LIB = os.path.join(BUILD, "librope3d.so")
+INCLUDE = os.path.join(os.path.dirname(HERE), "include")
+
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+SOURCES = [
+    os.path.join(CSRC, "rope3d_kernels.cu"),
+    os.path.join(CSRC, "rope3d_api.cpp"),
+    os.path.join(CSRC, "rope3d_internal.h"),
+    os.path.join(INCLUDE, "rope3d.h"),
+]
+
+
+def _cuda_home() -> str:
+    nvcc = shutil.which("nvcc")
+    if nvcc:
+        return os.path.dirname(os.path.dirname(os.path.realpath(nvcc)))
+    return os.environ.get("CUDA_HOME", "/usr/local/cuda")
+
+
+def _nvcc() -> str:
+    return os.path.join(_cuda_home(), "bin", "nvcc")
+
+
+def commands(out_dir: str = BUILD, extra_nvcc: list[str] | None = None):
+    cuda = _cuda_home()
+    kern_o = os.path.join(out_dir, "rope3d_kernels.o")
+    api_o = os.path.join(out_dir, "rope3d_api.o")
+    nvcc_compile = [
+        _nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-fmad=false",
+        "-Xcompiler", "-fPIC,-ffp-contract=off", "-Xptxas", "-v",
+        *(extra_nvcc or []),
+        "-c", os.path.join(CSRC, "rope3d_kernels.cu"), "-o", kern_o,
+    ]
+    gxx_compile = [
+        "g++", "-std=c++17", "-O2", "-fPIC", "-ffp-contract=off", "-fno-fast-math",
+        "-pthread", "-Wall", "-Wno-unused-function", f"-I{cuda}/include",
+        "-c", os.path.join(CSRC, "rope3d_api.cpp"), "-o", api_o,
+    ]
+    link = [_nvcc(), *ARCH, "-shared", kern_o, api_o, "-o", os.path.join(out_dir, "librope3d.so"),
+            "-Xcompiler", "-pthread"]
+    return [nvcc_compile, gxx_compile], link
+
+
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
+        return False
+    t = os.path.getmtime(lib)
+    return all(os.path.getmtime(s) <= t for s in SOURCES)
+
+
+def build(force: bool = False, verbose: bool = False, out_dir: str = BUILD) -> str:
+    """Compile and link; returns the library path. Both compiles run in parallel."""
+    lib = os.path.join(out_dir, "librope3d.so")
+    if not force and out_dir == BUILD and up_to_date(lib):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
+    compiles, link = commands(out_dir)
+    procs = [subprocess.Popen(c, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
+             for c in compiles]
+    logs = []
+    for c, p in zip(compiles, procs):
+        out, _ = p.communicate()
+        logs.append(out)
+        if p.returncode != 0:
+            raise RuntimeError(f"compile failed: {' '.join(c)}\n{out}")
+    r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed: {' '.join(link)}\n{r.stdout}")
+    with open(os.path.join(out_dir, "ptxas.log"), "w") as f:
+        f.write("\n".join(logs))
+    if verbose:
+        print("\n".join(logs))
+    return lib
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose=True))

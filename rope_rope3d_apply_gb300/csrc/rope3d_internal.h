@@ -1,0 +1,76 @@
+// rope3d_internal.h -- shared between the host API (rope3d_api.cpp) and the
+// kernels (rope3d_kernels.cu). Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace rope3d {
+
+// Unsigned division by a run-time constant, n / d for 0 <= n < 2^31 and
+// 1 <= d < 2^31, by a multiply-high and a shift (Granlund and Montgomery,
+// "Division by invariant integers using multiplication", PLDI 1994, the
+// round-up multiplier): with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// n / d = (mulhi(n, m) + n) >> l. Because n < 2^31, the sum cannot overflow.
+struct FastDiv {
+    uint32_t d;
+    uint32_t mul;
+    uint32_t shift;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;
+    while ((uint64_t(1) << l) < d) ++l;
+    const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
+    return FastDiv{d, static_cast<uint32_t>(m), l};
+}
+
+inline uint32_t fastdiv_host(uint32_t n, const FastDiv &f) {
+    const uint32_t hi = static_cast<uint32_t>((uint64_t(n) * f.mul) >> 32);
+    return (hi + n) >> f.shift;
+}
+
+// Largest number of work units (16-byte vectors or pairs) one launch handles;
+// keeps every in-kernel index below 2^31 with room for the unrolled stride.
+constexpr uint32_t kMaxUnitsPerLaunch = 1u << 30;
+
+// Tables up to this size are staged in shared memory; larger ones are read
+// through the read-only data path.
+constexpr uint32_t kMaxSmemTableBytes = 96 * 1024;
+
+// Launch description. Device layout of the tables: one buffer of float2
+// (cos, sin) entries, the T table [T][pT], then the H table [H][pH] at offH,
+// then the W table [W][pW] at offW (each offset a multiple of 4 entries).
+struct LaunchArgs {
+    const void *q;
+    const void *k;
+    void *q_out;
+    void *k_out;
+    const float2 *tables;
+    uint32_t table_len;     // float2 entries in the whole buffer
+    uint32_t offH, offW;    // entry offsets of the H and W tables
+    uint32_t pT, pH, pW;    // pairs per axis chunk (d_X / 2)
+    uint32_t T, H, W;       // grid extents
+    uint32_t heads, head_dim;
+    uint64_t rows;          // (batch, token) rows in the buffers of this call
+    uint64_t row0;          // global row index of the first row (host path chunks)
+    int dtype;              // ROPE3D_BF16 / ROPE3D_F32
+    bool vec16;             // take the 16-byte vector kernel
+};
+
+struct LaunchInfo {
+    int kernel;  // 1 = vector, 2 = per-pair
+    int grid;
+    int block;
+};
+
+// Test hook: lower the units-per-launch cap so that small inputs take the
+// multi-launch path (0 restores kMaxUnitsPerLaunch).
+void set_max_units_per_launch(uint32_t n);
+
+// Launch the rotation; splits into several launches when needed. Returns a
+// cudaError_t from the launch.
+cudaError_t launch_rope3d(const LaunchArgs &a, cudaStream_t stream, LaunchInfo *info);
+
+}  // namespace rope3d

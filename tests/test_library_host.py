@@ -1,0 +1,207 @@
+"""Host-side tests of the library that need no GPU: the C ABI exports, the
+table builder (bitwise against the oracle), the index-decode division, the
+preflight rules, the table cache's FIFO and reference counting, and the gate's
+bookkeeping."""
+from __future__ import annotations
+
+import ctypes
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import rope_rope3d_apply_gb300 as r
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rope_rope3d_apply_gb300 import build
+
+    build.build()
+    return r.load_library()
+
+
+@pytest.fixture
+def host_tables(lib):
+    """The cache in its host-memory test mode (no GPU needed)."""
+    r.rope3d_cache_clear()
+    r.rope3d_testing_host_tables(True)
+    yield
+    r.rope3d_cache_clear()
+    r.rope3d_testing_host_tables(False)
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(rope3d_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 20
+    raw = ctypes.CDLL(r.LIB_PATH)
+    missing = [n for n in names if not hasattr(raw, n)]
+    assert not missing, missing
+    assert lib.rope3d_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for code, name in r.STATUS.items():
+        s = r.rope3d_status_string(code)
+        assert name in s.replace("ROPE3D_", ""), (code, s)
+    assert "unknown" in r.rope3d_status_string(-99)
+
+
+@pytest.mark.parametrize("length,dim,base", [
+    (2, 16, 10000.0), (4, 16, 10000.0), (16, 24, 10000.0), (24, 32, 10000.0),
+    (96, 48, 10000.0), (64, 48, 10000.0), (63, 48, 10000.0), (1, 2, 10000.0),
+    (1000, 128, 10000.0), (7, 10, 3.5), (50, 64, 1e6),
+])
+def test_axis_table_matches_oracle_bitwise(lib, length, dim, base):
+    c, s = r.rope3d_axis_table_host(length, dim, base)
+    oc, os_ = oracle.axis_table(length, dim, base)
+    assert np.array_equal(c.view(np.uint32), oc.view(np.uint32))
+    assert np.array_equal(s.view(np.uint32), os_.view(np.uint32))
+
+
+def test_axis_table_rejects(lib):
+    for length, dim, base in [(0, 16, 1e4), (4, 15, 1e4), (4, 0, 1e4)]:
+        with pytest.raises(r.Rope3dError) as e:
+            r.rope3d_axis_table_host(length, dim, base)
+        assert e.value.name == "ERR_SHAPE"
+    for base in (0.0, -1.0, float("nan"), float("inf")):
+        with pytest.raises(r.Rope3dError) as e:
+            r.rope3d_axis_table_host(4, 16, base)
+        assert e.value.name == "ERR_ARG"
+
+
+def test_fastdiv_is_exact(lib):
+    g = np.random.Generator(np.random.PCG64(7))
+    divisors = [1, 2, 3, 5, 7, 16, 48, 63, 64, 96, 384, 9216, 65536, 221184, 442368,
+                (1 << 31) - 1, (1 << 30) + 1, 1 << 30]
+    divisors += [int(d) for d in g.integers(1, 1 << 31, 200)]
+    for d in divisors:
+        ns = [0, 1, d - 1, d, d + 1, (1 << 31) - 1, (1 << 31) - 2, 2 * d - 1, 2 * d]
+        ns += [int(n) for n in g.integers(0, 1 << 31, 200)]
+        for n in ns:
+            if 0 <= n < (1 << 31):
+                assert r.rope3d_testing_fastdiv(n, d) == n // d, (n, d)
+    assert r.rope3d_testing_fastdiv(1 << 31, 3) == -1
+    assert r.rope3d_testing_fastdiv(5, 0) == -1
+
+
+def _preflight_case(case, base, handles):
+    cfg = dict(base)
+    cfg.update(case["changes"])
+    elem = 4 if cfg["dtype"] == 1 else 2
+    numel = max(0, cfg["B"] * cfg["T"] * cfg["H"] * cfg["W"] * cfg["heads"] * cfg["head_dim"])
+    span = max(numel * elem, 1) + (1 << 20)
+    ptrs = {"q": 1 << 32, "k": (1 << 32) + span, "q_out": (1 << 32) + 2 * span,
+            "k_out": (1 << 32) + 3 * span}
+    for name in ("q", "k", "q_out", "k_out"):
+        v = case["changes"].get(name, "keep")
+        if v is None:
+            ptrs[name] = 0
+        elif isinstance(v, str) and v != "keep":
+            ref, _, off = v.partition("+")
+            ptrs[name] = ptrs[ref] + int(off or 0)
+        ptrs[name] += case["changes"].get(name + "_offset", 0)
+    tab = cfg.get("tables")
+    handle = None if tab is None else handles[(tab[0], tab[1], tab[2], tuple(tab[3]))]
+    return r.rope3d_preflight(ptrs["q"], ptrs["k"], ptrs["q_out"], ptrs["k_out"], handle,
+                              cfg["B"], cfg["T"], cfg["H"], cfg["W"], cfg["heads"],
+                              cfg["head_dim"], cfg["split"], cfg["dtype"], check_device=False)
+
+
+def test_preflight_rules_from_the_pages(lib, host_tables):
+    spec = json.load(open(os.path.join(ROOT, "tests", "golden", "preflight_cases.json")))
+    handles = {}
+    for case in [spec["base_case"]] + [dict(spec["base_case"], **c["changes"]) for c in spec["cases"]]:
+        tab = case.get("tables")
+        if tab is not None:
+            key = (tab[0], tab[1], tab[2], tuple(tab[3]))
+            if key not in handles:
+                handles[key] = r.rope3d_build_tables(*key[:3], key[3], 10000.0)
+    for case in spec["cases"]:
+        got = _preflight_case(case, spec["base_case"], handles)
+        assert r.STATUS[got] == case["status"], (case["name"], r.STATUS[got])
+    for h in handles.values():
+        h.close()
+
+
+def test_cache_fifo_refcount_and_key(lib, host_tables):
+    split = (16, 16, 16)
+    first = r.rope3d_build_tables(1, 1, 1, split)
+    held = [first]
+    for i in range(2, 17):
+        held.append(r.rope3d_build_tables(i, 1, 1, split))
+    st = r.rope3d_cache_stats()
+    assert st == {"entries": 16, "hits": 0, "misses": 16, "evictions": 0}
+    # a hit returns the same entry and does not refresh its age
+    again = r.rope3d_build_tables(1, 1, 1, split)
+    assert again.handle == first.handle
+    assert r.rope3d_cache_stats()["hits"] == 1
+    # the 17th entry evicts the oldest (grid 1x1x1) ...
+    held.append(r.rope3d_build_tables(17, 1, 1, split))
+    st = r.rope3d_cache_stats()
+    assert st["entries"] == 16 and st["evictions"] == 1
+    # ... whose handles stay valid while held
+    c, s = r.rope3d_tables_read(first, 0, from_device=True)
+    assert c.shape == (1, 8) and np.all(c == 1.0) and np.all(s == 0.0)
+    # building it again is a miss and a different entry
+    fresh = r.rope3d_build_tables(1, 1, 1, split)
+    assert fresh.handle != first.handle
+    assert r.rope3d_cache_stats()["misses"] == 18
+    # the key includes the split and the base
+    a = r.rope3d_build_tables(2, 4, 4, (16, 16, 16), 10000.0)
+    b = r.rope3d_build_tables(2, 4, 4, (16, 8, 24), 10000.0)
+    c_ = r.rope3d_build_tables(2, 4, 4, (16, 16, 16), 500.0)
+    assert len({a.handle, b.handle, c_.handle}) == 3
+    for t in held + [again, fresh, a, b, c_]:
+        t.close()
+
+
+def test_cached_tables_match_oracle(lib, host_tables):
+    for T, H, W, split in [(24, 96, 96, (32, 48, 48)), (16, 64, 63, (32, 48, 48)), (3, 5, 7, (4, 6, 8))]:
+        t = r.rope3d_build_tables(T, H, W, split)
+        otabs = oracle.tables(T, H, W, split)
+        for axis in range(3):
+            for dev in (False, True):
+                c, s = r.rope3d_tables_read(t, axis, from_device=dev)
+                assert np.array_equal(c.view(np.uint32), otabs[axis][0].view(np.uint32))
+                assert np.array_equal(s.view(np.uint32), otabs[axis][1].view(np.uint32))
+        t.close()
+
+
+def test_gate_bookkeeping_without_gpu(lib, host_tables):
+    r.rope3d_gate_reset()
+    assert r.rope3d_gate_get_mode() == r.GATE_FIRST
+    assert r.rope3d_gate_verdict(1, 2, 4, 4, 2, 48, (16, 16, 16), 10000.0, r.BF16) == 0
+    r.rope3d_gate_set_mode(r.GATE_OFF)
+    assert r.rope3d_gate_get_mode() == r.GATE_OFF
+    r.rope3d_gate_set_mode(r.GATE_FIRST)
+    with pytest.raises(r.Rope3dError):
+        r.rope3d_gate_set_mode(7)
+    with pytest.raises(r.Rope3dError):
+        r.rope3d_testing_corrupt_gate(-1)
+
+
+def test_build_tables_rejects(lib, host_tables):
+    for args, name in [((0, 4, 4, (16, 16, 16)), "ERR_SHAPE"), ((2, 4, 4, (15, 17, 16)), "ERR_SHAPE"),
+                       ((2, 4, 4, (0, 24, 24)), "ERR_SHAPE"), ((1 << 20, 1 << 11, 2, (2, 2, 2)), "ERR_SHAPE")]:
+        with pytest.raises(r.Rope3dError) as e:
+            r.rope3d_build_tables(*args)
+        assert e.value.name == name
+    with pytest.raises(r.Rope3dError) as e:
+        r.rope3d_build_tables(2, 4, 4, (16, 16, 16), -1.0)
+    assert e.value.name == "ERR_ARG"
