@@ -52,6 +52,8 @@ extern "C" {
 #define ROPE3D_ERR_TABLES   -9  /* the table handle does not match (T, H, W, split) */
 #define ROPE3D_ERR_NOMEM   -10  /* a device or host allocation failed             */
 #define ROPE3D_ERR_ARG     -11  /* another argument is out of range               */
+#define ROPE3D_ERR_SCRATCH -12  /* the tables do not fit the fixed table area of
+                                   rope3d_apply_pair_noalloc (64 KiB)             */
 
 /* ---- element types ----------------------------------------------------- */
 #define ROPE3D_BF16 0   /* bfloat16 in and out                                */
@@ -164,6 +166,41 @@ int rope3d_apply_pair_host(const void *q, const void *k, void *q_out, void *k_ou
 
 /* Free the staging buffers of rope3d_apply_pair_host (waits for the device). */
 int rope3d_release_scratch(void);
+
+/*
+ * rope3d_apply_pair_noalloc -- rope3d_apply_pair for callers that cannot
+ * allocate device memory. The paper has no counterpart: it exists because
+ * rope3d_build_tables allocates the cached tables with cudaMalloc, and some
+ * callers cannot call cudaMalloc (a process whose device memory belongs to
+ * another allocator or a fixed budget, or a pipeline that must not take
+ * cudaMalloc's implicit synchronisation). This call takes no table handle:
+ * it computes the three axis tables on the host (the values of
+ * rope3d_build_tables) and uploads them into a fixed 64 KiB table area in the
+ * library's static device memory, then launches the same kernels. It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   q, k, q_out, k_out, B, T, H, W, heads, head_dim, split, dtype, stream
+ *           as for rope3d_apply_pair (device pointers, caller-owned)
+ *   base    RoPE base, finite and > 0
+ *
+ * Limit: the tables, sum over X of L_X * d_X/2 entries of 8 bytes with each
+ * axis rounded up to 4 entries, must fit 64 KiB (8192 entries); larger grids
+ * return ROPE3D_ERR_SCRATCH before anything is copied or launched. The table
+ * area belongs to every GPU that loads the library until the process exits.
+ * The first call on each device looks up the area's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call shares the one area and leaves its tables there; nothing in it
+ * has to start at zero, because each call writes every entry it reads. Calls
+ * are serialised on the host, and calls on one stream are ordered, but calls
+ * whose work overlaps on the GPU (different streams) race on the area.
+ * The upload comes from pageable host memory, so the call waits for earlier
+ * work on `stream` before returning. The bit-exact gate does not run here.
+ * Errors: as rope3d_apply_pair (without TABLES and PARITY), ARG (base), SCRATCH.
+ */
+int rope3d_apply_pair_noalloc(const void *q, const void *k, void *q_out, void *k_out,
+                              int64_t B, int64_t T, int64_t H, int64_t W,
+                              int64_t heads, int64_t head_dim, const int32_t split[3],
+                              double base, int32_t dtype, void *stream);
 
 /*
  * rope3d_preflight -- the argument checks of rope3d_apply_pair without a

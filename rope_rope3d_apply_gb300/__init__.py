@@ -25,7 +25,7 @@ __all__ = [
     "rope3d_gate_get_mode", "rope3d_gate_reset", "rope3d_gate_verdict",
     "rope3d_testing_corrupt_gate", "rope3d_last_launch", "rope3d_status_string",
     "rope3d_release_scratch", "rope3d_testing_fastdiv", "rope3d_testing_host_tables",
-    "rope3d_testing_max_units_per_launch",
+    "rope3d_testing_max_units_per_launch", "rope3d_apply_pair_noalloc",
     "STATUS", "BF16", "F32", "GATE_OFF", "GATE_FIRST", "LIB_PATH",
 ]
 
@@ -37,7 +37,7 @@ GATE_OFF, GATE_FIRST = 0, 1
 STATUS = {
     0: "OK", -1: "ERR_NULL", -2: "ERR_SHAPE", -3: "ERR_DTYPE", -4: "ERR_ALIGN",
     -5: "ERR_ALIAS", -6: "ERR_DEVICE", -7: "ERR_PARITY", -8: "ERR_CUDA", -9: "ERR_TABLES",
-    -10: "ERR_NOMEM", -11: "ERR_ARG",
+    -10: "ERR_NOMEM", -11: "ERR_ARG", -12: "ERR_SCRATCH",
 }
 
 _lock = threading.Lock()
@@ -79,6 +79,7 @@ def _declare(lib):
         "rope3d_testing_fastdiv": ([i64, i64], i64),
         "rope3d_testing_host_tables": ([i32], c.c_int),
         "rope3d_testing_max_units_per_launch": ([i64], c.c_int),
+        "rope3d_apply_pair_noalloc": ([vp, vp, vp, vp] + [i64] * 6 + [vp, dbl, i32, vp], c.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -250,6 +251,32 @@ def rope3d_apply_pair_host(q, k, q_out, k_out, tables: Tables, stream=None):
         _ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), tables.handle, B, tables.T, tables.H,
         tables.W, heads, head_dim, _split(tables.split), dt, _stream(stream))
     _check(rc, "rope3d_apply_pair_host")
+    return q_out, k_out
+
+
+def rope3d_apply_pair_noalloc(q, k, q_out, k_out, T: int, H: int, W: int, split,
+                              base: float = 10000.0, stream=None):
+    """rope3d_apply_pair without a table handle, for callers that cannot
+    allocate device memory: the tables go into the library's fixed 64 KiB
+    static table area (see include/rope3d.h). q_out and k_out are required;
+    this function allocates nothing."""
+    for name, t in (("q", q), ("k", k), ("q_out", q_out), ("k_out", k_out)):
+        if not _contiguous(t):
+            raise ValueError(f"{name} must be contiguous")
+        if tuple(t.shape) != tuple(q.shape):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, q has {tuple(q.shape)}")
+    shape = tuple(int(v) for v in q.shape)
+    if len(shape) == 6:
+        B, heads, head_dim = shape[0], shape[4], shape[5]
+    elif len(shape) == 4 and shape[1] == T * H * W:
+        B, heads, head_dim = shape[0], shape[2], shape[3]
+    else:
+        raise ValueError("q must be [B, T*H*W, heads, head_dim] or [B, T, H, W, heads, head_dim]")
+    dt = _dtype_code(q)
+    rc = load_library().rope3d_apply_pair_noalloc(
+        _ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), B, int(T), int(H), int(W), heads, head_dim,
+        _split(split), float(base), dt, _stream(stream, q))
+    _check(rc, "rope3d_apply_pair_noalloc")
     return q_out, k_out
 
 

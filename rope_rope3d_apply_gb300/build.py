@@ -20,6 +20,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = [
     os.path.join(CSRC, "rope3d_kernels.cu"),
+    os.path.join(CSRC, "rope3d_noalloc.cu"),
     os.path.join(CSRC, "rope3d_api.cpp"),
     os.path.join(CSRC, "rope3d_internal.h"),
     os.path.join(INCLUDE, "rope3d.h"),
@@ -47,14 +48,20 @@ def commands(out_dir: str = BUILD, extra_nvcc: list[str] | None = None):
         *(extra_nvcc or []),
         "-c", os.path.join(CSRC, "rope3d_kernels.cu"), "-o", kern_o,
     ]
+    noalloc_o = os.path.join(out_dir, "rope3d_noalloc.o")
+    nvcc_noalloc = [
+        _nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-fmad=false",
+        "-Xcompiler", "-fPIC,-ffp-contract=off",
+        "-c", os.path.join(CSRC, "rope3d_noalloc.cu"), "-o", noalloc_o,
+    ]
     gxx_compile = [
         "g++", "-std=c++17", "-O2", "-fPIC", "-ffp-contract=off", "-fno-fast-math",
         "-pthread", "-Wall", "-Wno-unused-function", f"-I{cuda}/include",
         "-c", os.path.join(CSRC, "rope3d_api.cpp"), "-o", api_o,
     ]
-    link = [_nvcc(), *ARCH, "-shared", kern_o, api_o, "-o", os.path.join(out_dir, "librope3d.so"),
-            "-Xcompiler", "-pthread"]
-    return [nvcc_compile, gxx_compile], link
+    link = [_nvcc(), *ARCH, "-shared", kern_o, api_o, noalloc_o,
+            "-o", os.path.join(out_dir, "librope3d.so"), "-Xcompiler", "-pthread"]
+    return [nvcc_compile, gxx_compile, nvcc_noalloc], link
 
 
 def up_to_date(lib: str = LIB) -> bool:

@@ -400,6 +400,26 @@ extern "C" int rope3d_preflight(const void *q, const void *k, const void *q_out,
     return ROPE3D_OK;
 }
 
+// Checks of an entry point that takes no table handle: everything
+// rope3d_preflight checks except the tables, plus the device query. Allocates
+// nothing.
+int rope3d::check_call_without_tables(const void *q, const void *k, const void *q_out,
+                                      const void *k_out, int64_t B, int64_t T, int64_t H,
+                                      int64_t W, int64_t heads, int64_t head_dim,
+                                      const int32_t split[3], int32_t dtype) {
+    if (!split) return ROPE3D_ERR_NULL;
+    const Geom g = make_geom(B, T, H, W, heads, head_dim, split, dtype);
+    int rc = check_geom(g);
+    if (rc != ROPE3D_OK) return rc;
+    rc = check_pointers(q, k, q_out, k_out, g.bytes());
+    if (rc != ROPE3D_OK) return rc;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return ROPE3D_ERR_CUDA;
+    for (const void *p : {q, k, q_out, k_out})
+        if (!is_device_ptr(p, device)) return ROPE3D_ERR_DEVICE;
+    return ROPE3D_OK;
+}
+
 // ============================================================================
 // the gate: CPU eager order, compared element by element
 // ============================================================================
@@ -924,6 +944,7 @@ extern "C" const char *rope3d_status_string(int status) {
         case ROPE3D_ERR_TABLES: return "ROPE3D_ERR_TABLES: the tables do not match (T, H, W, split)";
         case ROPE3D_ERR_NOMEM: return "ROPE3D_ERR_NOMEM: an allocation failed";
         case ROPE3D_ERR_ARG: return "ROPE3D_ERR_ARG: an argument is out of range";
+        case ROPE3D_ERR_SCRATCH: return "ROPE3D_ERR_SCRATCH: the tables exceed the 64 KiB static table area of rope3d_apply_pair_noalloc";
         default: return "ROPE3D: unknown status";
     }
 }

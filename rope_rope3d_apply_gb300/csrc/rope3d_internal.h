@@ -73,4 +73,11 @@ void set_max_units_per_launch(uint32_t n);
 // cudaError_t from the launch.
 cudaError_t launch_rope3d(const LaunchArgs &a, cudaStream_t stream, LaunchInfo *info);
 
+// The argument checks of rope3d_apply_pair without a table handle (shape,
+// dtype, alignment, overlap, device memory of the current device). Returns a
+// ROPE3D_* status. Allocates nothing.
+int check_call_without_tables(const void *q, const void *k, const void *q_out, const void *k_out,
+                              int64_t B, int64_t T, int64_t H, int64_t W, int64_t heads,
+                              int64_t head_dim, const int32_t split[3], int32_t dtype);
+
 }  // namespace rope3d
