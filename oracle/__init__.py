@@ -54,6 +54,10 @@ def _declare(lib):
     lib.oracle_bf16_to_f32.restype = ctypes.c_float
     lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
     lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.oracle_f16_to_f32.restype = ctypes.c_float
+    lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_f16.restype = ctypes.c_uint16
     lib.oracle_axis_table.argtypes = [i64, i64, ctypes.c_double, f32p, f32p]
     lib.oracle_axis_table.restype = ctypes.c_int
     lib.oracle_rotate_pair_f32.argtypes = [ctypes.c_float] * 4 + [vp, vp]
@@ -63,6 +67,8 @@ def _declare(lib):
     lib.oracle_rope3d_bf16.restype = ctypes.c_int
     lib.oracle_rope3d_f32.argtypes = full
     lib.oracle_rope3d_f32.restype = ctypes.c_int
+    lib.oracle_rope3d_f16.argtypes = full
+    lib.oracle_rope3d_f16.restype = ctypes.c_int
     at = [vp, vp, i64, vp] + [i64] * 6 + [vp] + [vp] * 6
     lib.oracle_rope3d_bf16_at.argtypes = at
     lib.oracle_rope3d_bf16_at.restype = ctypes.c_int
@@ -110,6 +116,14 @@ def f32_to_bf16(value: float, lib=None) -> int:
     return int((lib or load()).oracle_f32_to_bf16(float(np.float32(value))))
 
 
+def f16_to_f32(bits: int, lib=None) -> float:
+    return (lib or load()).oracle_f16_to_f32(int(bits))
+
+
+def f32_to_f16(value: float, lib=None) -> int:
+    return int((lib or load()).oracle_f32_to_f16(float(np.float32(value))))
+
+
 def rotate_pair(even: float, odd: float, c: float, s: float, lib=None):
     """One pair in the eager order; returns float32 (y_even, y_odd)."""
     y = np.zeros(2, dtype=np.float32)
@@ -151,12 +165,13 @@ def _table_args(tabs):
 # the rotation
 # ---------------------------------------------------------------------------
 
-def rope3d(x: np.ndarray, shape, split, tabs, lib=None) -> np.ndarray:
+def rope3d(x: np.ndarray, shape, split, tabs, lib=None, f16: bool = False) -> np.ndarray:
     """Full oracle pass.
 
-    x: uint16 (bf16 bit patterns) or float32 array with B*T*H*W*heads*head_dim
-    elements in [B, T, H, W, heads, head_dim] order. shape = (B, T, H, W,
-    heads, head_dim). Returns an array of the same dtype and shape as x.
+    x: uint16 (bf16 bit patterns, or binary16 bit patterns with f16=True) or
+    float32 array with B*T*H*W*heads*head_dim elements in
+    [B, T, H, W, heads, head_dim] order. shape = (B, T, H, W, heads,
+    head_dim). Returns an array of the same dtype and shape as x.
     """
     lib = lib or load()
     B, T, H, W, heads, head_dim = (int(v) for v in shape)
@@ -167,11 +182,11 @@ def rope3d(x: np.ndarray, shape, split, tabs, lib=None) -> np.ndarray:
     sp = _split_arr(split)
     tb = _table_args(tabs)
     if x.dtype == np.uint16:
-        fn = lib.oracle_rope3d_bf16
+        fn = lib.oracle_rope3d_f16 if f16 else lib.oracle_rope3d_bf16
     elif x.dtype == np.float32:
         fn = lib.oracle_rope3d_f32
     else:
-        raise TypeError("x must be uint16 (bf16 bits) or float32")
+        raise TypeError("x must be uint16 (bf16 / f16 bits) or float32")
     rc = fn(_ptr(x), _ptr(y), B, T, H, W, heads, head_dim, _ptr(sp), *[_ptr(t) for t in tb])
     if rc != 0:
         raise ValueError(f"oracle rejected shape={shape} split={tuple(split)}")

@@ -67,6 +67,67 @@ uint16_t oracle_f32_to_bf16(float f)
 }
 
 /* ------------------------------------------------------------------------- */
+/* IEEE binary16 <-> binary32 (1 sign, 5 exponent bits biased by 15, 10      */
+/* fraction bits; subnormals are fraction * 2^-24).                          */
+/* ------------------------------------------------------------------------- */
+
+float oracle_f16_to_f32(uint16_t h)
+{
+    const uint32_t sign = (uint32_t)(h >> 15);
+    const uint32_t exponent = (uint32_t)(h >> 10) & 0x1fu;
+    const uint32_t fraction = (uint32_t)h & 0x3ffu;
+    double magnitude;
+    if (exponent == 0x1fu) {
+        if (fraction == 0) {
+            magnitude = INFINITY;
+        } else {
+            /* NaN: widen the payload into the binary32 fraction, quiet bit set */
+            uint32_t bits = (sign << 31) | 0x7fc00000u | (fraction << 13);
+            float f;
+            memcpy(&f, &bits, sizeof f);
+            return f;
+        }
+    } else if (exponent == 0) {
+        magnitude = ldexp((double)fraction, -24);           /* subnormal or zero */
+    } else {
+        magnitude = ldexp((double)(fraction | 0x400u), (int)exponent - 25);
+    }
+    float f = (float)magnitude;                              /* exact */
+    return sign ? -f : f;
+}
+
+uint16_t oracle_f32_to_f16(float f)
+{
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    const uint16_t sign = (uint16_t)((bits >> 16) & 0x8000u);
+    const uint32_t mag = bits & 0x7fffffffu;
+    if (mag > 0x7f800000u)                                   /* NaN stays a quiet NaN */
+        return (uint16_t)(sign | 0x7e00u | ((mag >> 13) & 0x1ffu));
+    if (mag >= 0x477ff000u)                                  /* >= 65520: inf */
+        return (uint16_t)(sign | 0x7c00u);
+    if (mag >= 0x38800000u) {                                /* normal binary16 */
+        uint32_t h = ((mag >> 23) - 112u) << 10 | ((mag >> 13) & 0x3ffu);
+        const uint32_t rest = mag & 0x1fffu;                 /* 13 dropped bits */
+        if (rest > 0x1000u || (rest == 0x1000u && (h & 1u)))
+            h += 1;                                          /* may carry into the exponent */
+        return (uint16_t)(sign | h);
+    }
+    if (mag <= 0x33000000u)                                  /* <= 2^-25: rounds to zero */
+        return sign;
+    /* subnormal binary16: round |f| / 2^-24 to an integer, ties to even */
+    const uint32_t full = (mag & 0x7fffffu) | 0x800000u;
+    const int e = (int)(mag >> 23) - 127;                    /* -25 .. -15 */
+    const int shift = -e - 1;                                /* 14 .. 24 */
+    uint32_t m = full >> shift;
+    const uint32_t rest = full & ((1u << shift) - 1u);
+    const uint32_t half = 1u << (shift - 1);
+    if (rest > half || (rest == half && (m & 1u)))
+        m += 1;
+    return (uint16_t)(sign | m);
+}
+
+/* ------------------------------------------------------------------------- */
 /* Axis tables ("实现拆解" step 1).                                           */
 /* cos_out and sin_out are row-major [length][dim/2].                        */
 /* ------------------------------------------------------------------------- */
@@ -208,6 +269,36 @@ int oracle_rope3d_f32(const float *x, float *y,
                         rotate_head_f32(v, t, h, w, split, cos_tab, sin_tab);
                         for (int64_t ch = 0; ch < head_dim; ++ch)
                             dst[ch] = v[ch];
+                    }
+    return 0;
+}
+
+int oracle_rope3d_f16(const uint16_t *x, uint16_t *y,
+                      int64_t B, int64_t T, int64_t H, int64_t W,
+                      int64_t heads, int64_t head_dim, const int32_t split[3],
+                      const float *cos_t, const float *sin_t,
+                      const float *cos_h, const float *sin_h,
+                      const float *cos_w, const float *sin_w)
+{
+    if (check_shape(B, T, H, W, heads, head_dim, split) != 0 ||
+        head_dim > ORACLE_MAX_HEAD_DIM)
+        return -1;
+    const float *const cos_tab[3] = {cos_t, cos_h, cos_w};
+    const float *const sin_tab[3] = {sin_t, sin_h, sin_w};
+    float v[ORACLE_MAX_HEAD_DIM];
+    int64_t row = 0;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t h = 0; h < H; ++h)
+                for (int64_t w = 0; w < W; ++w)
+                    for (int64_t head = 0; head < heads; ++head, ++row) {
+                        const uint16_t *src = x + row * head_dim;
+                        uint16_t *dst = y + row * head_dim;
+                        for (int64_t ch = 0; ch < head_dim; ++ch)
+                            v[ch] = oracle_f16_to_f32(src[ch]);
+                        rotate_head_f32(v, t, h, w, split, cos_tab, sin_tab);
+                        for (int64_t ch = 0; ch < head_dim; ++ch)
+                            dst[ch] = oracle_f32_to_f16(v[ch]);
                     }
     return 0;
 }

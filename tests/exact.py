@@ -82,6 +82,44 @@ def rn_bf16_bits(x) -> int:
     return bits | (0x8000 if negative else 0)
 
 
+def rn_f16_bits(x) -> int:
+    """IEEE binary16 bit pattern of the nearest binary16 to the float32 value
+    x (ties to even; 11-bit significand, exponents -14..15, subnormals down to
+    2**-24; beyond the largest finite value, inf; the sign of zero is kept)."""
+    x = np.float32(x)
+    negative = bool(np.signbit(x))
+    mag = Fraction(0) if x == 0 else _round_to_format(exact(x), 11, emin=-14, emax=15)
+    if mag == float("inf"):
+        bits = 0x7C00
+    elif mag == 0:
+        bits = 0
+    else:
+        e = mag.numerator.bit_length() - mag.denominator.bit_length()
+        if Fraction(2) ** e > mag:
+            e -= 1
+        if e < -14:                       # subnormal: fraction * 2**-24
+            frac = mag / Fraction(2) ** -24
+            assert frac.denominator == 1
+            bits = int(frac)
+        else:
+            m = mag / Fraction(2) ** (e - 10)
+            assert m.denominator == 1 and 1024 <= m < 2048
+            bits = ((e + 15) << 10) | (int(m) - 1024)
+    return bits | (0x8000 if negative else 0)
+
+
+def f16_value(bits: int) -> Fraction | float:
+    """Exact value of a finite binary16 bit pattern (inf for infinities)."""
+    sign = -1 if bits & 0x8000 else 1
+    e = (bits >> 10) & 0x1F
+    f = bits & 0x3FF
+    if e == 0x1F:
+        return sign * float("inf")
+    if e == 0:
+        return sign * Fraction(f) * Fraction(2) ** -24
+    return sign * Fraction(f + 1024) * Fraction(2) ** (e - 25)
+
+
 def _neg(x) -> bool:
     return bool(np.signbit(np.float32(x)))
 

@@ -112,6 +112,43 @@ def pin_bf16_conversions(lib):
     assert (nan & 0x7F80) == 0x7F80 and (nan & 0x7F) != 0
 
 
+def pin_f16_conversions(lib):
+    # widening: every finite bit pattern against its exact value
+    for bits in range(1 << 16):
+        if (bits & 0x7C00) == 0x7C00 and (bits & 0x3FF):
+            assert math.isnan(oracle.f16_to_f32(bits, lib))
+            continue
+        got = oracle.f16_to_f32(bits, lib)
+        want = exact.f16_value(bits)
+        assert got == float(want), hex(bits)
+        assert math.copysign(1, got) == (-1 if bits & 0x8000 else 1), hex(bits)
+    # narrowing: nearest binary16, ties to even, against the exact-rational model
+    specials = [1.0, 65504.0, 65519.99, 65520.0, 70000.0, 2.0 ** -24, 2.0 ** -25,
+                3 * 2.0 ** -25, 2.0 ** -25 * 1.0000001, 5 * 2.0 ** -26, 2.0 ** -14,
+                2.0 ** -14 - 2.0 ** -25, 1 + 2 ** -11, 1 + 3 * 2 ** -11, 0.0, -0.0, 1e-30,
+                -1e-8, 3.1415926, 2049.0, 2051.0, float(np.finfo(np.float32).max)]
+    vals = [np.float32(v) for v in specials]
+    g = _rng(5)
+    vals += list(exact.bits_f32(int(b)) for b in g.integers(0x30000000, 0x48000000, 6000))
+    vals += list(np.float32(v) for v in _random_f32(2000, 6, 100.0))
+    for v in vals:
+        v = np.float32(v)
+        assert oracle.f32_to_f16(v, lib) == exact.rn_f16_bits(v), repr(v)
+    assert oracle.f32_to_f16(np.float32(np.inf), lib) == 0x7C00
+    nan = oracle.f32_to_f16(np.float32(np.nan), lib)
+    assert (nan & 0x7C00) == 0x7C00 and (nan & 0x3FF) != 0
+
+
+def pin_f16_bruteforce(lib):
+    shape, split = (2, 3, 5, 7, 3, 18), (4, 6, 8)
+    tabs = oracle.tables(3, 5, 7, split, 10000.0, lib)
+    x = _random_f32(int(np.prod(shape)), 18, 1.0).astype(np.float16)
+    y = oracle.rope3d(x.view(np.uint16), shape, split, tabs, lib, f16=True).view(np.float16)
+    ref = brute_force_complex(x.astype(np.float64), shape, split, 10000.0)
+    err = np.abs(y.astype(np.float64) - ref).reshape(-1, 2).max(axis=1)
+    assert np.all(err <= (2.0 ** -11 + 2e-6) * pair_norms(x.astype(np.float32)) + 2.0 ** -25), err.max()
+
+
 def pin_rotate_pair_rounding(lib):
     # A product that rounds away only without fusion: e*c = 1 - 2**-46 rounds
     # to 1, so y0 = 1 - 1 = 0 exactly; a fused multiply-subtract gives -2**-46.
@@ -254,7 +291,8 @@ def pin_sampled_matches_full(lib):
 
 
 PINS = [
-    pin_bf16_conversions, pin_rotate_pair_rounding, pin_tables_high_precision,
+    pin_bf16_conversions, pin_f16_conversions, pin_f16_bruteforce,
+    pin_rotate_pair_rounding, pin_tables_high_precision,
     pin_complex_bruteforce, pin_position_zero_identity, pin_norm_preserved,
     pin_rotate_back, pin_marker_tables, pin_sampled_matches_full,
 ]
@@ -296,6 +334,11 @@ MUTATIONS = {
     "bf16_ties_away": ("uint32_t rounded = bits + 0x7fffu + kept_lsb;",
                        "uint32_t rounded = bits + 0x8000u;"),
     "sample_decode": ("const int64_t w = token % W;", "const int64_t w = token % H;"),
+    "f16_ties_away": ("if (rest > 0x1000u || (rest == 0x1000u && (h & 1u)))",
+                      "if (rest >= 0x1000u)"),
+    "f16_subnormal_shift": ("const int shift = -e - 1;", "const int shift = -e;"),
+    "f16_overflow_edge": ("if (mag >= 0x477ff000u)", "if (mag >= 0x477fe000u)"),
+    "f16_widen_bias": ("(int)exponent - 25", "(int)exponent - 24"),
 }
 
 
