@@ -23,6 +23,7 @@ rank's time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -44,10 +45,7 @@ import synthetic  # noqa: E402
 METRIC = "fused 3D RoPE Q+K: achieved HBM GB/s and % of GB300 peak; bit-exact vs oracle"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = [
-    os.path.join(ROOT, "rope_rope3d_apply_gb300", "csrc", "rope3d_kernels.cu"),
-    os.path.join(ROOT, "rope_rope3d_apply_gb300", "csrc", "rope3d_internal.h"),
-]
+KERNEL_SOURCES = [os.path.join(ROOT, "rope_rope3d_apply_gb300", "csrc", "rope3d_kernels.cu")]
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "rope3d_vec16_bf16_large.md")
 
 
@@ -61,6 +59,9 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
+    p.add_argument("--variant", default="contiguous", choices=["contiguous", "f16", "qkv_inplace"],
+                   help="contiguous Q/K (default); the same in fp16; or Q and K as views of a "
+                        "fused [B, N, 3, heads, head_dim] QKV buffer rotated in place")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
@@ -316,25 +317,38 @@ def run_ours(args, w):
     r.load_library()
 
     # inputs: pinned host buffers (also the end-to-end inputs), then device copies
-    np_dt = np.uint16 if w.dtype == "bf16" else np.float32
-    t_dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    np_dt = np.float32 if w.dtype == "f32" else np.uint16
+    t_dtype = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[w.dtype]
     shp = (w.B, w.N, w.heads, w.head_dim)
     host = [torch.empty(w.numel * w.elem_bytes, dtype=torch.uint8).pin_memory() for _ in range(4)]
     hq, hk, hqo, hko = (h.numpy().view(np_dt).reshape(shp) for h in host)
     synthetic.qk(w, hq.reshape(-1), hk.reshape(-1))
-    q = host[0].to(dev).view(t_dtype).view(shp)
-    k = host[1].to(dev).view(t_dtype).view(shp)
-    qo = torch.empty_like(q)
-    ko = torch.empty_like(k)
     tabs = r.rope3d_build_tables(w.T, w.H, w.W, w.split, w.base)
     stream = torch.cuda.current_stream(dev)
+    if args.variant == "qkv_inplace":
+        qkv = torch.zeros((w.B, w.N, 3, w.heads, w.head_dim), dtype=t_dtype, device=dev)
+        q, k = qkv[:, :, 0], qkv[:, :, 1]
+        q.copy_(host[0].to(dev).view(t_dtype).view(shp))
+        k.copy_(host[1].to(dev).view(t_dtype).view(shp))
+
+        def step():
+            r.rope3d_apply_pair_strided(q, k, tabs, q, k, stream=stream)
+    else:
+        q = host[0].to(dev).view(t_dtype).view(shp)
+        k = host[1].to(dev).view(t_dtype).view(shp)
+        qo = torch.empty_like(q)
+        ko = torch.empty_like(k)
+
+        def step():
+            r.rope3d_apply_pair(q, k, tabs, qo, ko, stream=stream)
 
     # warm-up (the first call also runs the library's bit-exact gate)
     for _ in range(max(args.warmup, 3)):
-        r.rope3d_apply_pair(q, k, tabs, qo, ko, stream=stream)
+        step()
     torch.cuda.synchronize(dev)
-    dt_code = r.BF16 if w.dtype == "bf16" else r.F32
-    verdict = r.rope3d_gate_verdict(w.B, w.T, w.H, w.W, w.heads, w.head_dim, w.split, w.base, dt_code)
+    dt_code = {"bf16": r.BF16, "f16": r.F16, "f32": r.F32}[w.dtype]
+    verdict = (r.rope3d_gate_verdict(w.B, w.T, w.H, w.W, w.heads, w.head_dim, w.split, w.base, dt_code)
+               if args.variant != "qkv_inplace" else 1)  # a strided call that returned was verified
     launch = r.rope3d_last_launch()
     launches_per_step = launches_per_call(w, launch["kernel"])
 
@@ -350,7 +364,7 @@ def run_ours(args, w):
     t_wall0 = time.time()
     for i in range(args.steps):
         starts[i].record(stream)
-        r.rope3d_apply_pair(q, k, tabs, qo, ko, stream=stream)
+        step()
         ends[i].record(stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
@@ -372,7 +386,7 @@ def run_ours(args, w):
 
     # end to end through the host-buffer entry point (copies inside the timed region)
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.variant != "qkv_inplace":
         r.rope3d_apply_pair_host(hq, hk, hqo, hko, tabs)  # warm-up: staging allocation
         if dist:
             dist.barrier()
@@ -392,7 +406,8 @@ def run_ours(args, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
-            "config": dict(workload_config(w), parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
+            "config": dict(workload_config(w), variant=args.variant,
+                           parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
             "token_heads_per_s": world * args.steps * w.token_heads / (total_ms / 1e3),
             "pct_of_peak_hbm": 100.0 * achieved / peak,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -418,6 +433,8 @@ def run_ours(args, w):
 def main():
     args = parse_args()
     w = synthetic.WORKLOADS[args.workload]
+    if args.variant == "f16":
+        w = dataclasses.replace(w, dtype="f16")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

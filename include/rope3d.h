@@ -40,7 +40,7 @@ extern "C" {
 #define ROPE3D_ERR_NULL     -1  /* a required pointer is NULL                     */
 #define ROPE3D_ERR_SHAPE    -2  /* a size <= 0, head_dim != d_T+d_H+d_W, a chunk
                                    odd or <= 0, or a size beyond the limits below  */
-#define ROPE3D_ERR_DTYPE    -3  /* dtype is not ROPE3D_BF16 or ROPE3D_F32         */
+#define ROPE3D_ERR_DTYPE    -3  /* dtype is not ROPE3D_BF16, ROPE3D_F32 or ROPE3D_F16 */
 #define ROPE3D_ERR_ALIGN    -4  /* a Q/K/output pointer is not 4-byte aligned     */
 #define ROPE3D_ERR_ALIAS    -5  /* an output overlaps an input or the other output */
 #define ROPE3D_ERR_DEVICE   -6  /* a pointer is not memory of the expected kind on
@@ -58,6 +58,8 @@ extern "C" {
 /* ---- element types ----------------------------------------------------- */
 #define ROPE3D_BF16 0   /* bfloat16 in and out                                */
 #define ROPE3D_F32  1   /* float32 in and out (same steps, identity cast)     */
+#define ROPE3D_F16  2   /* IEEE binary16 in and out (same steps, nearest-even
+                           cast to binary16)                                  */
 
 /* ---- limits -------------------------------------------------------------- */
 #define ROPE3D_MAX_HEAD_DIM 4096   /* head_dim above this -> ROPE3D_ERR_SHAPE  */
@@ -115,7 +117,7 @@ int rope3d_retain_tables(rope3d_tables *tables);
  *                 (q and k may overlap each other: they are only read)
  *   tables        a handle from rope3d_build_tables for the same T, H, W and
  *                 split
- *   dtype         ROPE3D_BF16 or ROPE3D_F32
+ *   dtype         ROPE3D_BF16, ROPE3D_F32 or ROPE3D_F16
  *   stream        cudaStream_t the kernel is launched on (NULL = default)
  *
  * The call is asynchronous on `stream`, except the first call for each
@@ -128,8 +130,8 @@ int rope3d_retain_tables(rope3d_tables *tables);
  * the refused call hold the kernel's result). So make the first call of a
  * configuration outside CUDA graph capture, or turn the gate off.
  *
- * 16-byte-aligned pointers with head_dim and every chunk a multiple of 8 (bf16)
- * or 4 (fp32) elements take the 16-byte vector kernel; any other valid input
+ * 16-byte-aligned pointers with head_dim and every chunk a multiple of 8 (bf16,
+ * fp16) or 4 (fp32) elements take the 16-byte vector kernel; any other valid input
  * takes the per-pair kernel with the same arithmetic.
  * Errors: NULL, SHAPE, DTYPE, ALIGN, ALIAS, DEVICE (a pointer that is not
  * device or managed memory of the current device), TABLES, PARITY, CUDA.
@@ -139,6 +141,56 @@ int rope3d_apply_pair(const void *q, const void *k, void *q_out, void *k_out,
                       int64_t B, int64_t T, int64_t H, int64_t W,
                       int64_t heads, int64_t head_dim, const int32_t split[3],
                       int32_t dtype, void *stream);
+
+/*
+ * rope3d_apply_pair_strided -- rope3d_apply_pair for strided views, including
+ * rotation in place. This extends the pages' kernel, whose preflight demands
+ * contiguous Q and K ("关键源码片段", can_use_ltx25_decoder_rope: is_contiguous),
+ * so that Q and K can be read straight out of a fused QKV projection buffer,
+ * out of a crop of a larger grid, and written back in place, without the copy
+ * that contiguity forces. Same arithmetic and tables.
+ *
+ *   q, k, q_out, k_out  device pointers to element (0, 0, 0, 0, 0, 0) of each
+ *                       view of logical shape [B, T, H, W, heads, head_dim]
+ *   *_strides           element strides of (batch, t, h, w, head), each >= 0;
+ *                       channels are contiguous (stride 1). For 16-bit types
+ *                       every stride must be even (pairs stay 4-byte aligned).
+ *   other arguments     as for rope3d_apply_pair
+ *
+ * In place: q_out == q with the same strides (and/or k_out == k) is allowed.
+ * Otherwise no element of an output may be an element of an input or of the
+ * other output: views whose address ranges intersect are accepted only when
+ * they have identical strides and provably disjoint elements (e.g. the Q, K
+ * and V thirds of one fused buffer); an output view must not map two indices
+ * to one element. Violations return ROPE3D_ERR_ALIAS.
+ * The gate works as in rope3d_apply_pair; its first-call check gathers the
+ * views into temporary contiguous device buffers (allocated and freed by
+ * that call; the inputs are gathered before the kernel runs, so in-place
+ * calls are checked too). Its key adds the four stride sets.
+ * Errors: as rope3d_apply_pair; ALIGN also for odd strides of 16-bit types;
+ * SHAPE for negative strides; NOMEM when the gate's buffers cannot be allocated.
+ */
+int rope3d_apply_pair_strided(const void *q, const void *k, void *q_out, void *k_out,
+                              const rope3d_tables *tables,
+                              int64_t B, int64_t T, int64_t H, int64_t W,
+                              int64_t heads, int64_t head_dim, const int32_t split[3],
+                              int32_t dtype,
+                              const int64_t q_strides[5], const int64_t k_strides[5],
+                              const int64_t q_out_strides[5], const int64_t k_out_strides[5],
+                              void *stream);
+
+/*
+ * rope3d_preflight_strided -- the checks of rope3d_apply_pair_strided without
+ * a launch; check_device = 0 skips the device-memory query (no GPU needed).
+ */
+int rope3d_preflight_strided(const void *q, const void *k, const void *q_out,
+                             const void *k_out, const rope3d_tables *tables,
+                             int64_t B, int64_t T, int64_t H, int64_t W,
+                             int64_t heads, int64_t head_dim, const int32_t split[3],
+                             int32_t dtype,
+                             const int64_t q_strides[5], const int64_t k_strides[5],
+                             const int64_t q_out_strides[5], const int64_t k_out_strides[5],
+                             int32_t check_device);
 
 /*
  * rope3d_apply_pair_host -- the same rotation for HOST buffers: the library

@@ -26,13 +26,14 @@ __all__ = [
     "rope3d_testing_corrupt_gate", "rope3d_last_launch", "rope3d_status_string",
     "rope3d_release_scratch", "rope3d_testing_fastdiv", "rope3d_testing_host_tables",
     "rope3d_testing_max_units_per_launch", "rope3d_apply_pair_noalloc",
-    "STATUS", "BF16", "F32", "GATE_OFF", "GATE_FIRST", "LIB_PATH",
+    "STATUS", "BF16", "F32", "F16", "GATE_OFF", "GATE_FIRST", "LIB_PATH",
+    "rope3d_apply_pair_strided", "rope3d_preflight_strided", "view_strides",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "librope3d.so")
 
-BF16, F32 = 0, 1
+BF16, F32, F16 = 0, 1, 2
 GATE_OFF, GATE_FIRST = 0, 1
 STATUS = {
     0: "OK", -1: "ERR_NULL", -2: "ERR_SHAPE", -3: "ERR_DTYPE", -4: "ERR_ALIGN",
@@ -80,6 +81,10 @@ def _declare(lib):
         "rope3d_testing_host_tables": ([i32], c.c_int),
         "rope3d_testing_max_units_per_launch": ([i64], c.c_int),
         "rope3d_apply_pair_noalloc": ([vp, vp, vp, vp] + [i64] * 6 + [vp, dbl, i32, vp], c.c_int),
+        "rope3d_apply_pair_strided": ([vp, vp, vp, vp, vp] + [i64] * 6 + [vp, i32] + [vp] * 4 + [vp],
+                                      c.c_int),
+        "rope3d_preflight_strided": ([vp, vp, vp, vp, vp] + [i64] * 6 + [vp, i32] + [vp] * 4 + [i32],
+                                     c.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -143,7 +148,9 @@ def _dtype_code(x) -> int:
         return BF16
     if dt in ("torch.float32", "float32"):
         return F32
-    raise TypeError(f"unsupported dtype {dt} (bfloat16 or float32)")
+    if dt in ("torch.float16", "float16"):
+        return F16
+    raise TypeError(f"unsupported dtype {dt} (bfloat16, float16 or float32)")
 
 
 def _contiguous(x) -> bool:
@@ -278,6 +285,72 @@ def rope3d_apply_pair_noalloc(q, k, q_out, k_out, T: int, H: int, W: int, split,
         _split(split), float(base), dt, _stream(stream, q))
     _check(rc, "rope3d_apply_pair_noalloc")
     return q_out, k_out
+
+
+def view_strides(x, T: int, H: int, W: int):
+    """(B, heads, head_dim) and the element strides of (batch, t, h, w, head)
+    of a [B, T, H, W, heads, head_dim] or [B, T*H*W, heads, head_dim] view
+    whose channels are contiguous."""
+    shape = tuple(int(v) for v in x.shape)
+    if hasattr(x, "stride") and callable(x.stride):
+        st = tuple(int(v) for v in x.stride())
+    else:  # numpy: byte strides
+        st = tuple(int(v) // x.itemsize for v in x.strides)
+    if st[-1] != 1 and shape[-1] > 1:
+        raise ValueError("channels (the last dimension) must be contiguous")
+    if len(shape) == 6:
+        if shape[1:4] != (T, H, W):
+            raise ValueError(f"view grid {shape[1:4]} != tables grid {(T, H, W)}")
+        return (shape[0], shape[4], shape[5]), st[:5]
+    if len(shape) == 4:
+        if shape[1] != T * H * W:
+            raise ValueError(f"view has {shape[1]} tokens, the tables' grid has {T * H * W}")
+        sn = st[1]
+        return (shape[0], shape[2], shape[3]), (st[0], H * W * sn, W * sn, sn, st[2])
+    raise ValueError("expected [B, T*H*W, heads, head_dim] or [B, T, H, W, heads, head_dim]")
+
+
+def _strides_arg(st):
+    return (ctypes.c_int64 * 5)(*[int(v) for v in st])
+
+
+def rope3d_apply_pair_strided(q, k, tables: Tables, q_out=None, k_out=None, stream=None):
+    """Rotate strided device views (e.g. Q and K slices of a fused QKV
+    buffer); q_out=q and k_out=k rotate in place. Missing outputs are
+    allocated contiguous with torch.empty."""
+    if q_out is None or k_out is None:
+        import torch
+
+        q_out = torch.empty(q.shape, dtype=q.dtype, device=q.device) if q_out is None else q_out
+        k_out = torch.empty(k.shape, dtype=k.dtype, device=k.device) if k_out is None else k_out
+    geo, sts = None, []
+    for name, t in (("q", q), ("k", k), ("q_out", q_out), ("k_out", k_out)):
+        g, st = view_strides(t, tables.T, tables.H, tables.W)
+        if geo is not None and g != geo:
+            raise ValueError(f"{name} has (B, heads, head_dim) {g}, q has {geo}")
+        geo = g
+        sts.append(_strides_arg(st))
+    dt = _dtype_code(q)
+    for t in (k, q_out, k_out):
+        if _dtype_code(t) != dt:
+            raise TypeError("q, k, q_out and k_out must have one dtype")
+    B, heads, head_dim = geo
+    rc = load_library().rope3d_apply_pair_strided(
+        _ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), tables.handle, B, tables.T, tables.H,
+        tables.W, heads, head_dim, _split(tables.split), dt, *sts, _stream(stream, q))
+    _check(rc, "rope3d_apply_pair_strided")
+    return q_out, k_out
+
+
+def rope3d_preflight_strided(ptrs, strides, tables, B, T, H, W, heads, head_dim, split, dtype,
+                             check_device=True) -> int:
+    """Status that rope3d_apply_pair_strided would return before launching.
+    ptrs: (q, k, q_out, k_out) addresses; strides: four 5-tuples (or None)."""
+    handle = tables.handle if isinstance(tables, Tables) else (tables or 0)
+    sts = [None if st is None else _strides_arg(st) for st in strides]
+    return load_library().rope3d_preflight_strided(
+        *[_ptr(p) for p in ptrs], handle, int(B), int(T), int(H), int(W), int(heads),
+        int(head_dim), _split(split), int(dtype), *sts, 1 if check_device else 0)
 
 
 def rope3d_preflight(q, k, q_out, k_out, tables, B, T, H, W, heads, head_dim, split, dtype,

@@ -17,6 +17,7 @@
 // Build with -ffp-contract=off: the gate's CPU rotation must round every
 // product and sum on its own, like the kernel.
 #include <algorithm>
+#include <array>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -307,7 +308,8 @@ struct Geom {
 };
 
 int check_geom(const Geom &g) {
-    if (g.dtype != ROPE3D_BF16 && g.dtype != ROPE3D_F32) return ROPE3D_ERR_DTYPE;
+    if (g.dtype != ROPE3D_BF16 && g.dtype != ROPE3D_F32 && g.dtype != ROPE3D_F16)
+        return ROPE3D_ERR_DTYPE;
     if (g.B <= 0 || g.heads <= 0 || g.head_dim <= 0) return ROPE3D_ERR_SHAPE;
     int rc = check_grid(g.T, g.H, g.W, g.split);
     if (rc != ROPE3D_OK) return rc;
@@ -459,6 +461,60 @@ inline uint16_t narrow_bf16(float f) {
     return static_cast<uint16_t>(upper);
 }
 
+// binary16 <-> float for the gate, from the format's layout (5 exponent bits
+// biased by 15, 10 fraction bits, subnormals fraction * 2^-24).
+inline float widen_f16(uint16_t h) {
+    const uint32_t sign = static_cast<uint32_t>(h & 0x8000u) << 16;
+    const uint32_t e = (h >> 10) & 0x1fu;
+    const uint32_t m = h & 0x3ffu;
+    uint32_t bits;
+    if (e == 0x1fu) {
+        bits = sign | 0x7f800000u | (m << 13);
+    } else if (e != 0) {
+        bits = sign | ((e + 112u) << 23) | (m << 13);
+    } else if (m == 0) {
+        bits = sign;
+    } else {
+        // subnormal: normalise the fraction
+        uint32_t mm = m;
+        uint32_t shift = 0;
+        while (!(mm & 0x400u)) {
+            mm <<= 1;
+            ++shift;
+        }
+        bits = sign | ((113u - shift) << 23) | ((mm & 0x3ffu) << 13);
+    }
+    float f;
+    std::memcpy(&f, &bits, 4);
+    return f;
+}
+
+inline uint16_t narrow_f16(float f) {
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    const uint32_t sign = (u >> 16) & 0x8000u;
+    const int32_t exp = static_cast<int32_t>((u >> 23) & 0xffu);
+    const uint32_t mant = u & 0x7fffffu;
+    if (exp == 0xff) return static_cast<uint16_t>(sign | 0x7c00u | (mant ? 0x200u | (mant >> 13) : 0u));
+    if (exp == 0) return static_cast<uint16_t>(sign);  // far below the smallest binary16
+    const int32_t e16 = exp - 112;                     // binary16 biased exponent
+    const uint32_t sig = mant | 0x800000u;             // 24-bit significand
+    const int32_t shift = e16 >= 1 ? 13 : 14 - e16;    // bits dropped from sig
+    if (shift >= 25) return static_cast<uint16_t>(sign);  // below half the smallest subnormal
+    uint32_t kept = sig >> shift;
+    const uint32_t dropped = sig & ((1u << shift) - 1u);
+    const uint32_t halfway = 1u << (shift - 1);
+    if (dropped > halfway || (dropped == halfway && (kept & 1u))) ++kept;
+    const uint32_t result = e16 >= 1 ? (static_cast<uint32_t>(e16) << 10) + (kept - 0x400u) : kept;
+    if (result >= 0x7c00u) return static_cast<uint16_t>(sign | 0x7c00u);
+    return static_cast<uint16_t>(sign | result);
+}
+
+inline bool same_or_both_nan_f16(uint16_t a, uint16_t b) {
+    if (a == b) return true;
+    return (a & 0x7fffu) > 0x7c00u && (b & 0x7fffu) > 0x7c00u;
+}
+
 inline bool same_or_both_nan_f32(uint32_t a, uint32_t b) {
     if (a == b) return true;
     return (a & 0x7fffffffu) > 0x7f800000u && (b & 0x7fffffffu) > 0x7f800000u;
@@ -514,6 +570,9 @@ int64_t verify_rows(const Geom &g, const rope3d_tables *t, const PairPlan &plan,
                 if (g.dtype == ROPE3D_BF16) {
                     ev = widen_bf16(static_cast<const uint16_t *>(in)[i]);
                     od = widen_bf16(static_cast<const uint16_t *>(in)[i + 1]);
+                } else if (g.dtype == ROPE3D_F16) {
+                    ev = widen_f16(static_cast<const uint16_t *>(in)[i]);
+                    od = widen_f16(static_cast<const uint16_t *>(in)[i + 1]);
                 } else {
                     ev = static_cast<const float *>(in)[i];
                     od = static_cast<const float *>(in)[i + 1];
@@ -528,6 +587,10 @@ int64_t verify_rows(const Geom &g, const rope3d_tables *t, const PairPlan &plan,
                     const uint16_t *o = static_cast<const uint16_t *>(out);
                     bad += !same_or_both_nan_bf16(narrow_bf16(y0), o[i]);
                     bad += !same_or_both_nan_bf16(narrow_bf16(y1), o[i + 1]);
+                } else if (g.dtype == ROPE3D_F16) {
+                    const uint16_t *o = static_cast<const uint16_t *>(out);
+                    bad += !same_or_both_nan_f16(narrow_f16(y0), o[i]);
+                    bad += !same_or_both_nan_f16(narrow_f16(y1), o[i + 1]);
                 } else {
                     const uint32_t *o = static_cast<const uint32_t *>(out);
                     uint32_t b0, b1;
@@ -715,6 +778,274 @@ extern "C" int rope3d_apply_pair(const void *q, const void *k, void *q_out, void
 }
 
 // ============================================================================
+// strided views and rotation in place
+// ============================================================================
+
+namespace {
+
+// A strided view of logical shape [B, T, H, W, heads, head_dim]: element
+// strides of the six dimensions (the channel stride is 1).
+struct View {
+    uintptr_t base;
+    int64_t n[6];
+    int64_t s[6];
+    int64_t esize;
+    uintptr_t lo() const { return base; }
+    uintptr_t hi() const {  // one past the last byte
+        int64_t last = 0;
+        for (int i = 0; i < 6; ++i) last += (n[i] - 1) * s[i];
+        return base + static_cast<uintptr_t>((last + 1) * esize);
+    }
+};
+
+View make_view(const void *p, const Geom &g, const int64_t st[5]) {
+    View v{reinterpret_cast<uintptr_t>(p), {g.B, g.T, g.H, g.W, g.heads, g.head_dim},
+           {st[0], st[1], st[2], st[3], st[4], 1}, g.esize};
+    return v;
+}
+
+// Is delta (elements) a difference of two element offsets of one view, i.e.
+// delta = sum_i d_i * s_i with |d_i| <= n_i - 1? Depth-first over the
+// dimensions by decreasing stride, bounding each d_i by what the smaller
+// dimensions can still reach. Gives up (answers yes) past `budget` nodes.
+bool reachable(int64_t delta, const std::vector<std::pair<int64_t, int64_t>> &dims, size_t k,
+               const std::vector<int64_t> &reach, int64_t *budget) {
+    if (--*budget < 0) return true;
+    if (k == dims.size()) return delta == 0;
+    const int64_t s = dims[k].first, n = dims[k].second;
+    const int64_t m = reach[k + 1];
+    if (s == 0) return reachable(delta, dims, k + 1, reach, budget);
+    // d * s in [delta - m, delta + m]
+    auto floor_div = [](int64_t a, int64_t b) { return a >= 0 ? a / b : -((-a + b - 1) / b); };
+    const int64_t lo = std::max(-(n - 1), -floor_div(-(delta - m), s));
+    const int64_t hi = std::min(n - 1, floor_div(delta + m, s));
+    for (int64_t d = lo; d <= hi; ++d)
+        if (reachable(delta - d * s, dims, k + 1, reach, budget)) return true;
+    return false;
+}
+
+std::vector<std::pair<int64_t, int64_t>> sorted_dims(const View &v) {
+    std::vector<std::pair<int64_t, int64_t>> dims;
+    for (int i = 0; i < 6; ++i)
+        if (v.n[i] > 1) dims.emplace_back(v.s[i], v.n[i]);
+    std::sort(dims.begin(), dims.end(), [](auto &a, auto &b) { return a.first > b.first; });
+    return dims;
+}
+
+// Could the two views share an element? Exact for views with identical
+// strides and sizes whose bases differ by a whole number of elements;
+// otherwise answered from the byte ranges.
+bool may_share(const View &a, const View &b) {
+    if (a.hi() <= b.lo() || b.hi() <= a.lo()) return false;
+    if (!std::equal(a.s, a.s + 6, b.s) || !std::equal(a.n, a.n + 6, b.n) || a.esize != b.esize)
+        return true;
+    const int64_t diff = static_cast<int64_t>(b.base) - static_cast<int64_t>(a.base);
+    if (diff % a.esize != 0) return true;
+    const auto dims = sorted_dims(a);
+    std::vector<int64_t> reach(dims.size() + 1, 0);
+    for (size_t k = dims.size(); k-- > 0;) reach[k] = reach[k + 1] + (dims[k].second - 1) * dims[k].first;
+    int64_t budget = 1 << 16;
+    return reachable(diff / a.esize, dims, 0, reach, &budget);
+}
+
+// Is there a nonzero (d_i), |d_i| <= n_i - 1, with sum_i d_i * s_i == delta?
+// Same search as reachable(), tracking whether some d_i is nonzero.
+bool reachable_nonzero(int64_t delta, const std::vector<std::pair<int64_t, int64_t>> &dims,
+                       size_t k, const std::vector<int64_t> &reach, bool nonzero,
+                       int64_t *budget) {
+    if (--*budget < 0) return true;
+    if (k == dims.size()) return delta == 0 && nonzero;
+    const int64_t s = dims[k].first, n = dims[k].second;
+    if (s == 0) return true;  // two indices along this dimension meet (n > 1)
+    const int64_t m = reach[k + 1];
+    auto floor_div = [](int64_t a, int64_t b) { return a >= 0 ? a / b : -((-a + b - 1) / b); };
+    const int64_t lo = std::max(-(n - 1), -floor_div(-(delta - m), s));
+    const int64_t hi = std::min(n - 1, floor_div(delta + m, s));
+    for (int64_t d = lo; d <= hi; ++d)
+        if (reachable_nonzero(delta - d * s, dims, k + 1, reach, nonzero || d != 0, budget))
+            return true;
+    return false;
+}
+
+// Does the view map two different indices to one element? Exact (a nonzero
+// index difference whose offset is zero), answering yes if the search runs
+// past its budget.
+bool self_overlapping(const View &v) {
+    const auto dims = sorted_dims(v);
+    std::vector<int64_t> reach(dims.size() + 1, 0);
+    for (size_t k = dims.size(); k-- > 0;) reach[k] = reach[k + 1] + (dims[k].second - 1) * dims[k].first;
+    int64_t budget = 1 << 16;
+    return reachable_nonzero(0, dims, 0, reach, false, &budget);
+}
+
+bool same_view(const View &a, const View &b) {
+    return a.base == b.base && std::equal(a.s, a.s + 6, b.s) && std::equal(a.n, a.n + 6, b.n);
+}
+
+int check_strided(const void *q, const void *k, const void *qo, const void *ko, const Geom &g,
+                  const int64_t *const st[4]) {
+    const void *ptrs[4] = {q, k, qo, ko};
+    for (int i = 0; i < 4; ++i)
+        if (!ptrs[i] || !st[i]) return ROPE3D_ERR_NULL;
+    const int64_t extents[5] = {g.B, g.T, g.H, g.W, g.heads};
+    for (int i = 0; i < 4; ++i)
+        for (int j = 0; j < 5; ++j) {
+            if (st[i][j] < 0 || st[i][j] > (int64_t(1) << 50)) return ROPE3D_ERR_SHAPE;
+            if (g.esize == 2 && extents[j] > 1 && (st[i][j] % 2) != 0) return ROPE3D_ERR_ALIGN;
+        }
+    for (const void *p : ptrs)
+        if (reinterpret_cast<uintptr_t>(p) % 4 != 0) return ROPE3D_ERR_ALIGN;
+    View v[4];
+    for (int i = 0; i < 4; ++i) v[i] = make_view(ptrs[i], g, st[i]);
+    // the whole footprint must stay inside the address space
+    for (int i = 0; i < 4; ++i)
+        if (v[i].hi() < v[i].lo()) return ROPE3D_ERR_SHAPE;
+    for (int o = 2; o < 4; ++o)
+        if (self_overlapping(v[o])) return ROPE3D_ERR_ALIAS;
+    // each output against each input (exact in-place identity allowed for its
+    // own input) and against the other output
+    const bool inplace_q = same_view(v[2], v[0]);
+    const bool inplace_k = same_view(v[3], v[1]);
+    if (!inplace_q && may_share(v[2], v[0])) return ROPE3D_ERR_ALIAS;
+    if (!inplace_k && may_share(v[3], v[1])) return ROPE3D_ERR_ALIAS;
+    if (may_share(v[2], v[1]) || may_share(v[3], v[0]) || may_share(v[2], v[3]))
+        return ROPE3D_ERR_ALIAS;
+    return ROPE3D_OK;
+}
+
+int preflight_strided(const void *q, const void *k, const void *qo, const void *ko,
+                      const rope3d_tables *tables, const Geom &g, const int32_t split[3],
+                      const int64_t *const st[4], bool check_device) {
+    if (!split) return ROPE3D_ERR_NULL;
+    int rc = check_geom(g);
+    if (rc != ROPE3D_OK) return rc;
+    rc = check_strided(q, k, qo, ko, g, st);
+    if (rc != ROPE3D_OK) return rc;
+    rc = check_tables(tables, g);
+    if (rc != ROPE3D_OK || !check_device) return rc;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return ROPE3D_ERR_CUDA;
+    if (tables->host_backed || tables->device != device) return ROPE3D_ERR_DEVICE;
+    for (const void *p : {q, k, qo, ko})
+        if (!is_device_ptr(p, device)) return ROPE3D_ERR_DEVICE;
+    return ROPE3D_OK;
+}
+
+using StridedKey = std::pair<GateKey, std::array<int64_t, 20>>;
+std::map<StridedKey, int> g_verdicts_strided;  // 1 verified, 2 refused
+
+bool vec16_strided_ok(const Geom &g, const void *const ptrs[4], const int64_t *const st[4]) {
+    const int64_t vec = 16 / g.esize;
+    if (g.head_dim % vec != 0) return false;
+    for (int a = 0; a < 3; ++a)
+        if (g.split[a] % vec != 0) return false;
+    const int64_t extents[5] = {g.B, g.T, g.H, g.W, g.heads};
+    for (int i = 0; i < 4; ++i) {
+        if (reinterpret_cast<uintptr_t>(ptrs[i]) % 16 != 0) return false;
+        for (int j = 0; j < 5; ++j)
+            if (extents[j] > 1 && st[i][j] % vec != 0) return false;
+    }
+    return true;
+}
+
+}  // namespace
+
+extern "C" int rope3d_preflight_strided(const void *q, const void *k, const void *q_out,
+                                        const void *k_out, const rope3d_tables *tables,
+                                        int64_t B, int64_t T, int64_t H, int64_t W,
+                                        int64_t heads, int64_t head_dim, const int32_t split[3],
+                                        int32_t dtype, const int64_t q_strides[5],
+                                        const int64_t k_strides[5],
+                                        const int64_t q_out_strides[5],
+                                        const int64_t k_out_strides[5], int32_t check_device) {
+    const Geom g = make_geom(B, T, H, W, heads, head_dim, split, dtype);
+    const int64_t *const st[4] = {q_strides, k_strides, q_out_strides, k_out_strides};
+    return preflight_strided(q, k, q_out, k_out, tables, g, split, st, check_device != 0);
+}
+
+extern "C" int rope3d_apply_pair_strided(const void *q, const void *k, void *q_out, void *k_out,
+                                         const rope3d_tables *tables, int64_t B, int64_t T,
+                                         int64_t H, int64_t W, int64_t heads, int64_t head_dim,
+                                         const int32_t split[3], int32_t dtype,
+                                         const int64_t q_strides[5], const int64_t k_strides[5],
+                                         const int64_t q_out_strides[5],
+                                         const int64_t k_out_strides[5], void *stream) {
+    const Geom g = make_geom(B, T, H, W, heads, head_dim, split, dtype);
+    const int64_t *const st[4] = {q_strides, k_strides, q_out_strides, k_out_strides};
+    int rc = preflight_strided(q, k, q_out, k_out, tables, g, split, st, true);
+    if (rc != ROPE3D_OK) return rc;
+
+    StridedKey key{gate_key(tables->device, g, tables->base), {}};
+    for (int i = 0; i < 4; ++i)
+        for (int j = 0; j < 5; ++j) key.second[i * 5 + j] = st[i][j];
+    bool verify = false;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        auto it = g_verdicts_strided.find(key);
+        if (it != g_verdicts_strided.end() && it->second == 2) return ROPE3D_ERR_PARITY;
+        verify = g_gate_mode.load() == ROPE3D_GATE_FIRST && it == g_verdicts_strided.end();
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t bytes = static_cast<size_t>(g.bytes());
+    void *copy[4] = {nullptr, nullptr, nullptr, nullptr};
+    auto free_copies = [&] {
+        for (void *&c : copy)
+            if (c) cudaFree(c), c = nullptr;
+    };
+    if (verify) {
+        // the inputs are gathered before the kernel runs: in-place calls overwrite them
+        for (void *&c : copy)
+            if (cudaMalloc(&c, bytes) != cudaSuccess) {
+                c = nullptr;
+                cudaGetLastError();
+                free_copies();
+                return ROPE3D_ERR_NOMEM;
+            }
+        for (int i = 0; i < 2; ++i)
+            if (rope3d::launch_gather(i == 0 ? q : k, st[i], copy[i], static_cast<int>(g.esize),
+                                      g.B, g.T, g.H, g.W, g.heads, g.head_dim, s) != cudaSuccess) {
+                free_copies();
+                return ROPE3D_ERR_CUDA;
+            }
+    }
+    const void *ptrs[4] = {q, k, q_out, k_out};
+    LaunchArgs a = make_launch(g, tables, q, k, q_out, k_out, g.rows(), 0,
+                               vec16_strided_ok(g, ptrs, st));
+    a.strided = true;
+    for (int i = 0; i < 4; ++i)
+        for (int j = 0; j < 5; ++j) a.strides[i][j] = st[i][j];
+    LaunchInfo info{};
+    if (rope3d::launch_rope3d(a, s, &info) != cudaSuccess) {
+        free_copies();
+        return ROPE3D_ERR_CUDA;
+    }
+    t_last = info;
+    if (!verify) return ROPE3D_OK;
+
+    for (int i = 0; i < 2; ++i)
+        if (rope3d::launch_gather(i == 0 ? q_out : k_out, st[2 + i], copy[2 + i],
+                                  static_cast<int>(g.esize), g.B, g.T, g.H, g.W, g.heads,
+                                  g.head_dim, s) != cudaSuccess) {
+            free_copies();
+            return ROPE3D_ERR_CUDA;
+        }
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+        free_copies();
+        return ROPE3D_ERR_CUDA;
+    }
+    int64_t bad;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);  // the staging is shared
+        bad = verify_device(g, tables, copy[0], copy[1], copy[2], copy[3], tables->device);
+    }
+    free_copies();
+    if (bad < 0) return ROPE3D_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_verdicts_strided[key] = bad == 0 ? 1 : 2;
+    return bad == 0 ? ROPE3D_OK : ROPE3D_ERR_PARITY;
+}
+
+// ============================================================================
 // host-buffer pipeline
 // ============================================================================
 
@@ -885,6 +1216,7 @@ extern "C" int rope3d_gate_get_mode(void) { return g_gate_mode.load(); }
 extern "C" int rope3d_gate_reset(void) {
     std::lock_guard<std::mutex> lock(g_mutex);
     g_verdicts.clear();
+    g_verdicts_strided.clear();
     g_corrupt.store(0);
     return ROPE3D_OK;
 }
@@ -935,7 +1267,7 @@ extern "C" const char *rope3d_status_string(int status) {
         case ROPE3D_OK: return "ROPE3D_OK";
         case ROPE3D_ERR_NULL: return "ROPE3D_ERR_NULL: a required pointer is NULL";
         case ROPE3D_ERR_SHAPE: return "ROPE3D_ERR_SHAPE: invalid sizes or split";
-        case ROPE3D_ERR_DTYPE: return "ROPE3D_ERR_DTYPE: dtype must be ROPE3D_BF16 or ROPE3D_F32";
+        case ROPE3D_ERR_DTYPE: return "ROPE3D_ERR_DTYPE: dtype must be ROPE3D_BF16, ROPE3D_F32 or ROPE3D_F16";
         case ROPE3D_ERR_ALIGN: return "ROPE3D_ERR_ALIGN: a pointer is not 4-byte aligned";
         case ROPE3D_ERR_ALIAS: return "ROPE3D_ERR_ALIAS: an output overlaps another buffer";
         case ROPE3D_ERR_DEVICE: return "ROPE3D_ERR_DEVICE: a pointer is not memory of the expected kind on the current device";

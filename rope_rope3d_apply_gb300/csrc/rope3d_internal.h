@@ -55,9 +55,21 @@ struct LaunchArgs {
     uint32_t heads, head_dim;
     uint64_t rows;          // (batch, token) rows in the buffers of this call
     uint64_t row0;          // global row index of the first row (host path chunks)
-    int dtype;              // ROPE3D_BF16 / ROPE3D_F32
+    int dtype;              // ROPE3D_BF16 / ROPE3D_F32 / ROPE3D_F16
     bool vec16;             // take the 16-byte vector kernel
+    // Strided views: element strides of (batch, t, h, w, head) for Q, K,
+    // Q_out, K_out (channels are contiguous). When `strided` is false the
+    // buffers are contiguous and the strides are unused.
+    bool strided;
+    int64_t strides[4][5];
 };
+
+// Copy a strided view ([B, T, H, W, heads, head_dim], element strides of
+// (batch, t, h, w, head), contiguous channels) into a contiguous buffer.
+// elem_bytes is 2 or 4.
+cudaError_t launch_gather(const void *src, const int64_t strides[5], void *dst, int elem_bytes,
+                          uint64_t B, uint32_t T, uint32_t H, uint32_t W, uint32_t heads,
+                          uint32_t head_dim, cudaStream_t stream);
 
 struct LaunchInfo {
     int kernel;  // 1 = vector, 2 = per-pair

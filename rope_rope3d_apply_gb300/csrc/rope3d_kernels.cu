@@ -10,9 +10,9 @@
 //
 // What differs from that kernel (which decodes one pair per thread with 64-bit
 // division and reads cos/sin with __ldg):
-//   * one thread owns a 16-byte vector of Q and the same vector of K (8 bf16 =
-//     4 pairs, or 4 fp32 = 2 pairs), loaded with streaming 128-bit loads that
-//     bypass L1, and stores the two results with evict-first 128-bit stores;
+//   * one thread owns a 16-byte vector of Q and the same vector of K (8 bf16 or
+//     fp16 = 4 pairs, or 4 fp32 = 2 pairs), loaded with streaming 128-bit loads
+//     that bypass L1, and stores the two results with evict-first 128-bit stores;
 //   * the three axis tables are staged once per CTA into shared memory as
 //     interleaved (cos, sin) float2 entries, so the 4 pairs of a vector read
 //     their 4 table entries with two 128-bit shared loads;
@@ -23,13 +23,20 @@
 //     32-bit multiply-high divisions by precomputed constants.
 // Inputs that cannot take 16-byte vectors (unaligned pointers, chunks that
 // are not a multiple of the vector) run the per-pair kernel, same arithmetic.
+// Strided views (Q and K taken straight out of a fused QKV buffer, a crop of a
+// larger grid, or rotation in place) run the strided variants of both kernels:
+// same arithmetic, addresses from per-tensor (batch, t, h, w, head) strides,
+// and loads through the coherent path so that in-place rotation is safe.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/rope3d.h"
 #include "rope3d_internal.h"
@@ -56,32 +63,72 @@ struct KParams {
     uint32_t row0_mod_N;    // first row of this launch, modulo N
 };
 
+// Element strides of (batch, t, h, w, head) for Q, K, Q_out, K_out, and the
+// batch index of the launch's first row (strided kernels only).
+struct KStrides {
+    long long s[4][5];
+    uint32_t b0;
+};
+
 __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) {
     return (__umulhi(n, f.mul) + n) >> f.shift;
 }
 
-// Entry index of the table entry for pair `pair_in_head` of row `row`.
-__device__ __forceinline__ uint32_t table_index(const KParams &p, uint32_t row,
+// Grid coordinates of row `row` of the launch: token (t, h, w) and the batch
+// offset from the launch's first batch.
+struct GridPos {
+    uint32_t t, h, w, db;
+};
+
+__device__ __forceinline__ GridPos grid_pos(const KParams &p, uint32_t row) {
+    const uint32_t q = fdiv(row, p.N);
+    uint32_t tok = row - q * p.N.d + p.row0_mod_N;
+    const uint32_t carry = tok >= p.N.d ? 1u : 0u;
+    tok -= carry * p.N.d;
+    GridPos g;
+    g.t = fdiv(tok, p.HW);
+    const uint32_t rem = tok - g.t * p.HW.d;
+    g.h = fdiv(rem, p.Wd);
+    g.w = rem - g.h * p.Wd.d;
+    g.db = q + carry;
+    return g;
+}
+
+// Entry index of the table entry for pair `pair_in_head` at grid position g.
+__device__ __forceinline__ uint32_t table_index(const KParams &p, const GridPos &g,
                                                 uint32_t pair_in_head) {
-    uint32_t tok = row - fdiv(row, p.N) * p.N.d + p.row0_mod_N;
-    tok = tok >= p.N.d ? tok - p.N.d : tok;
-    const uint32_t t = fdiv(tok, p.HW);
-    const uint32_t rem = tok - t * p.HW.d;
-    const uint32_t h = fdiv(rem, p.Wd);
-    const uint32_t w = rem - h * p.Wd.d;
-    const uint32_t it = t * p.pT + pair_in_head;
-    const uint32_t ih = p.offH + h * p.pH + (pair_in_head - p.pT);
-    const uint32_t iw = p.offW + w * p.pW + (pair_in_head - p.pT - p.pH);
+    const uint32_t it = g.t * p.pT + pair_in_head;
+    const uint32_t ih = p.offH + g.h * p.pH + (pair_in_head - p.pT);
+    const uint32_t iw = p.offW + g.w * p.pW + (pair_in_head - p.pT - p.pH);
     return pair_in_head < p.pT ? it : (pair_in_head < p.pT + p.pH ? ih : iw);
+}
+
+// Element offset of (row at g, head, channel) in tensor i of a strided call.
+__device__ __forceinline__ long long strided_offset(const KStrides &st, int i, const GridPos &g,
+                                                    uint32_t head, uint32_t channel) {
+    const long long *s = st.s[i];
+    return (long long)(st.b0 + g.db) * s[0] + (long long)g.t * s[1] + (long long)g.h * s[2] +
+           (long long)g.w * s[3] + (long long)head * s[4] + channel;
 }
 
 // ---- memory access ---------------------------------------------------------
 
+// Read-only streaming load (inputs never alias outputs in contiguous calls).
 __device__ __forceinline__ uint4 ld_stream_v4(const void *ptr) {
     uint4 r;
     asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
         : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
         : "l"(ptr));
+    return r;
+}
+
+// Coherent streaming load (strided calls, which may rotate in place).
+__device__ __forceinline__ uint4 ld_coherent_v4(const void *ptr) {
+    uint4 r;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(ptr)
+                 : "memory");
     return r;
 }
 
@@ -112,27 +159,43 @@ __device__ __forceinline__ Rot rotate(float even, float odd, float c, float s) {
     return Rot{__fsub_rn(even_cos, odd_sin), __fadd_rn(even_sin, odd_cos)};
 }
 
-// One 32-bit word holding a bf16 pair: the even element is the low half
-// (lower address). bf16 -> f32 widening is a 16-bit shift.
-__device__ __forceinline__ uint32_t rotate_bf16_word(uint32_t word, float c, float s) {
-    const float even = __uint_as_float(word << 16);
-    const float odd = __uint_as_float(word & 0xffff0000u);
+// One 32-bit word holding a 16-bit pair: the even element is the low half
+// (lower address). bf16 -> f32 widening is a 16-bit shift; binary16 is widened
+// exactly by the conversion instruction. Both narrow to nearest, ties to even.
+template <int kType>
+__device__ __forceinline__ uint32_t rotate_word16(uint32_t word, float c, float s) {
+    float even, odd;
+    if constexpr (kType == ROPE3D_BF16) {
+        even = __uint_as_float(word << 16);
+        odd = __uint_as_float(word & 0xffff0000u);
+    } else {
+        __half2 h;
+        memcpy(&h, &word, sizeof h);
+        const float2 f = __half22float2(h);
+        even = f.x;
+        odd = f.y;
+    }
     const Rot r = rotate(even, odd, c, s);
-    const __nv_bfloat162 packed = __floats2bfloat162_rn(r.y0, r.y1);  // .x = y0 (low)
     uint32_t out;
-    memcpy(&out, &packed, sizeof out);
+    if constexpr (kType == ROPE3D_BF16) {
+        const __nv_bfloat162 packed = __floats2bfloat162_rn(r.y0, r.y1);  // .x = y0 (low)
+        memcpy(&out, &packed, sizeof out);
+    } else {
+        const __half2 packed = __floats2half2_rn(r.y0, r.y1);  // .x = y0 (low)
+        memcpy(&out, &packed, sizeof out);
+    }
     return out;
 }
 
-template <bool kBf16>
+template <int kType>
 __device__ __forceinline__ uint4 rotate_vec(const uint4 v, const float4 cs01, const float4 cs23) {
     uint4 o;
-    if constexpr (kBf16) {
-        // 8 bf16 = 4 pairs; entries (c0, s0, c1, s1) and (c2, s2, c3, s3)
-        o.x = rotate_bf16_word(v.x, cs01.x, cs01.y);
-        o.y = rotate_bf16_word(v.y, cs01.z, cs01.w);
-        o.z = rotate_bf16_word(v.z, cs23.x, cs23.y);
-        o.w = rotate_bf16_word(v.w, cs23.z, cs23.w);
+    if constexpr (kType != ROPE3D_F32) {
+        // 8 16-bit elements = 4 pairs; entries (c0, s0, c1, s1) and (c2, s2, c3, s3)
+        o.x = rotate_word16<kType>(v.x, cs01.x, cs01.y);
+        o.y = rotate_word16<kType>(v.y, cs01.z, cs01.w);
+        o.z = rotate_word16<kType>(v.z, cs23.x, cs23.y);
+        o.w = rotate_word16<kType>(v.w, cs23.z, cs23.w);
     } else {
         // 4 fp32 = 2 pairs; entries (c0, s0, c1, s1)
         const Rot a = rotate(__uint_as_float(v.x), __uint_as_float(v.y), cs01.x, cs01.y);
@@ -167,17 +230,26 @@ __device__ __forceinline__ float4 tab4(const float2 *tab, uint32_t idx) {
     }
 }
 
-// ---- 16-byte vector kernel ---------------------------------------------------
+template <bool kSmem>
+__device__ __forceinline__ float2 tab1(const float2 *tab, uint32_t idx) {
+    if constexpr (kSmem) {
+        return tab[idx];
+    } else {
+        return __ldg(tab + idx);
+    }
+}
+
+// ---- 16-byte vector kernel, contiguous buffers -----------------------------
 // Requires: 16-byte aligned pointers, head_dim and each chunk a multiple of the
 // vector's element count (so a vector never straddles a chunk, head or row, and
-// the first table entry of a vector is a multiple of 4 (bf16) or 2 (fp32)).
+// the first table entry of a vector is a multiple of 4 (16-bit) or 2 (fp32)).
 
-template <bool kBf16, bool kSmem>
+template <int kType, bool kSmem>
 __global__ void __launch_bounds__(kBlock)
-rope3d_vec16_kernel(const KParams p) {
+rope3d_vec16_kernel(const KParams p, const KStrides) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const float2 *tab = stage_tables<kSmem>(p, reinterpret_cast<float2 *>(smem_raw));
-    constexpr uint32_t kPairsPerVec = kBf16 ? 4 : 2;
+    constexpr uint32_t kPairsPerVec = kType == ROPE3D_F32 ? 2 : 4;
 
     const uint4 *q = static_cast<const uint4 *>(p.q);
     const uint4 *k = static_cast<const uint4 *>(p.k);
@@ -202,14 +274,14 @@ rope3d_vec16_kernel(const KParams p) {
             const uint32_t row = fdiv(vv, p.per_row);
             const uint32_t r = vv - row * p.per_row.d;
             const uint32_t g = r - fdiv(r, p.per_head) * p.per_head.d;
-            idx[u] = table_index(p, row, g * kPairsPerVec);
+            idx[u] = table_index(p, grid_pos(p, row), g * kPairsPerVec);
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const float4 cs01 = tab4<kSmem>(tab, idx[u]);
-            const float4 cs23 = kBf16 ? tab4<kSmem>(tab, idx[u] + 2) : cs01;
-            st_stream_v4(qo + v + u * stride, rotate_vec<kBf16>(qv[u], cs01, cs23));
-            st_stream_v4(ko + v + u * stride, rotate_vec<kBf16>(kv[u], cs01, cs23));
+            const float4 cs23 = kType != ROPE3D_F32 ? tab4<kSmem>(tab, idx[u] + 2) : cs01;
+            st_stream_v4(qo + v + u * stride, rotate_vec<kType>(qv[u], cs01, cs23));
+            st_stream_v4(ko + v + u * stride, rotate_vec<kType>(kv[u], cs01, cs23));
         }
     }
     // ragged tail: at most kUnroll - 1 more vectors per thread
@@ -219,67 +291,184 @@ rope3d_vec16_kernel(const KParams p) {
         const uint32_t row = fdiv(v, p.per_row);
         const uint32_t r = v - row * p.per_row.d;
         const uint32_t g = r - fdiv(r, p.per_head) * p.per_head.d;
-        const uint32_t i = table_index(p, row, g * kPairsPerVec);
+        const uint32_t i = table_index(p, grid_pos(p, row), g * kPairsPerVec);
         const float4 cs01 = tab4<kSmem>(tab, i);
-        const float4 cs23 = kBf16 ? tab4<kSmem>(tab, i + 2) : cs01;
-        st_stream_v4(qo + v, rotate_vec<kBf16>(qv, cs01, cs23));
-        st_stream_v4(ko + v, rotate_vec<kBf16>(kv, cs01, cs23));
+        const float4 cs23 = kType != ROPE3D_F32 ? tab4<kSmem>(tab, i + 2) : cs01;
+        st_stream_v4(qo + v, rotate_vec<kType>(qv, cs01, cs23));
+        st_stream_v4(ko + v, rotate_vec<kType>(kv, cs01, cs23));
     }
 }
 
-// ---- per-pair kernel (any valid alignment and split) -------------------------
+// ---- 16-byte vector kernel, strided views ----------------------------------
+// Requires, besides the contiguous kernel's conditions, every stride a multiple
+// of the vector's element count.
 
-template <bool kBf16, bool kSmem>
+template <int kType, bool kSmem>
 __global__ void __launch_bounds__(kBlock)
-rope3d_pair_kernel(const KParams p) {
+rope3d_vec16_strided_kernel(const KParams p, const KStrides st) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const float2 *tab = stage_tables<kSmem>(p, reinterpret_cast<float2 *>(smem_raw));
+    constexpr uint32_t kPairsPerVec = kType == ROPE3D_F32 ? 2 : 4;
+    constexpr uint32_t kElemsPerVec = 2 * kPairsPerVec;
+    constexpr int kElemBytes = kType == ROPE3D_F32 ? 4 : 2;
+
+    const char *q = static_cast<const char *>(p.q);
+    const char *k = static_cast<const char *>(p.k);
+    char *qo = static_cast<char *>(p.q_out);
+    char *ko = static_cast<char *>(p.k_out);
+
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t v = blockIdx.x * blockDim.x + threadIdx.x; v < p.units; v += stride) {
+        const uint32_t row = fdiv(v, p.per_row);
+        const uint32_t r = v - row * p.per_row.d;
+        const uint32_t head = fdiv(r, p.per_head);
+        const uint32_t g = r - head * p.per_head.d;
+        const GridPos pos = grid_pos(p, row);
+        const uint32_t channel = g * kElemsPerVec;
+        const uint4 qv = ld_coherent_v4(q + strided_offset(st, 0, pos, head, channel) * kElemBytes);
+        const uint4 kv = ld_coherent_v4(k + strided_offset(st, 1, pos, head, channel) * kElemBytes);
+        const uint32_t i = table_index(p, pos, g * kPairsPerVec);
+        const float4 cs01 = tab4<kSmem>(tab, i);
+        const float4 cs23 = kType != ROPE3D_F32 ? tab4<kSmem>(tab, i + 2) : cs01;
+        st_stream_v4(qo + strided_offset(st, 2, pos, head, channel) * kElemBytes,
+                     rotate_vec<kType>(qv, cs01, cs23));
+        st_stream_v4(ko + strided_offset(st, 3, pos, head, channel) * kElemBytes,
+                     rotate_vec<kType>(kv, cs01, cs23));
+    }
+}
+
+// ---- per-pair kernels (any valid alignment and split) -----------------------
+
+template <int kType>
+__device__ __forceinline__ void rotate_pair_at(const char *q, const char *k, char *qo, char *ko,
+                                               float2 cs, bool coherent) {
+    if constexpr (kType != ROPE3D_F32) {
+        // a 16-bit pair is one 4-byte aligned word
+        const uint32_t qw = coherent ? *reinterpret_cast<const volatile uint32_t *>(q)
+                                     : ld_nc_u32(q);
+        const uint32_t kw = coherent ? *reinterpret_cast<const volatile uint32_t *>(k)
+                                     : ld_nc_u32(k);
+        *reinterpret_cast<uint32_t *>(qo) = rotate_word16<kType>(qw, cs.x, cs.y);
+        *reinterpret_cast<uint32_t *>(ko) = rotate_word16<kType>(kw, cs.x, cs.y);
+    } else {
+        // an fp32 pair may be only 4-byte aligned: two scalar accesses
+        const float *qf = reinterpret_cast<const float *>(q);
+        const float *kf = reinterpret_cast<const float *>(k);
+        float qe, qd, ke, kd;
+        if (coherent) {
+            qe = *reinterpret_cast<const volatile float *>(qf);
+            qd = *reinterpret_cast<const volatile float *>(qf + 1);
+            ke = *reinterpret_cast<const volatile float *>(kf);
+            kd = *reinterpret_cast<const volatile float *>(kf + 1);
+        } else {
+            qe = __ldg(qf);
+            qd = __ldg(qf + 1);
+            ke = __ldg(kf);
+            kd = __ldg(kf + 1);
+        }
+        const Rot a = rotate(qe, qd, cs.x, cs.y);
+        const Rot b = rotate(ke, kd, cs.x, cs.y);
+        float *qof = reinterpret_cast<float *>(qo);
+        float *kof = reinterpret_cast<float *>(ko);
+        qof[0] = a.y0;
+        qof[1] = a.y1;
+        kof[0] = b.y0;
+        kof[1] = b.y1;
+    }
+}
+
+template <int kType, bool kSmem>
+__global__ void __launch_bounds__(kBlock)
+rope3d_pair_kernel(const KParams p, const KStrides) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const float2 *tab = stage_tables<kSmem>(p, reinterpret_cast<float2 *>(smem_raw));
+    constexpr size_t kPairBytes = kType == ROPE3D_F32 ? 8 : 4;
+    const char *q = static_cast<const char *>(p.q);
+    const char *k = static_cast<const char *>(p.k);
+    char *qo = static_cast<char *>(p.q_out);
+    char *ko = static_cast<char *>(p.k_out);
     const uint32_t stride = gridDim.x * blockDim.x;
     for (uint32_t v = blockIdx.x * blockDim.x + threadIdx.x; v < p.units; v += stride) {
         const uint32_t row = fdiv(v, p.per_row);
         const uint32_t r = v - row * p.per_row.d;
         const uint32_t pair = r - fdiv(r, p.per_head) * p.per_head.d;
-        const float2 cs = kSmem ? tab[table_index(p, row, pair)]
-                                : __ldg(tab + table_index(p, row, pair));
-        if constexpr (kBf16) {
-            // a bf16 pair is one 4-byte aligned word
-            const uint32_t *q = static_cast<const uint32_t *>(p.q);
-            const uint32_t *k = static_cast<const uint32_t *>(p.k);
-            uint32_t *qo = static_cast<uint32_t *>(p.q_out);
-            uint32_t *ko = static_cast<uint32_t *>(p.k_out);
-            qo[v] = rotate_bf16_word(ld_nc_u32(q + v), cs.x, cs.y);
-            ko[v] = rotate_bf16_word(ld_nc_u32(k + v), cs.x, cs.y);
-        } else {
-            // an fp32 pair may be only 4-byte aligned: two scalar accesses
-            const float *q = static_cast<const float *>(p.q);
-            const float *k = static_cast<const float *>(p.k);
-            float *qo = static_cast<float *>(p.q_out);
-            float *ko = static_cast<float *>(p.k_out);
-            const Rot a = rotate(__ldg(q + 2 * size_t(v)), __ldg(q + 2 * size_t(v) + 1), cs.x, cs.y);
-            const Rot b = rotate(__ldg(k + 2 * size_t(v)), __ldg(k + 2 * size_t(v) + 1), cs.x, cs.y);
-            qo[2 * size_t(v)] = a.y0;
-            qo[2 * size_t(v) + 1] = a.y1;
-            ko[2 * size_t(v)] = b.y0;
-            ko[2 * size_t(v) + 1] = b.y1;
-        }
+        const float2 cs = tab1<kSmem>(tab, table_index(p, grid_pos(p, row), pair));
+        const size_t off = size_t(v) * kPairBytes;
+        rotate_pair_at<kType>(q + off, k + off, qo + off, ko + off, cs, false);
+    }
+}
+
+template <int kType, bool kSmem>
+__global__ void __launch_bounds__(kBlock)
+rope3d_pair_strided_kernel(const KParams p, const KStrides st) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const float2 *tab = stage_tables<kSmem>(p, reinterpret_cast<float2 *>(smem_raw));
+    constexpr int kElemBytes = kType == ROPE3D_F32 ? 4 : 2;
+    const char *q = static_cast<const char *>(p.q);
+    const char *k = static_cast<const char *>(p.k);
+    char *qo = static_cast<char *>(p.q_out);
+    char *ko = static_cast<char *>(p.k_out);
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t v = blockIdx.x * blockDim.x + threadIdx.x; v < p.units; v += stride) {
+        const uint32_t row = fdiv(v, p.per_row);
+        const uint32_t r = v - row * p.per_row.d;
+        const uint32_t head = fdiv(r, p.per_head);
+        const uint32_t pair = r - head * p.per_head.d;
+        const GridPos pos = grid_pos(p, row);
+        const float2 cs = tab1<kSmem>(tab, table_index(p, pos, pair));
+        const uint32_t channel = 2 * pair;
+        rotate_pair_at<kType>(q + strided_offset(st, 0, pos, head, channel) * kElemBytes,
+                              k + strided_offset(st, 1, pos, head, channel) * kElemBytes,
+                              qo + strided_offset(st, 2, pos, head, channel) * kElemBytes,
+                              ko + strided_offset(st, 3, pos, head, channel) * kElemBytes, cs,
+                              true);
+    }
+}
+
+// ---- gather of a strided view into a contiguous buffer ----------------------
+
+template <int kElemBytes>
+__global__ void __launch_bounds__(kBlock)
+rope3d_gather_kernel(const char *src, char *dst, const KParams p, const KStrides st) {
+    // units = elements of this launch; per_row = heads * head_dim, per_head = head_dim
+    using Word = typename std::conditional<kElemBytes == 2, uint16_t, uint32_t>::type;
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < p.units; e += stride) {
+        const uint32_t row = fdiv(e, p.per_row);
+        const uint32_t r = e - row * p.per_row.d;
+        const uint32_t head = fdiv(r, p.per_head);
+        const uint32_t c = r - head * p.per_head.d;
+        const GridPos pos = grid_pos(p, row);
+        const Word w = *reinterpret_cast<const Word *>(src + strided_offset(st, 0, pos, head, c) *
+                                                                  kElemBytes);
+        *reinterpret_cast<Word *>(dst + size_t(e) * kElemBytes) = w;
     }
 }
 
 // ---- launch ----------------------------------------------------------------
 
-using KernelFn = void (*)(KParams);
+using KernelFn = void (*)(KParams, KStrides);
 
-KernelFn pick(bool vec16, bool bf16, bool smem) {
-    if (vec16) {
-        if (bf16) return smem ? rope3d_vec16_kernel<true, true> : rope3d_vec16_kernel<true, false>;
-        return smem ? rope3d_vec16_kernel<false, true> : rope3d_vec16_kernel<false, false>;
-    }
-    if (bf16) return smem ? rope3d_pair_kernel<true, true> : rope3d_pair_kernel<true, false>;
-    return smem ? rope3d_pair_kernel<false, true> : rope3d_pair_kernel<false, false>;
+template <int kType>
+KernelFn pick_type(bool vec16, bool strided, bool smem) {
+    if (vec16 && !strided)
+        return smem ? rope3d_vec16_kernel<kType, true> : rope3d_vec16_kernel<kType, false>;
+    if (vec16)
+        return smem ? rope3d_vec16_strided_kernel<kType, true>
+                    : rope3d_vec16_strided_kernel<kType, false>;
+    if (!strided)
+        return smem ? rope3d_pair_kernel<kType, true> : rope3d_pair_kernel<kType, false>;
+    return smem ? rope3d_pair_strided_kernel<kType, true> : rope3d_pair_strided_kernel<kType, false>;
+}
+
+KernelFn pick(int dtype, bool vec16, bool strided, bool smem) {
+    if (dtype == ROPE3D_BF16) return pick_type<ROPE3D_BF16>(vec16, strided, smem);
+    if (dtype == ROPE3D_F16) return pick_type<ROPE3D_F16>(vec16, strided, smem);
+    return pick_type<ROPE3D_F32>(vec16, strided, smem);
 }
 
 constexpr int kMaxDevices = 64;
-constexpr int kNumVariants = 8;
+constexpr int kNumVariants = 32;
 
 struct DeviceCache {
     bool init = false;
@@ -292,17 +481,18 @@ struct DeviceCache {
 std::mutex g_dev_mutex;
 DeviceCache g_dev[kMaxDevices];
 
-int variant_id(bool vec16, bool bf16, bool smem) {
-    return (vec16 ? 4 : 0) | (bf16 ? 2 : 0) | (smem ? 1 : 0);
+int variant_id(int dtype, bool vec16, bool strided, bool smem) {
+    return (dtype << 3) | (vec16 ? 4 : 0) | (strided ? 2 : 0) | (smem ? 1 : 0);
 }
 
 // Grid size: enough CTAs to fill every SM at full residency, no more than
 // the work needs.
-cudaError_t grid_for(KernelFn fn, int vid, size_t smem, uint64_t units, int *grid) {
+cudaError_t grid_for(const void *fn, int vid, size_t smem, uint64_t units, int *grid) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= kMaxDevices || vid < 0 || vid >= kNumVariants)
+        return cudaErrorInvalidValue;
     std::lock_guard<std::mutex> lock(g_dev_mutex);
     DeviceCache &dc = g_dev[dev];
     if (!dc.init) {
@@ -311,8 +501,7 @@ cudaError_t grid_for(KernelFn fn, int vid, size_t smem, uint64_t units, int *gri
         dc.init = true;
     }
     if (!dc.attr_set[vid]) {
-        e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kMaxSmemTableBytes));
         if (e != cudaSuccess) return e;
         dc.attr_set[vid] = true;
@@ -332,6 +521,15 @@ cudaError_t grid_for(KernelFn fn, int vid, size_t smem, uint64_t units, int *gri
 
 std::atomic<uint32_t> g_max_units{kMaxUnitsPerLaunch};
 
+void fill_geometry(KParams &p, uint32_t units_per_row, uint32_t units_per_head, uint32_t T,
+                   uint32_t H, uint32_t W) {
+    p.per_row = make_fastdiv(units_per_row);
+    p.per_head = make_fastdiv(units_per_head);
+    p.N = make_fastdiv(T * H * W);
+    p.HW = make_fastdiv(H * W);
+    p.Wd = make_fastdiv(W);
+}
+
 }  // namespace
 
 void set_max_units_per_launch(uint32_t n) {
@@ -339,8 +537,7 @@ void set_max_units_per_launch(uint32_t n) {
 }
 
 cudaError_t launch_rope3d(const LaunchArgs &a, cudaStream_t stream, LaunchInfo *info) {
-    const bool bf16 = a.dtype == ROPE3D_BF16;
-    const uint32_t esize = bf16 ? 2 : 4;
+    const uint32_t esize = a.dtype == ROPE3D_F32 ? 4 : 2;
     const uint32_t elems_per_unit = a.vec16 ? 16 / esize : 2;
     const uint64_t row_elems = uint64_t(a.heads) * a.head_dim;
     const uint32_t units_per_row = static_cast<uint32_t>(row_elems / elems_per_unit);
@@ -349,8 +546,8 @@ cudaError_t launch_rope3d(const LaunchArgs &a, cudaStream_t stream, LaunchInfo *
     const size_t table_bytes = size_t(a.table_len) * sizeof(float2);
     const bool smem = table_bytes <= kMaxSmemTableBytes;
     const size_t smem_bytes = smem ? table_bytes : 0;
-    const KernelFn fn = pick(a.vec16, bf16, smem);
-    const int vid = variant_id(a.vec16, bf16, smem);
+    const KernelFn fn = pick(a.dtype, a.vec16, a.strided, smem);
+    const int vid = variant_id(a.dtype, a.vec16, a.strided, smem);
 
     KParams p{};
     p.tab = a.tables;
@@ -360,27 +557,36 @@ cudaError_t launch_rope3d(const LaunchArgs &a, cudaStream_t stream, LaunchInfo *
     p.pT = a.pT;
     p.pH = a.pH;
     p.pW = a.pW;
-    p.per_row = make_fastdiv(units_per_row);
-    p.per_head = make_fastdiv(units_per_head);
-    p.N = make_fastdiv(N);
-    p.HW = make_fastdiv(a.H * a.W);
-    p.Wd = make_fastdiv(a.W);
+    fill_geometry(p, units_per_row, units_per_head, a.T, a.H, a.W);
+    KStrides st{};
+    if (a.strided)
+        for (int i = 0; i < 4; ++i)
+            for (int j = 0; j < 5; ++j) st.s[i][j] = a.strides[i][j];
 
     const uint64_t cap = g_max_units.load(std::memory_order_relaxed);
     const uint64_t rows_per_launch = cap / units_per_row > 0 ? cap / units_per_row : 1;
     for (uint64_t r = 0; r < a.rows; r += rows_per_launch) {
         const uint64_t nrows = (a.rows - r) < rows_per_launch ? (a.rows - r) : rows_per_launch;
-        const uint64_t elem_off = r * row_elems;
-        p.q = static_cast<const char *>(a.q) + elem_off * esize;
-        p.k = static_cast<const char *>(a.k) + elem_off * esize;
-        p.q_out = static_cast<char *>(a.q_out) + elem_off * esize;
-        p.k_out = static_cast<char *>(a.k_out) + elem_off * esize;
+        if (a.strided) {
+            // strided views address rows by (batch, t, h, w): pointers stay put
+            p.q = a.q;
+            p.k = a.k;
+            p.q_out = a.q_out;
+            p.k_out = a.k_out;
+            st.b0 = static_cast<uint32_t>((a.row0 + r) / N);
+        } else {
+            const uint64_t elem_off = r * row_elems;
+            p.q = static_cast<const char *>(a.q) + elem_off * esize;
+            p.k = static_cast<const char *>(a.k) + elem_off * esize;
+            p.q_out = static_cast<char *>(a.q_out) + elem_off * esize;
+            p.k_out = static_cast<char *>(a.k_out) + elem_off * esize;
+        }
         p.units = static_cast<uint32_t>(nrows * units_per_row);
         p.row0_mod_N = static_cast<uint32_t>((a.row0 + r) % N);
         int grid = 0;
-        cudaError_t e = grid_for(fn, vid, smem_bytes, p.units, &grid);
+        cudaError_t e = grid_for(reinterpret_cast<const void *>(fn), vid, smem_bytes, p.units, &grid);
         if (e != cudaSuccess) return e;
-        fn<<<grid, kBlock, smem_bytes, stream>>>(p);
+        fn<<<grid, kBlock, smem_bytes, stream>>>(p, st);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         if (info) {
@@ -388,6 +594,41 @@ cudaError_t launch_rope3d(const LaunchArgs &a, cudaStream_t stream, LaunchInfo *
             info->grid = grid;
             info->block = kBlock;
         }
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_gather(const void *src, const int64_t strides[5], void *dst, int elem_bytes,
+                          uint64_t B, uint32_t T, uint32_t H, uint32_t W, uint32_t heads,
+                          uint32_t head_dim, cudaStream_t stream) {
+    const uint64_t row_elems = uint64_t(heads) * head_dim;
+    const uint64_t rows = B * T * H * W;
+    const uint32_t N = T * H * W;
+    KParams p{};
+    fill_geometry(p, static_cast<uint32_t>(row_elems), head_dim, T, H, W);
+    KStrides st{};
+    for (int j = 0; j < 5; ++j) st.s[0][j] = strides[j];
+    const uint64_t rows_per_launch = std::max<uint64_t>(1, kMaxUnitsPerLaunch / row_elems);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    for (uint64_t r = 0; r < rows; r += rows_per_launch) {
+        const uint64_t nrows = std::min<uint64_t>(rows - r, rows_per_launch);
+        p.units = static_cast<uint32_t>(nrows * row_elems);
+        p.row0_mod_N = static_cast<uint32_t>(r % N);
+        st.b0 = static_cast<uint32_t>(r / N);
+        const uint64_t need = (uint64_t(p.units) + kBlock - 1) / kBlock;
+        const int grid = static_cast<int>(std::min<uint64_t>(need, uint64_t(sms) * 4));
+        char *d = static_cast<char *>(dst) + r * row_elems * elem_bytes;
+        if (elem_bytes == 2)
+            rope3d_gather_kernel<2><<<grid, kBlock, 0, stream>>>(static_cast<const char *>(src), d, p, st);
+        else
+            rope3d_gather_kernel<4><<<grid, kBlock, 0, stream>>>(static_cast<const char *>(src), d, p, st);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }

@@ -38,7 +38,7 @@ class Workload:
     base: float = 10000.0
     sigma: float = 1.0
     seed: int = 0
-    dtype: str = "bf16"          # "bf16" or "f32"
+    dtype: str = "bf16"          # "bf16", "f16" or "f32"
     repeat: int = 1              # calls per step sharing one table set
     note: str = field(default="", compare=False)
 
@@ -56,7 +56,7 @@ class Workload:
 
     @property
     def elem_bytes(self) -> int:
-        return 2 if self.dtype == "bf16" else 4
+        return 4 if self.dtype == "f32" else 2
 
     @property
     def table_bytes(self) -> int:
@@ -99,17 +99,22 @@ def _chunk(seed: int, which: int, i: int, n: int, sigma: float, dtype: str) -> n
     v = g.standard_normal(n, dtype=np.float32)
     if sigma != 1.0:
         v *= np.float32(sigma)
-    return f32_to_bf16_bits(v) if dtype == "bf16" else v
+    if dtype == "bf16":
+        return f32_to_bf16_bits(v)
+    if dtype == "f16":
+        return v.astype(np.float16).view(np.uint16)   # nearest binary16, ties to even
+    return v
 
 
 def normal(numel: int, sigma: float, seed: int, which: int, dtype: str = "bf16",
            out: np.ndarray | None = None, threads: int | None = None) -> np.ndarray:
-    """numel values (uint16 bf16 bits or float32) of tensor ``which`` of ``seed``.
+    """numel values (uint16 bf16 / binary16 bits, or float32) of tensor
+    ``which`` of ``seed``.
 
     ``out`` may be a preallocated 1-D array (for instance a view of pinned host
     memory) of the right dtype; it is filled in place.
     """
-    np_dtype = np.uint16 if dtype == "bf16" else np.float32
+    np_dtype = np.float32 if dtype == "f32" else np.uint16
     if out is None:
         out = np.empty(numel, dtype=np_dtype)
     if out.dtype != np_dtype or out.size != numel:

@@ -205,3 +205,104 @@ def test_build_tables_rejects(lib, host_tables):
     with pytest.raises(r.Rope3dError) as e:
         r.rope3d_build_tables(2, 4, 4, (16, 16, 16), -1.0)
     assert e.value.name == "ERR_ARG"
+
+
+# ---------------------------------------------------------------------------
+# strided views: the overlap analysis of rope3d_apply_pair_strided
+# ---------------------------------------------------------------------------
+
+def _contig_strides(B, T, H, W, heads, hd):
+    return (T * H * W * heads * hd, H * W * heads * hd, W * heads * hd, heads * hd, hd)
+
+
+def _status(ptrs, strides, tables, dims, split=(16, 16, 16), dtype=0):
+    B, T, H, W, heads, hd = dims
+    return r.STATUS[r.rope3d_preflight_strided(ptrs, strides, tables, B, T, H, W, heads, hd,
+                                               split, dtype, check_device=False)]
+
+
+def test_strided_fused_qkv_layouts(lib, host_tables):
+    dims = (2, 2, 4, 4, 3, 48)
+    B, T, H, W, heads, hd = dims
+    N = T * H * W
+    tabs = r.rope3d_build_tables(T, H, W, (16, 16, 16))
+    base = 1 << 32
+    far = 1 << 40
+    out = _contig_strides(*dims)
+    # [B, N, 3, heads, hd]: Q, K, V thirds
+    s3 = (N * 3 * heads * hd, H * W * 3 * heads * hd, W * 3 * heads * hd, 3 * heads * hd, hd)
+    q, k, v = base, base + 2 * heads * hd, base + 4 * heads * hd
+    assert _status((q, k, far, far + (1 << 30)), (s3, s3, out, out), tabs, dims) == "OK"
+    assert _status((q, k, q, k), (s3, s3, s3, s3), tabs, dims) == "OK"            # in place
+    assert _status((q, k, v, far), (s3, s3, s3, out), tabs, dims) == "OK"         # Q_out into V
+    assert _status((q, k, k, far), (s3, s3, s3, out), tabs, dims) == "ERR_ALIAS"  # Q_out onto K
+    assert _status((q, k, v, v), (s3, s3, s3, s3), tabs, dims) == "ERR_ALIAS"     # outputs collide
+    assert _status((q, k, q + 4, k), (s3, s3, s3, s3), tabs, dims) == "ERR_ALIAS"  # off by two elements
+    # [B, N, heads, 3, hd]: interleaved per head
+    si = (N * heads * 3 * hd, H * W * heads * 3 * hd, W * heads * 3 * hd, heads * 3 * hd, 3 * hd)
+    q, k = base, base + 2 * hd
+    assert _status((q, k, q, k), (si, si, si, si), tabs, dims) == "OK"
+    assert _status((q, k, k, q), (si, si, si, si), tabs, dims) == "ERR_ALIAS"     # swapped
+    tabs.close()
+
+
+def test_strided_rejections(lib, host_tables):
+    dims = (1, 2, 4, 4, 2, 48)
+    tabs = r.rope3d_build_tables(2, 4, 4, (16, 16, 16))
+    c = _contig_strides(*dims)
+    p = (1 << 32, 1 << 34, 1 << 36, 1 << 38)
+    assert _status(p, (c, c, c, c), tabs, dims) == "OK"
+    bcast = (c[0], c[1], c[2], c[3], 0)  # two heads written to one place
+    assert _status(p, (c, c, bcast, c), tabs, dims) == "ERR_ALIAS"
+    assert _status(p, (c, c, c, (c[0], c[1], -c[2], c[3], c[4])), tabs, dims) == "ERR_SHAPE"
+    odd = (c[0], c[1], c[2], c[3], 49)
+    assert _status(p, (odd, c, c, c), tabs, dims) == "ERR_ALIGN"
+    assert _status(p, (odd, c, c, c), tabs, dims, dtype=1) == "OK"  # fp32 pairs need no even stride
+    assert _status(p, (None, c, c, c), tabs, dims) == "ERR_NULL"
+    assert _status((p[0] + 2, p[1], p[2], p[3]), (c, c, c, c), tabs, dims) == "ERR_ALIGN"
+    # a crop of a larger grid, and another crop of the same buffer
+    big = (1 * 4 * 8 * 8 * 2 * 48, 8 * 8 * 2 * 48, 8 * 2 * 48, 2 * 48, 48)
+    b0 = 1 << 32
+    crop_a = b0
+    crop_b = b0 + 2 * (4 * 2 * 48)             # 4 columns to the right: disjoint
+    crop_c = b0 + 2 * (2 * 2 * 48)             # 2 columns to the right: overlaps crop_a
+    assert _status((crop_a, p[1], crop_b, p[3]), (big, c, big, c), tabs, dims) == "OK"
+    assert _status((crop_a, p[1], crop_c, p[3]), (big, c, big, c), tabs, dims) == "ERR_ALIAS"
+    tabs.close()
+
+
+def _elements(base, shape, strides):
+    idx = np.indices(shape).reshape(len(shape), -1)
+    return set((base + (idx * np.array(strides)[:, None]).sum(axis=0)).tolist())
+
+
+def test_strided_overlap_matches_brute_force(lib, host_tables):
+    """For outputs with identical strides, ERR_ALIAS exactly when the two
+    views share an element (enumerated)."""
+    g = np.random.Generator(np.random.PCG64(21))
+    tabs = {}
+    checked = alias = 0
+    while checked < 300:
+        B, T, H, W, heads = (int(v) for v in g.integers(1, 4, 5))
+        hd = int(g.choice([6, 12]))
+        split = (2, 2, hd - 4)
+        key = (T, H, W, split)
+        if key not in tabs:
+            tabs[key] = r.rope3d_build_tables(T, H, W, split)
+        shape = (B, T, H, W, heads, hd)
+        strides = tuple(int(v) * 2 for v in g.integers(0, 40, 5)) + (1,)
+        # only non-self-overlapping output views (else the call is refused anyway)
+        if len(_elements(0, shape, strides)) != int(np.prod(shape)):
+            continue
+        off = int(g.integers(-300, 300)) * 2
+        ob = 1 << 32
+        st5 = strides[:5]
+        got = _status((1 << 44, 1 << 45, ob, ob + 2 * off), ((0,) * 4 + (hd,), (0,) * 4 + (hd,), st5, st5),
+                      tabs[key], shape, split)
+        want = "ERR_ALIAS" if _elements(0, shape, strides) & _elements(off, shape, strides) else "OK"
+        assert got == want, (shape, strides, off)
+        checked += 1
+        alias += want == "ERR_ALIAS"
+    assert 30 < alias < 270  # both outcomes exercised
+    for t in tabs.values():
+        t.close()
