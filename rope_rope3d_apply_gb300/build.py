@@ -71,13 +71,14 @@ def up_to_date(lib: str = LIB) -> bool:
     return all(os.path.getmtime(s) <= t for s in SOURCES)
 
 
-def build(force: bool = False, verbose: bool = False, out_dir: str = BUILD) -> str:
-    """Compile and link; returns the library path. Both compiles run in parallel."""
+def build(force: bool = False, verbose: bool = False, out_dir: str = BUILD,
+          extra_nvcc: list[str] | None = None) -> str:
+    """Compile and link; returns the library path. The compiles run in parallel."""
     lib = os.path.join(out_dir, "librope3d.so")
     if not force and out_dir == BUILD and up_to_date(lib):
         return lib
     os.makedirs(out_dir, exist_ok=True)
-    compiles, link = commands(out_dir)
+    compiles, link = commands(out_dir, extra_nvcc)
     procs = [subprocess.Popen(c, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
              for c in compiles]
     logs = []

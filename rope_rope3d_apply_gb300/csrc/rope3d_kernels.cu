@@ -47,6 +47,21 @@ namespace {
 constexpr int kBlock = 512;
 constexpr int kUnroll = 2;
 
+// Strided vector kernel: vectors per tensor in flight per thread, and the
+// resident CTAs per SM its register budget is sized for.
+#ifndef ROPE3D_STRIDED_UNROLL
+#define ROPE3D_STRIDED_UNROLL 2
+#endif
+#ifndef ROPE3D_STRIDED_MIN_CTAS
+#define ROPE3D_STRIDED_MIN_CTAS 0
+#endif
+constexpr int kStridedUnroll = ROPE3D_STRIDED_UNROLL;
+#if ROPE3D_STRIDED_MIN_CTAS > 0
+#define ROPE3D_STRIDED_BOUNDS __launch_bounds__(kBlock, ROPE3D_STRIDED_MIN_CTAS)
+#else
+#define ROPE3D_STRIDED_BOUNDS __launch_bounds__(kBlock)
+#endif
+
 struct KParams {
     const void *q;
     const void *k;
@@ -123,9 +138,11 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *ptr) {
 }
 
 // Coherent streaming load (strided calls, which may rotate in place).
+// The asm is volatile so that it is never moved past the stores of the
+// previous iteration, which may write the same buffer (in place).
 __device__ __forceinline__ uint4 ld_coherent_v4(const void *ptr) {
     uint4 r;
-    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                  : "l"(ptr)
                  : "memory");
@@ -303,8 +320,8 @@ rope3d_vec16_kernel(const KParams p, const KStrides) {
 // Requires, besides the contiguous kernel's conditions, every stride a multiple
 // of the vector's element count.
 
-template <int kType, bool kSmem>
-__global__ void __launch_bounds__(kBlock)
+template <int kType, bool kSmem, bool kSame>
+__global__ void ROPE3D_STRIDED_BOUNDS
 rope3d_vec16_strided_kernel(const KParams p, const KStrides st) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const float2 *tab = stage_tables<kSmem>(p, reinterpret_cast<float2 *>(smem_raw));
@@ -317,22 +334,65 @@ rope3d_vec16_strided_kernel(const KParams p, const KStrides st) {
     char *qo = static_cast<char *>(p.q_out);
     char *ko = static_cast<char *>(p.k_out);
 
+    // kSame: the four views share one set of strides (e.g. Q and K of a fused
+    // QKV buffer rotated in place), so one offset serves all four pointers
+    auto off = [&](int i, const GridPos &pos, uint32_t head, uint32_t c) {
+        return strided_offset(st, kSame ? 0 : i, pos, head, c) * kElemBytes;
+    };
+
+    // position of vector vv: grid coordinates, head, and its first channel
+    struct Where {
+        GridPos pos;
+        uint32_t head, g;
+    };
+    auto where = [&](uint32_t vv) {
+        Where x;
+        const uint32_t row = fdiv(vv, p.per_row);
+        const uint32_t r = vv - row * p.per_row.d;
+        x.head = fdiv(r, p.per_head);
+        x.g = r - x.head * p.per_head.d;
+        x.pos = grid_pos(p, row);
+        return x;
+    };
+
     const uint32_t stride = gridDim.x * blockDim.x;
-    for (uint32_t v = blockIdx.x * blockDim.x + threadIdx.x; v < p.units; v += stride) {
-        const uint32_t row = fdiv(v, p.per_row);
-        const uint32_t r = v - row * p.per_row.d;
-        const uint32_t head = fdiv(r, p.per_head);
-        const uint32_t g = r - head * p.per_head.d;
-        const GridPos pos = grid_pos(p, row);
-        const uint32_t channel = g * kElemsPerVec;
-        const uint4 qv = ld_coherent_v4(q + strided_offset(st, 0, pos, head, channel) * kElemBytes);
-        const uint4 kv = ld_coherent_v4(k + strided_offset(st, 1, pos, head, channel) * kElemBytes);
-        const uint32_t i = table_index(p, pos, g * kPairsPerVec);
+    uint32_t v = blockIdx.x * blockDim.x + threadIdx.x;
+    // main loop: kStridedUnroll vectors of Q and of K in flight per thread; all loads
+    // of an iteration come before its stores, and no two threads touch one
+    // element, so rotating in place is safe
+    for (; v + (kStridedUnroll - 1) * stride < p.units; v += kStridedUnroll * stride) {
+        Where x[kStridedUnroll];
+        uint4 qv[kStridedUnroll], kv[kStridedUnroll];
+#pragma unroll
+        for (int u = 0; u < kStridedUnroll; ++u) {
+            x[u] = where(v + u * stride);
+            const uint32_t c = x[u].g * kElemsPerVec;
+            qv[u] = ld_coherent_v4(q + off(0, x[u].pos, x[u].head, c));
+            kv[u] = ld_coherent_v4(k + off(1, x[u].pos, x[u].head, c));
+        }
+#pragma unroll
+        for (int u = 0; u < kStridedUnroll; ++u) {
+            const uint32_t c = x[u].g * kElemsPerVec;
+            const uint32_t i = table_index(p, x[u].pos, x[u].g * kPairsPerVec);
+            const float4 cs01 = tab4<kSmem>(tab, i);
+            const float4 cs23 = kType != ROPE3D_F32 ? tab4<kSmem>(tab, i + 2) : cs01;
+            st_stream_v4(qo + off(2, x[u].pos, x[u].head, c),
+                         rotate_vec<kType>(qv[u], cs01, cs23));
+            st_stream_v4(ko + off(3, x[u].pos, x[u].head, c),
+                         rotate_vec<kType>(kv[u], cs01, cs23));
+        }
+    }
+    for (; v < p.units; v += stride) {
+        const Where x = where(v);
+        const uint32_t c = x.g * kElemsPerVec;
+        const uint4 qv = ld_coherent_v4(q + off(0, x.pos, x.head, c));
+        const uint4 kv = ld_coherent_v4(k + off(1, x.pos, x.head, c));
+        const uint32_t i = table_index(p, x.pos, x.g * kPairsPerVec);
         const float4 cs01 = tab4<kSmem>(tab, i);
         const float4 cs23 = kType != ROPE3D_F32 ? tab4<kSmem>(tab, i + 2) : cs01;
-        st_stream_v4(qo + strided_offset(st, 2, pos, head, channel) * kElemBytes,
+        st_stream_v4(qo + off(2, x.pos, x.head, c),
                      rotate_vec<kType>(qv, cs01, cs23));
-        st_stream_v4(ko + strided_offset(st, 3, pos, head, channel) * kElemBytes,
+        st_stream_v4(ko + off(3, x.pos, x.head, c),
                      rotate_vec<kType>(kv, cs01, cs23));
     }
 }
@@ -450,25 +510,28 @@ rope3d_gather_kernel(const char *src, char *dst, const KParams p, const KStrides
 using KernelFn = void (*)(KParams, KStrides);
 
 template <int kType>
-KernelFn pick_type(bool vec16, bool strided, bool smem) {
+KernelFn pick_type(bool vec16, bool strided, bool same, bool smem) {
     if (vec16 && !strided)
         return smem ? rope3d_vec16_kernel<kType, true> : rope3d_vec16_kernel<kType, false>;
+    if (vec16 && same)
+        return smem ? rope3d_vec16_strided_kernel<kType, true, true>
+                    : rope3d_vec16_strided_kernel<kType, false, true>;
     if (vec16)
-        return smem ? rope3d_vec16_strided_kernel<kType, true>
-                    : rope3d_vec16_strided_kernel<kType, false>;
+        return smem ? rope3d_vec16_strided_kernel<kType, true, false>
+                    : rope3d_vec16_strided_kernel<kType, false, false>;
     if (!strided)
         return smem ? rope3d_pair_kernel<kType, true> : rope3d_pair_kernel<kType, false>;
     return smem ? rope3d_pair_strided_kernel<kType, true> : rope3d_pair_strided_kernel<kType, false>;
 }
 
-KernelFn pick(int dtype, bool vec16, bool strided, bool smem) {
-    if (dtype == ROPE3D_BF16) return pick_type<ROPE3D_BF16>(vec16, strided, smem);
-    if (dtype == ROPE3D_F16) return pick_type<ROPE3D_F16>(vec16, strided, smem);
-    return pick_type<ROPE3D_F32>(vec16, strided, smem);
+KernelFn pick(int dtype, bool vec16, bool strided, bool same, bool smem) {
+    if (dtype == ROPE3D_BF16) return pick_type<ROPE3D_BF16>(vec16, strided, same, smem);
+    if (dtype == ROPE3D_F16) return pick_type<ROPE3D_F16>(vec16, strided, same, smem);
+    return pick_type<ROPE3D_F32>(vec16, strided, same, smem);
 }
 
 constexpr int kMaxDevices = 64;
-constexpr int kNumVariants = 32;
+constexpr int kNumVariants = 48;
 
 struct DeviceCache {
     bool init = false;
@@ -481,8 +544,8 @@ struct DeviceCache {
 std::mutex g_dev_mutex;
 DeviceCache g_dev[kMaxDevices];
 
-int variant_id(int dtype, bool vec16, bool strided, bool smem) {
-    return (dtype << 3) | (vec16 ? 4 : 0) | (strided ? 2 : 0) | (smem ? 1 : 0);
+int variant_id(int dtype, bool vec16, bool strided, bool same, bool smem) {
+    return (dtype << 4) | (vec16 ? 8 : 0) | (strided ? 4 : 0) | (same ? 2 : 0) | (smem ? 1 : 0);
 }
 
 // Grid size: enough CTAs to fill every SM at full residency, no more than
@@ -546,8 +609,11 @@ cudaError_t launch_rope3d(const LaunchArgs &a, cudaStream_t stream, LaunchInfo *
     const size_t table_bytes = size_t(a.table_len) * sizeof(float2);
     const bool smem = table_bytes <= kMaxSmemTableBytes;
     const size_t smem_bytes = smem ? table_bytes : 0;
-    const KernelFn fn = pick(a.dtype, a.vec16, a.strided, smem);
-    const int vid = variant_id(a.dtype, a.vec16, a.strided, smem);
+    bool same = a.strided;
+    for (int i = 1; i < 4 && same; ++i)
+        for (int j = 0; j < 5; ++j) same = same && a.strides[i][j] == a.strides[0][j];
+    const KernelFn fn = pick(a.dtype, a.vec16, a.strided, same, smem);
+    const int vid = variant_id(a.dtype, a.vec16, a.strided, same, smem);
 
     KParams p{};
     p.tab = a.tables;
