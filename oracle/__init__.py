@@ -213,3 +213,34 @@ def rope3d_at(x: np.ndarray, indices: np.ndarray, shape, split, tabs, lib=None) 
     if rc != 0:
         raise ValueError("oracle rejected the sample request")
     return out
+
+
+# ---------------------------------------------------------------------------
+# patchify / unpatchify (sglang PR #34471 review, "关键源码片段", _patchify in
+# ltx_2_5_diffusion_decoder.py): space-to-depth over H and W,
+# (B, C, F, H, W) -> (B, C*p*p, F, H/p, W/p), channels packed in the order
+# (channel, width offset, height offset). Written out as the page's three
+# steps: split H and W into (blocks, offset), move the offsets next to the
+# channel in the order (width offset, height offset), merge. Exact (a
+# permutation), so numpy reshape/transpose is the whole definition.
+# _unpatchify is named on the page without code; our reading is the exact
+# inverse of _patchify.
+# ---------------------------------------------------------------------------
+
+def patchify(x: np.ndarray, p: int) -> np.ndarray:
+    B, C, F, H, W = x.shape
+    if H % p or W % p:
+        raise ValueError("H and W must be multiples of the patch size")
+    t = x.reshape(B, C, F, H // p, p, W // p, p)            # (b, c, f, i, ph, j, pw)
+    t = t.transpose(0, 1, 6, 4, 2, 3, 5)                    # (b, c, pw, ph, f, i, j)
+    return np.ascontiguousarray(t).reshape(B, C * p * p, F, H // p, W // p)
+
+
+def unpatchify(y: np.ndarray, p: int) -> np.ndarray:
+    B, Cpp, F, Hp, Wp = y.shape
+    if Cpp % (p * p):
+        raise ValueError("channels must be a multiple of p*p")
+    C = Cpp // (p * p)
+    t = y.reshape(B, C, p, p, F, Hp, Wp)                    # (b, c, pw, ph, f, i, j)
+    t = t.transpose(0, 1, 4, 5, 3, 6, 2)                    # (b, c, f, i, ph, j, pw)
+    return np.ascontiguousarray(t).reshape(B, C, F, Hp * p, Wp * p)
