@@ -62,6 +62,11 @@ def parse_args():
     p.add_argument("--variant", default="contiguous", choices=["contiguous", "f16", "qkv_inplace"],
                    help="contiguous Q/K (default); the same in fp16; or Q and K as views of a "
                         "fused [B, N, 3, heads, head_dim] QKV buffer rotated in place")
+    p.add_argument("--op", default="rope", choices=["rope", "patchify"],
+                   help="rope: the fused 3D RoPE (default); patchify: the decoder's "
+                        "space-to-depth layout kernel and its inverse")
+    p.add_argument("--graph", action="store_true",
+                   help="capture one step's calls in a CUDA graph and time its replays")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
@@ -78,10 +83,13 @@ def workload_config(w: synthetic.Workload) -> dict:
                      f"{w.dtype} N(0,{w.sigma:g}) seed {w.seed}"),
         "B": w.B, "T": w.T, "H": w.H, "W": w.W, "heads": w.heads, "head_dim": w.head_dim,
         "split": list(w.split), "io_dtype": w.dtype,
-        "bytes_per_step": w.bytes_per_call,
-        "token_heads_per_step": w.token_heads,
-        "l2": ("no flush: each step reads and writes %.2f GB, far more than the 129 MB L2"
-               % (w.bytes_per_call / 1e9)) if w.bytes_per_call > 1 << 30 else
+        "bytes_per_call": w.bytes_per_call,
+        "calls_per_step": w.repeat,
+        "bytes_per_step": w.bytes_per_call * w.repeat,
+        "token_heads_per_step": w.token_heads * w.repeat,
+        "l2": ("no flush: each step reads and writes %.2f GB in distinct buffers, more than "
+               "the 129 MB L2" % (w.bytes_per_call * w.repeat / 1e9))
+              if w.bytes_per_call * w.repeat > 1 << 30 else
               "inputs smaller than L2: numbers include L2 reuse",
     }
 
@@ -334,23 +342,42 @@ def run_ours(args, w):
         def step():
             r.rope3d_apply_pair_strided(q, k, tabs, q, k, stream=stream)
     else:
-        q = host[0].to(dev).view(t_dtype).view(shp)
-        k = host[1].to(dev).view(t_dtype).view(shp)
-        qo = torch.empty_like(q)
-        ko = torch.empty_like(k)
+        # one buffer set per call of a step (the stage-4 tile runs 24 attention
+        # blocks, each with its own Q and K, sharing one table set)
+        sets = []
+        for _ in range(w.repeat):
+            q = host[0].to(dev).view(t_dtype).view(shp)
+            k = host[1].to(dev).view(t_dtype).view(shp)
+            sets.append((q, k, torch.empty_like(q), torch.empty_like(k)))
 
         def step():
-            r.rope3d_apply_pair(q, k, tabs, qo, ko, stream=stream)
+            for q, k, qo, ko in sets:
+                r.rope3d_apply_pair(q, k, tabs, qo, ko, stream=stream)
 
     # warm-up (the first call also runs the library's bit-exact gate)
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize(dev)
+    if args.graph:
+        # capture one step's calls in a CUDA graph (the gate has verified this
+        # configuration during warm-up, so no call synchronises) and replay it
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+            stream = torch.cuda.current_stream(dev)
+            step()
+        stream = torch.cuda.current_stream(dev)
+
+        def step():
+            graph.replay()
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize(dev)
     dt_code = {"bf16": r.BF16, "f16": r.F16, "f32": r.F32}[w.dtype]
     verdict = (r.rope3d_gate_verdict(w.B, w.T, w.H, w.W, w.heads, w.head_dim, w.split, w.base, dt_code)
                if args.variant != "qkv_inplace" else 1)  # a strided call that returned was verified
     launch = r.rope3d_last_launch()
-    launches_per_step = launches_per_call(w, launch["kernel"])
+    calls = w.repeat if args.variant != "qkv_inplace" else 1
+    launches_per_step = calls * launches_per_call(w, launch["kernel"])
 
     # timed region: exactly K steps, per-launch events on the launching stream
     clocks = ClockSampler(smi_gpu_id(local))
@@ -378,15 +405,15 @@ def run_ours(args, w):
 
     total_ms = max_over_ranks(total_ms, dist, dev)
 
-    bytes_step = w.bytes_per_call
+    bytes_step = w.bytes_per_call * calls
     value = world * args.steps * bytes_step / (total_ms / 1e3) / 1e9
-    kernel_ms = statistics.fmean(per_launch)
-    achieved = bytes_step / (kernel_ms / 1e3) / 1e9
+    kernel_ms = statistics.fmean(per_launch) / calls   # per call (one launch per call)
+    achieved = w.bytes_per_call / (kernel_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
 
     # end to end through the host-buffer entry point (copies inside the timed region)
     e2e = None
-    if not args.no_e2e and args.variant != "qkv_inplace":
+    if not args.no_e2e and args.variant != "qkv_inplace" and w.repeat == 1:
         r.rope3d_apply_pair_host(hq, hk, hqo, hko, tabs)  # warm-up: staging allocation
         if dist:
             dist.barrier()
@@ -408,7 +435,8 @@ def run_ours(args, w):
             "dtype": "f32", "data": "synthetic",
             "config": dict(workload_config(w), variant=args.variant,
                            parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
-            "token_heads_per_s": world * args.steps * w.token_heads / (total_ms / 1e3),
+            "token_heads_per_s": world * args.steps * calls * w.token_heads / (total_ms / 1e3),
+            "calls_per_step": calls, "cuda_graph": bool(args.graph),
             "pct_of_peak_hbm": 100.0 * achieved / peak,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic_per_launch(w),
@@ -430,8 +458,85 @@ def run_ours(args, w):
     return 0
 
 
+# The patchify workload: a stand-in for the decoder's pixel-space volume (the
+# page gives neither the patch size nor the shape): bf16, 1.07 GB each way.
+PATCHIFY = dict(B=1, C=32, F=16, H=512, W=512, p=4)
+
+
+def run_patchify(args):
+    """Time rope3d_patchify (the step) and rope3d_unpatchify on PATCHIFY."""
+    import torch
+
+    import rope_rope3d_apply_gb300 as r
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    r.load_library()
+    c = PATCHIFY
+    shape = (c["B"], c["C"], c["F"], c["H"], c["W"])
+    n = int(np.prod(shape))
+    host = torch.empty(n * 2, dtype=torch.uint8).pin_memory()
+    synthetic.normal(n, 1.0, 9, 0, "bf16", out=host.numpy().view(np.uint16))
+    x = host.to(dev).view(torch.bfloat16).view(shape)
+    p = c["p"]
+    y = torch.empty((c["B"], c["C"] * p * p, c["F"], c["H"] // p, c["W"] // p),
+                    dtype=x.dtype, device=dev)
+    x2 = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(args.warmup, 3)):
+        r.rope3d_patchify(x, p, y, stream=stream)
+        r.rope3d_unpatchify(y, p, x2, stream=stream)
+    torch.cuda.synchronize(dev)
+    assert torch.equal(x2.view(torch.int16), x.view(torch.int16))
+    kernel = r.rope3d_patchify_last_kernel()
+
+    def timed(fn):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(args.steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / args.steps
+
+    clocks = ClockSampler(smi_gpu_id(dev.index))
+    clocks.start()
+    time.sleep(0.3)
+    t0 = time.time()
+    ms_fwd = timed(lambda: r.rope3d_patchify(x, p, y, stream=stream))
+    t1 = time.time()
+    ms_inv = timed(lambda: r.rope3d_unpatchify(y, p, x2, stream=stream))
+    time.sleep(0.25)
+    clocks.stop()
+    moved = 2 * n * 2
+    peak, peak_kind = measured_peak()
+    achieved = moved / (ms_fwd / 1e3) / 1e9
+    line = {
+        "op": "patchify", "metric": "patchify (space-to-depth) achieved HBM GB/s", "value": achieved,
+        "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_fwd,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "patchify: x (B=%d, C=%d, F=%d, H=%d, W=%d) bf16, p=%d" % (
+            c["B"], c["C"], c["F"], c["H"], c["W"], p), "bytes_per_step": moved,
+            "l2": "no flush: 1.07 GB read and written per step"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)", "kernel_ms": ms_fwd},
+        "unpatchify": {"ms": ms_inv, "GBps": moved / (ms_inv / 1e3) / 1e9,
+                       "frac": moved / (ms_inv / 1e3) / 1e9 / peak},
+        "kernel": {1: "vector", 2: "element"}.get(kernel, "?"),
+        "clocks": clocks.summary(t0, t1), "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.op == "patchify":
+        return run_patchify(args)
     w = synthetic.WORKLOADS[args.workload]
     if args.variant == "f16":
         w = dataclasses.replace(w, dtype="f16")

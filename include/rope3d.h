@@ -193,6 +193,44 @@ int rope3d_preflight_strided(const void *q, const void *k, const void *q_out,
                              int32_t check_device);
 
 /*
+ * rope3d_patchify -- space-to-depth of the decoder's pixel/latent volume
+ * (sglang PR #34471 review, "关键源码片段", _patchify of
+ * ltx_2_5_diffusion_decoder.py): x of shape (B, C, F, H, W) becomes y of shape
+ * (B, C*p*p, F, H/p, W/p) with channels packed as (channel, width offset,
+ * height offset):  y[b, (c*p + pw)*p + ph, f, i, j] = x[b, c, f, i*p + ph, j*p + pw].
+ * A bit-exact permutation: the element type only sets its size.
+ *
+ *   x, y        device pointers, contiguous, caller-owned, not overlapping,
+ *               aligned to elem_bytes
+ *   B, C, F, H, W   sizes of x; H and W multiples of p; B*C*F < 2^31,
+ *               H*W <= 2^30
+ *   p           patch size >= 1 (1, 2, 4 and 8 take the 16-byte vector kernel
+ *               when W/p is a multiple of 16/elem_bytes and both pointers are
+ *               16-byte aligned; other cases take an element kernel)
+ *   elem_bytes  1, 2, 4 or 8
+ *   stream      cudaStream_t; asynchronous
+ * Errors: NULL, SHAPE, DTYPE (elem_bytes), ALIGN, ALIAS, DEVICE, CUDA.
+ */
+int rope3d_patchify(const void *x, void *y, int64_t B, int64_t C, int64_t F, int64_t H,
+                    int64_t W, int64_t p, int32_t elem_bytes, void *stream);
+
+/*
+ * rope3d_unpatchify -- the exact inverse of rope3d_patchify (the page names
+ * _unpatchify without code): y (B, C*p*p, F, H/p, W/p) back to x
+ * (B, C, F, H, W). Arguments as rope3d_patchify, with B, C, F, H, W the sizes
+ * of x.
+ */
+int rope3d_unpatchify(const void *y, void *x, int64_t B, int64_t C, int64_t F, int64_t H,
+                      int64_t W, int64_t p, int32_t elem_bytes, void *stream);
+
+/* The host-side checks of rope3d_patchify / rope3d_unpatchify (no GPU needed). */
+int rope3d_patchify_check(const void *src, const void *dst, int64_t B, int64_t C, int64_t F,
+                          int64_t H, int64_t W, int64_t p, int32_t elem_bytes);
+
+/* Kernel of the last successful patchify call on this thread: 1 vector, 2 element. */
+int rope3d_patchify_last_kernel(void);
+
+/*
  * rope3d_apply_pair_host -- the same rotation for HOST buffers: the library
  * streams Q and K to the GPU in token chunks, rotates each chunk with the same
  * kernel, and streams Q_out and K_out back, overlapping the two copy

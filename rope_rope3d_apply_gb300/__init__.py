@@ -28,6 +28,7 @@ __all__ = [
     "rope3d_testing_max_units_per_launch", "rope3d_apply_pair_noalloc",
     "STATUS", "BF16", "F32", "F16", "GATE_OFF", "GATE_FIRST", "LIB_PATH",
     "rope3d_apply_pair_strided", "rope3d_preflight_strided", "view_strides",
+    "rope3d_patchify", "rope3d_unpatchify", "rope3d_patchify_check", "rope3d_patchify_last_kernel",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -83,6 +84,10 @@ def _declare(lib):
         "rope3d_apply_pair_noalloc": ([vp, vp, vp, vp] + [i64] * 6 + [vp, dbl, i32, vp], c.c_int),
         "rope3d_apply_pair_strided": ([vp, vp, vp, vp, vp] + [i64] * 6 + [vp, i32] + [vp] * 4 + [vp],
                                       c.c_int),
+        "rope3d_patchify": ([vp, vp] + [i64] * 6 + [i32, vp], c.c_int),
+        "rope3d_unpatchify": ([vp, vp] + [i64] * 6 + [i32, vp], c.c_int),
+        "rope3d_patchify_check": ([vp, vp] + [i64] * 6 + [i32], c.c_int),
+        "rope3d_patchify_last_kernel": ([], c.c_int),
         "rope3d_preflight_strided": ([vp, vp, vp, vp, vp] + [i64] * 6 + [vp, i32] + [vp] * 4 + [i32],
                                      c.c_int),
     }
@@ -351,6 +356,61 @@ def rope3d_preflight_strided(ptrs, strides, tables, B, T, H, W, heads, head_dim,
     return load_library().rope3d_preflight_strided(
         *[_ptr(p) for p in ptrs], handle, int(B), int(T), int(H), int(W), int(heads),
         int(head_dim), _split(split), int(dtype), *sts, 1 if check_device else 0)
+
+
+def _elem_bytes(t) -> int:
+    if hasattr(t, "element_size"):
+        return int(t.element_size())
+    return int(t.itemsize)
+
+
+def rope3d_patchify(x, p: int, y=None, stream=None):
+    """Space-to-depth (B, C, F, H, W) -> (B, C*p*p, F, H/p, W/p), channels in
+    the order (channel, width offset, height offset). x and y are contiguous
+    device tensors; y is allocated with torch.empty when not given."""
+    B, C, F, H, W = (int(v) for v in x.shape)
+    if y is None:
+        import torch
+
+        y = torch.empty((B, C * p * p, F, H // p, W // p), dtype=x.dtype, device=x.device)
+    for name, t in (("x", x), ("y", y)):
+        if not _contiguous(t):
+            raise ValueError(f"{name} must be contiguous")
+    if tuple(int(v) for v in y.shape) != (B, C * p * p, F, H // p, W // p) or y.dtype != x.dtype:
+        raise ValueError("y must have shape (B, C*p*p, F, H/p, W/p) and the dtype of x")
+    _check(load_library().rope3d_patchify(_ptr(x), _ptr(y), B, C, F, H, W, int(p),
+                                          _elem_bytes(x), _stream(stream, x)), "rope3d_patchify")
+    return y
+
+
+def rope3d_unpatchify(y, p: int, x=None, stream=None):
+    """Inverse of rope3d_patchify: (B, C*p*p, F, H/p, W/p) -> (B, C, F, H, W)."""
+    B, Cpp, F, Hp, Wp = (int(v) for v in y.shape)
+    if Cpp % (p * p):
+        raise ValueError("channels must be a multiple of p*p")
+    C, H, W = Cpp // (p * p), Hp * p, Wp * p
+    if x is None:
+        import torch
+
+        x = torch.empty((B, C, F, H, W), dtype=y.dtype, device=y.device)
+    for name, t in (("x", x), ("y", y)):
+        if not _contiguous(t):
+            raise ValueError(f"{name} must be contiguous")
+    if tuple(int(v) for v in x.shape) != (B, C, F, H, W) or x.dtype != y.dtype:
+        raise ValueError("x must have shape (B, C, F, H, W) and the dtype of y")
+    _check(load_library().rope3d_unpatchify(_ptr(y), _ptr(x), B, C, F, H, W, int(p),
+                                            _elem_bytes(y), _stream(stream, y)), "rope3d_unpatchify")
+    return x
+
+
+def rope3d_patchify_check(src, dst, B, C, F, H, W, p, elem_bytes) -> str:
+    """Name of the status the host-side checks give (no GPU needed)."""
+    return STATUS[load_library().rope3d_patchify_check(_ptr(src), _ptr(dst), int(B), int(C), int(F),
+                                                       int(H), int(W), int(p), int(elem_bytes))]
+
+
+def rope3d_patchify_last_kernel() -> int:
+    return int(load_library().rope3d_patchify_last_kernel())
 
 
 def rope3d_preflight(q, k, q_out, k_out, tables, B, T, H, W, heads, head_dim, split, dtype,

@@ -21,6 +21,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = [
     os.path.join(CSRC, "rope3d_kernels.cu"),
     os.path.join(CSRC, "rope3d_noalloc.cu"),
+    os.path.join(CSRC, "rope3d_patchify.cu"),
     os.path.join(CSRC, "rope3d_api.cpp"),
     os.path.join(CSRC, "rope3d_internal.h"),
     os.path.join(INCLUDE, "rope3d.h"),
@@ -54,14 +55,19 @@ def commands(out_dir: str = BUILD, extra_nvcc: list[str] | None = None):
         "-Xcompiler", "-fPIC,-ffp-contract=off",
         "-c", os.path.join(CSRC, "rope3d_noalloc.cu"), "-o", noalloc_o,
     ]
+    patch_o = os.path.join(out_dir, "rope3d_patchify.o")
+    nvcc_patch = [
+        _nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+        "-Xptxas", "-v", "-c", os.path.join(CSRC, "rope3d_patchify.cu"), "-o", patch_o,
+    ]
     gxx_compile = [
         "g++", "-std=c++17", "-O2", "-fPIC", "-ffp-contract=off", "-fno-fast-math",
         "-pthread", "-Wall", "-Wno-unused-function", f"-I{cuda}/include",
         "-c", os.path.join(CSRC, "rope3d_api.cpp"), "-o", api_o,
     ]
-    link = [_nvcc(), *ARCH, "-shared", kern_o, api_o, noalloc_o,
+    link = [_nvcc(), *ARCH, "-shared", kern_o, api_o, noalloc_o, patch_o,
             "-o", os.path.join(out_dir, "librope3d.so"), "-Xcompiler", "-pthread"]
-    return [nvcc_compile, gxx_compile, nvcc_noalloc], link
+    return [nvcc_compile, gxx_compile, nvcc_noalloc, nvcc_patch], link
 
 
 def up_to_date(lib: str = LIB) -> bool:

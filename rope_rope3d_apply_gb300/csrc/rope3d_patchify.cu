@@ -1,0 +1,316 @@
+// rope3d_patchify.cu -- space-to-depth layout kernels of the LTX-2.5 diffusion
+// decoder: rope3d_patchify and rope3d_unpatchify.
+//
+// sglang PR #34471 review, "关键源码片段", _patchify in
+// ltx_2_5_diffusion_decoder.py: x of shape (B, C, F, H, W) becomes
+// y of shape (B, C*p*p, F, H/p, W/p) with the channels packed in the order
+// (channel, width offset, height offset):
+//     y[b, (c*p + pw)*p + ph, f, i, j] = x[b, c, f, i*p + ph, j*p + pw].
+// _unpatchify (named there without code) is its exact inverse.
+//
+// The work is a pure permutation, bound by HBM bandwidth. One thread owns a
+// run of V = 16 / elem_bytes consecutive output columns j of one input row
+// (b, c, f, h): it loads the p*V input elements that feed them (p 16-byte
+// loads, contiguous across the warp), de-interleaves them in registers by
+// width offset, and stores p 16-byte vectors, one into each of the p output
+// rows (c, pw, ph) -- also contiguous across the warp. Unpatchify runs the same
+// loop backwards. Shapes whose rows are not a whole number of vectors, or
+// patch sizes other than 1, 2, 4 and 8, take an element-per-thread kernel.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/rope3d.h"
+#include "rope3d_internal.h"
+
+namespace {
+
+using rope3d::FastDiv;
+using rope3d::make_fastdiv;
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) {
+    return (__umulhi(n, f.mul) + n) >> f.shift;
+}
+
+template <int ES> struct ElemT;
+template <> struct ElemT<1> { using T = uint8_t; };
+template <> struct ElemT<2> { using T = uint16_t; };
+template <> struct ElemT<4> { using T = uint32_t; };
+template <> struct ElemT<8> { using T = uint64_t; };
+
+struct PParams {
+    const char *src;
+    char *dst;
+    uint32_t units;        // work units of this launch
+    FastDiv per_row;       // units per input row (b, c, f, h)
+    FastDiv Hd;            // H
+    FastDiv CF, Fd;        // C*F, F
+    FastDiv pd;            // p (scalar kernels)
+    FastDiv Wd;            // W (scalar kernels)
+    uint32_t bcf0;         // first (b, c, f) of this launch
+    uint32_t C, F, H, W, p;
+    uint32_t Hp, Wp;
+};
+
+// Decoded input row: global (b, c, f) index, and h split into (i, ph).
+struct Row {
+    uint32_t b, c, f, i, ph;
+    uint64_t row;          // global row index (b, c, f, h)
+};
+
+__device__ __forceinline__ Row decode_row(const PParams &q, uint32_t row_local, uint32_t p) {
+    Row r;
+    const uint32_t bcf_local = fdiv(row_local, q.Hd);
+    const uint32_t h = row_local - bcf_local * q.H;
+    const uint32_t bcf = q.bcf0 + bcf_local;
+    r.b = fdiv(bcf, q.CF);
+    const uint32_t rem = bcf - r.b * q.CF.d;
+    r.c = fdiv(rem, q.Fd);
+    r.f = rem - r.c * q.F;
+    r.i = h / p;
+    r.ph = h - r.i * p;
+    r.row = uint64_t(bcf) * q.H + h;
+    return r;
+}
+
+// Element offset of output row (b, c, pw, ph, f, i) of the patchified tensor.
+__device__ __forceinline__ uint64_t patched_row(const PParams &q, const Row &r, uint32_t pw,
+                                                uint32_t p) {
+    const uint64_t ch = (uint64_t(r.b) * q.C + r.c) * p * p + uint64_t(pw) * p + r.ph;
+    return ((ch * q.F + r.f) * q.Hp + r.i) * q.Wp;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void *ptr) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(ptr));
+    return v;
+}
+
+__device__ __forceinline__ void st_cs_v4(void *ptr, const uint4 &v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};"
+                 :
+                 : "l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// ---- vector kernels ----------------------------------------------------------
+
+template <int P, int ES, bool kForward>
+__global__ void __launch_bounds__(kThreads)
+patchify_vec_kernel(const PParams q) {
+    using E = typename ElemT<ES>::T;
+    constexpr int V = 16 / ES;  // output columns per thread and width offset
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < q.units; u += stride) {
+        const uint32_t row_local = fdiv(u, q.per_row);
+        const uint32_t jv = u - row_local * q.per_row.d;
+        const Row r = decode_row(q, row_local, P);
+        const uint64_t x_off = r.row * q.W + uint64_t(jv) * V * P;   // elements of x
+        const uint64_t col = uint64_t(jv) * V;                       // first output column
+        E e[V * P];
+        if constexpr (kForward) {
+            uint4 raw[P];
+#pragma unroll
+            for (int k = 0; k < P; ++k)
+                raw[k] = ld_nc_v4(q.src + (x_off * ES) + 16 * k);
+            memcpy(e, raw, sizeof raw);
+#pragma unroll
+            for (int pw = 0; pw < P; ++pw) {
+                E o[V];
+#pragma unroll
+                for (int t = 0; t < V; ++t) o[t] = e[t * P + pw];
+                uint4 ov;
+                memcpy(&ov, o, sizeof ov);
+                st_cs_v4(q.dst + (patched_row(q, r, pw, P) + col) * ES, ov);
+            }
+        } else {
+#pragma unroll
+            for (int pw = 0; pw < P; ++pw) {
+                const uint4 iv = ld_nc_v4(q.src + (patched_row(q, r, pw, P) + col) * ES);
+                E in[V];
+                memcpy(in, &iv, sizeof iv);
+#pragma unroll
+                for (int t = 0; t < V; ++t) e[t * P + pw] = in[t];
+            }
+            uint4 raw[P];
+            memcpy(raw, e, sizeof raw);
+#pragma unroll
+            for (int k = 0; k < P; ++k) st_cs_v4(q.dst + (x_off * ES) + 16 * k, raw[k]);
+        }
+    }
+}
+
+// ---- element kernels (any patch size, any row length) ----------------------
+
+template <int ES, bool kForward>
+__global__ void __launch_bounds__(kThreads)
+patchify_elem_kernel(const PParams q) {
+    using E = typename ElemT<ES>::T;
+    const E *src = reinterpret_cast<const E *>(q.src);
+    E *dst = reinterpret_cast<E *>(q.dst);
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < q.units; u += stride) {
+        const uint32_t row_local = fdiv(u, q.Wd);
+        const uint32_t w = u - row_local * q.W;
+        const Row r = decode_row(q, row_local, q.p);
+        const uint32_t j = fdiv(w, q.pd);
+        const uint32_t pw = w - j * q.p;
+        const uint64_t x_idx = r.row * q.W + w;
+        const uint64_t y_idx = patched_row(q, r, pw, q.p) + j;
+        if constexpr (kForward) {
+            dst[y_idx] = src[x_idx];
+        } else {
+            dst[x_idx] = src[y_idx];
+        }
+    }
+}
+
+using PFn = void (*)(PParams);
+
+template <int ES, bool kForward>
+PFn pick_vec(uint32_t p) {
+    switch (p) {
+        case 1: return patchify_vec_kernel<1, ES, kForward>;
+        case 2: return patchify_vec_kernel<2, ES, kForward>;
+        case 4: return patchify_vec_kernel<4, ES, kForward>;
+        case 8: return patchify_vec_kernel<8, ES, kForward>;
+        default: return nullptr;
+    }
+}
+
+template <bool kForward>
+PFn pick(int es, uint32_t p, bool vec) {
+    if (vec) {
+        switch (es) {
+            case 1: return pick_vec<1, kForward>(p);
+            case 2: return pick_vec<2, kForward>(p);
+            case 4: return pick_vec<4, kForward>(p);
+            case 8: return pick_vec<8, kForward>(p);
+        }
+        return nullptr;
+    }
+    switch (es) {
+        case 1: return patchify_elem_kernel<1, kForward>;
+        case 2: return patchify_elem_kernel<2, kForward>;
+        case 4: return patchify_elem_kernel<4, kForward>;
+        case 8: return patchify_elem_kernel<8, kForward>;
+    }
+    return nullptr;
+}
+
+bool device_ptr(const void *p, int device) {
+    cudaPointerAttributes attr{};
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (attr.type == cudaMemoryTypeManaged) return true;
+    return attr.type == cudaMemoryTypeDevice && attr.device == device;
+}
+
+thread_local int t_patch_kernel = 0;  // 1 vector, 2 element
+
+int run(bool forward, const void *src, void *dst, int64_t B, int64_t C, int64_t F, int64_t H,
+        int64_t W, int64_t p, int32_t elem_bytes, void *stream, bool check_device) {
+    if (!src || !dst) return ROPE3D_ERR_NULL;
+    if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)
+        return ROPE3D_ERR_DTYPE;
+    if (B <= 0 || C <= 0 || F <= 0 || H <= 0 || W <= 0 || p <= 0) return ROPE3D_ERR_SHAPE;
+    if (H % p != 0 || W % p != 0) return ROPE3D_ERR_SHAPE;
+    const int64_t lim = (int64_t(1) << 31) - 1;
+    if (B * C > lim || B * C * F > lim || H > lim || W > lim || C * p * p > lim)
+        return ROPE3D_ERR_SHAPE;
+    const double total = double(B) * C * F * H * W * elem_bytes;
+    if (total > 1.0e18) return ROPE3D_ERR_SHAPE;
+    const uint64_t bytes = uint64_t(B) * C * F * H * W * elem_bytes;
+    const uintptr_t s = reinterpret_cast<uintptr_t>(src), d = reinterpret_cast<uintptr_t>(dst);
+    if (s % elem_bytes != 0 || d % elem_bytes != 0) return ROPE3D_ERR_ALIGN;
+    if (s < d + bytes && d < s + bytes) return ROPE3D_ERR_ALIAS;
+    const uint64_t units_per_plane_elem = uint64_t(H) * uint64_t(W);
+    if (units_per_plane_elem > rope3d::kMaxUnitsPerLaunch) return ROPE3D_ERR_SHAPE;
+    if (!check_device) return ROPE3D_OK;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return ROPE3D_ERR_CUDA;
+    if (!device_ptr(src, device) || !device_ptr(dst, device)) return ROPE3D_ERR_DEVICE;
+
+    const uint32_t V = 16 / elem_bytes;
+    const uint32_t Wp = static_cast<uint32_t>(W / p);
+    const bool vec = (p == 1 || p == 2 || p == 4 || p == 8) && Wp % V == 0 && s % 16 == 0 &&
+                     d % 16 == 0;
+    const PFn fn = forward ? pick<true>(elem_bytes, static_cast<uint32_t>(p), vec)
+                           : pick<false>(elem_bytes, static_cast<uint32_t>(p), vec);
+    if (!fn) return ROPE3D_ERR_ARG;
+    const uint64_t units_per_row = vec ? Wp / V : uint64_t(W);
+
+    PParams q{};
+    q.src = static_cast<const char *>(src);
+    q.dst = static_cast<char *>(dst);
+    q.per_row = make_fastdiv(static_cast<uint32_t>(units_per_row));
+    q.Hd = make_fastdiv(static_cast<uint32_t>(H));
+    q.CF = make_fastdiv(static_cast<uint32_t>(C * F));
+    q.Fd = make_fastdiv(static_cast<uint32_t>(F));
+    q.pd = make_fastdiv(static_cast<uint32_t>(p));
+    q.Wd = make_fastdiv(static_cast<uint32_t>(W));
+    q.C = static_cast<uint32_t>(C);
+    q.F = static_cast<uint32_t>(F);
+    q.H = static_cast<uint32_t>(H);
+    q.W = static_cast<uint32_t>(W);
+    q.p = static_cast<uint32_t>(p);
+    q.Hp = static_cast<uint32_t>(H / p);
+    q.Wp = Wp;
+
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return ROPE3D_ERR_CUDA;
+    // launches cover whole (b, c, f) planes so that a launch's rows start at h = 0
+    const uint64_t rows_per_plane = uint64_t(H);
+    const uint64_t planes = uint64_t(B) * C * F;
+    const uint64_t units_per_plane = rows_per_plane * units_per_row;
+    // units_per_plane <= H * W <= 2^30 (checked above)
+    const uint64_t planes_per_launch = rope3d::kMaxUnitsPerLaunch / units_per_plane;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (uint64_t p0 = 0; p0 < planes; p0 += planes_per_launch) {
+        const uint64_t np = std::min(planes_per_launch, planes - p0);
+        q.units = static_cast<uint32_t>(np * units_per_plane);
+        q.bcf0 = static_cast<uint32_t>(p0);
+        const uint64_t need = (uint64_t(q.units) + kThreads - 1) / kThreads;
+        const int grid = static_cast<int>(std::min<uint64_t>(need, uint64_t(sms) * 8));
+        fn<<<grid, kThreads, 0, st>>>(q);
+        if (cudaGetLastError() != cudaSuccess) return ROPE3D_ERR_CUDA;
+    }
+    t_patch_kernel = vec ? 1 : 2;
+    return ROPE3D_OK;
+}
+
+}  // namespace
+
+extern "C" int rope3d_patchify(const void *x, void *y, int64_t B, int64_t C, int64_t F,
+                               int64_t H, int64_t W, int64_t p, int32_t elem_bytes,
+                               void *stream) {
+    const int rc = run(true, x, y, B, C, F, H, W, p, elem_bytes, stream, false);
+    if (rc != ROPE3D_OK) return rc;
+    return run(true, x, y, B, C, F, H, W, p, elem_bytes, stream, true);
+}
+
+extern "C" int rope3d_unpatchify(const void *y, void *x, int64_t B, int64_t C, int64_t F,
+                                 int64_t H, int64_t W, int64_t p, int32_t elem_bytes,
+                                 void *stream) {
+    const int rc = run(false, y, x, B, C, F, H, W, p, elem_bytes, stream, false);
+    if (rc != ROPE3D_OK) return rc;
+    return run(false, y, x, B, C, F, H, W, p, elem_bytes, stream, true);
+}
+
+extern "C" int rope3d_patchify_check(const void *src, const void *dst, int64_t B, int64_t C,
+                                     int64_t F, int64_t H, int64_t W, int64_t p,
+                                     int32_t elem_bytes) {
+    return run(true, src, const_cast<void *>(dst), B, C, F, H, W, p, elem_bytes, nullptr, false);
+}
+
+extern "C" int rope3d_patchify_last_kernel(void) { return t_patch_kernel; }

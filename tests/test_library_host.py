@@ -306,3 +306,21 @@ def test_strided_overlap_matches_brute_force(lib, host_tables):
     assert 30 < alias < 270  # both outcomes exercised
     for t in tabs.values():
         t.close()
+
+
+def test_patchify_host_checks(lib):
+    P = 1 << 32
+    Q = 1 << 36
+    ok = (P, Q, 1, 3, 2, 8, 8, 4, 2)
+    assert r.rope3d_patchify_check(*ok) == "OK"
+    cases = {
+        "ERR_NULL": (0, Q, 1, 3, 2, 8, 8, 4, 2),
+        "ERR_DTYPE": (P, Q, 1, 3, 2, 8, 8, 4, 3),
+        "ERR_SHAPE": (P, Q, 1, 3, 2, 8, 6, 4, 2),      # W not a multiple of p
+        "ERR_ALIGN": (P + 1, Q, 1, 3, 2, 8, 8, 4, 2),
+        "ERR_ALIAS": (P, P + 64, 1, 3, 2, 8, 8, 4, 2),
+    }
+    for want, args in cases.items():
+        assert r.rope3d_patchify_check(*args) == want, want
+    assert r.rope3d_patchify_check(P, Q, 1, 3, 2, 8, 8, 0, 2) == "ERR_SHAPE"
+    assert r.rope3d_patchify_check(P, Q, 1, 3, 2, 9, 9, 3, 1) == "OK"
