@@ -761,7 +761,8 @@ extern "C" int rope3d_apply_pair(const void *q, const void *k, void *q_out, void
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool vec16 = vec16_ok(g, q, k, q_out, k_out);
-    const LaunchArgs a = make_launch(g, tables, q, k, q_out, k_out, g.rows(), 0, vec16);
+    LaunchArgs a = make_launch(g, tables, q, k, q_out, k_out, g.rows(), 0, vec16);
+    a.pdl = true;
     LaunchInfo info{};
     if (rope3d::launch_rope3d(a, s, &info) != cudaSuccess) return ROPE3D_ERR_CUDA;
     t_last = info;
@@ -1012,6 +1013,7 @@ extern "C" int rope3d_apply_pair_strided(const void *q, const void *k, void *q_o
     LaunchArgs a = make_launch(g, tables, q, k, q_out, k_out, g.rows(), 0,
                                vec16_strided_ok(g, ptrs, st));
     a.strided = true;
+    a.pdl = !verify;  // the gate's gathers precede the kernel on this stream
     for (int i = 0; i < 4; ++i)
         for (int j = 0; j < 5; ++j) a.strides[i][j] = st[i][j];
     LaunchInfo info{};

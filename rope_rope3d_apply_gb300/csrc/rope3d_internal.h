@@ -62,6 +62,12 @@ struct LaunchArgs {
     // buffers are contiguous and the strides are unused.
     bool strided;
     int64_t strides[4][5];
+    // Launch with programmatic stream serialization (the kernel may start
+    // while the previous kernel of the stream drains; it waits for it before
+    // touching Q, K or the outputs). Only for launches whose preceding stream
+    // work is kernels or already complete: not after an upload of the tables
+    // or a cross-stream wait in the same call.
+    bool pdl;
 };
 
 // Copy a strided view ([B, T, H, W, heads, head_dim], element strides of

@@ -226,15 +226,29 @@ __device__ __forceinline__ uint4 rotate_vec(const uint4 v, const float4 cs01, co
     return o;
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream finishes:
+// it lets its own successor launch early, stages the tables (which no kernel
+// writes), and only then waits until every earlier grid has completed and its
+// writes are visible, before it touches Q, K or the outputs. Launched without
+// that attribute, both instructions return at once.
+__device__ __forceinline__ void allow_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void wait_for_prerequisite_grids() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 template <bool kSmem>
 __device__ __forceinline__ const float2 *stage_tables(const KParams &p, float2 *smem) {
+    allow_dependents_launch();
     if constexpr (kSmem) {
         for (uint32_t i = threadIdx.x; i < p.tab_len; i += blockDim.x) smem[i] = __ldg(p.tab + i);
         __syncthreads();
-        return smem;
-    } else {
-        return p.tab;
     }
+    wait_for_prerequisite_grids();
+    return kSmem ? smem : p.tab;
 }
 
 template <bool kSmem>
@@ -652,7 +666,18 @@ cudaError_t launch_rope3d(const LaunchArgs &a, cudaStream_t stream, LaunchInfo *
         int grid = 0;
         cudaError_t e = grid_for(reinterpret_cast<const void *>(fn), vid, smem_bytes, p.units, &grid);
         if (e != cudaSuccess) return e;
-        fn<<<grid, kBlock, smem_bytes, stream>>>(p, st);
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kBlock);
+        cfg.dynamicSmemBytes = smem_bytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = a.pdl ? attr : nullptr;
+        cfg.numAttrs = a.pdl ? 1 : 0;
+        e = cudaLaunchKernelEx(&cfg, fn, p, st);
+        if (e != cudaSuccess) return e;
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         if (info) {

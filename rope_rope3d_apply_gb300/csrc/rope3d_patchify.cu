@@ -101,48 +101,93 @@ __device__ __forceinline__ void st_cs_v4(void *ptr, const uint4 &v) {
 }
 
 // ---- vector kernels ----------------------------------------------------------
+// The x side of a warp's 32 units is one contiguous run of 32*P 16-byte chunks
+// (units are consecutive runs of x rows, and x rows are contiguous). A unit
+// owns P consecutive chunks, so if each lane moved its own chunks every warp
+// access would touch every other 32-byte sector. Instead the warp moves the
+// run chunk-by-chunk across lanes (lane t handles chunks t, t+32, ...), fully
+// coalesced, and swaps it through shared memory into per-unit order. The y
+// side is coalesced per width offset as it is. A warp whose 32 units are not
+// all in range (the last one) moves its chunks lane by lane.
+
+// Shared-memory slot of chunk c of a warp's run: an XOR swizzle of the low three
+// bits, so that both lane-contiguous and lane-strided (by P) accesses hit eight
+// different 16-byte bank groups per quarter warp.
+__device__ __forceinline__ uint32_t swz(uint32_t c) { return c ^ ((c >> 3) & 7u); }
 
 template <int P, int ES, bool kForward>
 __global__ void __launch_bounds__(kThreads)
 patchify_vec_kernel(const PParams q) {
     using E = typename ElemT<ES>::T;
     constexpr int V = 16 / ES;  // output columns per thread and width offset
+    __shared__ uint4 stage[kThreads / 32][32 * P];
+    const uint32_t lane = threadIdx.x & 31u;
+    uint4 *ws = stage[threadIdx.x >> 5];
     const uint32_t stride = gridDim.x * blockDim.x;
-    for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < q.units; u += stride) {
+    for (uint32_t base = blockIdx.x * blockDim.x + (threadIdx.x & ~31u); base < q.units;
+         base += stride) {
+        const uint32_t u = base + lane;
+        const bool whole = base + 31 < q.units;   // warp-uniform
+        const bool active = u < q.units;
         const uint32_t row_local = fdiv(u, q.per_row);
         const uint32_t jv = u - row_local * q.per_row.d;
         const Row r = decode_row(q, row_local, P);
-        const uint64_t x_off = r.row * q.W + uint64_t(jv) * V * P;   // elements of x
         const uint64_t col = uint64_t(jv) * V;                       // first output column
+        // byte offset in x of the warp's first unit (units map to x contiguously)
+        const uint32_t base_row = fdiv(base, q.per_row);
+        const uint32_t base_jv = base - base_row * q.per_row.d;
+        const uint64_t xb = ((uint64_t(q.bcf0) * q.H + base_row) * q.W + uint64_t(base_jv) * V * P) * ES;
         E e[V * P];
+        uint4 raw[P];
         if constexpr (kForward) {
-            uint4 raw[P];
+            if (whole) {
 #pragma unroll
-            for (int k = 0; k < P; ++k)
-                raw[k] = ld_nc_v4(q.src + (x_off * ES) + 16 * k);
-            memcpy(e, raw, sizeof raw);
+                for (int k = 0; k < P; ++k) ws[swz(k * 32 + lane)] = ld_nc_v4(q.src + xb + 16 * (k * 32 + lane));
+                __syncwarp();
 #pragma unroll
-            for (int pw = 0; pw < P; ++pw) {
-                E o[V];
+                for (int k = 0; k < P; ++k) raw[k] = ws[swz(lane * P + k)];
+                __syncwarp();
+            } else if (active) {
+                const uint64_t x_off = r.row * q.W + uint64_t(jv) * V * P;
 #pragma unroll
-                for (int t = 0; t < V; ++t) o[t] = e[t * P + pw];
-                uint4 ov;
-                memcpy(&ov, o, sizeof ov);
-                st_cs_v4(q.dst + (patched_row(q, r, pw, P) + col) * ES, ov);
+                for (int k = 0; k < P; ++k) raw[k] = ld_nc_v4(q.src + x_off * ES + 16 * k);
+            }
+            if (active) {
+                memcpy(e, raw, sizeof raw);
+#pragma unroll
+                for (int pw = 0; pw < P; ++pw) {
+                    E o[V];
+#pragma unroll
+                    for (int t = 0; t < V; ++t) o[t] = e[t * P + pw];
+                    uint4 ov;
+                    memcpy(&ov, o, sizeof ov);
+                    st_cs_v4(q.dst + (patched_row(q, r, pw, P) + col) * ES, ov);
+                }
             }
         } else {
+            if (active) {
 #pragma unroll
-            for (int pw = 0; pw < P; ++pw) {
-                const uint4 iv = ld_nc_v4(q.src + (patched_row(q, r, pw, P) + col) * ES);
-                E in[V];
-                memcpy(in, &iv, sizeof iv);
+                for (int pw = 0; pw < P; ++pw) {
+                    const uint4 iv = ld_nc_v4(q.src + (patched_row(q, r, pw, P) + col) * ES);
+                    E in[V];
+                    memcpy(in, &iv, sizeof iv);
 #pragma unroll
-                for (int t = 0; t < V; ++t) e[t * P + pw] = in[t];
+                    for (int t = 0; t < V; ++t) e[t * P + pw] = in[t];
+                }
+                memcpy(raw, e, sizeof raw);
             }
-            uint4 raw[P];
-            memcpy(raw, e, sizeof raw);
+            if (whole) {
 #pragma unroll
-            for (int k = 0; k < P; ++k) st_cs_v4(q.dst + (x_off * ES) + 16 * k, raw[k]);
+                for (int k = 0; k < P; ++k) ws[swz(lane * P + k)] = raw[k];
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < P; ++k) st_cs_v4(q.dst + xb + 16 * (k * 32 + lane), ws[swz(k * 32 + lane)]);
+                __syncwarp();
+            } else if (active) {
+                const uint64_t x_off = r.row * q.W + uint64_t(jv) * V * P;
+#pragma unroll
+                for (int k = 0; k < P; ++k) st_cs_v4(q.dst + x_off * ES + 16 * k, raw[k]);
+            }
         }
     }
 }
