@@ -74,6 +74,14 @@ def _declare(lib):
     lib.oracle_rope3d_bf16_at.restype = ctypes.c_int
     lib.oracle_rope3d_f32_at.argtypes = at
     lib.oracle_rope3d_f32_at.restype = ctypes.c_int
+    lib.oracle_neox_cache.argtypes = [i64, i64, ctypes.c_double, vp]
+    lib.oracle_neox_cache.restype = ctypes.c_int
+    lib.oracle_neox_pair16.argtypes = [ctypes.c_uint16] * 4 + [ctypes.c_int, vp, vp]
+    lib.oracle_neox_pair16.restype = None
+    lib.oracle_neox_pair_f32.argtypes = [ctypes.c_float] * 4 + [vp, vp]
+    lib.oracle_neox_pair_f32.restype = None
+    lib.oracle_rope_neox.argtypes = [vp, vp, i64, i64, i64, vp, vp, i64, ctypes.c_int]
+    lib.oracle_rope_neox.restype = ctypes.c_int
     return lib
 
 
@@ -244,3 +252,40 @@ def unpatchify(y: np.ndarray, p: int) -> np.ndarray:
     t = y.reshape(B, C, p, p, F, Hp, Wp)                    # (b, c, pw, ph, f, i, j)
     t = t.transpose(0, 1, 4, 5, 3, 6, 2)                    # (b, c, f, i, ph, j, pw)
     return np.ascontiguousarray(t).reshape(B, C, F, Hp * p, Wp * p)
+
+
+# ---------------------------------------------------------------------------
+# NeoX-style RoPE of the Gemma3 text encoder (sglang PR #24660 review,
+# "关键源码片段", gemma_3.py): see rope3d_oracle.c.
+# ---------------------------------------------------------------------------
+
+KIND = {"bf16": 0, "f32": 1, "f16": 2}
+
+
+def neox_cache(max_position: int, rotary_dim: int, base: float = 10000.0, lib=None) -> np.ndarray:
+    """[max_position, rotary_dim] float32 rows [cos | sin]."""
+    c = np.empty((max_position, rotary_dim), np.float32)
+    if (lib or load()).oracle_neox_cache(max_position, rotary_dim, float(base), _ptr(c)) != 0:
+        raise ValueError("bad cache arguments")
+    return c
+
+
+def neox_pair16(x1: int, x2: int, c: int, s: int, dtype: str = "bf16", lib=None):
+    y = np.zeros(2, np.uint16)
+    (lib or load()).oracle_neox_pair16(int(x1), int(x2), int(c), int(s), KIND[dtype],
+                                       _ptr(y), _ptr(y) + 2)
+    return int(y[0]), int(y[1])
+
+
+def rope_neox(x: np.ndarray, tokens: int, heads: int, head_dim: int, positions: np.ndarray,
+              cache: np.ndarray, dtype: str, lib=None) -> np.ndarray:
+    """x: [tokens, heads, head_dim] (uint16 bits for bf16/f16, float32 for f32)."""
+    x = np.ascontiguousarray(x)
+    y = np.empty_like(x)
+    pos = np.ascontiguousarray(positions, dtype=np.int64)
+    cache = np.ascontiguousarray(cache, dtype=np.float32)
+    rc = (lib or load()).oracle_rope_neox(_ptr(x), _ptr(y), tokens, heads, head_dim, _ptr(pos),
+                                          _ptr(cache), cache.shape[0], KIND[dtype])
+    if rc != 0:
+        raise ValueError("oracle_rope_neox rejected its arguments")
+    return y

@@ -395,3 +395,105 @@ int oracle_rope3d_f32_at(const float *x, const int64_t *indices, int64_t n,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* NeoX-style RoPE of the Gemma3 text encoder (sglang PR #24660 review,      */
+/* "关键源码片段", gemma_3.py _apply_rotary_pos_emb): the rows of a           */
+/* cos_sin_cache [max_position][rotary_dim] = [cos | sin] are gathered by     */
+/* token position, duplicated to the full rotary width and cast to the input  */
+/* dtype; then q * cos + rotate_half(q) * sin in that dtype, where            */
+/* rotate_half(x) = (-x2, x1) for the halves x1 = x[:d/2], x2 = x[d/2:].     */
+/* Each tensor operation rounds to the input dtype: a product of two         */
+/* 16-bit values is exact in float and rounded once; the sum of two 16-bit   */
+/* values is rounded to float and then to the 16-bit type (the order a       */
+/* PyTorch 16-bit add takes). rotary_dim is head_dim (the page passes        */
+/* rotary_dim=head_dim).                                                     */
+/* ------------------------------------------------------------------------- */
+
+/* Cache rows in the page's layout: cos of p * base^(-2j/d) for j < d/2, then
+ * the sines (standard RoPE angles; the page builds the cache with get_rope,
+ * whose formula it does not print). */
+int oracle_neox_cache(int64_t max_position, int64_t rotary_dim, double base, float *cache)
+{
+    if (max_position <= 0 || rotary_dim <= 0 || (rotary_dim % 2) != 0 || !(base > 0.0))
+        return -1;
+    const int64_t half = rotary_dim / 2;
+    for (int64_t p = 0; p < max_position; ++p)
+        for (int64_t j = 0; j < half; ++j) {
+            double exponent = -(2.0 * (double)j) / (double)rotary_dim;
+            double angle = (double)p * pow(base, exponent);
+            cache[p * rotary_dim + j] = (float)cos(angle);
+            cache[p * rotary_dim + half + j] = (float)sin(angle);
+        }
+    return 0;
+}
+
+/* One NeoX pair (x1 at channel j, x2 at channel j + d/2) in 16-bit storage:
+ * c and s are already cast to the storage type. kind: 0 bf16, 2 fp16. */
+static uint16_t to16(float f, int kind) { return kind == 0 ? oracle_f32_to_bf16(f) : oracle_f32_to_f16(f); }
+static float from16(uint16_t h, int kind) { return kind == 0 ? oracle_bf16_to_f32(h) : oracle_f16_to_f32(h); }
+
+void oracle_neox_pair16(uint16_t x1, uint16_t x2, uint16_t c, uint16_t s, int kind,
+                        uint16_t *y1, uint16_t *y2)
+{
+    const float fx1 = from16(x1, kind), fx2 = from16(x2, kind);
+    const float fc = from16(c, kind), fs = from16(s, kind);
+    /* q * cos */
+    const uint16_t x1c = to16(fx1 * fc, kind);
+    const uint16_t x2c = to16(fx2 * fc, kind);
+    /* rotate_half(q) * sin: (-x2) * sin for the first half, x1 * sin for the second */
+    const float neg_x2 = -fx2;
+    const uint16_t nx2s = to16(neg_x2 * fs, kind);
+    const uint16_t x1s = to16(fx1 * fs, kind);
+    /* the sum, rounded to float and then to the storage type */
+    const float sum1 = from16(x1c, kind) + from16(nx2s, kind);
+    const float sum2 = from16(x2c, kind) + from16(x1s, kind);
+    *y1 = to16(sum1, kind);
+    *y2 = to16(sum2, kind);
+}
+
+void oracle_neox_pair_f32(float x1, float x2, float c, float s, float *y1, float *y2)
+{
+    const float x1c = x1 * c;
+    const float x2c = x2 * c;
+    const float neg_x2 = -x2;
+    const float nx2s = neg_x2 * s;
+    const float x1s = x1 * s;
+    *y1 = x1c + nx2s;
+    *y2 = x2c + x1s;
+}
+
+/* x, y: [tokens][heads][head_dim] contiguous; kind 0 bf16 / 2 fp16 (uint16
+ * bits) or 1 fp32. Positions outside [0, max_position) are rejected. */
+int oracle_rope_neox(const void *x, void *y, int64_t tokens, int64_t heads, int64_t head_dim,
+                     const int64_t *positions, const float *cache, int64_t max_position, int kind)
+{
+    if (tokens <= 0 || heads <= 0 || head_dim <= 0 || (head_dim % 2) != 0)
+        return -1;
+    const int64_t half = head_dim / 2;
+    for (int64_t t = 0; t < tokens; ++t) {
+        const int64_t p = positions[t];
+        if (p < 0 || p >= max_position)
+            return -1;
+        const float *cs = cache + p * head_dim;
+        for (int64_t h = 0; h < heads; ++h) {
+            const int64_t row = (t * heads + h) * head_dim;
+            for (int64_t j = 0; j < half; ++j) {
+                if (kind == 1) {
+                    const float *xf = (const float *)x;
+                    float *yf = (float *)y;
+                    oracle_neox_pair_f32(xf[row + j], xf[row + half + j], cs[j], cs[half + j],
+                                         &yf[row + j], &yf[row + half + j]);
+                } else {
+                    const uint16_t *xh = (const uint16_t *)x;
+                    uint16_t *yh = (uint16_t *)y;
+                    const uint16_t c16 = to16(cs[j], kind);          /* cos.to(q.dtype) */
+                    const uint16_t s16 = to16(cs[half + j], kind);   /* sin.to(q.dtype) */
+                    oracle_neox_pair16(xh[row + j], xh[row + half + j], c16, s16, kind,
+                                       &yh[row + j], &yh[row + half + j]);
+                }
+            }
+        }
+    }
+    return 0;
+}
