@@ -62,7 +62,7 @@ def parse_args():
     p.add_argument("--variant", default="contiguous", choices=["contiguous", "f16", "qkv_inplace"],
                    help="contiguous Q/K (default); the same in fp16; or Q and K as views of a "
                         "fused [B, N, 3, heads, head_dim] QKV buffer rotated in place")
-    p.add_argument("--op", default="rope", choices=["rope", "patchify"],
+    p.add_argument("--op", default="rope", choices=["rope", "patchify", "neox"],
                    help="rope: the fused 3D RoPE (default); patchify: the decoder's "
                         "space-to-depth layout kernel and its inverse")
     p.add_argument("--graph", action="store_true",
@@ -533,10 +533,76 @@ def run_patchify(args):
     return 0
 
 
+# The NeoX workload: a Gemma3-like prefill (the page gives no sizes): 65,536
+# tokens, 8 query heads and 4 key heads of 256 channels, bf16, positions
+# 0..65535 into a 131,072-row cache.
+NEOX = dict(tokens=65536, q_heads=8, k_heads=4, head_dim=256, max_position=131072)
+
+
+def run_neox(args):
+    """Time rope3d_apply_neox on NEOX (one launch per step)."""
+    import torch
+
+    import rope_rope3d_apply_gb300 as r
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    r.load_library()
+    c = NEOX
+    t, qh, kh, hd = c["tokens"], c["q_heads"], c["k_heads"], c["head_dim"]
+    q = torch.from_numpy(synthetic.normal(t * qh * hd, 1.0, 11, 0, "bf16").view(np.int16)) \
+        .view(torch.bfloat16).reshape(t, qh, hd).to(dev)
+    k = torch.from_numpy(synthetic.normal(t * kh * hd, 1.0, 11, 1, "bf16").view(np.int16)) \
+        .view(torch.bfloat16).reshape(t, kh, hd).to(dev)
+    pos = torch.arange(t, dtype=torch.int64, device=dev)
+    cache = torch.from_numpy(r.rope3d_neox_cache_host(c["max_position"], hd)).to(dev)
+    qo, ko = torch.empty_like(q), torch.empty_like(k)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(args.warmup, 3)):
+        r.rope3d_apply_neox(q, k, pos, cache, qo, ko, stream=stream)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(smi_gpu_id(dev.index))
+    clocks.start()
+    time.sleep(0.3)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    a.record(stream)
+    for _ in range(args.steps):
+        r.rope3d_apply_neox(q, k, pos, cache, qo, ko, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    time.sleep(0.25)
+    clocks.stop()
+    ms = a.elapsed_time(b) / args.steps
+    moved = (qh + kh) * hd * 2 * 2 * t + t * hd * 4 + t * 8
+    peak, peak_kind = measured_peak()
+    achieved = moved / (ms / 1e3) / 1e9
+    line = {
+        "op": "neox", "metric": "NeoX RoPE (Q+K) achieved HBM GB/s", "value": achieved, "unit": UNIT,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "neox: %d tokens, %d/%d heads x %d, cache %d rows, positions 0..%d" % (
+            t, qh, kh, hd, c["max_position"], t - 1), "bytes_per_step": moved,
+            "l2": "no flush: %.2f GB per step, more than the 129 MB L2" % (moved / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)", "kernel_ms": ms},
+        "kernel": {1: "vector", 2: "pair"}.get(r.rope3d_neox_last_kernel(), "?"),
+        "clocks": clocks.summary(t0, t1), "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.op == "patchify":
         return run_patchify(args)
+    if args.op == "neox":
+        return run_neox(args)
     w = synthetic.WORKLOADS[args.workload]
     if args.variant == "f16":
         w = dataclasses.replace(w, dtype="f16")

@@ -231,6 +231,55 @@ int rope3d_patchify_check(const void *src, const void *dst, int64_t B, int64_t C
 int rope3d_patchify_last_kernel(void);
 
 /*
+ * rope3d_apply_neox -- NeoX-style rotary embedding of the Gemma3 text encoder
+ * (sglang PR #24660 review, "关键源码片段", gemma_3.py _apply_rotary_pos_emb):
+ * for each token, row positions[t] of cos_sin_cache = [cos | sin] is cast to
+ * the input dtype and applied to both halves of every head of Q and K:
+ *     y = x * cos + rotate_half(x) * sin,  rotate_half(x) = (-x2, x1),
+ * x1, x2 the halves of head_dim, each tensor operation rounded to the input
+ * dtype (products rounded once; sums rounded to float, then to the dtype).
+ *
+ *   q, k          device, [tokens, q_heads, head_dim] / [tokens, k_heads,
+ *                 head_dim] contiguous, 4-byte aligned
+ *   q_out, k_out  device outputs of the same shapes; q_out == q and/or
+ *                 k_out == k rotate in place; otherwise an output overlaps
+ *                 nothing (nor the positions, cache or counter)
+ *   positions     device int64 [tokens], 8-byte aligned
+ *   cos_sin_cache device fp32 [max_position][head_dim], 4-byte aligned (16 for
+ *                 the vector kernel); rotary_dim is head_dim
+ *   dtype         ROPE3D_BF16, ROPE3D_F16 or ROPE3D_F32
+ *   invalid_count optional device int32: a position outside [0, max_position)
+ *                 leaves its outputs unwritten and adds the number of skipped
+ *                 work units (16-byte vectors or pairs) here; the caller zeroes
+ *                 it. NULL: skipped silently.
+ *   stream        cudaStream_t; asynchronous
+ * The bit-exact gate does not run here. Errors: NULL, SHAPE (sizes <= 0, odd
+ * head_dim, head_dim > ROPE3D_MAX_HEAD_DIM), DTYPE, ALIGN, ALIAS, DEVICE, CUDA.
+ */
+int rope3d_apply_neox(const void *q, const void *k, void *q_out, void *k_out,
+                      const int64_t *positions, const float *cos_sin_cache,
+                      int64_t max_position, int64_t tokens, int64_t q_heads, int64_t k_heads,
+                      int64_t head_dim, int32_t dtype, int32_t *invalid_count, void *stream);
+
+/* The host-side checks of rope3d_apply_neox, without a launch or device queries. */
+int rope3d_neox_check(const void *q, const void *k, const void *q_out, const void *k_out,
+                      const int64_t *positions, const float *cos_sin_cache,
+                      int64_t max_position, int64_t tokens, int64_t q_heads, int64_t k_heads,
+                      int64_t head_dim, int32_t dtype, const int32_t *invalid_count);
+
+/*
+ * rope3d_neox_cache_host -- fill a host cos_sin_cache [max_position][rotary_dim]
+ * in the layout above: cos then sin of p * base^(-2j/rotary_dim), j < rotary_dim/2,
+ * in double, rounded once to float (standard RoPE angles; the page builds the
+ * cache with get_rope and does not print its formula).
+ * Errors: NULL, SHAPE, ARG (base).
+ */
+int rope3d_neox_cache_host(int64_t max_position, int64_t rotary_dim, double base, float *cache);
+
+/* Kernel of the last successful rope3d_apply_neox on this thread: 1 vector, 2 pair. */
+int rope3d_neox_last_kernel(void);
+
+/*
  * rope3d_apply_pair_host -- the same rotation for HOST buffers: the library
  * streams Q and K to the GPU in token chunks, rotates each chunk with the same
  * kernel, and streams Q_out and K_out back, overlapping the two copy

@@ -29,6 +29,7 @@ __all__ = [
     "STATUS", "BF16", "F32", "F16", "GATE_OFF", "GATE_FIRST", "LIB_PATH",
     "rope3d_apply_pair_strided", "rope3d_preflight_strided", "view_strides",
     "rope3d_patchify", "rope3d_unpatchify", "rope3d_patchify_check", "rope3d_patchify_last_kernel",
+    "rope3d_apply_neox", "rope3d_neox_check", "rope3d_neox_cache_host", "rope3d_neox_last_kernel",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -88,6 +89,10 @@ def _declare(lib):
         "rope3d_unpatchify": ([vp, vp] + [i64] * 6 + [i32, vp], c.c_int),
         "rope3d_patchify_check": ([vp, vp] + [i64] * 6 + [i32], c.c_int),
         "rope3d_patchify_last_kernel": ([], c.c_int),
+        "rope3d_apply_neox": ([vp] * 6 + [i64] * 5 + [i32, vp, vp], c.c_int),
+        "rope3d_neox_check": ([vp] * 6 + [i64] * 5 + [i32, vp], c.c_int),
+        "rope3d_neox_cache_host": ([i64, i64, dbl, vp], c.c_int),
+        "rope3d_neox_last_kernel": ([], c.c_int),
         "rope3d_preflight_strided": ([vp, vp, vp, vp, vp] + [i64] * 6 + [vp, i32] + [vp] * 4 + [i32],
                                      c.c_int),
     }
@@ -411,6 +416,66 @@ def rope3d_patchify_check(src, dst, B, C, F, H, W, p, elem_bytes) -> str:
 
 def rope3d_patchify_last_kernel() -> int:
     return int(load_library().rope3d_patchify_last_kernel())
+
+
+def rope3d_neox_cache_host(max_position: int, rotary_dim: int, base: float = 10000.0):
+    """Host cos_sin_cache [max_position, rotary_dim] = [cos | sin] (float32 numpy)."""
+    import numpy as np
+
+    c = np.empty((max_position, rotary_dim), np.float32)
+    _check(load_library().rope3d_neox_cache_host(int(max_position), int(rotary_dim), float(base),
+                                                 _ptr(c)), "rope3d_neox_cache_host")
+    return c
+
+
+def rope3d_apply_neox(q, k, positions, cos_sin_cache, q_out=None, k_out=None,
+                      invalid_count=None, stream=None):
+    """NeoX-style RoPE (Gemma3): q [tokens, q_heads, head_dim], k [tokens,
+    k_heads, head_dim], positions int64 [tokens], cos_sin_cache float32
+    [max_position, head_dim], all on the device. q_out=q / k_out=k rotate in
+    place; missing outputs are allocated with torch.empty_like."""
+    if q_out is None or k_out is None:
+        import torch
+
+        q_out = torch.empty_like(q) if q_out is None else q_out
+        k_out = torch.empty_like(k) if k_out is None else k_out
+    for name, t in (("q", q), ("k", k), ("q_out", q_out), ("k_out", k_out),
+                    ("positions", positions), ("cos_sin_cache", cos_sin_cache)):
+        if not _contiguous(t):
+            raise ValueError(f"{name} must be contiguous")
+    if q.dim() != 3 or k.dim() != 3 or q.shape[0] != k.shape[0] or q.shape[2] != k.shape[2]:
+        raise ValueError("q and k must be [tokens, heads, head_dim] with one tokens and head_dim")
+    if tuple(q_out.shape) != tuple(q.shape) or tuple(k_out.shape) != tuple(k.shape):
+        raise ValueError("outputs must have the shapes of q and k")
+    tokens, q_heads, head_dim = (int(v) for v in q.shape)
+    k_heads = int(k.shape[1])
+    if str(positions.dtype) != "torch.int64" or positions.numel() != tokens:
+        raise ValueError("positions must be int64 with one entry per token")
+    if str(cos_sin_cache.dtype) != "torch.float32" or cos_sin_cache.dim() != 2 or \
+            int(cos_sin_cache.shape[1]) != head_dim:
+        raise ValueError("cos_sin_cache must be float32 [max_position, head_dim]")
+    dt = _dtype_code(q)
+    for t in (k, q_out, k_out):
+        if _dtype_code(t) != dt:
+            raise TypeError("q, k, q_out and k_out must have one dtype")
+    rc = load_library().rope3d_apply_neox(
+        _ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), _ptr(positions), _ptr(cos_sin_cache),
+        int(cos_sin_cache.shape[0]), tokens, q_heads, k_heads, head_dim, dt,
+        _ptr(invalid_count), _stream(stream, q))
+    _check(rc, "rope3d_apply_neox")
+    return q_out, k_out
+
+
+def rope3d_neox_check(ptrs, max_position, tokens, q_heads, k_heads, head_dim, dtype) -> str:
+    """Status name of the host-side checks of rope3d_apply_neox. ptrs: (q, k,
+    q_out, k_out, positions, cache, invalid_count) addresses."""
+    return STATUS[load_library().rope3d_neox_check(*[_ptr(p) for p in ptrs[:6]], int(max_position),
+                                                   int(tokens), int(q_heads), int(k_heads),
+                                                   int(head_dim), int(dtype), _ptr(ptrs[6]))]
+
+
+def rope3d_neox_last_kernel() -> int:
+    return int(load_library().rope3d_neox_last_kernel())
 
 
 def rope3d_preflight(q, k, q_out, k_out, tables, B, T, H, W, heads, head_dim, split, dtype,

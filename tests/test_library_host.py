@@ -324,3 +324,35 @@ def test_patchify_host_checks(lib):
         assert r.rope3d_patchify_check(*args) == want, want
     assert r.rope3d_patchify_check(P, Q, 1, 3, 2, 8, 8, 0, 2) == "ERR_SHAPE"
     assert r.rope3d_patchify_check(P, Q, 1, 3, 2, 9, 9, 3, 1) == "OK"
+
+
+def test_neox_cache_matches_oracle_bitwise(lib):
+    for max_pos, d, base in [(64, 16, 10000.0), (4096, 256, 10000.0), (33, 6, 1e6)]:
+        got = r.rope3d_neox_cache_host(max_pos, d, base)
+        want = oracle.neox_cache(max_pos, d, base)
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_neox_host_checks(lib):
+    base = 1 << 32
+    step = 1 << 28
+    ptrs = [base + i * step for i in range(7)]
+    ok = (4096, 100, 8, 4, 256, r.BF16)
+    assert r.rope3d_neox_check(ptrs, *ok) == "OK"
+    inplace = ptrs[:2] + ptrs[:2] + ptrs[4:]
+    assert r.rope3d_neox_check(inplace, *ok) == "OK"
+    swapped = ptrs[:2] + [ptrs[1], ptrs[0]] + ptrs[4:]
+    assert r.rope3d_neox_check(swapped, *ok) == "ERR_ALIAS"
+    onto_cache = ptrs[:2] + [ptrs[5], ptrs[3]] + ptrs[4:]
+    assert r.rope3d_neox_check(onto_cache, *ok) == "ERR_ALIAS"
+    assert r.rope3d_neox_check(ptrs, 4096, 100, 8, 4, 255, r.BF16) == "ERR_SHAPE"
+    assert r.rope3d_neox_check(ptrs, 4096, 0, 8, 4, 256, r.BF16) == "ERR_SHAPE"
+    assert r.rope3d_neox_check(ptrs, 4096, 100, 8, 4, 256, 7) == "ERR_DTYPE"
+    bad = list(ptrs)
+    bad[4] += 4    # positions must be 8-byte aligned
+    assert r.rope3d_neox_check(bad, *ok) == "ERR_ALIGN"
+    nul = list(ptrs)
+    nul[5] = 0
+    assert r.rope3d_neox_check(nul, *ok) == "ERR_NULL"
+    no_counter = ptrs[:6] + [0]
+    assert r.rope3d_neox_check(no_counter, *ok) == "OK"
