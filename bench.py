@@ -189,6 +189,25 @@ class ClockSampler:
                 "samples": len(used), "samples_in_window": len(inside)}
 
 
+def same_box_copy_gbs(torch, dev) -> float:
+    """A torch copy of 1 Gi bf16 elements on this GPU (read + write bytes,
+    best of 10, CUDA events), the way the measured peak was taken: shows how
+    this GPU compares with the one the peak was measured on."""
+    x = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev)
+    y = torch.empty_like(x)
+    best = 0.0
+    for _ in range(11):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        y.copy_(x)
+        b.record()
+        torch.cuda.synchronize(dev)
+        best = max(best, 2 * x.numel() * 2 / (a.elapsed_time(b) / 1e3) / 1e9)
+    del x, y
+    return best
+
+
 def launches_per_call(w: synthetic.Workload, kernel: int) -> int:
     """Kernel launches of one call: one per 2^30 work units (16-byte vectors or
     pairs), whole rows per launch."""
@@ -424,6 +443,7 @@ def run_ours(args, w):
 
     total_ms = max_over_ranks(total_ms, dist, dev)
 
+    box_copy = same_box_copy_gbs(torch, dev)
     bytes_step = w.bytes_per_call * calls
     value = world * args.steps * bytes_step / (total_ms / 1e3) / 1e9
     kernel_ms = statistics.fmean(per_launch) / calls   # per call (one launch per call)
@@ -460,7 +480,9 @@ def run_ours(args, w):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic_per_launch(w),
                          "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
-                         "kernel_ms": kernel_ms},
+                         "kernel_ms": kernel_ms,
+                         "same_box_copy_gbs": box_copy,
+                         "frac_of_same_box_copy": achieved / box_copy if box_copy else None},
             "clocks": clk,
             "gpu_launches": args.steps * launches_per_step,
             "kernel": {"variant": {1: "vec16", 2: "pair"}.get(launch["kernel"], "?"),

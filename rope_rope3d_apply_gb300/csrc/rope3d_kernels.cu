@@ -44,8 +44,21 @@
 namespace rope3d {
 namespace {
 
-constexpr int kBlock = 512;
-constexpr int kUnroll = 2;
+// Threads per CTA and vectors of Q (and of K) in flight per thread in the
+// contiguous vector kernel (compile-time, overridable for tuning sweeps).
+#ifndef ROPE3D_BLOCK
+#define ROPE3D_BLOCK 512
+#endif
+#ifndef ROPE3D_UNROLL
+#define ROPE3D_UNROLL 2
+#endif
+constexpr int kBlock = ROPE3D_BLOCK;
+constexpr int kUnroll = ROPE3D_UNROLL;
+#ifdef ROPE3D_MIN_CTAS
+#define ROPE3D_VEC_BOUNDS __launch_bounds__(kBlock, ROPE3D_MIN_CTAS)
+#else
+#define ROPE3D_VEC_BOUNDS __launch_bounds__(kBlock)
+#endif
 
 // Strided vector kernel: vectors per tensor in flight per thread, and the
 // resident CTAs per SM its register budget is sized for.
@@ -276,7 +289,7 @@ __device__ __forceinline__ float2 tab1(const float2 *tab, uint32_t idx) {
 // the first table entry of a vector is a multiple of 4 (16-bit) or 2 (fp32)).
 
 template <int kType, bool kSmem>
-__global__ void __launch_bounds__(kBlock)
+__global__ void ROPE3D_VEC_BOUNDS
 rope3d_vec16_kernel(const KParams p, const KStrides) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const float2 *tab = stage_tables<kSmem>(p, reinterpret_cast<float2 *>(smem_raw));
