@@ -381,3 +381,13 @@ def test_planted_fma_contraction_is_caught(tmp_path):
     lib = _build_mutant(tmp_path, "fma", "float y0", "float y0", extra=extra)
     with pytest.raises(AssertionError):
         pin_rotate_pair_rounding(lib)
+
+
+def test_tables_match_the_committed_digest():
+    """The oracle's tables (from the host C library's pow, cos and sin) equal
+    the digest tests/golden/make_golden.py wrote; it was checked on both
+    x86-64 and aarch64 hosts."""
+    from tests.golden import make_golden
+
+    want = open(os.path.join(os.path.dirname(__file__), "golden", "oracle_tables_sha256.txt")).read().strip()
+    assert make_golden.tables_digest() == want
