@@ -289,3 +289,61 @@ def rope_neox(x: np.ndarray, tokens: int, heads: int, head_dim: int, positions: 
     if rc != 0:
         raise ValueError("oracle_rope_neox rejected its arguments")
     return y
+
+
+# ---------------------------------------------------------------------------
+# 3D neighbourhood attention with the decoder's RoPE on Q and K (sglang
+# PR #34471 review, "关键源码片段": the decoder attends with NATTEN's na3d; the
+# PR #35698 review, "功能与动机": 3D RoPE precedes each of its attention
+# blocks). Neighbourhood attention as published (Hassani et al.,
+# "Neighborhood Attention Transformer", CVPR 2023): a query attends to the
+# k_t x k_h x k_w grid window centred on it, shifted to stay inside the grid
+# at the borders (window start min(max(i - k//2, 0), L - k) per axis).
+# Scores q.k / sqrt(head_dim), softmax over the window, weights times V.
+# Evaluated in float64 on the bf16 inputs (after the exact RoPE of rope3d).
+# ---------------------------------------------------------------------------
+
+def na_window_starts(length: int, k: int) -> np.ndarray:
+    i = np.arange(length)
+    return np.minimum(np.maximum(i - k // 2, 0), length - k)
+
+
+def na3d(q: np.ndarray, k: np.ndarray, v: np.ndarray, shape, kernel) -> np.ndarray:
+    """q, k, v: float64 [B, T, H, W, heads, d]; kernel (kt, kh, kw) odd and no
+    larger than the grid. Returns float64 [B, T, H, W, heads, d]."""
+    B, T, H, W, heads, d = shape
+    kt, kh, kw = kernel
+    if min(kt, kh, kw) < 1 or kt > T or kh > H or kw > W or not (kt % 2 and kh % 2 and kw % 2):
+        raise ValueError("kernel sizes must be odd and fit the grid")
+    q = q.reshape(shape)
+    k = k.reshape(shape)
+    v = v.reshape(shape)
+    st, sh, sw = na_window_starts(T, kt), na_window_starts(H, kh), na_window_starts(W, kw)
+    # key coordinates of every (query, window slot): [T, H, W, kt*kh*kw] each
+    dt, dh, dw = np.meshgrid(np.arange(kt), np.arange(kh), np.arange(kw), indexing="ij")
+    kt_idx = st[:, None, None, None] + dt.reshape(1, 1, 1, -1)
+    kh_idx = sh[None, :, None, None] + dh.reshape(1, 1, 1, -1)
+    kw_idx = sw[None, None, :, None] + dw.reshape(1, 1, 1, -1)
+    kt_idx, kh_idx, kw_idx = np.broadcast_arrays(kt_idx, kh_idx, kw_idx)
+    out = np.empty(shape, np.float64)
+    scale = 1.0 / np.sqrt(d)
+    for b in range(B):
+        kk = k[b][kt_idx, kh_idx, kw_idx]          # [T, H, W, n, heads, d]
+        vv = v[b][kt_idx, kh_idx, kw_idx]
+        s = np.einsum("thwed,thwned->thwen", q[b], kk) * scale   # [T, H, W, heads, n]
+        s = s - s.max(axis=-1, keepdims=True)
+        p = np.exp(s)
+        p /= p.sum(axis=-1, keepdims=True)
+        out[b] = np.einsum("thwen,thwned->thwed", p, vv)
+    return out
+
+
+def rope_na3d(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, shape, split, tabs,
+              kernel, rope: bool = True, lib=None) -> np.ndarray:
+    """bf16 inputs (uint16 bits): RoPE on Q and K exactly as rope3d (bf16
+    outputs), then na3d in float64. Returns float64."""
+    if rope:
+        q_bits = rope3d(q_bits, shape, split, tabs, lib)
+        k_bits = rope3d(k_bits, shape, split, tabs, lib)
+    to64 = lambda b: (np.ascontiguousarray(b).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)  # noqa: E731
+    return na3d(to64(q_bits), to64(k_bits), to64(v_bits), shape, kernel)
