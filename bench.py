@@ -62,7 +62,7 @@ def parse_args():
     p.add_argument("--variant", default="contiguous", choices=["contiguous", "f16", "qkv_inplace"],
                    help="contiguous Q/K (default); the same in fp16; or Q and K as views of a "
                         "fused [B, N, 3, heads, head_dim] QKV buffer rotated in place")
-    p.add_argument("--op", default="rope", choices=["rope", "patchify", "neox"],
+    p.add_argument("--op", default="rope", choices=["rope", "patchify", "neox", "na3d"],
                    help="rope: the fused 3D RoPE (default); patchify: the decoder's "
                         "space-to-depth layout kernel and its inverse")
     p.add_argument("--graph", action="store_true",
@@ -638,8 +638,94 @@ def run_neox(args):
     return 0
 
 
+# The fused attention workload: the stage-5 tile geometry (1 x 16 x 64 x 64
+# tokens, 16 heads x 128, bf16) with a 3 x 7 x 7 neighbourhood (the pages give
+# no window size).
+NA3D = dict(B=1, T=16, H=64, W=64, heads=16, split=(32, 48, 48), kernel=(3, 7, 7))
+
+
+def run_na3d(args):
+    """rope3d_na3d with the RoPE fused (the step) against the unfused pair:
+    rope3d_apply_pair followed by rope3d_na3d on the rotated Q and K."""
+    import torch
+
+    import rope_rope3d_apply_gb300 as r
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    r.load_library()
+    c = NA3D
+    N = c["T"] * c["H"] * c["W"]
+    shp = (c["B"], N, c["heads"], 128)
+    n = int(np.prod(shp))
+    q, k, v = (torch.from_numpy(synthetic.normal(n, 1.0, 12, i, "bf16").view(np.int16))
+               .view(torch.bfloat16).reshape(shp).to(dev) for i in range(3))
+    tabs = r.rope3d_build_tables(c["T"], c["H"], c["W"], c["split"])
+    out = torch.empty_like(q)
+    qr, kr = torch.empty_like(q), torch.empty_like(k)
+    stream = torch.cuda.current_stream(dev)
+
+    def fused():
+        r.rope3d_na3d(q, k, v, tabs, c["kernel"], out, stream=stream)
+
+    def unfused():
+        r.rope3d_apply_pair(q, k, tabs, qr, kr, stream=stream)
+        r.rope3d_na3d(qr, kr, v, tabs, c["kernel"], out, apply_rope=False, stream=stream)
+
+    def timed(fn, steps):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / steps
+
+    clocks = ClockSampler(smi_gpu_id(dev.index))
+    clocks.start()
+    time.sleep(0.3)
+    t0 = time.time()
+    ms_fused = timed(fused, args.steps)
+    t1 = time.time()
+    ms_unfused = timed(unfused, args.steps)
+    time.sleep(0.25)
+    clocks.stop()
+    kt, kh, kw = c["kernel"]
+    window = kt * kh * kw
+    flops = 4.0 * 128 * window * N * c["heads"] * c["B"]           # q.k and p.v over each window
+    tflops = flops / (ms_fused / 1e3) / 1e12
+    peak = 1898.6
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+        kind = "measured"
+    except (OSError, KeyError, ValueError):
+        kind = "fallback"
+    line = {
+        "op": "na3d", "metric": "fused RoPE + 3D neighbourhood attention, useful TFLOP/s",
+        "value": tflops, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_fused, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "na3d: B=%d, T=%d, H=%d, W=%d, heads=%d x 128, window %dx%dx%d" % (
+            c["B"], c["T"], c["H"], c["W"], c["heads"], kt, kh, kw), "useful_flops": flops},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tflops / peak, "traffic": None,
+                     "peak_source": f"{kind} bf16_tflops (cuBLAS burst)", "kernel_ms": ms_fused},
+        "unfused_ms": ms_unfused, "fusion_saving_ms": ms_unfused - ms_fused,
+        "clocks": clocks.summary(t0, t1), "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.op == "na3d":
+        return run_na3d(args)
     if args.op == "patchify":
         return run_patchify(args)
     if args.op == "neox":

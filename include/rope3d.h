@@ -280,6 +280,34 @@ int rope3d_neox_cache_host(int64_t max_position, int64_t rotary_dim, double base
 int rope3d_neox_last_kernel(void);
 
 /*
+ * rope3d_na3d -- 3D neighbourhood attention with the RoPE fused into its
+ * prologue. The decoder rotates Q and K before each attention block ("功能与动机")
+ * and attends with NATTEN's 3D neighbourhood attention (sglang PR #34471
+ * review, "关键源码片段", _na3d); rotating the Q and K tiles inside the
+ * attention kernel removes the write and re-read of Q_out and K_out.
+ * The rotation is rope3d_apply_pair's, bit for bit (bf16 operands); the
+ * attention is the published neighbourhood attention: a query attends to the
+ * k_t x k_h x k_w window centred on it, shifted inside the grid at borders,
+ * with softmax(q.k / sqrt(head_dim)); bf16 tensor-core products, fp32
+ * accumulation and softmax, bf16 output.
+ *
+ *   q, k, v, out  device, bf16, [B, T, H, W, heads, 128] contiguous, 16-byte
+ *                 aligned; out overlaps no input
+ *   tables, split as rope3d_apply_pair (used when apply_rope != 0; every
+ *                 chunk a multiple of 8; tables <= 48 KB)
+ *   kernel_size   (k_t, k_h, k_w), odd, each no larger than its grid extent
+ *   apply_rope    1: rotate Q and K first (fused); 0: Q and K are used as
+ *                 given (the unfused path's second kernel)
+ *   stream        cudaStream_t; asynchronous
+ * Limits: head_dim 128; T, H, W < 1024. The bit-exact gate does not run here.
+ * Errors: NULL, SHAPE, ALIGN (16 bytes), ALIAS, TABLES, DEVICE, CUDA.
+ */
+int rope3d_na3d(const void *q, const void *k, const void *v, void *out,
+                const rope3d_tables *tables, int64_t B, int64_t T, int64_t H, int64_t W,
+                int64_t heads, int64_t head_dim, const int32_t split[3],
+                const int32_t kernel_size[3], int32_t apply_rope, void *stream);
+
+/*
  * rope3d_apply_pair_host -- the same rotation for HOST buffers: the library
  * streams Q and K to the GPU in token chunks, rotates each chunk with the same
  * kernel, and streams Q_out and K_out back, overlapping the two copy

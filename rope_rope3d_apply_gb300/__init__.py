@@ -30,6 +30,7 @@ __all__ = [
     "rope3d_apply_pair_strided", "rope3d_preflight_strided", "view_strides",
     "rope3d_patchify", "rope3d_unpatchify", "rope3d_patchify_check", "rope3d_patchify_last_kernel",
     "rope3d_apply_neox", "rope3d_neox_check", "rope3d_neox_cache_host", "rope3d_neox_last_kernel",
+    "rope3d_na3d",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -93,6 +94,7 @@ def _declare(lib):
         "rope3d_neox_check": ([vp] * 6 + [i64] * 5 + [i32, vp], c.c_int),
         "rope3d_neox_cache_host": ([i64, i64, dbl, vp], c.c_int),
         "rope3d_neox_last_kernel": ([], c.c_int),
+        "rope3d_na3d": ([vp] * 5 + [i64] * 6 + [vp, vp, i32, vp], c.c_int),
         "rope3d_preflight_strided": ([vp, vp, vp, vp, vp] + [i64] * 6 + [vp, i32] + [vp] * 4 + [i32],
                                      c.c_int),
     }
@@ -476,6 +478,31 @@ def rope3d_neox_check(ptrs, max_position, tokens, q_heads, k_heads, head_dim, dt
 
 def rope3d_neox_last_kernel() -> int:
     return int(load_library().rope3d_neox_last_kernel())
+
+
+def rope3d_na3d(q, k, v, tables: Tables, kernel_size, out=None, apply_rope: bool = True,
+                stream=None):
+    """3D neighbourhood attention over [B, T*H*W, heads, 128] (or 6-D) bf16
+    device tensors, with Q and K rotated inside the kernel when apply_rope."""
+    if out is None:
+        import torch
+
+        out = torch.empty_like(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if not _contiguous(t):
+            raise ValueError(f"{name} must be contiguous")
+        if tuple(t.shape) != tuple(q.shape):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, q has {tuple(q.shape)}")
+        if _dtype_code(t) != BF16:
+            raise TypeError("rope3d_na3d takes bf16 tensors")
+    B, heads, head_dim = _geometry(q, tables)
+    ks = (ctypes.c_int32 * 3)(*[int(x) for x in kernel_size])
+    rc = load_library().rope3d_na3d(_ptr(q), _ptr(k), _ptr(v), _ptr(out), tables.handle, B,
+                                    tables.T, tables.H, tables.W, heads, head_dim,
+                                    _split(tables.split), ks, 1 if apply_rope else 0,
+                                    _stream(stream, q))
+    _check(rc, "rope3d_na3d")
+    return out
 
 
 def rope3d_preflight(q, k, q_out, k_out, tables, B, T, H, W, heads, head_dim, split, dtype,

@@ -23,6 +23,7 @@ SOURCES = [
     os.path.join(CSRC, "rope3d_noalloc.cu"),
     os.path.join(CSRC, "rope3d_patchify.cu"),
     os.path.join(CSRC, "rope3d_neox.cu"),
+    os.path.join(CSRC, "rope3d_na3d.cu"),
     os.path.join(CSRC, "rope3d_api.cpp"),
     os.path.join(CSRC, "rope3d_internal.h"),
     os.path.join(INCLUDE, "rope3d.h"),
@@ -67,14 +68,20 @@ def commands(out_dir: str = BUILD, extra_nvcc: list[str] | None = None):
         "-Xcompiler", "-fPIC,-ffp-contract=off", "-Xptxas", "-v",
         "-c", os.path.join(CSRC, "rope3d_neox.cu"), "-o", neox_o,
     ]
+    na_o = os.path.join(out_dir, "rope3d_na3d.o")
+    nvcc_na = [
+        _nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-fmad=false",
+        "-Xcompiler", "-fPIC,-ffp-contract=off", "-Xptxas", "-v",
+        "-c", os.path.join(CSRC, "rope3d_na3d.cu"), "-o", na_o,
+    ]
     gxx_compile = [
         "g++", "-std=c++17", "-O2", "-fPIC", "-ffp-contract=off", "-fno-fast-math",
         "-pthread", "-Wall", "-Wno-unused-function", f"-I{cuda}/include",
         "-c", os.path.join(CSRC, "rope3d_api.cpp"), "-o", api_o,
     ]
-    link = [_nvcc(), *ARCH, "-shared", kern_o, api_o, noalloc_o, patch_o, neox_o,
+    link = [_nvcc(), *ARCH, "-shared", kern_o, api_o, noalloc_o, patch_o, neox_o, na_o,
             "-o", os.path.join(out_dir, "librope3d.so"), "-Xcompiler", "-pthread"]
-    return [nvcc_compile, gxx_compile, nvcc_noalloc, nvcc_patch, nvcc_neox], link
+    return [nvcc_compile, gxx_compile, nvcc_noalloc, nvcc_patch, nvcc_neox, nvcc_na], link
 
 
 def up_to_date(lib: str = LIB) -> bool:

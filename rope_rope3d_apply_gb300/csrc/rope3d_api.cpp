@@ -262,6 +262,21 @@ extern "C" int rope3d_tables_read(const rope3d_tables *t, int32_t axis, int32_t 
     return ROPE3D_OK;
 }
 
+// The device layout of a handle, for kernels outside this file.
+int rope3d::tables_layout(const rope3d_tables *t, const float2 **dev, uint32_t *len,
+                          uint32_t offsets[3], int64_t dims[3], int32_t split[3], int *device,
+                          bool *host_backed) {
+    if (!t) return ROPE3D_ERR_NULL;
+    *dev = t->dev;
+    *len = t->len;
+    std::copy(t->offset, t->offset + 3, offsets);
+    std::copy(t->dims, t->dims + 3, dims);
+    std::copy(t->split, t->split + 3, split);
+    *device = t->device;
+    *host_backed = t->host_backed;
+    return ROPE3D_OK;
+}
+
 extern "C" int rope3d_cache_stats(int64_t *entries, int64_t *hits, int64_t *misses,
                                   int64_t *evictions) {
     std::lock_guard<std::mutex> lock(g_mutex);

@@ -99,3 +99,12 @@ int check_call_without_tables(const void *q, const void *k, const void *q_out, c
                               int64_t head_dim, const int32_t split[3], int32_t dtype);
 
 }  // namespace rope3d
+
+struct rope3d_tables;
+namespace rope3d {
+// The device layout of a table handle: the float2 (cos, sin) buffer, its
+// length in entries, the entry offsets of the T, H and W tables, the key, the
+// device it lives on, and whether it is the host-memory test mode.
+int tables_layout(const rope3d_tables *t, const float2 **dev, uint32_t *len, uint32_t offsets[3],
+                  int64_t dims[3], int32_t split[3], int *device, bool *host_backed);
+}  // namespace rope3d

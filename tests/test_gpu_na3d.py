@@ -1,0 +1,115 @@
+"""GPU checks of rope3d_na3d (3D neighbourhood attention with the RoPE fused
+into its prologue) against the float64 oracle, and of the fusion itself: the
+fused kernel must give the same bits as the same kernel fed with Q and K
+rotated by rope3d_apply_pair.
+
+Tolerance (derived from the arithmetic): the rotated operands are exact
+bf16; scores accumulate in fp32; the probabilities are rounded to bf16
+(relative 2^-9) before the tensor-core P.V product while the normaliser
+uses the unrounded ones, and the output is rounded to bf16 (2^-9 of |O|):
+|O - O_ref| <= 2^-7 * sum_k p_k |v_k| + 2^-8 |O_ref| + 1e-6, twice the
+first-order bound."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU hosts
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import rope_rope3d_apply_gb300 as r  # noqa: E402
+
+DEV = torch.device("cuda:0")
+
+
+def bf16(a):
+    return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16)
+
+
+def to_f64(t):
+    return (t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16).astype(np.uint32)
+            << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+CASES = [
+    # (B, T, H, W, heads), split, kernel
+    ((1, 3, 12, 12, 2), (32, 48, 48), (3, 5, 5)),
+    ((2, 2, 9, 17, 1), (32, 48, 48), (1, 3, 7)),      # partial query blocks at both edges
+    ((1, 5, 8, 8, 2), (48, 40, 40), (5, 7, 7)),        # windows covering the grid
+    ((1, 4, 16, 24, 1), (32, 48, 48), (3, 7, 7)),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-{c[2]}" for c in CASES])
+def test_na3d_matches_oracle(case):
+    (B, T, H, W, heads), split, kernel = case
+    shape6 = (B, T, H, W, heads, 128)
+    n = int(np.prod(shape6))
+    q_np = synthetic.normal(n, 1.0, 300, 0, "bf16")
+    k_np = synthetic.normal(n, 1.0, 300, 1, "bf16")
+    v_np = synthetic.normal(n, 1.0, 300, 2, "bf16")
+    shp = (B, T * H * W, heads, 128)
+    q, k, v = (bf16(a).reshape(shp).to(DEV) for a in (q_np, k_np, v_np))
+    tabs = r.rope3d_build_tables(T, H, W, split)
+    out = r.rope3d_na3d(q, k, v, tabs, kernel)
+    torch.cuda.synchronize()
+    got = to_f64(out).reshape(shape6)
+    otabs = oracle.tables(T, H, W, split)
+    ref = oracle.rope_na3d(q_np, k_np, v_np, shape6, split, otabs, kernel)
+    qr = oracle.rope3d(q_np, shape6, split, otabs)
+    kr = oracle.rope3d(k_np, shape6, split, otabs)
+    vf = (v_np.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    to64 = lambda b: (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)  # noqa: E731
+    absv = oracle.na3d(to64(qr), to64(kr), np.abs(vf), shape6, kernel)
+    bound = 2.0 ** -7 * absv + 2.0 ** -8 * np.abs(ref) + 1e-6
+    err = np.abs(got - ref)
+    assert np.all(err <= bound), (err.max(), (err / bound).max())
+    tabs.close()
+
+
+def test_fused_equals_unfused_bitwise():
+    """The fused prologue rotates exactly as rope3d_apply_pair does."""
+    B, T, H, W, heads, split, kernel = 1, 3, 10, 13, 2, (32, 48, 48), (3, 5, 5)
+    shp = (B, T * H * W, heads, 128)
+    n = int(np.prod(shp))
+    q, k, v = (bf16(synthetic.normal(n, 1.0, 301, i, "bf16")).reshape(shp).to(DEV) for i in range(3))
+    tabs = r.rope3d_build_tables(T, H, W, split)
+    fused = r.rope3d_na3d(q, k, v, tabs, kernel, apply_rope=True)
+    qr, kr = r.rope3d_apply_pair(q, k, tabs)
+    unfused = r.rope3d_na3d(qr, kr, v, tabs, kernel, apply_rope=False)
+    torch.cuda.synchronize()
+    assert torch.equal(fused.view(torch.int16), unfused.view(torch.int16))
+    tabs.close()
+
+
+def test_single_key_window_returns_v():
+    B, T, H, W, heads = 1, 2, 9, 10, 3
+    shp = (B, T * H * W, heads, 128)
+    n = int(np.prod(shp))
+    q, k, v = (bf16(synthetic.normal(n, 1.0, 302, i, "bf16")).reshape(shp).to(DEV) for i in range(3))
+    tabs = r.rope3d_build_tables(T, H, W, (32, 48, 48))
+    out = r.rope3d_na3d(q, k, v, tabs, (1, 1, 1))
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), v.view(torch.int16))
+    tabs.close()
+
+
+def test_na3d_rejections():
+    B, T, H, W, heads = 1, 3, 8, 8, 1
+    tabs = r.rope3d_build_tables(T, H, W, (32, 48, 48))
+    shp = (B, T * H * W, heads, 128)
+    q = torch.zeros(shp, dtype=torch.bfloat16, device=DEV)
+    for kernel, name in [((2, 3, 3), "ERR_SHAPE"), ((5, 3, 3), "ERR_SHAPE"), ((1, 9, 3), "ERR_SHAPE")]:
+        with pytest.raises(r.Rope3dError) as e:
+            r.rope3d_na3d(q, q, q, tabs, kernel)
+        assert e.value.name == name
+    with pytest.raises(r.Rope3dError) as e:
+        r.rope3d_na3d(q, q, q, tabs, (3, 3, 3), out=q)
+    assert e.value.name == "ERR_ALIAS"
+    tabs.close()
