@@ -16,11 +16,16 @@
 // min(max(i - k/2, 0), L - k) per axis), with softmax(q.k / sqrt(d)) weights.
 //
 // Work decomposition: a CTA of 4 warps owns one (batch, head) and a block of
-// 1 x 8 x 8 query tokens; its key region is the union of their windows, visited
-// in chunks of 64 keys. Each warp holds 16 query rows; S = Q K^T and O += P V
-// run on the tensor cores as bf16 m16n8k16 MMAs with fp32 accumulators, with a
+// 1 x 8 x 8 query tokens; each warp holds 2 x 8 of them (16 MMA rows), so the
+// union of its windows spans whole rows of the block's key region. The region
+// (the union of the block's windows) is visited in chunks of whole region rows
+// (at most 64 keys); inside a chunk a warp's keys are one contiguous range,
+// and the warp runs its MMAs on that range only. S = Q K^T and O += P V run on
+// the tensor cores as bf16 m16n8k16 MMAs with fp32 accumulators, with a
 // flash-style online softmax in registers (running max and sum per row) and a
-// per-element window mask. Tables (when rotating) sit in shared memory.
+// per-element window mask. Chunks are double-buffered: the next chunk's K is
+// loaded into registers and its V copied asynchronously while the current one
+// is computed; K is rotated on its way from registers to shared memory.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -36,11 +41,16 @@ namespace {
 constexpr int kHD = 128;             // head_dim
 constexpr int kQB = 64;              // queries per CTA (1 x 8 x 8)
 constexpr int kQBH = 8, kQBW = 8;
-constexpr int kKC = 64;              // keys per chunk
-constexpr int kWarps = 4;
+constexpr int kKC = 64;              // at most this many keys per chunk
+constexpr int kWarps = 4;            // warp i: block rows 2i and 2i + 1
 constexpr int kThreads = kWarps * 32;
 constexpr int kRow = kHD + 8;        // padded smem row (bf16): 272 bytes
+constexpr int kVecs = kKC * (kHD / 8) / kThreads;   // 16-byte vectors per thread per chunk
 constexpr uint32_t kMaxTableBytes = 48 * 1024;
+constexpr size_t kFixedSmem = size_t(4) * kKC * kRow * 2;   // K and V, two buffers each
+static_assert(kQB == kQBH * kQBW && kQB == kWarps * 16 && kQBW == 8,
+              "a warp holds two 8-wide rows of the query block");
+static_assert(kVecs * kThreads == kQB * (kHD / 8), "the Q tile and a K chunk move alike");
 
 struct NAParams {
     const uint16_t *q, *k, *v;
@@ -72,17 +82,27 @@ __device__ __forceinline__ uint32_t rot_word(uint32_t word, float c, float s) {
     return out;
 }
 
-// Rotate the 8 channels [ch, ch + 8) of a token at grid position (t, h, w).
-// Every chunk of the split is a multiple of 8 channels, so the 4 pairs lie in
-// one axis and read 4 consecutive (cos, sin) entries: two 16-byte loads (the
-// entry index is a multiple of 4, so they are aligned).
-__device__ __forceinline__ uint4 rot_vec(uint4 v, const float2 *tab, const NAParams &p, int t,
-                                         int h, int w, int ch) {
-    const uint32_t pair = ch / 2;
-    uint32_t idx;
-    if (pair < p.pT) idx = t * p.pT + pair;
-    else if (pair < p.pT + p.pH) idx = p.offH + h * p.pH + (pair - p.pT);
-    else idx = p.offW + w * p.pW + (pair - p.pT - p.pH);
+// Where a thread's 8 channels [8 cv, 8 cv + 8) read the tables. Every chunk of
+// the split is a multiple of 8 channels, so the 4 pairs lie in one axis and
+// the entries of position pos are 4 consecutive (cos, sin) at base + pos *
+// stride: a multiple of 4, so two aligned 16-byte loads.
+struct TabSlot {
+    uint32_t base, stride;
+    int axis;   // 0: t, 1: h, 2: w
+};
+
+__device__ __forceinline__ TabSlot tab_slot(const NAParams &p, int cv) {
+    const uint32_t pair = 4 * cv;
+    if (pair < p.pT) return {pair, p.pT, 0};
+    if (pair < p.pT + p.pH) return {p.offH + (pair - p.pT), p.pH, 1};
+    return {p.offW + (pair - p.pT - p.pH), p.pW, 2};
+}
+
+// Rotate the 8 channels of a TabSlot for a token at grid position (t, h, w).
+__device__ __forceinline__ uint4 rot_vec(uint4 v, const float2 *tab, const TabSlot &ts, int t,
+                                         int h, int w) {
+    const int pos = ts.axis == 0 ? t : (ts.axis == 1 ? h : w);
+    const uint32_t idx = ts.base + uint32_t(pos) * ts.stride;
     const float4 a = *reinterpret_cast<const float4 *>(tab + idx);
     const float4 b = *reinterpret_cast<const float4 *>(tab + idx + 2);
     return make_uint4(rot_word(v.x, a.x, a.y), rot_word(v.y, a.z, a.w), rot_word(v.z, b.x, b.y),
@@ -99,8 +119,12 @@ __device__ __forceinline__ void cp_async16(void *dst_smem, const void *src) {
                  : "memory");
 }
 
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
 __device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
@@ -133,14 +157,29 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return u;
 }
 
-__global__ void __launch_bounds__(kThreads)
+// 2^x on the special-function unit (relative error about 2^-22; results below
+// the smallest normal flush to zero, far under the bf16 rounding of P).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// A chunk of the key region: frame t, region rows rb + i S (i < nr; ri = rb
+// minus the region's first row), columns [c0, c0 + cw), nseg 16-slot segments
+// per row; key (i, j) sits in slot i * 16 nseg + j.
+struct Chunk {
+    int t, rb, ri, nr, c0, cw, nseg;
+};
+
+template <bool kRope>
+__global__ void __launch_bounds__(kThreads, 2)
 rope3d_na3d_kernel(const NAParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
-    uint16_t *sQ = reinterpret_cast<uint16_t *>(smem);
-    uint16_t *sK = sQ + kQB * kRow;
-    uint16_t *sV = sK + kKC * kRow;
-    int *sKey = reinterpret_cast<int *>(sV + kKC * kRow);          // packed key coordinates
-    float2 *sTab = reinterpret_cast<float2 *>(sKey + kKC);
+    uint16_t *sK = reinterpret_cast<uint16_t *>(smem);        // [2][kKC][kRow]
+    uint16_t *sV = sK + 2 * kKC * kRow;                        // [2][kKC][kRow]
+    float2 *sTab = reinterpret_cast<float2 *>(sV + 2 * kKC * kRow);
+    uint16_t *sQ = sV + kKC * kRow;   // the Q tile borrows V's second buffer
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, tq = lane & 3;
@@ -154,69 +193,131 @@ rope3d_na3d_kernel(const NAParams p) {
     const int b = blk / p.heads;
     const int h0 = bh * kQBH, w0 = bw * kQBW;
 
-    if (p.rope) {
-        for (uint32_t i = tid; i < p.tab_len; i += kThreads) sTab[i] = p.tab[i];
-        __syncthreads();
-    }
-    const size_t tok_stride = size_t(p.heads) * kHD;            // elements per token
-    auto token_index = [&](int t, int h, int w) {
-        return ((size_t(b) * p.T + t) * p.H + h) * p.W + w;
-    };
+    // A thread moves channel block cv of tile slots slot0 + 8 m (16 threads
+    // per 256-byte row: coalesced).
+    const int cv = tid & 15, slot0 = tid >> 4;
+    const TabSlot ts = tab_slot(p, cv);
+    const long long tok = (long long)p.heads * kHD;             // elements per token
+    const long long grid_row = (long long)p.W * tok, frame = (long long)p.H * grid_row;
+    const long long batch0 = (long long)b * p.T * frame + (long long)head * kHD + cv * 8;
 
-    // ---- Q tile: 64 rows x 128 channels copied asynchronously, then rotated in
-    // shared memory
-    for (int i = tid; i < kQB * (kHD / 8); i += kThreads) {
-        const int row = i / (kHD / 8), cv = i % (kHD / 8);
-        const int h = h0 + row / kQBW, w = w0 + row % kQBW;
-        uint16_t *dst = sQ + row * kRow + cv * 8;
-        if (h < p.H && w < p.W)
-            cp_async16(dst, p.q + token_index(qt, h, w) * tok_stride + size_t(head) * kHD + cv * 8);
-        else
-            *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
-    }
-    cp_async_wait_all();
-    __syncthreads();
-    if (p.rope) {
-        for (int i = tid; i < kQB * (kHD / 8); i += kThreads) {
-            const int cv = i / kQB, row = i % kQB;   // one channel column per warp
-            const int h = h0 + row / kQBW, w = w0 + row % kQBW;
-            if (h < p.H && w < p.W) {
-                uint4 *ptr = reinterpret_cast<uint4 *>(sQ + row * kRow + cv * 8);
-                *ptr = rot_vec(*ptr, sTab, p, qt, h, w, cv * 8);
-            }
-        }
-    }
-
-    // key region: the union of the block's windows
-    const int rt0 = na_start(qt, p.T, p.kt), rt1 = rt0 + p.kt;
+    // Key region: the union of the block's windows. It is visited in chunks of
+    // at most kKC key slots; a region row takes 16 slots per 16 columns (the
+    // slots past its last column hold zeros), so one k16 MMA step covers 16
+    // columns of one row. Chunk ri of a frame holds the rows ri, ri + S,
+    // ri + 2 S, ...: a warp's windows span consecutive rows, which meet every
+    // chunk in about the same number of rows, so the warps share each chunk's
+    // work evenly. A row wider than kKC columns is cut into column groups.
+    const int rt0 = na_start(qt, p.T, p.kt);
     const int hl = min(h0 + kQBH, p.H) - 1, wl = min(w0 + kQBW, p.W) - 1;
     const int rh0 = na_start(h0, p.H, p.kh), rh1 = na_start(hl, p.H, p.kh) + p.kh;
     const int rw0 = na_start(w0, p.W, p.kw), rw1 = na_start(wl, p.W, p.kw) + p.kw;
     const int RH = rh1 - rh0, RW = rw1 - rw0;
-    const int R = (rt1 - rt0) * RH * RW;
+    const int CW = min(RW, kKC);                                // columns per chunk row
+    const int CH = min(RH, kKC / (16 * ((CW + 15) / 16)));       // rows per chunk (>= 1)
+    const int S = (RH + CH - 1) / CH, ncc = (RW + CW - 1) / CW;
+    const int n_chunks = p.kt * S * ncc;
+    const int qR = RH / S, mR = RH - qR * S;   // chunk ri holds qR + (ri < mR) rows
+    // chunks in order: column group fastest, then ri, then the frame
+    int it_ci = 0, it_ri = 0, it_dt = 0;
+    auto next_chunk = [&]() {
+        Chunk k;
+        k.t = rt0 + it_dt;
+        k.ri = it_ri;
+        k.rb = rh0 + it_ri;
+        k.nr = qR + (it_ri < mR ? 1 : 0);
+        k.c0 = rw0 + it_ci * CW;
+        k.cw = min(CW, rw1 - k.c0);
+        k.nseg = (k.cw + 15) >> 4;
+        if (++it_ci == ncc) {
+            it_ci = 0;
+            if (++it_ri == S) {
+                it_ri = 0;
+                ++it_dt;
+            }
+        }
+        return k;
+    };
 
-    // this thread's two query rows (g and g + 8 of its warp): window starts
-    int wh[2], ww[2];   // window starts of the two rows in h and w (t: the region's)
-    bool rvalid[2];
+    // K of a chunk goes through registers when it is rotated (on the way to
+    // shared memory), else it is copied asynchronously like V. Slots past a
+    // row's last column get zeros, so every slot a warp reads holds finite
+    // values.
+    uint4 kreg[kVecs];
+    int kpos[kVecs];   // packed (h, w) of a K vector to rotate; -1: zeros; -2: no slot
+    auto issue = [&](const Chunk &k, int buf) {
+        const int sw = 16 * k.nseg;
+        long long off = batch0 + k.t * frame + k.rb * grid_row + (long long)(k.c0 + slot0) * tok;
+        const long long wrap = S * grid_row - sw * tok;   // to the chunk's next row
+        int i = 0, j = slot0;                               // slot0 < 8 < sw
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int row = warp * 16 + g + 8 * r;
-        const int h = h0 + row / kQBW, w = w0 + row % kQBW;
-        rvalid[r] = h < p.H && w < p.W;
-        wh[r] = na_start(min(h, p.H - 1), p.H, p.kh);
-        ww[r] = na_start(min(w, p.W - 1), p.W, p.kw);
-    }
-    // the box of this warp's windows in (h, w): chunks with no key inside it
-    // are skipped by the whole warp
-    int box_h0 = min(wh[0], wh[1]), box_h1 = max(wh[0], wh[1]) + p.kh;
-    int box_w0 = min(ww[0], ww[1]), box_w1 = max(ww[0], ww[1]) + p.kw;
+        for (int m = 0; m < kVecs; ++m) {
+            const int slot = slot0 + 8 * m;
+            uint16_t *dk = sK + (buf * kKC + slot) * kRow + cv * 8;
+            uint16_t *dv = sV + (buf * kKC + slot) * kRow + cv * 8;
+            if (kRope) kpos[m] = -2;
+            if (i < k.nr) {
+                if (j < k.cw) {
+                    if (kRope) {
+                        kreg[m] = __ldg(reinterpret_cast<const uint4 *>(p.k + off));
+                        kpos[m] = ((k.rb + i * S) << 10) | (k.c0 + j);
+                    } else {
+                        cp_async16(dk, p.k + off);
+                    }
+                    cp_async16(dv, p.v + off);
+                } else {
+                    if (kRope) kpos[m] = -1;
+                    else *reinterpret_cast<uint4 *>(dk) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(dv) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            j += 8;
+            off += 8 * tok;
+            if (j >= sw) {
+                j -= sw;
+                ++i;
+                off += wrap;
+            }
+        }
+    };
+    auto store_k = [&](int t, int buf) {   // rotating path only
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        box_h0 = min(box_h0, __shfl_xor_sync(0xffffffffu, box_h0, off));
-        box_h1 = max(box_h1, __shfl_xor_sync(0xffffffffu, box_h1, off));
-        box_w0 = min(box_w0, __shfl_xor_sync(0xffffffffu, box_w0, off));
-        box_w1 = max(box_w1, __shfl_xor_sync(0xffffffffu, box_w1, off));
+        for (int m = 0; m < kVecs; ++m) {
+            const int pos = kpos[m];
+            if (pos != -2) {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (pos >= 0) v = rot_vec(kreg[m], sTab, ts, t, pos >> 10, pos & 1023);
+                *reinterpret_cast<uint4 *>(sK + (buf * kKC + slot0 + 8 * m) * kRow + cv * 8) = v;
+            }
+        }
+    };
+
+    // ---- prologue: tables, the Q tile, the first chunk
+    if (kRope)
+        for (uint32_t i = tid; i < p.tab_len; i += kThreads) sTab[i] = p.tab[i];
+    uint4 qreg[kVecs];
+#pragma unroll
+    for (int m = 0; m < kVecs; ++m) {
+        const int r = slot0 + 8 * m;   // block row r: (h0 + r / 8, w0 + r % 8)
+        const int h = h0 + r / kQBW, w = w0 + r % kQBW;
+        qreg[m] = make_uint4(0, 0, 0, 0);
+        if (h < p.H && w < p.W)
+            qreg[m] = __ldg(reinterpret_cast<const uint4 *>(
+                p.q + batch0 + qt * frame + h * grid_row + (long long)w * tok));
     }
+    Chunk cur = next_chunk();
+    issue(cur, 0);
+    cp_async_commit();
+    if (kRope) __syncthreads();   // tables staged
+#pragma unroll
+    for (int m = 0; m < kVecs; ++m) {
+        const int r = slot0 + 8 * m;
+        const int h = h0 + r / kQBW, w = w0 + r % kQBW;
+        uint4 v = qreg[m];
+        if (kRope && h < p.H && w < p.W) v = rot_vec(v, sTab, ts, qt, h, w);
+        *reinterpret_cast<uint4 *>(sQ + r * kRow + cv * 8) = v;
+    }
+    if (kRope) store_k(cur.t, 0);
     __syncthreads();
 
     // Q fragments of this warp's 16 rows, all 8 k-steps
@@ -227,159 +328,169 @@ rope3d_na3d_kernel(const NAParams p) {
         ldsm_x4(smem_addr(a), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
     }
 
+    // this thread's two query rows: block rows 2 warp (MMA row g) and
+    // 2 warp + 1 (MMA row g + 8), both in column w0 + g
+    const int hq = h0 + 2 * warp, wq = w0 + g;
+    const int ww = na_start(min(wq, p.W - 1), p.W, p.kw);
+    const int wh0 = na_start(min(hq, p.H - 1), p.H, p.kh);
+    const int wh1 = na_start(min(hq + 1, p.H - 1), p.H, p.kh);
+    const bool cvalid = wq < p.W;
+    const bool rvalid0 = hq < p.H && cvalid, rvalid1 = hq + 1 < p.H && cvalid;
+    // The warp's windows span region rows [box_h0, box_h1) and every column;
+    // chunk ri meets them in its rows [qb + (ri < mb), qu + (ri < mu)).
+    const int bl = wh0 - rh0, bu = (hq < p.H ? wh1 + p.kh : wh0) - rh0;
+    const int qb = bl / S, mb = bl - qb * S, qu = bu / S, mu = bu - qu * S;
+    // column tests of this lane's keys: bit 4 seg + 2 half + kq for column
+    // 16 seg + 8 half + 2 tq + kq of a chunk row; recomputed per column group
+    uint32_t colbits = 0;
+    int colbits_c0 = -1;
+
     float o[kHD / 8][4];
 #pragma unroll
     for (int n = 0; n < kHD / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const int mi = lane >> 3, rr = lane & 7;
 
-    for (int c0 = 0; c0 < R; c0 += kKC) {
-        __syncthreads();   // the previous chunk's K and V are no longer read
-        // ---- K and V chunk copied asynchronously, key coordinates; then K is
-        // rotated in shared memory
-        for (int i = tid; i < kKC * (kHD / 8); i += kThreads) {
-            const int row = i / (kHD / 8), cv = i % (kHD / 8);
-            const int r = c0 + row;
-            uint16_t *dk = sK + row * kRow + cv * 8;
-            uint16_t *dv = sV + row * kRow + cv * 8;
-            if (r < R) {
-                const int dt = r / (RH * RW), rem = r - dt * RH * RW;
-                const int dh = rem / RW, dw = rem - dh * RW;
-                const int t = rt0 + dt, h = rh0 + dh, w = rw0 + dw;
-                const size_t off = token_index(t, h, w) * tok_stride + size_t(head) * kHD + cv * 8;
-                cp_async16(dk, p.k + off);
-                cp_async16(dv, p.v + off);
-                if (cv == 0) sKey[row] = (t << 20) | (h << 10) | w;
-            } else {
-                *reinterpret_cast<uint4 *>(dk) = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4 *>(dv) = make_uint4(0, 0, 0, 0);
-                if (cv == 0) sKey[row] = -1;
-            }
+    for (int c = 0; c < n_chunks; ++c) {
+        const int buf = c & 1;
+        cp_async_wait_all();   // this thread's copies of chunk c
+        __syncthreads();       // everyone's, K stored, chunk c - 1 no longer read
+        Chunk nxt{};
+        if (c + 1 < n_chunks) {
+            nxt = next_chunk();
+            issue(nxt, buf ^ 1);
         }
-        cp_async_wait_all();
-        __syncthreads();
-        if (p.rope) {
-            for (int i = tid; i < kKC * (kHD / 8); i += kThreads) {
-                const int cv = i / kKC, row = i % kKC;   // one channel column per warp
-                const int key = sKey[row];
-                if (key >= 0) {
-                    uint4 *ptr = reinterpret_cast<uint4 *>(sK + row * kRow + cv * 8);
-                    *ptr = rot_vec(*ptr, sTab, p, key >> 20, (key >> 10) & 1023, key & 1023, cv * 8);
+        cp_async_commit();
+
+        const int ilo = qb + (cur.ri < mb ? 1 : 0), ihi = qu + (cur.ri < mu ? 1 : 0);
+        const int nq = (ihi - ilo) * cur.nseg;   // k16 steps of this warp (<= kKC / 16)
+        if (nq > 0) {
+            if (cur.c0 != colbits_c0) {
+                colbits_c0 = cur.c0;
+                colbits = 0;
+#pragma unroll
+                for (int bit = 0; bit < 16; ++bit) {
+                    const int j = (bit >> 2) * 16 + ((bit >> 1) & 1) * 8 + 2 * tq + (bit & 1);
+                    if (j < cur.cw && unsigned(cur.c0 + j - ww) < unsigned(p.kw)) colbits |= 1u << bit;
                 }
             }
-            __syncthreads();
-        }
+            const int j0 = ilo * 16 * cur.nseg;   // first slot
+            const uint16_t *Kb = sK + (buf * kKC + j0) * kRow;
+            const uint16_t *Vb = sV + (buf * kKC + j0) * kRow;
 
-        // skip the chunk if none of its keys falls in this warp's window box
-        {
-            bool any = false;
+            // ---- S = Q K^T, step q covering slots [16 q, 16 q + 16)
+            float s[kKC / 8][4];
 #pragma unroll
-            for (int j = 0; j < kKC / 32; ++j) {
-                const int key = sKey[lane + 32 * j];
-                if (key >= 0) {
-                    const int kh_ = (key >> 10) & 1023, kw_ = key & 1023;
-                    any |= kh_ >= box_h0 && kh_ < box_h1 && kw_ >= box_w0 && kw_ < box_w1;
-                }
-            }
-            if (!__any_sync(0xffffffffu, any)) continue;
-        }
-
-        // ---- S = Q K^T for this warp's 16 rows x 64 keys
-        float s[kKC / 8][4];
-#pragma unroll
-        for (int n = 0; n < kKC / 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-        for (int np = 0; np < kKC / 16; ++np) {
+            for (int n = 0; n < kKC / 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+            const uint32_t kaddr = smem_addr(Kb + ((mi >> 1) * 8 + rr) * kRow + (mi & 1) * 8);
 #pragma unroll
             for (int ks = 0; ks < kHD / 16; ++ks) {
-                const int mi = lane >> 3, rr = lane & 7;
-                const uint16_t *bp = sK + (np * 16 + rr + (mi >> 1) * 8) * kRow + ks * 16 + (mi & 1) * 8;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(smem_addr(bp), b0, b1, b2, b3);
-                mma(s[2 * np], qa[ks], b0, b1);
-                mma(s[2 * np + 1], qa[ks], b2, b3);
+#pragma unroll
+                for (int q = 0; q < kKC / 16; ++q) {
+                    if (q < nq) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(kaddr + q * 16 * kRow * 2 + ks * 32, b0, b1, b2, b3);
+                        mma(s[2 * q], qa[ks], b0, b1);
+                        mma(s[2 * q + 1], qa[ks], b2, b3);
+                    }
+                }
             }
-        }
 
-        // ---- mask, online softmax
-        float cmax[2] = {-INFINITY, -INFINITY};
+            // ---- mask, online softmax. Every key of the region lies in each
+            // row's t window (the block is one frame): only h and w are tested.
+            float cmax0 = -INFINITY, cmax1 = -INFINITY;
+            int hk = cur.rb + ilo * S, seg = 0;
 #pragma unroll
-        for (int n = 0; n < kKC / 8; ++n) {
+            for (int q = 0; q < kKC / 16; ++q) {
+                if (q < nq) {
+                    const bool row0 = rvalid0 && unsigned(hk - wh0) < unsigned(p.kh);
+                    const bool row1 = rvalid1 && unsigned(hk - wh1) < unsigned(p.kh);
+                    const uint32_t cb = colbits >> (4 * seg);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = e >> 1;
-                const int key = sKey[n * 8 + 2 * tq + (e & 1)];
-                // every key of the region lies in each row's t window (the block
-                // is one frame), so only h and w are tested
-                const bool ok = key >= 0 && rvalid[r] &&
-                                unsigned(((key >> 10) & 1023) - wh[r]) < unsigned(p.kh) &&
-                                unsigned((key & 1023) - ww[r]) < unsigned(p.kw);
-                s[n][e] = ok ? s[n][e] * p.scale_log2 : -INFINITY;
-                cmax[r] = fmaxf(cmax[r], s[n][e]);
+                    for (int e = 0; e < 8; ++e) {   // half = e >> 2, row = (e >> 1) & 1, kq = e & 1
+                        const bool col = (cb >> (((e >> 2) << 1) | (e & 1))) & 1u;
+                        float &x = s[2 * q + (e >> 2)][e & 3];
+                        const bool ok = col && (((e >> 1) & 1) ? row1 : row0);
+                        x = ok ? x * p.scale_log2 : -INFINITY;
+                        if ((e >> 1) & 1) cmax1 = fmaxf(cmax1, x);
+                        else cmax0 = fmaxf(cmax0, x);
+                    }
+                    if (++seg == cur.nseg) {
+                        seg = 0;
+                        hk += S;
+                    }
+                }
             }
-        }
-        float corr[2];
+            cmax0 = fmaxf(cmax0, __shfl_xor_sync(0xffffffffu, cmax0, 1));
+            cmax0 = fmaxf(cmax0, __shfl_xor_sync(0xffffffffu, cmax0, 2));
+            cmax1 = fmaxf(cmax1, __shfl_xor_sync(0xffffffffu, cmax1, 1));
+            cmax1 = fmaxf(cmax1, __shfl_xor_sync(0xffffffffu, cmax1, 2));
+            const float mn0 = fmaxf(m0, cmax0), mn1 = fmaxf(m1, cmax1);
+            // a row with no key yet keeps max -inf: subtract 0 instead (every
+            // score is -inf there, so every weight is 0)
+            const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float corr0 = ex2(m0 - ms0), corr1 = ex2(m1 - ms1);
+            m0 = mn0;
+            m1 = mn1;
+            float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            cmax[r] = fmaxf(cmax[r], __shfl_xor_sync(0xffffffffu, cmax[r], 1));
-            cmax[r] = fmaxf(cmax[r], __shfl_xor_sync(0xffffffffu, cmax[r], 2));
-            const float mn = fmaxf(m[r], cmax[r]);
-            corr[r] = (mn == -INFINITY) ? 1.f : exp2f(m[r] - mn);   // m = -inf -> 0 unless mn is -inf
-            m[r] = mn;
-            l[r] *= corr[r];
-        }
-        float psum[2] = {0.f, 0.f};
-#pragma unroll
-        for (int n = 0; n < kKC / 8; ++n) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = e >> 1;
-                const float pv = (s[n][e] == -INFINITY) ? 0.f : exp2f(s[n][e] - m[r]);
-                s[n][e] = pv;
-                psum[r] += pv;
+            for (int n = 0; n < kKC / 8; ++n) {
+                if (n < 2 * nq) {
+                    s[n][0] = ex2(s[n][0] - ms0);
+                    s[n][1] = ex2(s[n][1] - ms0);
+                    s[n][2] = ex2(s[n][2] - ms1);
+                    s[n][3] = ex2(s[n][3] - ms1);
+                    ps0 += s[n][0] + s[n][1];
+                    ps1 += s[n][2] + s[n][3];
+                }
             }
-        }
+            ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
+            ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
+            ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
+            ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
+            l0 = l0 * corr0 + ps0;
+            l1 = l1 * corr1 + ps1;
+            if (__any_sync(0xffffffffu, corr0 != 1.f || corr1 != 1.f)) {
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            psum[r] += __shfl_xor_sync(0xffffffffu, psum[r], 1);
-            psum[r] += __shfl_xor_sync(0xffffffffu, psum[r], 2);
-            l[r] += psum[r];
-        }
-#pragma unroll
-        for (int n = 0; n < kHD / 8; ++n) {
-            o[n][0] *= corr[0];
-            o[n][1] *= corr[0];
-            o[n][2] *= corr[1];
-            o[n][3] *= corr[1];
-        }
+                for (int n = 0; n < kHD / 8; ++n) {
+                    o[n][0] *= corr0;
+                    o[n][1] *= corr0;
+                    o[n][2] *= corr1;
+                    o[n][3] *= corr1;
+                }
+            }
 
-        // ---- O += P V
+            // ---- O += P V
+            const uint32_t vaddr = smem_addr(Vb + (rr + (mi & 1) * 8) * kRow + (mi >> 1) * 8);
 #pragma unroll
-        for (int kk = 0; kk < kKC / 16; ++kk) {
-            uint32_t pa[4];
-            pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-            pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-            pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-            pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+            for (int q = 0; q < kKC / 16; ++q) {
+                if (q < nq) {
+                    uint32_t pa[4];
+                    pa[0] = pack_bf16(s[2 * q][0], s[2 * q][1]);
+                    pa[1] = pack_bf16(s[2 * q][2], s[2 * q][3]);
+                    pa[2] = pack_bf16(s[2 * q + 1][0], s[2 * q + 1][1]);
+                    pa[3] = pack_bf16(s[2 * q + 1][2], s[2 * q + 1][3]);
 #pragma unroll
-            for (int np = 0; np < kHD / 16; ++np) {
-                const int mi = lane >> 3, rr = lane & 7;
-                const uint16_t *bp = sV + (kk * 16 + rr + (mi & 1) * 8) * kRow + np * 16 + (mi >> 1) * 8;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(smem_addr(bp), b0, b1, b2, b3);
-                mma(o[2 * np], pa, b0, b1);
-                mma(o[2 * np + 1], pa, b2, b3);
+                    for (int np = 0; np < kHD / 16; ++np) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(vaddr + q * 16 * kRow * 2 + np * 32, b0, b1, b2, b3);
+                        mma(o[2 * np], pa, b0, b1);
+                        mma(o[2 * np + 1], pa, b2, b3);
+                    }
+                }
             }
         }
+        if (kRope && c + 1 < n_chunks) store_k(nxt.t, buf ^ 1);
+        cur = nxt;
     }
 
     // ---- normalise and store
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-        if (!rvalid[r]) continue;
-        const int row = warp * 16 + g + 8 * r;
-        const int h = h0 + row / kQBW, w = w0 + row % kQBW;
-        const float inv = l[r] > 0.f ? 1.f / l[r] : 0.f;
-        uint16_t *dst = p.out + token_index(qt, h, w) * tok_stride + size_t(head) * kHD;
+        if (!(r == 0 ? rvalid0 : rvalid1)) continue;
+        const float l = r == 0 ? l0 : l1;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint16_t *dst = p.out + batch0 - cv * 8 + qt * frame + (hq + r) * grid_row + (long long)wq * tok;
 #pragma unroll
         for (int n = 0; n < kHD / 8; ++n) {
             const uint32_t pk = pack_bf16(o[n][2 * r] * inv, o[n][2 * r + 1] * inv);
@@ -473,13 +584,18 @@ extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *ou
     p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(kHD)));
     const uint64_t blocks = uint64_t(B) * heads * T * p.nbh * p.nbw;
     if (blocks > 0x7fffffffull) return ROPE3D_ERR_SHAPE;
-    const size_t smem = size_t(kQB + 2 * kKC) * kRow * 2 + kKC * sizeof(int) +
-                        (apply_rope ? size_t(p.tab_len) * sizeof(float2) : 0);
-    static const cudaError_t attr_rc = cudaFuncSetAttribute(
-        rope3d_na3d_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        int(size_t(kQB + 2 * kKC) * kRow * 2 + kKC * sizeof(int) + kMaxTableBytes));
-    if (attr_rc != cudaSuccess) return ROPE3D_ERR_CUDA;
-    rope3d_na3d_kernel<<<unsigned(blocks), kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
+    const size_t smem = kFixedSmem + (apply_rope ? size_t(p.tab_len) * sizeof(float2) : 0);
+    static const cudaError_t attr_rc[2] = {
+        cudaFuncSetAttribute(rope3d_na3d_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kFixedSmem)),
+        cudaFuncSetAttribute(rope3d_na3d_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kFixedSmem + kMaxTableBytes))};
+    if (attr_rc[0] != cudaSuccess || attr_rc[1] != cudaSuccess) return ROPE3D_ERR_CUDA;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (apply_rope)
+        rope3d_na3d_kernel<true><<<unsigned(blocks), kThreads, smem, st>>>(p);
+    else
+        rope3d_na3d_kernel<false><<<unsigned(blocks), kThreads, smem, st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return ROPE3D_ERR_CUDA;
     return ROPE3D_OK;
 }

@@ -43,6 +43,8 @@ CASES = [
     ((2, 2, 9, 17, 1), (32, 48, 48), (1, 3, 7)),      # partial query blocks at both edges
     ((1, 5, 8, 8, 2), (48, 40, 40), (5, 7, 7)),        # windows covering the grid
     ((1, 4, 16, 24, 1), (32, 48, 48), (3, 7, 7)),
+    ((1, 2, 6, 80, 1), (32, 48, 48), (1, 3, 67)),      # a region row of 74 keys: split in columns
+    ((1, 2, 12, 40, 1), (32, 48, 48), (1, 9, 33)),     # region rows of 40 keys: three 16-key steps
 ]
 
 
