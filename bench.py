@@ -672,6 +672,9 @@ def run_na3d(args):
         r.rope3d_apply_pair(q, k, tabs, qr, kr, stream=stream)
         r.rope3d_na3d(qr, kr, v, tabs, c["kernel"], out, apply_rope=False, stream=stream)
 
+    def attention_only():
+        r.rope3d_na3d(qr, kr, v, tabs, c["kernel"], out, apply_rope=False, stream=stream)
+
     def timed(fn, steps):
         for _ in range(max(args.warmup, 3)):
             fn()
@@ -692,6 +695,7 @@ def run_na3d(args):
     ms_fused = timed(fused, args.steps)
     t1 = time.time()
     ms_unfused = timed(unfused, args.steps)
+    ms_attention = timed(attention_only, args.steps)
     time.sleep(0.25)
     clocks.stop()
     kt, kh, kw = c["kernel"]
@@ -716,6 +720,8 @@ def run_na3d(args):
                      "frac": tflops / peak, "traffic": None,
                      "peak_source": f"{kind} bf16_tflops (cuBLAS burst)", "kernel_ms": ms_fused},
         "unfused_ms": ms_unfused, "fusion_saving_ms": ms_unfused - ms_fused,
+        "attention_only_ms": ms_attention,
+        "attention_only_tflops": flops / (ms_attention / 1e3) / 1e12,
         "clocks": clocks.summary(t0, t1), "gpu_launches": args.steps,
     }
     print(json.dumps(line), flush=True)

@@ -18,14 +18,14 @@
 // Work decomposition: a CTA of 4 warps owns one (batch, head) and a block of
 // 1 x 8 x 8 query tokens; each warp holds 2 x 8 of them (16 MMA rows), so the
 // union of its windows spans whole rows of the block's key region. The region
-// (the union of the block's windows) is visited in chunks of whole region rows
-// (at most 64 keys); inside a chunk a warp's keys are one contiguous range,
-// and the warp runs its MMAs on that range only. S = Q K^T and O += P V run on
-// the tensor cores as bf16 m16n8k16 MMAs with fp32 accumulators, with a
-// flash-style online softmax in registers (running max and sum per row) and a
-// per-element window mask. Chunks are double-buffered: the next chunk's K is
-// loaded into registers and its V copied asynchronously while the current one
-// is computed; K is rotated on its way from registers to shared memory.
+// (the union of the block's windows) is visited in chunks of region rows (at
+// most 64 key slots, 16 per row); inside a chunk a warp's keys are one
+// contiguous run of slots, and the warp runs its MMAs on that run only.
+// S = Q K^T and O += P V run on the tensor cores as bf16 m16n8k16 MMAs with
+// fp32 accumulators, with a flash-style online softmax in registers and a
+// per-element window mask. Chunks are double-buffered: the next chunk's K and
+// V are copied asynchronously while the current one is computed; when
+// rotating, each thread then rotates the K vectors it copied, in place.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -35,6 +35,19 @@
 
 #include "../../include/rope3d.h"
 #include "rope3d_internal.h"
+
+// Tuning: resident CTAs per SM the register allocation aims at (the
+// unrotated kernel fits three in shared memory; the rotating one, with its
+// tables, two), and log2 of the largest softmax weight before a rescale.
+#ifndef NA_MIN_CTAS
+#define NA_MIN_CTAS 3
+#endif
+#ifndef NA_MIN_CTAS_ROPE
+#define NA_MIN_CTAS_ROPE 2
+#endif
+#ifndef NA_LAZY
+#define NA_LAZY 8.0f
+#endif
 
 namespace {
 
@@ -47,6 +60,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kRow = kHD + 8;        // padded smem row (bf16): 272 bytes
 constexpr int kVecs = kKC * (kHD / 8) / kThreads;   // 16-byte vectors per thread per chunk
 constexpr uint32_t kMaxTableBytes = 48 * 1024;
+constexpr float kLazy = NA_LAZY;     // log2 of the largest weight before a rescale
 constexpr size_t kFixedSmem = size_t(4) * kKC * kRow * 2;   // K and V, two buffers each
 static_assert(kQB == kQBH * kQBW && kQB == kWarps * 16 && kQBW == 8,
               "a warp holds two 8-wide rows of the query block");
@@ -60,7 +74,6 @@ struct NAParams {
     int B, T, H, W, heads;
     int kt, kh, kw;
     int nbh, nbw;            // query blocks along H and W
-    int rope;
     float scale_log2;        // log2(e) / sqrt(head_dim)
 };
 
@@ -173,7 +186,7 @@ struct Chunk {
 };
 
 template <bool kRope>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, kRope ? NA_MIN_CTAS_ROPE : NA_MIN_CTAS)
 rope3d_na3d_kernel(const NAParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     uint16_t *sK = reinterpret_cast<uint16_t *>(smem);        // [2][kKC][kRow]
@@ -197,6 +210,7 @@ rope3d_na3d_kernel(const NAParams p) {
     // per 256-byte row: coalesced).
     const int cv = tid & 15, slot0 = tid >> 4;
     const TabSlot ts = tab_slot(p, cv);
+    const float2 *tab = sTab;
     const long long tok = (long long)p.heads * kHD;             // elements per token
     const long long grid_row = (long long)p.W * tok, frame = (long long)p.H * grid_row;
     const long long batch0 = (long long)b * p.T * frame + (long long)head * kHD + cv * 8;
@@ -239,12 +253,9 @@ rope3d_na3d_kernel(const NAParams p) {
         return k;
     };
 
-    // K of a chunk goes through registers when it is rotated (on the way to
-    // shared memory), else it is copied asynchronously like V. Slots past a
-    // row's last column get zeros, so every slot a warp reads holds finite
-    // values.
-    uint4 kreg[kVecs];
-    int kpos[kVecs];   // packed (h, w) of a K vector to rotate; -1: zeros; -2: no slot
+    // K and V of a chunk are copied asynchronously. Slots past a row's last
+    // column get zeros, so every slot a warp reads holds finite values.
+    int kpos[kVecs];   // packed (h, w) of a K vector to rotate, else -1
     auto issue = [&](const Chunk &k, int buf) {
         const int sw = 16 * k.nseg;
         long long off = batch0 + k.t * frame + k.rb * grid_row + (long long)(k.c0 + slot0) * tok;
@@ -255,19 +266,14 @@ rope3d_na3d_kernel(const NAParams p) {
             const int slot = slot0 + 8 * m;
             uint16_t *dk = sK + (buf * kKC + slot) * kRow + cv * 8;
             uint16_t *dv = sV + (buf * kKC + slot) * kRow + cv * 8;
-            if (kRope) kpos[m] = -2;
+            if (kRope) kpos[m] = -1;
             if (i < k.nr) {
                 if (j < k.cw) {
-                    if (kRope) {
-                        kreg[m] = __ldg(reinterpret_cast<const uint4 *>(p.k + off));
-                        kpos[m] = ((k.rb + i * S) << 10) | (k.c0 + j);
-                    } else {
-                        cp_async16(dk, p.k + off);
-                    }
+                    cp_async16(dk, p.k + off);
                     cp_async16(dv, p.v + off);
+                    if (kRope) kpos[m] = ((k.rb + i * S) << 10) | (k.c0 + j);
                 } else {
-                    if (kRope) kpos[m] = -1;
-                    else *reinterpret_cast<uint4 *>(dk) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(dk) = make_uint4(0, 0, 0, 0);
                     *reinterpret_cast<uint4 *>(dv) = make_uint4(0, 0, 0, 0);
                 }
             }
@@ -280,14 +286,16 @@ rope3d_na3d_kernel(const NAParams p) {
             }
         }
     };
-    auto store_k = [&](int t, int buf) {   // rotating path only
+    // Rotating path: a thread waits for its own copies of K and rotates them
+    // in place (no other thread touches those 16-byte vectors).
+    auto rotate_k = [&](int t, int buf) {
+        cp_async_wait_all();
 #pragma unroll
         for (int m = 0; m < kVecs; ++m) {
             const int pos = kpos[m];
-            if (pos != -2) {
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (pos >= 0) v = rot_vec(kreg[m], sTab, ts, t, pos >> 10, pos & 1023);
-                *reinterpret_cast<uint4 *>(sK + (buf * kKC + slot0 + 8 * m) * kRow + cv * 8) = v;
+            if (pos >= 0) {
+                uint4 *ptr = reinterpret_cast<uint4 *>(sK + (buf * kKC + slot0 + 8 * m) * kRow + cv * 8);
+                *ptr = rot_vec(*ptr, tab, ts, t, pos >> 10, pos & 1023);
             }
         }
     };
@@ -314,10 +322,10 @@ rope3d_na3d_kernel(const NAParams p) {
         const int r = slot0 + 8 * m;
         const int h = h0 + r / kQBW, w = w0 + r % kQBW;
         uint4 v = qreg[m];
-        if (kRope && h < p.H && w < p.W) v = rot_vec(v, sTab, ts, qt, h, w);
+        if (kRope && h < p.H && w < p.W) v = rot_vec(v, tab, ts, qt, h, w);
         *reinterpret_cast<uint4 *>(sQ + r * kRow + cv * 8) = v;
     }
-    if (kRope) store_k(cur.t, 0);
+    if (kRope) rotate_k(cur.t, 0);
     __syncthreads();
 
     // Q fragments of this warp's 16 rows, all 8 k-steps
@@ -398,10 +406,11 @@ rope3d_na3d_kernel(const NAParams p) {
 
             // ---- mask, online softmax. Every key of the region lies in each
             // row's t window (the block is one frame): only h and w are tested.
-            float cmax0 = -INFINITY, cmax1 = -INFINITY;
             int hk = cur.rb + ilo * S, seg = 0;
+            float qmax0[kKC / 16], qmax1[kKC / 16];
 #pragma unroll
             for (int q = 0; q < kKC / 16; ++q) {
+                qmax0[q] = qmax1[q] = -INFINITY;
                 if (q < nq) {
                     const bool row0 = rvalid0 && unsigned(hk - wh0) < unsigned(p.kh);
                     const bool row1 = rvalid1 && unsigned(hk - wh1) < unsigned(p.kh);
@@ -412,45 +421,34 @@ rope3d_na3d_kernel(const NAParams p) {
                         float &x = s[2 * q + (e >> 2)][e & 3];
                         const bool ok = col && (((e >> 1) & 1) ? row1 : row0);
                         x = ok ? x * p.scale_log2 : -INFINITY;
-                        if ((e >> 1) & 1) cmax1 = fmaxf(cmax1, x);
-                        else cmax0 = fmaxf(cmax0, x);
                     }
+                    qmax0[q] = fmaxf(fmaxf(s[2 * q][0], s[2 * q][1]), fmaxf(s[2 * q + 1][0], s[2 * q + 1][1]));
+                    qmax1[q] = fmaxf(fmaxf(s[2 * q][2], s[2 * q][3]), fmaxf(s[2 * q + 1][2], s[2 * q + 1][3]));
                     if (++seg == cur.nseg) {
                         seg = 0;
                         hk += S;
                     }
                 }
             }
+            float cmax0 = fmaxf(fmaxf(qmax0[0], qmax0[1]), fmaxf(qmax0[2], qmax0[3]));
+            float cmax1 = fmaxf(fmaxf(qmax1[0], qmax1[1]), fmaxf(qmax1[2], qmax1[3]));
             cmax0 = fmaxf(cmax0, __shfl_xor_sync(0xffffffffu, cmax0, 1));
             cmax0 = fmaxf(cmax0, __shfl_xor_sync(0xffffffffu, cmax0, 2));
             cmax1 = fmaxf(cmax1, __shfl_xor_sync(0xffffffffu, cmax1, 1));
             cmax1 = fmaxf(cmax1, __shfl_xor_sync(0xffffffffu, cmax1, 2));
+            // Weights are exp2(score - ref) with ref a running reference per
+            // row. The reference moves up to the row's maximum (and O and l
+            // are rescaled) only when the maximum exceeds it by more than
+            // kLazy, so weights stay below 2^kLazy; a row with no key yet has
+            // reference -inf and subtracts 0 (every score is -inf there).
             const float mn0 = fmaxf(m0, cmax0), mn1 = fmaxf(m1, cmax1);
-            // a row with no key yet keeps max -inf: subtract 0 instead (every
-            // score is -inf there, so every weight is 0)
-            const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float corr0 = ex2(m0 - ms0), corr1 = ex2(m1 - ms1);
-            m0 = mn0;
-            m1 = mn1;
-            float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-            for (int n = 0; n < kKC / 8; ++n) {
-                if (n < 2 * nq) {
-                    s[n][0] = ex2(s[n][0] - ms0);
-                    s[n][1] = ex2(s[n][1] - ms0);
-                    s[n][2] = ex2(s[n][2] - ms1);
-                    s[n][3] = ex2(s[n][3] - ms1);
-                    ps0 += s[n][0] + s[n][1];
-                    ps1 += s[n][2] + s[n][3];
-                }
-            }
-            ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
-            ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
-            ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
-            ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
-            l0 = l0 * corr0 + ps0;
-            l1 = l1 * corr1 + ps1;
-            if (__any_sync(0xffffffffu, corr0 != 1.f || corr1 != 1.f)) {
+            if (__any_sync(0xffffffffu, mn0 > m0 + kLazy || mn1 > m1 + kLazy)) {
+                const float corr0 = m0 == -INFINITY ? 0.f : ex2(m0 - mn0);
+                const float corr1 = m1 == -INFINITY ? 0.f : ex2(m1 - mn1);
+                m0 = mn0;
+                m1 = mn1;
+                l0 *= corr0;
+                l1 *= corr1;
 #pragma unroll
                 for (int n = 0; n < kHD / 8; ++n) {
                     o[n][0] *= corr0;
@@ -459,6 +457,31 @@ rope3d_na3d_kernel(const NAParams p) {
                     o[n][3] *= corr1;
                 }
             }
+            const float ms0 = m0 == -INFINITY ? 0.f : m0, ms1 = m1 == -INFINITY ? 0.f : m1;
+            float qs0[kKC / 16], qs1[kKC / 16];
+#pragma unroll
+            for (int q = 0; q < kKC / 16; ++q) {
+                qs0[q] = qs1[q] = 0.f;
+                if (q < nq) {
+#pragma unroll
+                    for (int n = 2 * q; n < 2 * q + 2; ++n) {
+                        s[n][0] = ex2(s[n][0] - ms0);
+                        s[n][1] = ex2(s[n][1] - ms0);
+                        s[n][2] = ex2(s[n][2] - ms1);
+                        s[n][3] = ex2(s[n][3] - ms1);
+                    }
+                    qs0[q] = (s[2 * q][0] + s[2 * q][1]) + (s[2 * q + 1][0] + s[2 * q + 1][1]);
+                    qs1[q] = (s[2 * q][2] + s[2 * q][3]) + (s[2 * q + 1][2] + s[2 * q + 1][3]);
+                }
+            }
+            float ps0 = (qs0[0] + qs0[1]) + (qs0[2] + qs0[3]);
+            float ps1 = (qs1[0] + qs1[1]) + (qs1[2] + qs1[3]);
+            ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
+            ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
+            ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
+            ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
+            l0 += ps0;
+            l1 += ps1;
 
             // ---- O += P V
             const uint32_t vaddr = smem_addr(Vb + (rr + (mi & 1) * 8) * kRow + (mi >> 1) * 8);
@@ -480,7 +503,7 @@ rope3d_na3d_kernel(const NAParams p) {
                 }
             }
         }
-        if (kRope && c + 1 < n_chunks) store_k(nxt.t, buf ^ 1);
+        if (kRope && c + 1 < n_chunks) rotate_k(nxt.t, buf ^ 1);
         cur = nxt;
     }
 
@@ -580,7 +603,6 @@ extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *ou
     p.kw = kw;
     p.nbh = int((H + kQBH - 1) / kQBH);
     p.nbw = int((W + kQBW - 1) / kQBW);
-    p.rope = apply_rope ? 1 : 0;
     p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(kHD)));
     const uint64_t blocks = uint64_t(B) * heads * T * p.nbh * p.nbw;
     if (blocks > 0x7fffffffull) return ROPE3D_ERR_SHAPE;
