@@ -189,12 +189,15 @@ class ClockSampler:
                 "samples": len(used), "samples_in_window": len(inside)}
 
 
-def same_box_copy_gbs(torch, dev) -> float:
-    """A torch copy of 1 Gi bf16 elements on this GPU (read + write bytes,
-    best of 10, CUDA events), the way the measured peak was taken: shows how
-    this GPU compares with the one the peak was measured on."""
+def same_box_copy_gbs(torch, dev, sustained_s: float = 1.0):
+    """A torch copy of 1 Gi bf16 elements on this GPU (read + write bytes, CUDA
+    events): the best of 10 single copies, the way the measured peak was
+    taken (how this GPU compares with the one the peak was measured on), and
+    the average of back-to-back copies over about `sustained_s` seconds, timed
+    like the kernel's own steps (the like-for-like ratio)."""
     x = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev)
     y = torch.empty_like(x)
+    nbytes = 2 * x.numel() * 2
     best = 0.0
     for _ in range(11):
         a = torch.cuda.Event(enable_timing=True)
@@ -203,9 +206,18 @@ def same_box_copy_gbs(torch, dev) -> float:
         y.copy_(x)
         b.record()
         torch.cuda.synchronize(dev)
-        best = max(best, 2 * x.numel() * 2 / (a.elapsed_time(b) / 1e3) / 1e9)
+        best = max(best, nbytes / (a.elapsed_time(b) / 1e3) / 1e9)
+    reps = max(10, int(sustained_s * best * 1e9 / nbytes))
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        y.copy_(x)
+    b.record()
+    torch.cuda.synchronize(dev)
+    sustained = reps * nbytes / (a.elapsed_time(b) / 1e3) / 1e9
     del x, y
-    return best
+    return best, sustained
 
 
 def launches_per_call(w: synthetic.Workload, kernel: int) -> int:
@@ -443,7 +455,7 @@ def run_ours(args, w):
 
     total_ms = max_over_ranks(total_ms, dist, dev)
 
-    box_copy = same_box_copy_gbs(torch, dev)
+    box_copy, box_copy_sustained = same_box_copy_gbs(torch, dev)
     bytes_step = w.bytes_per_call * calls
     value = world * args.steps * bytes_step / (total_ms / 1e3) / 1e9
     kernel_ms = statistics.fmean(per_launch) / calls   # per call (one launch per call)
@@ -482,7 +494,10 @@ def run_ours(args, w):
                          "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
                          "kernel_ms": kernel_ms,
                          "same_box_copy_gbs": box_copy,
-                         "frac_of_same_box_copy": achieved / box_copy if box_copy else None},
+                         "frac_of_same_box_copy": achieved / box_copy if box_copy else None,
+                         "same_box_copy_sustained_gbs": box_copy_sustained,
+                         "frac_of_same_box_copy_sustained":
+                             achieved / box_copy_sustained if box_copy_sustained else None},
             "clocks": clk,
             "gpu_launches": args.steps * launches_per_step,
             "kernel": {"variant": {1: "vec16", 2: "pair"}.get(launch["kernel"], "?"),

@@ -144,7 +144,7 @@ __device__ __forceinline__ long long strided_offset(const KStrides &st, int i, c
 // Read-only streaming load (inputs never alias outputs in contiguous calls).
 __device__ __forceinline__ uint4 ld_stream_v4(const void *ptr) {
     uint4 r;
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm("ld.global.nc.L1::no_allocate.L2::128B.v4.u32 {%0, %1, %2, %3}, [%4];"
         : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
         : "l"(ptr));
     return r;
@@ -155,7 +155,7 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *ptr) {
 // previous iteration, which may write the same buffer (in place).
 __device__ __forceinline__ uint4 ld_coherent_v4(const void *ptr) {
     uint4 r;
-    asm volatile("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.L1::no_allocate.L2::128B.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                  : "l"(ptr)
                  : "memory");

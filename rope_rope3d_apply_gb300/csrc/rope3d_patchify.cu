@@ -87,7 +87,7 @@ __device__ __forceinline__ uint64_t patched_row(const PParams &q, const Row &r, 
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void *ptr) {
     uint4 v;
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm("ld.global.nc.L1::no_allocate.L2::128B.v4.u32 {%0, %1, %2, %3}, [%4];"
         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
         : "l"(ptr));
     return v;
