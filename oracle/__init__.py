@@ -347,3 +347,40 @@ def rope_na3d(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, shape,
         k_bits = rope3d(k_bits, shape, split, tabs, lib)
     to64 = lambda b: (np.ascontiguousarray(b).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)  # noqa: E731
     return na3d(to64(q_bits), to64(k_bits), to64(v_bits), shape, kernel)
+
+
+def rope_na3d_at(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, shape, split, tabs,
+                 kernel, queries, rope: bool = True, lib=None):
+    """rope_na3d for single queries, one at a time: queries is a list of
+    (b, t, h, w, head). Each query vector and each key of its window is rotated
+    element by element (rope3d_at), then the window's softmax attention is
+    taken in float64. Returns (out, absv), each [len(queries), head_dim]:
+    the attention output and the same weights applied to |v|."""
+    B, T, H, W, heads, d = (int(x) for x in shape)
+    kt, kh, kw = kernel
+    st, sh, sw = na_window_starts(T, kt), na_window_starts(H, kh), na_window_starts(W, kw)
+    q_flat = np.ascontiguousarray(q_bits).reshape(-1)
+    k_flat = np.ascontiguousarray(k_bits).reshape(-1)
+    v_flat = np.ascontiguousarray(v_bits).reshape(-1)
+    to64 = lambda b: (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)  # noqa: E731
+    chan = np.arange(d, dtype=np.int64)
+
+    def row(b, t, h, w, e):   # flat index of channel 0 of (b, t, h, w, head e)
+        return ((((b * T + t) * H + h) * W + w) * heads + e) * d
+
+    out = np.empty((len(queries), d))
+    absv = np.empty((len(queries), d))
+    for n, (b, t, h, w, e) in enumerate(queries):
+        qi = row(b, t, h, w, e) + chan
+        qv = rope3d_at(q_flat, qi, shape, split, tabs, lib) if rope else q_flat[qi]
+        keys = [row(b, tt, hh, ww, e) for tt in range(st[t], st[t] + kt)
+                for hh in range(sh[h], sh[h] + kh) for ww in range(sw[w], sw[w] + kw)]
+        ki = (np.array(keys, dtype=np.int64)[:, None] + chan[None, :]).reshape(-1)
+        kv = rope3d_at(k_flat, ki, shape, split, tabs, lib) if rope else k_flat[ki]
+        vv = to64(v_flat[ki]).reshape(len(keys), d)
+        s = to64(kv).reshape(len(keys), d) @ to64(qv) / np.sqrt(d)
+        p = np.exp(s - s.max())
+        p /= p.sum()
+        out[n] = p @ vv
+        absv[n] = p @ np.abs(vv)
+    return out, absv

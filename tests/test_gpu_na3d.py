@@ -115,3 +115,44 @@ def test_na3d_rejections():
         r.rope3d_na3d(q, q, q, tabs, (3, 3, 3), out=q)
     assert e.value.name == "ERR_ALIAS"
     tabs.close()
+
+
+def _bench_queries(B, T, H, W, heads, count, seed):
+    """Corners, edges and centre of the grid, then seeded random queries."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    fixed = []
+    for t in (0, T // 2, T - 1):
+        for h in (0, 1, H // 2, H - 2, H - 1):
+            for w in (0, 3, W // 2, W - 1):
+                fixed.append((0, t, h, w, int(g.integers(heads))))
+    rand = [tuple(int(x) for x in (g.integers(B), g.integers(T), g.integers(H), g.integers(W),
+                                   g.integers(heads))) for _ in range(count - len(fixed))]
+    return fixed + rand
+
+
+def test_na3d_full_size_sampled():
+    """The attention workload bench.py times (1 x 16 x 64 x 64 tokens, 16
+    heads x 128, bf16, window 3 x 7 x 7, same seeds), launched as the bench
+    launches it: 192 sampled queries of the fused kernel against the oracle
+    computed one query at a time, and the unfused pair bit-identical to it."""
+    B, T, H, W, heads, split, kernel = 1, 16, 64, 64, 16, (32, 48, 48), (3, 7, 7)
+    shape6 = (B, T, H, W, heads, 128)
+    shp = (B, T * H * W, heads, 128)
+    n = int(np.prod(shp))
+    bits = [synthetic.normal(n, 1.0, 12, i, "bf16") for i in range(3)]
+    q, k, v = (bf16(a).reshape(shp).to(DEV) for a in bits)
+    tabs = r.rope3d_build_tables(T, H, W, split)
+    fused = r.rope3d_na3d(q, k, v, tabs, kernel)
+    qr, kr = r.rope3d_apply_pair(q, k, tabs)
+    unfused = r.rope3d_na3d(qr, kr, v, tabs, kernel, apply_rope=False)
+    torch.cuda.synchronize()
+    assert torch.equal(fused.view(torch.int16), unfused.view(torch.int16))
+    queries = _bench_queries(B, T, H, W, heads, 192, 304)
+    got_all = fused.view(shape6)
+    got = to_f64(torch.stack([got_all[b, t, h, w, e] for b, t, h, w, e in queries]))
+    otabs = oracle.tables(T, H, W, split)
+    ref, absv = oracle.rope_na3d_at(*bits, shape6, split, otabs, kernel, queries)
+    bound = 2.0 ** -7 * absv + 2.0 ** -8 * np.abs(ref) + 1e-6
+    err = np.abs(got - ref)
+    assert np.all(err <= bound), (err.max(), (err / bound).max())
+    tabs.close()

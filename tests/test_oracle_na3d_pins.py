@@ -76,3 +76,31 @@ def test_border_rule_hand_example():
     assert oracle.na_window_starts(5, 5).tolist() == [0, 0, 0, 0, 0]
     with pytest.raises(ValueError):
         oracle.na3d(np.zeros(24), np.zeros(24), np.zeros(24), (1, 2, 3, 4, 1, 1), (3, 3, 3))
+
+
+def test_single_query_oracle_equals_full_pass():
+    """rope_na3d_at (one query at a time, element-by-element rotation) gives
+    the full pass's outputs, and its |v| sums are the full pass on |v|; so the
+    sampled checks at full size rest on the same pins as the full pass."""
+    B, T, H, W, heads, d = shape = (2, 3, 6, 7, 2, 16)
+    split, kernel = (4, 6, 6), (3, 3, 5)
+    g = _rng(11)
+    n = int(np.prod(shape))
+    to_bits = lambda a: (a.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)  # noqa: E731
+    q, k, v = (to_bits(g.normal(size=n)) for _ in range(3))
+    tabs = oracle.tables(T, H, W, split)
+    full = oracle.rope_na3d(q, k, v, shape, split, tabs, kernel)
+    qr = oracle.rope3d(q, shape, split, tabs)
+    kr = oracle.rope3d(k, shape, split, tabs)
+    to64 = lambda b: (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)  # noqa: E731
+    full_abs = oracle.na3d(to64(qr), to64(kr), np.abs(to64(v)), shape, kernel)
+    queries = list(itertools.product(range(B), range(T), range(H), range(W), range(heads)))
+    out, absv = oracle.rope_na3d_at(q, k, v, shape, split, tabs, kernel, queries)
+    ref = np.array([full[b, t, h, w, e] for b, t, h, w, e in queries])
+    ref_abs = np.array([full_abs[b, t, h, w, e] for b, t, h, w, e in queries])
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-14)
+    assert np.allclose(absv, ref_abs, rtol=1e-12, atol=1e-14)
+    # without the rotation it is plain neighbourhood attention
+    out0, _ = oracle.rope_na3d_at(q, k, v, shape, split, tabs, kernel, queries[:40], rope=False)
+    plain = oracle.na3d(to64(q), to64(k), to64(v), shape, kernel)
+    assert np.allclose(out0, [plain[x] for x in queries[:40]], rtol=1e-12, atol=1e-14)
