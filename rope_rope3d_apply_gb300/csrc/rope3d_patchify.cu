@@ -110,6 +110,16 @@ __device__ __forceinline__ void st_cs_v4(void *ptr, const uint4 &v) {
 // side is coalesced per width offset as it is. A warp whose 32 units are not
 // all in range (the last one) moves its chunks lane by lane.
 
+// Programmatic dependent launch: a kernel lets the next kernel of the stream
+// start launching at once, and waits for the grids before it to complete (and
+// their writes to become visible) before it touches memory, so back-to-back
+// launches overlap one kernel's tail with the next one's launch. Launched
+// without the attribute, both instructions return at once.
+__device__ __forceinline__ void pdl_begin() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Shared-memory slot of chunk c of a warp's run: an XOR swizzle of the low three
 // bits, so that both lane-contiguous and lane-strided (by P) accesses hit eight
 // different 16-byte bank groups per quarter warp.
@@ -121,6 +131,7 @@ patchify_vec_kernel(const PParams q) {
     using E = typename ElemT<ES>::T;
     constexpr int V = 16 / ES;  // output columns per thread and width offset
     __shared__ uint4 stage[kThreads / 32][32 * P];
+    pdl_begin();
     const uint32_t lane = threadIdx.x & 31u;
     uint4 *ws = stage[threadIdx.x >> 5];
     const uint32_t stride = gridDim.x * blockDim.x;
@@ -200,6 +211,7 @@ patchify_elem_kernel(const PParams q) {
     using E = typename ElemT<ES>::T;
     const E *src = reinterpret_cast<const E *>(q.src);
     E *dst = reinterpret_cast<E *>(q.dst);
+    pdl_begin();
     const uint32_t stride = gridDim.x * blockDim.x;
     for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < q.units; u += stride) {
         const uint32_t row_local = fdiv(u, q.Wd);
@@ -327,8 +339,19 @@ int run(bool forward, const void *src, void *dst, int64_t B, int64_t C, int64_t 
         q.bcf0 = static_cast<uint32_t>(p0);
         const uint64_t need = (uint64_t(q.units) + kThreads - 1) / kThreads;
         const int grid = static_cast<int>(std::min<uint64_t>(need, uint64_t(sms) * 8));
-        fn<<<grid, kThreads, 0, st>>>(q);
-        if (cudaGetLastError() != cudaSuccess) return ROPE3D_ERR_CUDA;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.stream = st;
+        cudaLaunchAttribute attr{};
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, fn, q) != cudaSuccess) {
+            cudaGetLastError();
+            return ROPE3D_ERR_CUDA;
+        }
     }
     t_patch_kernel = vec ? 1 : 2;
     return ROPE3D_OK;
