@@ -195,11 +195,22 @@ struct Pack2<ROPE3D_F16> {
     static __device__ __forceinline__ T2 from_floats(float a, float b) { return __floats2half2_rn(a, b); }
 };
 
+// Programmatic dependent launch: a kernel lets the next kernel of the stream
+// start launching at once, and waits for the grids before it to complete (and
+// their writes to become visible) before it touches memory, so back-to-back
+// launches overlap one kernel's tail with the next one's launch. Launched
+// without the attribute, both instructions return at once.
+__device__ __forceinline__ void pdl_begin() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 template <int kType>
 __global__ void __launch_bounds__(kThreads)
 rope3d_neox_vec_kernel(const NParams p) {
     constexpr int kElemBytes = kType == ROPE3D_F32 ? 4 : 2;
     constexpr int V = 16 / kElemBytes;   // channels per vector
+    pdl_begin();
     const uint32_t stride = gridDim.x * blockDim.x;
     for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < p.units; u += stride) {
         Unit x;
@@ -256,6 +267,7 @@ template <int kType>
 __global__ void __launch_bounds__(kThreads)
 rope3d_neox_pair_kernel(const NParams p) {
     constexpr int kElemBytes = kType == ROPE3D_F32 ? 4 : 2;
+    pdl_begin();
     const uint32_t stride = gridDim.x * blockDim.x;
     for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < p.units; u += stride) {
         Unit x;
@@ -398,8 +410,19 @@ int neox(const void *q, const void *k, void *q_out, void *k_out, const int64_t *
         p.units = static_cast<uint32_t>(nt * per_token);
         const uint64_t need = (uint64_t(p.units) + kThreads - 1) / kThreads;
         const int grid = static_cast<int>(std::min<uint64_t>(need, uint64_t(sms) * 8));
-        fn<<<grid, kThreads, 0, st>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return ROPE3D_ERR_CUDA;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.stream = st;
+        cudaLaunchAttribute attr{};
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, fn, p) != cudaSuccess) {
+            cudaGetLastError();
+            return ROPE3D_ERR_CUDA;
+        }
     }
     t_neox_kernel = vec ? 1 : 2;
     return ROPE3D_OK;
