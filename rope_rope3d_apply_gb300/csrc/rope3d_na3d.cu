@@ -178,6 +178,59 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// S = Q K^T over NQ 16-key steps (keys q * 16 .. q * 16 + 15 of the warp's
+// run start at kaddr + q * 16 rows), software-pipelined: the B fragments of
+// k-step ks + 1 are loaded while the MMAs of k-step ks issue.
+template <int NQ>
+__device__ __forceinline__ void qk_steps(float (&s)[kKC / 8][4], const uint32_t (&qa)[kHD / 16][4],
+                                         uint32_t kaddr) {
+    uint32_t bf[2][NQ][4];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+        ldsm_x4(kaddr + q * 16 * kRow * 2, bf[0][q][0], bf[0][q][1], bf[0][q][2], bf[0][q][3]);
+#pragma unroll
+    for (int ks = 0; ks < kHD / 16; ++ks) {
+        const int cb = ks & 1;
+        if (ks + 1 < kHD / 16) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q)
+                ldsm_x4(kaddr + q * 16 * kRow * 2 + (ks + 1) * 32, bf[cb ^ 1][q][0], bf[cb ^ 1][q][1],
+                        bf[cb ^ 1][q][2], bf[cb ^ 1][q][3]);
+        }
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            mma(s[2 * q], qa[ks], bf[cb][q][0], bf[cb][q][1]);
+            mma(s[2 * q + 1], qa[ks], bf[cb][q][2], bf[cb][q][3]);
+        }
+    }
+}
+
+// O += P V over NQ 16-key steps (P from the S registers, rounded to bf16),
+// software-pipelined over the 8 column blocks of V in the same way.
+template <int NQ>
+__device__ __forceinline__ void pv_steps(float (&o)[kHD / 8][4], const float (&s)[kKC / 8][4],
+                                         uint32_t vaddr) {
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        uint32_t pa[4];
+        pa[0] = pack_bf16(s[2 * q][0], s[2 * q][1]);
+        pa[1] = pack_bf16(s[2 * q][2], s[2 * q][3]);
+        pa[2] = pack_bf16(s[2 * q + 1][0], s[2 * q + 1][1]);
+        pa[3] = pack_bf16(s[2 * q + 1][2], s[2 * q + 1][3]);
+        uint32_t bf[2][4];
+        ldsm_x4_t(vaddr + q * 16 * kRow * 2, bf[0][0], bf[0][1], bf[0][2], bf[0][3]);
+#pragma unroll
+        for (int np = 0; np < kHD / 16; ++np) {
+            const int cb = np & 1;
+            if (np + 1 < kHD / 16)
+                ldsm_x4_t(vaddr + q * 16 * kRow * 2 + (np + 1) * 32, bf[cb ^ 1][0], bf[cb ^ 1][1],
+                          bf[cb ^ 1][2], bf[cb ^ 1][3]);
+            mma(o[2 * np], pa, bf[cb][0], bf[cb][1]);
+            mma(o[2 * np + 1], pa, bf[cb][2], bf[cb][3]);
+        }
+    }
+}
+
 // A chunk of the key region: frame t, region rows rb + i S (i < nr; ri = rb
 // minus the region's first row), columns [c0, c0 + cw), nseg 16-slot segments
 // per row; key (i, j) sits in slot i * 16 nseg + j.
@@ -391,17 +444,11 @@ rope3d_na3d_kernel(const NAParams p) {
 #pragma unroll
             for (int n = 0; n < kKC / 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
             const uint32_t kaddr = smem_addr(Kb + ((mi >> 1) * 8 + rr) * kRow + (mi & 1) * 8);
-#pragma unroll
-            for (int ks = 0; ks < kHD / 16; ++ks) {
-#pragma unroll
-                for (int q = 0; q < kKC / 16; ++q) {
-                    if (q < nq) {
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(kaddr + q * 16 * kRow * 2 + ks * 32, b0, b1, b2, b3);
-                        mma(s[2 * q], qa[ks], b0, b1);
-                        mma(s[2 * q + 1], qa[ks], b2, b3);
-                    }
-                }
+            switch (nq) {   // 1 to kKC / 16 steps; two in most chunks
+                case 1: qk_steps<1>(s, qa, kaddr); break;
+                case 2: qk_steps<2>(s, qa, kaddr); break;
+                case 3: qk_steps<3>(s, qa, kaddr); break;
+                default: qk_steps<4>(s, qa, kaddr); break;
             }
 
             // ---- mask, online softmax. Every key of the region lies in each
@@ -485,22 +532,11 @@ rope3d_na3d_kernel(const NAParams p) {
 
             // ---- O += P V
             const uint32_t vaddr = smem_addr(Vb + (rr + (mi & 1) * 8) * kRow + (mi >> 1) * 8);
-#pragma unroll
-            for (int q = 0; q < kKC / 16; ++q) {
-                if (q < nq) {
-                    uint32_t pa[4];
-                    pa[0] = pack_bf16(s[2 * q][0], s[2 * q][1]);
-                    pa[1] = pack_bf16(s[2 * q][2], s[2 * q][3]);
-                    pa[2] = pack_bf16(s[2 * q + 1][0], s[2 * q + 1][1]);
-                    pa[3] = pack_bf16(s[2 * q + 1][2], s[2 * q + 1][3]);
-#pragma unroll
-                    for (int np = 0; np < kHD / 16; ++np) {
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4_t(vaddr + q * 16 * kRow * 2 + np * 32, b0, b1, b2, b3);
-                        mma(o[2 * np], pa, b0, b1);
-                        mma(o[2 * np + 1], pa, b2, b3);
-                    }
-                }
+            switch (nq) {
+                case 1: pv_steps<1>(o, s, vaddr); break;
+                case 2: pv_steps<2>(o, s, vaddr); break;
+                case 3: pv_steps<3>(o, s, vaddr); break;
+                default: pv_steps<4>(o, s, vaddr); break;
             }
         }
         if (kRope && c + 1 < n_chunks) rotate_k(nxt.t, buf ^ 1);
