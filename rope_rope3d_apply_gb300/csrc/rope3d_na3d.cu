@@ -32,6 +32,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <type_traits>
 
 #include "../../include/rope3d.h"
 #include "rope3d_internal.h"
@@ -439,26 +440,25 @@ rope3d_na3d_kernel(const NAParams p) {
             const uint16_t *Kb = sK + (buf * kKC + j0) * kRow;
             const uint16_t *Vb = sV + (buf * kKC + j0) * kRow;
 
-            // ---- S = Q K^T, step q covering slots [16 q, 16 q + 16)
-            float s[kKC / 8][4];
-#pragma unroll
-            for (int n = 0; n < kKC / 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
             const uint32_t kaddr = smem_addr(Kb + ((mi >> 1) * 8 + rr) * kRow + (mi & 1) * 8);
-            switch (nq) {   // 1 to kKC / 16 steps; two in most chunks
-                case 1: qk_steps<1>(s, qa, kaddr); break;
-                case 2: qk_steps<2>(s, qa, kaddr); break;
-                case 3: qk_steps<3>(s, qa, kaddr); break;
-                default: qk_steps<4>(s, qa, kaddr); break;
-            }
-
-            // ---- mask, online softmax. Every key of the region lies in each
-            // row's t window (the block is one frame): only h and w are tested.
-            int hk = cur.rb + ilo * S, seg = 0;
-            float qmax0[kKC / 16], qmax1[kKC / 16];
+            const uint32_t vaddr = smem_addr(Vb + (rr + (mi & 1) * 8) * kRow + (mi >> 1) * 8);
+            // the chunk's work for NQ 16-key steps (compiled for 1 to kKC / 16;
+            // two in most chunks), step q covering slots [16 q, 16 q + 16)
+            auto steps = [&](auto nq_const) {
+                constexpr int NQ = decltype(nq_const)::value;
+                // ---- S = Q K^T
+                float s[kKC / 8][4];
 #pragma unroll
-            for (int q = 0; q < kKC / 16; ++q) {
-                qmax0[q] = qmax1[q] = -INFINITY;
-                if (q < nq) {
+                for (int n = 0; n < 2 * NQ; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+                qk_steps<NQ>(s, qa, kaddr);
+
+                // ---- mask, online softmax. Every key of the region lies in
+                // each row's t window (the block is one frame): only h and w
+                // are tested.
+                int hk = cur.rb + ilo * S, seg = 0;
+                float cmax0 = -INFINITY, cmax1 = -INFINITY;
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
                     const bool row0 = rvalid0 && unsigned(hk - wh0) < unsigned(p.kh);
                     const bool row1 = rvalid1 && unsigned(hk - wh1) < unsigned(p.kh);
                     const uint32_t cb = colbits >> (4 * seg);
@@ -469,47 +469,45 @@ rope3d_na3d_kernel(const NAParams p) {
                         const bool ok = col && (((e >> 1) & 1) ? row1 : row0);
                         x = ok ? x * p.scale_log2 : -INFINITY;
                     }
-                    qmax0[q] = fmaxf(fmaxf(s[2 * q][0], s[2 * q][1]), fmaxf(s[2 * q + 1][0], s[2 * q + 1][1]));
-                    qmax1[q] = fmaxf(fmaxf(s[2 * q][2], s[2 * q][3]), fmaxf(s[2 * q + 1][2], s[2 * q + 1][3]));
+                    cmax0 = fmaxf(cmax0, fmaxf(fmaxf(s[2 * q][0], s[2 * q][1]),
+                                               fmaxf(s[2 * q + 1][0], s[2 * q + 1][1])));
+                    cmax1 = fmaxf(cmax1, fmaxf(fmaxf(s[2 * q][2], s[2 * q][3]),
+                                               fmaxf(s[2 * q + 1][2], s[2 * q + 1][3])));
                     if (++seg == cur.nseg) {
                         seg = 0;
                         hk += S;
                     }
                 }
-            }
-            float cmax0 = fmaxf(fmaxf(qmax0[0], qmax0[1]), fmaxf(qmax0[2], qmax0[3]));
-            float cmax1 = fmaxf(fmaxf(qmax1[0], qmax1[1]), fmaxf(qmax1[2], qmax1[3]));
-            cmax0 = fmaxf(cmax0, __shfl_xor_sync(0xffffffffu, cmax0, 1));
-            cmax0 = fmaxf(cmax0, __shfl_xor_sync(0xffffffffu, cmax0, 2));
-            cmax1 = fmaxf(cmax1, __shfl_xor_sync(0xffffffffu, cmax1, 1));
-            cmax1 = fmaxf(cmax1, __shfl_xor_sync(0xffffffffu, cmax1, 2));
-            // Weights are exp2(score - ref) with ref a running reference per
-            // row. The reference moves up to the row's maximum (and O and l
-            // are rescaled) only when the maximum exceeds it by more than
-            // kLazy, so weights stay below 2^kLazy; a row with no key yet has
-            // reference -inf and subtracts 0 (every score is -inf there).
-            const float mn0 = fmaxf(m0, cmax0), mn1 = fmaxf(m1, cmax1);
-            if (__any_sync(0xffffffffu, mn0 > m0 + kLazy || mn1 > m1 + kLazy)) {
-                const float corr0 = m0 == -INFINITY ? 0.f : ex2(m0 - mn0);
-                const float corr1 = m1 == -INFINITY ? 0.f : ex2(m1 - mn1);
-                m0 = mn0;
-                m1 = mn1;
-                l0 *= corr0;
-                l1 *= corr1;
+                cmax0 = fmaxf(cmax0, __shfl_xor_sync(0xffffffffu, cmax0, 1));
+                cmax0 = fmaxf(cmax0, __shfl_xor_sync(0xffffffffu, cmax0, 2));
+                cmax1 = fmaxf(cmax1, __shfl_xor_sync(0xffffffffu, cmax1, 1));
+                cmax1 = fmaxf(cmax1, __shfl_xor_sync(0xffffffffu, cmax1, 2));
+                // Weights are exp2(score - ref) with ref a running reference
+                // per row. The reference moves up to the row's maximum (and O
+                // and l are rescaled) only when the maximum exceeds it by more
+                // than kLazy, so weights stay below 2^kLazy; a row with no key
+                // yet has reference -inf and subtracts 0 (every score is -inf
+                // there).
+                const float mn0 = fmaxf(m0, cmax0), mn1 = fmaxf(m1, cmax1);
+                if (__any_sync(0xffffffffu, mn0 > m0 + kLazy || mn1 > m1 + kLazy)) {
+                    const float corr0 = m0 == -INFINITY ? 0.f : ex2(m0 - mn0);
+                    const float corr1 = m1 == -INFINITY ? 0.f : ex2(m1 - mn1);
+                    m0 = mn0;
+                    m1 = mn1;
+                    l0 *= corr0;
+                    l1 *= corr1;
 #pragma unroll
-                for (int n = 0; n < kHD / 8; ++n) {
-                    o[n][0] *= corr0;
-                    o[n][1] *= corr0;
-                    o[n][2] *= corr1;
-                    o[n][3] *= corr1;
+                    for (int n = 0; n < kHD / 8; ++n) {
+                        o[n][0] *= corr0;
+                        o[n][1] *= corr0;
+                        o[n][2] *= corr1;
+                        o[n][3] *= corr1;
+                    }
                 }
-            }
-            const float ms0 = m0 == -INFINITY ? 0.f : m0, ms1 = m1 == -INFINITY ? 0.f : m1;
-            float qs0[kKC / 16], qs1[kKC / 16];
+                const float ms0 = m0 == -INFINITY ? 0.f : m0, ms1 = m1 == -INFINITY ? 0.f : m1;
+                float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-            for (int q = 0; q < kKC / 16; ++q) {
-                qs0[q] = qs1[q] = 0.f;
-                if (q < nq) {
+                for (int q = 0; q < NQ; ++q) {
 #pragma unroll
                     for (int n = 2 * q; n < 2 * q + 2; ++n) {
                         s[n][0] = ex2(s[n][0] - ms0);
@@ -517,26 +515,24 @@ rope3d_na3d_kernel(const NAParams p) {
                         s[n][2] = ex2(s[n][2] - ms1);
                         s[n][3] = ex2(s[n][3] - ms1);
                     }
-                    qs0[q] = (s[2 * q][0] + s[2 * q][1]) + (s[2 * q + 1][0] + s[2 * q + 1][1]);
-                    qs1[q] = (s[2 * q][2] + s[2 * q][3]) + (s[2 * q + 1][2] + s[2 * q + 1][3]);
+                    ps0 += (s[2 * q][0] + s[2 * q][1]) + (s[2 * q + 1][0] + s[2 * q + 1][1]);
+                    ps1 += (s[2 * q][2] + s[2 * q][3]) + (s[2 * q + 1][2] + s[2 * q + 1][3]);
                 }
-            }
-            float ps0 = (qs0[0] + qs0[1]) + (qs0[2] + qs0[3]);
-            float ps1 = (qs1[0] + qs1[1]) + (qs1[2] + qs1[3]);
-            ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
-            ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
-            ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
-            ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
-            l0 += ps0;
-            l1 += ps1;
+                ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
+                ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
+                ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
+                ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
+                l0 += ps0;
+                l1 += ps1;
 
-            // ---- O += P V
-            const uint32_t vaddr = smem_addr(Vb + (rr + (mi & 1) * 8) * kRow + (mi >> 1) * 8);
+                // ---- O += P V
+                pv_steps<NQ>(o, s, vaddr);
+            };
             switch (nq) {
-                case 1: pv_steps<1>(o, s, vaddr); break;
-                case 2: pv_steps<2>(o, s, vaddr); break;
-                case 3: pv_steps<3>(o, s, vaddr); break;
-                default: pv_steps<4>(o, s, vaddr); break;
+                case 1: steps(std::integral_constant<int, 1>{}); break;
+                case 2: steps(std::integral_constant<int, 2>{}); break;
+                case 3: steps(std::integral_constant<int, 3>{}); break;
+                default: steps(std::integral_constant<int, 4>{}); break;
             }
         }
         if (kRope && c + 1 < n_chunks) rotate_k(nxt.t, buf ^ 1);
