@@ -96,20 +96,45 @@ __device__ __forceinline__ uint32_t rot_word(uint32_t word, float c, float s) {
     return out;
 }
 
-// Where a thread's 8 channels [8 cv, 8 cv + 8) read the tables. Every chunk of
-// the split is a multiple of 8 channels, so the 4 pairs lie in one axis and
-// the entries of position pos are 4 consecutive (cos, sin) at base + pos *
-// stride: a multiple of 4, so two aligned 16-byte loads.
+// The tables in shared memory. Each position's row of an axis holds its P
+// (cos, sin) entries split in two halves: the first two entries of every
+// group of four pairs, then the last two. A thread's group g of a row is
+// then one 16-byte load at 2 g and one at P / 2 + 2 g, and the threads of a
+// warp, which take consecutive groups, read consecutive 16-byte words
+// (interleaved groups put their loads 32 bytes apart: bank conflicts).
+//
+// Where a thread's 8 channels [8 cv, 8 cv + 8) read: every chunk of the
+// split is a multiple of 8 channels, so the 4 pairs (group g of its axis) lie
+// in one axis; the row of position pos starts at off + pos * P.
 struct TabSlot {
-    uint32_t base, stride;
-    int axis;   // 0: t, 1: h, 2: w
+    uint32_t base, stride, half;   // off + 2 g, P, P / 2
+    int axis;                      // 0: t, 1: h, 2: w
 };
 
 __device__ __forceinline__ TabSlot tab_slot(const NAParams &p, int cv) {
     const uint32_t pair = 4 * cv;
-    if (pair < p.pT) return {pair, p.pT, 0};
-    if (pair < p.pT + p.pH) return {p.offH + (pair - p.pT), p.pH, 1};
-    return {p.offW + (pair - p.pT - p.pH), p.pW, 2};
+    if (pair < p.pT) return {pair / 2, p.pT, p.pT / 2, 0};
+    if (pair < p.pT + p.pH) return {p.offH + (pair - p.pT) / 2, p.pH, p.pH / 2, 1};
+    return {p.offW + (pair - p.pT - p.pH) / 2, p.pW, p.pW / 2, 2};
+}
+
+// Copy the tables into shared memory in the split layout above: one group
+// of four pairs (two 16-byte words) per step.
+__device__ __forceinline__ void stage_tables(const NAParams &p, float2 *dst, int tid, int nthreads) {
+    const uint32_t groups = p.tab_len / 4;
+    for (uint32_t gi = tid; gi < groups; gi += nthreads) {
+        const uint32_t e = 4 * gi;   // first entry of the group
+        uint32_t off, P;
+        if (e < p.offH) off = 0, P = p.pT;
+        else if (e < p.offW) off = p.offH, P = p.pH;
+        else off = p.offW, P = p.pW;
+        const uint32_t pos = (e - off) / P, pair = (e - off) - pos * P;
+        const uint32_t row = off + pos * P;
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(p.tab + e));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(p.tab + e + 2));
+        *reinterpret_cast<float4 *>(dst + row + pair / 2) = a;
+        *reinterpret_cast<float4 *>(dst + row + P / 2 + pair / 2) = b;
+    }
 }
 
 // Rotate the 8 channels of a TabSlot for a token at grid position (t, h, w).
@@ -118,7 +143,7 @@ __device__ __forceinline__ uint4 rot_vec(uint4 v, const float2 *tab, const TabSl
     const int pos = ts.axis == 0 ? t : (ts.axis == 1 ? h : w);
     const uint32_t idx = ts.base + uint32_t(pos) * ts.stride;
     const float4 a = *reinterpret_cast<const float4 *>(tab + idx);
-    const float4 b = *reinterpret_cast<const float4 *>(tab + idx + 2);
+    const float4 b = *reinterpret_cast<const float4 *>(tab + idx + ts.half);
     return make_uint4(rot_word(v.x, a.x, a.y), rot_word(v.y, a.z, a.w), rot_word(v.z, b.x, b.y),
                       rot_word(v.w, b.z, b.w));
 }
@@ -356,7 +381,7 @@ rope3d_na3d_kernel(const NAParams p) {
 
     // ---- prologue: tables, the Q tile, the first chunk
     if (kRope)
-        for (uint32_t i = tid; i < p.tab_len; i += kThreads) sTab[i] = p.tab[i];
+        stage_tables(p, sTab, tid, kThreads);
     uint4 qreg[kVecs];
 #pragma unroll
     for (int m = 0; m < kVecs; ++m) {
