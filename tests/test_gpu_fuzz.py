@@ -1,7 +1,9 @@
 """Seeded random shapes through every GPU entry point, each compared with the
 oracle bit for bit: grids, head counts, splits, dtypes, bases, pointer
-offsets, padded (strided) views, in-place calls, patch sizes and NeoX head
-layouts drawn from a fixed generator, so that every run checks the same cases."""
+offsets, padded (strided) views, in-place calls, patch sizes, NeoX head
+layouts and neighbourhood-attention windows drawn from a fixed generator, so
+that every run checks the same cases (the attention against the float64
+oracle within its derived bound, everything else bit for bit)."""
 from __future__ import annotations
 
 import numpy as np
@@ -156,3 +158,42 @@ def test_fuzz_neox(seed):
     torch.cuda.synchronize()
     assert np.array_equal(bits(to_np(qo)), bits(oracle.rope_neox(q_np, tokens, qh, hd, positions, cache, dtype).reshape(-1)))
     assert np.array_equal(bits(to_np(ko)), bits(oracle.rope_neox(k_np, tokens, kh, hd, positions, cache, dtype).reshape(-1)))
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_fuzz_na3d(seed):
+    """Neighbourhood attention on random grids, heads, batches, splits and
+    odd windows, with and without the rotation: within the derived bound of
+    the float64 oracle, and the fused kernel equal to the unfused pair."""
+    g = np.random.Generator(np.random.PCG64(8000 + seed))
+    B = int(g.integers(1, 3))
+    T, H, W = int(g.integers(1, 6)), int(g.integers(1, 21)), int(g.integers(1, 21))
+    heads = int(g.integers(1, 4))
+    dT = 8 * int(g.integers(1, 7))
+    dH = 8 * int(g.integers(1, 15 - dT // 8))
+    split = (dT, dH, 128 - dT - dH)
+    kernel = tuple(int(2 * g.integers(0, (L + 1) // 2) + 1) for L in (T, H, W))
+    rope = bool(g.integers(0, 2))
+    shape6 = (B, T, H, W, heads, 128)
+    n = int(np.prod(shape6))
+    q_np, k_np, v_np = (draw(n, 9000 + seed, i, "bf16") for i in range(3))
+    shp = (B, T * H * W, heads, 128)
+    q, k, v = (np_to_torch(a, "bf16").reshape(shp).to(DEV) for a in (q_np, k_np, v_np))
+    tabs = r.rope3d_build_tables(T, H, W, split)
+    out = r.rope3d_na3d(q, k, v, tabs, kernel, apply_rope=rope)
+    if rope:
+        qr, kr = r.rope3d_apply_pair(q, k, tabs)
+        unfused = r.rope3d_na3d(qr, kr, v, tabs, kernel, apply_rope=False)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), unfused.view(torch.int16))
+    torch.cuda.synchronize()
+    to64 = lambda b: (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)  # noqa: E731
+    got = to64(to_np(out)).reshape(shape6)
+    otabs = oracle.tables(T, H, W, split)
+    ref = oracle.rope_na3d(q_np, k_np, v_np, shape6, split, otabs, kernel, rope=rope)
+    qr_np = oracle.rope3d(q_np, shape6, split, otabs) if rope else q_np
+    kr_np = oracle.rope3d(k_np, shape6, split, otabs) if rope else k_np
+    absv = oracle.na3d(to64(qr_np), to64(kr_np), np.abs(to64(v_np)), shape6, kernel)
+    bound = 2.0 ** -7 * absv + 2.0 ** -8 * np.abs(ref) + 1e-6
+    assert np.all(np.abs(got - ref) <= bound), (seed, shape6, split, kernel, rope)
+    tabs.close()

@@ -45,6 +45,7 @@ CASES = [
     ((1, 4, 16, 24, 1), (32, 48, 48), (3, 7, 7)),
     ((1, 2, 6, 80, 1), (32, 48, 48), (1, 3, 67)),      # a region row of 74 keys: split in columns
     ((1, 2, 12, 40, 1), (32, 48, 48), (1, 9, 33)),     # region rows of 40 keys: three 16-key steps
+    ((2, 4, 13, 11, 3), (16, 56, 56), (3, 5, 7)),      # two batches, three heads, odd grid, split
 ]
 
 
