@@ -254,11 +254,18 @@ def smi_gpu_id(local: int) -> str:
         return ids[local] if local < len(ids) else str(local)
 
 
-def oracle_sample_step(w: synthetic.Workload, frames: int, rows: int, cache: dict):
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def oracle_sample_step(w: synthetic.Workload, frames: int, rows: int, cache: dict, pool=None,
+                       jobs: int = 1):
     """One oracle pass over Q and K of a leading sub-grid of batch 0: the first
     `rows` rows (h) of frame 0 when frames == 1, else the first `frames` whole
     frames. Those tokens use the same table rows as in the full workload, so
-    the sub-grid is the same computation as that part of the workload.
+    the sub-grid is the same computation as that part of the workload. With a
+    thread pool, frame 0's rows are cut into `jobs` blocks (each with its rows
+    of the H table, so positions are unchanged) that run concurrently.
     Returns the algorithmic bytes of the pass."""
     import oracle
 
@@ -271,8 +278,22 @@ def oracle_sample_step(w: synthetic.Workload, frames: int, rows: int, cache: dic
         tabs = oracle.tables(frames, rows, w.W, w.split, w.base)
         cache[key] = (shape, q, k, tabs)
     shape, q, k, tabs = cache[key]
-    oracle.rope3d(q, shape, w.split, tabs)
-    oracle.rope3d(k, shape, w.split, tabs)
+    if pool is None or frames != 1 or jobs <= 1:
+        oracle.rope3d(q, shape, w.split, tabs)
+        oracle.rope3d(k, shape, w.split, tabs)
+    else:
+        per_row = w.W * w.heads * w.head_dim
+        (tt, (ch, sh), tw) = tabs
+        bounds = np.linspace(0, rows, min(jobs, rows) + 1).astype(int)
+
+        def job(i):
+            r0, r1 = int(bounds[i]), int(bounds[i + 1])
+            sub = (tt, (ch[r0:r1], sh[r0:r1]), tw)
+            shp = (1, 1, r1 - r0, w.W, w.heads, w.head_dim)
+            oracle.rope3d(q[r0 * per_row:r1 * per_row], shp, w.split, sub)
+            oracle.rope3d(k[r0 * per_row:r1 * per_row], shp, w.split, sub)
+
+        list(pool.map(job, range(len(bounds) - 1)))
     return 4 * q.size * w.elem_bytes + sum(8 * n * (d // 2) for n, d in zip(shape[1:4], w.split))
 
 
@@ -306,9 +327,33 @@ def cpu_baseline(w: synthetic.Workload, seconds: float, q=None, k=None) -> dict:
     moved = 4 * n * w.elem_bytes + sum(8 * m * (d // 2) for m, d in zip((t, w.H, w.W), w.split))
     what = (f"the whole workload ({b} x {t} frames)" if (b, t) == (w.B, w.T)
             else f"{b} whole batch(es)" if t == w.T else f"frames 0..{t - 1} of batch 0")
-    return {"value": moved / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+    line = {"value": moved / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": (f"{what}: {b * t * w.H * w.W} tokens x {w.heads} heads, Q and K, "
                        f"{moved / 1e9:.3f} GB algorithmic, in {dt:.2f} s on one thread")}
+    # The same sample on every host core: the unchanged oracle, one frame per
+    # job (its T-table row sliced, so positions are those of the full grid);
+    # the C oracle runs without the interpreter lock.
+    from concurrent.futures import ThreadPoolExecutor
+
+    cores = host_cores()
+    (ct, st), th, tw = tabs
+    one_frame = (1, 1, w.H, w.W, w.heads, w.head_dim)
+
+    def frame_job(i):
+        bi, ti = divmod(i, t)
+        base = (bi * w.T + ti) * per_frame
+        ft = ((ct[ti:ti + 1], st[ti:ti + 1]), th, tw)
+        oracle.rope3d(q[base:base + per_frame], one_frame, w.split, ft)
+        oracle.rope3d(k[base:base + per_frame], one_frame, w.split, ft)
+
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        t0 = time.perf_counter()
+        list(ex.map(frame_job, range(b * t)))
+        dt_all = time.perf_counter() - t0
+    line["all_cores"] = {"value": moved / dt_all / 1e9, "unit": UNIT, "cores": cores,
+                         "sample": f"the same sample, one frame per job, {cores} threads, "
+                                   f"in {dt_all:.2f} s"}
+    return line
 
 
 # ---------------------------------------------------------------------------
@@ -322,30 +367,36 @@ def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    from concurrent.futures import ThreadPoolExecutor
+
+    cores = host_cores()
     cache = {}
     oracle_sample_step(w, 1, 1, cache)  # inputs drawn once, outside the estimate
     t0 = time.perf_counter()
     oracle_sample_step(w, 1, 1, cache)
     per_row = time.perf_counter() - t0
     budget = 120.0 / max(1, args.steps + args.warmup)
-    rows = int(max(1, min(w.H, budget / max(per_row, 1e-6))))
-    for _ in range(max(args.warmup, 0)):
-        oracle_sample_step(w, 1, rows, cache)
-    t0 = time.perf_counter()
-    moved = 0
-    for _ in range(args.steps):
-        moved += oracle_sample_step(w, 1, rows, cache)
-    dt = time.perf_counter() - t0
+    # rows per step: about the budget's worth of work across the cores
+    rows = int(max(1, min(w.H, cores * budget / max(per_row, 1e-6))))
+    with ThreadPoolExecutor(max_workers=cores) as pool:
+        for _ in range(max(args.warmup, 0)):
+            oracle_sample_step(w, 1, rows, cache, pool, cores)
+        t0 = time.perf_counter()
+        moved = 0
+        for _ in range(args.steps):
+            moved += oracle_sample_step(w, 1, rows, cache, pool, cores)
+        dt = time.perf_counter() - t0
     value = moved / dt / 1e9
+    used = min(cores, rows)
     sample = (f"each step: rows h=0..{rows - 1} of frame 0 of batch 0 ({rows * w.W} tokens x "
-              f"{w.heads} heads, Q and K), oracle single thread")
+              f"{w.heads} heads, Q and K), oracle in {used} concurrent row blocks")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * dt / max(args.steps, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_config(w),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }

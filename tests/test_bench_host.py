@@ -23,9 +23,43 @@ def test_reference_arm_prints_one_json_line():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["cores"] <= bench_host_cores()
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["steps"] == 2 and d["higher_is_better"] is True
+
+
+def bench_host_cores():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    return bench.host_cores()
+
+
+def test_cpu_baseline_single_and_all_cores():
+    """cpu_baseline times the oracle on one thread and, on the same sample,
+    on every host core (one frame per job); the per-frame jobs compute
+    exactly what the single pass computes."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    import oracle
+    import synthetic
+
+    w = synthetic.WORKLOADS["stage0"]
+    line = bench.cpu_baseline(w, 0.5)
+    assert line["cores"] == 1 and line["value"] > 0
+    assert line["all_cores"]["cores"] == bench.host_cores() and line["all_cores"]["value"] > 0
+    q, _ = synthetic.qk(w)
+    q = q.reshape(-1)
+    tabs = oracle.tables(w.T, w.H, w.W, w.split, w.base)
+    full = oracle.rope3d(q, (w.B, w.T, w.H, w.W, w.heads, w.head_dim), w.split, tabs)
+    per_frame = w.H * w.W * w.heads * w.head_dim
+    (ct, st), th, tw = tabs
+    frames = [oracle.rope3d(q[i * per_frame:(i + 1) * per_frame], (1, 1, w.H, w.W, w.heads, w.head_dim),
+                            w.split, ((ct[i:i + 1], st[i:i + 1]), th, tw)) for i in range(w.T)]
+    assert np.array_equal(np.concatenate(frames), full.reshape(-1))
 
 
 def test_launch_count():
