@@ -475,6 +475,20 @@ int rope3d_testing_host_tables(int32_t on);
  */
 int rope3d_testing_max_units_per_launch(int64_t n);
 
+/*
+ * rope3d_debug_bounds -- the bounds checks of a debug build. A library built
+ * with -DROPE3D_DEBUG_BOUNDS=1 (build(debug_bounds=True)) checks every index
+ * its kernels compute (table entries, strided and permuted offsets, token
+ * and key positions, shared-memory slots) before the access it guards; a
+ * failed check adds one to an error count and skips the access, so the kernel
+ * finishes. This takes the place of a memory checker where none can run.
+ *   errors  out: failed checks since the last reset (0 in a normal build)
+ *   reset   nonzero: clear the count after reading it
+ * Returns 1 when the library was built with the checks, 0 when not.
+ * Synchronises the device (debug builds). Errors: NULL, CUDA.
+ */
+int rope3d_debug_bounds(int64_t *errors, int32_t reset);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,11 +30,13 @@ __all__ = [
     "rope3d_apply_pair_strided", "rope3d_preflight_strided", "view_strides",
     "rope3d_patchify", "rope3d_unpatchify", "rope3d_patchify_check", "rope3d_patchify_last_kernel",
     "rope3d_apply_neox", "rope3d_neox_check", "rope3d_neox_cache_host", "rope3d_neox_last_kernel",
-    "rope3d_na3d",
+    "rope3d_na3d", "rope3d_debug_bounds",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "_build", "librope3d.so")
+# The library this module loads; ROPE3D_LIB names another build of it (for
+# example the bounds-checking debug build) to load instead.
+LIB_PATH = os.environ.get("ROPE3D_LIB") or os.path.join(HERE, "_build", "librope3d.so")
 
 BF16, F32, F16 = 0, 1, 2
 GATE_OFF, GATE_FIRST = 0, 1
@@ -83,6 +85,7 @@ def _declare(lib):
         "rope3d_testing_fastdiv": ([i64, i64], i64),
         "rope3d_testing_host_tables": ([i32], c.c_int),
         "rope3d_testing_max_units_per_launch": ([i64], c.c_int),
+        "rope3d_debug_bounds": ([vp, i32], c.c_int),
         "rope3d_apply_pair_noalloc": ([vp, vp, vp, vp] + [i64] * 6 + [vp, dbl, i32, vp], c.c_int),
         "rope3d_apply_pair_strided": ([vp, vp, vp, vp, vp] + [i64] * 6 + [vp, i32] + [vp] * 4 + [vp],
                                       c.c_int),
@@ -582,6 +585,16 @@ def rope3d_testing_fastdiv(n: int, d: int) -> int:
 def rope3d_testing_max_units_per_launch(n: int):
     _check(load_library().rope3d_testing_max_units_per_launch(int(n)),
            "rope3d_testing_max_units_per_launch")
+
+
+def rope3d_debug_bounds(reset: bool = True):
+    """(built_with_checks, failed_checks): the bounds checks of a debug build
+    (see build(debug_bounds=True)); the count is cleared when reset."""
+    n = ctypes.c_int64()
+    rc = load_library().rope3d_debug_bounds(ctypes.byref(n), 1 if reset else 0)
+    if rc < 0:
+        _check(rc, "rope3d_debug_bounds")
+    return bool(rc), int(n.value)
 
 
 def rope3d_last_launch():

@@ -1211,6 +1211,18 @@ extern "C" int rope3d_apply_pair_host(const void *q, const void *k, void *q_out,
     return gate_record(key, bad);
 }
 
+extern "C" int rope3d_debug_bounds(int64_t *errors, int32_t reset) {
+    if (!errors) return ROPE3D_ERR_NULL;
+    int64_t total = 0;
+    for (int64_t n : {rope3d::kernels_bound_errors(reset != 0), rope3d::patchify_bound_errors(reset != 0),
+                      rope3d::neox_bound_errors(reset != 0), rope3d::na3d_bound_errors(reset != 0)}) {
+        if (n < 0) return ROPE3D_ERR_CUDA;
+        total += n;
+    }
+    *errors = total;
+    return ROPE3D_DEBUG_BOUNDS ? 1 : 0;
+}
+
 extern "C" int rope3d_release_scratch(void) {
     std::lock_guard<std::mutex> lock(g_pipe_mutex);
     for (auto &kv : g_pipes) destroy_pipe(kv.second);

@@ -100,6 +100,22 @@ int check_call_without_tables(const void *q, const void *k, const void *q_out, c
 
 }  // namespace rope3d
 
+// Debug builds compile every kernel with -DROPE3D_DEBUG_BOUNDS=1: each computed
+// index is checked before the access it guards; a failed check counts in the
+// kernel file's error word and skips the access.
+#ifndef ROPE3D_DEBUG_BOUNDS
+#define ROPE3D_DEBUG_BOUNDS 0
+#endif
+
+namespace rope3d {
+// Per kernel file: the bound-check error count (0 without the checks), -1 on a
+// CUDA error; reset clears it.
+int64_t kernels_bound_errors(bool reset);
+int64_t patchify_bound_errors(bool reset);
+int64_t neox_bound_errors(bool reset);
+int64_t na3d_bound_errors(bool reset);
+}  // namespace rope3d
+
 struct rope3d_tables;
 namespace rope3d {
 // The device layout of a table handle: the float2 (cos, sin) buffer, its

@@ -92,11 +92,33 @@ struct KParams {
 };
 
 // Element strides of (batch, t, h, w, head) for Q, K, Q_out, K_out, and the
-// batch index of the launch's first row (strided kernels only).
+// batch index of the launch's first row (strided kernels only); lim: the bytes
+// each of the four buffers spans from its pointer, for the bounds checks of
+// debug builds.
 struct KStrides {
     long long s[4][5];
     uint32_t b0;
+    unsigned long long lim[4];
 };
+
+// Debug builds (-DROPE3D_DEBUG_BOUNDS=1) check each computed index before the
+// access it guards: a failed check adds one to this file's error word and
+// skips the access (never a trap); rope3d_debug_bounds() reads the words.
+// Without the flag every check is `true` and compiles away.
+#if ROPE3D_DEBUG_BOUNDS
+__device__ unsigned int g_bound_errors;
+__device__ __forceinline__ bool bound_ok(unsigned long long off, unsigned long long len,
+                                         unsigned long long lim) {
+    if (off + len <= lim) return true;
+    atomicAdd(&g_bound_errors, 1u);
+    return false;
+}
+#else
+__device__ __forceinline__ constexpr bool bound_ok(unsigned long long, unsigned long long,
+                                                   unsigned long long) {
+    return true;
+}
+#endif
 
 __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) {
     return (__umulhi(n, f.mul) + n) >> f.shift;
@@ -265,8 +287,9 @@ __device__ __forceinline__ const float2 *stage_tables(const KParams &p, float2 *
 }
 
 template <bool kSmem>
-__device__ __forceinline__ float4 tab4(const float2 *tab, uint32_t idx) {
+__device__ __forceinline__ float4 tab4(const float2 *tab, uint32_t idx, uint32_t len) {
     // idx is a multiple of 2 entries: one 16-byte load of two (cos, sin) entries
+    if (!bound_ok(idx, 2, len)) return make_float4(0.f, 0.f, 0.f, 0.f);
     if constexpr (kSmem) {
         return *reinterpret_cast<const float4 *>(tab + idx);
     } else {
@@ -275,7 +298,8 @@ __device__ __forceinline__ float4 tab4(const float2 *tab, uint32_t idx) {
 }
 
 template <bool kSmem>
-__device__ __forceinline__ float2 tab1(const float2 *tab, uint32_t idx) {
+__device__ __forceinline__ float2 tab1(const float2 *tab, uint32_t idx, uint32_t len) {
+    if (!bound_ok(idx, 1, len)) return make_float2(0.f, 0.f);
     if constexpr (kSmem) {
         return tab[idx];
     } else {
@@ -322,8 +346,8 @@ rope3d_vec16_kernel(const KParams p, const KStrides) {
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const float4 cs01 = tab4<kSmem>(tab, idx[u]);
-            const float4 cs23 = kType != ROPE3D_F32 ? tab4<kSmem>(tab, idx[u] + 2) : cs01;
+            const float4 cs01 = tab4<kSmem>(tab, idx[u], p.tab_len);
+            const float4 cs23 = kType != ROPE3D_F32 ? tab4<kSmem>(tab, idx[u] + 2, p.tab_len) : cs01;
             st_stream_v4(qo + v + u * stride, rotate_vec<kType>(qv[u], cs01, cs23));
             st_stream_v4(ko + v + u * stride, rotate_vec<kType>(kv[u], cs01, cs23));
         }
@@ -336,8 +360,8 @@ rope3d_vec16_kernel(const KParams p, const KStrides) {
         const uint32_t r = v - row * p.per_row.d;
         const uint32_t g = r - fdiv(r, p.per_head) * p.per_head.d;
         const uint32_t i = table_index(p, grid_pos(p, row), g * kPairsPerVec);
-        const float4 cs01 = tab4<kSmem>(tab, i);
-        const float4 cs23 = kType != ROPE3D_F32 ? tab4<kSmem>(tab, i + 2) : cs01;
+        const float4 cs01 = tab4<kSmem>(tab, i, p.tab_len);
+        const float4 cs23 = kType != ROPE3D_F32 ? tab4<kSmem>(tab, i + 2, p.tab_len) : cs01;
         st_stream_v4(qo + v, rotate_vec<kType>(qv, cs01, cs23));
         st_stream_v4(ko + v, rotate_vec<kType>(kv, cs01, cs23));
     }
@@ -394,33 +418,33 @@ rope3d_vec16_strided_kernel(const KParams p, const KStrides st) {
         for (int u = 0; u < kStridedUnroll; ++u) {
             x[u] = where(v + u * stride);
             const uint32_t c = x[u].g * kElemsPerVec;
-            qv[u] = ld_coherent_v4(q + off(0, x[u].pos, x[u].head, c));
-            kv[u] = ld_coherent_v4(k + off(1, x[u].pos, x[u].head, c));
+            const long long oq = off(0, x[u].pos, x[u].head, c), ok = off(1, x[u].pos, x[u].head, c);
+            qv[u] = bound_ok(oq, 16, st.lim[0]) ? ld_coherent_v4(q + oq) : make_uint4(0, 0, 0, 0);
+            kv[u] = bound_ok(ok, 16, st.lim[1]) ? ld_coherent_v4(k + ok) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < kStridedUnroll; ++u) {
             const uint32_t c = x[u].g * kElemsPerVec;
             const uint32_t i = table_index(p, x[u].pos, x[u].g * kPairsPerVec);
-            const float4 cs01 = tab4<kSmem>(tab, i);
-            const float4 cs23 = kType != ROPE3D_F32 ? tab4<kSmem>(tab, i + 2) : cs01;
-            st_stream_v4(qo + off(2, x[u].pos, x[u].head, c),
-                         rotate_vec<kType>(qv[u], cs01, cs23));
-            st_stream_v4(ko + off(3, x[u].pos, x[u].head, c),
-                         rotate_vec<kType>(kv[u], cs01, cs23));
+            const float4 cs01 = tab4<kSmem>(tab, i, p.tab_len);
+            const float4 cs23 = kType != ROPE3D_F32 ? tab4<kSmem>(tab, i + 2, p.tab_len) : cs01;
+            const long long o2 = off(2, x[u].pos, x[u].head, c), o3 = off(3, x[u].pos, x[u].head, c);
+            if (bound_ok(o2, 16, st.lim[2])) st_stream_v4(qo + o2, rotate_vec<kType>(qv[u], cs01, cs23));
+            if (bound_ok(o3, 16, st.lim[3])) st_stream_v4(ko + o3, rotate_vec<kType>(kv[u], cs01, cs23));
         }
     }
     for (; v < p.units; v += stride) {
         const Where x = where(v);
         const uint32_t c = x.g * kElemsPerVec;
-        const uint4 qv = ld_coherent_v4(q + off(0, x.pos, x.head, c));
-        const uint4 kv = ld_coherent_v4(k + off(1, x.pos, x.head, c));
+        const long long oq = off(0, x.pos, x.head, c), ok = off(1, x.pos, x.head, c);
+        const uint4 qv = bound_ok(oq, 16, st.lim[0]) ? ld_coherent_v4(q + oq) : make_uint4(0, 0, 0, 0);
+        const uint4 kv = bound_ok(ok, 16, st.lim[1]) ? ld_coherent_v4(k + ok) : make_uint4(0, 0, 0, 0);
         const uint32_t i = table_index(p, x.pos, x.g * kPairsPerVec);
-        const float4 cs01 = tab4<kSmem>(tab, i);
-        const float4 cs23 = kType != ROPE3D_F32 ? tab4<kSmem>(tab, i + 2) : cs01;
-        st_stream_v4(qo + off(2, x.pos, x.head, c),
-                     rotate_vec<kType>(qv, cs01, cs23));
-        st_stream_v4(ko + off(3, x.pos, x.head, c),
-                     rotate_vec<kType>(kv, cs01, cs23));
+        const float4 cs01 = tab4<kSmem>(tab, i, p.tab_len);
+        const float4 cs23 = kType != ROPE3D_F32 ? tab4<kSmem>(tab, i + 2, p.tab_len) : cs01;
+        const long long o2 = off(2, x.pos, x.head, c), o3 = off(3, x.pos, x.head, c);
+        if (bound_ok(o2, 16, st.lim[2])) st_stream_v4(qo + o2, rotate_vec<kType>(qv, cs01, cs23));
+        if (bound_ok(o3, 16, st.lim[3])) st_stream_v4(ko + o3, rotate_vec<kType>(kv, cs01, cs23));
     }
 }
 
@@ -466,7 +490,7 @@ __device__ __forceinline__ void rotate_pair_at(const char *q, const char *k, cha
 
 template <int kType, bool kSmem>
 __global__ void __launch_bounds__(kBlock)
-rope3d_pair_kernel(const KParams p, const KStrides) {
+rope3d_pair_kernel(const KParams p, const KStrides st) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const float2 *tab = stage_tables<kSmem>(p, reinterpret_cast<float2 *>(smem_raw));
     constexpr size_t kPairBytes = kType == ROPE3D_F32 ? 8 : 4;
@@ -479,9 +503,11 @@ rope3d_pair_kernel(const KParams p, const KStrides) {
         const uint32_t row = fdiv(v, p.per_row);
         const uint32_t r = v - row * p.per_row.d;
         const uint32_t pair = r - fdiv(r, p.per_head) * p.per_head.d;
-        const float2 cs = tab1<kSmem>(tab, table_index(p, grid_pos(p, row), pair));
+        const float2 cs = tab1<kSmem>(tab, table_index(p, grid_pos(p, row), pair), p.tab_len);
         const size_t off = size_t(v) * kPairBytes;
-        rotate_pair_at<kType>(q + off, k + off, qo + off, ko + off, cs, false);
+        if (bound_ok(off, kPairBytes, st.lim[0]) && bound_ok(off, kPairBytes, st.lim[1]) &&
+            bound_ok(off, kPairBytes, st.lim[2]) && bound_ok(off, kPairBytes, st.lim[3]))
+            rotate_pair_at<kType>(q + off, k + off, qo + off, ko + off, cs, false);
     }
 }
 
@@ -502,13 +528,15 @@ rope3d_pair_strided_kernel(const KParams p, const KStrides st) {
         const uint32_t head = fdiv(r, p.per_head);
         const uint32_t pair = r - head * p.per_head.d;
         const GridPos pos = grid_pos(p, row);
-        const float2 cs = tab1<kSmem>(tab, table_index(p, pos, pair));
+        const float2 cs = tab1<kSmem>(tab, table_index(p, pos, pair), p.tab_len);
         const uint32_t channel = 2 * pair;
-        rotate_pair_at<kType>(q + strided_offset(st, 0, pos, head, channel) * kElemBytes,
-                              k + strided_offset(st, 1, pos, head, channel) * kElemBytes,
-                              qo + strided_offset(st, 2, pos, head, channel) * kElemBytes,
-                              ko + strided_offset(st, 3, pos, head, channel) * kElemBytes, cs,
-                              true);
+        long long o[4];
+        bool in = true;
+        for (int i = 0; i < 4; ++i) {
+            o[i] = strided_offset(st, i, pos, head, channel) * kElemBytes;
+            in = bound_ok(o[i], 2 * kElemBytes, st.lim[i]) && in;
+        }
+        if (in) rotate_pair_at<kType>(q + o[0], k + o[1], qo + o[2], ko + o[3], cs, true);
     }
 }
 
@@ -526,9 +554,10 @@ rope3d_gather_kernel(const char *src, char *dst, const KParams p, const KStrides
         const uint32_t head = fdiv(r, p.per_head);
         const uint32_t c = r - head * p.per_head.d;
         const GridPos pos = grid_pos(p, row);
-        const Word w = *reinterpret_cast<const Word *>(src + strided_offset(st, 0, pos, head, c) *
-                                                                  kElemBytes);
-        *reinterpret_cast<Word *>(dst + size_t(e) * kElemBytes) = w;
+        const long long o = strided_offset(st, 0, pos, head, c) * kElemBytes;
+        if (bound_ok(o, kElemBytes, st.lim[0]) && bound_ok(size_t(e) * kElemBytes, kElemBytes, st.lim[1]))
+            *reinterpret_cast<Word *>(dst + size_t(e) * kElemBytes) =
+                *reinterpret_cast<const Word *>(src + o);
     }
 }
 
@@ -652,9 +681,19 @@ cudaError_t launch_rope3d(const LaunchArgs &a, cudaStream_t stream, LaunchInfo *
     p.pW = a.pW;
     fill_geometry(p, units_per_row, units_per_head, a.T, a.H, a.W);
     KStrides st{};
-    if (a.strided)
-        for (int i = 0; i < 4; ++i)
-            for (int j = 0; j < 5; ++j) st.s[i][j] = a.strides[i][j];
+    if (a.strided) {
+        // a view's span: its farthest element (strides are >= 0) plus a head row
+        const uint64_t B = (a.row0 + a.rows + N - 1) / N;
+        const uint64_t ext[5] = {B, a.T, a.H, a.W, a.heads};
+        for (int i = 0; i < 4; ++i) {
+            uint64_t far = a.head_dim;
+            for (int j = 0; j < 5; ++j) {
+                st.s[i][j] = a.strides[i][j];
+                far += (ext[j] - 1) * uint64_t(a.strides[i][j]);
+            }
+            st.lim[i] = far * esize;
+        }
+    }
 
     const uint64_t cap = g_max_units.load(std::memory_order_relaxed);
     const uint64_t rows_per_launch = cap / units_per_row > 0 ? cap / units_per_row : 1;
@@ -673,6 +712,7 @@ cudaError_t launch_rope3d(const LaunchArgs &a, cudaStream_t stream, LaunchInfo *
             p.k = static_cast<const char *>(a.k) + elem_off * esize;
             p.q_out = static_cast<char *>(a.q_out) + elem_off * esize;
             p.k_out = static_cast<char *>(a.k_out) + elem_off * esize;
+            for (int i = 0; i < 4; ++i) st.lim[i] = nrows * row_elems * esize;
         }
         p.units = static_cast<uint32_t>(nrows * units_per_row);
         p.row0_mod_N = static_cast<uint32_t>((a.row0 + r) % N);
@@ -711,7 +751,13 @@ cudaError_t launch_gather(const void *src, const int64_t strides[5], void *dst, 
     KParams p{};
     fill_geometry(p, static_cast<uint32_t>(row_elems), head_dim, T, H, W);
     KStrides st{};
-    for (int j = 0; j < 5; ++j) st.s[0][j] = strides[j];
+    uint64_t far = head_dim;
+    const uint64_t ext[5] = {B, T, H, W, heads};
+    for (int j = 0; j < 5; ++j) {
+        st.s[0][j] = strides[j];
+        far += (ext[j] - 1) * uint64_t(strides[j]);
+    }
+    st.lim[0] = far * elem_bytes;   // the source view
     const uint64_t rows_per_launch = std::max<uint64_t>(1, kMaxUnitsPerLaunch / row_elems);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -727,6 +773,7 @@ cudaError_t launch_gather(const void *src, const int64_t strides[5], void *dst, 
         const uint64_t need = (uint64_t(p.units) + kBlock - 1) / kBlock;
         const int grid = static_cast<int>(std::min<uint64_t>(need, uint64_t(sms) * 4));
         char *d = static_cast<char *>(dst) + r * row_elems * elem_bytes;
+        st.lim[1] = nrows * row_elems * elem_bytes;   // this launch's part of dst
         if (elem_bytes == 2)
             rope3d_gather_kernel<2><<<grid, kBlock, 0, stream>>>(static_cast<const char *>(src), d, p, st);
         else
@@ -735,6 +782,27 @@ cudaError_t launch_gather(const void *src, const int64_t strides[5], void *dst, 
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+}  // namespace rope3d
+
+namespace rope3d {
+
+// This file's bound-check error count (0 unless built with the checks);
+// `reset` clears it. Synchronises the device when built with the checks.
+int64_t kernels_bound_errors(bool reset) {
+#if ROPE3D_DEBUG_BOUNDS
+    unsigned int n = 0;
+    if (cudaMemcpyFromSymbol(&n, g_bound_errors, sizeof(n)) != cudaSuccess) return -1;
+    if (reset) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_bound_errors, &zero, sizeof(zero)) != cudaSuccess) return -1;
+    }
+    return n;
+#else
+    (void)reset;
+    return 0;
+#endif
 }
 
 }  // namespace rope3d

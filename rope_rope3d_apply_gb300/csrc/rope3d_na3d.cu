@@ -76,6 +76,7 @@ struct NAParams {
     int kt, kh, kw;
     int nbh, nbw;            // query blocks along H and W
     float scale_log2;        // log2(e) / sqrt(head_dim)
+    unsigned long long total;   // elements of each of q, k, v, out (debug bound checks)
 };
 
 __device__ __forceinline__ int na_start(int i, int L, int k) {
@@ -137,11 +138,31 @@ __device__ __forceinline__ void stage_tables(const NAParams &p, float2 *dst, int
     }
 }
 
-// Rotate the 8 channels of a TabSlot for a token at grid position (t, h, w).
+// Debug builds (-DROPE3D_DEBUG_BOUNDS=1) check each computed index before the
+// access it guards: a failed check counts in this file's error word and skips
+// the access (never a trap). Otherwise every check compiles away.
+#if ROPE3D_DEBUG_BOUNDS
+__device__ unsigned int g_bound_errors;
+__device__ __forceinline__ bool bound_ok(unsigned long long off, unsigned long long len,
+                                         unsigned long long lim) {
+    if (off + len <= lim) return true;
+    atomicAdd(&g_bound_errors, 1u);
+    return false;
+}
+#else
+__device__ __forceinline__ constexpr bool bound_ok(unsigned long long, unsigned long long,
+                                                   unsigned long long) {
+    return true;
+}
+#endif
+
+// Rotate the 8 channels of a TabSlot for a token at grid position (t, h, w)
+// (tables of len entries).
 __device__ __forceinline__ uint4 rot_vec(uint4 v, const float2 *tab, const TabSlot &ts, int t,
-                                         int h, int w) {
+                                         int h, int w, uint32_t len) {
     const int pos = ts.axis == 0 ? t : (ts.axis == 1 ? h : w);
     const uint32_t idx = ts.base + uint32_t(pos) * ts.stride;
+    if (!bound_ok(idx, 2, len) || !bound_ok(idx + ts.half, 2, len)) return v;
     const float4 a = *reinterpret_cast<const float4 *>(tab + idx);
     const float4 b = *reinterpret_cast<const float4 *>(tab + idx + ts.half);
     return make_uint4(rot_word(v.x, a.x, a.y), rot_word(v.y, a.z, a.w), rot_word(v.z, b.x, b.y),
@@ -348,8 +369,10 @@ rope3d_na3d_kernel(const NAParams p) {
             if (kRope) kpos[m] = -1;
             if (i < k.nr) {
                 if (j < k.cw) {
-                    cp_async16(dk, p.k + off);
-                    cp_async16(dv, p.v + off);
+                    if (bound_ok(off, 8, p.total) && bound_ok(slot, 1, kKC)) {
+                        cp_async16(dk, p.k + off);
+                        cp_async16(dv, p.v + off);
+                    }
                     if (kRope) kpos[m] = ((k.rb + i * S) << 10) | (k.c0 + j);
                 } else {
                     *reinterpret_cast<uint4 *>(dk) = make_uint4(0, 0, 0, 0);
@@ -374,7 +397,7 @@ rope3d_na3d_kernel(const NAParams p) {
             const int pos = kpos[m];
             if (pos >= 0) {
                 uint4 *ptr = reinterpret_cast<uint4 *>(sK + (buf * kKC + slot0 + 8 * m) * kRow + cv * 8);
-                *ptr = rot_vec(*ptr, tab, ts, t, pos >> 10, pos & 1023);
+                *ptr = rot_vec(*ptr, tab, ts, t, pos >> 10, pos & 1023, p.tab_len);
             }
         }
     };
@@ -388,9 +411,9 @@ rope3d_na3d_kernel(const NAParams p) {
         const int r = slot0 + 8 * m;   // block row r: (h0 + r / 8, w0 + r % 8)
         const int h = h0 + r / kQBW, w = w0 + r % kQBW;
         qreg[m] = make_uint4(0, 0, 0, 0);
-        if (h < p.H && w < p.W)
-            qreg[m] = __ldg(reinterpret_cast<const uint4 *>(
-                p.q + batch0 + qt * frame + h * grid_row + (long long)w * tok));
+        const long long qo = batch0 + qt * frame + h * grid_row + (long long)w * tok;
+        if (h < p.H && w < p.W && bound_ok(qo, 8, p.total))
+            qreg[m] = __ldg(reinterpret_cast<const uint4 *>(p.q + qo));
     }
     Chunk cur = next_chunk();
     issue(cur, 0);
@@ -401,7 +424,7 @@ rope3d_na3d_kernel(const NAParams p) {
         const int r = slot0 + 8 * m;
         const int h = h0 + r / kQBW, w = w0 + r % kQBW;
         uint4 v = qreg[m];
-        if (kRope && h < p.H && w < p.W) v = rot_vec(v, tab, ts, qt, h, w);
+        if (kRope && h < p.H && w < p.W) v = rot_vec(v, tab, ts, qt, h, w, p.tab_len);
         *reinterpret_cast<uint4 *>(sQ + r * kRow + cv * 8) = v;
     }
     if (kRope) rotate_k(cur.t, 0);
@@ -451,7 +474,8 @@ rope3d_na3d_kernel(const NAParams p) {
 
         const int ilo = qb + (cur.ri < mb ? 1 : 0), ihi = qu + (cur.ri < mu ? 1 : 0);
         const int nq = (ihi - ilo) * cur.nseg;   // k16 steps of this warp (<= kKC / 16)
-        if (nq > 0) {
+        // (debug builds: the warp's slots [16 nseg ilo, + 16 nq) lie in the buffer)
+        if (nq > 0 && bound_ok(ilo * 16 * cur.nseg, 16 * nq, kKC)) {
             if (cur.c0 != colbits_c0) {
                 colbits_c0 = cur.c0;
                 colbits = 0;
@@ -570,7 +594,9 @@ rope3d_na3d_kernel(const NAParams p) {
         if (!(r == 0 ? rvalid0 : rvalid1)) continue;
         const float l = r == 0 ? l0 : l1;
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint16_t *dst = p.out + batch0 - cv * 8 + qt * frame + (hq + r) * grid_row + (long long)wq * tok;
+        const long long oo = batch0 - cv * 8 + qt * frame + (hq + r) * grid_row + (long long)wq * tok;
+        if (!bound_ok(oo, kHD, p.total)) continue;
+        uint16_t *dst = p.out + oo;
 #pragma unroll
         for (int n = 0; n < kHD / 8; ++n) {
             const uint32_t pk = pack_bf16(o[n][2 * r] * inv, o[n][2 * r + 1] * inv);
@@ -590,6 +616,25 @@ bool on_device(const void *ptr, int device) {
 }
 
 }  // namespace
+
+namespace rope3d {
+
+int64_t na3d_bound_errors(bool reset) {
+#if ROPE3D_DEBUG_BOUNDS
+    unsigned int n = 0;
+    if (cudaMemcpyFromSymbol(&n, g_bound_errors, sizeof(n)) != cudaSuccess) return -1;
+    if (reset) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_bound_errors, &zero, sizeof(zero)) != cudaSuccess) return -1;
+    }
+    return n;
+#else
+    (void)reset;
+    return 0;
+#endif
+}
+
+}  // namespace rope3d
 
 extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *out,
                            const rope3d_tables *tables, int64_t B, int64_t T, int64_t H,
@@ -661,6 +706,7 @@ extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *ou
     p.nbh = int((H + kQBH - 1) / kQBH);
     p.nbw = int((W + kQBW - 1) / kQBW);
     p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(kHD)));
+    p.total = static_cast<unsigned long long>(B * T * H * W * heads) * kHD;
     const uint64_t blocks = uint64_t(B) * heads * T * p.nbh * p.nbw;
     if (blocks > 0x7fffffffull) return ROPE3D_ERR_SHAPE;
     const size_t smem = kFixedSmem + (apply_rope ? size_t(p.tab_len) * sizeof(float2) : 0);

@@ -54,7 +54,26 @@ struct NParams {
     FastDiv per_token;        // units per token: (q_heads + k_heads) * per_head
     FastDiv per_head;         // units per head row
     uint32_t q_heads, k_heads, head_dim, half;
+    unsigned long long q_bytes, k_bytes;   // tensor sizes, for the debug bound checks
 };
+
+// Debug builds (-DROPE3D_DEBUG_BOUNDS=1) check each computed offset before the
+// accesses it guards: a failed check counts in this file's error word and
+// skips the unit (never a trap). Otherwise every check compiles away.
+#if ROPE3D_DEBUG_BOUNDS
+__device__ unsigned int g_bound_errors;
+__device__ __forceinline__ bool bound_ok(unsigned long long off, unsigned long long len,
+                                         unsigned long long lim) {
+    if (off + len <= lim) return true;
+    atomicAdd(&g_bound_errors, 1u);
+    return false;
+}
+#else
+__device__ __forceinline__ constexpr bool bound_ok(unsigned long long, unsigned long long,
+                                                   unsigned long long) {
+    return true;
+}
+#endif
 
 // ---- rounding to the storage type --------------------------------------------
 
@@ -137,7 +156,8 @@ __device__ __forceinline__ void st_v4(void *ptr, const uint4 &v) {
 }
 
 // Locate unit u: token, head row (Q heads first, then K heads) and the first
-// channel j of the unit in the first half. Returns false for an invalid position.
+// channel j of the unit in the first half. Returns 1 for an invalid position,
+// 2 for an offset that fails a debug bound check, else 0.
 struct Unit {
     const char *in;
     char *out;
@@ -146,24 +166,28 @@ struct Unit {
 };
 
 template <int kElemBytes>
-__device__ __forceinline__ bool locate(const NParams &p, uint32_t u, uint32_t elems_per_unit,
-                                       Unit *x) {
+__device__ __forceinline__ int locate(const NParams &p, uint32_t u, uint32_t elems_per_unit,
+                                      Unit *x) {
     const uint32_t tl = fdiv(u, p.per_token);
     const uint32_t r = u - tl * p.per_token.d;
     const uint32_t hrow = fdiv(r, p.per_head);
     const uint32_t g = r - hrow * p.per_head.d;
     const uint64_t token = uint64_t(p.token0) + tl;
     const int64_t pos = __ldg(p.positions + token);
-    if (pos < 0 || uint64_t(pos) >= p.max_position) return false;
+    if (pos < 0 || uint64_t(pos) >= p.max_position) return 1;
     const bool is_q = hrow < p.q_heads;
     const uint32_t h = is_q ? hrow : hrow - p.q_heads;
     const uint64_t heads = is_q ? p.q_heads : p.k_heads;
     const uint64_t off = ((token * heads + h) * p.head_dim) * kElemBytes;
+    if (!bound_ok(off, uint64_t(p.head_dim) * kElemBytes, is_q ? p.q_bytes : p.k_bytes) ||
+        !bound_ok(uint64_t(pos) * p.head_dim * 4, uint64_t(p.head_dim) * 4,
+                  p.max_position * p.head_dim * 4))
+        return 2;
     x->in = (is_q ? p.q : p.k) + off;
     x->out = (is_q ? p.q_out : p.k_out) + off;
     x->row = p.cache + uint64_t(pos) * p.head_dim;
     x->j = g * elems_per_unit;
-    return true;
+    return 0;
 }
 
 // Packed 16-bit form of neox_pair for two adjacent channels. Every operation
@@ -214,8 +238,8 @@ rope3d_neox_vec_kernel(const NParams p) {
     const uint32_t stride = gridDim.x * blockDim.x;
     for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < p.units; u += stride) {
         Unit x;
-        if (!locate<kElemBytes>(p, u, V, &x)) {
-            if (p.invalid) atomicAdd(p.invalid, 1);
+        if (const int bad = locate<kElemBytes>(p, u, V, &x)) {
+            if (bad == 1 && p.invalid) atomicAdd(p.invalid, 1);
             continue;
         }
         const uint4 a = ld_v4(x.in + size_t(x.j) * kElemBytes);
@@ -271,8 +295,8 @@ rope3d_neox_pair_kernel(const NParams p) {
     const uint32_t stride = gridDim.x * blockDim.x;
     for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < p.units; u += stride) {
         Unit x;
-        if (!locate<kElemBytes>(p, u, 1, &x)) {
-            if (p.invalid) atomicAdd(p.invalid, 1);
+        if (const int bad = locate<kElemBytes>(p, u, 1, &x)) {
+            if (bad == 1 && p.invalid) atomicAdd(p.invalid, 1);
             continue;
         }
         const char *a = x.in + size_t(x.j) * kElemBytes;
@@ -397,6 +421,8 @@ int neox(const void *q, const void *k, void *q_out, void *k_out, const int64_t *
     p.k_heads = static_cast<uint32_t>(k_heads);
     p.head_dim = static_cast<uint32_t>(head_dim);
     p.half = half;
+    p.q_bytes = static_cast<unsigned long long>(tokens) * q_heads * head_dim * es;
+    p.k_bytes = static_cast<unsigned long long>(tokens) * k_heads * head_dim * es;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
         return ROPE3D_ERR_CUDA;
@@ -429,6 +455,25 @@ int neox(const void *q, const void *k, void *q_out, void *k_out, const int64_t *
 }
 
 }  // namespace
+
+namespace rope3d {
+
+int64_t neox_bound_errors(bool reset) {
+#if ROPE3D_DEBUG_BOUNDS
+    unsigned int n = 0;
+    if (cudaMemcpyFromSymbol(&n, g_bound_errors, sizeof(n)) != cudaSuccess) return -1;
+    if (reset) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_bound_errors, &zero, sizeof(zero)) != cudaSuccess) return -1;
+    }
+    return n;
+#else
+    (void)reset;
+    return 0;
+#endif
+}
+
+}  // namespace rope3d
 
 extern "C" int rope3d_apply_neox(const void *q, const void *k, void *q_out, void *k_out,
                                  const int64_t *positions, const float *cos_sin_cache,

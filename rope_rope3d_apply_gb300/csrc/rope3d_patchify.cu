@@ -55,7 +55,26 @@ struct PParams {
     uint32_t bcf0;         // first (b, c, f) of this launch
     uint32_t C, F, H, W, p;
     uint32_t Hp, Wp;
+    unsigned long long total;   // bytes of x (and of y), for the debug bound checks
 };
+
+// Debug builds (-DROPE3D_DEBUG_BOUNDS=1) check each computed byte offset
+// before the access it guards: a failed check counts in this file's error word
+// and skips the access (never a trap). Otherwise every check compiles away.
+#if ROPE3D_DEBUG_BOUNDS
+__device__ unsigned int g_bound_errors;
+__device__ __forceinline__ bool bound_ok(unsigned long long off, unsigned long long len,
+                                         unsigned long long lim) {
+    if (off + len <= lim) return true;
+    atomicAdd(&g_bound_errors, 1u);
+    return false;
+}
+#else
+__device__ __forceinline__ constexpr bool bound_ok(unsigned long long, unsigned long long,
+                                                   unsigned long long) {
+    return true;
+}
+#endif
 
 // Decoded input row: global (b, c, f) index, and h split into (i, ph).
 struct Row {
@@ -153,7 +172,10 @@ patchify_vec_kernel(const PParams q) {
         if constexpr (kForward) {
             if (whole) {
 #pragma unroll
-                for (int k = 0; k < P; ++k) ws[swz(k * 32 + lane)] = ld_nc_v4(q.src + xb + 16 * (k * 32 + lane));
+                for (int k = 0; k < P; ++k) {
+                    const uint64_t o = xb + 16 * (k * 32 + lane);
+                    ws[swz(k * 32 + lane)] = bound_ok(o, 16, q.total) ? ld_nc_v4(q.src + o) : make_uint4(0, 0, 0, 0);
+                }
                 __syncwarp();
 #pragma unroll
                 for (int k = 0; k < P; ++k) raw[k] = ws[swz(lane * P + k)];
@@ -161,7 +183,10 @@ patchify_vec_kernel(const PParams q) {
             } else if (active) {
                 const uint64_t x_off = r.row * q.W + uint64_t(jv) * V * P;
 #pragma unroll
-                for (int k = 0; k < P; ++k) raw[k] = ld_nc_v4(q.src + x_off * ES + 16 * k);
+                for (int k = 0; k < P; ++k) {
+                    const uint64_t o = x_off * ES + 16 * k;
+                    raw[k] = bound_ok(o, 16, q.total) ? ld_nc_v4(q.src + o) : make_uint4(0, 0, 0, 0);
+                }
             }
             if (active) {
                 memcpy(e, raw, sizeof raw);
@@ -172,14 +197,16 @@ patchify_vec_kernel(const PParams q) {
                     for (int t = 0; t < V; ++t) o[t] = e[t * P + pw];
                     uint4 ov;
                     memcpy(&ov, o, sizeof ov);
-                    st_cs_v4(q.dst + (patched_row(q, r, pw, P) + col) * ES, ov);
+                    const uint64_t yo = (patched_row(q, r, pw, P) + col) * ES;
+                    if (bound_ok(yo, 16, q.total)) st_cs_v4(q.dst + yo, ov);
                 }
             }
         } else {
             if (active) {
 #pragma unroll
                 for (int pw = 0; pw < P; ++pw) {
-                    const uint4 iv = ld_nc_v4(q.src + (patched_row(q, r, pw, P) + col) * ES);
+                    const uint64_t o = (patched_row(q, r, pw, P) + col) * ES;
+                    const uint4 iv = bound_ok(o, 16, q.total) ? ld_nc_v4(q.src + o) : make_uint4(0, 0, 0, 0);
                     E in[V];
                     memcpy(in, &iv, sizeof iv);
 #pragma unroll
@@ -192,12 +219,18 @@ patchify_vec_kernel(const PParams q) {
                 for (int k = 0; k < P; ++k) ws[swz(lane * P + k)] = raw[k];
                 __syncwarp();
 #pragma unroll
-                for (int k = 0; k < P; ++k) st_cs_v4(q.dst + xb + 16 * (k * 32 + lane), ws[swz(k * 32 + lane)]);
+                for (int k = 0; k < P; ++k) {
+                    const uint64_t o = xb + 16 * (k * 32 + lane);
+                    if (bound_ok(o, 16, q.total)) st_cs_v4(q.dst + o, ws[swz(k * 32 + lane)]);
+                }
                 __syncwarp();
             } else if (active) {
                 const uint64_t x_off = r.row * q.W + uint64_t(jv) * V * P;
 #pragma unroll
-                for (int k = 0; k < P; ++k) st_cs_v4(q.dst + x_off * ES + 16 * k, raw[k]);
+                for (int k = 0; k < P; ++k) {
+                    const uint64_t o = x_off * ES + 16 * k;
+                    if (bound_ok(o, 16, q.total)) st_cs_v4(q.dst + o, raw[k]);
+                }
             }
         }
     }
@@ -221,6 +254,7 @@ patchify_elem_kernel(const PParams q) {
         const uint32_t pw = w - j * q.p;
         const uint64_t x_idx = r.row * q.W + w;
         const uint64_t y_idx = patched_row(q, r, pw, q.p) + j;
+        if (!bound_ok(x_idx * ES, ES, q.total) || !bound_ok(y_idx * ES, ES, q.total)) continue;
         if constexpr (kForward) {
             dst[y_idx] = src[x_idx];
         } else {
@@ -322,6 +356,7 @@ int run(bool forward, const void *src, void *dst, int64_t B, int64_t C, int64_t 
     q.p = static_cast<uint32_t>(p);
     q.Hp = static_cast<uint32_t>(H / p);
     q.Wp = Wp;
+    q.total = bytes;
 
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
@@ -358,6 +393,25 @@ int run(bool forward, const void *src, void *dst, int64_t B, int64_t C, int64_t 
 }
 
 }  // namespace
+
+namespace rope3d {
+
+int64_t patchify_bound_errors(bool reset) {
+#if ROPE3D_DEBUG_BOUNDS
+    unsigned int n = 0;
+    if (cudaMemcpyFromSymbol(&n, g_bound_errors, sizeof(n)) != cudaSuccess) return -1;
+    if (reset) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_bound_errors, &zero, sizeof(zero)) != cudaSuccess) return -1;
+    }
+    return n;
+#else
+    (void)reset;
+    return 0;
+#endif
+}
+
+}  // namespace rope3d
 
 extern "C" int rope3d_patchify(const void *x, void *y, int64_t B, int64_t C, int64_t F,
                                int64_t H, int64_t W, int64_t p, int32_t elem_bytes,

@@ -17,3 +17,17 @@ def oracle_lib():
     import oracle
 
     return oracle.load()
+
+
+@pytest.fixture(autouse=True)
+def no_failed_bound_checks(request):
+    """Under a bounds-checking debug build of the library (ROPE3D_LIB), every
+    GPU test must end with no failed index check."""
+    yield
+    if request.node.get_closest_marker("gpu") is None or not os.environ.get("ROPE3D_LIB"):
+        return
+    import rope_rope3d_apply_gb300 as r
+
+    built, errors = r.rope3d_debug_bounds(reset=True)
+    if built:
+        assert errors == 0, f"{errors} failed bound checks"

@@ -356,3 +356,10 @@ def test_neox_host_checks(lib):
     assert r.rope3d_neox_check(nul, *ok) == "ERR_NULL"
     no_counter = ptrs[:6] + [0]
     assert r.rope3d_neox_check(no_counter, *ok) == "OK"
+
+
+def test_normal_build_has_no_bound_checks(lib):
+    """The normal build compiles the debug bounds checks away and says so."""
+    if os.environ.get("ROPE3D_LIB"):
+        pytest.skip("a different build was named")
+    assert r.rope3d_debug_bounds() == (False, 0)
