@@ -489,6 +489,14 @@ int rope3d_testing_max_units_per_launch(int64_t n);
  */
 int rope3d_debug_bounds(int64_t *errors, int32_t reset);
 
+/*
+ * Test hook of the debug build: the rotation kernels see every table n
+ * entries shorter than it is (the memory stays valid), so their table-index
+ * checks must fire and count; 0 restores. Errors: ARG in a normal build or
+ * for n < 0.
+ */
+int rope3d_testing_debug_shrink_tables(int32_t n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,7 +30,7 @@ __all__ = [
     "rope3d_apply_pair_strided", "rope3d_preflight_strided", "view_strides",
     "rope3d_patchify", "rope3d_unpatchify", "rope3d_patchify_check", "rope3d_patchify_last_kernel",
     "rope3d_apply_neox", "rope3d_neox_check", "rope3d_neox_cache_host", "rope3d_neox_last_kernel",
-    "rope3d_na3d", "rope3d_debug_bounds",
+    "rope3d_na3d", "rope3d_debug_bounds", "rope3d_testing_debug_shrink_tables",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -86,6 +86,7 @@ def _declare(lib):
         "rope3d_testing_host_tables": ([i32], c.c_int),
         "rope3d_testing_max_units_per_launch": ([i64], c.c_int),
         "rope3d_debug_bounds": ([vp, i32], c.c_int),
+        "rope3d_testing_debug_shrink_tables": ([i32], c.c_int),
         "rope3d_apply_pair_noalloc": ([vp, vp, vp, vp] + [i64] * 6 + [vp, dbl, i32, vp], c.c_int),
         "rope3d_apply_pair_strided": ([vp, vp, vp, vp, vp] + [i64] * 6 + [vp, i32] + [vp] * 4 + [vp],
                                       c.c_int),
@@ -595,6 +596,11 @@ def rope3d_debug_bounds(reset: bool = True):
     if rc < 0:
         _check(rc, "rope3d_debug_bounds")
     return bool(rc), int(n.value)
+
+
+def rope3d_testing_debug_shrink_tables(n: int):
+    _check(load_library().rope3d_testing_debug_shrink_tables(int(n)),
+           "rope3d_testing_debug_shrink_tables")
 
 
 def rope3d_last_launch():

@@ -716,6 +716,11 @@ bool vec16_ok(const Geom &g, const void *q, const void *k, const void *qo, const
     return true;
 }
 
+// Debug builds' test hook: launches see the tables this many entries shorter
+// than they are (the memory stays valid), so the kernels' table-index checks
+// must fire.
+std::atomic<uint32_t> g_debug_shrink{0};
+
 LaunchArgs make_launch(const Geom &g, const rope3d_tables *t, const void *q, const void *k,
                        void *qo, void *ko, int64_t rows, int64_t row0, bool vec16) {
     LaunchArgs a{};
@@ -725,6 +730,10 @@ LaunchArgs make_launch(const Geom &g, const rope3d_tables *t, const void *q, con
     a.k_out = ko;
     a.tables = t->dev;
     a.table_len = t->len;
+    if (ROPE3D_DEBUG_BOUNDS) {   // test hook: see rope3d_testing_debug_shrink_tables
+        const uint32_t shrink = g_debug_shrink.load(std::memory_order_relaxed);
+        a.table_len = shrink < a.table_len ? a.table_len - shrink : 0;
+    }
     a.offH = t->offset[1];
     a.offW = t->offset[2];
     a.pT = static_cast<uint32_t>(g.split[0] / 2);
@@ -1221,6 +1230,13 @@ extern "C" int rope3d_debug_bounds(int64_t *errors, int32_t reset) {
     }
     *errors = total;
     return ROPE3D_DEBUG_BOUNDS ? 1 : 0;
+}
+
+extern "C" int rope3d_testing_debug_shrink_tables(int32_t n) {
+    if (!ROPE3D_DEBUG_BOUNDS) return ROPE3D_ERR_ARG;
+    if (n < 0) return ROPE3D_ERR_ARG;
+    g_debug_shrink.store(static_cast<uint32_t>(n));
+    return ROPE3D_OK;
 }
 
 extern "C" int rope3d_release_scratch(void) {

@@ -20,8 +20,8 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU hosts
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SUITES = ["test_gpu_parity.py", "test_gpu_strided.py", "test_gpu_patchify.py", "test_gpu_neox.py",
-          "test_gpu_na3d.py", "test_gpu_fuzz.py"]
+SUITES = ["test_gpu_debug_checks_fire.py", "test_gpu_parity.py", "test_gpu_strided.py",
+          "test_gpu_patchify.py", "test_gpu_neox.py", "test_gpu_na3d.py", "test_gpu_fuzz.py"]
 
 
 def test_suites_pass_under_the_bounds_checking_build():
@@ -33,7 +33,9 @@ def test_suites_pass_under_the_bounds_checking_build():
            *[os.path.join(ROOT, "tests", s) for s in SUITES]]
     out = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=1800)
     assert out.returncode == 0, out.stdout[-4000:] + out.stderr[-2000:]
-    assert " passed" in out.stdout
+    summary = out.stdout.strip().splitlines()[-1]
+    # every test ran, the one that makes the checks fire included
+    assert " passed" in summary and "skipped" not in summary, summary
 
 
 def test_debug_build_reports_itself():
