@@ -297,7 +297,11 @@ int rope3d_neox_last_kernel(void);
  *                 chunk a multiple of 8; tables <= 48 KB)
  *   kernel_size   (k_t, k_h, k_w), odd, each no larger than its grid extent
  *   apply_rope    1: rotate Q and K first (fused); 0: Q and K are used as
- *                 given (the unfused path's second kernel)
+ *                 given (the unfused path's second kernel). Measured, the
+ *                 unfused pair (rope3d_apply_pair, then apply_rope = 0) is
+ *                 faster: every key is rotated by each of the ~10 CTAs whose
+ *                 key region holds it, which costs more than the round trip
+ *                 of Q_out and K_out.
  *   stream        cudaStream_t; asynchronous
  * Limits: head_dim 128; T, H, W < 1024. The bit-exact gate does not run here.
  * Errors: NULL, SHAPE, ALIGN (16 bytes), ALIAS, TABLES, DEVICE, CUDA.

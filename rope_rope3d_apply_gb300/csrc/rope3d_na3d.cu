@@ -9,6 +9,9 @@
 // staged into shared memory, with exactly the arithmetic of rope3d_apply_pair
 // (four rounded fp32 products, one subtract, one add, a nearest-even cast to
 // bf16), so the rotated operands are bit-identical to the unfused path's.
+// Each key lies in the key regions of about ten CTAs and is rotated by each
+// of them, which costs more than the round trip saves: rope3d_apply_pair
+// followed by this kernel with apply_rope = 0 is the faster way to run it.
 //
 // Neighbourhood attention as published (Hassani et al., "Neighborhood Attention
 // Transformer", CVPR 2023): a query at (t, h, w) attends to the k_t x k_h x k_w
