@@ -157,3 +157,35 @@ def test_na3d_full_size_sampled():
     err = np.abs(got - ref)
     assert np.all(err <= bound), (err.max(), (err / bound).max())
     tabs.close()
+
+
+def test_na3d_large_scores_rescale_often():
+    """Q and K with sigma 3: scores spread over tens of log2 units, so row
+    maxima jump by more than 2^8 from chunk to chunk and the running
+    reference (and O, l) is rescaled many times; still within the bound."""
+    B, T, H, W, heads, split, kernel = 1, 3, 16, 16, 2, (32, 48, 48), (3, 7, 7)
+    shape6 = (B, T, H, W, heads, 128)
+    n = int(np.prod(shape6))
+    q_np = synthetic.normal(n, 3.0, 305, 0, "bf16")
+    k_np = synthetic.normal(n, 3.0, 305, 1, "bf16")
+    v_np = synthetic.normal(n, 1.0, 305, 2, "bf16")
+    shp = (B, T * H * W, heads, 128)
+    q, k, v = (bf16(a).reshape(shp).to(DEV) for a in (q_np, k_np, v_np))
+    tabs = r.rope3d_build_tables(T, H, W, split)
+    out = r.rope3d_na3d(q, k, v, tabs, kernel)
+    torch.cuda.synchronize()
+    got = to_f64(out).reshape(shape6)
+    otabs = oracle.tables(T, H, W, split)
+    ref = oracle.rope_na3d(q_np, k_np, v_np, shape6, split, otabs, kernel)
+    to64 = lambda b: (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)  # noqa: E731
+    qr = oracle.rope3d(q_np, shape6, split, otabs)
+    kr = oracle.rope3d(k_np, shape6, split, otabs)
+    # the scores do spread (shown on each token's score with itself): over
+    # more than 16 log2 units, twice the rescale threshold
+    scores = np.einsum("thwed,thwed->thwe", to64(qr).reshape(shape6)[0], to64(kr).reshape(shape6)[0])
+    assert np.ptp(scores) / np.sqrt(128) * 1.4427 > 16
+    absv = oracle.na3d(to64(qr), to64(kr), np.abs(to64(v_np)), shape6, kernel)
+    bound = 2.0 ** -7 * absv + 2.0 ** -8 * np.abs(ref) + 1e-6
+    err = np.abs(got - ref)
+    assert np.all(err <= bound), (err.max(), (err / bound).max())
+    tabs.close()
