@@ -532,7 +532,7 @@ def run_ours(args, w):
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
             "config": dict(workload_config(w), variant=args.variant,
@@ -622,7 +622,7 @@ def run_patchify(args):
     achieved = moved / (ms_fwd / 1e3) / 1e9
     line = {
         "op": "patchify", "metric": "patchify (space-to-depth) achieved HBM GB/s", "value": achieved,
-        "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_fwd,
+        "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_fwd,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": "patchify: x (B=%d, C=%d, F=%d, H=%d, W=%d) bf16, p=%d" % (
@@ -688,7 +688,7 @@ def run_neox(args):
     achieved = moved / (ms / 1e3) / 1e9
     line = {
         "op": "neox", "metric": "NeoX RoPE (Q+K) achieved HBM GB/s", "value": achieved, "unit": UNIT,
-        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": "neox: %d tokens, %d/%d heads x %d, cache %d rows, positions 0..%d" % (
@@ -777,7 +777,7 @@ def run_na3d(args):
         kind = "fallback"
     line = {
         "op": "na3d", "metric": "fused RoPE + 3D neighbourhood attention, useful TFLOP/s",
-        "value": tflops, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "value": tflops, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": ms_fused, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "na3d: B=%d, T=%d, H=%d, W=%d, heads=%d x 128, window %dx%dx%d" % (
