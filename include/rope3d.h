@@ -299,9 +299,10 @@ int rope3d_neox_last_kernel(void);
  *   apply_rope    1: rotate Q and K first (fused); 0: Q and K are used as
  *                 given (the unfused path's second kernel). Measured, the
  *                 unfused pair (rope3d_apply_pair, then apply_rope = 0) is
- *                 faster: every key is rotated by each of the ~10 CTAs whose
- *                 key region holds it, which costs more than the round trip
- *                 of Q_out and K_out.
+ *                 faster than apply_rope = 1: every key is rotated by each of
+ *                 the ~10 CTAs whose key region holds it, which costs more
+ *                 than the round trip of Q_out and K_out. The fast fused form
+ *                 is rope3d_na3d_rotate_once below.
  *   stream        cudaStream_t; asynchronous
  * Limits: head_dim 128; T, H, W < 1024. The bit-exact gate does not run here.
  * Errors: NULL, SHAPE, ALIGN (16 bytes), ALIAS, TABLES, DEVICE, CUDA.
@@ -310,6 +311,31 @@ int rope3d_na3d(const void *q, const void *k, const void *v, void *out,
                 const rope3d_tables *tables, int64_t B, int64_t T, int64_t H, int64_t W,
                 int64_t heads, int64_t head_dim, const int32_t split[3],
                 const int32_t kernel_size[3], int32_t apply_rope, void *stream);
+
+/*
+ * rope3d_na3d_rotate_once -- rope3d_na3d with the RoPE applied, rotating
+ * every element of Q and K exactly once. A first kernel rotates K into k_rot
+ * (16-byte vectors, rope3d_apply_pair's arithmetic); the attention kernel
+ * then rotates each Q tile while staging it (a query tile is read by one CTA
+ * only) and reads the keys from k_rot. Q_out is never written, and no key is
+ * rotated more than once. The result is bit-identical to rope3d_apply_pair
+ * followed by rope3d_na3d with apply_rope = 0, and k_rot holds that path's
+ * K_out.
+ *
+ *   q, k, v, out, tables, B, T, H, W, heads, head_dim, split, kernel_size,
+ *   stream        as rope3d_na3d with apply_rope = 1
+ *   k_rot         device, bf16, K's shape, 16-byte aligned, caller-owned;
+ *                 receives the rotated K. k_rot == k rotates K in place;
+ *                 otherwise k_rot overlaps no other argument.
+ * Two kernels on `stream`, asynchronous; the second is launched with
+ * programmatic stream serialization and waits for the first before it reads
+ * K. Limits as rope3d_na3d. The bit-exact gate does not run here.
+ * Errors: NULL, SHAPE, ALIGN (16 bytes), ALIAS, TABLES, DEVICE, CUDA.
+ */
+int rope3d_na3d_rotate_once(const void *q, const void *k, const void *v, void *k_rot,
+                            void *out, const rope3d_tables *tables, int64_t B, int64_t T,
+                            int64_t H, int64_t W, int64_t heads, int64_t head_dim,
+                            const int32_t split[3], const int32_t kernel_size[3], void *stream);
 
 /*
  * rope3d_apply_pair_host -- the same rotation for HOST buffers: the library
@@ -340,7 +366,7 @@ int rope3d_release_scratch(void);
 
 /*
  * rope3d_apply_pair_noalloc -- rope3d_apply_pair for callers that cannot
- * allocate device memory. The paper has no counterpart: it exists because
+ * allocate device memory. The sglang PR #35698 kernel has no counterpart: it exists because
  * rope3d_build_tables allocates the cached tables with cudaMalloc, and some
  * callers cannot call cudaMalloc (a process whose device memory belongs to
  * another allocator or a fixed budget, or a pipeline that must not take
@@ -474,7 +500,8 @@ int rope3d_testing_host_tables(int32_t on);
  * Test hook: cap the work units (16-byte vectors or pairs) of one kernel
  * launch at n, so that small inputs exercise the split into several launches
  * that very large inputs take (rows never straddle two launches; a row larger
- * than n gets a launch of its own). 0 restores the default cap of 2^30.
+ * than n gets a launch of its own). Applies to the rotation kernels and to
+ * the K pass of rope3d_na3d_rotate_once. 0 restores the default cap of 2^30.
  * Errors: ARG for n < 0 or n > 2^30.
  */
 int rope3d_testing_max_units_per_launch(int64_t n);

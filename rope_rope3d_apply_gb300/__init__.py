@@ -30,7 +30,8 @@ __all__ = [
     "rope3d_apply_pair_strided", "rope3d_preflight_strided", "view_strides",
     "rope3d_patchify", "rope3d_unpatchify", "rope3d_patchify_check", "rope3d_patchify_last_kernel",
     "rope3d_apply_neox", "rope3d_neox_check", "rope3d_neox_cache_host", "rope3d_neox_last_kernel",
-    "rope3d_na3d", "rope3d_debug_bounds", "rope3d_testing_debug_shrink_tables",
+    "rope3d_na3d", "rope3d_na3d_rotate_once", "rope3d_debug_bounds",
+    "rope3d_testing_debug_shrink_tables",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -99,6 +100,7 @@ def _declare(lib):
         "rope3d_neox_cache_host": ([i64, i64, dbl, vp], c.c_int),
         "rope3d_neox_last_kernel": ([], c.c_int),
         "rope3d_na3d": ([vp] * 5 + [i64] * 6 + [vp, vp, i32, vp], c.c_int),
+        "rope3d_na3d_rotate_once": ([vp] * 6 + [i64] * 6 + [vp, vp, vp], c.c_int),
         "rope3d_preflight_strided": ([vp, vp, vp, vp, vp] + [i64] * 6 + [vp, i32] + [vp] * 4 + [i32],
                                      c.c_int),
     }
@@ -507,6 +509,33 @@ def rope3d_na3d(q, k, v, tables: Tables, kernel_size, out=None, apply_rope: bool
                                     _stream(stream, q))
     _check(rc, "rope3d_na3d")
     return out
+
+
+def rope3d_na3d_rotate_once(q, k, v, tables: Tables, kernel_size, out=None, k_rot=None,
+                            stream=None):
+    """rope3d_na3d with Q and K rotated, each element once: K is rotated into
+    k_rot (allocated when None; k_rot=k rotates in place), then the attention
+    rotates its Q tiles. Returns (out, k_rot)."""
+    import torch
+
+    if out is None:
+        out = torch.empty_like(q)
+    if k_rot is None:
+        k_rot = torch.empty_like(k)
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("k_rot", k_rot)):
+        if not _contiguous(t):
+            raise ValueError(f"{name} must be contiguous")
+        if tuple(t.shape) != tuple(q.shape):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, q has {tuple(q.shape)}")
+        if _dtype_code(t) != BF16:
+            raise TypeError("rope3d_na3d_rotate_once takes bf16 tensors")
+    B, heads, head_dim = _geometry(q, tables)
+    ks = (ctypes.c_int32 * 3)(*[int(x) for x in kernel_size])
+    rc = load_library().rope3d_na3d_rotate_once(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(k_rot), _ptr(out), tables.handle, B, tables.T, tables.H,
+        tables.W, heads, head_dim, _split(tables.split), ks, _stream(stream, q))
+    _check(rc, "rope3d_na3d_rotate_once")
+    return out, k_rot
 
 
 def rope3d_preflight(q, k, q_out, k_out, tables, B, T, H, W, heads, head_dim, split, dtype,

@@ -1302,6 +1302,7 @@ extern "C" int64_t rope3d_testing_fastdiv(int64_t n, int64_t d) {
 extern "C" int rope3d_testing_max_units_per_launch(int64_t n) {
     if (n < 0 || n > int64_t(rope3d::kMaxUnitsPerLaunch)) return ROPE3D_ERR_ARG;
     rope3d::set_max_units_per_launch(static_cast<uint32_t>(n));
+    rope3d::na3d_set_max_units_per_launch(static_cast<uint32_t>(n));
     return ROPE3D_OK;
 }
 

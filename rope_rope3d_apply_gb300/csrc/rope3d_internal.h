@@ -86,6 +86,8 @@ struct LaunchInfo {
 // Test hook: lower the units-per-launch cap so that small inputs take the
 // multi-launch path (0 restores kMaxUnitsPerLaunch).
 void set_max_units_per_launch(uint32_t n);
+// The same for the K pass of rope3d_na3d_rotate_once.
+void na3d_set_max_units_per_launch(uint32_t n);
 
 // Launch the rotation; splits into several launches when needed. Returns a
 // cudaError_t from the launch.

@@ -1,17 +1,22 @@
 // rope3d_na3d.cu -- 3D neighbourhood attention with the decoder's RoPE fused
-// into its prologue: rope3d_na3d.
+// into it: rope3d_na3d and rope3d_na3d_rotate_once.
 //
 // Before each attention block the LTX-2.5 diffusion decoder rotates Q and K
 // (sglang PR #35698 review, "功能与动机" and "实现拆解"); its attention is
 // NATTEN's 3D neighbourhood attention (sglang PR #34471 review, "关键源码片段",
-// _na3d). Fusing the rotation into the attention kernel removes the round trip
-// of Q_out and K_out through HBM: Q and K tiles are rotated while they are
-// staged into shared memory, with exactly the arithmetic of rope3d_apply_pair
-// (four rounded fp32 products, one subtract, one add, a nearest-even cast to
-// bf16), so the rotated operands are bit-identical to the unfused path's.
-// Each key lies in the key regions of about ten CTAs and is rotated by each
-// of them, which costs more than the round trip saves: rope3d_apply_pair
-// followed by this kernel with apply_rope = 0 is the faster way to run it.
+// _na3d). Fusing the rotation into the attention removes HBM round trips of
+// the rotated operands. The rotation is exactly rope3d_apply_pair's (four
+// rounded fp32 products, one subtract, one add, a nearest-even cast to bf16),
+// so the rotated operands are bit-identical to the unfused path's. Three
+// forms of the attention kernel:
+//  - kRotNone: Q and K come rotated (rope3d_apply_pair first; apply_rope = 0);
+//  - kRotQK: Q and every K tile are rotated while staged into shared memory
+//    (apply_rope = 1). Each key lies in the key regions of about ten CTAs and
+//    is rotated by each of them, which costs more than the round trip saves;
+//  - kRotQ: a first kernel rotates K once, 16-byte vector by vector, and the
+//    attention rotates only its Q tile, which no other CTA reads
+//    (rope3d_na3d_rotate_once). Every element is rotated once and Q_out is
+//    never written: the fastest of the three.
 //
 // Neighbourhood attention as published (Hassani et al., "Neighborhood Attention
 // Transformer", CVPR 2023): a query at (t, h, w) attends to the k_t x k_h x k_w
@@ -32,6 +37,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -122,6 +128,18 @@ __device__ __forceinline__ TabSlot tab_slot(const NAParams &p, int cv) {
     return {p.offW + (pair - p.pT - p.pH) / 2, p.pW, p.pW / 2, 2};
 }
 
+// The same for the tables as they lie in global memory: row pos of an axis
+// holds its P entries in pair order, so the 4 pairs of channel block cv
+// (pair index j of the axis) are the 16-byte words at off + pos P + j and
+// 2 entries further.
+__device__ __forceinline__ TabSlot tab_slot_global(uint32_t pT, uint32_t pH, uint32_t pW,
+                                                   uint32_t offH, uint32_t offW, int cv) {
+    const uint32_t pair = 4 * cv;
+    if (pair < pT) return {pair, pT, 2, 0};
+    if (pair < pT + pH) return {offH + (pair - pT), pH, 2, 1};
+    return {offW + (pair - pT - pH), pW, 2, 2};
+}
+
 // Copy the tables into shared memory in the split layout above: one group
 // of four pairs (two 16-byte words) per step.
 __device__ __forceinline__ void stage_tables(const NAParams &p, float2 *dst, int tid, int nthreads) {
@@ -159,17 +177,30 @@ __device__ __forceinline__ constexpr bool bound_ok(unsigned long long, unsigned 
 }
 #endif
 
-// Rotate the 8 channels of a TabSlot for a token at grid position (t, h, w)
-// (tables of len entries).
+// Rotate the 8 channels of a TabSlot at position pos of its axis (tables of
+// len entries; kGlobal: read through the read-only data path, else shared).
+template <bool kGlobal>
+__device__ __forceinline__ uint4 rot_vec_at(uint4 v, const float2 *tab, const TabSlot &ts,
+                                            uint32_t pos, uint32_t len) {
+    const uint32_t idx = ts.base + pos * ts.stride;
+    if (!bound_ok(idx, 2, len) || !bound_ok(idx + ts.half, 2, len)) return v;
+    float4 a, b;
+    if constexpr (kGlobal) {
+        a = __ldg(reinterpret_cast<const float4 *>(tab + idx));
+        b = __ldg(reinterpret_cast<const float4 *>(tab + idx + ts.half));
+    } else {
+        a = *reinterpret_cast<const float4 *>(tab + idx);
+        b = *reinterpret_cast<const float4 *>(tab + idx + ts.half);
+    }
+    return make_uint4(rot_word(v.x, a.x, a.y), rot_word(v.y, a.z, a.w), rot_word(v.z, b.x, b.y),
+                      rot_word(v.w, b.z, b.w));
+}
+
+// The same for a token at grid position (t, h, w), tables in shared memory.
 __device__ __forceinline__ uint4 rot_vec(uint4 v, const float2 *tab, const TabSlot &ts, int t,
                                          int h, int w, uint32_t len) {
     const int pos = ts.axis == 0 ? t : (ts.axis == 1 ? h : w);
-    const uint32_t idx = ts.base + uint32_t(pos) * ts.stride;
-    if (!bound_ok(idx, 2, len) || !bound_ok(idx + ts.half, 2, len)) return v;
-    const float4 a = *reinterpret_cast<const float4 *>(tab + idx);
-    const float4 b = *reinterpret_cast<const float4 *>(tab + idx + ts.half);
-    return make_uint4(rot_word(v.x, a.x, a.y), rot_word(v.y, a.z, a.w), rot_word(v.z, b.x, b.y),
-                      rot_word(v.w, b.z, b.w));
+    return rot_vec_at<false>(v, tab, ts, uint32_t(pos), len);
 }
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -288,9 +319,16 @@ struct Chunk {
     int t, rb, ri, nr, c0, cw, nseg;
 };
 
-template <bool kRope>
-__global__ void __launch_bounds__(kThreads, kRope ? NA_MIN_CTAS_ROPE : NA_MIN_CTAS)
+// What the attention kernel rotates: nothing (Q and K come rotated), Q and
+// every K tile it copies, or Q alone (K was rotated once beforehand by
+// rope3d_na3d_rotate_k_kernel; the launch then waits for that kernel before
+// its first copy of K).
+enum RotMode : int { kRotNone = 0, kRotQK = 1, kRotQ = 2 };
+
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, kMode == kRotQK ? NA_MIN_CTAS_ROPE : NA_MIN_CTAS)
 rope3d_na3d_kernel(const NAParams p) {
+    constexpr bool kRotK = kMode == kRotQK;
     extern __shared__ __align__(16) unsigned char smem[];
     uint16_t *sK = reinterpret_cast<uint16_t *>(smem);        // [2][kKC][kRow]
     uint16_t *sV = sK + 2 * kKC * kRow;                        // [2][kKC][kRow]
@@ -369,14 +407,14 @@ rope3d_na3d_kernel(const NAParams p) {
             const int slot = slot0 + 8 * m;
             uint16_t *dk = sK + (buf * kKC + slot) * kRow + cv * 8;
             uint16_t *dv = sV + (buf * kKC + slot) * kRow + cv * 8;
-            if (kRope) kpos[m] = -1;
+            if (kRotK) kpos[m] = -1;
             if (i < k.nr) {
                 if (j < k.cw) {
                     if (bound_ok(off, 8, p.total) && bound_ok(slot, 1, kKC)) {
                         cp_async16(dk, p.k + off);
                         cp_async16(dv, p.v + off);
                     }
-                    if (kRope) kpos[m] = ((k.rb + i * S) << 10) | (k.c0 + j);
+                    if (kRotK) kpos[m] = ((k.rb + i * S) << 10) | (k.c0 + j);
                 } else {
                     *reinterpret_cast<uint4 *>(dk) = make_uint4(0, 0, 0, 0);
                     *reinterpret_cast<uint4 *>(dv) = make_uint4(0, 0, 0, 0);
@@ -406,9 +444,24 @@ rope3d_na3d_kernel(const NAParams p) {
     };
 
     // ---- prologue: tables, the Q tile, the first chunk
-    if (kRope)
-        stage_tables(p, sTab, tid, kThreads);
+    if (kRotK) stage_tables(p, sTab, tid, kThreads);
     uint4 qreg[kVecs];
+    // Q rotated here (kRotQ): a thread's vectors are the block rows m of one
+    // column, (h0 + m, w0 + slot0), so its T or W table words are the same for
+    // all of them and are loaded once; H words are loaded per row.
+    const TabSlot tsg = tab_slot_global(p.pT, p.pH, p.pW, p.offH, p.offW, cv);
+    const bool col_ok = w0 + slot0 < p.W;
+    float4 qta[kMode == kRotQ ? kVecs : 1], qtb[kMode == kRotQ ? kVecs : 1];
+    if constexpr (kMode == kRotQ) {
+        qta[0] = qtb[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (tsg.axis != 1 && col_ok) {
+            const uint32_t idx = tsg.base + uint32_t(tsg.axis == 0 ? qt : w0 + slot0) * tsg.stride;
+            if (bound_ok(idx, 4, p.tab_len)) {
+                qta[0] = __ldg(reinterpret_cast<const float4 *>(p.tab + idx));
+                qtb[0] = __ldg(reinterpret_cast<const float4 *>(p.tab + idx + 2));
+            }
+        }
+    }
 #pragma unroll
     for (int m = 0; m < kVecs; ++m) {
         const int r = slot0 + 8 * m;   // block row r: (h0 + r / 8, w0 + r % 8)
@@ -417,20 +470,43 @@ rope3d_na3d_kernel(const NAParams p) {
         const long long qo = batch0 + qt * frame + h * grid_row + (long long)w * tok;
         if (h < p.H && w < p.W && bound_ok(qo, 8, p.total))
             qreg[m] = __ldg(reinterpret_cast<const uint4 *>(p.q + qo));
+        if constexpr (kMode == kRotQ) {
+            if (tsg.axis == 1) {
+                const uint32_t idx = tsg.base + uint32_t(h) * tsg.stride;
+                qta[m] = qtb[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (h < p.H && col_ok && bound_ok(idx, 4, p.tab_len)) {
+                    qta[m] = __ldg(reinterpret_cast<const float4 *>(p.tab + idx));
+                    qtb[m] = __ldg(reinterpret_cast<const float4 *>(p.tab + idx + 2));
+                }
+            } else if (m > 0) {
+                qta[m] = qta[0];
+                qtb[m] = qtb[0];
+            }
+        }
     }
+    // K comes from the kernel before this one in the stream (launched with
+    // programmatic serialization): wait for it before the first copy.
+    if (kMode == kRotQ) asm volatile("griddepcontrol.wait;" ::: "memory");
     Chunk cur = next_chunk();
     issue(cur, 0);
     cp_async_commit();
-    if (kRope) __syncthreads();   // tables staged
+    if (kRotK) __syncthreads();   // tables staged
 #pragma unroll
     for (int m = 0; m < kVecs; ++m) {
         const int r = slot0 + 8 * m;
         const int h = h0 + r / kQBW, w = w0 + r % kQBW;
         uint4 v = qreg[m];
-        if (kRope && h < p.H && w < p.W) v = rot_vec(v, tab, ts, qt, h, w, p.tab_len);
+        if (h < p.H && w < p.W) {
+            if constexpr (kMode == kRotQK) v = rot_vec(v, tab, ts, qt, h, w, p.tab_len);
+            if constexpr (kMode == kRotQ) {
+                const float4 a = qta[m], b = qtb[m];
+                v = make_uint4(rot_word(v.x, a.x, a.y), rot_word(v.y, a.z, a.w),
+                               rot_word(v.z, b.x, b.y), rot_word(v.w, b.z, b.w));
+            }
+        }
         *reinterpret_cast<uint4 *>(sQ + r * kRow + cv * 8) = v;
     }
-    if (kRope) rotate_k(cur.t, 0);
+    if (kRotK) rotate_k(cur.t, 0);
     __syncthreads();
 
     // Q fragments of this warp's 16 rows, all 8 k-steps
@@ -587,7 +663,7 @@ rope3d_na3d_kernel(const NAParams p) {
                 default: steps(std::integral_constant<int, 4>{}); break;
             }
         }
-        if (kRope && c + 1 < n_chunks) rotate_k(nxt.t, buf ^ 1);
+        if (kRotK && c + 1 < n_chunks) rotate_k(nxt.t, buf ^ 1);
         cur = nxt;
     }
 
@@ -608,6 +684,71 @@ rope3d_na3d_kernel(const NAParams p) {
     }
 }
 
+// ---- K rotated once, before the attention (rope3d_na3d_rotate_once) -------
+// K [tokens, heads, 128] bf16 is rotated vector by vector into k_rot with the
+// eager arithmetic above; one launch covers a whole number of tokens.
+struct RKParams {
+    const uint4 *k;
+    uint4 *k_rot;
+    const float2 *tab;
+    uint32_t tab_len, offH, offW, pT, pH, pW;
+    uint32_t units;                  // 16-byte vectors of this launch (< 2^30)
+    uint32_t tok0;                   // grid index (t H + h) W + w of the first token
+    rope3d::FastDiv heads, Wd, Hd, HWd, Td;
+};
+
+constexpr int kRotThreads = 512, kRotUnroll = 4;
+static_assert(kRotThreads % (kHD / 8) == 0, "a thread keeps one channel block");
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const rope3d::FastDiv &f) {
+    return (__umulhi(n, f.mul) + n) >> f.shift;
+}
+
+// Plain (coherent) loads: k_rot may be k itself.
+__device__ __forceinline__ uint4 ld_v4(const uint4 *ptr) {
+    uint4 r;
+    asm volatile("ld.global.L1::no_allocate.L2::128B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(ptr)
+                 : "memory");
+    return r;
+}
+
+// Grid coordinate on `axis` of the token of vector vv.
+__device__ __forceinline__ uint32_t axis_pos(const RKParams &p, uint32_t vv, int axis) {
+    const uint32_t gt = p.tok0 + fdiv(vv >> 4, p.heads);   // < 2^31
+    if (axis == 2) return gt - fdiv(gt, p.Wd) * p.Wd.d;
+    if (axis == 1) {
+        const uint32_t r = fdiv(gt, p.Wd);
+        return r - fdiv(r, p.Hd) * p.Hd.d;
+    }
+    const uint32_t r = fdiv(gt, p.HWd);
+    return r - fdiv(r, p.Td) * p.Td.d;
+}
+
+__global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(const RKParams p) {
+    // The attention kernel may launch now; it waits for this grid to finish
+    // before it reads K.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint32_t stride = gridDim.x * kRotThreads;   // a multiple of 16
+    uint32_t v = blockIdx.x * kRotThreads + threadIdx.x;
+    const TabSlot ts = tab_slot_global(p.pT, p.pH, p.pW, p.offH, p.offW, int(v & 15));
+    for (; v + (kRotUnroll - 1) * stride < p.units; v += kRotUnroll * stride) {
+        uint4 x[kRotUnroll];
+#pragma unroll
+        for (int u = 0; u < kRotUnroll; ++u)
+            if (bound_ok(v + u * stride, 1, p.units)) x[u] = ld_v4(p.k + v + u * stride);
+#pragma unroll
+        for (int u = 0; u < kRotUnroll; ++u) {
+            const uint32_t vv = v + u * stride;
+            if (!bound_ok(vv, 1, p.units)) continue;
+            p.k_rot[vv] = rot_vec_at<true>(x[u], p.tab, ts, axis_pos(p, vv, ts.axis), p.tab_len);
+        }
+    }
+    for (; v < p.units; v += stride)
+        p.k_rot[v] = rot_vec_at<true>(ld_v4(p.k + v), p.tab, ts, axis_pos(p, v, ts.axis), p.tab_len);
+}
+
 bool on_device(const void *ptr, int device) {
     cudaPointerAttributes attr{};
     if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
@@ -621,6 +762,14 @@ bool on_device(const void *ptr, int device) {
 }  // namespace
 
 namespace rope3d {
+
+// Vectors per launch of the K pass (rope3d_testing_max_units_per_launch
+// lowers it so that small inputs take several launches).
+static std::atomic<uint32_t> g_na3d_max_units{kMaxUnitsPerLaunch};
+
+void na3d_set_max_units_per_launch(uint32_t n) {
+    g_na3d_max_units.store(n == 0 || n > kMaxUnitsPerLaunch ? kMaxUnitsPerLaunch : n);
+}
 
 int64_t na3d_bound_errors(bool reset) {
 #if ROPE3D_DEBUG_BOUNDS
@@ -639,10 +788,14 @@ int64_t na3d_bound_errors(bool reset) {
 
 }  // namespace rope3d
 
-extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *out,
-                           const rope3d_tables *tables, int64_t B, int64_t T, int64_t H,
-                           int64_t W, int64_t heads, int64_t head_dim, const int32_t split[3],
-                           const int32_t kernel_size[3], int32_t apply_rope, void *stream) {
+namespace {
+
+// The checks and kernel arguments shared by rope3d_na3d and
+// rope3d_na3d_rotate_once (apply_rope: the tables are used).
+int na3d_setup(const void *q, const void *k, const void *v, const void *out,
+               const rope3d_tables *tables, int64_t B, int64_t T, int64_t H, int64_t W,
+               int64_t heads, int64_t head_dim, const int32_t split[3],
+               const int32_t kernel_size[3], bool apply_rope, NAParams &p) {
     if (!q || !k || !v || !out || !kernel_size || (apply_rope && (!tables || !split)))
         return ROPE3D_ERR_NULL;
     if (B <= 0 || T <= 0 || H <= 0 || W <= 0 || heads <= 0) return ROPE3D_ERR_SHAPE;
@@ -653,7 +806,7 @@ extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *ou
     if (kt < 1 || kh < 1 || kw < 1 || kt % 2 == 0 || kh % 2 == 0 || kw % 2 == 0 || kt > T ||
         kh > H || kw > W)
         return ROPE3D_ERR_SHAPE;
-    for (const void *ptr : {q, k, v, static_cast<const void *>(out)})
+    for (const void *ptr : {q, k, v, out})
         if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return ROPE3D_ERR_ALIGN;
     const uint64_t bytes = uint64_t(B * T * H * W * heads) * kHD * 2;
     const uintptr_t o = reinterpret_cast<uintptr_t>(out);
@@ -661,7 +814,7 @@ extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *ou
         const uintptr_t x = reinterpret_cast<uintptr_t>(ptr);
         if (o < x + bytes && x < o + bytes) return ROPE3D_ERR_ALIAS;
     }
-    NAParams p{};
+    p = NAParams{};
     if (apply_rope) {
         const float2 *dev = nullptr;
         uint32_t len = 0, offs[3];
@@ -691,13 +844,13 @@ extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *ou
     }
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return ROPE3D_ERR_CUDA;
-    for (const void *ptr : {q, k, v, static_cast<const void *>(out)})
+    for (const void *ptr : {q, k, v, out})
         if (!on_device(ptr, device)) return ROPE3D_ERR_DEVICE;
 
     p.q = static_cast<const uint16_t *>(q);
     p.k = static_cast<const uint16_t *>(k);
     p.v = static_cast<const uint16_t *>(v);
-    p.out = static_cast<uint16_t *>(out);
+    p.out = static_cast<uint16_t *>(const_cast<void *>(out));
     p.B = int(B);
     p.T = int(T);
     p.H = int(H);
@@ -712,18 +865,130 @@ extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *ou
     p.total = static_cast<unsigned long long>(B * T * H * W * heads) * kHD;
     const uint64_t blocks = uint64_t(B) * heads * T * p.nbh * p.nbw;
     if (blocks > 0x7fffffffull) return ROPE3D_ERR_SHAPE;
+    return ROPE3D_OK;
+}
+
+uint32_t na3d_blocks(const NAParams &p) {
+    return uint32_t(uint64_t(p.B) * p.heads * p.T * p.nbh * p.nbw);
+}
+
+// Dynamic shared memory limits of the three instances, set once.
+bool na3d_attributes() {
+    static const bool ok = [] {
+        const cudaError_t rc[3] = {
+            cudaFuncSetAttribute(rope3d_na3d_kernel<kRotNone>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(kFixedSmem)),
+            cudaFuncSetAttribute(rope3d_na3d_kernel<kRotQK>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(kFixedSmem + kMaxTableBytes)),
+            cudaFuncSetAttribute(rope3d_na3d_kernel<kRotQ>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(kFixedSmem))};
+        return rc[0] == cudaSuccess && rc[1] == cudaSuccess && rc[2] == cudaSuccess;
+    }();
+    return ok;
+}
+
+}  // namespace
+
+extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *out,
+                           const rope3d_tables *tables, int64_t B, int64_t T, int64_t H,
+                           int64_t W, int64_t heads, int64_t head_dim, const int32_t split[3],
+                           const int32_t kernel_size[3], int32_t apply_rope, void *stream) {
+    NAParams p;
+    const int rc = na3d_setup(q, k, v, out, tables, B, T, H, W, heads, head_dim, split,
+                              kernel_size, apply_rope != 0, p);
+    if (rc != ROPE3D_OK) return rc;
+    if (!na3d_attributes()) return ROPE3D_ERR_CUDA;
     const size_t smem = kFixedSmem + (apply_rope ? size_t(p.tab_len) * sizeof(float2) : 0);
-    static const cudaError_t attr_rc[2] = {
-        cudaFuncSetAttribute(rope3d_na3d_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kFixedSmem)),
-        cudaFuncSetAttribute(rope3d_na3d_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kFixedSmem + kMaxTableBytes))};
-    if (attr_rc[0] != cudaSuccess || attr_rc[1] != cudaSuccess) return ROPE3D_ERR_CUDA;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (apply_rope)
-        rope3d_na3d_kernel<true><<<unsigned(blocks), kThreads, smem, st>>>(p);
+        rope3d_na3d_kernel<kRotQK><<<na3d_blocks(p), kThreads, smem, st>>>(p);
     else
-        rope3d_na3d_kernel<false><<<unsigned(blocks), kThreads, smem, st>>>(p);
+        rope3d_na3d_kernel<kRotNone><<<na3d_blocks(p), kThreads, smem, st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return ROPE3D_ERR_CUDA;
+    return ROPE3D_OK;
+}
+
+extern "C" int rope3d_na3d_rotate_once(const void *q, const void *k, const void *v, void *k_rot,
+                                       void *out, const rope3d_tables *tables, int64_t B,
+                                       int64_t T, int64_t H, int64_t W, int64_t heads,
+                                       int64_t head_dim, const int32_t split[3],
+                                       const int32_t kernel_size[3], void *stream) {
+    NAParams p;
+    int rc = na3d_setup(q, k, v, out, tables, B, T, H, W, heads, head_dim, split, kernel_size,
+                        true, p);
+    if (rc != ROPE3D_OK) return rc;
+    if (!k_rot) return ROPE3D_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(k_rot) % 16 != 0) return ROPE3D_ERR_ALIGN;
+    // k_rot is k (in place) or overlaps nothing
+    const uint64_t bytes = p.total * 2;
+    const uintptr_t r = reinterpret_cast<uintptr_t>(k_rot);
+    for (const void *ptr : {q, k, v, static_cast<const void *>(out)}) {
+        const uintptr_t x = reinterpret_cast<uintptr_t>(ptr);
+        if (ptr == k && k_rot == k) continue;
+        if (r < x + bytes && x < r + bytes) return ROPE3D_ERR_ALIAS;
+    }
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return ROPE3D_ERR_CUDA;
+    if (!on_device(k_rot, device)) return ROPE3D_ERR_DEVICE;
+    if (uint64_t(heads) * (kHD / 8) > rope3d::kMaxUnitsPerLaunch) return ROPE3D_ERR_SHAPE;
+    if (!na3d_attributes()) return ROPE3D_ERR_CUDA;
+    static const int sms = [] {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        return n;
+    }();
+    if (sms <= 0) return ROPE3D_ERR_CUDA;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    // 1. K -> k_rot, in launches of whole tokens below 2^30 vectors each
+    RKParams rp{};
+    rp.tab = p.tab;
+    rp.tab_len = p.tab_len;
+    rp.offH = p.offH;
+    rp.offW = p.offW;
+    rp.pT = p.pT;
+    rp.pH = p.pH;
+    rp.pW = p.pW;
+    const uint32_t vec_per_tok = uint32_t(heads) * (kHD / 8);
+    rp.heads = rope3d::make_fastdiv(uint32_t(heads));
+    rp.Wd = rope3d::make_fastdiv(uint32_t(W));
+    rp.Hd = rope3d::make_fastdiv(uint32_t(H));
+    rp.HWd = rope3d::make_fastdiv(uint32_t(H * W));
+    rp.Td = rope3d::make_fastdiv(uint32_t(T));
+    const uint64_t tokens = uint64_t(B) * T * H * W, grid_tokens = uint64_t(T) * H * W;
+    const uint64_t cap = rope3d::g_na3d_max_units.load(std::memory_order_relaxed);
+    const uint64_t per_launch = cap / vec_per_tok > 0 ? cap / vec_per_tok : 1;
+    for (uint64_t t0 = 0; t0 < tokens; t0 += per_launch) {
+        const uint64_t n = tokens - t0 < per_launch ? tokens - t0 : per_launch;
+        rp.k = static_cast<const uint4 *>(k) + t0 * vec_per_tok;
+        rp.k_rot = static_cast<uint4 *>(k_rot) + t0 * vec_per_tok;
+        rp.units = uint32_t(n * vec_per_tok);
+        rp.tok0 = uint32_t(t0 % grid_tokens);
+        const uint64_t want = (uint64_t(rp.units) + kRotThreads - 1) / kRotThreads;
+        const uint32_t grid = uint32_t(want < uint64_t(3) * sms ? want : uint64_t(3) * sms);
+        rope3d_na3d_rotate_k_kernel<<<grid, kRotThreads, 0, st>>>(rp);
+        if (cudaGetLastError() != cudaSuccess) return ROPE3D_ERR_CUDA;
+    }
+
+    // 2. the attention on k_rot, rotating its Q tiles; launched with
+    // programmatic serialization, it waits for step 1 before reading K
+    p.k = static_cast<const uint16_t *>(k_rot);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(na3d_blocks(p));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kFixedSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, rope3d_na3d_kernel<kRotQ>, p) != cudaSuccess) {
+        cudaGetLastError();
+        return ROPE3D_ERR_CUDA;
+    }
     return ROPE3D_OK;
 }

@@ -164,7 +164,7 @@ def test_fuzz_neox(seed):
 def test_fuzz_na3d(seed):
     """Neighbourhood attention on random grids, heads, batches, splits and
     odd windows, with and without the rotation: within the derived bound of
-    the float64 oracle, and the fused kernel equal to the unfused pair."""
+    the float64 oracle, and both fused forms equal to the unfused pair."""
     g = np.random.Generator(np.random.PCG64(8000 + seed))
     B = int(g.integers(1, 3))
     T, H, W = int(g.integers(1, 6)), int(g.integers(1, 21)), int(g.integers(1, 21))
@@ -184,8 +184,11 @@ def test_fuzz_na3d(seed):
     if rope:
         qr, kr = r.rope3d_apply_pair(q, k, tabs)
         unfused = r.rope3d_na3d(qr, kr, v, tabs, kernel, apply_rope=False)
+        once, k_rot = r.rope3d_na3d_rotate_once(q, k, v, tabs, kernel)
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), unfused.view(torch.int16))
+        assert torch.equal(once.view(torch.int16), unfused.view(torch.int16))
+        assert torch.equal(k_rot.view(torch.int16), kr.view(torch.int16))
     torch.cuda.synchronize()
     to64 = lambda b: (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)  # noqa: E731
     got = to64(to_np(out)).reshape(shape6)

@@ -1,6 +1,7 @@
 """GPU checks of rope3d_na3d (3D neighbourhood attention with the RoPE fused
-into its prologue) against the float64 oracle, and of the fusion itself: the
-fused kernel must give the same bits as the same kernel fed with Q and K
+into its prologue) and rope3d_na3d_rotate_once (K rotated once beforehand, Q
+in the prologue) against the float64 oracle, and of the fusion itself: both
+fused forms must give the same bits as the attention kernel fed with Q and K
 rotated by rope3d_apply_pair.
 
 Tolerance (derived from the arithmetic): the rotated operands are exact
@@ -49,8 +50,19 @@ CASES = [
 ]
 
 
+def attend(path, q, k, v, tabs, kernel):
+    """The attention with the RoPE applied, by one of the two fused forms."""
+    if path == "qk":
+        return r.rope3d_na3d(q, k, v, tabs, kernel)
+    return r.rope3d_na3d_rotate_once(q, k, v, tabs, kernel)[0]
+
+
+PATHS = ["qk", "once"]
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-{c[2]}" for c in CASES])
-def test_na3d_matches_oracle(case):
+def test_na3d_matches_oracle(case, path):
     (B, T, H, W, heads), split, kernel = case
     shape6 = (B, T, H, W, heads, 128)
     n = int(np.prod(shape6))
@@ -60,7 +72,7 @@ def test_na3d_matches_oracle(case):
     shp = (B, T * H * W, heads, 128)
     q, k, v = (bf16(a).reshape(shp).to(DEV) for a in (q_np, k_np, v_np))
     tabs = r.rope3d_build_tables(T, H, W, split)
-    out = r.rope3d_na3d(q, k, v, tabs, kernel)
+    out = attend(path, q, k, v, tabs, kernel)
     torch.cuda.synchronize()
     got = to_f64(out).reshape(shape6)
     otabs = oracle.tables(T, H, W, split)
@@ -88,6 +100,74 @@ def test_fused_equals_unfused_bitwise():
     unfused = r.rope3d_na3d(qr, kr, v, tabs, kernel, apply_rope=False)
     torch.cuda.synchronize()
     assert torch.equal(fused.view(torch.int16), unfused.view(torch.int16))
+    tabs.close()
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-{c[2]}" for c in CASES])
+def test_rotate_once_equals_unfused_bitwise(case):
+    """K rotated once beforehand and Q in the attention prologue: the unfused
+    pair's output bits, and k_rot is rope3d_apply_pair's K_out; the same with
+    K rotated in place (k_rot = k)."""
+    (B, T, H, W, heads), split, kernel = case
+    shp = (B, T * H * W, heads, 128)
+    n = int(np.prod(shp))
+    q, k, v = (bf16(synthetic.normal(n, 1.0, 306, i, "bf16")).reshape(shp).to(DEV) for i in range(3))
+    tabs = r.rope3d_build_tables(T, H, W, split)
+    qr, kr = r.rope3d_apply_pair(q, k, tabs)
+    unfused = r.rope3d_na3d(qr, kr, v, tabs, kernel, apply_rope=False)
+    out, k_rot = r.rope3d_na3d_rotate_once(q, k, v, tabs, kernel)
+    kk = k.clone()
+    out2, k_rot2 = r.rope3d_na3d_rotate_once(q, kk, v, tabs, kernel, k_rot=kk)
+    torch.cuda.synchronize()
+    assert k_rot2 is kk
+    for a, b in ((out, unfused), (k_rot, kr), (out2, unfused), (kk, kr)):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    tabs.close()
+
+
+@pytest.mark.parametrize("cap", [1, 176, 4096])
+def test_rotate_once_split_k_pass(cap):
+    """The K pass cut into launches of whole tokens (1 token, 5 tokens, 128
+    tokens per launch, across the batch boundary): the same bits as one
+    launch."""
+    B, T, H, W, heads, split, kernel = 2, 3, 10, 13, 2, (32, 48, 48), (3, 5, 5)
+    shp = (B, T * H * W, heads, 128)
+    n = int(np.prod(shp))
+    q, k, v = (bf16(synthetic.normal(n, 1.0, 307, i, "bf16")).reshape(shp).to(DEV) for i in range(3))
+    tabs = r.rope3d_build_tables(T, H, W, split)
+    one, k_one = r.rope3d_na3d_rotate_once(q, k, v, tabs, kernel)
+    try:
+        r.rope3d_testing_max_units_per_launch(cap)
+        split_out, k_split = r.rope3d_na3d_rotate_once(q, k, v, tabs, kernel)
+        torch.cuda.synchronize()
+    finally:
+        r.rope3d_testing_max_units_per_launch(0)
+    assert torch.equal(split_out.view(torch.int16), one.view(torch.int16))
+    assert torch.equal(k_split.view(torch.int16), k_one.view(torch.int16))
+    tabs.close()
+
+
+def test_rotate_once_rejections():
+    B, T, H, W, heads = 1, 3, 8, 8, 1
+    tabs = r.rope3d_build_tables(T, H, W, (32, 48, 48))
+    shp = (B, T * H * W, heads, 128)
+    n = int(np.prod(shp))
+    q, k, v = (torch.zeros(shp, dtype=torch.bfloat16, device=DEV) for _ in range(3))
+    out = torch.empty_like(q)
+    for k_rot in (q, v, out):
+        with pytest.raises(r.Rope3dError) as e:
+            r.rope3d_na3d_rotate_once(q, k, v, tabs, (3, 3, 3), out=out, k_rot=k_rot)
+        assert e.value.name == "ERR_ALIAS"
+    flat = torch.empty(n + 8, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(r.Rope3dError) as e:
+        r.rope3d_na3d_rotate_once(q, k, v, tabs, (3, 3, 3), out=out, k_rot=flat[1:n + 1].view(shp))
+    assert e.value.name == "ERR_ALIGN"
+    # k_rot overlapping k without being k (one token further on)
+    kbig = torch.zeros(n + 128, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(r.Rope3dError) as e:
+        r.rope3d_na3d_rotate_once(q, kbig[:n].view(shp), v, tabs, (3, 3, 3), out=out,
+                                  k_rot=kbig[128:].view(shp))
+    assert e.value.name == "ERR_ALIAS"
     tabs.close()
 
 
@@ -135,7 +215,8 @@ def test_na3d_full_size_sampled():
     """The attention workload bench.py times (1 x 16 x 64 x 64 tokens, 16
     heads x 128, bf16, window 3 x 7 x 7, same seeds), launched as the bench
     launches it: 192 sampled queries of the fused kernel against the oracle
-    computed one query at a time, and the unfused pair bit-identical to it."""
+    computed one query at a time, and the unfused pair and the rotate-once
+    form bit-identical to it."""
     B, T, H, W, heads, split, kernel = 1, 16, 64, 64, 16, (32, 48, 48), (3, 7, 7)
     shape6 = (B, T, H, W, heads, 128)
     shp = (B, T * H * W, heads, 128)
@@ -146,8 +227,12 @@ def test_na3d_full_size_sampled():
     fused = r.rope3d_na3d(q, k, v, tabs, kernel)
     qr, kr = r.rope3d_apply_pair(q, k, tabs)
     unfused = r.rope3d_na3d(qr, kr, v, tabs, kernel, apply_rope=False)
+    once, k_rot = r.rope3d_na3d_rotate_once(q, k, v, tabs, kernel)
     torch.cuda.synchronize()
     assert torch.equal(fused.view(torch.int16), unfused.view(torch.int16))
+    assert torch.equal(once.view(torch.int16), unfused.view(torch.int16))
+    assert torch.equal(k_rot.view(torch.int16), kr.view(torch.int16))
+    del once, k_rot
     queries = _bench_queries(B, T, H, W, heads, 192, 304)
     got_all = fused.view(shape6)
     got = to_f64(torch.stack([got_all[b, t, h, w, e] for b, t, h, w, e in queries]))
@@ -159,7 +244,8 @@ def test_na3d_full_size_sampled():
     tabs.close()
 
 
-def test_na3d_large_scores_rescale_often():
+@pytest.mark.parametrize("path", PATHS)
+def test_na3d_large_scores_rescale_often(path):
     """Q and K with sigma 3: scores spread over tens of log2 units, so row
     maxima jump by more than 2^8 from chunk to chunk and the running
     reference (and O, l) is rescaled many times; still within the bound."""
@@ -172,7 +258,7 @@ def test_na3d_large_scores_rescale_often():
     shp = (B, T * H * W, heads, 128)
     q, k, v = (bf16(a).reshape(shp).to(DEV) for a in (q_np, k_np, v_np))
     tabs = r.rope3d_build_tables(T, H, W, split)
-    out = r.rope3d_na3d(q, k, v, tabs, kernel)
+    out = attend(path, q, k, v, tabs, kernel)
     torch.cuda.synchronize()
     got = to_f64(out).reshape(shape6)
     otabs = oracle.tables(T, H, W, split)
