@@ -667,20 +667,33 @@ rope3d_na3d_kernel(const NAParams p) {
         cur = nxt;
     }
 
-    // ---- normalise and store
+    // ---- normalise into a shared-memory tile (over K's first buffer, free
+    // once every warp is past the last chunk), then store it as coalesced
+    // 16-byte vectors, 16 threads per 256-byte row
+    __syncthreads();
+    uint16_t *sO = sK;   // [kQB][kRow]; block row r = warp 16 + 8 half + g
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-        if (!(r == 0 ? rvalid0 : rvalid1)) continue;
         const float l = r == 0 ? l0 : l1;
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        const long long oo = batch0 - cv * 8 + qt * frame + (hq + r) * grid_row + (long long)wq * tok;
-        if (!bound_ok(oo, kHD, p.total)) continue;
-        uint16_t *dst = p.out + oo;
+        uint16_t *row = sO + (warp * 16 + 8 * r + g) * kRow + 2 * tq;
 #pragma unroll
-        for (int n = 0; n < kHD / 8; ++n) {
-            const uint32_t pk = pack_bf16(o[n][2 * r] * inv, o[n][2 * r + 1] * inv);
-            *reinterpret_cast<uint32_t *>(dst + n * 8 + 2 * tq) = pk;
-        }
+        for (int n = 0; n < kHD / 8; ++n)
+            *reinterpret_cast<uint32_t *>(row + n * 8) =
+                pack_bf16(o[n][2 * r] * inv, o[n][2 * r + 1] * inv);
+    }
+    __syncthreads();
+    // (not unrolled: unrolled, this loop made ptxas spill 96 bytes and the
+    // kernel 16 % slower)
+    const int hb = hq - 2 * warp, wb = wq - g;   // the block's first row and column
+#pragma unroll 1
+    for (int m = 0; m < kVecs; ++m) {
+        const int r = slot0 + 8 * m;
+        const int h = hb + r / kQBW, w = wb + r % kQBW;
+        const long long oo = batch0 + qt * frame + h * grid_row + (long long)w * tok;
+        if (h < p.H && w < p.W && bound_ok(oo, 8, p.total))
+            *reinterpret_cast<uint4 *>(p.out + oo) =
+                *reinterpret_cast<const uint4 *>(sO + r * kRow + cv * 8);
     }
 }
 
