@@ -338,6 +338,20 @@ int rope3d_na3d_rotate_once(const void *q, const void *k, const void *v, void *k
                             const int32_t split[3], const int32_t kernel_size[3], void *stream);
 
 /*
+ * rope3d_na3d_preflight -- the checks of rope3d_na3d (k_rot NULL) or of
+ * rope3d_na3d_rotate_once (k_rot given) without a launch: the status that
+ * call would return before launching. apply_rope as for rope3d_na3d (implied
+ * when k_rot is given). check_device = 0 skips the device queries (the
+ * tables' device and the pointers' memory type), so the pointer, size,
+ * window, alignment, overlap and table-key checks run without a GPU.
+ */
+int rope3d_na3d_preflight(const void *q, const void *k, const void *v, const void *k_rot,
+                          const void *out, const rope3d_tables *tables, int64_t B, int64_t T,
+                          int64_t H, int64_t W, int64_t heads, int64_t head_dim,
+                          const int32_t split[3], const int32_t kernel_size[3],
+                          int32_t apply_rope, int32_t check_device);
+
+/*
  * rope3d_apply_pair_host -- the same rotation for HOST buffers: the library
  * streams Q and K to the GPU in token chunks, rotates each chunk with the same
  * kernel, and streams Q_out and K_out back, overlapping the two copy

@@ -30,7 +30,7 @@ __all__ = [
     "rope3d_apply_pair_strided", "rope3d_preflight_strided", "view_strides",
     "rope3d_patchify", "rope3d_unpatchify", "rope3d_patchify_check", "rope3d_patchify_last_kernel",
     "rope3d_apply_neox", "rope3d_neox_check", "rope3d_neox_cache_host", "rope3d_neox_last_kernel",
-    "rope3d_na3d", "rope3d_na3d_rotate_once", "rope3d_debug_bounds",
+    "rope3d_na3d", "rope3d_na3d_rotate_once", "rope3d_na3d_preflight", "rope3d_debug_bounds",
     "rope3d_testing_debug_shrink_tables",
 ]
 
@@ -101,6 +101,7 @@ def _declare(lib):
         "rope3d_neox_last_kernel": ([], c.c_int),
         "rope3d_na3d": ([vp] * 5 + [i64] * 6 + [vp, vp, i32, vp], c.c_int),
         "rope3d_na3d_rotate_once": ([vp] * 6 + [i64] * 6 + [vp, vp, vp], c.c_int),
+        "rope3d_na3d_preflight": ([vp] * 6 + [i64] * 6 + [vp, vp, i32, i32], c.c_int),
         "rope3d_preflight_strided": ([vp, vp, vp, vp, vp] + [i64] * 6 + [vp, i32] + [vp] * 4 + [i32],
                                      c.c_int),
     }
@@ -536,6 +537,21 @@ def rope3d_na3d_rotate_once(q, k, v, tables: Tables, kernel_size, out=None, k_ro
         tables.W, heads, head_dim, _split(tables.split), ks, _stream(stream, q))
     _check(rc, "rope3d_na3d_rotate_once")
     return out, k_rot
+
+
+def rope3d_na3d_preflight(q, k, v, k_rot, out, tables, B, T, H, W, heads, kernel_size,
+                          apply_rope=True, head_dim=128, split=None, check_device=True) -> str:
+    """Status name that rope3d_na3d (k_rot None) or rope3d_na3d_rotate_once
+    would return before launching; pointers may be plain integers."""
+    handle = tables.handle if isinstance(tables, Tables) else (tables or 0)
+    if split is None and isinstance(tables, Tables):
+        split = tables.split
+    ks = (ctypes.c_int32 * 3)(*[int(x) for x in kernel_size])
+    rc = load_library().rope3d_na3d_preflight(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(k_rot), _ptr(out), handle, int(B), int(T), int(H),
+        int(W), int(heads), int(head_dim), _split(split) if split is not None else None, ks,
+        1 if apply_rope else 0, 1 if check_device else 0)
+    return STATUS.get(rc, str(rc))
 
 
 def rope3d_preflight(q, k, q_out, k_out, tables, B, T, H, W, heads, head_dim, split, dtype,

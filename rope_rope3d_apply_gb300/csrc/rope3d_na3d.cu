@@ -804,12 +804,15 @@ int64_t na3d_bound_errors(bool reset) {
 namespace {
 
 // The checks and kernel arguments shared by rope3d_na3d and
-// rope3d_na3d_rotate_once (apply_rope: the tables are used).
-int na3d_setup(const void *q, const void *k, const void *v, const void *out,
-               const rope3d_tables *tables, int64_t B, int64_t T, int64_t H, int64_t W,
-               int64_t heads, int64_t head_dim, const int32_t split[3],
-               const int32_t kernel_size[3], bool apply_rope, NAParams &p) {
-    if (!q || !k || !v || !out || !kernel_size || (apply_rope && (!tables || !split)))
+// rope3d_na3d_rotate_once (apply_rope: the tables are used; with_k_rot: the
+// k_rot buffer of rope3d_na3d_rotate_once). The pointer, size, overlap and
+// table-key checks make no CUDA call; check_device adds the device queries.
+int na3d_setup(const void *q, const void *k, const void *v, const void *out, const void *k_rot,
+               bool with_k_rot, const rope3d_tables *tables, int64_t B, int64_t T, int64_t H,
+               int64_t W, int64_t heads, int64_t head_dim, const int32_t split[3],
+               const int32_t kernel_size[3], bool apply_rope, bool check_device, NAParams &p) {
+    if (!q || !k || !v || !out || !kernel_size || (apply_rope && (!tables || !split)) ||
+        (with_k_rot && !k_rot))
         return ROPE3D_ERR_NULL;
     if (B <= 0 || T <= 0 || H <= 0 || W <= 0 || heads <= 0) return ROPE3D_ERR_SHAPE;
     if (head_dim != kHD) return ROPE3D_ERR_SHAPE;
@@ -819,14 +822,19 @@ int na3d_setup(const void *q, const void *k, const void *v, const void *out,
     if (kt < 1 || kh < 1 || kw < 1 || kt % 2 == 0 || kh % 2 == 0 || kw % 2 == 0 || kt > T ||
         kh > H || kw > W)
         return ROPE3D_ERR_SHAPE;
-    for (const void *ptr : {q, k, v, out})
+    for (const void *ptr : {q, k, v, out, with_k_rot ? k_rot : q})
         if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return ROPE3D_ERR_ALIGN;
     const uint64_t bytes = uint64_t(B * T * H * W * heads) * kHD * 2;
-    const uintptr_t o = reinterpret_cast<uintptr_t>(out);
-    for (const void *ptr : {q, k, v}) {
-        const uintptr_t x = reinterpret_cast<uintptr_t>(ptr);
-        if (o < x + bytes && x < o + bytes) return ROPE3D_ERR_ALIAS;
-    }
+    auto overlap = [bytes](const void *a, const void *b) {
+        const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+        return x < y + bytes && y < x + bytes;
+    };
+    for (const void *ptr : {q, k, v})
+        if (overlap(out, ptr)) return ROPE3D_ERR_ALIAS;
+    // k_rot is k itself (rotation in place) or overlaps nothing
+    if (with_k_rot)
+        for (const void *ptr : {q, k, v, out})
+            if (!(ptr == k && k_rot == k) && overlap(k_rot, ptr)) return ROPE3D_ERR_ALIAS;
     p = NAParams{};
     if (apply_rope) {
         const float2 *dev = nullptr;
@@ -844,9 +852,11 @@ int na3d_setup(const void *q, const void *k, const void *v, const void *out,
             split[2] % 8)
             return ROPE3D_ERR_SHAPE;
         if (len * sizeof(float2) > kMaxTableBytes) return ROPE3D_ERR_SHAPE;
-        int cur = 0;
-        if (cudaGetDevice(&cur) != cudaSuccess) return ROPE3D_ERR_CUDA;
-        if (host_backed || tdev != cur) return ROPE3D_ERR_DEVICE;
+        if (check_device) {
+            int cur = 0;
+            if (cudaGetDevice(&cur) != cudaSuccess) return ROPE3D_ERR_CUDA;
+            if (host_backed || tdev != cur) return ROPE3D_ERR_DEVICE;
+        }
         p.tab = dev;
         p.tab_len = len;
         p.offH = offs[1];
@@ -855,10 +865,16 @@ int na3d_setup(const void *q, const void *k, const void *v, const void *out,
         p.pH = split[1] / 2;
         p.pW = split[2] / 2;
     }
-    int device = 0;
-    if (cudaGetDevice(&device) != cudaSuccess) return ROPE3D_ERR_CUDA;
-    for (const void *ptr : {q, k, v, out})
-        if (!on_device(ptr, device)) return ROPE3D_ERR_DEVICE;
+    if (with_k_rot && uint64_t(heads) * (kHD / 8) > rope3d::kMaxUnitsPerLaunch)
+        return ROPE3D_ERR_SHAPE;
+    const uint64_t blocks = uint64_t(B) * heads * T * ((H + kQBH - 1) / kQBH) * ((W + kQBW - 1) / kQBW);
+    if (blocks > 0x7fffffffull) return ROPE3D_ERR_SHAPE;
+    if (check_device) {
+        int device = 0;
+        if (cudaGetDevice(&device) != cudaSuccess) return ROPE3D_ERR_CUDA;
+        for (const void *ptr : {q, k, v, out, with_k_rot ? k_rot : q})
+            if (!on_device(ptr, device)) return ROPE3D_ERR_DEVICE;
+    }
 
     p.q = static_cast<const uint16_t *>(q);
     p.k = static_cast<const uint16_t *>(k);
@@ -876,8 +892,6 @@ int na3d_setup(const void *q, const void *k, const void *v, const void *out,
     p.nbw = int((W + kQBW - 1) / kQBW);
     p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(kHD)));
     p.total = static_cast<unsigned long long>(B * T * H * W * heads) * kHD;
-    const uint64_t blocks = uint64_t(B) * heads * T * p.nbh * p.nbw;
-    if (blocks > 0x7fffffffull) return ROPE3D_ERR_SHAPE;
     return ROPE3D_OK;
 }
 
@@ -908,8 +922,8 @@ extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *ou
                            int64_t W, int64_t heads, int64_t head_dim, const int32_t split[3],
                            const int32_t kernel_size[3], int32_t apply_rope, void *stream) {
     NAParams p;
-    const int rc = na3d_setup(q, k, v, out, tables, B, T, H, W, heads, head_dim, split,
-                              kernel_size, apply_rope != 0, p);
+    const int rc = na3d_setup(q, k, v, out, nullptr, false, tables, B, T, H, W, heads, head_dim,
+                              split, kernel_size, apply_rope != 0, true, p);
     if (rc != ROPE3D_OK) return rc;
     if (!na3d_attributes()) return ROPE3D_ERR_CUDA;
     const size_t smem = kFixedSmem + (apply_rope ? size_t(p.tab_len) * sizeof(float2) : 0);
@@ -928,23 +942,9 @@ extern "C" int rope3d_na3d_rotate_once(const void *q, const void *k, const void 
                                        int64_t head_dim, const int32_t split[3],
                                        const int32_t kernel_size[3], void *stream) {
     NAParams p;
-    int rc = na3d_setup(q, k, v, out, tables, B, T, H, W, heads, head_dim, split, kernel_size,
-                        true, p);
+    const int rc = na3d_setup(q, k, v, out, k_rot, true, tables, B, T, H, W, heads, head_dim,
+                              split, kernel_size, true, true, p);
     if (rc != ROPE3D_OK) return rc;
-    if (!k_rot) return ROPE3D_ERR_NULL;
-    if (reinterpret_cast<uintptr_t>(k_rot) % 16 != 0) return ROPE3D_ERR_ALIGN;
-    // k_rot is k (in place) or overlaps nothing
-    const uint64_t bytes = p.total * 2;
-    const uintptr_t r = reinterpret_cast<uintptr_t>(k_rot);
-    for (const void *ptr : {q, k, v, static_cast<const void *>(out)}) {
-        const uintptr_t x = reinterpret_cast<uintptr_t>(ptr);
-        if (ptr == k && k_rot == k) continue;
-        if (r < x + bytes && x < r + bytes) return ROPE3D_ERR_ALIAS;
-    }
-    int device = 0;
-    if (cudaGetDevice(&device) != cudaSuccess) return ROPE3D_ERR_CUDA;
-    if (!on_device(k_rot, device)) return ROPE3D_ERR_DEVICE;
-    if (uint64_t(heads) * (kHD / 8) > rope3d::kMaxUnitsPerLaunch) return ROPE3D_ERR_SHAPE;
     if (!na3d_attributes()) return ROPE3D_ERR_CUDA;
     static const int sms = [] {
         int dev = 0, n = 0;
@@ -1004,4 +1004,16 @@ extern "C" int rope3d_na3d_rotate_once(const void *q, const void *k, const void 
         return ROPE3D_ERR_CUDA;
     }
     return ROPE3D_OK;
+}
+
+extern "C" int rope3d_na3d_preflight(const void *q, const void *k, const void *v, const void *k_rot,
+                                     const void *out, const rope3d_tables *tables, int64_t B,
+                                     int64_t T, int64_t H, int64_t W, int64_t heads,
+                                     int64_t head_dim, const int32_t split[3],
+                                     const int32_t kernel_size[3], int32_t apply_rope,
+                                     int32_t check_device) {
+    NAParams p;
+    return na3d_setup(q, k, v, out, k_rot, k_rot != nullptr, tables, B, T, H, W, heads, head_dim,
+                      split, kernel_size, apply_rope != 0 || k_rot != nullptr, check_device != 0,
+                      p);
 }

@@ -326,6 +326,45 @@ def test_patchify_host_checks(lib):
     assert r.rope3d_patchify_check(P, Q, 1, 3, 2, 9, 9, 3, 1) == "OK"
 
 
+def test_na3d_host_checks(lib, host_tables):
+    """The argument checks of rope3d_na3d and rope3d_na3d_rotate_once without
+    a GPU: tables in host memory, addresses that are never dereferenced."""
+    T, H, W, heads = 3, 8, 8, 2
+    tabs = r.rope3d_build_tables(T, H, W, (32, 48, 48))
+    base, step = 1 << 32, 1 << 24     # tensors of 98,304 bytes, far apart
+    q, k, v, kr, out = (base + i * step for i in range(5))
+
+    def chk(*a, **kw):
+        return r.rope3d_na3d_preflight(*a, check_device=False, **kw)
+
+    args = (tabs, 1, T, H, W, heads, (3, 3, 3))
+    assert chk(q, k, v, None, out, *args) == "OK"
+    assert chk(q, k, v, kr, out, *args) == "OK"
+    assert chk(q, k, v, k, out, *args) == "OK"                      # K rotated in place
+    assert chk(q, k, v, None, out, None, 1, T, H, W, heads, (3, 3, 3), apply_rope=False) == "OK"
+    # pointers
+    assert chk(0, k, v, None, out, *args) == "ERR_NULL"
+    assert chk(q, k, v, None, 0, *args) == "ERR_NULL"
+    assert chk(q, k, v, None, out, None, 1, T, H, W, heads, (3, 3, 3),
+               split=(32, 48, 48)) == "ERR_NULL"                   # rotation without tables
+    assert chk(q + 8, k, v, None, out, *args) == "ERR_ALIGN"
+    assert chk(q, k, v, kr + 8, out, *args) == "ERR_ALIGN"
+    # overlaps: out with an input; k_rot with anything but exactly k
+    assert chk(q, k, v, None, q + 4096, *args) == "ERR_ALIAS"
+    for bad in (q, v, out, k + 4096, k - 4096):
+        assert chk(q, k, v, bad, out, *args) == "ERR_ALIAS", bad - base
+    # windows and sizes
+    assert chk(q, k, v, None, out, tabs, 1, T, H, W, heads, (2, 3, 3)) == "ERR_SHAPE"   # even
+    assert chk(q, k, v, None, out, tabs, 1, T, H, W, heads, (5, 3, 3)) == "ERR_SHAPE"   # > T
+    assert chk(q, k, v, None, out, *args, head_dim=64) == "ERR_SHAPE"
+    # the tables' key, and chunks the kernel's 16-byte vectors cannot take
+    assert chk(q, k, v, None, out, tabs, 1, T, H + 1, W, heads, (3, 3, 3)) == "ERR_TABLES"
+    odd = r.rope3d_build_tables(T, H, W, (36, 44, 48))
+    assert chk(q, k, v, kr, out, odd, 1, T, H, W, heads, (3, 3, 3)) == "ERR_SHAPE"
+    odd.close()
+    tabs.close()
+
+
 def test_neox_cache_matches_oracle_bitwise(lib):
     for max_pos, d, base in [(64, 16, 10000.0), (4096, 256, 10000.0), (33, 6, 1e6)]:
         got = r.rope3d_neox_cache_host(max_pos, d, base)
