@@ -60,19 +60,26 @@ constexpr int kUnroll = ROPE3D_UNROLL;
 #define ROPE3D_VEC_BOUNDS __launch_bounds__(kBlock)
 #endif
 
-// Strided vector kernel: vectors per tensor in flight per thread, and the
-// resident CTAs per SM its register budget is sized for.
+// Strided vector kernel: threads per CTA, vectors per tensor in flight per
+// thread, and the resident CTAs per SM its register budget is sized for. At
+// its 43-44 registers, 384 threads fit three CTAs per SM (1,152 threads) where
+// 512 fit two; measured on a fused QKV buffer rotated in place, 384 x 2 was
+// the fastest of 256-1,024 threads and 2-4 vectors.
+#ifndef ROPE3D_STRIDED_BLOCK
+#define ROPE3D_STRIDED_BLOCK 384
+#endif
 #ifndef ROPE3D_STRIDED_UNROLL
 #define ROPE3D_STRIDED_UNROLL 2
 #endif
 #ifndef ROPE3D_STRIDED_MIN_CTAS
 #define ROPE3D_STRIDED_MIN_CTAS 0
 #endif
+constexpr int kStridedBlock = ROPE3D_STRIDED_BLOCK;
 constexpr int kStridedUnroll = ROPE3D_STRIDED_UNROLL;
 #if ROPE3D_STRIDED_MIN_CTAS > 0
-#define ROPE3D_STRIDED_BOUNDS __launch_bounds__(kBlock, ROPE3D_STRIDED_MIN_CTAS)
+#define ROPE3D_STRIDED_BOUNDS __launch_bounds__(kStridedBlock, ROPE3D_STRIDED_MIN_CTAS)
 #else
-#define ROPE3D_STRIDED_BOUNDS __launch_bounds__(kBlock)
+#define ROPE3D_STRIDED_BOUNDS __launch_bounds__(kStridedBlock)
 #endif
 
 struct KParams {
@@ -606,7 +613,7 @@ int variant_id(int dtype, bool vec16, bool strided, bool same, bool smem) {
 
 // Grid size: enough CTAs to fill every SM at full residency, no more than
 // the work needs.
-cudaError_t grid_for(const void *fn, int vid, size_t smem, uint64_t units, int *grid) {
+cudaError_t grid_for(const void *fn, int vid, size_t smem, uint64_t units, int block, int *grid) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -627,13 +634,13 @@ cudaError_t grid_for(const void *fn, int vid, size_t smem, uint64_t units, int *
     }
     if (dc.occ[vid] == 0 || dc.occ_smem[vid] != smem) {
         int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kBlock, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, block, smem);
         if (e != cudaSuccess) return e;
         dc.occ[vid] = n > 0 ? n : 1;
         dc.occ_smem[vid] = smem;
     }
     const uint64_t full = uint64_t(dc.sm_count) * dc.occ[vid];
-    const uint64_t need = (units + kBlock - 1) / kBlock;
+    const uint64_t need = (units + block - 1) / block;
     *grid = static_cast<int>(need < full ? (need > 0 ? need : 1) : full);
     return cudaSuccess;
 }
@@ -670,6 +677,7 @@ cudaError_t launch_rope3d(const LaunchArgs &a, cudaStream_t stream, LaunchInfo *
         for (int j = 0; j < 5; ++j) same = same && a.strides[i][j] == a.strides[0][j];
     const KernelFn fn = pick(a.dtype, a.vec16, a.strided, same, smem);
     const int vid = variant_id(a.dtype, a.vec16, a.strided, same, smem);
+    const int block = a.vec16 && a.strided ? kStridedBlock : kBlock;
 
     KParams p{};
     p.tab = a.tables;
@@ -717,11 +725,12 @@ cudaError_t launch_rope3d(const LaunchArgs &a, cudaStream_t stream, LaunchInfo *
         p.units = static_cast<uint32_t>(nrows * units_per_row);
         p.row0_mod_N = static_cast<uint32_t>((a.row0 + r) % N);
         int grid = 0;
-        cudaError_t e = grid_for(reinterpret_cast<const void *>(fn), vid, smem_bytes, p.units, &grid);
+        cudaError_t e =
+            grid_for(reinterpret_cast<const void *>(fn), vid, smem_bytes, p.units, block, &grid);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(kBlock);
+        cfg.blockDim = dim3(block);
         cfg.dynamicSmemBytes = smem_bytes;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
@@ -736,7 +745,7 @@ cudaError_t launch_rope3d(const LaunchArgs &a, cudaStream_t stream, LaunchInfo *
         if (info) {
             info->kernel = a.vec16 ? 1 : 2;
             info->grid = grid;
-            info->block = kBlock;
+            info->block = block;
         }
     }
     return cudaSuccess;
