@@ -326,7 +326,9 @@ int rope3d_na3d(const void *q, const void *k, const void *v, void *out,
  *   stream        as rope3d_na3d with apply_rope = 1
  *   k_rot         device, bf16, K's shape, 16-byte aligned, caller-owned;
  *                 receives the rotated K. k_rot == k rotates K in place;
- *                 otherwise k_rot overlaps no other argument.
+ *                 otherwise k_rot overlaps no other argument. In either case
+ *                 k_rot overlaps none of q, v and out (so q may share K's
+ *                 memory only when K is not rotated in place).
  * Two kernels on `stream`, asynchronous; the second is launched with
  * programmatic stream serialization and waits for the first before it reads
  * K. Limits as rope3d_na3d. The bit-exact gate does not run here.

@@ -831,10 +831,14 @@ int na3d_setup(const void *q, const void *k, const void *v, const void *out, con
     };
     for (const void *ptr : {q, k, v})
         if (overlap(out, ptr)) return ROPE3D_ERR_ALIAS;
-    // k_rot is k itself (rotation in place) or overlaps nothing
-    if (with_k_rot)
-        for (const void *ptr : {q, k, v, out})
-            if (!(ptr == k && k_rot == k) && overlap(k_rot, ptr)) return ROPE3D_ERR_ALIAS;
+    // k_rot is k itself (rotation in place) or overlaps nothing; either way it
+    // overlaps none of q, v and out (when K is rotated in place, Q may not
+    // share its memory: the attention reads Q while the K pass may still run)
+    if (with_k_rot) {
+        for (const void *ptr : {q, v, out})
+            if (overlap(k_rot, ptr)) return ROPE3D_ERR_ALIAS;
+        if (k_rot != k && overlap(k_rot, k)) return ROPE3D_ERR_ALIAS;
+    }
     p = NAParams{};
     if (apply_rope) {
         const float2 *dev = nullptr;

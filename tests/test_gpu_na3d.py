@@ -162,6 +162,10 @@ def test_rotate_once_rejections():
     with pytest.raises(r.Rope3dError) as e:
         r.rope3d_na3d_rotate_once(q, k, v, tabs, (3, 3, 3), out=out, k_rot=flat[1:n + 1].view(shp))
     assert e.value.name == "ERR_ALIGN"
+    # K rotated in place while Q is read from the same memory
+    with pytest.raises(r.Rope3dError) as e:
+        r.rope3d_na3d_rotate_once(k, k, v, tabs, (3, 3, 3), out=out, k_rot=k)
+    assert e.value.name == "ERR_ALIAS"
     # k_rot overlapping k without being k (one token further on)
     kbig = torch.zeros(n + 128, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(r.Rope3dError) as e:

@@ -353,6 +353,12 @@ def test_na3d_host_checks(lib, host_tables):
     assert chk(q, k, v, None, q + 4096, *args) == "ERR_ALIAS"
     for bad in (q, v, out, k + 4096, k - 4096):
         assert chk(q, k, v, bad, out, *args) == "ERR_ALIAS", bad - base
+    # Q may share K's memory (both only read), but not when K is rotated in place
+    assert chk(k, k, v, kr, out, *args) == "OK"
+    assert chk(k, k, v, None, out, *args) == "OK"
+    assert chk(k, k, v, k, out, *args) == "ERR_ALIAS"
+    assert chk(k + 4096, k, v, k, out, *args) == "ERR_ALIAS"
+    assert chk(q, k, k + 4096, k, out, *args) == "ERR_ALIAS"     # V inside K, K rotated in place
     # windows and sizes
     assert chk(q, k, v, None, out, tabs, 1, T, H, W, heads, (2, 3, 3)) == "ERR_SHAPE"   # even
     assert chk(q, k, v, None, out, tabs, 1, T, H, W, heads, (5, 3, 3)) == "ERR_SHAPE"   # > T
