@@ -243,7 +243,8 @@ int rope3d_patchify_last_kernel(void);
  *                 head_dim] contiguous, 4-byte aligned
  *   q_out, k_out  device outputs of the same shapes; q_out == q and/or
  *                 k_out == k rotate in place; otherwise an output overlaps
- *                 nothing (nor the positions, cache or counter)
+ *                 no input. An output never overlaps the other input, the
+ *                 other output, the positions, the cache or the counter.
  *   positions     device int64 [tokens], 8-byte aligned
  *   cos_sin_cache device fp32 [max_position][head_dim], 4-byte aligned (16 for
  *                 the vector kernel); rotary_dim is head_dim

@@ -379,10 +379,12 @@ int neox(const void *q, const void *k, void *q_out, void *k_out, const int64_t *
     const uint64_t qb = uint64_t(tokens) * q_heads * head_dim * es;
     const uint64_t kb = uint64_t(tokens) * k_heads * head_dim * es;
     const uint64_t pb = uint64_t(tokens) * 8, cb = uint64_t(max_position) * head_dim * 4;
-    // outputs: in place exactly, or disjoint from everything
+    // outputs: an output is its own input exactly (in place) or disjoint from
+    // it, and never overlaps the other input or the other output (a Q output
+    // written in place over K's memory would be read back by the K units)
     const bool q_in_place = P[2] == P[0], k_in_place = P[3] == P[1];
-    if ((!q_in_place && (overlap(P[2], qb, P[0], qb) || overlap(P[2], qb, P[1], kb))) ||
-        (!k_in_place && (overlap(P[3], kb, P[1], kb) || overlap(P[3], kb, P[0], qb))) ||
+    if ((!q_in_place && overlap(P[2], qb, P[0], qb)) || overlap(P[2], qb, P[1], kb) ||
+        (!k_in_place && overlap(P[3], kb, P[1], kb)) || overlap(P[3], kb, P[0], qb) ||
         overlap(P[2], qb, P[3], kb))
         return ROPE3D_ERR_ALIAS;
     for (int o = 2; o < 4; ++o) {

@@ -390,6 +390,13 @@ def test_neox_host_checks(lib):
     assert r.rope3d_neox_check(swapped, *ok) == "ERR_ALIAS"
     onto_cache = ptrs[:2] + [ptrs[5], ptrs[3]] + ptrs[4:]
     assert r.rope3d_neox_check(onto_cache, *ok) == "ERR_ALIAS"
+    # Q and K may share memory (both only read) unless one is rotated in place
+    same = [ptrs[0], ptrs[0]] + ptrs[2:]
+    assert r.rope3d_neox_check(same, 4096, 100, 8, 8, 256, r.BF16) == "OK"
+    q_in_place_over_k = [ptrs[0], ptrs[0], ptrs[0]] + ptrs[3:]
+    assert r.rope3d_neox_check(q_in_place_over_k, 4096, 100, 8, 8, 256, r.BF16) == "ERR_ALIAS"
+    k_in_place_over_q = [ptrs[0], ptrs[0], ptrs[2], ptrs[0]] + ptrs[4:]
+    assert r.rope3d_neox_check(k_in_place_over_q, 4096, 100, 8, 8, 256, r.BF16) == "ERR_ALIAS"
     assert r.rope3d_neox_check(ptrs, 4096, 100, 8, 4, 255, r.BF16) == "ERR_SHAPE"
     assert r.rope3d_neox_check(ptrs, 4096, 0, 8, 4, 256, r.BF16) == "ERR_SHAPE"
     assert r.rope3d_neox_check(ptrs, 4096, 100, 8, 4, 256, 7) == "ERR_DTYPE"
