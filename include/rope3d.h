@@ -383,18 +383,20 @@ int rope3d_release_scratch(void);
 
 /*
  * rope3d_apply_pair_noalloc -- rope3d_apply_pair for callers that cannot
- * allocate device memory. The sglang PR #35698 kernel has no counterpart: it exists because
- * rope3d_build_tables allocates the cached tables with cudaMalloc, and some
- * callers cannot call cudaMalloc (a process whose device memory belongs to
- * another allocator or a fixed budget, or a pipeline that must not take
- * cudaMalloc's implicit synchronisation). This call takes no table handle:
- * it computes the three axis tables on the host (the values of
+ * allocate device memory. This call has no counterpart in the pages: it
+ * exists because rope3d_build_tables allocates the cached tables with
+ * cudaMalloc, and some callers cannot call cudaMalloc (a process whose device
+ * memory belongs to another allocator or a fixed budget, or a pipeline that
+ * must not take cudaMalloc's implicit synchronisation). This call takes no
+ * table handle: it computes the three axis tables on the host (the values of
  * rope3d_build_tables) and uploads them into a fixed 64 KiB table area in the
  * library's static device memory, then launches the same kernels. It calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *
  *   q, k, q_out, k_out, B, T, H, W, heads, head_dim, split, dtype, stream
- *           as for rope3d_apply_pair (device pointers, caller-owned)
+ *           as for rope3d_apply_pair (device pointers, caller-owned; the
+ *           library cannot see the buffers' extents, so the caller must pass
+ *           buffers of [B, T*H*W, heads, head_dim] elements of `dtype`)
  *   base    RoPE base, finite and > 0
  *
  * Limit: the tables, sum over X of L_X * d_X/2 entries of 8 bytes with each
@@ -403,13 +405,18 @@ int rope3d_release_scratch(void);
  * area belongs to every GPU that loads the library until the process exits.
  * The first call on each device looks up the area's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * The address is kept for the life of the process, so calls after a
+ * cudaDeviceReset of that device are unsupported.
  * Every call shares the one area and leaves its tables there; nothing in it
  * has to start at zero, because each call writes every entry it reads. Calls
  * are serialised on the host, and calls on one stream are ordered, but calls
  * whose work overlaps on the GPU (different streams) race on the area.
  * The upload comes from pageable host memory, so the call waits for earlier
- * work on `stream` before returning. The bit-exact gate does not run here.
- * Errors: as rope3d_apply_pair (without TABLES and PARITY), ARG (base), SCRATCH.
+ * work on `stream` before returning; a stream in capture mode cannot record
+ * that upload and is refused with ROPE3D_ERR_ARG before anything is enqueued.
+ * The bit-exact gate does not run here.
+ * Errors: as rope3d_apply_pair (without TABLES and PARITY), ARG (base, or a
+ * capturing stream), SCRATCH.
  */
 int rope3d_apply_pair_noalloc(const void *q, const void *k, void *q_out, void *k_out,
                               int64_t B, int64_t T, int64_t H, int64_t W,

@@ -222,34 +222,47 @@ def rope3d_build_tables(T: int, H: int, W: int, split, base: float = 10000.0,
     return Tables(out.value)
 
 
-def _geometry(q, tables: Tables):
+def _grid_geometry(q, T: int, H: int, W: int):
     """(B, heads, head_dim) of q laid out as [B, T*H*W, heads, head_dim] or
-    [B, T, H, W, heads, head_dim]."""
+    [B, T, H, W, heads, head_dim] over the grid (T, H, W)."""
     shape = tuple(int(v) for v in q.shape)
-    N = tables.T * tables.H * tables.W
+    grid = (int(T), int(H), int(W))
     if len(shape) == 6:
-        if shape[1:4] != (tables.T, tables.H, tables.W):
-            raise ValueError(f"q grid {shape[1:4]} != tables grid {(tables.T, tables.H, tables.W)}")
+        if shape[1:4] != grid:
+            raise ValueError(f"q grid {shape[1:4]} != the call's grid {grid}")
         return shape[0], shape[4], shape[5]
     if len(shape) == 4:
+        N = grid[0] * grid[1] * grid[2]
         if shape[1] != N:
-            raise ValueError(f"q has {shape[1]} tokens, the tables' grid has {N}")
+            raise ValueError(f"q has {shape[1]} tokens, the grid {grid} has {N}")
         return shape[0], shape[2], shape[3]
     raise ValueError("q must be [B, T*H*W, heads, head_dim] or [B, T, H, W, heads, head_dim]")
 
 
-def _marshal(q, k, q_out, k_out, tables: Tables):
+def _geometry(q, tables: Tables):
+    return _grid_geometry(q, tables.T, tables.H, tables.W)
+
+
+def _marshal_grid(q, k, q_out, k_out, T: int, H: int, W: int):
+    """Checks that the four buffers are contiguous, of q's shape and of q's
+    dtype, and that q covers the grid; returns (B, heads, head_dim, dtype).
+    The C ABI takes bare pointers and cannot see a buffer's extent, so these
+    checks are what keeps a call inside the caller's memory."""
     for name, t in (("q", q), ("k", k), ("q_out", q_out), ("k_out", k_out)):
         if not _contiguous(t):
             raise ValueError(f"{name} must be contiguous")
         if tuple(t.shape) != tuple(q.shape):
             raise ValueError(f"{name} has shape {tuple(t.shape)}, q has {tuple(q.shape)}")
-    B, heads, head_dim = _geometry(q, tables)
+    B, heads, head_dim = _grid_geometry(q, T, H, W)
     dt = _dtype_code(q)
     for t in (k, q_out, k_out):
         if _dtype_code(t) != dt:
             raise TypeError("q, k, q_out and k_out must have one dtype")
     return B, heads, head_dim, dt
+
+
+def _marshal(q, k, q_out, k_out, tables: Tables):
+    return _marshal_grid(q, k, q_out, k_out, tables.T, tables.H, tables.W)
 
 
 def rope3d_apply_pair(q, k, tables: Tables, q_out=None, k_out=None, stream=None):
@@ -285,20 +298,9 @@ def rope3d_apply_pair_noalloc(q, k, q_out, k_out, T: int, H: int, W: int, split,
     """rope3d_apply_pair without a table handle, for callers that cannot
     allocate device memory: the tables go into the library's fixed 64 KiB
     static table area (see include/rope3d.h). q_out and k_out are required;
-    this function allocates nothing."""
-    for name, t in (("q", q), ("k", k), ("q_out", q_out), ("k_out", k_out)):
-        if not _contiguous(t):
-            raise ValueError(f"{name} must be contiguous")
-        if tuple(t.shape) != tuple(q.shape):
-            raise ValueError(f"{name} has shape {tuple(t.shape)}, q has {tuple(q.shape)}")
-    shape = tuple(int(v) for v in q.shape)
-    if len(shape) == 6:
-        B, heads, head_dim = shape[0], shape[4], shape[5]
-    elif len(shape) == 4 and shape[1] == T * H * W:
-        B, heads, head_dim = shape[0], shape[2], shape[3]
-    else:
-        raise ValueError("q must be [B, T*H*W, heads, head_dim] or [B, T, H, W, heads, head_dim]")
-    dt = _dtype_code(q)
+    this function allocates nothing. The buffers are checked as for
+    rope3d_apply_pair: contiguous, one shape and one dtype, covering the grid."""
+    B, heads, head_dim, dt = _marshal_grid(q, k, q_out, k_out, T, H, W)
     rc = load_library().rope3d_apply_pair_noalloc(
         _ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), B, int(T), int(H), int(W), heads, head_dim,
         _split(split), float(base), dt, _stream(stream, q))

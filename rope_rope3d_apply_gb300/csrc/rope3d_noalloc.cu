@@ -15,7 +15,12 @@
 // every GPU that loads the library holds it until the process exits. In host
 // code its name is only a host-side stand-in for the symbol, so the device
 // address is looked up once per device with cudaGetSymbolAddress and that
-// address is what the kernel receives.
+// address is what the kernel receives. The address is kept for the life of
+// the process: calls after a cudaDeviceReset of that device are unsupported.
+//
+// The upload comes from pageable host memory, which a stream in capture mode
+// cannot record; a capturing stream is therefore refused before anything is
+// enqueued, so that the caller's capture is not invalidated.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -95,6 +100,14 @@ extern "C" int rope3d_apply_pair_noalloc(const void *q, const void *k, void *q_o
         if (total > kStaticTableEntries) return ROPE3D_ERR_SCRATCH;
     }
 
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &capture) != cudaSuccess) {
+        cudaGetLastError();
+        return ROPE3D_ERR_CUDA;
+    }
+    if (capture != cudaStreamCaptureStatusNone) return ROPE3D_ERR_ARG;
+
     std::lock_guard<std::mutex> lock(g_mutex);
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return ROPE3D_ERR_CUDA;
@@ -103,7 +116,6 @@ extern "C" int rope3d_apply_pair_noalloc(const void *q, const void *k, void *q_o
     if (rc != ROPE3D_OK) return rc;
 
     for (int a = 0; a < 3; ++a) fill_axis(lengths[a], split[a], base, offset[a]);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     // From pageable memory: returns once the values have been taken from
     // g_host_tables, so the next call may overwrite them.
     if (cudaMemcpyAsync(tables, g_host_tables, total * sizeof(float2), cudaMemcpyHostToDevice,

@@ -415,3 +415,23 @@ def test_normal_build_has_no_bound_checks(lib):
     if os.environ.get("ROPE3D_LIB"):
         pytest.skip("a different build was named")
     assert r.rope3d_debug_bounds() == (False, 0)
+
+
+def test_noalloc_binding_checks_extents_and_dtypes_before_the_call(lib):
+    """The C ABI takes bare pointers, so the binding's checks are what keep a
+    call inside the caller's buffers: a grid that does not match the buffers'
+    shape, or an output dtype other than q's, raises before any library call."""
+    shp6 = (1, 2, 4, 4, 2, 48)
+    q = np.zeros(shp6, np.uint16)
+    k, qo, ko = q.copy(), q.copy(), q.copy()
+    with pytest.raises(ValueError):
+        r.rope3d_apply_pair_noalloc(q, k, qo, ko, 2, 4, 8, (16, 16, 16))
+    with pytest.raises(ValueError):
+        r.rope3d_apply_pair_noalloc(q.reshape(1, 32, 2, 48), k.reshape(1, 32, 2, 48),
+                                    qo.reshape(1, 32, 2, 48), ko.reshape(1, 32, 2, 48),
+                                    2, 4, 2, (16, 16, 16))
+    with pytest.raises(TypeError):
+        r.rope3d_apply_pair_noalloc(q.astype(np.float32), k.astype(np.float32), qo, ko,
+                                    2, 4, 4, (16, 16, 16))
+    with pytest.raises(ValueError):
+        r.rope3d_apply_pair_noalloc(q, k, qo[:, :1], ko, 2, 4, 4, (16, 16, 16))
