@@ -384,3 +384,50 @@ def rope_na3d_at(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, sha
         out[n] = p @ vv
         absv[n] = p @ np.abs(vv)
     return out, absv
+
+
+# ---------------------------------------------------------------------------
+# The LTX DiT's RoPE frequency vector (sglang PR #24660 review, "关键源码片段",
+# ltx_2.py, the frequency generation that replaced _ltx2_rope_freq_grid_np):
+# n = dim // num_rope_elems evenly spaced exponents from 0 to 1, theta raised
+# to each, times pi, halved, the result cast to float32. Every step runs in
+# the page's freqs_dtype: float64 when double_precision is set, else float32.
+# The page then combines the vector with the positions grid and elides how;
+# that part is not defined here.
+#
+# Readings (the page fixes the precision of each step, not the rounding of
+# the framework routines it calls):
+# - linspace value i is the nearest value of the precision to i / (n - 1)
+#   (n = 1 gives the start, 0);
+# - pow is correctly rounded in the precision (float32: the float64 power,
+#   then one rounding to float32);
+# - pi is the nearest value of the precision to pi, the product is rounded
+#   once, and the halving is exact.
+# ---------------------------------------------------------------------------
+
+def dit_rope_freqs(dim: int, num_rope_elems: int, theta: float = 10000.0,
+                   double_precision: bool = True) -> np.ndarray:
+    """float32 [dim // num_rope_elems] frequencies, in the page's order of
+    steps: linspace, pow, times pi, divided by 2, cast."""
+    if dim <= 0 or num_rope_elems <= 0 or dim // num_rope_elems == 0:
+        raise ValueError("dim // num_rope_elems must be at least 1")
+    if not (np.isfinite(theta) and theta > 0):
+        raise ValueError("theta must be finite and > 0")
+    n = dim // num_rope_elems
+    # step 1: linspace(0, 1, n) in freqs_dtype
+    if n == 1:
+        lin = np.zeros(1, np.float64)
+    else:
+        lin = np.arange(n, dtype=np.float64) / np.float64(n - 1)
+    if double_precision:
+        # steps 2-4 in float64
+        pow_indices = np.power(np.float64(theta), lin)
+        freqs = pow_indices * np.float64(np.pi) / np.float64(2.0)
+    else:
+        # steps 2-4 in float32
+        lin32 = lin.astype(np.float32)
+        theta32 = np.float32(theta)
+        pow_indices = np.power(np.float64(theta32), lin32.astype(np.float64)).astype(np.float32)
+        freqs = pow_indices * np.float32(np.pi) / np.float32(2.0)
+    # step 5: cast to float32
+    return freqs.astype(np.float32)
