@@ -448,6 +448,28 @@ int rope3d_axis_table_host(int64_t length, int64_t dim, double base,
                            float *cos_out, float *sin_out);
 
 /*
+ * rope3d_dit_freqs_host -- the RoPE frequency vector of the LTX DiT (sglang
+ * PR #24660 review, "关键源码片段", ltx_2.py, the device-side frequency
+ * generation that replaced _ltx2_rope_freq_grid_np):
+ *     freqs[i] = float32( theta ** linspace(0, 1, n)[i] * pi / 2 ),
+ *     n = dim / num_rope_elems (integer division),
+ * every step in float64 when double_precision != 0, else in float32. How the
+ * page combines the vector with the positions grid is elided there and is not
+ * provided here. Readings of what the page leaves to the framework: linspace
+ * value i is the nearest value of the precision to i / (n - 1) (n = 1 gives
+ * 0); the power is correctly rounded in the precision (the float32 power is
+ * the float64 power rounded once); pi is the nearest value of the precision;
+ * each product is rounded once and the halving is exact.
+ *
+ *   dim, num_rope_elems  > 0 with 1 <= dim / num_rope_elems <= 2^24
+ *   theta                finite and > 0
+ *   out                  caller-owned host memory of dim / num_rope_elems floats
+ * No GPU needed. Errors: NULL, SHAPE, ARG (theta).
+ */
+int rope3d_dit_freqs_host(int64_t dim, int64_t num_rope_elems, double theta,
+                          int32_t double_precision, float *out);
+
+/*
  * rope3d_tables_info -- the key of a handle: dims = (T, H, W), split, base.
  * Any output pointer may be NULL.
  */

@@ -31,7 +31,7 @@ __all__ = [
     "rope3d_patchify", "rope3d_unpatchify", "rope3d_patchify_check", "rope3d_patchify_last_kernel",
     "rope3d_apply_neox", "rope3d_neox_check", "rope3d_neox_cache_host", "rope3d_neox_last_kernel",
     "rope3d_na3d", "rope3d_na3d_rotate_once", "rope3d_na3d_preflight", "rope3d_debug_bounds",
-    "rope3d_testing_debug_shrink_tables",
+    "rope3d_testing_debug_shrink_tables", "rope3d_dit_freqs_host",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -71,6 +71,7 @@ def _declare(lib):
         "rope3d_release_scratch": ([], c.c_int),
         "rope3d_preflight": ([vp, vp, vp, vp, vp] + [i64] * 6 + [vp, i32, i32], c.c_int),
         "rope3d_axis_table_host": ([i64, i64, dbl, vp, vp], c.c_int),
+        "rope3d_dit_freqs_host": ([i64, i64, dbl, i32, vp], c.c_int),
         "rope3d_tables_info": ([vp, vp, vp, vp], c.c_int),
         "rope3d_tables_read": ([vp, i32, i32, vp, vp], c.c_int),
         "rope3d_cache_stats": ([vp, vp, vp, vp], c.c_int),
@@ -574,6 +575,21 @@ def rope3d_axis_table_host(length: int, dim: int, base: float = 10000.0):
     _check(load_library().rope3d_axis_table_host(int(length), int(dim), float(base),
                                                  _ptr(c), _ptr(s)), "rope3d_axis_table_host")
     return c, s
+
+
+def rope3d_dit_freqs_host(dim: int, num_rope_elems: int, theta: float = 10000.0,
+                          double_precision: bool = True):
+    """The LTX DiT's RoPE frequency vector, float32 [dim // num_rope_elems]
+    (see rope3d_dit_freqs_host in include/rope3d.h)."""
+    import numpy as np
+
+    if dim <= 0 or num_rope_elems <= 0:
+        raise ValueError("dim and num_rope_elems must be > 0")
+    out = np.empty(max(dim // num_rope_elems, 1), dtype=np.float32)
+    _check(load_library().rope3d_dit_freqs_host(int(dim), int(num_rope_elems), float(theta),
+                                                int(bool(double_precision)), _ptr(out)),
+           "rope3d_dit_freqs_host")
+    return out
 
 
 def rope3d_tables_read(tables: Tables, axis: int, from_device: bool = False):

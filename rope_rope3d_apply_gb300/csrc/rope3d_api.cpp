@@ -139,6 +139,40 @@ extern "C" int rope3d_axis_table_host(int64_t length, int64_t dim, double base,
     return ROPE3D_OK;
 }
 
+// ----------------------------------------------------------------------------
+// The LTX DiT's RoPE frequency vector: n = dim / num_rope_elems exponents
+// evenly spaced over [0, 1], theta to each power, times pi, halved, cast to
+// float. Every step in double (double_precision) or in float; the float power
+// is the double power rounded once, i.e. correctly rounded except within a
+// double ulp of a float rounding boundary.
+// ----------------------------------------------------------------------------
+extern "C" int rope3d_dit_freqs_host(int64_t dim, int64_t num_rope_elems, double theta,
+                                     int32_t double_precision, float *out) {
+    if (!out) return ROPE3D_ERR_NULL;
+    if (dim <= 0 || num_rope_elems <= 0 || dim / num_rope_elems == 0) return ROPE3D_ERR_SHAPE;
+    if (dim / num_rope_elems > (int64_t(1) << 24)) return ROPE3D_ERR_SHAPE;
+    if (!valid_base(theta)) return ROPE3D_ERR_ARG;
+    const int64_t n = dim / num_rope_elems;
+    const double last = static_cast<double>(n - 1);
+    const double kPi = 3.14159265358979323846;
+    for (int64_t i = 0; i < n; ++i) {
+        // exponent i / (n - 1), rounded once in the working precision
+        const double exponent = n == 1 ? 0.0 : static_cast<double>(i) / last;
+        if (double_precision) {
+            const double scaled = std::pow(theta, exponent) * kPi;
+            out[i] = static_cast<float>(scaled / 2.0);
+        } else {
+            const float exponent_f = static_cast<float>(exponent);
+            const float theta_f = static_cast<float>(theta);
+            const float power_f = static_cast<float>(
+                std::pow(static_cast<double>(theta_f), static_cast<double>(exponent_f)));
+            const float scaled_f = power_f * static_cast<float>(kPi);
+            out[i] = scaled_f / 2.0f;
+        }
+    }
+    return ROPE3D_OK;
+}
+
 extern "C" int rope3d_build_tables(int64_t T, int64_t H, int64_t W, const int32_t split[3],
                                    double base, void *stream, rope3d_tables **out) {
     if (!split || !out) return ROPE3D_ERR_NULL;

@@ -435,3 +435,26 @@ def test_noalloc_binding_checks_extents_and_dtypes_before_the_call(lib):
                                     2, 4, 4, (16, 16, 16))
     with pytest.raises(ValueError):
         r.rope3d_apply_pair_noalloc(q, k, qo[:, :1], ko, 2, 4, 4, (16, 16, 16))
+
+
+@pytest.mark.parametrize("double_precision", [True, False])
+@pytest.mark.parametrize("dim,elems,theta", [
+    (4096, 6, 10000.0), (2048, 2, 10000.0), (128, 6, 10000.0), (3072, 6, 10000.0),
+    (96, 6, 1.0e6), (60, 6, 2.5), (12, 6, 10000.0), (6, 6, 10000.0), (7, 6, 10000.0),
+    (1 << 20, 6, 10000.0), (60, 6, 1.0),
+])
+def test_dit_freqs_match_oracle_bitwise(lib, dim, elems, theta, double_precision):
+    got = r.rope3d_dit_freqs_host(dim, elems, theta, double_precision)
+    want = oracle.dit_rope_freqs(dim, elems, theta, double_precision)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_dit_freqs_rejects(lib):
+    for args, name in [((5, 6, 1e4), "ERR_SHAPE"), ((12, 0, 1e4), "ERR_SHAPE"),
+                       ((12, 6, 0.0), "ERR_ARG"), ((12, 6, float("nan")), "ERR_ARG"),
+                       ((12, 6, -3.0), "ERR_ARG")]:
+        with pytest.raises((r.Rope3dError, ValueError)) as e:
+            r.rope3d_dit_freqs_host(*args)
+        if isinstance(e.value, r.Rope3dError):
+            assert e.value.name == name, args
+    assert lib.rope3d_dit_freqs_host(12, 6, 1e4, 1, None) == -1
