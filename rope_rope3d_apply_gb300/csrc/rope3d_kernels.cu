@@ -82,6 +82,17 @@ constexpr int kStridedUnroll = ROPE3D_STRIDED_UNROLL;
 #define ROPE3D_STRIDED_BOUNDS __launch_bounds__(kStridedBlock)
 #endif
 
+// Tables of the contiguous vector kernel up to this many bytes are staged in
+// shared memory; larger ones are read through the read-only (L1) path.
+#ifndef ROPE3D_VEC_SMEM_TABLE_MAX
+#define ROPE3D_VEC_SMEM_TABLE_MAX (96 * 1024)
+#endif
+// 1: the contiguous vector kernel asks L2 for each thread's first vectors of
+// Q and K before it waits for the previous grid of the stream.
+#ifndef ROPE3D_PREFETCH_FIRST
+#define ROPE3D_PREFETCH_FIRST 0
+#endif
+
 struct KParams {
     const void *q;
     const void *k;
@@ -282,15 +293,30 @@ __device__ __forceinline__ void wait_for_prerequisite_grids() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Stages the tables (kSmem) and waits for the earlier grids; the caller has
+// already let its successor launch.
 template <bool kSmem>
-__device__ __forceinline__ const float2 *stage_tables(const KParams &p, float2 *smem) {
-    allow_dependents_launch();
+__device__ __forceinline__ const float2 *stage_tables_then_wait(const KParams &p, float2 *smem) {
     if constexpr (kSmem) {
         for (uint32_t i = threadIdx.x; i < p.tab_len; i += blockDim.x) smem[i] = __ldg(p.tab + i);
         __syncthreads();
     }
     wait_for_prerequisite_grids();
     return kSmem ? smem : p.tab;
+}
+
+template <bool kSmem>
+__device__ __forceinline__ const float2 *stage_tables(const KParams &p, float2 *smem) {
+    allow_dependents_launch();
+    return stage_tables_then_wait<kSmem>(p, smem);
+}
+
+// A hint that moves the 128-byte line holding ptr into L2. It carries no
+// memory-model meaning: L2 is where every SM of the GPU sees global memory, so
+// a line fetched before an earlier grid writes it is updated there by that
+// write, and a load after griddepcontrol.wait reads the written value.
+__device__ __forceinline__ void prefetch_l2(const void *ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 
 template <bool kSmem>
@@ -323,7 +349,6 @@ template <int kType, bool kSmem>
 __global__ void ROPE3D_VEC_BOUNDS
 rope3d_vec16_kernel(const KParams p, const KStrides) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    const float2 *tab = stage_tables<kSmem>(p, reinterpret_cast<float2 *>(smem_raw));
     constexpr uint32_t kPairsPerVec = kType == ROPE3D_F32 ? 2 : 4;
 
     const uint4 *q = static_cast<const uint4 *>(p.q);
@@ -333,6 +358,18 @@ rope3d_vec16_kernel(const KParams p, const KStrides) {
 
     const uint32_t stride = gridDim.x * blockDim.x;
     uint32_t v = blockIdx.x * blockDim.x + threadIdx.x;
+
+    allow_dependents_launch();
+    if constexpr (ROPE3D_PREFETCH_FIRST != 0) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            if (v + u * stride < p.units) {
+                prefetch_l2(q + v + u * stride);
+                prefetch_l2(k + v + u * stride);
+            }
+        }
+    }
+    const float2 *tab = stage_tables_then_wait<kSmem>(p, reinterpret_cast<float2 *>(smem_raw));
 
     // main loop: kUnroll vectors of Q and of K in flight per thread
     for (; v + (kUnroll - 1) * stride < p.units; v += kUnroll * stride) {
@@ -670,7 +707,10 @@ cudaError_t launch_rope3d(const LaunchArgs &a, cudaStream_t stream, LaunchInfo *
     const uint32_t units_per_head = a.head_dim / elems_per_unit;
     const uint32_t N = a.T * a.H * a.W;
     const size_t table_bytes = size_t(a.table_len) * sizeof(float2);
-    const bool smem = table_bytes <= kMaxSmemTableBytes;
+    const size_t smem_max = a.vec16 && !a.strided
+                                ? std::min<size_t>(ROPE3D_VEC_SMEM_TABLE_MAX, kMaxSmemTableBytes)
+                                : kMaxSmemTableBytes;
+    const bool smem = table_bytes <= smem_max;
     const size_t smem_bytes = smem ? table_bytes : 0;
     bool same = a.strided;
     for (int i = 1; i < 4 && same; ++i)
