@@ -27,7 +27,6 @@ import dataclasses
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -46,7 +45,22 @@ METRIC = "fused 3D RoPE Q+K: achieved HBM GB/s and % of GB300 peak; bit-exact vs
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = [os.path.join(ROOT, "rope_rope3d_apply_gb300", "csrc", "rope3d_kernels.cu")]
-TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "rope3d_vec16_bf16_large.md")
+
+# DRAM traffic of one launch of the contiguous bf16 vector kernel, from one
+# ncu capture (dram__bytes_read.sum, dram__bytes_write.sum; one launch, 2 GB
+# on the device) of the stage-5 tile, 1,073,768,448 algorithmic bytes:
+#   python bench.py --workload stage5 --steps 2 --warmup 3 --no-e2e --no-cpu-baseline
+#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
+#       --clock-control none -k regex:rope3d_vec16_kernel -s 4 -c 1 (the same command)
+# Valid while the kernel source hashes to `kernel_source`; a launch of another
+# size gets the same bytes per algorithmic byte (scaled by the units it moves).
+TRAFFIC_RECORD = {
+    "kernel_source": "ae41e94be201bd5f",
+    "workload": "stage5",
+    "algorithmic_bytes": 1_073_768_448,
+    "dram_read_bytes": 536_930_304,
+    "dram_write_bytes": 485_344_256,
+}
 
 
 def parse_args():
@@ -113,33 +127,83 @@ def kernel_source_hash() -> str:
 
 
 def traffic_per_launch(w: synthetic.Workload):
-    """DRAM bytes per launch from the committed ncu summary, when it was taken
-    on the current kernel source; otherwise None."""
-    try:
-        text = open(TRAFFIC_SUMMARY).read()
-    except OSError:
+    """DRAM bytes of one launch: the recorded capture's bytes per algorithmic
+    byte times this launch's algorithmic bytes, while the kernel source is the
+    one captured (bf16 contiguous calls only); otherwise None."""
+    rec = TRAFFIC_RECORD
+    if w.dtype != "bf16" or kernel_source_hash() != rec["kernel_source"]:
         return None
-    src = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
-    per_byte = re.search(r"dram_bytes_per_algorithmic_byte:\s*([0-9.]+)", text)
-    if not src or not per_byte or src.group(1) != kernel_source_hash():
-        return None
-    return int(float(per_byte.group(1)) * w.bytes_per_call)
+    per_byte = (rec["dram_read_bytes"] + rec["dram_write_bytes"]) / rec["algorithmic_bytes"]
+    return int(per_byte * w.bytes_per_call)
+
+
+class NvmlClocks:
+    """Read-only NVML queries (SM clock, its maximum, the clock-event reasons)
+    through the driver's libnvidia-ml, for one GPU given by PCI bus id."""
+
+    SM = 1  # NVML_CLOCK_SM
+    # reason bits of nvmlDeviceGetCurrentClocksEventReasons, by the names the
+    # nvidia-smi query uses (hw_slowdown includes the power-brake slowdown)
+    REASONS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8 | 0x80),
+               ("sw_thermal_slowdown", 0x20), ("hw_thermal_slowdown", 0x40))
+
+    def __init__(self, pci_bus_id: str):
+        import ctypes
+
+        self.c = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.h)) != 0:
+            raise OSError(f"no NVML device at {pci_bus_id}")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM, ctypes.byref(mx)) != 0:
+            raise OSError("nvmlDeviceGetMaxClockInfo failed")
+        self.max_mhz = float(mx.value)
+
+    def read(self):
+        c = self.c
+        clk, bits = c.c_uint(), c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, c.byref(clk)) != 0:
+            return None
+        if self.reasons_fn(self.h, c.byref(bits)) != 0:
+            return None
+        reasons = [n for n, b in self.REASONS if bits.value & b]
+        return float(clk.value), self.max_mhz, reasons
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons every 100 ms while running."""
+    """SM clocks and throttle reasons while running: NVML every 5 ms (several
+    samples even inside a timed region of a few tens of milliseconds), else
+    nvidia-smi every 100 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_S = 0.005
 
     def __init__(self, gpu_id: str):
         self.gpu = gpu_id
         self.samples = []  # (time, sm_mhz, max_mhz, reasons)
+        self.source = None
         self._proc = None
         self._thread = None
+        self._stop = threading.Event()
 
     def start(self):
+        try:
+            nvml = NvmlClocks(self.gpu)
+        except (OSError, AttributeError):
+            nvml = None
+        if nvml is not None and nvml.read() is not None:
+            self.source = "nvml, every 5 ms"
+            self._thread = threading.Thread(target=self._poll, args=(nvml,), daemon=True)
+            self._thread.start()
+            return
         try:
             self._proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
@@ -148,8 +212,16 @@ class ClockSampler:
         except OSError:
             self._proc = None
             return
+        self.source = "nvidia-smi, every 100 ms"
         self._thread = threading.Thread(target=self._read, daemon=True)
         self._thread.start()
+
+    def _poll(self, nvml):
+        while not self._stop.is_set():
+            s = nvml.read()
+            if s is not None:
+                self.samples.append((time.time(), *s))
+            self._stop.wait(self.PERIOD_S)
 
     def _read(self):
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -165,6 +237,7 @@ class ClockSampler:
             self.samples.append((time.time(), sm, mx, reasons))
 
     def stop(self):
+        self._stop.set()
         if self._proc:
             self._proc.terminate()
             try:
@@ -182,11 +255,12 @@ class ClockSampler:
             mid = 0.5 * (t0 + t1)
             used = [min(self.samples, key=lambda s: abs(s[0] - mid))]
         if not used:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": self.source}
         reasons = sorted({r for s in used for r in s[3]})
         return {"sm_mhz": statistics.median(s[1] for s in used),
                 "sm_max_mhz": max(s[2] for s in used), "reasons": reasons,
-                "samples": len(used), "samples_in_window": len(inside)}
+                "samples": len(used), "samples_in_window": len(inside), "source": self.source}
 
 
 def same_box_copy_gbs(torch, dev, sustained_s: float = 1.0):

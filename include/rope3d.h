@@ -90,8 +90,17 @@ typedef struct rope3d_tables rope3d_tables;  /* opaque, refcounted */
  *
  * A cache hit returns the existing entry (and does not refresh its age). When
  * a 17th entry is inserted the oldest is unlinked from the cache; its memory
- * is freed when its last reference is released, so handles stay valid.
- * Device memory: one buffer per entry, allocated by the library.
+ * is released when its last reference is released, so handles stay valid.
+ * Release is stream-ordered and never waits for the device: every launch that
+ * reads a handle's tables records an event on its stream, and a released
+ * buffer is freed (cudaFreeAsync, on a stream of the library's own) once all
+ * of those events have completed, checked on later calls into the cache
+ * (rope3d_build_tables, rope3d_release_tables, rope3d_cache_clear,
+ * rope3d_cache_retired). Launches into a capturing stream are not tracked: a
+ * CUDA graph that holds such a launch reads the tables on every replay, so
+ * keep a reference to the handle for as long as the graph may run.
+ * Device memory: one buffer per entry from the device's stream-ordered
+ * allocator (cudaMallocAsync on `stream`; cudaMalloc where it is unsupported).
  * Errors: NULL, SHAPE, ARG (bad base), NOMEM, CUDA.
  */
 int rope3d_build_tables(int64_t T, int64_t H, int64_t W, const int32_t split[3],
@@ -491,6 +500,12 @@ int rope3d_cache_stats(int64_t *entries, int64_t *hits, int64_t *misses,
                        int64_t *evictions);
 /* Unlink every entry (held handles stay valid) and zero the counters. */
 int rope3d_cache_clear(void);
+/*
+ * Free the released table buffers whose last launches have completed;
+ * *waiting (may be NULL) receives how many released buffers are still waiting
+ * for launches in flight. Never waits for the device.
+ */
+int rope3d_cache_retired(int64_t *waiting);
 
 /* ---- verification gate ("实现拆解" step 4: BitExactFusionGate) ------------ */
 #define ROPE3D_GATE_OFF   0  /* never verify                                   */

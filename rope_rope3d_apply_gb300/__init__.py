@@ -31,7 +31,7 @@ __all__ = [
     "rope3d_patchify", "rope3d_unpatchify", "rope3d_patchify_check", "rope3d_patchify_last_kernel",
     "rope3d_apply_neox", "rope3d_neox_check", "rope3d_neox_cache_host", "rope3d_neox_last_kernel",
     "rope3d_na3d", "rope3d_na3d_rotate_once", "rope3d_na3d_preflight", "rope3d_debug_bounds",
-    "rope3d_testing_debug_shrink_tables", "rope3d_dit_freqs_host",
+    "rope3d_testing_debug_shrink_tables", "rope3d_dit_freqs_host", "rope3d_cache_retired",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -76,6 +76,7 @@ def _declare(lib):
         "rope3d_tables_read": ([vp, i32, i32, vp, vp], c.c_int),
         "rope3d_cache_stats": ([vp, vp, vp, vp], c.c_int),
         "rope3d_cache_clear": ([], c.c_int),
+        "rope3d_cache_retired": ([vp], c.c_int),
         "rope3d_gate_set_mode": ([i32], c.c_int),
         "rope3d_gate_get_mode": ([], c.c_int),
         "rope3d_gate_reset": ([], c.c_int),
@@ -608,6 +609,14 @@ def rope3d_cache_stats() -> dict:
     v = [ctypes.c_int64() for _ in range(4)]
     _check(load_library().rope3d_cache_stats(*[ctypes.byref(x) for x in v]), "rope3d_cache_stats")
     return dict(zip(("entries", "hits", "misses", "evictions"), (x.value for x in v)))
+
+
+def rope3d_cache_retired() -> int:
+    """Free released table buffers whose launches have completed; returns how
+    many released buffers still wait for launches in flight."""
+    n = ctypes.c_int64()
+    _check(load_library().rope3d_cache_retired(ctypes.byref(n)), "rope3d_cache_retired")
+    return int(n.value)
 
 
 def rope3d_cache_clear():

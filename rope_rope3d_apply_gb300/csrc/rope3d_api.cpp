@@ -57,9 +57,14 @@ struct rope3d_tables {
     // at a multiple of 4 entries
     float2 *dev = nullptr;
     bool host_backed = false;  // test mode: dev points to host memory
+    bool pooled = false;       // dev comes from the stream-ordered allocator
     uint32_t offset[3] = {0, 0, 0};
     uint32_t len = 0;          // float2 entries including padding
     std::atomic<int64_t> refs{0};
+    // Events recorded after the launches that read `dev` and have not been
+    // seen complete yet (oldest first).
+    std::mutex use_mutex;
+    std::deque<cudaEvent_t> uses;
 };
 
 namespace {
@@ -72,25 +77,134 @@ struct CacheState {
     bool host_tables = false;
 } g_cache;
 
-void free_tables(rope3d_tables *t) {
+// ---- releasing table memory in stream order --------------------------------
+// A launch that reads a handle's tables records an event on its stream; when
+// the handle's last reference goes, its buffer is retired and freed only once
+// every one of those events has completed. Nothing waits for the device:
+// retired buffers are checked (and freed) on later calls into the cache.
+
+std::mutex g_event_mutex;                               // guards g_event_pool
+std::map<int, std::vector<cudaEvent_t>> g_event_pool;   // spare events per device
+
+cudaEvent_t take_event(int device) {
+    {
+        std::lock_guard<std::mutex> lock(g_event_mutex);
+        std::vector<cudaEvent_t> &spare = g_event_pool[device];
+        if (!spare.empty()) {
+            cudaEvent_t e = spare.back();
+            spare.pop_back();
+            return e;
+        }
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return e;
+}
+
+void give_event(int device, cudaEvent_t e) {
+    std::lock_guard<std::mutex> lock(g_event_mutex);
+    g_event_pool[device].push_back(e);
+}
+
+// True once the work the event captured has finished. A failed query also
+// counts as finished: the context is then unusable and nothing runs on it.
+bool event_done(cudaEvent_t e) {
+    const cudaError_t rc = cudaEventQuery(e);
+    if (rc == cudaSuccess) return true;
+    cudaGetLastError();  // clear cudaErrorNotReady (or the failure) from the thread's last error
+    return rc != cudaErrorNotReady;
+}
+
+// Drop the completed events of t (all of them when `all`, else from the front
+// up to the first pending one); returns whether none is left. Caller holds
+// t->use_mutex.
+bool prune_uses(rope3d_tables *t, bool all) {
+    for (auto it = t->uses.begin(); it != t->uses.end();) {
+        if (event_done(*it)) {
+            give_event(t->device, *it);
+            it = t->uses.erase(it);
+        } else if (all) {
+            ++it;
+        } else {
+            break;
+        }
+    }
+    return t->uses.empty();
+}
+
+std::mutex g_retire_mutex;                 // guards g_retired and g_release_streams
+std::vector<rope3d_tables *> g_retired;    // released, waiting for their last launches
+std::map<int, cudaStream_t> g_release_streams;
+
+// Free t's memory now (its launches have all completed). Caller holds
+// g_retire_mutex when t is device-backed and pooled.
+void free_now(rope3d_tables *t) {
+    for (cudaEvent_t e : t->uses) give_event(t->device, e);
+    t->uses.clear();
     if (t->dev) {
         if (t->host_backed) {
             std::free(t->dev);
         } else {
-            // work that still reads the tables may be in flight on any stream
-            int cur = 0;
+            int cur = -1;
             cudaGetDevice(&cur);
-            cudaSetDevice(t->device);
-            cudaDeviceSynchronize();
-            cudaFree(t->dev);
-            cudaSetDevice(cur);
+            if (cur != t->device) cudaSetDevice(t->device);
+            if (t->pooled) {
+                // on a stream of the library's own, so that no caller's stream
+                // is ordered behind the free
+                cudaStream_t &rs = g_release_streams[t->device];
+                if (!rs && cudaStreamCreateWithFlags(&rs, cudaStreamNonBlocking) != cudaSuccess) {
+                    rs = nullptr;
+                    cudaGetLastError();
+                }
+                if (!rs || cudaFreeAsync(t->dev, rs) != cudaSuccess) cudaGetLastError();
+            } else {
+                cudaFree(t->dev);
+            }
+            if (cur >= 0 && cur != t->device) cudaSetDevice(cur);
         }
     }
     delete t;
 }
 
+// Free every retired buffer whose launches have completed; returns how many
+// are still waiting.
+int64_t drain_retired() {
+    std::lock_guard<std::mutex> lock(g_retire_mutex);
+    for (auto it = g_retired.begin(); it != g_retired.end();) {
+        rope3d_tables *t = *it;
+        bool done;
+        {
+            std::lock_guard<std::mutex> ul(t->use_mutex);
+            done = prune_uses(t, true);
+        }
+        if (done) {
+            free_now(t);
+            it = g_retired.erase(it);
+        } else {
+            ++it;
+        }
+    }
+    return static_cast<int64_t>(g_retired.size());
+}
+
+void retire(rope3d_tables *t) {
+    std::lock_guard<std::mutex> lock(g_retire_mutex);
+    bool done;
+    {
+        std::lock_guard<std::mutex> ul(t->use_mutex);
+        done = t->host_backed || prune_uses(t, true);
+    }
+    if (done)
+        free_now(t);
+    else
+        g_retired.push_back(t);
+}
+
 void drop_ref(rope3d_tables *t) {
-    if (t->refs.fetch_sub(1) == 1) free_tables(t);
+    if (t->refs.fetch_sub(1) == 1) retire(t);
 }
 
 bool valid_base(double base) { return std::isfinite(base) && base > 0.0; }
@@ -181,6 +295,7 @@ extern "C" int rope3d_build_tables(int64_t T, int64_t H, int64_t W, const int32_
     if (rc != ROPE3D_OK) return rc;
     if (!valid_base(base)) return ROPE3D_ERR_ARG;
 
+    drain_retired();
     int device = -1;
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!g_cache.host_tables) {
@@ -226,15 +341,22 @@ extern "C" int rope3d_build_tables(int64_t T, int64_t H, int64_t W, const int32_
         std::memcpy(t->dev, packed.data(), bytes);
         t->host_backed = true;
     } else {
-        if (cudaMalloc(&t->dev, bytes) != cudaSuccess) {
-            t->dev = nullptr;
-            cudaGetLastError();
-            return ROPE3D_ERR_NOMEM;
-        }
         cudaStream_t s = static_cast<cudaStream_t>(stream);
+        // the stream-ordered allocator, so that a later free waits for no one
+        if (cudaMallocAsync(reinterpret_cast<void **>(&t->dev), bytes, s) == cudaSuccess) {
+            t->pooled = true;
+        } else {
+            cudaGetLastError();
+            if (cudaMalloc(&t->dev, bytes) != cudaSuccess) {
+                t->dev = nullptr;
+                cudaGetLastError();
+                return ROPE3D_ERR_NOMEM;
+            }
+        }
         if (cudaMemcpyAsync(t->dev, packed.data(), bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
             cudaStreamSynchronize(s) != cudaSuccess) {
-            free_tables(t.release());
+            std::lock_guard<std::mutex> rl(g_retire_mutex);
+            free_now(t.release());
             return ROPE3D_ERR_CUDA;
         }
     }
@@ -254,6 +376,39 @@ extern "C" int rope3d_build_tables(int64_t T, int64_t H, int64_t W, const int32_
 extern "C" int rope3d_release_tables(rope3d_tables *tables) {
     if (!tables) return ROPE3D_ERR_NULL;
     drop_ref(tables);
+    drain_retired();
+    return ROPE3D_OK;
+}
+
+extern "C" int rope3d_cache_retired(int64_t *waiting) {
+    const int64_t n = drain_retired();
+    if (waiting) *waiting = n;
+    return ROPE3D_OK;
+}
+
+// Record that a launch on `stream` reads t's tables (see retire()). Launches
+// into a capturing stream are not tracked: a graph keeps using the tables'
+// memory on every replay, so its owner keeps a reference for the graph's life.
+int rope3d::tables_note_use(const rope3d_tables *tc, cudaStream_t stream) {
+    rope3d_tables *t = const_cast<rope3d_tables *>(tc);
+    if (!t) return ROPE3D_ERR_NULL;
+    if (t->host_backed) return ROPE3D_OK;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        return ROPE3D_ERR_CUDA;
+    }
+    if (cap != cudaStreamCaptureStatusNone) return ROPE3D_OK;
+    std::lock_guard<std::mutex> lock(t->use_mutex);
+    prune_uses(t, t->uses.size() > 64);
+    cudaEvent_t e = take_event(t->device);
+    if (!e) return ROPE3D_ERR_CUDA;
+    if (cudaEventRecord(e, stream) != cudaSuccess) {
+        cudaGetLastError();
+        give_event(t->device, e);
+        return ROPE3D_ERR_CUDA;
+    }
+    t->uses.push_back(e);
     return ROPE3D_OK;
 }
 
@@ -322,13 +477,16 @@ extern "C" int rope3d_cache_stats(int64_t *entries, int64_t *hits, int64_t *miss
 }
 
 extern "C" int rope3d_cache_clear(void) {
-    std::lock_guard<std::mutex> lock(g_mutex);
-    while (!g_cache.fifo.empty()) {
-        rope3d_tables *t = g_cache.fifo.front();
-        g_cache.fifo.pop_front();
-        drop_ref(t);
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        while (!g_cache.fifo.empty()) {
+            rope3d_tables *t = g_cache.fifo.front();
+            g_cache.fifo.pop_front();
+            drop_ref(t);
+        }
+        g_cache.hits = g_cache.misses = g_cache.evictions = 0;
     }
-    g_cache.hits = g_cache.misses = g_cache.evictions = 0;
+    drain_retired();
     return ROPE3D_OK;
 }
 
@@ -824,6 +982,7 @@ extern "C" int rope3d_apply_pair(const void *q, const void *k, void *q_out, void
     LaunchInfo info{};
     if (rope3d::launch_rope3d(a, s, &info) != cudaSuccess) return ROPE3D_ERR_CUDA;
     t_last = info;
+    if (rope3d::tables_note_use(tables, s) != ROPE3D_OK) return ROPE3D_ERR_CUDA;
     if (!verify) return ROPE3D_OK;
 
     if (cudaStreamSynchronize(s) != cudaSuccess) return ROPE3D_ERR_CUDA;
@@ -1080,6 +1239,10 @@ extern "C" int rope3d_apply_pair_strided(const void *q, const void *k, void *q_o
         return ROPE3D_ERR_CUDA;
     }
     t_last = info;
+    if (rope3d::tables_note_use(tables, s) != ROPE3D_OK) {
+        free_copies();
+        return ROPE3D_ERR_CUDA;
+    }
     if (!verify) return ROPE3D_OK;
 
     for (int i = 0; i < 2; ++i)
@@ -1232,7 +1395,9 @@ extern "C" int rope3d_apply_pair_host(const void *q, const void *k, void *q_out,
             return ROPE3D_ERR_CUDA;
         const LaunchArgs a = make_launch(g, tables, p.buf[s][0], p.buf[s][1], p.buf[s][2],
                                          p.buf[s][3], n, r, vec16);
-        if (rope3d::launch_rope3d(a, p.s_comp, &info) != cudaSuccess) return ROPE3D_ERR_CUDA;
+        if (rope3d::launch_rope3d(a, p.s_comp, &info) != cudaSuccess ||
+            rope3d::tables_note_use(tables, p.s_comp) != ROPE3D_OK)
+            return ROPE3D_ERR_CUDA;
         if (cudaEventRecord(p.ev_comp[s], p.s_comp) != cudaSuccess ||
             cudaStreamWaitEvent(p.s_d2h, p.ev_comp[s], 0) != cudaSuccess)
             return ROPE3D_ERR_CUDA;

@@ -125,4 +125,8 @@ namespace rope3d {
 // device it lives on, and whether it is the host-memory test mode.
 int tables_layout(const rope3d_tables *t, const float2 **dev, uint32_t *len, uint32_t offsets[3],
                   int64_t dims[3], int32_t split[3], int *device, bool *host_backed);
+// Record that work just enqueued on `stream` reads t's tables, so that t's
+// memory outlives that work when its last reference is released. Returns a
+// ROPE3D_* status.
+int tables_note_use(const rope3d_tables *t, cudaStream_t stream);
 }  // namespace rope3d

@@ -87,6 +87,12 @@ constexpr int kStridedUnroll = ROPE3D_STRIDED_UNROLL;
 #ifndef ROPE3D_VEC_SMEM_TABLE_MAX
 #define ROPE3D_VEC_SMEM_TABLE_MAX (96 * 1024)
 #endif
+// Resident CTAs per SM the contiguous vector kernel's grid is sized for
+// (0: as many as fit). Fewer than fit leave room for the next kernel of the
+// stream to become resident while this one still runs.
+#ifndef ROPE3D_VEC_GRID_CTAS
+#define ROPE3D_VEC_GRID_CTAS 0
+#endif
 // 1: the contiguous vector kernel asks L2 for each thread's first vectors of
 // Q and K before it waits for the previous grid of the stream.
 #ifndef ROPE3D_PREFETCH_FIRST
@@ -650,7 +656,8 @@ int variant_id(int dtype, bool vec16, bool strided, bool same, bool smem) {
 
 // Grid size: enough CTAs to fill every SM at full residency, no more than
 // the work needs.
-cudaError_t grid_for(const void *fn, int vid, size_t smem, uint64_t units, int block, int *grid) {
+cudaError_t grid_for(const void *fn, int vid, size_t smem, uint64_t units, int block, int *grid,
+                     int max_ctas_per_sm = 0) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -676,7 +683,8 @@ cudaError_t grid_for(const void *fn, int vid, size_t smem, uint64_t units, int b
         dc.occ[vid] = n > 0 ? n : 1;
         dc.occ_smem[vid] = smem;
     }
-    const uint64_t full = uint64_t(dc.sm_count) * dc.occ[vid];
+    const int per_sm = max_ctas_per_sm > 0 ? std::min(max_ctas_per_sm, dc.occ[vid]) : dc.occ[vid];
+    const uint64_t full = uint64_t(dc.sm_count) * per_sm;
     const uint64_t need = (units + block - 1) / block;
     *grid = static_cast<int>(need < full ? (need > 0 ? need : 1) : full);
     return cudaSuccess;
@@ -765,8 +773,8 @@ cudaError_t launch_rope3d(const LaunchArgs &a, cudaStream_t stream, LaunchInfo *
         p.units = static_cast<uint32_t>(nrows * units_per_row);
         p.row0_mod_N = static_cast<uint32_t>((a.row0 + r) % N);
         int grid = 0;
-        cudaError_t e =
-            grid_for(reinterpret_cast<const void *>(fn), vid, smem_bytes, p.units, block, &grid);
+        cudaError_t e = grid_for(reinterpret_cast<const void *>(fn), vid, smem_bytes, p.units,
+                                 block, &grid, a.vec16 && !a.strided ? ROPE3D_VEC_GRID_CTAS : 0);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(grid);

@@ -937,6 +937,7 @@ extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *ou
     else
         rope3d_na3d_kernel<kRotNone><<<na3d_blocks(p), kThreads, smem, st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return ROPE3D_ERR_CUDA;
+    if (apply_rope && rope3d::tables_note_use(tables, st) != ROPE3D_OK) return ROPE3D_ERR_CUDA;
     return ROPE3D_OK;
 }
 
@@ -1007,6 +1008,7 @@ extern "C" int rope3d_na3d_rotate_once(const void *q, const void *k, const void 
         cudaGetLastError();
         return ROPE3D_ERR_CUDA;
     }
+    if (rope3d::tables_note_use(tables, st) != ROPE3D_OK) return ROPE3D_ERR_CUDA;
     return ROPE3D_OK;
 }
 

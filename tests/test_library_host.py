@@ -458,3 +458,17 @@ def test_dit_freqs_rejects(lib):
         if isinstance(e.value, r.Rope3dError):
             assert e.value.name == name, args
     assert lib.rope3d_dit_freqs_host(12, 6, 1e4, 1, None) == -1
+
+
+def test_released_host_tables_are_freed_at_once(lib, host_tables):
+    """Host-memory test tables have no launches to wait for: eviction and
+    release free them on the spot."""
+    first = r.rope3d_build_tables(2, 4, 4, (16, 16, 16))
+    others = [r.rope3d_build_tables(2, 4, 5 + i, (16, 16, 16)) for i in range(16)]
+    assert r.rope3d_cache_stats()["evictions"] == 1
+    first.close()
+    assert r.rope3d_cache_retired() == 0
+    for t in others:
+        t.close()
+    r.rope3d_cache_clear()
+    assert r.rope3d_cache_retired() == 0
