@@ -79,6 +79,9 @@ def parse_args():
     p.add_argument("--op", default="rope", choices=["rope", "patchify", "neox", "na3d"],
                    help="rope: the fused 3D RoPE (default); patchify: the decoder's "
                         "space-to-depth layout kernel and its inverse")
+    p.add_argument("--na3d-kernel", type=int, default=0, choices=[0, 1, 2],
+                   help="--op na3d: 0 the library's choice, 1 the tensor-core (tcgen05) "
+                        "attention, 2 the warp-MMA attention")
     p.add_argument("--graph", action="store_true",
                    help="capture one step's calls in a CUDA graph and time its replays")
     p.add_argument("--no-e2e", action="store_true")
@@ -803,6 +806,7 @@ def run_na3d(args):
     q, k, v = (torch.from_numpy(synthetic.normal(n, 1.0, 12, i, "bf16").view(np.int16))
                .view(torch.bfloat16).reshape(shp).to(dev) for i in range(3))
     tabs = r.rope3d_build_tables(c["T"], c["H"], c["W"], c["split"])
+    r.rope3d_testing_na3d_kernel(args.na3d_kernel)
     out = torch.empty_like(q)
     qr, kr = torch.empty_like(q), torch.empty_like(k)
     stream = torch.cuda.current_stream(dev)
@@ -866,6 +870,8 @@ def run_na3d(args):
                      "frac": tflops / peak, "traffic": None,
                      "peak_source": f"{kind} bf16_tflops (cuBLAS burst)", "kernel_ms": ms_once},
         "step": "rope3d_na3d_rotate_once (K pass + attention rotating its Q tiles)",
+        "attention_kernel": {1: "tcgen05 (tensor memory)", 2: "warp-level mma.sync"}.get(
+            r.rope3d_testing_na3d_last_kernel(), "?"),
         "unfused_ms": ms_unfused, "fusion_saving_ms": ms_unfused - ms_once,
         "fused_per_cta_ms": ms_fused,
         "attention_only_ms": ms_attention,

@@ -298,8 +298,9 @@ int rope3d_neox_last_kernel(void);
  * The rotation is rope3d_apply_pair's, bit for bit (bf16 operands); the
  * attention is the published neighbourhood attention: a query attends to the
  * k_t x k_h x k_w window centred on it, shifted inside the grid at borders,
- * with softmax(q.k / sqrt(head_dim)); bf16 tensor-core products, fp32
- * accumulation and softmax, bf16 output.
+ * with softmax(q.k / sqrt(head_dim)); bf16 tensor-core products with fp32
+ * accumulation (see the test hooks below for the two kernels), fp32 softmax,
+ * bf16 output.
  *
  *   q, k, v, out  device, bf16, [B, T, H, W, heads, 128] contiguous, 16-byte
  *                 aligned; out overlaps no input
@@ -362,6 +363,26 @@ int rope3d_na3d_preflight(const void *q, const void *k, const void *v, const voi
                           int64_t H, int64_t W, int64_t heads, int64_t head_dim,
                           const int32_t split[3], const int32_t kernel_size[3],
                           int32_t apply_rope, int32_t check_device);
+
+/*
+ * Test hooks of the neighbourhood attention. Its attention has two kernels:
+ * one on the warp-level MMAs (the default) and one on the fifth-generation
+ * tensor cores (tcgen05 MMAs with fp32 accumulators in tensor memory; 2 x 8 x 8
+ * query blocks; it needs key-region rows of at most 80 keys, i.e.
+ * min(W, kw + 7) <= 80). Both are held to the same bound of the oracle, and
+ * all rotation modes of one kernel give the same bits.
+ *   rope3d_testing_na3d_kernel(which): 0 = the default, 1 = the tensor-core
+ *     kernel where the geometry allows it, 2 = the warp-MMA kernel. Errors: ARG.
+ *   rope3d_testing_na3d_last_kernel(): the kernel of this thread's last
+ *     attention launch: 1 tensor-core, 2 warp-MMA, 0 none yet.
+ *   rope3d_testing_na3d_wait_timeouts(count, reset): how many bounded waits
+ *     of the tensor-core kernel on its MMA completions ran out (0 unless
+ *     something is badly wrong; such a launch's output is not to be used);
+ *     reset clears the count. Synchronises with the device. Errors: NULL, CUDA.
+ */
+int rope3d_testing_na3d_kernel(int32_t which);
+int rope3d_testing_na3d_last_kernel(void);
+int rope3d_testing_na3d_wait_timeouts(int64_t *count, int32_t reset);
 
 /*
  * rope3d_apply_pair_host -- the same rotation for HOST buffers: the library

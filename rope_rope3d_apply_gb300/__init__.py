@@ -32,6 +32,8 @@ __all__ = [
     "rope3d_apply_neox", "rope3d_neox_check", "rope3d_neox_cache_host", "rope3d_neox_last_kernel",
     "rope3d_na3d", "rope3d_na3d_rotate_once", "rope3d_na3d_preflight", "rope3d_debug_bounds",
     "rope3d_testing_debug_shrink_tables", "rope3d_dit_freqs_host", "rope3d_cache_retired",
+    "rope3d_testing_na3d_kernel", "rope3d_testing_na3d_last_kernel",
+    "rope3d_testing_na3d_wait_timeouts",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -77,6 +79,9 @@ def _declare(lib):
         "rope3d_cache_stats": ([vp, vp, vp, vp], c.c_int),
         "rope3d_cache_clear": ([], c.c_int),
         "rope3d_cache_retired": ([vp], c.c_int),
+        "rope3d_testing_na3d_kernel": ([i32], c.c_int),
+        "rope3d_testing_na3d_last_kernel": ([], c.c_int),
+        "rope3d_testing_na3d_wait_timeouts": ([vp, i32], c.c_int),
         "rope3d_gate_set_mode": ([i32], c.c_int),
         "rope3d_gate_get_mode": ([], c.c_int),
         "rope3d_gate_reset": ([], c.c_int),
@@ -609,6 +614,25 @@ def rope3d_cache_stats() -> dict:
     v = [ctypes.c_int64() for _ in range(4)]
     _check(load_library().rope3d_cache_stats(*[ctypes.byref(x) for x in v]), "rope3d_cache_stats")
     return dict(zip(("entries", "hits", "misses", "evictions"), (x.value for x in v)))
+
+
+def rope3d_testing_na3d_kernel(which: int):
+    """0: the tensor-core attention where the geometry allows it (default);
+    1: the same; 2: always the warp-MMA kernel."""
+    _check(load_library().rope3d_testing_na3d_kernel(int(which)), "rope3d_testing_na3d_kernel")
+
+
+def rope3d_testing_na3d_last_kernel() -> int:
+    """1 tensor-core, 2 warp-MMA: the kernel of this thread's last attention launch."""
+    return int(load_library().rope3d_testing_na3d_last_kernel())
+
+
+def rope3d_testing_na3d_wait_timeouts(reset: bool = True) -> int:
+    """Bounded waits of the tensor-core attention that ran out (0 normally)."""
+    n = ctypes.c_int64()
+    _check(load_library().rope3d_testing_na3d_wait_timeouts(ctypes.byref(n), int(bool(reset))),
+           "rope3d_testing_na3d_wait_timeouts")
+    return int(n.value)
 
 
 def rope3d_cache_retired() -> int:

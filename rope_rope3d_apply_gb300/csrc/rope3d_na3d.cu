@@ -37,6 +37,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -762,6 +763,480 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
         p.k_rot[v] = rot_vec_at<true>(ld_v4(p.k + v), p.tab, ts, axis_pos(p, v, ts.axis), p.tab_len);
 }
 
+// ---- the attention on the fifth-generation tensor cores -------------------
+// A CTA of 256 threads owns one (batch, head) and a 2 x 8 x 8 block of queries:
+// the 128 rows of one tcgen05 MMA (M = 128). The union of the block's windows
+// (its key region) is streamed in chunks of whole region rows of one frame,
+// at most kTcN keys each. Per chunk:
+//   1. the chunk's K is copied (cp.async, 16-byte vectors) into a K-major
+//      tile with the 128-byte swizzle; one thread issues S = Q K^T as eight
+//      k16 MMAs (N = the chunk's keys, rounded up to 16) into tensor memory;
+//   2. V is copied meanwhile (V of the previous chunk is no longer read);
+//   3. each query row's S is read back from tensor memory by two threads
+//      (every other 16-key group each: warps w and w + 4 share the 32 lanes
+//      of tensor memory that warp w reaches), masked to the query's window, scaled
+//      and turned into weights with the same online softmax as the warp-MMA
+//      kernel (the reference moves only when a row maximum passes it by more
+//      than 2^kLazy; O in tensor memory is rescaled then);
+//   4. the bf16 weights P go to a K-major swizzled tile, and one thread issues
+//      O += P V as k16 MMAs with V read as an MN-major operand.
+// The next chunk's K is copied while 3 and 4 run. Q (rotated here in the
+// rotating modes) stays in shared memory for every chunk.
+// Shared memory (bytes; every tile 1024-aligned, the swizzle's period):
+//   Q  [2 column blocks][128 rows][128 B]        32,768
+//   K  [2 column blocks][kTcN rows][128 B]       20,480
+//   V  [2 column blocks][kTcN rows][128 B]       20,480
+//   P  [2 column blocks of 64 keys][128][128 B]  32,768
+//   row maxima and sums of the row's threads, two mbarriers, the TMEM address:
+// about 107 KB, so two CTAs share an SM and one's softmax overlaps the
+// other's copies and MMAs. Tensor memory: S in columns [0, N), O in [128, 256)
+// (256 columns per CTA, half of the SM's).
+constexpr int kTcThreads = 256;              // 8 warps: 2 threads per query row
+constexpr int kTcParts = kTcThreads / 128;   // threads (column parts) per query row
+constexpr int kTcM = 128;                    // queries per CTA: 2 x 8 x 8
+constexpr int kTcQT = 2, kTcQH = 8, kTcQW = 8;
+constexpr int kTcN = 80;                     // keys per chunk at most
+constexpr int kTcGroups = (kTcN / 16 + kTcParts - 1) / kTcParts;   // 16-key groups per thread
+constexpr int kTcPBlocks = (kTcN + 63) / 64; // 64-key column blocks of the P tile
+constexpr uint32_t kTcQCb = kTcM * 128;      // bytes of a column block of Q or P
+constexpr uint32_t kTcKvCb = kTcN * 128;     // bytes of a column block of K or V
+constexpr uint32_t kTcOffQ = 0;
+constexpr uint32_t kTcOffK = kTcOffQ + 2 * kTcQCb;
+constexpr uint32_t kTcOffV = kTcOffK + 2 * kTcKvCb;
+constexpr uint32_t kTcOffP = kTcOffV + 2 * kTcKvCb;
+constexpr uint32_t kTcOffRed = kTcOffP + kTcPBlocks * kTcQCb;       // float [2][kTcParts][128]
+constexpr uint32_t kTcOffBar = kTcOffRed + 2 * kTcParts * kTcM * 4;
+constexpr uint32_t kTcSmem = kTcOffBar + 64 + 1024;                 // + room to align to 1024
+constexpr uint32_t kTcColO = 128;                                   // first TMEM column of O
+constexpr uint32_t kTcTmemCols = 256;                               // per CTA: two CTAs per SM
+constexpr int kTcMaxRW = kTcN;                                      // a region row must fit a chunk
+static_assert(kTcOffK % 1024 == 0 && kTcOffV % 1024 == 0 && kTcOffP % 1024 == 0, "1024-aligned tiles");
+static_assert(kTcN % 16 == 0 && kTcN <= int(kTcColO), "S columns stay below O's");
+static_assert(kTcColO + 128 <= kTcTmemCols, "O fits the allocation");
+static_assert(2 * (kTcSmem + 1024) <= 228 * 1024, "two CTAs per SM");
+static_assert(kTcM % kTcParts == 0 && (128 / kTcParts) % 16 == 0, "O columns per thread");
+
+// Waits that gave up (a bounded wait on an MMA completion ran out); they are
+// counted here and reported by rope3d_testing_na3d_wait_timeouts.
+__device__ unsigned int g_na3d_wait_timeouts;
+
+// Shared-memory matrix descriptor of a tcgen05 operand: start address, the
+// leading and stride byte offsets (all in 16-byte units, 14 bits), the fixed
+// 0b001 at bits 46-48, and the 128-byte swizzle (2) in bits 61-63.
+__device__ __forceinline__ uint64_t tc_sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return uint64_t((addr & 0x3FFFFu) >> 4) | (uint64_t((lbo & 0x3FFFFu) >> 4) << 16) |
+           (uint64_t((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of a kind::f16 MMA: fp32 accumulators (bits 4-5 =
+// 1), bf16 A and B (bits 7-9, 10-12 = 1), B read MN-major when b_mn (bit 16),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__device__ __forceinline__ uint32_t tc_idesc(uint32_t m, uint32_t n, uint32_t b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory writes of this thread (plain stores and completed cp.async
+// copies) become visible to the tensor cores' reads.
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Wait for phase `parity` of an mbarrier for at most ~0.1 s of SM clocks.
+// Returns false (and counts) when it gave up; `dead` then skips every later
+// wait of this thread, so a CTA whose MMAs never complete still ends.
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, bool &dead) {
+    if (dead) return false;
+    const long long t0 = clock64();
+    while (true) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+        if (done) return true;
+        if (clock64() - t0 > 200000000ll) {
+            atomicAdd(&g_na3d_wait_timeouts, 1u);
+            dead = true;
+            return false;
+        }
+    }
+}
+
+// 16 consecutive fp32 columns of this warp's 32 lanes of tensor memory (lane
+// = thread), read and waited for.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16};"
+        ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
+          "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])),
+          "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+          "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+          "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+          "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
+// Byte offset of 16-byte chunk c (0..15: 8 elements each) of row `row` in a
+// K-major tile with the 128-byte swizzle: chunk c lies in column block c / 8,
+// and inside a 128-byte row the chunk index is XORed with row mod 8.
+__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t c, uint32_t cb_bytes) {
+    return (c >> 3) * cb_bytes + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+}
+
+// n / d by the multiply-high method of rope3d::FastDiv, its constants made on
+// the device (the region row width differs between border and inner blocks).
+__device__ __forceinline__ rope3d::FastDiv fastdiv_make_dev(uint32_t d) {
+    const uint32_t l = 32u - __clz(d - 1u);   // ceil(log2 d); 0 for d = 1
+    const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
+    return rope3d::FastDiv{d, uint32_t(m), l};
+}
+
+__device__ __forceinline__ void cp_async_wait_group1() {
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(kTcThreads, 2) rope3d_na3d_tc_kernel(const NAParams p, const int nbt) {
+    extern __shared__ unsigned char tc_raw[];
+    unsigned char *sm = tc_raw + ((1024u - (smem_addr(tc_raw) & 1023u)) & 1023u);
+    const uint32_t sQ = smem_addr(sm + kTcOffQ), sK = smem_addr(sm + kTcOffK);
+    const uint32_t sV = smem_addr(sm + kTcOffV), sP = smem_addr(sm + kTcOffP);
+    float *red_max = reinterpret_cast<float *>(sm + kTcOffRed);          // [kTcParts][128]
+    float *red_sum = red_max + kTcParts * kTcM;                           // [kTcParts][128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kTcOffBar);      // S done, O done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kTcOffBar + 16);
+    const uint32_t barS = smem_addr(&bars[0]), barO = smem_addr(&bars[1]);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int lg = warp & 3, qq = warp >> 2;        // TMEM lane group, column part
+    const int row = 32 * lg + lane;                  // this thread's query row
+
+    // which (batch, head, query block)
+    int blk = blockIdx.x;
+    const int bw = blk % p.nbw; blk /= p.nbw;
+    const int bh = blk % p.nbh; blk /= p.nbh;
+    const int bt = blk % nbt; blk /= nbt;
+    const int head = blk % p.heads;
+    const int b = blk / p.heads;
+    const int t0 = bt * kTcQT, h0 = bh * kTcQH, w0 = bw * kTcQW;
+
+    const long long tok = (long long)p.heads * kHD;   // elements per token
+    const long long head0 = (long long)head * kHD;
+    auto token_off = [&](int t, int h, int w) {       // element offset of (b, t, h, w, head, 0)
+        return (((long long)b * p.T + t) * p.H + h) * p.W * tok + (long long)w * tok + head0;
+    };
+
+    // the key region: frames [rt0, rt1), rows [rh0, rh0 + RH), columns [rw0, rw0 + RW)
+    const int rt0 = na_start(t0, p.T, p.kt), rt1 = na_start(min(t0 + 1, p.T - 1), p.T, p.kt) + p.kt;
+    const int rh0 = na_start(h0, p.H, p.kh);
+    const int RH = na_start(min(h0 + kTcQH - 1, p.H - 1), p.H, p.kh) + p.kh - rh0;
+    const int rw0 = na_start(w0, p.W, p.kw);
+    const int RW = na_start(min(w0 + kTcQW - 1, p.W - 1), p.W, p.kw) + p.kw - rw0;
+    const int CH = min(RH, kTcN / RW);               // region rows per chunk (>= 1: RW <= kTcN)
+    const int per_frame = (RH + CH - 1) / CH;
+    const int n_chunks = (rt1 - rt0) * per_frame;
+    const rope3d::FastDiv rwd = fastdiv_make_dev(uint32_t(RW));
+
+    // this thread's query and its window, in region coordinates
+    const int qt = t0 + (row >> 6), qh = h0 + ((row >> 3) & 7), qw = w0 + (row & 7);
+    const bool row_ok = qt < p.T && qh < p.H && qw < p.W;
+    const int st_q = na_start(min(qt, p.T - 1), p.T, p.kt);
+    const int ah = na_start(min(qh, p.H - 1), p.H, p.kh) - rh0;
+    const int aw = na_start(min(qw, p.W - 1), p.W, p.kw) - rw0;
+
+    // ---- set-up: barriers, tensor memory, the Q tile
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(barS) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(barO) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_addr(tmem_slot)), "r"(kTcTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // Q: 128 rows x 16 vectors; thread tid moves vector cv = tid % 16 of rows
+    // tid / 16 + (kTcThreads / 16) m (rotated on the way in the rotating modes)
+    {
+        const int cv = tid & 15;
+        const TabSlot tsg = tab_slot_global(p.pT, p.pH, p.pW, p.offH, p.offW, cv);
+#pragma unroll
+        for (int m = 0; m < kTcM * 16 / kTcThreads; ++m) {
+            const int r = (tid >> 4) + (kTcThreads / 16) * m;
+            const int t = t0 + (r >> 6), h = h0 + ((r >> 3) & 7), w = w0 + (r & 7);
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (t < p.T && h < p.H && w < p.W) {
+                const long long off = token_off(t, h, w) + cv * 8;
+                if (bound_ok(off, 8, p.total)) v = __ldg(reinterpret_cast<const uint4 *>(p.q + off));
+                if constexpr (kMode != kRotNone) {
+                    const int pos = tsg.axis == 0 ? t : (tsg.axis == 1 ? h : w);
+                    v = rot_vec_at<true>(v, p.tab, tsg, uint32_t(pos), p.tab_len);
+                }
+            }
+            *reinterpret_cast<uint4 *>(sm + kTcOffQ + sw128(r, cv, kTcQCb)) = v;
+        }
+    }
+    // K of the rotate-once form comes from the kernel before this one in the
+    // stream (programmatic serialization): wait for it before the first copy
+    if constexpr (kMode == kRotQ) asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // Copy the K (or V) rows of chunk c into tile `dst` (cp.async); rows past
+    // the chunk's keys up to the next multiple of 16 are zeroed. With kRotK the
+    // copied K vectors are rotated in place once they have landed (rot_k).
+    auto chunk_geom = [&](int c, int &f, int &r0, int &keys) {
+        f = rt0 + c / per_frame;
+        r0 = (c % per_frame) * CH;
+        keys = min(CH, RH - r0) * RW;
+    };
+    auto copy_rows = [&](int c, const uint16_t *src, unsigned char *dst) {
+        int f, r0, keys;
+        chunk_geom(c, f, r0, keys);
+        const int nvec = keys * 16;
+        for (int u = tid; u < nvec; u += kTcThreads) {
+            const uint32_t j = uint32_t(u) >> 4, cv = uint32_t(u) & 15;
+            const uint32_t rr = fdiv(j, rwd);
+            const int cc = int(j - rr * uint32_t(RW));
+            const long long off = token_off(f, rh0 + r0 + int(rr), rw0 + cc) + cv * 8;
+            if (bound_ok(off, 8, p.total) && bound_ok(j, 1, kTcN))
+                cp_async16(dst + sw128(j, cv, kTcKvCb), src + off);
+        }
+        const int npad = ((keys + 15) & ~15) - keys;
+        if (tid < npad * 16) {
+            const uint32_t j = uint32_t(keys + (tid >> 4)), cv = uint32_t(tid & 15);
+            if (bound_ok(j, 1, kTcN))
+                *reinterpret_cast<uint4 *>(dst + sw128(j, cv, kTcKvCb)) = make_uint4(0, 0, 0, 0);
+        }
+    };
+    auto rot_k = [&](int c) {
+        int f, r0, keys;
+        chunk_geom(c, f, r0, keys);
+        const int nvec = keys * 16;
+        const TabSlot tsg = tab_slot_global(p.pT, p.pH, p.pW, p.offH, p.offW, tid & 15);
+        for (int u = tid; u < nvec; u += kTcThreads) {
+            const uint32_t j = uint32_t(u) >> 4, cv = uint32_t(u) & 15;
+            const uint32_t rr = fdiv(j, rwd);
+            const int cc = int(j - rr * uint32_t(RW));
+            const int pos = tsg.axis == 0 ? f : (tsg.axis == 1 ? rh0 + r0 + int(rr) : rw0 + cc);
+            uint4 *ptr = reinterpret_cast<uint4 *>(sm + kTcOffK + sw128(j, cv, kTcKvCb));
+            *ptr = rot_vec_at<true>(*ptr, p.tab, tsg, uint32_t(pos), p.tab_len);
+        }
+    };
+
+    copy_rows(0, p.k, sm + kTcOffK);
+    cp_async_commit();
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem + (uint32_t(32 * lg) << 16);            // this warp's lanes
+    const uint32_t tO = tmem + kTcColO + (uint32_t(32 * lg) << 16);
+
+    float m_ref = -INFINITY, l_part = 0.f;   // running reference and this quarter's sum
+    bool dead = false, o_started = false;
+
+    for (int c = 0; c < n_chunks; ++c) {
+        int f, r0, keys;
+        chunk_geom(c, f, r0, keys);
+        const int N = (keys + 15) & ~15, ngrp = N >> 4;
+        // ---- [A] K of chunk c has landed; S = Q K^T
+        cp_async_wait_all();
+        if constexpr (kMode == kRotQK) rot_k(c);
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id = tc_idesc(kTcM, uint32_t(N), 0);
+#pragma unroll
+            for (int ks = 0; ks < kHD / 16; ++ks) {
+                const uint32_t koff = (ks & 3) * 32;   // 16 channels = 32 bytes
+                tc_mma(tmem, tc_sdesc(sQ + (ks >> 2) * kTcQCb + koff, 16, 1024),
+                       tc_sdesc(sK + (ks >> 2) * kTcKvCb + koff, 16, 1024), id, ks > 0);
+            }
+            tc_commit(barS);
+        }
+        // ---- V of chunk c, once O += P V of chunk c - 1 has finished with V and P
+        if (c > 0) tc_wait(barO, uint32_t(c - 1) & 1u, dead);
+        copy_rows(c, p.v, sm + kTcOffV);
+        cp_async_commit();
+        tc_wait(barS, uint32_t(c) & 1u, dead);
+        tc_fence_after();
+
+        // ---- this thread's groups of 16 keys: g = qq, qq + 4, ... First pass:
+        // which keys lie in the query's window (a 16-bit mask per group) and
+        // the largest scaled score among them.
+        const bool frame_ok = row_ok && unsigned(f - st_q) < unsigned(p.kt);
+        uint32_t win[kTcGroups];
+        float cmax = -INFINITY;
+#pragma unroll
+        for (int gi = 0; gi < kTcGroups; ++gi) {
+            win[gi] = 0u;
+            const int g = qq + kTcParts * gi;
+            if (g < ngrp) {
+                float x[16];
+                tc_ld16(tS + uint32_t(16 * g), x);
+                const uint32_t j0 = uint32_t(16 * g);
+                const uint32_t rr = fdiv(j0, rwd);
+                int cc = int(j0 - rr * uint32_t(RW));
+                int rel = r0 + int(rr) - ah;
+                uint32_t bits = 0;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const bool ok = frame_ok && int(j0) + e < keys &&
+                                    unsigned(rel) < unsigned(p.kh) && unsigned(cc - aw) < unsigned(p.kw);
+                    bits |= ok ? 1u << e : 0u;
+                    cmax = fmaxf(cmax, ok ? x[e] * p.scale_log2 : -INFINITY);
+                    if (++cc == RW) {
+                        cc = 0;
+                        ++rel;
+                    }
+                }
+                win[gi] = bits;
+            }
+        }
+        red_max[qq * kTcM + row] = cmax;
+        // ---- [B] every quarter's maximum is in; K is free (S is complete)
+        __syncthreads();
+        if (c + 1 < n_chunks) copy_rows(c + 1, p.k, sm + kTcOffK);
+        cp_async_commit();
+        float rmax = red_max[row];
+#pragma unroll
+        for (int i = 1; i < kTcParts; ++i) rmax = fmaxf(rmax, red_max[i * kTcM + row]);
+        const float mn = fmaxf(m_ref, rmax);
+        // The decision is the same for all threads of the row (the same
+        // inputs); the tensor-memory accesses are made by whole warps.
+        const bool move = mn > m_ref + kLazy;
+        float corr = 1.f;
+        if (move) {
+            corr = m_ref == -INFINITY ? 0.f : ex2(m_ref - mn);
+            m_ref = mn;
+            l_part *= corr;
+        }
+        if (o_started && __any_sync(0xffffffffu, move)) {
+            // O is stable: chunk c - 1's P V has completed (waited above)
+            float o[16];
+#pragma unroll
+            for (int h2 = 0; h2 < 128 / kTcParts / 16; ++h2) {
+                const uint32_t ta = tO + uint32_t(128 / kTcParts * qq + 16 * h2);
+                tc_ld16(ta, o);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o[i] *= corr;
+                tc_st16(ta, o);
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        }
+        // ---- second pass, weights: P (bf16) into the swizzled tile and this
+        // quarter's sum (S is read again: cheaper than keeping it live)
+        const float ms = m_ref == -INFINITY ? 0.f : m_ref;
+#pragma unroll
+        for (int gi = 0; gi < kTcGroups; ++gi) {
+            const int g = qq + kTcParts * gi;
+            if (g < ngrp) {
+                float x[16];
+                tc_ld16(tS + uint32_t(16 * g), x);
+                uint32_t w8[8];
+                float s = 0.f;
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                    const float a0 = (win[gi] >> e) & 1u ? ex2(x[e] * p.scale_log2 - ms) : 0.f;
+                    const float a1 = (win[gi] >> (e + 1)) & 1u ? ex2(x[e + 1] * p.scale_log2 - ms) : 0.f;
+                    s += a0 + a1;
+                    w8[e >> 1] = pack_bf16(a0, a1);
+                }
+                l_part += s;
+                *reinterpret_cast<uint4 *>(sm + kTcOffP + sw128(uint32_t(row), uint32_t(2 * g), kTcQCb)) =
+                    make_uint4(w8[0], w8[1], w8[2], w8[3]);
+                *reinterpret_cast<uint4 *>(sm + kTcOffP + sw128(uint32_t(row), uint32_t(2 * g + 1), kTcQCb)) =
+                    make_uint4(w8[4], w8[5], w8[6], w8[7]);
+            }
+        }
+        // ---- [C] P and V of chunk c are in place; O += P V
+        cp_async_wait_group1();   // V of chunk c (K of chunk c + 1 may still be in flight)
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id = tc_idesc(kTcM, kHD, 1);
+            for (int s = 0; s < ngrp; ++s)
+                tc_mma(tmem + kTcColO, tc_sdesc(sP + (s >> 2) * kTcQCb + (s & 3) * 32, 16, 1024),
+                       tc_sdesc(sV + s * 2048, kTcKvCb, 1024), id, (s > 0 || o_started) ? 1u : 0u);
+            tc_commit(barO);
+        }
+        o_started = true;
+    }
+
+    // ---- normalise and store this thread's quarter (32 channels) of its row
+    tc_wait(barO, uint32_t(n_chunks - 1) & 1u, dead);
+    tc_fence_after();
+    red_sum[qq * kTcM + row] = l_part;
+    __syncthreads();
+    float l = red_sum[row];
+#pragma unroll
+    for (int i = 1; i < kTcParts; ++i) l += red_sum[i * kTcM + row];
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    constexpr int kOCols = 128 / kTcParts;           // channels of this thread
+#pragma unroll
+    for (int h2 = 0; h2 < kOCols / 16; ++h2) {
+        float o[16];
+        tc_ld16(tO + uint32_t(kOCols * qq + 16 * h2), o);
+        uint32_t packed[8];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) packed[i / 2] = pack_bf16(o[i] * inv, o[i + 1] * inv);
+        if (row_ok) {
+            const long long off = token_off(qt, qh, qw) + kOCols * qq + 16 * h2;
+            if (bound_ok(off, 16, p.total)) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.out + off);
+                dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTcTmemCols) : "memory");
+}
+
 bool on_device(const void *ptr, int device) {
     cudaPointerAttributes attr{};
     if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
@@ -903,6 +1378,34 @@ uint32_t na3d_blocks(const NAParams &p) {
     return uint32_t(uint64_t(p.B) * p.heads * p.T * p.nbh * p.nbw);
 }
 
+// The tensor-core (tcgen05) kernel: 2 x 8 x 8 query blocks; it needs a key
+// region row (at most kw + 7 columns, or W) to fit one chunk of kTcN keys.
+int na3d_tc_nbt(const NAParams &p) { return (p.T + kTcQT - 1) / kTcQT; }
+
+uint32_t na3d_tc_blocks(const NAParams &p) {
+    return uint32_t(uint64_t(p.B) * p.heads * na3d_tc_nbt(p) * p.nbh * p.nbw);
+}
+
+// Which attention kernel runs: 0 = the library's default (the warp-MMA
+// kernel, measured faster so far), 1 = the tensor-core kernel where the
+// geometry allows it, 2 = the warp-MMA kernel (rope3d_testing_na3d_kernel).
+std::atomic<int> g_na3d_kernel{0};
+thread_local int g_na3d_last_kernel = 0;   // 1 tensor-core, 2 warp-MMA kernel
+
+bool na3d_use_tc(const NAParams &p) {
+    const int pick = g_na3d_kernel.load(std::memory_order_relaxed);
+    if (pick != 1) return false;
+    return std::min(p.W, p.kw + kTcQW - 1) <= kTcMaxRW;
+}
+
+template <int kMode>
+bool na3d_tc_attribute() {
+    static const bool ok = cudaFuncSetAttribute(rope3d_na3d_tc_kernel<kMode>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                int(kTcSmem)) == cudaSuccess;
+    return ok;
+}
+
 // Dynamic shared memory limits of the three instances, set once.
 bool na3d_attributes() {
     static const bool ok = [] {
@@ -929,13 +1432,24 @@ extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *ou
     const int rc = na3d_setup(q, k, v, out, nullptr, false, tables, B, T, H, W, heads, head_dim,
                               split, kernel_size, apply_rope != 0, true, p);
     if (rc != ROPE3D_OK) return rc;
-    if (!na3d_attributes()) return ROPE3D_ERR_CUDA;
-    const size_t smem = kFixedSmem + (apply_rope ? size_t(p.tab_len) * sizeof(float2) : 0);
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (apply_rope)
-        rope3d_na3d_kernel<kRotQK><<<na3d_blocks(p), kThreads, smem, st>>>(p);
-    else
-        rope3d_na3d_kernel<kRotNone><<<na3d_blocks(p), kThreads, smem, st>>>(p);
+    g_na3d_last_kernel = na3d_use_tc(p) ? 1 : 2;
+    if (na3d_use_tc(p)) {
+        if (apply_rope) {
+            if (!na3d_tc_attribute<kRotQK>()) return ROPE3D_ERR_CUDA;
+            rope3d_na3d_tc_kernel<kRotQK><<<na3d_tc_blocks(p), kTcThreads, kTcSmem, st>>>(p, na3d_tc_nbt(p));
+        } else {
+            if (!na3d_tc_attribute<kRotNone>()) return ROPE3D_ERR_CUDA;
+            rope3d_na3d_tc_kernel<kRotNone><<<na3d_tc_blocks(p), kTcThreads, kTcSmem, st>>>(p, na3d_tc_nbt(p));
+        }
+    } else {
+        if (!na3d_attributes()) return ROPE3D_ERR_CUDA;
+        const size_t smem = kFixedSmem + (apply_rope ? size_t(p.tab_len) * sizeof(float2) : 0);
+        if (apply_rope)
+            rope3d_na3d_kernel<kRotQK><<<na3d_blocks(p), kThreads, smem, st>>>(p);
+        else
+            rope3d_na3d_kernel<kRotNone><<<na3d_blocks(p), kThreads, smem, st>>>(p);
+    }
     if (cudaGetLastError() != cudaSuccess) return ROPE3D_ERR_CUDA;
     if (apply_rope && rope3d::tables_note_use(tables, st) != ROPE3D_OK) return ROPE3D_ERR_CUDA;
     return ROPE3D_OK;
@@ -994,21 +1508,52 @@ extern "C" int rope3d_na3d_rotate_once(const void *q, const void *k, const void 
     // 2. the attention on k_rot, rotating its Q tiles; launched with
     // programmatic serialization, it waits for step 1 before reading K
     p.k = static_cast<const uint16_t *>(k_rot);
+    const bool tc = na3d_use_tc(p);
+    g_na3d_last_kernel = tc ? 1 : 2;
+    if (tc && !na3d_tc_attribute<kRotQ>()) return ROPE3D_ERR_CUDA;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(na3d_blocks(p));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kFixedSmem;
+    cfg.gridDim = dim3(tc ? na3d_tc_blocks(p) : na3d_blocks(p));
+    cfg.blockDim = dim3(tc ? kTcThreads : kThreads);
+    cfg.dynamicSmemBytes = tc ? kTcSmem : kFixedSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, rope3d_na3d_kernel<kRotQ>, p) != cudaSuccess) {
+    const cudaError_t le = tc ? cudaLaunchKernelEx(&cfg, rope3d_na3d_tc_kernel<kRotQ>, p, na3d_tc_nbt(p))
+                              : cudaLaunchKernelEx(&cfg, rope3d_na3d_kernel<kRotQ>, p);
+    if (le != cudaSuccess) {
         cudaGetLastError();
         return ROPE3D_ERR_CUDA;
     }
     if (rope3d::tables_note_use(tables, st) != ROPE3D_OK) return ROPE3D_ERR_CUDA;
+    return ROPE3D_OK;
+}
+
+extern "C" int rope3d_testing_na3d_kernel(int32_t which) {
+    if (which < 0 || which > 2) return ROPE3D_ERR_ARG;
+    g_na3d_kernel.store(which);
+    return ROPE3D_OK;
+}
+
+extern "C" int rope3d_testing_na3d_last_kernel(void) { return g_na3d_last_kernel; }
+
+extern "C" int rope3d_testing_na3d_wait_timeouts(int64_t *count, int32_t reset) {
+    if (!count) return ROPE3D_ERR_NULL;
+    unsigned int n = 0;
+    if (cudaMemcpyFromSymbol(&n, g_na3d_wait_timeouts, sizeof(n)) != cudaSuccess) {
+        cudaGetLastError();
+        return ROPE3D_ERR_CUDA;
+    }
+    if (reset) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_na3d_wait_timeouts, &zero, sizeof(zero)) != cudaSuccess) {
+            cudaGetLastError();
+            return ROPE3D_ERR_CUDA;
+        }
+    }
+    *count = n;
     return ROPE3D_OK;
 }
 

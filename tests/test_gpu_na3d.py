@@ -28,6 +28,18 @@ import rope_rope3d_apply_gb300 as r  # noqa: E402
 
 DEV = torch.device("cuda:0")
 
+# The attention kernels: 1 = tensor-core (tcgen05), 2 = warp-level MMA (the
+# default). Each is held to the same bound.
+KERNELS = [1, 2]
+
+
+@pytest.fixture(autouse=True)
+def _kernel_choice_and_no_timeouts():
+    r.rope3d_testing_na3d_wait_timeouts(reset=True)
+    yield
+    r.rope3d_testing_na3d_kernel(0)
+    assert r.rope3d_testing_na3d_wait_timeouts(reset=True) == 0
+
 
 def bf16(a):
     return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16)
@@ -60,9 +72,11 @@ def attend(path, q, k, v, tabs, kernel):
 PATHS = ["qk", "once"]
 
 
+@pytest.mark.parametrize("which", KERNELS)
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-{c[2]}" for c in CASES])
-def test_na3d_matches_oracle(case, path):
+def test_na3d_matches_oracle(case, path, which):
+    r.rope3d_testing_na3d_kernel(which)
     (B, T, H, W, heads), split, kernel = case
     shape6 = (B, T, H, W, heads, 128)
     n = int(np.prod(shape6))
@@ -74,6 +88,7 @@ def test_na3d_matches_oracle(case, path):
     tabs = r.rope3d_build_tables(T, H, W, split)
     out = attend(path, q, k, v, tabs, kernel)
     torch.cuda.synchronize()
+    assert r.rope3d_testing_na3d_last_kernel() == which
     got = to_f64(out).reshape(shape6)
     otabs = oracle.tables(T, H, W, split)
     ref = oracle.rope_na3d(q_np, k_np, v_np, shape6, split, otabs, kernel)
@@ -88,8 +103,10 @@ def test_na3d_matches_oracle(case, path):
     tabs.close()
 
 
-def test_fused_equals_unfused_bitwise():
+@pytest.mark.parametrize("which", KERNELS)
+def test_fused_equals_unfused_bitwise(which):
     """The fused prologue rotates exactly as rope3d_apply_pair does."""
+    r.rope3d_testing_na3d_kernel(which)
     B, T, H, W, heads, split, kernel = 1, 3, 10, 13, 2, (32, 48, 48), (3, 5, 5)
     shp = (B, T * H * W, heads, 128)
     n = int(np.prod(shp))
@@ -103,11 +120,13 @@ def test_fused_equals_unfused_bitwise():
     tabs.close()
 
 
+@pytest.mark.parametrize("which", KERNELS)
 @pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-{c[2]}" for c in CASES])
-def test_rotate_once_equals_unfused_bitwise(case):
+def test_rotate_once_equals_unfused_bitwise(case, which):
     """K rotated once beforehand and Q in the attention prologue: the unfused
     pair's output bits, and k_rot is rope3d_apply_pair's K_out; the same with
     K rotated in place (k_rot = k)."""
+    r.rope3d_testing_na3d_kernel(which)
     (B, T, H, W, heads), split, kernel = case
     shp = (B, T * H * W, heads, 128)
     n = int(np.prod(shp))
@@ -233,6 +252,7 @@ def test_na3d_full_size_sampled():
     unfused = r.rope3d_na3d(qr, kr, v, tabs, kernel, apply_rope=False)
     once, k_rot = r.rope3d_na3d_rotate_once(q, k, v, tabs, kernel)
     torch.cuda.synchronize()
+    assert r.rope3d_testing_na3d_last_kernel() == 2    # the default: the warp-MMA kernel
     assert torch.equal(fused.view(torch.int16), unfused.view(torch.int16))
     assert torch.equal(once.view(torch.int16), unfused.view(torch.int16))
     assert torch.equal(k_rot.view(torch.int16), kr.view(torch.int16))
@@ -248,11 +268,13 @@ def test_na3d_full_size_sampled():
     tabs.close()
 
 
+@pytest.mark.parametrize("which", KERNELS)
 @pytest.mark.parametrize("path", PATHS)
-def test_na3d_large_scores_rescale_often(path):
+def test_na3d_large_scores_rescale_often(path, which):
     """Q and K with sigma 3: scores spread over tens of log2 units, so row
     maxima jump by more than 2^8 from chunk to chunk and the running
     reference (and O, l) is rescaled many times; still within the bound."""
+    r.rope3d_testing_na3d_kernel(which)
     B, T, H, W, heads, split, kernel = 1, 3, 16, 16, 2, (32, 48, 48), (3, 7, 7)
     shape6 = (B, T, H, W, heads, 128)
     n = int(np.prod(shape6))

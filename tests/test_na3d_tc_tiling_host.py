@@ -1,0 +1,265 @@
+"""A CPU model of the tensor-core neighbourhood-attention kernel's index
+arithmetic (rope_rope3d_apply_gb300/csrc/rope3d_na3d.cu,
+rope3d_na3d_tc_kernel), checked without a GPU.
+
+For every CTA (a 2 x 8 x 8 query block) the model walks the kernel's chunks
+of the key region with the kernel's own integer formulas (region bounds, rows
+per chunk, the row width's multiply-high division) and asserts that:
+  - every global token a thread copies is the key its tile row stands for and
+    lies inside the grid and the region; tile rows past a chunk's keys up to
+    the next multiple of 16 are the zeroed ones, and every shared-memory
+    offset lies in its tile;
+  - the ranges every tcgen05 MMA reads through its shared-memory descriptors
+    (Q, K, P: K-major with the 128-byte swizzle; V: MN-major, column blocks
+    kTcN x 128 bytes apart) lie inside their tiles, the MMA shapes are valid
+    (M = 128, N a multiple of 16 up to 256) and the tensor-memory columns of
+    S and O do not overlap;
+  - each query meets each key of its window exactly once through the
+    per-thread window masks, and no other key.
+It also checks the instruction and shared-memory descriptor encoders against
+the field layout they implement. The attention's arithmetic is left to the
+GPU tests, which compare the outputs with the float64 oracle."""
+from __future__ import annotations
+
+import pytest
+
+TC_N = 80                  # keys per chunk at most
+TC_M = 128                 # queries per CTA
+THREADS = 256              # two threads per query row
+PARTS = THREADS // TC_M
+P_BLOCKS = (TC_N + 63) // 64
+QT, QH, QW = 2, 8, 8
+Q_CB = TC_M * 128          # bytes per column block of Q or P
+KV_CB = TC_N * 128         # bytes per column block of K or V
+OFF_Q, OFF_K = 0, 2 * Q_CB
+OFF_V = OFF_K + 2 * KV_CB
+OFF_P = OFF_V + 2 * KV_CB
+OFF_RED = OFF_P + P_BLOCKS * Q_CB
+COL_O = 128
+TMEM_COLS = 256
+
+
+def na_start(i, L, k):
+    s = max(i - k // 2, 0)
+    return L - k if s + k > L else s
+
+
+def fastdiv_make(d):
+    """The kernel's device-side constants (ceil log2, multiplier)."""
+    l = (d - 1).bit_length() if d > 1 else 0
+    m = ((1 << 32) * ((1 << l) - d)) // d + 1
+    return d, m & 0xFFFFFFFF, l
+
+
+def fdiv(n, f):
+    d, m, l = f
+    return (((n * m) >> 32) + n) >> l
+
+
+def sw128(row, c, cb_bytes):
+    return (c >> 3) * cb_bytes + row * 128 + (((c & 7) ^ (row & 7)) << 4)
+
+
+def sdesc(addr, lbo, sbo):
+    return ((addr & 0x3FFFF) >> 4) | (((lbo & 0x3FFFF) >> 4) << 16) | \
+        (((sbo & 0x3FFFF) >> 4) << 32) | (1 << 46) | (2 << 61)
+
+
+def idesc(m, n, b_mn):
+    return (1 << 4) | (1 << 7) | (1 << 10) | (b_mn << 16) | ((n >> 3) << 17) | ((m >> 4) << 24)
+
+
+def test_descriptor_encoders():
+    # instruction descriptor: D fp32 (bits 4-5), A and B bf16 (7-9, 10-12),
+    # B major (16), N >> 3 (17-22), M >> 4 (24-28); everything else zero
+    for n in range(16, 257, 16):
+        for b_mn in (0, 1):
+            d = idesc(128, n, b_mn)
+            assert (d >> 4) & 3 == 1 and (d >> 7) & 7 == 1 and (d >> 10) & 7 == 1
+            assert (d >> 15) & 1 == 0 and (d >> 16) & 1 == b_mn
+            assert (d >> 17) & 0x3F == n // 8 and (d >> 23) & 1 == 0
+            assert (d >> 24) & 0x1F == 8 and d >> 29 == 0
+            assert d & 0b1111 == 0 and (d >> 6) & 1 == 0 and (d >> 13) & 3 == 0
+    # shared-memory descriptor: 14-bit fields of 16-byte units at 0, 16, 32,
+    # 0b001 at 46-48, the 128-byte swizzle (2) at 61-63
+    for addr in (0, 1024, 0x3FFF0, 139264 + 3 * 16384 + 96):
+        for lbo, sbo in ((16, 1024), (KV_CB, 1024)):
+            d = sdesc(addr, lbo, sbo)
+            assert d & 0x3FFF == addr >> 4 and (d >> 16) & 0x3FFF == lbo >> 4
+            assert (d >> 32) & 0x3FFF == sbo >> 4 and (d >> 46) & 7 == 1
+            assert (d >> 61) == 2 and (d >> 49) & 0xFFF == 0 and (d >> 14) & 3 == 0
+
+
+def test_device_fastdiv_of_region_widths():
+    for d in range(1, TC_N + 1):
+        f = fastdiv_make(d)
+        for n in list(range(0, 300)) + list(range(4096 - 300, 4096)):
+            assert fdiv(n, f) == n // d, (n, d)
+
+
+def test_shared_memory_layout():
+    assert all(o % 1024 == 0 for o in (OFF_K, OFF_V, OFF_P, OFF_RED))
+    total = OFF_RED + 2 * PARTS * TC_M * 4 + 64 + 1024
+    assert 2 * (total + 1024) <= 228 * 1024          # two CTAs per SM (1 KB reserved each)
+    assert COL_O + 128 <= TMEM_COLS and 2 * TMEM_COLS <= 512 and TC_N <= COL_O
+
+
+def check_block(T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
+    tok = heads * 128
+    t0, h0, w0 = bt * QT, bh * QH, bw * QW
+    rt0 = na_start(t0, T, kt)
+    rt1 = na_start(min(t0 + 1, T - 1), T, kt) + kt
+    rh0 = na_start(h0, H, kh)
+    RH = na_start(min(h0 + QH - 1, H - 1), H, kh) + kh - rh0
+    rw0 = na_start(w0, W, kw)
+    RW = na_start(min(w0 + QW - 1, W - 1), W, kw) + kw - rw0
+    assert 1 <= RW <= TC_N and 1 <= RH
+    CH = min(RH, TC_N // RW)
+    per_frame = (RH + CH - 1) // CH
+    n_chunks = (rt1 - rt0) * per_frame
+    rwd = fastdiv_make(RW)
+    # Q tile rows and their offsets
+    q_offsets = set()
+    for r in range(TC_M):
+        for cv in range(16):
+            o = sw128(r, cv, Q_CB)
+            assert 0 <= o < 2 * Q_CB
+            q_offsets.add(o)
+    assert len(q_offsets) == TC_M * 16
+    seen = {}
+    for c in range(n_chunks):
+        f = rt0 + c // per_frame
+        r0 = (c % per_frame) * CH
+        keys = min(CH, RH - r0) * RW
+        N = (keys + 15) & ~15
+        assert 16 <= N <= TC_N and N % 16 == 0
+        # copies of K (and V): tile row j holds key (f, rh0 + r0 + j / RW, rw0 + j % RW)
+        rows = {}
+        offs = set()
+        for u in range(keys * 16):
+            j, cv = u >> 4, u & 15
+            rr = fdiv(j, rwd)
+            cc = j - rr * RW
+            t, h, w = f, rh0 + r0 + rr, rw0 + cc
+            assert 0 <= t < T and rh0 <= h < rh0 + RH <= H and rw0 <= w < rw0 + RW <= W
+            assert j < TC_N
+            rows.setdefault(j, (t, h, w))
+            assert rows[j] == (t, h, w)
+            o = sw128(j, cv, KV_CB)
+            assert 0 <= o < 2 * KV_CB and o not in offs
+            offs.add(o)
+        npad = N - keys
+        assert npad * 16 <= THREADS
+        for tid in range(npad * 16):
+            j, cv = keys + (tid >> 4), tid & 15
+            assert j < N <= TC_N
+            o = sw128(j, cv, KV_CB)
+            assert o not in offs
+            offs.add(o)
+        assert len(offs) == N * 16
+        # S = Q K^T: eight k16 steps; A reads 128 rows of 32 bytes at koff in
+        # column block ks / 4, B reads N rows likewise
+        for ks in range(8):
+            koff = (ks & 3) * 32
+            a0 = OFF_Q + (ks >> 2) * Q_CB + koff
+            b0 = OFF_K + (ks >> 2) * KV_CB + koff
+            assert OFF_Q <= a0 and a0 - koff + TC_M * 128 <= OFF_Q + 2 * Q_CB
+            assert OFF_K <= b0 and b0 - koff + N * 128 <= OFF_K + 2 * KV_CB
+        # O += P V: N / 16 k16 steps; P in column block s / 4; V as an MN-major
+        # operand: 16 keys (2 groups of 8 rows, SBO = 1024) x 128 channels (2
+        # column blocks, LBO = KV_CB)
+        for s in range(N // 16):
+            pa = OFF_P + (s >> 2) * Q_CB + (s & 3) * 32
+            assert OFF_P <= pa and pa - (s & 3) * 32 + TC_M * 128 <= OFF_P + P_BLOCKS * Q_CB
+            va = OFF_V + s * 2048
+            assert OFF_V <= va and va + 1024 + 1024 + KV_CB <= OFF_V + 2 * KV_CB
+        assert N <= COL_O   # S columns [0, N) stay clear of O's [128, 256)
+        # the P tile: group g of a row goes to chunks 2 g and 2 g + 1
+        for g in range(N // 16):
+            for ch in (2 * g, 2 * g + 1):
+                assert ch // 8 < P_BLOCKS
+        # the softmax masks of every query row (thread part qq takes the
+        # groups qq, qq + PARTS, ...)
+        for row in range(TC_M):
+            qt, qh, qw = t0 + (row >> 6), h0 + ((row >> 3) & 7), w0 + (row & 7)
+            row_ok = qt < T and qh < H and qw < W
+            st_q = na_start(min(qt, T - 1), T, kt)
+            ah = na_start(min(qh, H - 1), H, kh) - rh0
+            aw = na_start(min(qw, W - 1), W, kw) - rw0
+            frame_ok = row_ok and 0 <= f - st_q < kt
+            for qq in range(PARTS):
+                for g in range(qq, N // 16, PARTS):
+                    j0 = 16 * g
+                    rr = fdiv(j0, rwd)
+                    cc = j0 - rr * RW
+                    rel = r0 + rr - ah
+                    for e in range(16):
+                        ok = frame_ok and j0 + e < keys and 0 <= rel < kh and 0 <= cc - aw < kw
+                        if ok:
+                            key = rows[j0 + e]
+                            meet = (qt, qh, qw) + key
+                            seen[meet] = seen.get(meet, 0) + 1
+                        cc += 1
+                        if cc == RW:
+                            cc = 0
+                            rel += 1
+    # every query of the block meets each key of its window once, and no other
+    expected = 0
+    for qt in range(t0, min(t0 + QT, T)):
+        for qh in range(h0, min(h0 + QH, H)):
+            for qw in range(w0, min(w0 + QW, W)):
+                st, sh, sw_ = na_start(qt, T, kt), na_start(qh, H, kh), na_start(qw, W, kw)
+                for tt in range(st, st + kt):
+                    for a in range(sh, sh + kh):
+                        for b in range(sw_, sw_ + kw):
+                            assert seen.get((qt, qh, qw, tt, a, b)) == 1, (qt, qh, qw, tt, a, b)
+                expected += kt * kh * kw
+    assert sum(seen.values()) == expected
+    return expected
+
+
+def check_grid(T, H, W, kt, kh, kw, blocks=None):
+    nbt, nbh, nbw = (T + QT - 1) // QT, (H + QH - 1) // QH, (W + QW - 1) // QW
+    if blocks is None:
+        blocks = [(bt, bh, bw) for bt in range(nbt) for bh in range(nbh) for bw in range(nbw)]
+    assert sum(check_block(T, H, W, kt, kh, kw, *blk) for blk in blocks) > 0
+
+
+def tc_eligible(W, kw):
+    """The host's choice: the tensor-core kernel when a region row fits a chunk."""
+    return min(W, kw + QW - 1) <= TC_N
+
+
+GEOMETRIES = [
+    (3, 12, 12, 3, 5, 5), (2, 9, 17, 1, 3, 7), (5, 8, 8, 5, 7, 7), (4, 16, 24, 3, 7, 7),
+    (3, 10, 13, 3, 5, 5), (2, 9, 10, 1, 1, 1), (3, 8, 8, 3, 3, 3), (1, 9, 10, 1, 3, 3),
+    (2, 20, 70, 1, 3, 67), (3, 17, 9, 3, 17, 9), (2, 5, 90, 1, 1, 73),
+    (2, 6, 80, 1, 3, 67), (2, 12, 40, 1, 9, 33), (2, 12, 30, 1, 5, 23), (4, 13, 11, 3, 5, 7),
+    (3, 16, 16, 3, 7, 7), (2, 30, 80, 1, 1, 79), (2, 9, 100, 1, 3, 73),
+]
+
+
+def test_eligibility_bounds_every_region_row():
+    """min(W, kw + 7) <= kTcN makes every block's region row fit a chunk."""
+    for W in range(1, 200):
+        for kw in range(1, W + 1, 2):
+            if not tc_eligible(W, kw):
+                continue
+            for w0 in range(0, W, QW):
+                rw0 = na_start(w0, W, kw)
+                RW = na_start(min(w0 + QW - 1, W - 1), W, kw) + kw - rw0
+                assert 1 <= RW <= TC_N
+
+
+@pytest.mark.parametrize("geom", GEOMETRIES, ids=[str(g) for g in GEOMETRIES])
+def test_tc_tiling_covers_every_window_once(geom):
+    assert tc_eligible(geom[2], geom[5])
+    check_grid(*geom)
+
+
+def test_tc_tiling_of_the_benchmark_geometry():
+    """16 x 64 x 64 tokens, window 3 x 7 x 7: corner, edge and inner blocks of
+    the first, a middle and the last frame pair."""
+    picks = [0, 1, 4, 7]
+    check_grid(16, 64, 64, 3, 7, 7,
+               blocks=[(bt, bh, bw) for bt in (0, 4, 7) for bh in picks for bw in picks])
