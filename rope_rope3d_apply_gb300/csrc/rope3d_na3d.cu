@@ -34,6 +34,7 @@
 // per-element window mask. Chunks are double-buffered: the next chunk's K and
 // V are copied asynchronously while the current one is computed; when
 // rotating, each thread then rotates the K vectors it copied, in place.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -768,10 +769,11 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 // the 128 rows of one tcgen05 MMA (M = 128). The union of the block's windows
 // (its key region) is streamed in chunks of whole region rows of one frame,
 // at most kTcN keys each. Per chunk:
-//   1. the chunk's K is copied (cp.async, 16-byte vectors) into a K-major
-//      tile with the 128-byte swizzle; one thread issues S = Q K^T as eight
-//      k16 MMAs (N = the chunk's keys, rounded up to 16) into tensor memory;
-//   2. V is copied meanwhile (V of the previous chunk is no longer read);
+//   1. the chunk's K arrives by TMA (two boxes, one per 64 channels, with
+//      the 128-byte swizzle: a K-major tile); one thread issues S = Q K^T as
+//      eight k16 MMAs (N = the chunk's keys, rounded up to 16) into tensor
+//      memory;
+//   2. V arrives meanwhile (V of the previous chunk is no longer read);
 //   3. each query row's S is read back from tensor memory by two threads
 //      (every other 16-key group each: warps w and w + 4 share the 32 lanes
 //      of tensor memory that warp w reaches), masked to the query's window, scaled
@@ -781,13 +783,14 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 //   4. the bf16 weights P go to a K-major swizzled tile, and one thread issues
 //      O += P V as k16 MMAs with V read as an MN-major operand.
 // The next chunk's K is copied while 3 and 4 run. Q (rotated here in the
-// rotating modes) stays in shared memory for every chunk.
+// rotating modes) stays in shared memory for every chunk. In the mode that
+// rotates K per CTA, the threads rotate each K tile in place once it lands.
 // Shared memory (bytes; every tile 1024-aligned, the swizzle's period):
 //   Q  [2 column blocks][128 rows][128 B]        32,768
 //   K  [2 column blocks][kTcN rows][128 B]       20,480
 //   V  [2 column blocks][kTcN rows][128 B]       20,480
 //   P  [2 column blocks of 64 keys][128][128 B]  32,768
-//   row maxima and sums of the row's threads, two mbarriers, the TMEM address:
+//   row maxima and sums of the row's threads, four mbarriers, the TMEM address:
 // about 107 KB, so two CTAs share an SM and one's softmax overlaps the
 // other's copies and MMAs. Tensor memory: S in columns [0, N), O in [128, 256)
 // (256 columns per CTA, half of the SM's).
@@ -805,7 +808,7 @@ constexpr uint32_t kTcOffK = kTcOffQ + 2 * kTcQCb;
 constexpr uint32_t kTcOffV = kTcOffK + 2 * kTcKvCb;
 constexpr uint32_t kTcOffP = kTcOffV + 2 * kTcKvCb;
 constexpr uint32_t kTcOffRed = kTcOffP + kTcPBlocks * kTcQCb;       // float [2][kTcParts][128]
-constexpr uint32_t kTcOffBar = kTcOffRed + 2 * kTcParts * kTcM * 4;
+constexpr uint32_t kTcOffBar = kTcOffRed + 2 * kTcParts * kTcM * 4;    // 4 mbarriers + TMEM address
 constexpr uint32_t kTcSmem = kTcOffBar + 64 + 1024;                 // + room to align to 1024
 constexpr uint32_t kTcColO = 128;                                   // first TMEM column of O
 constexpr uint32_t kTcTmemCols = 256;                               // per CTA: two CTAs per SM
@@ -860,6 +863,28 @@ __device__ __forceinline__ void tc_fence_after() {
 // copies) become visible to the tensor cores' reads.
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// The mbarrier's next phase completes once this arrival has happened and
+// `bytes` have been written by the copies that name it.
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    uint64_t state;
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 %0, [%1], %2;"
+                 : "=l"(state) : "r"(bar), "r"(bytes) : "memory");
+    asm volatile("" ::"l"(state));   // the arrival state is not needed
+}
+
+// One TMA tile of a 5-D tensor map (channels, head, w, h, frame) into shared
+// memory, completing on `bar`. The channel coordinate is 0 or 64: 0 or 128
+// bytes, a multiple of 16 as TMA requires.
+__device__ __forceinline__ void tma_load5(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                          int c2, int c3, int c4, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+          "r"(c4), "r"(bar)
+        : "memory");
 }
 
 // Wait for phase `parity` of an mbarrier for at most ~0.1 s of SM clocks.
@@ -928,21 +953,32 @@ __device__ __forceinline__ rope3d::FastDiv fastdiv_make_dev(uint32_t d) {
     return rope3d::FastDiv{d, uint32_t(m), l};
 }
 
-__device__ __forceinline__ void cp_async_wait_group1() {
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
-}
+
+// The launch-wide shape of a chunk: every TMA box is (64 channels, 1 head,
+// rwb columns, chb rows, 1 frame) with rwb = min(W, kw + 7), the widest key
+// region row of any block, and chb = kTcN / rwb rows; a block whose region
+// is narrower masks the extra columns. Key j of a chunk is tile row j: region
+// row j / rwb, column j % rwb of the box.
+struct TcShape {
+    int nbt;   // query blocks along T (2 frames each)
+    int rwb;   // box width (columns)
+    int chb;   // box height (rows per chunk)
+};
 
 template <int kMode>
-__global__ void __launch_bounds__(kTcThreads, 2) rope3d_na3d_tc_kernel(const NAParams p, const int nbt) {
+__global__ void __launch_bounds__(kTcThreads, 2)
+rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV) {
     extern __shared__ unsigned char tc_raw[];
     unsigned char *sm = tc_raw + ((1024u - (smem_addr(tc_raw) & 1023u)) & 1023u);
     const uint32_t sQ = smem_addr(sm + kTcOffQ), sK = smem_addr(sm + kTcOffK);
     const uint32_t sV = smem_addr(sm + kTcOffV), sP = smem_addr(sm + kTcOffP);
     float *red_max = reinterpret_cast<float *>(sm + kTcOffRed);          // [kTcParts][128]
     float *red_sum = red_max + kTcParts * kTcM;                           // [kTcParts][128]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kTcOffBar);      // S done, O done
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kTcOffBar + 16);
-    const uint32_t barS = smem_addr(&bars[0]), barO = smem_addr(&bars[1]);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kTcOffBar);      // K, V landed; S, O done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kTcOffBar + 32);
+    const uint32_t barK = smem_addr(&bars[0]), barV = smem_addr(&bars[1]);
+    const uint32_t barS = smem_addr(&bars[2]), barO = smem_addr(&bars[3]);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int lg = warp & 3, qq = warp >> 2;        // TMEM lane group, column part
@@ -952,7 +988,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) rope3d_na3d_tc_kernel(const NAP
     int blk = blockIdx.x;
     const int bw = blk % p.nbw; blk /= p.nbw;
     const int bh = blk % p.nbh; blk /= p.nbh;
-    const int bt = blk % nbt; blk /= nbt;
+    const int bt = blk % shp.nbt; blk /= shp.nbt;
     const int head = blk % p.heads;
     const int b = blk / p.heads;
     const int t0 = bt * kTcQT, h0 = bh * kTcQH, w0 = bw * kTcQW;
@@ -969,10 +1005,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) rope3d_na3d_tc_kernel(const NAP
     const int RH = na_start(min(h0 + kTcQH - 1, p.H - 1), p.H, p.kh) + p.kh - rh0;
     const int rw0 = na_start(w0, p.W, p.kw);
     const int RW = na_start(min(w0 + kTcQW - 1, p.W - 1), p.W, p.kw) + p.kw - rw0;
-    const int CH = min(RH, kTcN / RW);               // region rows per chunk (>= 1: RW <= kTcN)
-    const int per_frame = (RH + CH - 1) / CH;
+    const int rwb = shp.rwb, chb = shp.chb;          // RW <= rwb, chb * rwb <= kTcN
+    const int per_frame = (RH + chb - 1) / chb;
     const int n_chunks = (rt1 - rt0) * per_frame;
-    const rope3d::FastDiv rwd = fastdiv_make_dev(uint32_t(RW));
+    const rope3d::FastDiv rwd = fastdiv_make_dev(uint32_t(rwb));
+    const uint32_t box_bytes = uint32_t(2 * 128 * rwb * chb);   // both column blocks
 
     // this thread's query and its window, in region coordinates
     const int qt = t0 + (row >> 6), qh = h0 + ((row >> 3) & 7), qw = w0 + (row & 7);
@@ -980,18 +1017,41 @@ __global__ void __launch_bounds__(kTcThreads, 2) rope3d_na3d_tc_kernel(const NAP
     const int st_q = na_start(min(qt, p.T - 1), p.T, p.kt);
     const int ah = na_start(min(qh, p.H - 1), p.H, p.kh) - rh0;
     const int aw = na_start(min(qw, p.W - 1), p.W, p.kw) - rw0;
+    const int clo = max(aw, 0), chi = min(aw + p.kw, RW);   // window columns of a region row
 
-    // ---- set-up: barriers, tensor memory, the Q tile
+    auto chunk_geom = [&](int c, int &f, int &r0, int &nr) {
+        f = rt0 + c / per_frame;
+        r0 = (c % per_frame) * chb;
+        nr = min(chb, RH - r0);
+    };
+    // One thread: the TMA boxes of chunk c (both column blocks) into `dst`.
+    auto tma_chunk = [&](const CUtensorMap *map, uint32_t dst, uint32_t bar, int c) {
+        int f, r0, nr;
+        chunk_geom(c, f, r0, nr);
+        mbar_expect_tx(bar, box_bytes);
+        const int frame = b * p.T + f;
+        tma_load5(dst, map, 0, head, rw0, rh0 + r0, frame, bar);
+        tma_load5(dst + kTcKvCb, map, 64, head, rw0, rh0 + r0, frame, bar);
+    };
+
+    // ---- set-up: barriers, tensor memory, zeroed K and V tiles, the Q tile
     if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(barS) : "memory");
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(barO) : "memory");
+        for (int i = 0; i < 4; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[i])) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(smem_addr(tmem_slot)), "r"(kTcTmemCols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    // Tile rows past a box (up to the MMA's next multiple of 16) are never
+    // written by TMA: they start at zero and later hold earlier chunks' keys,
+    // finite either way, and their weights are 0.
+    for (uint32_t i = tid; i < 4 * kTcKvCb / 16; i += kTcThreads)
+        *reinterpret_cast<uint4 *>(sm + kTcOffK + 16 * i) = make_uint4(0, 0, 0, 0);
     // Q: 128 rows x 16 vectors; thread tid moves vector cv = tid % 16 of rows
     // tid / 16 + (kTcThreads / 16) m (rotated on the way in the rotating modes)
     {
@@ -1017,69 +1077,47 @@ __global__ void __launch_bounds__(kTcThreads, 2) rope3d_na3d_tc_kernel(const NAP
     // stream (programmatic serialization): wait for it before the first copy
     if constexpr (kMode == kRotQ) asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // Copy the K (or V) rows of chunk c into tile `dst` (cp.async); rows past
-    // the chunk's keys up to the next multiple of 16 are zeroed. With kRotK the
-    // copied K vectors are rotated in place once they have landed (rot_k).
-    auto chunk_geom = [&](int c, int &f, int &r0, int &keys) {
-        f = rt0 + c / per_frame;
-        r0 = (c % per_frame) * CH;
-        keys = min(CH, RH - r0) * RW;
-    };
-    auto copy_rows = [&](int c, const uint16_t *src, unsigned char *dst) {
-        int f, r0, keys;
-        chunk_geom(c, f, r0, keys);
-        const int nvec = keys * 16;
-        for (int u = tid; u < nvec; u += kTcThreads) {
-            const uint32_t j = uint32_t(u) >> 4, cv = uint32_t(u) & 15;
-            const uint32_t rr = fdiv(j, rwd);
-            const int cc = int(j - rr * uint32_t(RW));
-            const long long off = token_off(f, rh0 + r0 + int(rr), rw0 + cc) + cv * 8;
-            if (bound_ok(off, 8, p.total) && bound_ok(j, 1, kTcN))
-                cp_async16(dst + sw128(j, cv, kTcKvCb), src + off);
-        }
-        const int npad = ((keys + 15) & ~15) - keys;
-        if (tid < npad * 16) {
-            const uint32_t j = uint32_t(keys + (tid >> 4)), cv = uint32_t(tid & 15);
-            if (bound_ok(j, 1, kTcN))
-                *reinterpret_cast<uint4 *>(dst + sw128(j, cv, kTcKvCb)) = make_uint4(0, 0, 0, 0);
-        }
-    };
+    // kRotQK: the threads rotate chunk c's K rows in place once they have
+    // landed (rows and columns inside the region only: the others are masked)
     auto rot_k = [&](int c) {
-        int f, r0, keys;
-        chunk_geom(c, f, r0, keys);
-        const int nvec = keys * 16;
+        int f, r0, nr;
+        chunk_geom(c, f, r0, nr);
+        const int nvec = nr * rwb * 16;
         const TabSlot tsg = tab_slot_global(p.pT, p.pH, p.pW, p.offH, p.offW, tid & 15);
         for (int u = tid; u < nvec; u += kTcThreads) {
             const uint32_t j = uint32_t(u) >> 4, cv = uint32_t(u) & 15;
             const uint32_t rr = fdiv(j, rwd);
-            const int cc = int(j - rr * uint32_t(RW));
+            const int cc = int(j - rr * uint32_t(rwb));
+            if (cc >= RW) continue;
             const int pos = tsg.axis == 0 ? f : (tsg.axis == 1 ? rh0 + r0 + int(rr) : rw0 + cc);
             uint4 *ptr = reinterpret_cast<uint4 *>(sm + kTcOffK + sw128(j, cv, kTcKvCb));
             *ptr = rot_vec_at<true>(*ptr, p.tab, tsg, uint32_t(pos), p.tab_len);
         }
     };
 
-    copy_rows(0, p.k, sm + kTcOffK);
-    cp_async_commit();
-
+    fence_async_smem();   // the zeroed tiles and Q, before any TMA write or MMA read
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (tid == 0) tma_chunk(&tmK, sK, barK, 0);
     const uint32_t tmem = *tmem_slot;
     const uint32_t tS = tmem + (uint32_t(32 * lg) << 16);            // this warp's lanes
     const uint32_t tO = tmem + kTcColO + (uint32_t(32 * lg) << 16);
 
-    float m_ref = -INFINITY, l_part = 0.f;   // running reference and this quarter's sum
+    float m_ref = -INFINITY, l_part = 0.f;   // running reference and this part's sum
     bool dead = false, o_started = false;
 
     for (int c = 0; c < n_chunks; ++c) {
-        int f, r0, keys;
-        chunk_geom(c, f, r0, keys);
-        const int N = (keys + 15) & ~15, ngrp = N >> 4;
+        int f, r0, nr;
+        chunk_geom(c, f, r0, nr);
+        const int N = (nr * rwb + 15) & ~15, ngrp = N >> 4;
+        const uint32_t ph = uint32_t(c) & 1u;
         // ---- [A] K of chunk c has landed; S = Q K^T
-        cp_async_wait_all();
-        if constexpr (kMode == kRotQK) rot_k(c);
-        fence_async_smem();
+        tc_wait(barK, ph, dead);
+        if constexpr (kMode == kRotQK) {
+            rot_k(c);
+            fence_async_smem();
+        }
         tc_fence_before();
         __syncthreads();
         if (tid == 0) {
@@ -1093,16 +1131,18 @@ __global__ void __launch_bounds__(kTcThreads, 2) rope3d_na3d_tc_kernel(const NAP
             }
             tc_commit(barS);
         }
-        // ---- V of chunk c, once O += P V of chunk c - 1 has finished with V and P
-        if (c > 0) tc_wait(barO, uint32_t(c - 1) & 1u, dead);
-        copy_rows(c, p.v, sm + kTcOffV);
-        cp_async_commit();
-        tc_wait(barS, uint32_t(c) & 1u, dead);
+        // ---- V of chunk c, once O += P V of chunk c - 1 has finished with V
+        // and P; then the next chunk's K, once S has finished with K
+        if (c > 0) tc_wait(barO, ph ^ 1u, dead);
+        if (tid == 0) tma_chunk(&tmV, sV, barV, c);
+        tc_wait(barS, ph, dead);
         tc_fence_after();
+        if (tid == 0 && c + 1 < n_chunks) tma_chunk(&tmK, sK, barK, c + 1);
 
-        // ---- this thread's groups of 16 keys: g = qq, qq + 4, ... First pass:
-        // which keys lie in the query's window (a 16-bit mask per group) and
-        // the largest scaled score among them.
+        // ---- this thread's groups of 16 keys: g = qq, qq + kTcParts, ...
+        // First pass: which keys lie in the query's window (a 16-bit mask per
+        // group, built from whole region rows: a spanned row in the window
+        // contributes its columns [clo, chi)) and the largest raw score among them.
         const bool frame_ok = row_ok && unsigned(f - st_q) < unsigned(p.kt);
         uint32_t win[kTcGroups];
         float cmax = -INFINITY;
@@ -1114,29 +1154,26 @@ __global__ void __launch_bounds__(kTcThreads, 2) rope3d_na3d_tc_kernel(const NAP
                 float x[16];
                 tc_ld16(tS + uint32_t(16 * g), x);
                 const uint32_t j0 = uint32_t(16 * g);
-                const uint32_t rr = fdiv(j0, rwd);
-                int cc = int(j0 - rr * uint32_t(RW));
-                int rel = r0 + int(rr) - ah;
+                const int rr0 = int(fdiv(j0, rwd));
                 uint32_t bits = 0;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const bool ok = frame_ok && int(j0) + e < keys &&
-                                    unsigned(rel) < unsigned(p.kh) && unsigned(cc - aw) < unsigned(p.kw);
-                    bits |= ok ? 1u << e : 0u;
-                    cmax = fmaxf(cmax, ok ? x[e] * p.scale_log2 : -INFINITY);
-                    if (++cc == RW) {
-                        cc = 0;
-                        ++rel;
+                if (frame_ok) {
+                    // js: bit position of column 0 of chunk row rr
+                    for (int rr = rr0, js = rr0 * rwb - int(j0); js < 16 && rr < nr; ++rr, js += rwb) {
+                        if (unsigned(r0 + rr - ah) < unsigned(p.kh)) {
+                            const int a = max(js + clo, 0), b2 = min(js + chi, 16);
+                            if (a < b2) bits |= (0xFFFFu >> (16 - (b2 - a))) << a;
+                        }
                     }
                 }
                 win[gi] = bits;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) cmax = fmaxf(cmax, (bits >> e) & 1u ? x[e] : -INFINITY);
             }
         }
+        cmax *= p.scale_log2;   // a positive scale: the maximum of the scaled scores
         red_max[qq * kTcM + row] = cmax;
-        // ---- [B] every quarter's maximum is in; K is free (S is complete)
+        // ---- [B] every part's maximum is in
         __syncthreads();
-        if (c + 1 < n_chunks) copy_rows(c + 1, p.k, sm + kTcOffK);
-        cp_async_commit();
         float rmax = red_max[row];
 #pragma unroll
         for (int i = 1; i < kTcParts; ++i) rmax = fmaxf(rmax, red_max[i * kTcM + row]);
@@ -1164,7 +1201,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) rope3d_na3d_tc_kernel(const NAP
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
         // ---- second pass, weights: P (bf16) into the swizzled tile and this
-        // quarter's sum (S is read again: cheaper than keeping it live)
+        // part's sum (S is read again: cheaper than keeping it live)
         const float ms = m_ref == -INFINITY ? 0.f : m_ref;
 #pragma unroll
         for (int gi = 0; gi < kTcGroups; ++gi) {
@@ -1176,8 +1213,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) rope3d_na3d_tc_kernel(const NAP
                 float s = 0.f;
 #pragma unroll
                 for (int e = 0; e < 16; e += 2) {
-                    const float a0 = (win[gi] >> e) & 1u ? ex2(x[e] * p.scale_log2 - ms) : 0.f;
-                    const float a1 = (win[gi] >> (e + 1)) & 1u ? ex2(x[e + 1] * p.scale_log2 - ms) : 0.f;
+                    // outside the window: -inf, whose weight is 0
+                    const float x0 = (win[gi] >> e) & 1u ? x[e] : -INFINITY;
+                    const float x1 = (win[gi] >> (e + 1)) & 1u ? x[e + 1] : -INFINITY;
+                    const float a0 = ex2(__fmaf_rn(x0, p.scale_log2, -ms));
+                    const float a1 = ex2(__fmaf_rn(x1, p.scale_log2, -ms));
                     s += a0 + a1;
                     w8[e >> 1] = pack_bf16(a0, a1);
                 }
@@ -1188,12 +1228,12 @@ __global__ void __launch_bounds__(kTcThreads, 2) rope3d_na3d_tc_kernel(const NAP
                     make_uint4(w8[4], w8[5], w8[6], w8[7]);
             }
         }
-        // ---- [C] P and V of chunk c are in place; O += P V
-        cp_async_wait_group1();   // V of chunk c (K of chunk c + 1 may still be in flight)
+        // ---- [C] P is in place; once V has landed, O += P V
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         if (tid == 0) {
+            tc_wait(barV, ph, dead);
             tc_fence_after();
             const uint32_t id = tc_idesc(kTcM, kHD, 1);
             for (int s = 0; s < ngrp; ++s)
@@ -1204,7 +1244,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) rope3d_na3d_tc_kernel(const NAP
         o_started = true;
     }
 
-    // ---- normalise and store this thread's quarter (32 channels) of its row
+    // ---- normalise and store this thread's part (128 / kTcParts channels) of its row
     tc_wait(barO, uint32_t(n_chunks - 1) & 1u, dead);
     tc_fence_after();
     red_sum[qq * kTcM + row] = l_part;
@@ -1380,10 +1420,57 @@ uint32_t na3d_blocks(const NAParams &p) {
 
 // The tensor-core (tcgen05) kernel: 2 x 8 x 8 query blocks; it needs a key
 // region row (at most kw + 7 columns, or W) to fit one chunk of kTcN keys.
-int na3d_tc_nbt(const NAParams &p) { return (p.T + kTcQT - 1) / kTcQT; }
+TcShape na3d_tc_shape(const NAParams &p) {
+    TcShape shp;
+    shp.nbt = (p.T + kTcQT - 1) / kTcQT;
+    shp.rwb = std::min(p.W, p.kw + kTcQW - 1);
+    shp.chb = kTcN / shp.rwb;
+    return shp;
+}
 
 uint32_t na3d_tc_blocks(const NAParams &p) {
-    return uint32_t(uint64_t(p.B) * p.heads * na3d_tc_nbt(p) * p.nbh * p.nbw);
+    return uint32_t(uint64_t(p.B) * p.heads * na3d_tc_shape(p).nbt * p.nbh * p.nbw);
+}
+
+// cuTensorMapEncodeTiled, from the driver through the runtime's entry-point
+// query (the library does not link the driver library itself).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return EncodeTiledFn(nullptr);
+        }
+        return reinterpret_cast<EncodeTiledFn>(ptr);
+    }();
+    return fn;
+}
+
+// The tensor map of one of K and V for the tensor-core kernel: a 5-D view
+// (128 channels, heads, W, H, B * T frames) of the [B, T, H, W, heads, 128]
+// buffer, boxes of (64 channels, 1 head, rwb columns, chb rows, 1 frame) with
+// the 128-byte swizzle; coordinates past the grid read zeros.
+bool na3d_tc_map(CUtensorMap *map, const void *base, const NAParams &p, const TcShape &shp) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t tok = cuuint64_t(p.heads) * kHD * 2;   // bytes per token
+    const cuuint64_t dims[5] = {cuuint64_t(kHD), cuuint64_t(p.heads), cuuint64_t(p.W),
+                                cuuint64_t(p.H), cuuint64_t(p.B) * cuuint64_t(p.T)};
+    const cuuint64_t strides[4] = {cuuint64_t(kHD) * 2, tok, tok * cuuint64_t(p.W),
+                                   tok * cuuint64_t(p.W) * cuuint64_t(p.H)};
+    const cuuint32_t box[5] = {64, 1, cuuint32_t(shp.rwb), cuuint32_t(shp.chb), 1};
+    const cuuint32_t elem[5] = {1, 1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box,
+              elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Which attention kernel runs: 0 = the library's default (the warp-MMA
@@ -1435,12 +1522,15 @@ extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *ou
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     g_na3d_last_kernel = na3d_use_tc(p) ? 1 : 2;
     if (na3d_use_tc(p)) {
+        const TcShape shp = na3d_tc_shape(p);
+        CUtensorMap mk, mv;
+        if (!na3d_tc_map(&mk, p.k, p, shp) || !na3d_tc_map(&mv, p.v, p, shp)) return ROPE3D_ERR_CUDA;
         if (apply_rope) {
             if (!na3d_tc_attribute<kRotQK>()) return ROPE3D_ERR_CUDA;
-            rope3d_na3d_tc_kernel<kRotQK><<<na3d_tc_blocks(p), kTcThreads, kTcSmem, st>>>(p, na3d_tc_nbt(p));
+            rope3d_na3d_tc_kernel<kRotQK><<<na3d_tc_blocks(p), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv);
         } else {
             if (!na3d_tc_attribute<kRotNone>()) return ROPE3D_ERR_CUDA;
-            rope3d_na3d_tc_kernel<kRotNone><<<na3d_tc_blocks(p), kTcThreads, kTcSmem, st>>>(p, na3d_tc_nbt(p));
+            rope3d_na3d_tc_kernel<kRotNone><<<na3d_tc_blocks(p), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv);
         }
     } else {
         if (!na3d_attributes()) return ROPE3D_ERR_CUDA;
@@ -1510,7 +1600,11 @@ extern "C" int rope3d_na3d_rotate_once(const void *q, const void *k, const void 
     p.k = static_cast<const uint16_t *>(k_rot);
     const bool tc = na3d_use_tc(p);
     g_na3d_last_kernel = tc ? 1 : 2;
-    if (tc && !na3d_tc_attribute<kRotQ>()) return ROPE3D_ERR_CUDA;
+    const TcShape shp = na3d_tc_shape(p);
+    CUtensorMap mk{}, mv{};
+    if (tc && (!na3d_tc_attribute<kRotQ>() || !na3d_tc_map(&mk, p.k, p, shp) ||
+               !na3d_tc_map(&mv, p.v, p, shp)))
+        return ROPE3D_ERR_CUDA;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(tc ? na3d_tc_blocks(p) : na3d_blocks(p));
     cfg.blockDim = dim3(tc ? kTcThreads : kThreads);
@@ -1521,7 +1615,7 @@ extern "C" int rope3d_na3d_rotate_once(const void *q, const void *k, const void 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t le = tc ? cudaLaunchKernelEx(&cfg, rope3d_na3d_tc_kernel<kRotQ>, p, na3d_tc_nbt(p))
+    const cudaError_t le = tc ? cudaLaunchKernelEx(&cfg, rope3d_na3d_tc_kernel<kRotQ>, p, shp, mk, mv)
                               : cudaLaunchKernelEx(&cfg, rope3d_na3d_kernel<kRotQ>, p);
     if (le != cudaSuccess) {
         cudaGetLastError();

@@ -5,10 +5,10 @@ rope3d_na3d_tc_kernel), checked without a GPU.
 For every CTA (a 2 x 8 x 8 query block) the model walks the kernel's chunks
 of the key region with the kernel's own integer formulas (region bounds, rows
 per chunk, the row width's multiply-high division) and asserts that:
-  - every global token a thread copies is the key its tile row stands for and
-    lies inside the grid and the region; tile rows past a chunk's keys up to
-    the next multiple of 16 are the zeroed ones, and every shared-memory
-    offset lies in its tile;
+  - the TMA boxes (the launch-wide width min(W, kw + 7) x rows per chunk)
+    start at aligned channel coordinates and non-negative positions, land
+    inside their tiles, and every key a mask selects is a grid token of the
+    region (never a zero-filled box element);
   - the ranges every tcgen05 MMA reads through its shared-memory descriptors
     (Q, K, P: K-major with the 128-byte swizzle; V: MN-major, column blocks
     kTcN x 128 bytes apart) lie inside their tiles, the MMA shapes are valid
@@ -105,7 +105,6 @@ def test_shared_memory_layout():
 
 
 def check_block(T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
-    tok = heads * 128
     t0, h0, w0 = bt * QT, bh * QH, bw * QW
     rt0 = na_start(t0, T, kt)
     rt1 = na_start(min(t0 + 1, T - 1), T, kt) + kt
@@ -113,11 +112,14 @@ def check_block(T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
     RH = na_start(min(h0 + QH - 1, H - 1), H, kh) + kh - rh0
     rw0 = na_start(w0, W, kw)
     RW = na_start(min(w0 + QW - 1, W - 1), W, kw) + kw - rw0
-    assert 1 <= RW <= TC_N and 1 <= RH
-    CH = min(RH, TC_N // RW)
-    per_frame = (RH + CH - 1) // CH
+    # the launch-wide box: rwb columns (the widest region row), chb rows
+    rwb = min(W, kw + QW - 1)
+    chb = TC_N // rwb
+    assert 1 <= RW <= rwb <= TC_N and 1 <= RH and chb >= 1 and chb * rwb <= TC_N
+    assert rwb <= 256 and chb <= 256                 # TMA box dimensions
+    per_frame = (RH + chb - 1) // chb
     n_chunks = (rt1 - rt0) * per_frame
-    rwd = fastdiv_make(RW)
+    rwd = fastdiv_make(rwb)
     # Q tile rows and their offsets
     q_offsets = set()
     for r in range(TC_M):
@@ -129,34 +131,24 @@ def check_block(T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
     seen = {}
     for c in range(n_chunks):
         f = rt0 + c // per_frame
-        r0 = (c % per_frame) * CH
-        keys = min(CH, RH - r0) * RW
-        N = (keys + 15) & ~15
+        r0 = (c % per_frame) * chb
+        nr = min(chb, RH - r0)
+        N = (nr * rwb + 15) & ~15
         assert 16 <= N <= TC_N and N % 16 == 0
-        # copies of K (and V): tile row j holds key (f, rh0 + r0 + j / RW, rw0 + j % RW)
+        # the TMA boxes: channel coordinate 0 or 64 (0 or 128 bytes), the other
+        # coordinates never negative; box element (cc, rr) lands in tile row
+        # rr * rwb + cc; coordinates past the grid read zeros
+        assert rw0 >= 0 and rh0 + r0 >= 0 and 0 <= f < T
         rows = {}
-        offs = set()
-        for u in range(keys * 16):
-            j, cv = u >> 4, u & 15
-            rr = fdiv(j, rwd)
-            cc = j - rr * RW
-            t, h, w = f, rh0 + r0 + rr, rw0 + cc
-            assert 0 <= t < T and rh0 <= h < rh0 + RH <= H and rw0 <= w < rw0 + RW <= W
-            assert j < TC_N
-            rows.setdefault(j, (t, h, w))
-            assert rows[j] == (t, h, w)
-            o = sw128(j, cv, KV_CB)
-            assert 0 <= o < 2 * KV_CB and o not in offs
-            offs.add(o)
-        npad = N - keys
-        assert npad * 16 <= THREADS
-        for tid in range(npad * 16):
-            j, cv = keys + (tid >> 4), tid & 15
-            assert j < N <= TC_N
-            o = sw128(j, cv, KV_CB)
-            assert o not in offs
-            offs.add(o)
-        assert len(offs) == N * 16
+        for rr in range(chb):
+            for cc in range(rwb):
+                j = rr * rwb + cc
+                assert j < TC_N
+                h, w = rh0 + r0 + rr, rw0 + cc
+                rows[j] = (f, h, w) if (h < H and w < W) else None
+        for j in range(chb * rwb):
+            for cv in range(16):
+                assert 0 <= sw128(j, cv, KV_CB) < 2 * KV_CB
         # S = Q K^T: eight k16 steps; A reads 128 rows of 32 bytes at koff in
         # column block ks / 4, B reads N rows likewise
         for ks in range(8):
@@ -179,30 +171,37 @@ def check_block(T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
             for ch in (2 * g, 2 * g + 1):
                 assert ch // 8 < P_BLOCKS
         # the softmax masks of every query row (thread part qq takes the
-        # groups qq, qq + PARTS, ...)
+        # groups qq, qq + PARTS, ...): a group's 16-bit mask is built from the
+        # chunk rows it spans, each in the window contributing columns [clo, chi)
         for row in range(TC_M):
             qt, qh, qw = t0 + (row >> 6), h0 + ((row >> 3) & 7), w0 + (row & 7)
             row_ok = qt < T and qh < H and qw < W
             st_q = na_start(min(qt, T - 1), T, kt)
             ah = na_start(min(qh, H - 1), H, kh) - rh0
             aw = na_start(min(qw, W - 1), W, kw) - rw0
+            clo, chi = max(aw, 0), min(aw + kw, RW)
             frame_ok = row_ok and 0 <= f - st_q < kt
             for qq in range(PARTS):
                 for g in range(qq, N // 16, PARTS):
                     j0 = 16 * g
-                    rr = fdiv(j0, rwd)
-                    cc = j0 - rr * RW
-                    rel = r0 + rr - ah
+                    rr0 = fdiv(j0, rwd)
+                    bits = 0
+                    if frame_ok:
+                        rr, js = rr0, rr0 * rwb - j0
+                        while js < 16 and rr < nr:
+                            if 0 <= r0 + rr - ah < kh:
+                                a, b2 = max(js + clo, 0), min(js + chi, 16)
+                                if a < b2:
+                                    bits |= (0xFFFF >> (16 - (b2 - a))) << a
+                            rr += 1
+                            js += rwb
+                    assert bits < (1 << 16)
                     for e in range(16):
-                        ok = frame_ok and j0 + e < keys and 0 <= rel < kh and 0 <= cc - aw < kw
-                        if ok:
+                        if bits >> e & 1:
                             key = rows[j0 + e]
+                            assert key is not None          # never a zero-filled key
                             meet = (qt, qh, qw) + key
                             seen[meet] = seen.get(meet, 0) + 1
-                        cc += 1
-                        if cc == RW:
-                            cc = 0
-                            rel += 1
     # every query of the block meets each key of its window once, and no other
     expected = 0
     for qt in range(t0, min(t0 + QT, T)):
