@@ -76,7 +76,7 @@ def commands(out_dir: str = BUILD, extra_nvcc: list[str] | None = None,
     na_o = os.path.join(out_dir, "rope3d_na3d.o")
     nvcc_na = [
         _nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-fmad=false", *dbg,
-        "-Xcompiler", "-fPIC,-ffp-contract=off", "-Xptxas", "-v",
+        "-Xcompiler", "-fPIC,-ffp-contract=off", "-Xptxas", "-v", *(extra_nvcc or []),
         "-c", os.path.join(CSRC, "rope3d_na3d.cu"), "-o", na_o,
     ]
     gxx_compile = [

@@ -57,6 +57,9 @@
 #ifndef NA_MIN_CTAS_ROPE
 #define NA_MIN_CTAS_ROPE 2
 #endif
+#ifndef NA_TC_SUSPEND_NS   // time limit hint of the tensor-core kernel's mbarrier waits
+#define NA_TC_SUSPEND_NS 1000
+#endif
 #ifndef NA_LAZY
 #define NA_LAZY 8.0f
 #endif
@@ -765,59 +768,70 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 }
 
 // ---- the attention on the fifth-generation tensor cores -------------------
-// A CTA of 256 threads owns one (batch, head) and a 2 x 8 x 8 block of queries:
-// the 128 rows of one tcgen05 MMA (M = 128). The union of the block's windows
-// (its key region) is streamed in chunks of whole region rows of one frame,
-// at most kTcN keys each. Per chunk:
-//   1. the chunk's K arrives by TMA (two boxes, one per 64 channels, with
-//      the 128-byte swizzle: a K-major tile); one thread issues S = Q K^T as
-//      eight k16 MMAs (N = the chunk's keys, rounded up to 16) into tensor
-//      memory;
-//   2. V arrives meanwhile (V of the previous chunk is no longer read);
-//   3. each query row's S is read back from tensor memory by two threads
-//      (every other 16-key group each: warps w and w + 4 share the 32 lanes
-//      of tensor memory that warp w reaches), masked to the query's window, scaled
-//      and turned into weights with the same online softmax as the warp-MMA
-//      kernel (the reference moves only when a row maximum passes it by more
-//      than 2^kLazy; O in tensor memory is rescaled then);
-//   4. the bf16 weights P go to a K-major swizzled tile, and one thread issues
-//      O += P V as k16 MMAs with V read as an MN-major operand.
-// The next chunk's K is copied while 3 and 4 run. Q (rotated here in the
-// rotating modes) stays in shared memory for every chunk. In the mode that
-// rotates K per CTA, the threads rotate each K tile in place once it lands.
+// A CTA owns one (batch, head) and a 2 x 8 x 8 block of queries: the 128 rows
+// of a tcgen05 MMA (M = 128). The union of the block's windows (its key
+// region) is streamed in chunks of whole region rows of one frame, at most
+// kTcN keys each. The CTA's warps have one job each and hand work over through
+// mbarriers, so that the tensor cores, the copies and the softmax overlap:
+//   warp 0 (one thread): TMA copies of each chunk's K and V (two boxes each,
+//     one per 64 channels, with the 128-byte swizzle) into two-slot rings;
+//   warp 1 (one thread): the MMAs. S(c) = Q K(c)^T into one of two S buffers
+//     in tensor memory (eight k16 steps), then O += P(c-1) V(c-1) (V read as
+//     an MN-major operand); so S(c + 1) and P V of chunk c - 1 run while the
+//     softmax of chunk c does;
+//   warps 2-5 (the rotating modes): rotate each query block's Q tile, and in
+//     the mode that rotates K per CTA each K tile, in place once it lands;
+//   warps 6-13: the softmax. Each query row's S is read back from tensor
+//     memory by two threads (half of the chunk's columns each, in one batch of
+//     loads: warps w and w + 4 share the 32 lanes of tensor memory that warp w
+//     reaches), masked to the query's window (a 64-bit mask from the region
+//     rows the half spans; groups of 8 keys that no query of the warp needs
+//     are skipped), scaled, and turned into weights with the same online
+//     softmax as the
+//     warp-MMA kernel (the reference moves only when a row maximum passes it
+//     by more than 2^kLazy; O in tensor memory is rescaled then); the bf16
+//     weights go to one of two P tiles (K-major, swizzled).
+// Q (rotated here in the rotating modes) stays in shared memory for every chunk.
 // Shared memory (bytes; every tile 1024-aligned, the swizzle's period):
-//   Q  [2 column blocks][128 rows][128 B]        32,768
-//   K  [2 column blocks][kTcN rows][128 B]       20,480
-//   V  [2 column blocks][kTcN rows][128 B]       20,480
-//   P  [2 column blocks of 64 keys][128][128 B]  32,768
-//   row maxima and sums of the row's threads, four mbarriers, the TMEM address:
-// about 107 KB, so two CTAs share an SM and one's softmax overlaps the
-// other's copies and MMAs. Tensor memory: S in columns [0, N), O in [128, 256)
-// (256 columns per CTA, half of the SM's).
-constexpr int kTcThreads = 256;              // 8 warps: 2 threads per query row
-constexpr int kTcParts = kTcThreads / 128;   // threads (column parts) per query row
+//   Q  [2 column blocks][128 rows][128 B]               32,768
+//   K  [2 slots][2 column blocks][kTcN rows][128 B]     57,344
+//   V  [2 slots][2 column blocks][kTcN rows][128 B]     57,344
+//   P  [2 slots][2 column blocks of 64 keys][128][128 B] 65,536
+//   row maxima and sums of the row's two threads, 18 mbarriers, the TMEM address.
+// Tensor memory (all 512 columns: one CTA per SM): S in [0, 128) and
+// [128, 256), O in [256, 384).
+constexpr int kTcThreads = 448;              // 14 warps: TMA, MMA, 4 rotation, 8 softmax
+constexpr int kTcSoftWarp0 = 6;              // first softmax warp
+constexpr int kTcRotThreads = 128;           // warps 2-5
+constexpr int kTcSoftThreads = 256;          // 2 threads per query row
+constexpr int kTcParts = kTcSoftThreads / 128;
 constexpr int kTcM = 128;                    // queries per CTA: 2 x 8 x 8
 constexpr int kTcQT = 2, kTcQH = 8, kTcQW = 8;
-constexpr int kTcN = 80;                     // keys per chunk at most
-constexpr int kTcGroups = (kTcN / 16 + kTcParts - 1) / kTcParts;   // 16-key groups per thread
-constexpr int kTcPBlocks = (kTcN + 63) / 64; // 64-key column blocks of the P tile
+constexpr int kTcN = 112;                    // keys per chunk at most
+constexpr int kTcHalf = kTcN / kTcParts;     // columns of S a softmax thread reads at most
+constexpr int kTcPBlocks = (kTcN + 63) / 64; // 64-key column blocks of a P tile
 constexpr uint32_t kTcQCb = kTcM * 128;      // bytes of a column block of Q or P
 constexpr uint32_t kTcKvCb = kTcN * 128;     // bytes of a column block of K or V
+constexpr uint32_t kTcKvSlot = 2 * kTcKvCb;  // bytes of a K or V slot
+constexpr uint32_t kTcPSlot = kTcPBlocks * kTcQCb;
 constexpr uint32_t kTcOffQ = 0;
 constexpr uint32_t kTcOffK = kTcOffQ + 2 * kTcQCb;
-constexpr uint32_t kTcOffV = kTcOffK + 2 * kTcKvCb;
-constexpr uint32_t kTcOffP = kTcOffV + 2 * kTcKvCb;
-constexpr uint32_t kTcOffRed = kTcOffP + kTcPBlocks * kTcQCb;       // float [2][kTcParts][128]
-constexpr uint32_t kTcOffBar = kTcOffRed + 2 * kTcParts * kTcM * 4;    // 4 mbarriers + TMEM address
-constexpr uint32_t kTcSmem = kTcOffBar + 64 + 1024;                 // + room to align to 1024
-constexpr uint32_t kTcColO = 128;                                   // first TMEM column of O
-constexpr uint32_t kTcTmemCols = 256;                               // per CTA: two CTAs per SM
-constexpr int kTcMaxRW = kTcN;                                      // a region row must fit a chunk
-static_assert(kTcOffK % 1024 == 0 && kTcOffV % 1024 == 0 && kTcOffP % 1024 == 0, "1024-aligned tiles");
-static_assert(kTcN % 16 == 0 && kTcN <= int(kTcColO), "S columns stay below O's");
+constexpr uint32_t kTcOffV = kTcOffK + 2 * kTcKvSlot;
+constexpr uint32_t kTcOffP = kTcOffV + 2 * kTcKvSlot;
+constexpr uint32_t kTcOffRed = kTcOffP + 2 * kTcPSlot;      // float max [2][2][128], sum [2][128]
+constexpr uint32_t kTcOffBar = kTcOffRed + 6 * kTcM * 4;    // 21 mbarriers + TMEM address
+constexpr uint32_t kTcSmem = kTcOffBar + 176 + 1024;        // + room to align to 1024
+constexpr uint32_t kTcColS = 128;                           // S buffer b at column b * 128
+constexpr uint32_t kTcColO = 256;                           // O of block k at 256 + 128 (k & 1)
+constexpr uint32_t kTcTmemCols = 512;
+constexpr int kTcMaxRW = kTcN;                              // a region row must fit a chunk
+static_assert(kTcKvCb % 1024 == 0 && kTcOffK % 1024 == 0 && kTcOffV % 1024 == 0 &&
+              kTcOffP % 1024 == 0, "1024-aligned tiles");
+static_assert(kTcN % 16 == 0 && kTcN <= int(kTcColS), "an S buffer holds a chunk");
 static_assert(kTcColO + 128 <= kTcTmemCols, "O fits the allocation");
-static_assert(2 * (kTcSmem + 1024) <= 228 * 1024, "two CTAs per SM");
-static_assert(kTcM % kTcParts == 0 && (128 / kTcParts) % 16 == 0, "O columns per thread");
+static_assert(kTcSmem + 1024 <= 228 * 1024, "one CTA per SM");
+static_assert((128 / kTcParts) % 16 == 0, "O columns per thread");
+static_assert(kTcParts == 2 && kTcHalf == 56, "a half row: 32 + 16 + 8 columns, a 64-bit mask");
 
 // Waits that gave up (a bounded wait on an MMA completion ran out); they are
 // counted here and reported by rope3d_testing_na3d_wait_timeouts.
@@ -874,6 +888,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("" ::"l"(state));   // the arrival state is not needed
 }
 
+// One arrival on an mbarrier (release semantics at CTA scope: this thread's
+// earlier writes are visible to whoever waits for the phase).
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    uint64_t state;
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 %0, [%1];" : "=l"(state) : "r"(bar) : "memory");
+    asm volatile("" ::"l"(state));
+}
+
 // One TMA tile of a 5-D tensor map (channels, head, w, h, frame) into shared
 // memory, completing on `bar`. The channel coordinate is 0 or 64: 0 or 128
 // bytes, a multiple of 16 as TMA requires.
@@ -895,10 +917,19 @@ __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, bool &dea
     const long long t0 = clock64();
     while (true) {
         uint32_t done;
+#if NA_TC_SUSPEND_NS > 0
+        // the thread may be suspended for up to this long while it waits
+        // (fewer issue slots spent spinning)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done) : "r"(bar), "r"(parity), "n"(NA_TC_SUSPEND_NS) : "memory");
+#else
         asm volatile(
             "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+#endif
         if (done) return true;
         if (clock64() - t0 > 200000000ll) {
             atomicAdd(&g_na3d_wait_timeouts, 1u);
@@ -923,6 +954,68 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 and 8 consecutive fp32 columns, not waited for (tc_ld_wait_hold follows).
+__device__ __forceinline__ void tc_ld32_async(uint32_t taddr, float *v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+        "%29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_ld8_async(uint32_t taddr, float *v) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_ld16_async(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_ld4_async(uint32_t taddr, float *v) {
+    uint32_t r[4];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Wait for this thread's tensor-memory loads; the n registers of v pass
+// through the asm so that no use of them moves above the wait.
+template <int n>
+__device__ __forceinline__ void tc_ld_wait_hold(float *v) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < n; ++i) asm volatile("" : "+f"(v[i]));
 }
 
 __device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
@@ -960,85 +1053,112 @@ __device__ __forceinline__ rope3d::FastDiv fastdiv_make_dev(uint32_t d) {
 // is narrower masks the extra columns. Key j of a chunk is tile row j: region
 // row j / rwb, column j % rwb of the box.
 struct TcShape {
-    int nbt;   // query blocks along T (2 frames each)
-    int rwb;   // box width (columns)
-    int chb;   // box height (rows per chunk)
+    int nbt;     // query blocks along T (2 frames each)
+    int rwb;     // box width (columns)
+    int chb;     // box height (rows per chunk)
+    int total;   // query blocks of the launch
 };
 
+// One query block: its place and its key region (frames [rt0, rt0 + frames),
+// rows [rh0, rh0 + RH), columns [rw0, rw0 + RW)), cut into per_frame chunks
+// of chb region rows per frame.
+struct TcBlock {
+    int b, head, t0, h0, w0;
+    int rt0, rh0, RH, rw0, RW;
+    int per_frame, n_chunks;
+};
+
+__device__ __forceinline__ TcBlock tc_block(const NAParams &p, const TcShape &shp, int blk) {
+    TcBlock g;
+    g.w0 = (blk % p.nbw) * kTcQW; blk /= p.nbw;
+    g.h0 = (blk % p.nbh) * kTcQH; blk /= p.nbh;
+    g.t0 = (blk % shp.nbt) * kTcQT; blk /= shp.nbt;
+    g.head = blk % p.heads;
+    g.b = blk / p.heads;
+    g.rt0 = na_start(g.t0, p.T, p.kt);
+    const int rt1 = na_start(min(g.t0 + 1, p.T - 1), p.T, p.kt) + p.kt;
+    g.rh0 = na_start(g.h0, p.H, p.kh);
+    g.RH = na_start(min(g.h0 + kTcQH - 1, p.H - 1), p.H, p.kh) + p.kh - g.rh0;
+    g.rw0 = na_start(g.w0, p.W, p.kw);
+    g.RW = na_start(min(g.w0 + kTcQW - 1, p.W - 1), p.W, p.kw) + p.kw - g.rw0;
+    g.per_frame = (g.RH + shp.chb - 1) / shp.chb;
+    g.n_chunks = (rt1 - g.rt0) * g.per_frame;
+    return g;
+}
+
 template <int kMode>
-__global__ void __launch_bounds__(kTcThreads, 2)
-rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
     extern __shared__ unsigned char tc_raw[];
     unsigned char *sm = tc_raw + ((1024u - (smem_addr(tc_raw) & 1023u)) & 1023u);
     const uint32_t sQ = smem_addr(sm + kTcOffQ), sK = smem_addr(sm + kTcOffK);
     const uint32_t sV = smem_addr(sm + kTcOffV), sP = smem_addr(sm + kTcOffP);
-    float *red_max = reinterpret_cast<float *>(sm + kTcOffRed);          // [kTcParts][128]
-    float *red_sum = red_max + kTcParts * kTcM;                           // [kTcParts][128]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kTcOffBar);      // K, V landed; S, O done
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kTcOffBar + 32);
-    const uint32_t barK = smem_addr(&bars[0]), barV = smem_addr(&bars[1]);
-    const uint32_t barS = smem_addr(&bars[2]), barO = smem_addr(&bars[3]);
+    float *red_max = reinterpret_cast<float *>(sm + kTcOffRed);   // [chunk parity][part][128]
+    float *red_sum = red_max + 2 * kTcParts * kTcM;                 // [part][128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kTcOffBar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kTcOffBar + 21 * 8);
+    // mbarriers, two of each kind (one per ring slot s = chunk & 1), counted
+    // over the CTA's whole sequence of chunks:
+    //   kFull  K landed (TMA)          kReady  K rotated (kRotQK; 128 arrivals)
+    //   kEmpty S MMAs done with K      vFull   V landed (TMA)
+    //   vEmpty P V MMAs done with V    sFull   S written (MMA)
+    //   sEmpty softmax done with S (256 arrivals)
+    //   pFull  P written (256 arrivals)  pEmpty P V MMAs done with P (and O updated)
+    // and one of each per query block: qFull (Q landed), qReady (Q rotated;
+    // 128 arrivals), qEmpty (the block's S MMAs done with Q).
+    auto bar = [&](int kind, int slot) { return smem_addr(&bars[2 * kind + slot]); };
+    enum { kFull, kReady, kEmpty, vFull, vEmpty, sFull, sEmpty, pFull, pEmpty };
+    const uint32_t qFull = smem_addr(&bars[18]), qReady = smem_addr(&bars[19]);
+    const uint32_t qEmpty = smem_addr(&bars[20]);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int lg = warp & 3, qq = warp >> 2;        // TMEM lane group, column part
-    const int row = 32 * lg + lane;                  // this thread's query row
-
-    // which (batch, head, query block)
-    int blk = blockIdx.x;
-    const int bw = blk % p.nbw; blk /= p.nbw;
-    const int bh = blk % p.nbh; blk /= p.nbh;
-    const int bt = blk % shp.nbt; blk /= shp.nbt;
-    const int head = blk % p.heads;
-    const int b = blk / p.heads;
-    const int t0 = bt * kTcQT, h0 = bh * kTcQH, w0 = bw * kTcQW;
-
     const long long tok = (long long)p.heads * kHD;   // elements per token
-    const long long head0 = (long long)head * kHD;
-    auto token_off = [&](int t, int h, int w) {       // element offset of (b, t, h, w, head, 0)
-        return (((long long)b * p.T + t) * p.H + h) * p.W * tok + (long long)w * tok + head0;
-    };
-
-    // the key region: frames [rt0, rt1), rows [rh0, rh0 + RH), columns [rw0, rw0 + RW)
-    const int rt0 = na_start(t0, p.T, p.kt), rt1 = na_start(min(t0 + 1, p.T - 1), p.T, p.kt) + p.kt;
-    const int rh0 = na_start(h0, p.H, p.kh);
-    const int RH = na_start(min(h0 + kTcQH - 1, p.H - 1), p.H, p.kh) + p.kh - rh0;
-    const int rw0 = na_start(w0, p.W, p.kw);
-    const int RW = na_start(min(w0 + kTcQW - 1, p.W - 1), p.W, p.kw) + p.kw - rw0;
     const int rwb = shp.rwb, chb = shp.chb;          // RW <= rwb, chb * rwb <= kTcN
-    const int per_frame = (RH + chb - 1) / chb;
-    const int n_chunks = (rt1 - rt0) * per_frame;
     const rope3d::FastDiv rwd = fastdiv_make_dev(uint32_t(rwb));
     const uint32_t box_bytes = uint32_t(2 * 128 * rwb * chb);   // both column blocks
 
-    // this thread's query and its window, in region coordinates
-    const int qt = t0 + (row >> 6), qh = h0 + ((row >> 3) & 7), qw = w0 + (row & 7);
-    const bool row_ok = qt < p.T && qh < p.H && qw < p.W;
-    const int st_q = na_start(min(qt, p.T - 1), p.T, p.kt);
-    const int ah = na_start(min(qh, p.H - 1), p.H, p.kh) - rh0;
-    const int aw = na_start(min(qw, p.W - 1), p.W, p.kw) - rw0;
-    const int clo = max(aw, 0), chi = min(aw + p.kw, RW);   // window columns of a region row
-
-    auto chunk_geom = [&](int c, int &f, int &r0, int &nr) {
-        f = rt0 + c / per_frame;
-        r0 = (c % per_frame) * chb;
-        nr = min(chb, RH - r0);
+    // chunk c of block g: frame f, region rows [r0, r0 + nr)
+    auto chunk_geom = [&](const TcBlock &g, int c, int &f, int &r0, int &nr) {
+        f = g.rt0 + c / g.per_frame;
+        r0 = (c % g.per_frame) * chb;
+        nr = min(chb, g.RH - r0);
     };
-    // One thread: the TMA boxes of chunk c (both column blocks) into `dst`.
-    auto tma_chunk = [&](const CUtensorMap *map, uint32_t dst, uint32_t bar, int c) {
+    auto chunk_n = [&](const TcBlock &g, int c) {   // the MMA width: keys rounded up to 16
         int f, r0, nr;
-        chunk_geom(c, f, r0, nr);
-        mbar_expect_tx(bar, box_bytes);
-        const int frame = b * p.T + f;
-        tma_load5(dst, map, 0, head, rw0, rh0 + r0, frame, bar);
-        tma_load5(dst + kTcKvCb, map, 64, head, rw0, rh0 + r0, frame, bar);
+        chunk_geom(g, c, f, r0, nr);
+        return (nr * rwb + 15) & ~15;
+    };
+    // TMA copies of chunk c's K or V (both column blocks) into ring slot s
+    auto tma_chunk = [&](const TcBlock &g, int c, int s, bool v) {
+        int f, r0, nr;
+        chunk_geom(g, c, f, r0, nr);
+        const int frame = g.b * p.T + f;
+        const uint32_t full = bar(v ? vFull : kFull, s), dst = (v ? sV : sK) + s * kTcKvSlot;
+        const CUtensorMap *map = v ? &tmV : &tmK;
+        mbar_expect_tx(full, box_bytes);
+        tma_load5(dst, map, 0, g.head, g.rw0, g.rh0 + r0, frame, full);
+        tma_load5(dst + kTcKvCb, map, 64, g.head, g.rw0, g.rh0 + r0, frame, full);
+    };
+    auto tma_q = [&](const TcBlock &g) {   // the block's 2 x 8 x 8 queries, rows (t, h, w)
+        mbar_expect_tx(qFull, 2 * kTcQCb);
+        tma_load5(sQ, &tmQ, 0, g.head, g.w0, g.h0, g.b * p.T + g.t0, qFull);
+        tma_load5(sQ + kTcQCb, &tmQ, 64, g.head, g.w0, g.h0, g.b * p.T + g.t0, qFull);
     };
 
-    // ---- set-up: barriers, tensor memory, zeroed K and V tiles, the Q tile
+    // ---- set-up: barriers, tensor memory, zeroed pad rows
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[i])) : "memory");
+        for (int s = 0; s < 2; ++s) {
+            const int counts[9] = {1, kTcRotThreads, 1, 1, 1, 1, kTcSoftThreads, kTcSoftThreads, 1};
+            for (int kind = 0; kind < 9; ++kind)
+                asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar(kind, s)),
+                             "r"(counts[kind]) : "memory");
+        }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(qFull) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(qReady), "r"(kTcRotThreads) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(qEmpty) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmQ)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
     }
@@ -1048,226 +1168,305 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     // Tile rows past a box (up to the MMA's next multiple of 16) are never
-    // written by TMA: they start at zero and later hold earlier chunks' keys,
-    // finite either way, and their weights are 0.
-    for (uint32_t i = tid; i < 4 * kTcKvCb / 16; i += kTcThreads)
-        *reinterpret_cast<uint4 *>(sm + kTcOffK + 16 * i) = make_uint4(0, 0, 0, 0);
-    // Q: 128 rows x 16 vectors; thread tid moves vector cv = tid % 16 of rows
-    // tid / 16 + (kTcThreads / 16) m (rotated on the way in the rotating modes)
+    // written by TMA: zero them once (finite, with weight 0).
     {
-        const int cv = tid & 15;
-        const TabSlot tsg = tab_slot_global(p.pT, p.pH, p.pW, p.offH, p.offW, cv);
-#pragma unroll
-        for (int m = 0; m < kTcM * 16 / kTcThreads; ++m) {
-            const int r = (tid >> 4) + (kTcThreads / 16) * m;
-            const int t = t0 + (r >> 6), h = h0 + ((r >> 3) & 7), w = w0 + (r & 7);
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (t < p.T && h < p.H && w < p.W) {
-                const long long off = token_off(t, h, w) + cv * 8;
-                if (bound_ok(off, 8, p.total)) v = __ldg(reinterpret_cast<const uint4 *>(p.q + off));
-                if constexpr (kMode != kRotNone) {
-                    const int pos = tsg.axis == 0 ? t : (tsg.axis == 1 ? h : w);
-                    v = rot_vec_at<true>(v, p.tab, tsg, uint32_t(pos), p.tab_len);
-                }
-            }
-            *reinterpret_cast<uint4 *>(sm + kTcOffQ + sw128(r, cv, kTcQCb)) = v;
+        const int box_rows = rwb * chb, pad = ((box_rows + 15) & ~15) - box_rows;
+        for (int i = tid; i < 4 * 2 * pad * 8; i += kTcThreads) {   // 4 tiles x 2 column blocks x pad rows x 8 chunks
+            const int tile = i / (2 * pad * 8), rest = i % (2 * pad * 8);
+            const int cb = rest / (pad * 8), rr = (rest / 8) % pad, ch = rest % 8;
+            const uint32_t r = uint32_t(box_rows + rr);
+            *reinterpret_cast<uint4 *>(sm + kTcOffK + tile * kTcKvSlot + cb * kTcKvCb + r * 128 +
+                                       (((uint32_t(ch)) ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
         }
     }
-    // K of the rotate-once form comes from the kernel before this one in the
-    // stream (programmatic serialization): wait for it before the first copy
-    if constexpr (kMode == kRotQ) asm volatile("griddepcontrol.wait;" ::: "memory");
-
-    // kRotQK: the threads rotate chunk c's K rows in place once they have
-    // landed (rows and columns inside the region only: the others are masked)
-    auto rot_k = [&](int c) {
-        int f, r0, nr;
-        chunk_geom(c, f, r0, nr);
-        const int nvec = nr * rwb * 16;
-        const TabSlot tsg = tab_slot_global(p.pT, p.pH, p.pW, p.offH, p.offW, tid & 15);
-        for (int u = tid; u < nvec; u += kTcThreads) {
-            const uint32_t j = uint32_t(u) >> 4, cv = uint32_t(u) & 15;
-            const uint32_t rr = fdiv(j, rwd);
-            const int cc = int(j - rr * uint32_t(rwb));
-            if (cc >= RW) continue;
-            const int pos = tsg.axis == 0 ? f : (tsg.axis == 1 ? rh0 + r0 + int(rr) : rw0 + cc);
-            uint4 *ptr = reinterpret_cast<uint4 *>(sm + kTcOffK + sw128(j, cv, kTcKvCb));
-            *ptr = rot_vec_at<true>(*ptr, p.tab, tsg, uint32_t(pos), p.tab_len);
-        }
-    };
-
-    fence_async_smem();   // the zeroed tiles and Q, before any TMA write or MMA read
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0) tma_chunk(&tmK, sK, barK, 0);
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem + (uint32_t(32 * lg) << 16);            // this warp's lanes
-    const uint32_t tO = tmem + kTcColO + (uint32_t(32 * lg) << 16);
+    bool dead = false;
 
-    float m_ref = -INFINITY, l_part = 0.f;   // running reference and this part's sum
-    bool dead = false, o_started = false;
-
-    for (int c = 0; c < n_chunks; ++c) {
-        int f, r0, nr;
-        chunk_geom(c, f, r0, nr);
-        const int N = (nr * rwb + 15) & ~15, ngrp = N >> 4;
-        const uint32_t ph = uint32_t(c) & 1u;
-        // ---- [A] K of chunk c has landed; S = Q K^T
-        tc_wait(barK, ph, dead);
-        if constexpr (kMode == kRotQK) {
-            rot_k(c);
-            fence_async_smem();
-        }
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id = tc_idesc(kTcM, uint32_t(N), 0);
-#pragma unroll
-            for (int ks = 0; ks < kHD / 16; ++ks) {
-                const uint32_t koff = (ks & 3) * 32;   // 16 channels = 32 bytes
-                tc_mma(tmem, tc_sdesc(sQ + (ks >> 2) * kTcQCb + koff, 16, 1024),
-                       tc_sdesc(sK + (ks >> 2) * kTcKvCb + koff, 16, 1024), id, ks > 0);
+    if (warp == 0) {
+        // ---- TMA producer: each block's Q (once the previous block's S MMAs
+        // are done with Q), then its chunks' K and V into the rings
+        if (lane == 0) {
+            // K of the rotate-once form comes from the kernel before this one in
+            // the stream (programmatic serialization): wait for it first
+            if constexpr (kMode == kRotQ) asm volatile("griddepcontrol.wait;" ::: "memory");
+            int gc = 0;   // chunks of the CTA so far
+            for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
+                const TcBlock g = tc_block(p, shp, blk);
+                if (k >= 1) tc_wait(qEmpty, uint32_t(k - 1) & 1u, dead);
+                tma_q(g);
+                for (int c = 0; c < g.n_chunks; ++c, ++gc) {
+                    const int s = gc & 1;
+                    const uint32_t use = uint32_t(gc >> 1);
+                    if (gc >= 2) tc_wait(bar(kEmpty, s), (use - 1) & 1u, dead);
+                    tma_chunk(g, c, s, false);
+                    if (gc >= 2) tc_wait(bar(vEmpty, s), (use - 1) & 1u, dead);
+                    tma_chunk(g, c, s, true);
+                }
             }
-            tc_commit(barS);
         }
-        // ---- V of chunk c, once O += P V of chunk c - 1 has finished with V
-        // and P; then the next chunk's K, once S has finished with K
-        if (c > 0) tc_wait(barO, ph ^ 1u, dead);
-        if (tid == 0) tma_chunk(&tmV, sV, barV, c);
-        tc_wait(barS, ph, dead);
-        tc_fence_after();
-        if (tid == 0 && c + 1 < n_chunks) tma_chunk(&tmK, sK, barK, c + 1);
-
-        // ---- this thread's groups of 16 keys: g = qq, qq + kTcParts, ...
-        // First pass: which keys lie in the query's window (a 16-bit mask per
-        // group, built from whole region rows: a spanned row in the window
-        // contributes its columns [clo, chi)) and the largest raw score among them.
-        const bool frame_ok = row_ok && unsigned(f - st_q) < unsigned(p.kt);
-        uint32_t win[kTcGroups];
-        float cmax = -INFINITY;
+    } else if (warp == 1) {
+        // ---- MMA issuer: per block, S(c) then P V of chunk c - 1, and the
+        // block's last P V at its end
+        if (lane == 0) {
+            int gc = 0;
+            auto issue_pv = [&](const TcBlock &g, int c, int gg, uint32_t o_col) {
+                const int s = gg & 1;
+                const uint32_t use = uint32_t(gg >> 1);
+                tc_wait(bar(pFull, s), use & 1u, dead);
+                tc_wait(bar(vFull, s), use & 1u, dead);
+                tc_fence_after();
+                const uint32_t id = tc_idesc(kTcM, kHD, 1);
+                const int ngrp = chunk_n(g, c) >> 4;
+                const uint32_t pt = sP + s * kTcPSlot, vt = sV + s * kTcKvSlot;
+                for (int j = 0; j < ngrp; ++j)
+                    tc_mma(o_col, tc_sdesc(pt + (j >> 2) * kTcQCb + (j & 3) * 32, 16, 1024),
+                           tc_sdesc(vt + j * 2048, kTcKvCb, 1024), id, (j > 0 || c > 0) ? 1u : 0u);
+                tc_commit(bar(vEmpty, s));
+                tc_commit(bar(pEmpty, s));
+            };
+            for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
+                const TcBlock g = tc_block(p, shp, blk);
+                const uint32_t o_col = tmem + kTcColO + uint32_t(k & 1) * 128;
+                tc_wait(kMode == kRotNone ? qFull : qReady, uint32_t(k) & 1u, dead);
+                for (int c = 0; c < g.n_chunks; ++c, ++gc) {
+                    const int s = gc & 1;
+                    const uint32_t use = uint32_t(gc >> 1);
+                    tc_wait(bar(kMode == kRotQK ? kReady : kFull, s), use & 1u, dead);
+                    if (gc >= 2) tc_wait(bar(sEmpty, s), (use - 1) & 1u, dead);
+                    tc_fence_after();
+                    const uint32_t id = tc_idesc(kTcM, uint32_t(chunk_n(g, c)), 0);
+                    const uint32_t kt = sK + s * kTcKvSlot;
 #pragma unroll
-        for (int gi = 0; gi < kTcGroups; ++gi) {
-            win[gi] = 0u;
-            const int g = qq + kTcParts * gi;
-            if (g < ngrp) {
-                float x[16];
-                tc_ld16(tS + uint32_t(16 * g), x);
-                const uint32_t j0 = uint32_t(16 * g);
-                const int rr0 = int(fdiv(j0, rwd));
-                uint32_t bits = 0;
+                    for (int ks = 0; ks < kHD / 16; ++ks) {
+                        const uint32_t koff = (ks & 3) * 32;   // 16 channels = 32 bytes
+                        tc_mma(tmem + s * kTcColS, tc_sdesc(sQ + (ks >> 2) * kTcQCb + koff, 16, 1024),
+                               tc_sdesc(kt + (ks >> 2) * kTcKvCb + koff, 16, 1024), id, ks > 0);
+                    }
+                    tc_commit(bar(kEmpty, s));
+                    tc_commit(bar(sFull, s));
+                    if (c == g.n_chunks - 1) tc_commit(qEmpty);
+                    if (c >= 1) issue_pv(g, c - 1, gc - 1, o_col);
+                }
+                issue_pv(g, g.n_chunks - 1, gc - 1, o_col);
+            }
+        }
+    } else if (warp < kTcSoftWarp0) {
+        // ---- rotation warps: each block's Q tile (rotating modes), and in the
+        // mode that rotates K per CTA each K tile, in place once landed
+        if constexpr (kMode != kRotNone) {
+            const int rt = tid - 64;   // 0 .. kTcRotThreads - 1
+            const TabSlot tsg = tab_slot_global(p.pT, p.pH, p.pW, p.offH, p.offW, rt & 15);
+            int gc = 0;
+            for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
+                const TcBlock g = tc_block(p, shp, blk);
+                tc_wait(qFull, uint32_t(k) & 1u, dead);
+                for (int u = rt; u < kTcM * 16; u += kTcRotThreads) {
+                    const int r = u >> 4, cv = u & 15;
+                    const int t = g.t0 + (r >> 6), h = g.h0 + ((r >> 3) & 7), w = g.w0 + (r & 7);
+                    if (t < p.T && h < p.H && w < p.W) {
+                        const int pos = tsg.axis == 0 ? t : (tsg.axis == 1 ? h : w);
+                        uint4 *ptr = reinterpret_cast<uint4 *>(sm + kTcOffQ + sw128(r, cv, kTcQCb));
+                        *ptr = rot_vec_at<true>(*ptr, p.tab, tsg, uint32_t(pos), p.tab_len);
+                    }
+                }
+                fence_async_smem();
+                mbar_arrive(qReady);
+                if constexpr (kMode == kRotQK) {
+                    for (int c = 0; c < g.n_chunks; ++c, ++gc) {
+                        const int s = gc & 1;
+                        const uint32_t use = uint32_t(gc >> 1);
+                        int f, r0, nr;
+                        chunk_geom(g, c, f, r0, nr);
+                        tc_wait(bar(kFull, s), use & 1u, dead);
+                        const int nvec = nr * rwb * 16;
+                        for (int u = rt; u < nvec; u += kTcRotThreads) {
+                            const uint32_t j = uint32_t(u) >> 4, cv = uint32_t(u) & 15;
+                            const uint32_t rr = fdiv(j, rwd);
+                            const int cc = int(j - rr * uint32_t(rwb));
+                            if (cc >= g.RW) continue;   // outside the region: masked
+                            const int pos = tsg.axis == 0 ? f : (tsg.axis == 1 ? g.rh0 + r0 + int(rr) : g.rw0 + cc);
+                            uint4 *ptr = reinterpret_cast<uint4 *>(sm + kTcOffK + s * kTcKvSlot + sw128(j, cv, kTcKvCb));
+                            *ptr = rot_vec_at<true>(*ptr, p.tab, tsg, uint32_t(pos), p.tab_len);
+                        }
+                        fence_async_smem();
+                        mbar_arrive(bar(kReady, s));
+                    }
+                }
+            }
+        }
+    } else {
+        // ---- softmax warps: this thread's query row and column part
+        const int lg = warp & 3, qq = (warp - kTcSoftWarp0) >> 2;
+        const int row = 32 * lg + lane;
+        const uint32_t lanes = uint32_t(32 * lg) << 16;
+        int gc = 0;
+        for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
+            const TcBlock g = tc_block(p, shp, blk);
+            const int qt = g.t0 + (row >> 6), qh = g.h0 + ((row >> 3) & 7), qw = g.w0 + (row & 7);
+            const bool row_ok = qt < p.T && qh < p.H && qw < p.W;
+            const int st_q = na_start(min(qt, p.T - 1), p.T, p.kt);
+            const int ah = na_start(min(qh, p.H - 1), p.H, p.kh) - g.rh0;
+            const int aw = na_start(min(qw, p.W - 1), p.W, p.kw) - g.rw0;
+            const int clo = max(aw, 0), chi = min(aw + p.kw, g.RW);   // window columns of a region row
+            const uint32_t tO = tmem + kTcColO + uint32_t(k & 1) * 128 + lanes;
+            float m_ref = -INFINITY, l_part = 0.f;   // running reference and this part's sum
+
+            for (int c = 0; c < g.n_chunks; ++c, ++gc) {
+                const int s = gc & 1;
+                const uint32_t use = uint32_t(gc >> 1);
+                int f, r0, nr;
+                chunk_geom(g, c, f, r0, nr);
+                const uint32_t tS = tmem + s * kTcColS + lanes;
+                tc_wait(bar(sFull, s), use & 1u, dead);
+                tc_fence_after();
+
+                // this thread's half of the chunk's columns, [cb0, cb0 + nhalf),
+                // loaded at once as 32 + 16 + 8 columns; columns past nhalf stay
+                // inside this S buffer (cb0 + kTcHalf <= kTcN) and are masked.
+                // A warp's rows share their frame (lanes 0-63 of tensor memory are
+                // the block's first frame, 64-127 its second), so a frame outside
+                // the warp's time window is skipped by the whole warp: zero weights.
+                const int nhalf = ((nr * rwb + 15) & ~15) >> 1;   // a multiple of 8
+                const int cb0 = qq * nhalf;
+                const bool frame_ok = row_ok && unsigned(f - st_q) < unsigned(p.kt);
+                const bool warp_busy = __any_sync(0xffffffffu, frame_ok);
+                float x[kTcHalf];
+                if (warp_busy) {
+                    tc_ld32_async(tS + uint32_t(cb0), x);
+                    tc_ld16_async(tS + uint32_t(cb0 + 32), x + 32);
+                    tc_ld8_async(tS + uint32_t(cb0 + 48), x + 48);
+                    tc_ld_wait_hold<kTcHalf>(x);
+                }
+                // window mask: bit k stands for column cb0 + k; each chunk row the
+                // half spans that lies in the window contributes its columns [clo, chi)
+                uint64_t win = 0;
                 if (frame_ok) {
-                    // js: bit position of column 0 of chunk row rr
-                    for (int rr = rr0, js = rr0 * rwb - int(j0); js < 16 && rr < nr; ++rr, js += rwb) {
+                    const int rr0 = int(fdiv(uint32_t(cb0), rwd));
+                    for (int rr = rr0, js = rr0 * rwb - cb0; js < nhalf && rr < nr; ++rr, js += rwb) {
                         if (unsigned(r0 + rr - ah) < unsigned(p.kh)) {
-                            const int a = max(js + clo, 0), b2 = min(js + chi, 16);
-                            if (a < b2) bits |= (0xFFFFu >> (16 - (b2 - a))) << a;
+                            const int a = max(js + clo, 0), b2 = min(js + chi, nhalf);
+                            if (a < b2) win |= (~0ull >> (64 - (b2 - a))) << a;
                         }
                     }
                 }
-                win[gi] = bits;
+                // groups of 8 keys that no query of the warp has in its window are
+                // skipped by the whole warp (their weights are written as zeros)
+                uint32_t live = 0;   // bit k8: some lane of the warp needs group k8
+                float cmax = -INFINITY;
+                if (warp_busy) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) cmax = fmaxf(cmax, (bits >> e) & 1u ? x[e] : -INFINITY);
-            }
-        }
-        cmax *= p.scale_log2;   // a positive scale: the maximum of the scaled scores
-        red_max[qq * kTcM + row] = cmax;
-        // ---- [B] every part's maximum is in
-        __syncthreads();
-        float rmax = red_max[row];
+                    for (int k8 = 0; k8 < kTcHalf / 8; ++k8) {
+                        const bool need = __any_sync(0xffffffffu, ((win >> (8 * k8)) & 0xFFull) != 0);
+                        live |= need ? 1u << k8 : 0u;
+                        if (need) {
 #pragma unroll
-        for (int i = 1; i < kTcParts; ++i) rmax = fmaxf(rmax, red_max[i * kTcM + row]);
-        const float mn = fmaxf(m_ref, rmax);
-        // The decision is the same for all threads of the row (the same
-        // inputs); the tensor-memory accesses are made by whole warps.
-        const bool move = mn > m_ref + kLazy;
-        float corr = 1.f;
-        if (move) {
-            corr = m_ref == -INFINITY ? 0.f : ex2(m_ref - mn);
-            m_ref = mn;
-            l_part *= corr;
-        }
-        if (o_started && __any_sync(0xffffffffu, move)) {
-            // O is stable: chunk c - 1's P V has completed (waited above)
-            float o[16];
-#pragma unroll
-            for (int h2 = 0; h2 < 128 / kTcParts / 16; ++h2) {
-                const uint32_t ta = tO + uint32_t(128 / kTcParts * qq + 16 * h2);
-                tc_ld16(ta, o);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) o[i] *= corr;
-                tc_st16(ta, o);
-            }
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        }
-        // ---- second pass, weights: P (bf16) into the swizzled tile and this
-        // part's sum (S is read again: cheaper than keeping it live)
-        const float ms = m_ref == -INFINITY ? 0.f : m_ref;
-#pragma unroll
-        for (int gi = 0; gi < kTcGroups; ++gi) {
-            const int g = qq + kTcParts * gi;
-            if (g < ngrp) {
-                float x[16];
-                tc_ld16(tS + uint32_t(16 * g), x);
-                uint32_t w8[8];
-                float s = 0.f;
-#pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                    // outside the window: -inf, whose weight is 0
-                    const float x0 = (win[gi] >> e) & 1u ? x[e] : -INFINITY;
-                    const float x1 = (win[gi] >> (e + 1)) & 1u ? x[e + 1] : -INFINITY;
-                    const float a0 = ex2(__fmaf_rn(x0, p.scale_log2, -ms));
-                    const float a1 = ex2(__fmaf_rn(x1, p.scale_log2, -ms));
-                    s += a0 + a1;
-                    w8[e >> 1] = pack_bf16(a0, a1);
+                            for (int e = 0; e < 8; ++e) {
+                                const int kk = 8 * k8 + e;
+                                x[kk] = (win >> kk) & 1u ? x[kk] : -INFINITY;   // outside: weight 0
+                                cmax = fmaxf(cmax, x[kk]);
+                            }
+                        }
+                    }
                 }
-                l_part += s;
-                *reinterpret_cast<uint4 *>(sm + kTcOffP + sw128(uint32_t(row), uint32_t(2 * g), kTcQCb)) =
-                    make_uint4(w8[0], w8[1], w8[2], w8[3]);
-                *reinterpret_cast<uint4 *>(sm + kTcOffP + sw128(uint32_t(row), uint32_t(2 * g + 1), kTcQCb)) =
-                    make_uint4(w8[4], w8[5], w8[6], w8[7]);
+                cmax *= p.scale_log2;   // a positive scale: the maximum of the scaled scores
+                float *rm = red_max + (s * kTcParts) * kTcM;   // this chunk parity's [part][128]
+                rm[qq * kTcM + row] = cmax;
+                // the row's two threads (warps w and w + 4): a named barrier per pair
+                asm volatile("bar.sync %0, %1;" ::"r"(1 + lg), "n"(32 * kTcParts) : "memory");
+                float rmax = rm[row];
+#pragma unroll
+                for (int i = 1; i < kTcParts; ++i) rmax = fmaxf(rmax, rm[i * kTcM + row]);
+                const float mn = fmaxf(m_ref, rmax);
+                // The decisions are the same for the row's threads (the same
+                // inputs); tensor-memory accesses are made by whole warps. A row
+                // without a key so far has O = 0 and l = 0: nothing to rescale.
+                const bool move = mn > m_ref + kLazy;
+                const bool rescale = move && m_ref != -INFINITY;
+                float corr = 1.f;
+                if (move) {
+                    corr = m_ref == -INFINITY ? 0.f : ex2(m_ref - mn);
+                    m_ref = mn;
+                    l_part *= corr;
+                }
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // O must hold chunk c - 1's P V first (the same block)
+                    tc_wait(bar(pEmpty, (gc - 1) & 1), uint32_t((gc - 1) >> 1) & 1u, dead);
+                    tc_fence_after();
+                    float o[16];
+#pragma unroll
+                    for (int h2 = 0; h2 < 128 / kTcParts / 16; ++h2) {
+                        const uint32_t ta = tO + uint32_t(128 / kTcParts * qq + 16 * h2);
+                        tc_ld16(ta, o);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) o[i] *= corr;
+                        tc_st16(ta, o);
+                    }
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                }
+                // weights into P tile s, once P V of chunk gc - 2 is done with it
+                if (gc >= 2) tc_wait(bar(pEmpty, s), (use - 1) & 1u, dead);
+                const float ms = m_ref == -INFINITY ? 0.f : m_ref;
+                unsigned char *pt = sm + kTcOffP + s * kTcPSlot;
+                float sum = 0.f;
+#pragma unroll
+                for (int k8 = 0; k8 < kTcHalf / 8; ++k8) {
+                    if (8 * k8 < nhalf) {
+                        uint32_t w4[4] = {0u, 0u, 0u, 0u};
+                        if ((live >> k8) & 1u) {
+#pragma unroll
+                            for (int e = 0; e < 8; e += 2) {
+                                const float a0 = ex2(__fmaf_rn(x[8 * k8 + e], p.scale_log2, -ms));
+                                const float a1 = ex2(__fmaf_rn(x[8 * k8 + e + 1], p.scale_log2, -ms));
+                                sum += a0 + a1;
+                                w4[e >> 1] = pack_bf16(a0, a1);
+                            }
+                        }
+                        *reinterpret_cast<uint4 *>(pt + sw128(uint32_t(row), uint32_t((cb0 >> 3) + k8), kTcQCb)) =
+                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                }
+                l_part += sum;
+                fence_async_smem();   // P, for the MMA's reads
+                tc_fence_before();    // the reads of S (and O), before the hand-over
+                mbar_arrive(bar(sEmpty, s));
+                mbar_arrive(bar(pFull, s));
             }
-        }
-        // ---- [C] P is in place; once V has landed, O += P V
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_wait(barV, ph, dead);
-            tc_fence_after();
-            const uint32_t id = tc_idesc(kTcM, kHD, 1);
-            for (int s = 0; s < ngrp; ++s)
-                tc_mma(tmem + kTcColO, tc_sdesc(sP + (s >> 2) * kTcQCb + (s & 3) * 32, 16, 1024),
-                       tc_sdesc(sV + s * 2048, kTcKvCb, 1024), id, (s > 0 || o_started) ? 1u : 0u);
-            tc_commit(barO);
-        }
-        o_started = true;
-    }
 
-    // ---- normalise and store this thread's part (128 / kTcParts channels) of its row
-    tc_wait(barO, uint32_t(n_chunks - 1) & 1u, dead);
-    tc_fence_after();
-    red_sum[qq * kTcM + row] = l_part;
-    __syncthreads();
-    float l = red_sum[row];
+            // ---- normalise and store this thread's part (64 channels) of its row
+            tc_wait(bar(pEmpty, (gc - 1) & 1), uint32_t((gc - 1) >> 1) & 1u, dead);
+            tc_fence_after();
+            red_sum[qq * kTcM + row] = l_part;
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + lg), "n"(32 * kTcParts) : "memory");
+            float l = red_sum[row];
 #pragma unroll
-    for (int i = 1; i < kTcParts; ++i) l += red_sum[i * kTcM + row];
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    constexpr int kOCols = 128 / kTcParts;           // channels of this thread
+            for (int i = 1; i < kTcParts; ++i) l += red_sum[i * kTcM + row];
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            constexpr int kOCols = 128 / kTcParts;   // channels of this thread
 #pragma unroll
-    for (int h2 = 0; h2 < kOCols / 16; ++h2) {
-        float o[16];
-        tc_ld16(tO + uint32_t(kOCols * qq + 16 * h2), o);
-        uint32_t packed[8];
+            for (int h2 = 0; h2 < kOCols / 16; ++h2) {
+                float o[16];
+                tc_ld16(tO + uint32_t(kOCols * qq + 16 * h2), o);
+                uint32_t packed[8];
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) packed[i / 2] = pack_bf16(o[i] * inv, o[i + 1] * inv);
-        if (row_ok) {
-            const long long off = token_off(qt, qh, qw) + kOCols * qq + 16 * h2;
-            if (bound_ok(off, 16, p.total)) {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.out + off);
-                dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                for (int i = 0; i < 16; i += 2) packed[i / 2] = pack_bf16(o[i] * inv, o[i + 1] * inv);
+                if (row_ok) {
+                    const long long off = (((long long)g.b * p.T + qt) * p.H + qh) * p.W * tok +
+                                          (long long)qw * tok + (long long)g.head * kHD + kOCols * qq + 16 * h2;
+                    if (bound_ok(off, 16, p.total)) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.out + off);
+                        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                    }
+                }
             }
+            // the reads of O are complete before this block's O buffer is
+            // reused two blocks on (its first P V needs this thread's P first)
+            tc_fence_before();
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + lg), "n"(32 * kTcParts) : "memory");   // red_sum read by all
         }
     }
     tc_fence_before();
@@ -1425,11 +1624,21 @@ TcShape na3d_tc_shape(const NAParams &p) {
     shp.nbt = (p.T + kTcQT - 1) / kTcQT;
     shp.rwb = std::min(p.W, p.kw + kTcQW - 1);
     shp.chb = kTcN / shp.rwb;
+    shp.total = int(uint64_t(p.B) * p.heads * shp.nbt * p.nbh * p.nbw);
     return shp;
 }
 
-uint32_t na3d_tc_blocks(const NAParams &p) {
-    return uint32_t(uint64_t(p.B) * p.heads * na3d_tc_shape(p).nbt * p.nbh * p.nbw);
+// The persistent grid: one CTA per SM (each walks blocks blockIdx.x,
+// blockIdx.x + gridDim.x, ...), no more CTAs than blocks.
+uint32_t na3d_tc_grid(const TcShape &shp) {
+    static const int sms = [] {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 1;
+        return n > 0 ? n : 1;
+    }();
+    return uint32_t(std::min(shp.total, sms));
 }
 
 // cuTensorMapEncodeTiled, from the driver through the runtime's entry-point
@@ -1454,11 +1663,12 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-// The tensor map of one of K and V for the tensor-core kernel: a 5-D view
+// A tensor map of Q, K or V for the tensor-core kernel: a 5-D view
 // (128 channels, heads, W, H, B * T frames) of the [B, T, H, W, heads, 128]
-// buffer, boxes of (64 channels, 1 head, rwb columns, chb rows, 1 frame) with
-// the 128-byte swizzle; coordinates past the grid read zeros.
-bool na3d_tc_map(CUtensorMap *map, const void *base, const NAParams &p, const TcShape &shp) {
+// buffer, boxes of (64 channels, 1 head, bw columns, bh rows, bt frames) with
+// the 128-byte swizzle; coordinates past the view read zeros. K and V use
+// (rwb, chb, 1) boxes (a chunk), Q (8, 8, 2) boxes (a query block).
+bool na3d_tc_map(CUtensorMap *map, const void *base, const NAParams &p, int bw, int bh, int bt) {
     const EncodeTiledFn fn = encode_tiled();
     if (!fn) return false;
     const cuuint64_t tok = cuuint64_t(p.heads) * kHD * 2;   // bytes per token
@@ -1466,7 +1676,7 @@ bool na3d_tc_map(CUtensorMap *map, const void *base, const NAParams &p, const Tc
                                 cuuint64_t(p.H), cuuint64_t(p.B) * cuuint64_t(p.T)};
     const cuuint64_t strides[4] = {cuuint64_t(kHD) * 2, tok, tok * cuuint64_t(p.W),
                                    tok * cuuint64_t(p.W) * cuuint64_t(p.H)};
-    const cuuint32_t box[5] = {64, 1, cuuint32_t(shp.rwb), cuuint32_t(shp.chb), 1};
+    const cuuint32_t box[5] = {64, 1, cuuint32_t(bw), cuuint32_t(bh), cuuint32_t(bt)};
     const cuuint32_t elem[5] = {1, 1, 1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box,
               elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1523,14 +1733,16 @@ extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *ou
     g_na3d_last_kernel = na3d_use_tc(p) ? 1 : 2;
     if (na3d_use_tc(p)) {
         const TcShape shp = na3d_tc_shape(p);
-        CUtensorMap mk, mv;
-        if (!na3d_tc_map(&mk, p.k, p, shp) || !na3d_tc_map(&mv, p.v, p, shp)) return ROPE3D_ERR_CUDA;
+        CUtensorMap mq, mk, mv;
+        if (!na3d_tc_map(&mq, p.q, p, kTcQW, kTcQH, kTcQT) ||
+            !na3d_tc_map(&mk, p.k, p, shp.rwb, shp.chb, 1) || !na3d_tc_map(&mv, p.v, p, shp.rwb, shp.chb, 1))
+            return ROPE3D_ERR_CUDA;
         if (apply_rope) {
             if (!na3d_tc_attribute<kRotQK>()) return ROPE3D_ERR_CUDA;
-            rope3d_na3d_tc_kernel<kRotQK><<<na3d_tc_blocks(p), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv);
+            rope3d_na3d_tc_kernel<kRotQK><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mq, mk, mv);
         } else {
             if (!na3d_tc_attribute<kRotNone>()) return ROPE3D_ERR_CUDA;
-            rope3d_na3d_tc_kernel<kRotNone><<<na3d_tc_blocks(p), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv);
+            rope3d_na3d_tc_kernel<kRotNone><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mq, mk, mv);
         }
     } else {
         if (!na3d_attributes()) return ROPE3D_ERR_CUDA;
@@ -1601,12 +1813,13 @@ extern "C" int rope3d_na3d_rotate_once(const void *q, const void *k, const void 
     const bool tc = na3d_use_tc(p);
     g_na3d_last_kernel = tc ? 1 : 2;
     const TcShape shp = na3d_tc_shape(p);
-    CUtensorMap mk{}, mv{};
-    if (tc && (!na3d_tc_attribute<kRotQ>() || !na3d_tc_map(&mk, p.k, p, shp) ||
-               !na3d_tc_map(&mv, p.v, p, shp)))
+    CUtensorMap mq{}, mk{}, mv{};
+    if (tc && (!na3d_tc_attribute<kRotQ>() || !na3d_tc_map(&mq, p.q, p, kTcQW, kTcQH, kTcQT) ||
+               !na3d_tc_map(&mk, p.k, p, shp.rwb, shp.chb, 1) ||
+               !na3d_tc_map(&mv, p.v, p, shp.rwb, shp.chb, 1)))
         return ROPE3D_ERR_CUDA;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(tc ? na3d_tc_blocks(p) : na3d_blocks(p));
+    cfg.gridDim = dim3(tc ? na3d_tc_grid(shp) : na3d_blocks(p));
     cfg.blockDim = dim3(tc ? kTcThreads : kThreads);
     cfg.dynamicSmemBytes = tc ? kTcSmem : kFixedSmem;
     cfg.stream = st;
@@ -1615,7 +1828,7 @@ extern "C" int rope3d_na3d_rotate_once(const void *q, const void *k, const void 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t le = tc ? cudaLaunchKernelEx(&cfg, rope3d_na3d_tc_kernel<kRotQ>, p, shp, mk, mv)
+    const cudaError_t le = tc ? cudaLaunchKernelEx(&cfg, rope3d_na3d_tc_kernel<kRotQ>, p, shp, mq, mk, mv)
                               : cudaLaunchKernelEx(&cfg, rope3d_na3d_kernel<kRotQ>, p);
     if (le != cudaSuccess) {
         cudaGetLastError();

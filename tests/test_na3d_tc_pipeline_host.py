@@ -1,0 +1,252 @@
+"""A CPU model of the tensor-core attention kernel's hand-over protocol
+(rope_rope3d_apply_gb300/csrc/rope3d_na3d.cu, rope3d_na3d_tc_kernel): the TMA
+thread, the MMA thread, the rotation warps and the softmax threads of one
+persistent CTA walking several query blocks, each a sequence of the kernel's
+mbarrier waits, arrivals and buffer accesses, run in many random
+interleavings over model mbarriers (a phase counter, a pending arrival count
+and a transaction byte count each).
+
+It asserts, in every interleaving, that:
+  - every role runs to its end (no wait that can never be satisfied);
+  - a wait on parity P is never made while the barrier is two or more phases
+    past the phase it stands for (a parity wait cannot tell those apart);
+  - no ring slot, S buffer, P tile or O is written while a reader of the
+    previous contents may still be reading it, nor read before it is written:
+    K slot s is overwritten only after the S MMAs of its last chunk have
+    completed; V slot s only after that chunk's P V; S buffer s only after the
+    softmax read it; P tile s only after its P V; O is rescaled only after the
+    previous P V has completed, and P V of chunk c runs on P and V of chunk c;
+    Q is reloaded only after the previous block's S MMAs, and a block's first
+    P V overwrites an O buffer only after the block two earlier was read out.
+The MMAs' completions are modelled as separate asynchronous events (a commit
+arrives when the MMAs issued before it finish)."""
+from __future__ import annotations
+
+import random
+
+import pytest
+
+
+class Bar:
+    def __init__(self, count):
+        self.count = count
+        self.pending = count
+        self.phase = 0          # completed phases
+        self.tx = 0
+
+    def arrive(self):
+        self.pending -= 1
+        self._maybe_complete()
+
+    def expect_tx(self, n):
+        self.tx += n
+        self.arrive()
+
+    def complete_tx(self, n):
+        self.tx -= n
+        self._maybe_complete()
+
+    def _maybe_complete(self):
+        if self.pending == 0 and self.tx == 0:
+            self.phase += 1
+            self.pending = self.count
+
+    def ready(self, parity, want_phase):
+        """The kernel waits for parity (want_phase & 1) meaning 'phase
+        want_phase has completed'; the wait is only sound if the barrier is
+        at most one phase past it."""
+        assert self.phase <= want_phase + 1, "parity wait outrun by two phases"
+        assert parity == want_phase & 1
+        return self.phase >= want_phase + 1
+
+
+def simulate(blocks, rot_q, rot_k, seed):
+    """blocks: the chunk count of each query block the CTA walks in turn."""
+    rng = random.Random(seed)
+    B = {}
+    for s in (0, 1):
+        for kind, cnt in (("kFull", 1), ("kReady", 128), ("kEmpty", 1), ("vFull", 1), ("vEmpty", 1),
+                          ("sFull", 1), ("sEmpty", 256), ("pFull", 256), ("pEmpty", 1)):
+            B[kind, s] = Bar(cnt)
+    B["qFull"], B["qReady"], B["qEmpty"] = Bar(1), Bar(128), Bar(1)
+    state = {  # what each buffer holds
+        "K": [None, None], "V": [None, None], "S": [None, None], "P": [None, None],
+        "Q": None,                     # block whose Q tile is in place (and "rot")
+        "O": [(-1, -1), (-1, -1)],     # O buffer k & 1: (block, last chunk added)
+        "Oread": [-1, -1],             # O buffer: last block whose result was read out
+    }
+    inflight = []                      # asynchronous events: (kind, payload)
+    SOFT = 4                           # softmax threads modelled (arrivals scaled)
+    # global chunk g -> (block k, chunk c)
+    seq = [(k, c) for k, n in enumerate(blocks) for c in range(n)]
+
+    def producer():
+        g = 0
+        for k, n in enumerate(blocks):
+            if k >= 1:
+                yield ("wait", B["qEmpty"], (k - 1) & 1, k - 1)
+            B["qFull"].expect_tx(2)
+            inflight.append(("tma", ("Q", 0, k)))
+            for c in range(n):
+                s, use = g & 1, g >> 1
+                if g >= 2:
+                    yield ("wait", B["kEmpty", s], (use - 1) & 1, use - 1)
+                B["kFull", s].expect_tx(2)
+                inflight.append(("tma", ("K", s, g)))
+                if g >= 2:
+                    yield ("wait", B["vEmpty", s], (use - 1) & 1, use - 1)
+                B["vFull", s].expect_tx(2)
+                inflight.append(("tma", ("V", s, g)))
+                g += 1
+                yield None
+
+    def mma():
+        def issue_pv(k, c, g):
+            s, use = g & 1, g >> 1
+            yield ("wait", B["pFull", s], use & 1, use)
+            yield ("wait", B["vFull", s], use & 1, use)
+            assert state["P"][s] == g and state["V"][s] == g, "P V reads P and V of its chunk"
+            if c == 0:   # the block's first P V overwrites O buffer k & 1: read out two blocks ago
+                assert state["Oread"][k & 1] == k - 2 or (k < 2 and state["Oread"][k & 1] == -1)
+            inflight.append(("pv", (s, g, k, c)))
+        g = 0
+        for k, n in enumerate(blocks):
+            yield ("wait", B["qReady" if rot_q else "qFull"], k & 1, k)
+            for c in range(n):
+                s, use = g & 1, g >> 1
+                yield ("wait", B["kReady" if rot_k else "kFull", s], use & 1, use)
+                if g >= 2:
+                    yield ("wait", B["sEmpty", s], (use - 1) & 1, use - 1)
+                assert state["K"][s] == (g, "rot" if rot_k else "raw"), "S reads K of its chunk"
+                assert state["Q"] == (k, "rot" if rot_q else "raw"), "S reads Q of its block"
+                inflight.append(("s", (s, g, k, c == n - 1)))
+                if c >= 1:
+                    yield from issue_pv(k, c - 1, g - 1)
+                g += 1
+            yield from issue_pv(k, n - 1, g - 1)
+
+    def rotator(i):
+        g = 0
+        for k, n in enumerate(blocks):
+            if rot_q:
+                yield ("wait", B["qFull"], k & 1, k)
+                if i == 0:
+                    assert state["Q"] == (k, "raw")
+                    state["Q"] = (k, "rot")
+                for _ in range(32):
+                    B["qReady"].arrive()
+            for c in range(n):
+                if rot_k:
+                    s, use = g & 1, g >> 1
+                    yield ("wait", B["kFull", s], use & 1, use)
+                    if i == 0:
+                        assert state["K"][s] == (g, "raw")
+                        state["K"][s] = (g, "rot")
+                    for _ in range(32):
+                        B["kReady", s].arrive()
+                g += 1
+                yield None
+
+    def softmax(i):
+        g = 0
+        for k, n in enumerate(blocks):
+            m_valid = False
+            for c in range(n):
+                s, use = g & 1, g >> 1
+                yield ("wait", B["sFull", s], use & 1, use)
+                assert state["S"][s] == g, "the softmax reads S of its chunk"
+                yield None
+                rescale = m_valid and rng.random() < 0.3
+                m_valid = True
+                if rescale:
+                    prev = g - 1
+                    yield ("wait", B["pEmpty", prev & 1], (prev >> 1) & 1, prev >> 1)
+                    assert state["O"][k & 1] == (k, c - 1), "O rescaled after the previous P V"
+                if g >= 2:
+                    yield ("wait", B["pEmpty", s], (use - 1) & 1, use - 1)
+                assert state["P"][s] in (None, g - 2, g), "P tile free"
+                if i == 0:
+                    state["P"][s] = g
+                for _ in range(256 // SOFT):
+                    B["sEmpty", s].arrive()
+                    B["pFull", s].arrive()
+                g += 1
+                yield None
+            last = g - 1
+            yield ("wait", B["pEmpty", last & 1], (last >> 1) & 1, last >> 1)
+            assert state["O"][k & 1] == (k, n - 1), "the block's O is complete"
+            if i == 0:
+                state["Oread"][k & 1] = k
+
+    roles = [producer(), mma()] + [softmax(i) for i in range(SOFT)]
+    if rot_q or rot_k:
+        roles += [rotator(i) for i in range(4)]
+    waiting = [None] * len(roles)
+    done = [False] * len(roles)
+    steps = 0
+    while not all(done):
+        steps += 1
+        assert steps < 400000, "no progress"
+        choices = [i for i in range(len(roles)) if not done[i]]
+        runnable = [i for i in choices
+                    if waiting[i] is None or waiting[i][0].ready(waiting[i][1], waiting[i][2])]
+        if inflight and (not runnable or rng.random() < 0.4):
+            kinds = [kd for kd, _ in inflight]
+            if "tma" in kinds and (rng.random() < 0.5 or all(kd == "tma" for kd in kinds)):
+                tma_idx = [j for j, kd in enumerate(kinds) if kd == "tma"]
+                idx = rng.choice(tma_idx)
+            else:   # MMAs complete in issue order
+                idx = next(j for j, kd in enumerate(kinds) if kd in ("s", "pv"))
+            kind, pl = inflight.pop(idx)
+            if kind == "tma":
+                buf, s, x = pl
+                if buf == "Q":
+                    # the previous block's S MMAs are done with Q
+                    assert state["Q"] is None or state["Q"][0] == x - 1
+                    state["Q"] = (x, "raw")
+                    B["qFull"].complete_tx(2)
+                elif buf == "K":
+                    assert state["K"][s] is None or state["K"][s][0] <= x - 2
+                    state["K"][s] = (x, "raw")
+                    B["kFull", s].complete_tx(2)
+                else:
+                    assert state["V"][s] is None or state["V"][s] <= x - 2
+                    state["V"][s] = x
+                    B["vFull", s].complete_tx(2)
+            elif kind == "s":
+                s, g, k, last = pl
+                assert state["S"][s] is None or state["S"][s] == g - 2
+                state["S"][s] = g
+                B["kEmpty", s].arrive()      # the commits after S(g)
+                B["sFull", s].arrive()
+                if last:
+                    B["qEmpty"].arrive()
+            else:
+                s, g, k, c = pl
+                ob = state["O"][k & 1]
+                assert (c == 0) or ob == (k, c - 1), "P V in chunk order within the block"
+                state["O"][k & 1] = (k, c)
+                B["vEmpty", s].arrive()      # the two commits after P V(g)
+                B["pEmpty", s].arrive()
+            continue
+        assert runnable, "deadlock"
+        i = rng.choice(runnable)
+        waiting[i] = None
+        try:
+            ev = next(roles[i])
+            if ev is not None:
+                _, bar, parity, phase = ev
+                waiting[i] = (bar, parity, phase)
+        except StopIteration:
+            done[i] = True
+    assert not inflight
+
+
+BLOCKS = [[1], [3], [8], [1, 1, 1], [3, 2, 4], [8, 8, 6, 8], [2, 5, 1, 7, 3]]
+
+
+@pytest.mark.parametrize("blocks", BLOCKS, ids=[str(b) for b in BLOCKS])
+@pytest.mark.parametrize("mode", ["none", "q", "qk"])
+def test_pipeline_protocol(blocks, mode):
+    for seed in range(40):
+        simulate(blocks, mode != "none", mode == "qk", seed * 7919 + len(blocks))

@@ -23,20 +23,35 @@ from __future__ import annotations
 
 import pytest
 
-TC_N = 80                  # keys per chunk at most
 TC_M = 128                 # queries per CTA
-THREADS = 256              # two threads per query row
-PARTS = THREADS // TC_M
-P_BLOCKS = (TC_N + 63) // 64
 QT, QH, QW = 2, 8, 8
 Q_CB = TC_M * 128          # bytes per column block of Q or P
-KV_CB = TC_N * 128         # bytes per column block of K or V
-OFF_Q, OFF_K = 0, 2 * Q_CB
-OFF_V = OFF_K + 2 * KV_CB
-OFF_P = OFF_V + 2 * KV_CB
-OFF_RED = OFF_P + P_BLOCKS * Q_CB
-COL_O = 128
-TMEM_COLS = 256
+
+
+class Config:
+    """The kernel's layout: chunks of up to 112 keys, two-slot rings of K, V
+    and P tiles, two S buffers in tensor memory, one CTA per SM; 256 softmax
+    threads, two per query row."""
+
+    def __init__(self):
+        self.TC_N = 112
+        self.THREADS = 256          # softmax threads
+        self.CTAS = 1
+        self.PARTS = self.THREADS // TC_M
+        self.P_BLOCKS = (self.TC_N + 63) // 64
+        self.KV_CB = self.TC_N * 128
+        self.KV_SLOT = 2 * self.KV_CB
+        self.P_SLOT = self.P_BLOCKS * Q_CB
+        self.OFF_Q, self.OFF_K = 0, 2 * Q_CB
+        self.OFF_V = self.OFF_K + 2 * self.KV_SLOT
+        self.OFF_P = self.OFF_V + 2 * self.KV_SLOT
+        self.OFF_RED = self.OFF_P + 2 * self.P_SLOT
+        self.COL_S = 128            # S buffer s at column s * 128
+        self.COL_O = 256
+        self.TMEM_COLS = 512
+
+
+CONFIGS = {"tc": Config()}
 
 
 def na_start(i, L, k):
@@ -83,7 +98,7 @@ def test_descriptor_encoders():
     # shared-memory descriptor: 14-bit fields of 16-byte units at 0, 16, 32,
     # 0b001 at 46-48, the 128-byte swizzle (2) at 61-63
     for addr in (0, 1024, 0x3FFF0, 139264 + 3 * 16384 + 96):
-        for lbo, sbo in ((16, 1024), (KV_CB, 1024)):
+        for lbo, sbo in ((16, 1024), (80 * 128, 1024), (208 * 128, 1024)):
             d = sdesc(addr, lbo, sbo)
             assert d & 0x3FFF == addr >> 4 and (d >> 16) & 0x3FFF == lbo >> 4
             assert (d >> 32) & 0x3FFF == sbo >> 4 and (d >> 46) & 7 == 1
@@ -91,20 +106,25 @@ def test_descriptor_encoders():
 
 
 def test_device_fastdiv_of_region_widths():
-    for d in range(1, TC_N + 1):
+    for d in range(1, 208 + 1):
         f = fastdiv_make(d)
         for n in list(range(0, 300)) + list(range(4096 - 300, 4096)):
             assert fdiv(n, f) == n // d, (n, d)
 
 
-def test_shared_memory_layout():
-    assert all(o % 1024 == 0 for o in (OFF_K, OFF_V, OFF_P, OFF_RED))
-    total = OFF_RED + 2 * PARTS * TC_M * 4 + 64 + 1024
-    assert 2 * (total + 1024) <= 228 * 1024          # two CTAs per SM (1 KB reserved each)
-    assert COL_O + 128 <= TMEM_COLS and 2 * TMEM_COLS <= 512 and TC_N <= COL_O
+@pytest.mark.parametrize("cfg", sorted(CONFIGS))
+def test_shared_memory_layout(cfg):
+    c = CONFIGS[cfg]
+    assert all(o % 1024 == 0 for o in (c.OFF_K, c.OFF_V, c.OFF_P, c.OFF_RED, c.KV_CB, c.KV_SLOT))
+    total = c.OFF_RED + 12 * TC_M * 4 + 176 + 1024
+    assert c.CTAS * (total + 1024) <= 228 * 1024          # 1 KB reserved per CTA
+    assert c.TC_N <= c.COL_S and c.COL_S + c.TC_N <= c.COL_O and c.COL_O + 128 <= c.TMEM_COLS
 
 
-def check_block(T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
+def check_block(cfg, T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
+    TC_N, THREADS, PARTS, P_BLOCKS = cfg.TC_N, cfg.THREADS, cfg.PARTS, cfg.P_BLOCKS
+    KV_CB, OFF_Q, OFF_K, OFF_V, OFF_P = cfg.KV_CB, cfg.OFF_Q, cfg.OFF_K, cfg.OFF_V, cfg.OFF_P
+    COL_O, COL_S, KV_SLOT, P_SLOT = cfg.COL_O, cfg.COL_S, cfg.KV_SLOT, cfg.P_SLOT
     t0, h0, w0 = bt * QT, bh * QH, bw * QW
     rt0 = na_start(t0, T, kt)
     rt1 = na_start(min(t0 + 1, T - 1), T, kt) + kt
@@ -149,30 +169,49 @@ def check_block(T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
         for j in range(chb * rwb):
             for cv in range(16):
                 assert 0 <= sw128(j, cv, KV_CB) < 2 * KV_CB
+        # the rows the set-up zeroes (past the box, up to the next multiple
+        # of 16) are disjoint from the box's rows and inside each tile, and
+        # every MMA row past the box is one of them
+        box_rows = rwb * chb
+        pad = ((box_rows + 15) & ~15) - box_rows
+        zeroed = set(range(box_rows, box_rows + pad))
+        assert all(r < TC_N for r in zeroed) and not zeroed & set(range(box_rows))
+        assert set(range(box_rows, N)) <= zeroed
+        slot = c & 1   # ring slot of the chunk's K, V and P tiles and S buffer
+        ks_base, vs_base, ps_base = OFF_K + slot * KV_SLOT, OFF_V + slot * KV_SLOT, OFF_P + slot * P_SLOT
         # S = Q K^T: eight k16 steps; A reads 128 rows of 32 bytes at koff in
         # column block ks / 4, B reads N rows likewise
         for ks in range(8):
             koff = (ks & 3) * 32
             a0 = OFF_Q + (ks >> 2) * Q_CB + koff
-            b0 = OFF_K + (ks >> 2) * KV_CB + koff
+            b0 = ks_base + (ks >> 2) * KV_CB + koff
             assert OFF_Q <= a0 and a0 - koff + TC_M * 128 <= OFF_Q + 2 * Q_CB
-            assert OFF_K <= b0 and b0 - koff + N * 128 <= OFF_K + 2 * KV_CB
+            assert ks_base <= b0 and b0 - koff + N * 128 <= ks_base + KV_SLOT
         # O += P V: N / 16 k16 steps; P in column block s / 4; V as an MN-major
         # operand: 16 keys (2 groups of 8 rows, SBO = 1024) x 128 channels (2
         # column blocks, LBO = KV_CB)
         for s in range(N // 16):
-            pa = OFF_P + (s >> 2) * Q_CB + (s & 3) * 32
-            assert OFF_P <= pa and pa - (s & 3) * 32 + TC_M * 128 <= OFF_P + P_BLOCKS * Q_CB
-            va = OFF_V + s * 2048
-            assert OFF_V <= va and va + 1024 + 1024 + KV_CB <= OFF_V + 2 * KV_CB
-        assert N <= COL_O   # S columns [0, N) stay clear of O's [128, 256)
-        # the P tile: group g of a row goes to chunks 2 g and 2 g + 1
-        for g in range(N // 16):
-            for ch in (2 * g, 2 * g + 1):
-                assert ch // 8 < P_BLOCKS
-        # the softmax masks of every query row (thread part qq takes the
-        # groups qq, qq + PARTS, ...): a group's 16-bit mask is built from the
-        # chunk rows it spans, each in the window contributing columns [clo, chi)
+            pa = ps_base + (s >> 2) * Q_CB + (s & 3) * 32
+            assert ps_base <= pa and pa - (s & 3) * 32 + TC_M * 128 <= ps_base + P_SLOT
+            va = vs_base + s * 2048
+            assert vs_base <= va and va + 1024 + 1024 + KV_CB <= vs_base + KV_SLOT
+        # S buffer `slot` holds columns [slot * COL_S, + N), clear of the other and of O
+        assert slot * COL_S + N <= (slot + 1) * COL_S <= COL_O
+        # the softmax: thread part qq of a row reads columns [qq * npart, + 56)
+        # of its S buffer (npart = N / 2 used, the rest masked) and writes the
+        # weights of its npart columns 8 keys (16 bytes) at a time
+        npart = N // PARTS
+        assert PARTS == 2 and npart % 8 == 0 and npart <= 56
+        for qq in range(PARTS):
+            cb0 = qq * npart
+            assert cb0 + 56 <= COL_S                  # inside this S buffer
+            for k8 in range(7):
+                if 8 * k8 < npart:
+                    key = cb0 + 8 * k8
+                    assert key % 8 == 0 and (key >> 3) // 8 < P_BLOCKS
+        # the window masks of every query row: a 64-bit mask per thread part,
+        # built from the chunk rows its part spans, each in the window
+        # contributing columns [clo, chi)
         for row in range(TC_M):
             qt, qh, qw = t0 + (row >> 6), h0 + ((row >> 3) & 7), w0 + (row & 7)
             row_ok = qt < T and qh < H and qw < W
@@ -182,26 +221,25 @@ def check_block(T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
             clo, chi = max(aw, 0), min(aw + kw, RW)
             frame_ok = row_ok and 0 <= f - st_q < kt
             for qq in range(PARTS):
-                for g in range(qq, N // 16, PARTS):
-                    j0 = 16 * g
-                    rr0 = fdiv(j0, rwd)
-                    bits = 0
-                    if frame_ok:
-                        rr, js = rr0, rr0 * rwb - j0
-                        while js < 16 and rr < nr:
-                            if 0 <= r0 + rr - ah < kh:
-                                a, b2 = max(js + clo, 0), min(js + chi, 16)
-                                if a < b2:
-                                    bits |= (0xFFFF >> (16 - (b2 - a))) << a
-                            rr += 1
-                            js += rwb
-                    assert bits < (1 << 16)
-                    for e in range(16):
-                        if bits >> e & 1:
-                            key = rows[j0 + e]
-                            assert key is not None          # never a zero-filled key
-                            meet = (qt, qh, qw) + key
-                            seen[meet] = seen.get(meet, 0) + 1
+                cb0 = qq * npart
+                win = 0
+                if frame_ok:
+                    rr = fdiv(cb0, rwd)
+                    js = rr * rwb - cb0
+                    while js < npart and rr < nr:
+                        if 0 <= r0 + rr - ah < kh:
+                            a, b2 = max(js + clo, 0), min(js + chi, npart)
+                            if a < b2:
+                                win |= ((1 << 64) - 1 >> (64 - (b2 - a))) << a
+                        rr += 1
+                        js += rwb
+                assert win < (1 << npart)
+                for k in range(npart):
+                    if win >> k & 1:
+                        key = rows[cb0 + k]
+                        assert key is not None          # never a zero-filled key
+                        meet = (qt, qh, qw) + key
+                        seen[meet] = seen.get(meet, 0) + 1
     # every query of the block meets each key of its window once, and no other
     expected = 0
     for qt in range(t0, min(t0 + QT, T)):
@@ -217,16 +255,16 @@ def check_block(T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
     return expected
 
 
-def check_grid(T, H, W, kt, kh, kw, blocks=None):
+def check_grid(cfg, T, H, W, kt, kh, kw, blocks=None):
     nbt, nbh, nbw = (T + QT - 1) // QT, (H + QH - 1) // QH, (W + QW - 1) // QW
     if blocks is None:
         blocks = [(bt, bh, bw) for bt in range(nbt) for bh in range(nbh) for bw in range(nbw)]
-    assert sum(check_block(T, H, W, kt, kh, kw, *blk) for blk in blocks) > 0
+    assert sum(check_block(cfg, T, H, W, kt, kh, kw, *blk) for blk in blocks) > 0
 
 
-def tc_eligible(W, kw):
+def tc_eligible(W, kw, tc_n=112):
     """The host's choice: the tensor-core kernel when a region row fits a chunk."""
-    return min(W, kw + QW - 1) <= TC_N
+    return min(W, kw + QW - 1) <= tc_n
 
 
 GEOMETRIES = [
@@ -238,11 +276,13 @@ GEOMETRIES = [
 ]
 
 
-def test_eligibility_bounds_every_region_row():
+@pytest.mark.parametrize("cfg", sorted(CONFIGS))
+def test_eligibility_bounds_every_region_row(cfg):
     """min(W, kw + 7) <= kTcN makes every block's region row fit a chunk."""
-    for W in range(1, 200):
+    TC_N = CONFIGS[cfg].TC_N
+    for W in range(1, 240):
         for kw in range(1, W + 1, 2):
-            if not tc_eligible(W, kw):
+            if not tc_eligible(W, kw, TC_N):
                 continue
             for w0 in range(0, W, QW):
                 rw0 = na_start(w0, W, kw)
@@ -250,15 +290,17 @@ def test_eligibility_bounds_every_region_row():
                 assert 1 <= RW <= TC_N
 
 
+@pytest.mark.parametrize("cfg", sorted(CONFIGS))
 @pytest.mark.parametrize("geom", GEOMETRIES, ids=[str(g) for g in GEOMETRIES])
-def test_tc_tiling_covers_every_window_once(geom):
-    assert tc_eligible(geom[2], geom[5])
-    check_grid(*geom)
+def test_tc_tiling_covers_every_window_once(geom, cfg):
+    assert tc_eligible(geom[2], geom[5], CONFIGS[cfg].TC_N)
+    check_grid(CONFIGS[cfg], *geom)
 
 
-def test_tc_tiling_of_the_benchmark_geometry():
+@pytest.mark.parametrize("cfg", sorted(CONFIGS))
+def test_tc_tiling_of_the_benchmark_geometry(cfg):
     """16 x 64 x 64 tokens, window 3 x 7 x 7: corner, edge and inner blocks of
     the first, a middle and the last frame pair."""
     picks = [0, 1, 4, 7]
-    check_grid(16, 64, 64, 3, 7, 7,
+    check_grid(CONFIGS[cfg], 16, 64, 64, 3, 7, 7,
                blocks=[(bt, bh, bw) for bt in (0, 4, 7) for bh in picks for bw in picks])
