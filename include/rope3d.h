@@ -366,13 +366,15 @@ int rope3d_na3d_preflight(const void *q, const void *k, const void *v, const voi
 
 /*
  * Test hooks of the neighbourhood attention. Its attention has two kernels:
- * one on the warp-level MMAs (the default) and one on the fifth-generation
- * tensor cores (tcgen05 MMAs with fp32 accumulators in tensor memory; 2 x 8 x 8
- * query blocks; it needs key-region rows of at most 80 keys, i.e.
- * min(W, kw + 7) <= 80). Both are held to the same bound of the oracle, and
- * all rotation modes of one kernel give the same bits.
+ * one on the fifth-generation tensor cores (tcgen05 MMAs with fp32
+ * accumulators in tensor memory; 2 x 8 x 8 query blocks; it needs key-region
+ * rows of at most 112 keys, i.e. min(W, kw + 7) <= 112), the default wherever
+ * that holds, and one on the warp-level MMAs, for every other geometry. Both
+ * are held to the same bound of the oracle, and all rotation modes of one
+ * kernel give the same bits.
  *   rope3d_testing_na3d_kernel(which): 0 = the default, 1 = the tensor-core
- *     kernel where the geometry allows it, 2 = the warp-MMA kernel. Errors: ARG.
+ *     kernel where the geometry allows it (the same as 0), 2 = the warp-MMA
+ *     kernel always. Errors: ARG.
  *   rope3d_testing_na3d_last_kernel(): the kernel of this thread's last
  *     attention launch: 1 tensor-core, 2 warp-MMA, 0 none yet.
  *   rope3d_testing_na3d_wait_timeouts(count, reset): how many bounded waits

@@ -768,19 +768,24 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 }
 
 // ---- the attention on the fifth-generation tensor cores -------------------
-// A CTA owns one (batch, head) and a 2 x 8 x 8 block of queries: the 128 rows
-// of a tcgen05 MMA (M = 128). The union of the block's windows (its key
-// region) is streamed in chunks of whole region rows of one frame, at most
-// kTcN keys each. The CTA's warps have one job each and hand work over through
-// mbarriers, so that the tensor cores, the copies and the softmax overlap:
+// A query block is one (batch, head) and 2 x 8 x 8 queries: the 128 rows of a
+// tcgen05 MMA (M = 128). The union of the block's windows (its key region) is
+// streamed in chunks of whole region rows of one frame, at most kTcN keys
+// each. One persistent CTA per SM walks the blocks blockIdx.x, + gridDim.x,
+// ...; its warps have one job each and hand work over through mbarriers
+// (counted over the CTA's whole sequence of chunks and blocks), so that the
+// tensor cores, the copies and the softmax overlap, also across blocks:
 //   warp 0 (one thread): TMA copies of each chunk's K and V (two boxes each,
 //     one per 64 channels, with the 128-byte swizzle) into two-slot rings;
 //   warp 1 (one thread): the MMAs. S(c) = Q K(c)^T into one of two S buffers
 //     in tensor memory (eight k16 steps), then O += P(c-1) V(c-1) (V read as
 //     an MN-major operand); so S(c + 1) and P V of chunk c - 1 run while the
 //     softmax of chunk c does;
-//   warps 2-5 (the rotating modes): rotate each query block's Q tile, and in
-//     the mode that rotates K per CTA each K tile, in place once it lands;
+//   warps 2-5: each query block's Q tile, read from global memory into
+//     registers (and rotated there in the rotating modes) while the previous
+//     block still uses the Q buffer, then written into it in the swizzled
+//     layout; in the mode that rotates K per CTA, each K tile too, in place
+//     once it lands;
 //   warps 6-13: the softmax. Each query row's S is read back from tensor
 //     memory by two threads (half of the chunk's columns each, in one batch of
 //     loads: warps w and w + 4 share the 32 lanes of tensor memory that warp w
@@ -791,13 +796,16 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 //     warp-MMA kernel (the reference moves only when a row maximum passes it
 //     by more than 2^kLazy; O in tensor memory is rescaled then); the bf16
 //     weights go to one of two P tiles (K-major, swizzled).
-// Q (rotated here in the rotating modes) stays in shared memory for every chunk.
+// Q stays in shared memory for every chunk of its block.
 // Shared memory (bytes; every tile 1024-aligned, the swizzle's period):
 //   Q  [2 column blocks][128 rows][128 B]               32,768
 //   K  [2 slots][2 column blocks][kTcN rows][128 B]     57,344
 //   V  [2 slots][2 column blocks][kTcN rows][128 B]     57,344
 //   P  [2 slots][2 column blocks of 64 keys][128][128 B] 65,536
-//   row maxima and sums of the row's two threads, 18 mbarriers, the TMEM address.
+//   row maxima and sums of the row's two threads, 20 mbarriers, the TMEM address.
+// Tensor memory (512 columns): S buffers at columns 0 and 128, O of even and
+// odd blocks at 256 and 384 (the next block's P V starts while the epilogue
+// reads the previous O).
 // Tensor memory (all 512 columns: one CTA per SM): S in [0, 128) and
 // [128, 256), O in [256, 384).
 constexpr int kTcThreads = 448;              // 14 warps: TMA, MMA, 4 rotation, 8 softmax
@@ -819,7 +827,7 @@ constexpr uint32_t kTcOffK = kTcOffQ + 2 * kTcQCb;
 constexpr uint32_t kTcOffV = kTcOffK + 2 * kTcKvSlot;
 constexpr uint32_t kTcOffP = kTcOffV + 2 * kTcKvSlot;
 constexpr uint32_t kTcOffRed = kTcOffP + 2 * kTcPSlot;      // float max [2][2][128], sum [2][128]
-constexpr uint32_t kTcOffBar = kTcOffRed + 6 * kTcM * 4;    // 21 mbarriers + TMEM address
+constexpr uint32_t kTcOffBar = kTcOffRed + 6 * kTcM * 4;    // 20 mbarriers + TMEM address
 constexpr uint32_t kTcSmem = kTcOffBar + 176 + 1024;        // + room to align to 1024
 constexpr uint32_t kTcColS = 128;                           // S buffer b at column b * 128
 constexpr uint32_t kTcColO = 256;                           // O of block k at 256 + 128 (k & 1)
@@ -999,15 +1007,6 @@ __device__ __forceinline__ void tc_ld16_async(uint32_t taddr, float *v) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tc_ld4_async(uint32_t taddr, float *v) {
-    uint32_t r[4];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(taddr)
-                 : "memory");
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 // Wait for this thread's tensor-memory loads; the n registers of v pass
 // through the asm so that no use of them moves above the wait.
@@ -1088,8 +1087,8 @@ __device__ __forceinline__ TcBlock tc_block(const NAParams &p, const TcShape &sh
 
 template <int kMode>
 __global__ void __launch_bounds__(kTcThreads, 1)
-rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant__ CUtensorMap tmQ,
-                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV) {
     extern __shared__ unsigned char tc_raw[];
     unsigned char *sm = tc_raw + ((1024u - (smem_addr(tc_raw) & 1023u)) & 1023u);
     const uint32_t sQ = smem_addr(sm + kTcOffQ), sK = smem_addr(sm + kTcOffK);
@@ -1097,7 +1096,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     float *red_max = reinterpret_cast<float *>(sm + kTcOffRed);   // [chunk parity][part][128]
     float *red_sum = red_max + 2 * kTcParts * kTcM;                 // [part][128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kTcOffBar);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kTcOffBar + 21 * 8);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kTcOffBar + 20 * 8);
     // mbarriers, two of each kind (one per ring slot s = chunk & 1), counted
     // over the CTA's whole sequence of chunks:
     //   kFull  K landed (TMA)          kReady  K rotated (kRotQK; 128 arrivals)
@@ -1105,12 +1104,11 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     //   vEmpty P V MMAs done with V    sFull   S written (MMA)
     //   sEmpty softmax done with S (256 arrivals)
     //   pFull  P written (256 arrivals)  pEmpty P V MMAs done with P (and O updated)
-    // and one of each per query block: qFull (Q landed), qReady (Q rotated;
-    // 128 arrivals), qEmpty (the block's S MMAs done with Q).
+    // and one of each per query block: qReady (the Q tile written, rotated in
+    // the rotating modes; 128 arrivals), qEmpty (the block's S MMAs done with Q).
     auto bar = [&](int kind, int slot) { return smem_addr(&bars[2 * kind + slot]); };
     enum { kFull, kReady, kEmpty, vFull, vEmpty, sFull, sEmpty, pFull, pEmpty };
-    const uint32_t qFull = smem_addr(&bars[18]), qReady = smem_addr(&bars[19]);
-    const uint32_t qEmpty = smem_addr(&bars[20]);
+    const uint32_t qReady = smem_addr(&bars[18]), qEmpty = smem_addr(&bars[19]);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long tok = (long long)p.heads * kHD;   // elements per token
@@ -1140,11 +1138,6 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         tma_load5(dst, map, 0, g.head, g.rw0, g.rh0 + r0, frame, full);
         tma_load5(dst + kTcKvCb, map, 64, g.head, g.rw0, g.rh0 + r0, frame, full);
     };
-    auto tma_q = [&](const TcBlock &g) {   // the block's 2 x 8 x 8 queries, rows (t, h, w)
-        mbar_expect_tx(qFull, 2 * kTcQCb);
-        tma_load5(sQ, &tmQ, 0, g.head, g.w0, g.h0, g.b * p.T + g.t0, qFull);
-        tma_load5(sQ + kTcQCb, &tmQ, 64, g.head, g.w0, g.h0, g.b * p.T + g.t0, qFull);
-    };
 
     // ---- set-up: barriers, tensor memory, zeroed pad rows
     if (tid == 0) {
@@ -1154,11 +1147,9 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar(kind, s)),
                              "r"(counts[kind]) : "memory");
         }
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(qFull) : "memory");
         asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(qReady), "r"(kTcRotThreads) : "memory");
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(qEmpty) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmQ)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
     }
@@ -1187,8 +1178,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     bool dead = false;
 
     if (warp == 0) {
-        // ---- TMA producer: each block's Q (once the previous block's S MMAs
-        // are done with Q), then its chunks' K and V into the rings
+        // ---- TMA producer: each block's chunks' K and V into the rings
         if (lane == 0) {
             // K of the rotate-once form comes from the kernel before this one in
             // the stream (programmatic serialization): wait for it first
@@ -1196,8 +1186,6 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             int gc = 0;   // chunks of the CTA so far
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
                 const TcBlock g = tc_block(p, shp, blk);
-                if (k >= 1) tc_wait(qEmpty, uint32_t(k - 1) & 1u, dead);
-                tma_q(g);
                 for (int c = 0; c < g.n_chunks; ++c, ++gc) {
                     const int s = gc & 1;
                     const uint32_t use = uint32_t(gc >> 1);
@@ -1231,7 +1219,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
                 const TcBlock g = tc_block(p, shp, blk);
                 const uint32_t o_col = tmem + kTcColO + uint32_t(k & 1) * 128;
-                tc_wait(kMode == kRotNone ? qFull : qReady, uint32_t(k) & 1u, dead);
+                tc_wait(qReady, uint32_t(k) & 1u, dead);
                 for (int c = 0; c < g.n_chunks; ++c, ++gc) {
                     const int s = gc & 1;
                     const uint32_t use = uint32_t(gc >> 1);
@@ -1255,24 +1243,49 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             }
         }
     } else if (warp < kTcSoftWarp0) {
-        // ---- rotation warps: each block's Q tile (rotating modes), and in the
-        // mode that rotates K per CTA each K tile, in place once landed
-        if constexpr (kMode != kRotNone) {
+        // ---- Q warps: each block's Q tile through registers (read from global
+        // memory and, in the rotating modes, rotated before the previous block
+        // is done with the Q buffer; then written into it in the layout of a
+        // 128-byte-swizzled TMA box); in the mode that rotates K per CTA, each
+        // K tile too, in place once it lands.
+        // Thread rt holds 16-byte vector cv = rt % 16 of query rows
+        // rt / 16 + 8 i, i = 0 .. 15: a row is (t, h, w) = (i / 8, i % 8, rt / 16)
+        // from the block's corner, so a warp reads two tokens' 256 bytes.
+        {
             const int rt = tid - 64;   // 0 .. kTcRotThreads - 1
-            const TabSlot tsg = tab_slot_global(p.pT, p.pH, p.pW, p.offH, p.offW, rt & 15);
-            int gc = 0;
+            const int cv = rt & 15, qw_off = rt >> 4;
+            [[maybe_unused]] const TabSlot tsg = tab_slot_global(p.pT, p.pH, p.pW, p.offH, p.offW, cv);
+            [[maybe_unused]] int gc = 0;
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
                 const TcBlock g = tc_block(p, shp, blk);
-                tc_wait(qFull, uint32_t(k) & 1u, dead);
-                for (int u = rt; u < kTcM * 16; u += kTcRotThreads) {
-                    const int r = u >> 4, cv = u & 15;
-                    const int t = g.t0 + (r >> 6), h = g.h0 + ((r >> 3) & 7), w = g.w0 + (r & 7);
+                const int w = g.w0 + qw_off;
+                uint4 qv[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int t = g.t0 + (i >> 3), h = g.h0 + (i & 7);
+                    qv[i] = make_uint4(0u, 0u, 0u, 0u);   // outside the grid: zeros
                     if (t < p.T && h < p.H && w < p.W) {
-                        const int pos = tsg.axis == 0 ? t : (tsg.axis == 1 ? h : w);
-                        uint4 *ptr = reinterpret_cast<uint4 *>(sm + kTcOffQ + sw128(r, cv, kTcQCb));
-                        *ptr = rot_vec_at<true>(*ptr, p.tab, tsg, uint32_t(pos), p.tab_len);
+                        const long long off = (((long long)g.b * p.T + t) * p.H + h) * p.W * tok +
+                                              (long long)w * tok + (long long)g.head * kHD + 8 * cv;
+                        if (bound_ok(off, 8, p.total))
+                            qv[i] = __ldg(reinterpret_cast<const uint4 *>(p.q + off));
                     }
                 }
+                if constexpr (kMode != kRotNone) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int t = g.t0 + (i >> 3), h = g.h0 + (i & 7);
+                        if (t < p.T && h < p.H && w < p.W) {
+                            const int pos = tsg.axis == 0 ? t : (tsg.axis == 1 ? h : w);
+                            qv[i] = rot_vec_at<true>(qv[i], p.tab, tsg, uint32_t(pos), p.tab_len);
+                        }
+                    }
+                }
+                // the previous block's S MMAs are done with the Q buffer
+                if (k >= 1) tc_wait(qEmpty, uint32_t(k - 1) & 1u, dead);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    *reinterpret_cast<uint4 *>(sm + kTcOffQ + sw128(uint32_t(qw_off + 8 * i), uint32_t(cv), kTcQCb)) = qv[i];
                 fence_async_smem();
                 mbar_arrive(qReady);
                 if constexpr (kMode == kRotQK) {
@@ -1341,6 +1354,9 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                     tc_ld8_async(tS + uint32_t(cb0 + 48), x + 48);
                     tc_ld_wait_hold<kTcHalf>(x);
                 }
+                // S is in registers: the MMA may write S(c + 2) into this buffer
+                tc_fence_before();
+                mbar_arrive(bar(sEmpty, s));
                 // window mask: bit k stands for column cb0 + k; each chunk row the
                 // half spans that lies in the window contributes its columns [clo, chi)
                 uint64_t win = 0;
@@ -1392,21 +1408,6 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                     m_ref = mn;
                     l_part *= corr;
                 }
-                if (__any_sync(0xffffffffu, rescale)) {
-                    // O must hold chunk c - 1's P V first (the same block)
-                    tc_wait(bar(pEmpty, (gc - 1) & 1), uint32_t((gc - 1) >> 1) & 1u, dead);
-                    tc_fence_after();
-                    float o[16];
-#pragma unroll
-                    for (int h2 = 0; h2 < 128 / kTcParts / 16; ++h2) {
-                        const uint32_t ta = tO + uint32_t(128 / kTcParts * qq + 16 * h2);
-                        tc_ld16(ta, o);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) o[i] *= corr;
-                        tc_st16(ta, o);
-                    }
-                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                }
                 // weights into P tile s, once P V of chunk gc - 2 is done with it
                 if (gc >= 2) tc_wait(bar(pEmpty, s), (use - 1) & 1u, dead);
                 const float ms = m_ref == -INFINITY ? 0.f : m_ref;
@@ -1430,9 +1431,25 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                     }
                 }
                 l_part += sum;
+                // O rescaled after the weights are out (the row's S values are
+                // no longer held), before P V of this chunk adds to it
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // O must hold chunk c - 1's P V first (the same block)
+                    tc_wait(bar(pEmpty, (gc - 1) & 1), uint32_t((gc - 1) >> 1) & 1u, dead);
+                    tc_fence_after();
+                    float o[16];
+#pragma unroll 1   // (unrolled, the loads are hoisted and registers spill)
+                    for (int h2 = 0; h2 < 128 / kTcParts / 16; ++h2) {
+                        const uint32_t ta = tO + uint32_t(128 / kTcParts * qq + 16 * h2);
+                        tc_ld16(ta, o);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) o[i] *= corr;
+                        tc_st16(ta, o);
+                    }
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                }
                 fence_async_smem();   // P, for the MMA's reads
-                tc_fence_before();    // the reads of S (and O), before the hand-over
-                mbar_arrive(bar(sEmpty, s));
+                tc_fence_before();    // the accesses of O, before the hand-over
                 mbar_arrive(bar(pFull, s));
             }
 
@@ -1663,11 +1680,11 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-// A tensor map of Q, K or V for the tensor-core kernel: a 5-D view
+// A tensor map of K or V for the tensor-core kernel: a 5-D view
 // (128 channels, heads, W, H, B * T frames) of the [B, T, H, W, heads, 128]
 // buffer, boxes of (64 channels, 1 head, bw columns, bh rows, bt frames) with
-// the 128-byte swizzle; coordinates past the view read zeros. K and V use
-// (rwb, chb, 1) boxes (a chunk), Q (8, 8, 2) boxes (a query block).
+// the 128-byte swizzle; coordinates past the view read zeros. A chunk is a
+// (rwb, chb, 1) box.
 bool na3d_tc_map(CUtensorMap *map, const void *base, const NAParams &p, int bw, int bh, int bt) {
     const EncodeTiledFn fn = encode_tiled();
     if (!fn) return false;
@@ -1683,15 +1700,16 @@ bool na3d_tc_map(CUtensorMap *map, const void *base, const NAParams &p, int bw, 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Which attention kernel runs: 0 = the library's default (the warp-MMA
-// kernel, measured faster so far), 1 = the tensor-core kernel where the
-// geometry allows it, 2 = the warp-MMA kernel (rope3d_testing_na3d_kernel).
+// Which attention kernel runs: 0 = the library's default and 1 = the
+// tensor-core kernel wherever the geometry allows it (the faster of the two
+// in every rotation mode on the 16 x 64 x 64, 16-head, 3 x 7 x 7 workload),
+// else the warp-MMA kernel; 2 = always the warp-MMA kernel
+// (rope3d_testing_na3d_kernel).
 std::atomic<int> g_na3d_kernel{0};
 thread_local int g_na3d_last_kernel = 0;   // 1 tensor-core, 2 warp-MMA kernel
 
 bool na3d_use_tc(const NAParams &p) {
-    const int pick = g_na3d_kernel.load(std::memory_order_relaxed);
-    if (pick != 1) return false;
+    if (g_na3d_kernel.load(std::memory_order_relaxed) == 2) return false;
     return std::min(p.W, p.kw + kTcQW - 1) <= kTcMaxRW;
 }
 
@@ -1733,16 +1751,15 @@ extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *ou
     g_na3d_last_kernel = na3d_use_tc(p) ? 1 : 2;
     if (na3d_use_tc(p)) {
         const TcShape shp = na3d_tc_shape(p);
-        CUtensorMap mq, mk, mv;
-        if (!na3d_tc_map(&mq, p.q, p, kTcQW, kTcQH, kTcQT) ||
-            !na3d_tc_map(&mk, p.k, p, shp.rwb, shp.chb, 1) || !na3d_tc_map(&mv, p.v, p, shp.rwb, shp.chb, 1))
+        CUtensorMap mk, mv;
+        if (!na3d_tc_map(&mk, p.k, p, shp.rwb, shp.chb, 1) || !na3d_tc_map(&mv, p.v, p, shp.rwb, shp.chb, 1))
             return ROPE3D_ERR_CUDA;
         if (apply_rope) {
             if (!na3d_tc_attribute<kRotQK>()) return ROPE3D_ERR_CUDA;
-            rope3d_na3d_tc_kernel<kRotQK><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mq, mk, mv);
+            rope3d_na3d_tc_kernel<kRotQK><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv);
         } else {
             if (!na3d_tc_attribute<kRotNone>()) return ROPE3D_ERR_CUDA;
-            rope3d_na3d_tc_kernel<kRotNone><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mq, mk, mv);
+            rope3d_na3d_tc_kernel<kRotNone><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv);
         }
     } else {
         if (!na3d_attributes()) return ROPE3D_ERR_CUDA;
@@ -1813,9 +1830,8 @@ extern "C" int rope3d_na3d_rotate_once(const void *q, const void *k, const void 
     const bool tc = na3d_use_tc(p);
     g_na3d_last_kernel = tc ? 1 : 2;
     const TcShape shp = na3d_tc_shape(p);
-    CUtensorMap mq{}, mk{}, mv{};
-    if (tc && (!na3d_tc_attribute<kRotQ>() || !na3d_tc_map(&mq, p.q, p, kTcQW, kTcQH, kTcQT) ||
-               !na3d_tc_map(&mk, p.k, p, shp.rwb, shp.chb, 1) ||
+    CUtensorMap mk{}, mv{};
+    if (tc && (!na3d_tc_attribute<kRotQ>() || !na3d_tc_map(&mk, p.k, p, shp.rwb, shp.chb, 1) ||
                !na3d_tc_map(&mv, p.v, p, shp.rwb, shp.chb, 1)))
         return ROPE3D_ERR_CUDA;
     cudaLaunchConfig_t cfg{};
@@ -1828,7 +1844,7 @@ extern "C" int rope3d_na3d_rotate_once(const void *q, const void *k, const void 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t le = tc ? cudaLaunchKernelEx(&cfg, rope3d_na3d_tc_kernel<kRotQ>, p, shp, mq, mk, mv)
+    const cudaError_t le = tc ? cudaLaunchKernelEx(&cfg, rope3d_na3d_tc_kernel<kRotQ>, p, shp, mk, mv)
                               : cudaLaunchKernelEx(&cfg, rope3d_na3d_kernel<kRotQ>, p);
     if (le != cudaSuccess) {
         cudaGetLastError();

@@ -28,8 +28,8 @@ import rope_rope3d_apply_gb300 as r  # noqa: E402
 
 DEV = torch.device("cuda:0")
 
-# The attention kernels: 1 = tensor-core (tcgen05), 2 = warp-level MMA (the
-# default). Each is held to the same bound.
+# The attention kernels: 1 = tensor-core (tcgen05; the default where its
+# geometry allows), 2 = warp-level MMA. Each is held to the same bound.
 KERNELS = [1, 2]
 
 
@@ -234,10 +234,12 @@ def _bench_queries(B, T, H, W, heads, count, seed):
     return fixed + rand
 
 
-def test_na3d_full_size_sampled():
+@pytest.mark.parametrize("which", [0, 2])
+def test_na3d_full_size_sampled(which):
     """The attention workload bench.py times (1 x 16 x 64 x 64 tokens, 16
     heads x 128, bf16, window 3 x 7 x 7, same seeds), launched as the bench
-    launches it: 192 sampled queries of the fused kernel against the oracle
+    launches it (the default kernel, the tensor-core one here; and the
+    warp-MMA kernel): 192 sampled queries of the fused kernel against the oracle
     computed one query at a time, and the unfused pair and the rotate-once
     form bit-identical to it."""
     B, T, H, W, heads, split, kernel = 1, 16, 64, 64, 16, (32, 48, 48), (3, 7, 7)
@@ -247,12 +249,13 @@ def test_na3d_full_size_sampled():
     bits = [synthetic.normal(n, 1.0, 12, i, "bf16") for i in range(3)]
     q, k, v = (bf16(a).reshape(shp).to(DEV) for a in bits)
     tabs = r.rope3d_build_tables(T, H, W, split)
+    r.rope3d_testing_na3d_kernel(which)
     fused = r.rope3d_na3d(q, k, v, tabs, kernel)
     qr, kr = r.rope3d_apply_pair(q, k, tabs)
     unfused = r.rope3d_na3d(qr, kr, v, tabs, kernel, apply_rope=False)
     once, k_rot = r.rope3d_na3d_rotate_once(q, k, v, tabs, kernel)
     torch.cuda.synchronize()
-    assert r.rope3d_testing_na3d_last_kernel() == 2    # the default: the warp-MMA kernel
+    assert r.rope3d_testing_na3d_last_kernel() == (1 if which == 0 else 2)
     assert torch.equal(fused.view(torch.int16), unfused.view(torch.int16))
     assert torch.equal(once.view(torch.int16), unfused.view(torch.int16))
     assert torch.equal(k_rot.view(torch.int16), kr.view(torch.int16))

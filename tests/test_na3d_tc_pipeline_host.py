@@ -1,7 +1,8 @@
 """A CPU model of the tensor-core attention kernel's hand-over protocol
 (rope_rope3d_apply_gb300/csrc/rope3d_na3d.cu, rope3d_na3d_tc_kernel): the TMA
-thread, the MMA thread, the rotation warps and the softmax threads of one
-persistent CTA walking several query blocks, each a sequence of the kernel's
+thread, the MMA thread, the Q warps (which write each block's Q tile and, in
+the mode that rotates K per CTA, rotate the K tiles) and the softmax threads
+of one persistent CTA walking several query blocks, each a sequence of the kernel's
 mbarrier waits, arrivals and buffer accesses, run in many random
 interleavings over model mbarriers (a phase counter, a pending arrival count
 and a transaction byte count each).
@@ -16,7 +17,7 @@ It asserts, in every interleaving, that:
     completed; V slot s only after that chunk's P V; S buffer s only after the
     softmax read it; P tile s only after its P V; O is rescaled only after the
     previous P V has completed, and P V of chunk c runs on P and V of chunk c;
-    Q is reloaded only after the previous block's S MMAs, and a block's first
+    Q is rewritten only after the previous block's S MMAs, and a block's first
     P V overwrites an O buffer only after the block two earlier was read out.
 The MMAs' completions are modelled as separate asynchronous events (a commit
 arrives when the MMAs issued before it finish)."""
@@ -68,10 +69,10 @@ def simulate(blocks, rot_q, rot_k, seed):
         for kind, cnt in (("kFull", 1), ("kReady", 128), ("kEmpty", 1), ("vFull", 1), ("vEmpty", 1),
                           ("sFull", 1), ("sEmpty", 256), ("pFull", 256), ("pEmpty", 1)):
             B[kind, s] = Bar(cnt)
-    B["qFull"], B["qReady"], B["qEmpty"] = Bar(1), Bar(128), Bar(1)
+    B["qReady"], B["qEmpty"] = Bar(128), Bar(1)
     state = {  # what each buffer holds
         "K": [None, None], "V": [None, None], "S": [None, None], "P": [None, None],
-        "Q": None,                     # block whose Q tile is in place (and "rot")
+        "Q": None,                     # (block, "rot" or "raw") of the Q tile in place
         "O": [(-1, -1), (-1, -1)],     # O buffer k & 1: (block, last chunk added)
         "Oread": [-1, -1],             # O buffer: last block whose result was read out
     }
@@ -83,10 +84,6 @@ def simulate(blocks, rot_q, rot_k, seed):
     def producer():
         g = 0
         for k, n in enumerate(blocks):
-            if k >= 1:
-                yield ("wait", B["qEmpty"], (k - 1) & 1, k - 1)
-            B["qFull"].expect_tx(2)
-            inflight.append(("tma", ("Q", 0, k)))
             for c in range(n):
                 s, use = g & 1, g >> 1
                 if g >= 2:
@@ -111,7 +108,7 @@ def simulate(blocks, rot_q, rot_k, seed):
             inflight.append(("pv", (s, g, k, c)))
         g = 0
         for k, n in enumerate(blocks):
-            yield ("wait", B["qReady" if rot_q else "qFull"], k & 1, k)
+            yield ("wait", B["qReady"], k & 1, k)
             for c in range(n):
                 s, use = g & 1, g >> 1
                 yield ("wait", B["kReady" if rot_k else "kFull", s], use & 1, use)
@@ -125,16 +122,17 @@ def simulate(blocks, rot_q, rot_k, seed):
                 g += 1
             yield from issue_pv(k, n - 1, g - 1)
 
-    def rotator(i):
+    def q_warp(i):
         g = 0
         for k, n in enumerate(blocks):
-            if rot_q:
-                yield ("wait", B["qFull"], k & 1, k)
-                if i == 0:
-                    assert state["Q"] == (k, "raw")
-                    state["Q"] = (k, "rot")
-                for _ in range(32):
-                    B["qReady"].arrive()
+            yield None                 # Q of block k read (and rotated) into registers
+            if k >= 1:                 # the previous block's S MMAs are done with Q
+                yield ("wait", B["qEmpty"], (k - 1) & 1, k - 1)
+            if i == 0:
+                assert state["Q"] is None or state["Q"][0] == k - 1
+                state["Q"] = (k, "rot" if rot_q else "raw")
+            for _ in range(32):
+                B["qReady"].arrive()
             for c in range(n):
                 if rot_k:
                     s, use = g & 1, g >> 1
@@ -155,20 +153,22 @@ def simulate(blocks, rot_q, rot_k, seed):
                 s, use = g & 1, g >> 1
                 yield ("wait", B["sFull", s], use & 1, use)
                 assert state["S"][s] == g, "the softmax reads S of its chunk"
+                for _ in range(256 // SOFT):   # S held in registers: released at once
+                    B["sEmpty", s].arrive()
                 yield None
                 rescale = m_valid and rng.random() < 0.3
                 m_valid = True
-                if rescale:
-                    prev = g - 1
-                    yield ("wait", B["pEmpty", prev & 1], (prev >> 1) & 1, prev >> 1)
-                    assert state["O"][k & 1] == (k, c - 1), "O rescaled after the previous P V"
                 if g >= 2:
                     yield ("wait", B["pEmpty", s], (use - 1) & 1, use - 1)
                 assert state["P"][s] in (None, g - 2, g), "P tile free"
                 if i == 0:
                     state["P"][s] = g
+                yield None
+                if rescale:                    # after the weights are written
+                    prev = g - 1
+                    yield ("wait", B["pEmpty", prev & 1], (prev >> 1) & 1, prev >> 1)
+                    assert state["O"][k & 1] == (k, c - 1), "O rescaled after the previous P V"
                 for _ in range(256 // SOFT):
-                    B["sEmpty", s].arrive()
                     B["pFull", s].arrive()
                 g += 1
                 yield None
@@ -178,9 +178,7 @@ def simulate(blocks, rot_q, rot_k, seed):
             if i == 0:
                 state["Oread"][k & 1] = k
 
-    roles = [producer(), mma()] + [softmax(i) for i in range(SOFT)]
-    if rot_q or rot_k:
-        roles += [rotator(i) for i in range(4)]
+    roles = [producer(), mma()] + [softmax(i) for i in range(SOFT)] + [q_warp(i) for i in range(4)]
     waiting = [None] * len(roles)
     done = [False] * len(roles)
     steps = 0
@@ -200,12 +198,7 @@ def simulate(blocks, rot_q, rot_k, seed):
             kind, pl = inflight.pop(idx)
             if kind == "tma":
                 buf, s, x = pl
-                if buf == "Q":
-                    # the previous block's S MMAs are done with Q
-                    assert state["Q"] is None or state["Q"][0] == x - 1
-                    state["Q"] = (x, "raw")
-                    B["qFull"].complete_tx(2)
-                elif buf == "K":
+                if buf == "K":
                     assert state["K"][s] is None or state["K"][s][0] <= x - 2
                     state["K"][s] = (x, "raw")
                     B["kFull", s].complete_tx(2)
@@ -215,6 +208,7 @@ def simulate(blocks, rot_q, rot_k, seed):
                     B["vFull", s].complete_tx(2)
             elif kind == "s":
                 s, g, k, last = pl
+                assert state["Q"][0] == k, "Q kept until the block's S MMAs complete"
                 assert state["S"][s] is None or state["S"][s] == g - 2
                 state["S"][s] = g
                 B["kEmpty", s].arrive()      # the commits after S(g)

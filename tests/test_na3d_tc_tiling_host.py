@@ -112,11 +112,38 @@ def test_device_fastdiv_of_region_widths():
             assert fdiv(n, f) == n // d, (n, d)
 
 
+def test_q_warps_write_every_q_tile_chunk_once():
+    """The Q warps: thread rt (0 .. 127) writes 16-byte vector cv = rt % 16 of
+    query rows rt / 16 + 8 i (i = 0 .. 15), the query (t, h, w) = (i / 8,
+    i % 8, rt / 16) from the block's corner, which is the query the MMA row
+    and the softmax thread of that row stand for (row = 64 t + 8 h + w); each
+    of the tile's 2048 chunks is written once, inside the 32 KB Q tile, and
+    a warp reads two tokens' 256 contiguous bytes."""
+    seen = set()
+    for rt in range(128):
+        cv, qw = rt & 15, rt >> 4
+        for i in range(16):
+            r = qw + 8 * i
+            t, h, w = i >> 3, i & 7, qw
+            assert (r >> 6, (r >> 3) & 7, r & 7) == (t, h, w)
+            a = sw128(r, cv, Q_CB)
+            assert 0 <= a and a + 16 <= 2 * Q_CB and a % 16 == 0
+            seen.add(a)
+    assert len(seen) == 2048
+    for warp in range(4):
+        for i in range(16):
+            toks = {}
+            for lane in range(32):
+                rt = 32 * warp + lane
+                toks.setdefault(rt >> 4, set()).add(rt & 15)
+            assert len(toks) == 2 and all(v == set(range(16)) for v in toks.values())
+
+
 @pytest.mark.parametrize("cfg", sorted(CONFIGS))
 def test_shared_memory_layout(cfg):
     c = CONFIGS[cfg]
     assert all(o % 1024 == 0 for o in (c.OFF_K, c.OFF_V, c.OFF_P, c.OFF_RED, c.KV_CB, c.KV_SLOT))
-    total = c.OFF_RED + 12 * TC_M * 4 + 176 + 1024
+    total = c.OFF_RED + 3 * c.PARTS * TC_M * 4 + 176 + 1024   # maxima [2][parts], sums [parts]
     assert c.CTAS * (total + 1024) <= 228 * 1024          # 1 KB reserved per CTA
     assert c.TC_N <= c.COL_S and c.COL_S + c.TC_N <= c.COL_O and c.COL_O + 128 <= c.TMEM_COLS
 
