@@ -814,8 +814,15 @@ def run_na3d(args):
     def once():
         r.rope3d_na3d_rotate_once(q, k, v, tabs, c["kernel"], out, k_rot=kr, stream=stream)
 
-    def fused():
+    def fused():   # K rotated once into the library's pooled scratch
         r.rope3d_na3d(q, k, v, tabs, c["kernel"], out, stream=stream)
+
+    def fused_per_cta():   # Q and every K tile rotated inside each CTA
+        r.rope3d_testing_na3d_per_cta(True)
+        try:
+            r.rope3d_na3d(q, k, v, tabs, c["kernel"], out, stream=stream)
+        finally:
+            r.rope3d_testing_na3d_per_cta(False)
 
     def unfused():
         r.rope3d_apply_pair(q, k, tabs, qr, kr, stream=stream)
@@ -844,6 +851,7 @@ def run_na3d(args):
     ms_once = timed(once, args.steps)
     t1 = time.time()
     ms_fused = timed(fused, args.steps)
+    ms_per_cta = timed(fused_per_cta, args.steps)
     ms_unfused = timed(unfused, args.steps)
     ms_attention = timed(attention_only, args.steps)
     time.sleep(0.25)
@@ -873,7 +881,7 @@ def run_na3d(args):
         "attention_kernel": {1: "tcgen05 (tensor memory)", 2: "warp-level mma.sync"}.get(
             r.rope3d_testing_na3d_last_kernel(), "?"),
         "unfused_ms": ms_unfused, "fusion_saving_ms": ms_unfused - ms_once,
-        "fused_per_cta_ms": ms_fused,
+        "fused_ms": ms_fused, "fused_per_cta_ms": ms_per_cta,
         "attention_only_ms": ms_attention,
         "attention_only_tflops": flops / (ms_attention / 1e3) / 1e12,
         "clocks": clocks.summary(t0, t1), "gpu_launches": 2 * args.steps,

@@ -307,13 +307,14 @@ int rope3d_neox_last_kernel(void);
  *   tables, split as rope3d_apply_pair (used when apply_rope != 0; every
  *                 chunk a multiple of 8; tables <= 48 KB)
  *   kernel_size   (k_t, k_h, k_w), odd, each no larger than its grid extent
- *   apply_rope    1: rotate Q and K first (fused); 0: Q and K are used as
- *                 given (the unfused path's second kernel). Measured, the
- *                 unfused pair (rope3d_apply_pair, then apply_rope = 0) is
- *                 faster than apply_rope = 1: every key is rotated by each of
- *                 the ~10 CTAs whose key region holds it, which costs more
- *                 than the round trip of Q_out and K_out. The fast fused form
- *                 is rope3d_na3d_rotate_once below.
+ *   apply_rope    1: rotate Q and K first (fused), as
+ *                 rope3d_na3d_rotate_once does, with K rotated into scratch
+ *                 of K's size that the library takes from a per-device
+ *                 memory pool in stream order (cudaMallocFromPoolAsync before
+ *                 the two launches, cudaFreeAsync after them; the pool keeps
+ *                 the memory for later calls until rope3d_cache_clear trims
+ *                 it); 0: Q and K are used as given (the unfused path's
+ *                 second kernel).
  *   stream        cudaStream_t; asynchronous
  * Limits: head_dim 128; T, H, W < 1024. The bit-exact gate does not run here.
  * Errors: NULL, SHAPE, ALIGN (16 bytes), ALIAS, TABLES, DEVICE, CUDA.
@@ -377,6 +378,11 @@ int rope3d_na3d_preflight(const void *q, const void *k, const void *v, const voi
  *     kernel always. Errors: ARG.
  *   rope3d_testing_na3d_last_kernel(): the kernel of this thread's last
  *     attention launch: 1 tensor-core, 2 warp-MMA, 0 none yet.
+ *   rope3d_testing_na3d_per_cta(on): 1 = rope3d_na3d with apply_rope = 1
+ *     runs the kernel form that rotates Q and every K tile inside each CTA
+ *     (no scratch; every key is rotated by each of the CTAs whose key region
+ *     holds it, which measured slower than rotating K once); 0 = the default.
+ *     Errors: ARG.
  *   rope3d_testing_na3d_wait_timeouts(count, reset): how many bounded waits
  *     of the tensor-core kernel on its MMA completions ran out (0 unless
  *     something is badly wrong; such a launch's output is not to be used);
@@ -384,6 +390,7 @@ int rope3d_na3d_preflight(const void *q, const void *k, const void *v, const voi
  */
 int rope3d_testing_na3d_kernel(int32_t which);
 int rope3d_testing_na3d_last_kernel(void);
+int rope3d_testing_na3d_per_cta(int32_t on);
 int rope3d_testing_na3d_wait_timeouts(int64_t *count, int32_t reset);
 
 /*
@@ -521,7 +528,8 @@ int rope3d_tables_read(const rope3d_tables *tables, int32_t axis, int32_t from_d
 /* Counters since the last rope3d_cache_clear(); any pointer may be NULL. */
 int rope3d_cache_stats(int64_t *entries, int64_t *hits, int64_t *misses,
                        int64_t *evictions);
-/* Unlink every entry (held handles stay valid) and zero the counters. */
+/* Unlink every entry (held handles stay valid), zero the counters, and return
+ * the memory that rope3d_na3d's scratch pools keep to the device. */
 int rope3d_cache_clear(void);
 /*
  * Free the released table buffers whose last launches have completed;

@@ -32,7 +32,7 @@ __all__ = [
     "rope3d_apply_neox", "rope3d_neox_check", "rope3d_neox_cache_host", "rope3d_neox_last_kernel",
     "rope3d_na3d", "rope3d_na3d_rotate_once", "rope3d_na3d_preflight", "rope3d_debug_bounds",
     "rope3d_testing_debug_shrink_tables", "rope3d_dit_freqs_host", "rope3d_cache_retired",
-    "rope3d_testing_na3d_kernel", "rope3d_testing_na3d_last_kernel",
+    "rope3d_testing_na3d_kernel", "rope3d_testing_na3d_last_kernel", "rope3d_testing_na3d_per_cta",
     "rope3d_testing_na3d_wait_timeouts",
 ]
 
@@ -81,6 +81,7 @@ def _declare(lib):
         "rope3d_cache_retired": ([vp], c.c_int),
         "rope3d_testing_na3d_kernel": ([i32], c.c_int),
         "rope3d_testing_na3d_last_kernel": ([], c.c_int),
+        "rope3d_testing_na3d_per_cta": ([c.c_int32], c.c_int),
         "rope3d_testing_na3d_wait_timeouts": ([vp, i32], c.c_int),
         "rope3d_gate_set_mode": ([i32], c.c_int),
         "rope3d_gate_get_mode": ([], c.c_int),
@@ -499,7 +500,8 @@ def rope3d_neox_last_kernel() -> int:
 def rope3d_na3d(q, k, v, tables: Tables, kernel_size, out=None, apply_rope: bool = True,
                 stream=None):
     """3D neighbourhood attention over [B, T*H*W, heads, 128] (or 6-D) bf16
-    device tensors, with Q and K rotated inside the kernel when apply_rope."""
+    device tensors, with Q and K rotated first when apply_rope (K once, into
+    scratch the library takes from its pool; Q inside the attention)."""
     if out is None:
         import torch
 
@@ -625,6 +627,12 @@ def rope3d_testing_na3d_kernel(which: int):
 def rope3d_testing_na3d_last_kernel() -> int:
     """1 tensor-core, 2 warp-MMA: the kernel of this thread's last attention launch."""
     return int(load_library().rope3d_testing_na3d_last_kernel())
+
+
+def rope3d_testing_na3d_per_cta(on: bool):
+    """True: rope3d_na3d with the RoPE runs the kernel form that rotates Q and
+    every K tile inside each CTA (no scratch); False: the default."""
+    _check(load_library().rope3d_testing_na3d_per_cta(1 if on else 0), "rope3d_testing_na3d_per_cta")
 
 
 def rope3d_testing_na3d_wait_timeouts(reset: bool = True) -> int:

@@ -487,6 +487,7 @@ extern "C" int rope3d_cache_clear(void) {
         g_cache.hits = g_cache.misses = g_cache.evictions = 0;
     }
     drain_retired();
+    rope3d::na3d_scratch_trim();
     return ROPE3D_OK;
 }
 

@@ -128,5 +128,8 @@ int tables_layout(const rope3d_tables *t, const float2 **dev, uint32_t *len, uin
 // Record that work just enqueued on `stream` reads t's tables, so that t's
 // memory outlives that work when its last reference is released. Returns a
 // ROPE3D_* status.
+// Return the memory the attention's scratch pools keep (rope3d_na3d's K
+// scratch) to the device, except what is still in use.
+void na3d_scratch_trim();
 int tables_note_use(const rope3d_tables *t, cudaStream_t stream);
 }  // namespace rope3d

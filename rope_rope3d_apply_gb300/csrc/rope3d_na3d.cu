@@ -43,6 +43,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <type_traits>
 
 #include "../../include/rope3d.h"
@@ -1739,50 +1740,14 @@ bool na3d_attributes() {
 
 }  // namespace
 
-extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *out,
-                           const rope3d_tables *tables, int64_t B, int64_t T, int64_t H,
-                           int64_t W, int64_t heads, int64_t head_dim, const int32_t split[3],
-                           const int32_t kernel_size[3], int32_t apply_rope, void *stream) {
-    NAParams p;
-    const int rc = na3d_setup(q, k, v, out, nullptr, false, tables, B, T, H, W, heads, head_dim,
-                              split, kernel_size, apply_rope != 0, true, p);
-    if (rc != ROPE3D_OK) return rc;
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    g_na3d_last_kernel = na3d_use_tc(p) ? 1 : 2;
-    if (na3d_use_tc(p)) {
-        const TcShape shp = na3d_tc_shape(p);
-        CUtensorMap mk, mv;
-        if (!na3d_tc_map(&mk, p.k, p, shp.rwb, shp.chb, 1) || !na3d_tc_map(&mv, p.v, p, shp.rwb, shp.chb, 1))
-            return ROPE3D_ERR_CUDA;
-        if (apply_rope) {
-            if (!na3d_tc_attribute<kRotQK>()) return ROPE3D_ERR_CUDA;
-            rope3d_na3d_tc_kernel<kRotQK><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv);
-        } else {
-            if (!na3d_tc_attribute<kRotNone>()) return ROPE3D_ERR_CUDA;
-            rope3d_na3d_tc_kernel<kRotNone><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv);
-        }
-    } else {
-        if (!na3d_attributes()) return ROPE3D_ERR_CUDA;
-        const size_t smem = kFixedSmem + (apply_rope ? size_t(p.tab_len) * sizeof(float2) : 0);
-        if (apply_rope)
-            rope3d_na3d_kernel<kRotQK><<<na3d_blocks(p), kThreads, smem, st>>>(p);
-        else
-            rope3d_na3d_kernel<kRotNone><<<na3d_blocks(p), kThreads, smem, st>>>(p);
-    }
-    if (cudaGetLastError() != cudaSuccess) return ROPE3D_ERR_CUDA;
-    if (apply_rope && rope3d::tables_note_use(tables, st) != ROPE3D_OK) return ROPE3D_ERR_CUDA;
-    return ROPE3D_OK;
-}
+namespace {
 
-extern "C" int rope3d_na3d_rotate_once(const void *q, const void *k, const void *v, void *k_rot,
-                                       void *out, const rope3d_tables *tables, int64_t B,
-                                       int64_t T, int64_t H, int64_t W, int64_t heads,
-                                       int64_t head_dim, const int32_t split[3],
-                                       const int32_t kernel_size[3], void *stream) {
-    NAParams p;
-    const int rc = na3d_setup(q, k, v, out, k_rot, true, tables, B, T, H, W, heads, head_dim,
-                              split, kernel_size, true, true, p);
-    if (rc != ROPE3D_OK) return rc;
+// The rotate-once form on checked arguments (na3d_setup with the tables):
+// K rotated into k_rot by the K pass, then the attention on k_rot rotating
+// its Q tiles.
+int na3d_launch_rotate_once(NAParams &p, const void *k, void *k_rot, const rope3d_tables *tables,
+                            int64_t B, int64_t T, int64_t H, int64_t W, int64_t heads,
+                            cudaStream_t st) {
     if (!na3d_attributes()) return ROPE3D_ERR_CUDA;
     static const int sms = [] {
         int dev = 0, n = 0;
@@ -1792,7 +1757,6 @@ extern "C" int rope3d_na3d_rotate_once(const void *q, const void *k, const void 
         return n;
     }();
     if (sms <= 0) return ROPE3D_ERR_CUDA;
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     // 1. K -> k_rot, in launches of whole tokens below 2^30 vectors each
     RKParams rp{};
@@ -1854,6 +1818,122 @@ extern "C" int rope3d_na3d_rotate_once(const void *q, const void *k, const void 
     return ROPE3D_OK;
 }
 
+// The pools rope3d_na3d takes its K scratch from: one per device, made on
+// first use, keeping freed memory for later calls (no release threshold)
+// until rope3d_cache_clear trims them.
+std::mutex g_pool_mutex;
+constexpr int kMaxDevices = 64;
+cudaMemPool_t g_pools[kMaxDevices] = {};
+
+cudaMemPool_t scratch_pool(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_pool_mutex);
+    if (!g_pools[dev]) {
+        cudaMemPoolProps props{};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        uint64_t keep = ~uint64_t(0);
+        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+            cudaGetLastError();
+            cudaMemPoolDestroy(pool);
+            return nullptr;
+        }
+        g_pools[dev] = pool;
+    }
+    return g_pools[dev];
+}
+
+// 1: rope3d_na3d with the RoPE runs the kernel that rotates Q and every K
+// tile per CTA (rope3d_testing_na3d_per_cta).
+std::atomic<int> g_na3d_per_cta{0};
+
+}  // namespace
+
+namespace rope3d {
+
+void na3d_scratch_trim() {
+    std::lock_guard<std::mutex> lock(g_pool_mutex);
+    for (cudaMemPool_t pool : g_pools)
+        if (pool && cudaMemPoolTrimTo(pool, 0) != cudaSuccess) cudaGetLastError();
+}
+
+}  // namespace rope3d
+
+extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *out,
+                           const rope3d_tables *tables, int64_t B, int64_t T, int64_t H,
+                           int64_t W, int64_t heads, int64_t head_dim, const int32_t split[3],
+                           const int32_t kernel_size[3], int32_t apply_rope, void *stream) {
+    NAParams p;
+    const int rc = na3d_setup(q, k, v, out, nullptr, false, tables, B, T, H, W, heads, head_dim,
+                              split, kernel_size, apply_rope != 0, true, p);
+    if (rc != ROPE3D_OK) return rc;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (apply_rope && g_na3d_per_cta.load(std::memory_order_relaxed) == 0) {
+        // K rotated once into scratch of K's size, taken from and returned to
+        // the pool in stream order around the two launches
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) {
+            cudaGetLastError();
+            return ROPE3D_ERR_CUDA;
+        }
+        const cudaMemPool_t pool = scratch_pool(dev);
+        void *k_rot = nullptr;
+        if (!pool || cudaMallocFromPoolAsync(&k_rot, p.total * 2, pool, st) != cudaSuccess) {
+            cudaGetLastError();
+            return ROPE3D_ERR_CUDA;
+        }
+        const int lrc = na3d_launch_rotate_once(p, k, k_rot, tables, B, T, H, W, heads, st);
+        if (cudaFreeAsync(k_rot, st) != cudaSuccess) {
+            cudaGetLastError();
+            return ROPE3D_ERR_CUDA;
+        }
+        return lrc;
+    }
+    g_na3d_last_kernel = na3d_use_tc(p) ? 1 : 2;
+    if (na3d_use_tc(p)) {
+        const TcShape shp = na3d_tc_shape(p);
+        CUtensorMap mk, mv;
+        if (!na3d_tc_map(&mk, p.k, p, shp.rwb, shp.chb, 1) || !na3d_tc_map(&mv, p.v, p, shp.rwb, shp.chb, 1))
+            return ROPE3D_ERR_CUDA;
+        if (apply_rope) {
+            if (!na3d_tc_attribute<kRotQK>()) return ROPE3D_ERR_CUDA;
+            rope3d_na3d_tc_kernel<kRotQK><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv);
+        } else {
+            if (!na3d_tc_attribute<kRotNone>()) return ROPE3D_ERR_CUDA;
+            rope3d_na3d_tc_kernel<kRotNone><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv);
+        }
+    } else {
+        if (!na3d_attributes()) return ROPE3D_ERR_CUDA;
+        const size_t smem = kFixedSmem + (apply_rope ? size_t(p.tab_len) * sizeof(float2) : 0);
+        if (apply_rope)
+            rope3d_na3d_kernel<kRotQK><<<na3d_blocks(p), kThreads, smem, st>>>(p);
+        else
+            rope3d_na3d_kernel<kRotNone><<<na3d_blocks(p), kThreads, smem, st>>>(p);
+    }
+    if (cudaGetLastError() != cudaSuccess) return ROPE3D_ERR_CUDA;
+    if (apply_rope && rope3d::tables_note_use(tables, st) != ROPE3D_OK) return ROPE3D_ERR_CUDA;
+    return ROPE3D_OK;
+}
+
+extern "C" int rope3d_na3d_rotate_once(const void *q, const void *k, const void *v, void *k_rot,
+                                       void *out, const rope3d_tables *tables, int64_t B,
+                                       int64_t T, int64_t H, int64_t W, int64_t heads,
+                                       int64_t head_dim, const int32_t split[3],
+                                       const int32_t kernel_size[3], void *stream) {
+    NAParams p;
+    const int rc = na3d_setup(q, k, v, out, k_rot, true, tables, B, T, H, W, heads, head_dim,
+                              split, kernel_size, true, true, p);
+    if (rc != ROPE3D_OK) return rc;
+    return na3d_launch_rotate_once(p, k, k_rot, tables, B, T, H, W, heads,
+                                   static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int rope3d_testing_na3d_kernel(int32_t which) {
     if (which < 0 || which > 2) return ROPE3D_ERR_ARG;
     g_na3d_kernel.store(which);
@@ -1861,6 +1941,12 @@ extern "C" int rope3d_testing_na3d_kernel(int32_t which) {
 }
 
 extern "C" int rope3d_testing_na3d_last_kernel(void) { return g_na3d_last_kernel; }
+
+extern "C" int rope3d_testing_na3d_per_cta(int32_t on) {
+    if (on != 0 && on != 1) return ROPE3D_ERR_ARG;
+    g_na3d_per_cta.store(on);
+    return ROPE3D_OK;
+}
 
 extern "C" int rope3d_testing_na3d_wait_timeouts(int64_t *count, int32_t reset) {
     if (!count) return ROPE3D_ERR_NULL;

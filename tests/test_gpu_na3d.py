@@ -38,6 +38,7 @@ def _kernel_choice_and_no_timeouts():
     r.rope3d_testing_na3d_wait_timeouts(reset=True)
     yield
     r.rope3d_testing_na3d_kernel(0)
+    r.rope3d_testing_na3d_per_cta(False)
     assert r.rope3d_testing_na3d_wait_timeouts(reset=True) == 0
 
 
@@ -63,13 +64,16 @@ CASES = [
 
 
 def attend(path, q, k, v, tabs, kernel):
-    """The attention with the RoPE applied, by one of the two fused forms."""
-    if path == "qk":
+    """The attention with the RoPE applied: rope3d_na3d (K rotated once into
+    the library's scratch), the same with every K tile rotated per CTA, or
+    rope3d_na3d_rotate_once (K rotated into the caller's buffer)."""
+    if path in ("qk", "per_cta"):
+        r.rope3d_testing_na3d_per_cta(path == "per_cta")
         return r.rope3d_na3d(q, k, v, tabs, kernel)
     return r.rope3d_na3d_rotate_once(q, k, v, tabs, kernel)[0]
 
 
-PATHS = ["qk", "once"]
+PATHS = ["qk", "per_cta", "once"]
 
 
 @pytest.mark.parametrize("which", KERNELS)
@@ -103,10 +107,12 @@ def test_na3d_matches_oracle(case, path, which):
     tabs.close()
 
 
+@pytest.mark.parametrize("per_cta", [False, True])
 @pytest.mark.parametrize("which", KERNELS)
-def test_fused_equals_unfused_bitwise(which):
-    """The fused prologue rotates exactly as rope3d_apply_pair does."""
+def test_fused_equals_unfused_bitwise(which, per_cta):
+    """The fused forms rotate exactly as rope3d_apply_pair does."""
     r.rope3d_testing_na3d_kernel(which)
+    r.rope3d_testing_na3d_per_cta(per_cta)
     B, T, H, W, heads, split, kernel = 1, 3, 10, 13, 2, (32, 48, 48), (3, 5, 5)
     shp = (B, T * H * W, heads, 128)
     n = int(np.prod(shp))
@@ -117,6 +123,36 @@ def test_fused_equals_unfused_bitwise(which):
     unfused = r.rope3d_na3d(qr, kr, v, tabs, kernel, apply_rope=False)
     torch.cuda.synchronize()
     assert torch.equal(fused.view(torch.int16), unfused.view(torch.int16))
+    tabs.close()
+
+
+def test_fused_scratch_is_stream_ordered():
+    """rope3d_na3d with the RoPE takes its K scratch from the library's pool
+    in stream order: calls queued on two streams, one held back by a spin
+    kernel, both give the unfused bits; rope3d_cache_clear then returns the
+    pool's memory."""
+    B, T, H, W, heads, split, kernel = 1, 4, 16, 24, 2, (32, 48, 48), (3, 7, 7)
+    shp = (B, T * H * W, heads, 128)
+    n = int(np.prod(shp))
+    q, k, v = (bf16(synthetic.normal(n, 1.0, 307, i, "bf16")).reshape(shp).to(DEV) for i in range(3))
+    tabs = r.rope3d_build_tables(T, H, W, split)
+    qr, kr = r.rope3d_apply_pair(q, k, tabs)
+    want = r.rope3d_na3d(qr, kr, v, tabs, kernel, apply_rope=False)
+    outs = [torch.empty_like(q) for _ in range(4)]
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(s1):
+        torch.cuda._sleep(int(0.2 * 2.0e9))
+    for i in range(4):
+        r.rope3d_na3d(q, k, v, tabs, kernel, outs[i], stream=s1 if i % 2 == 0 else s2)
+    s1.synchronize()
+    s2.synchronize()
+    for o in outs:
+        assert torch.equal(o.view(torch.int16), want.view(torch.int16))
+    r.rope3d_cache_clear()
+    again = r.rope3d_na3d(q, k, v, tabs, kernel)
+    torch.cuda.synchronize()
+    assert torch.equal(again.view(torch.int16), want.view(torch.int16))
     tabs.close()
 
 
@@ -254,9 +290,14 @@ def test_na3d_full_size_sampled(which):
     qr, kr = r.rope3d_apply_pair(q, k, tabs)
     unfused = r.rope3d_na3d(qr, kr, v, tabs, kernel, apply_rope=False)
     once, k_rot = r.rope3d_na3d_rotate_once(q, k, v, tabs, kernel)
+    r.rope3d_testing_na3d_per_cta(True)
+    per_cta = r.rope3d_na3d(q, k, v, tabs, kernel)
+    r.rope3d_testing_na3d_per_cta(False)
     torch.cuda.synchronize()
     assert r.rope3d_testing_na3d_last_kernel() == (1 if which == 0 else 2)
     assert torch.equal(fused.view(torch.int16), unfused.view(torch.int16))
+    assert torch.equal(per_cta.view(torch.int16), unfused.view(torch.int16))
+    del per_cta
     assert torch.equal(once.view(torch.int16), unfused.view(torch.int16))
     assert torch.equal(k_rot.view(torch.int16), kr.view(torch.int16))
     del once, k_rot
