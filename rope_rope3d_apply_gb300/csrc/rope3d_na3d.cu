@@ -1335,9 +1335,6 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 int f, r0, nr;
                 chunk_geom(g, c, f, r0, nr);
                 const uint32_t tS = tmem + s * kTcColS + lanes;
-                tc_wait(bar(sFull, s), use & 1u, dead);
-                tc_fence_after();
-
                 // this thread's half of the chunk's columns, [cb0, cb0 + nhalf),
                 // loaded at once as 32 + 16 + 8 columns; columns past nhalf stay
                 // inside this S buffer (cb0 + kTcHalf <= kTcN) and are masked.
@@ -1347,19 +1344,9 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 const int nhalf = ((nr * rwb + 15) & ~15) >> 1;   // a multiple of 8
                 const int cb0 = qq * nhalf;
                 const bool frame_ok = row_ok && unsigned(f - st_q) < unsigned(p.kt);
-                const bool warp_busy = __any_sync(0xffffffffu, frame_ok);
-                float x[kTcHalf];
-                if (warp_busy) {
-                    tc_ld32_async(tS + uint32_t(cb0), x);
-                    tc_ld16_async(tS + uint32_t(cb0 + 32), x + 32);
-                    tc_ld8_async(tS + uint32_t(cb0 + 48), x + 48);
-                    tc_ld_wait_hold<kTcHalf>(x);
-                }
-                // S is in registers: the MMA may write S(c + 2) into this buffer
-                tc_fence_before();
-                mbar_arrive(bar(sEmpty, s));
-                // window mask: bit k stands for column cb0 + k; each chunk row the
-                // half spans that lies in the window contributes its columns [clo, chi)
+                // window mask (geometry only, so made before S is waited for): bit
+                // k stands for column cb0 + k; each chunk row the half spans that
+                // lies in the window contributes its columns [clo, chi)
                 uint64_t win = 0;
                 if (frame_ok) {
                     const int rr0 = int(fdiv(uint32_t(cb0), rwd));
@@ -1371,24 +1358,42 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                     }
                 }
                 // groups of 8 keys that no query of the warp has in its window are
-                // skipped by the whole warp (their weights are written as zeros)
-                uint32_t live = 0;   // bit k8: some lane of the warp needs group k8
-                float cmax = -INFINITY;
-                if (warp_busy) {
+                // skipped by the whole warp (their weights are written as zeros);
+                // a warp with no live group does not read S at all
+                uint32_t need = 0;
 #pragma unroll
-                    for (int k8 = 0; k8 < kTcHalf / 8; ++k8) {
-                        const bool need = __any_sync(0xffffffffu, ((win >> (8 * k8)) & 0xFFull) != 0);
-                        live |= need ? 1u << k8 : 0u;
-                        if (need) {
+                for (int k8 = 0; k8 < kTcHalf / 8; ++k8)
+                    need |= ((win >> (8 * k8)) & 0xFFull) != 0 ? 1u << k8 : 0u;
+                const uint32_t live = __reduce_or_sync(0xffffffffu, need);
+                tc_wait(bar(sFull, s), use & 1u, dead);
+                tc_fence_after();
+                float x[kTcHalf];
+                if (live != 0) {
+                    tc_ld32_async(tS + uint32_t(cb0), x);
+                    tc_ld16_async(tS + uint32_t(cb0 + 32), x + 32);
+                    tc_ld8_async(tS + uint32_t(cb0 + 48), x + 48);
+                    tc_ld_wait_hold<kTcHalf>(x);
+                }
+                // S is in registers: the MMA may write S(c + 2) into this buffer
+                tc_fence_before();
+                mbar_arrive(bar(sEmpty, s));
+                // the masked maximum, as eight independent partial maxima
+                float pm[8];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int kk = 8 * k8 + e;
-                                x[kk] = (win >> kk) & 1u ? x[kk] : -INFINITY;   // outside: weight 0
-                                cmax = fmaxf(cmax, x[kk]);
-                            }
+                for (int e = 0; e < 8; ++e) pm[e] = -INFINITY;
+#pragma unroll
+                for (int k8 = 0; k8 < kTcHalf / 8; ++k8) {
+                    if ((live >> k8) & 1u) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int kk = 8 * k8 + e;
+                            x[kk] = (win >> kk) & 1u ? x[kk] : -INFINITY;   // outside: weight 0
+                            pm[e] = fmaxf(pm[e], x[kk]);
                         }
                     }
                 }
+                float cmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
                 cmax *= p.scale_log2;   // a positive scale: the maximum of the scaled scores
                 float *rm = red_max + (s * kTcParts) * kTcM;   // this chunk parity's [part][128]
                 rm[qq * kTcM + row] = cmax;
@@ -1413,7 +1418,9 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 if (gc >= 2) tc_wait(bar(pEmpty, s), (use - 1) & 1u, dead);
                 const float ms = m_ref == -INFINITY ? 0.f : m_ref;
                 unsigned char *pt = sm + kTcOffP + s * kTcPSlot;
-                float sum = 0.f;
+                // exponent arguments and the row sum in packed pairs (two sums)
+                const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-ms, -ms);
+                float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int k8 = 0; k8 < kTcHalf / 8; ++k8) {
                     if (8 * k8 < nhalf) {
@@ -1421,9 +1428,9 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                         if ((live >> k8) & 1u) {
 #pragma unroll
                             for (int e = 0; e < 8; e += 2) {
-                                const float a0 = ex2(__fmaf_rn(x[8 * k8 + e], p.scale_log2, -ms));
-                                const float a1 = ex2(__fmaf_rn(x[8 * k8 + e + 1], p.scale_log2, -ms));
-                                sum += a0 + a1;
+                                const float2 t = __ffma2_rn(make_float2(x[8 * k8 + e], x[8 * k8 + e + 1]), sc2, nm2);
+                                const float a0 = ex2(t.x), a1 = ex2(t.y);
+                                sum2[(e >> 1) & 1] = __fadd2_rn(sum2[(e >> 1) & 1], make_float2(a0, a1));
                                 w4[e >> 1] = pack_bf16(a0, a1);
                             }
                         }
@@ -1431,7 +1438,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                             make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
                 }
-                l_part += sum;
+                l_part += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
                 // O rescaled after the weights are out (the row's S values are
                 // no longer held), before P V of this chunk adds to it
                 if (__any_sync(0xffffffffu, rescale)) {
