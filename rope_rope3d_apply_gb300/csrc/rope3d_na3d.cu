@@ -265,6 +265,13 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// The largest of three floats (one three-input max instruction).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float y;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+    return y;
+}
+
 // S = Q K^T over NQ 16-key steps (keys q * 16 .. q * 16 + 15 of the warp's
 // run start at kaddr + q * 16 rows), software-pipelined: the B fragments of
 // k-step ks + 1 are loaded while the MMAs of k-step ks issue.
@@ -923,6 +930,14 @@ __device__ __forceinline__ void tma_load5(uint32_t dst, const CUtensorMap *map, 
 // wait of this thread, so a CTA whose MMAs never complete still ends.
 __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, bool &dead) {
     if (dead) return false;
+    {
+        uint32_t done;   // the phase has usually completed already
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+        if (done) return true;
+    }
     const long long t0 = clock64();
     while (true) {
         uint32_t done;
@@ -1117,21 +1132,24 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     const rope3d::FastDiv rwd = fastdiv_make_dev(uint32_t(rwb));
     const uint32_t box_bytes = uint32_t(2 * 128 * rwb * chb);   // both column blocks
 
-    // chunk c of block g: frame f, region rows [r0, r0 + nr)
-    auto chunk_geom = [&](const TcBlock &g, int c, int &f, int &r0, int &nr) {
-        f = g.rt0 + c / g.per_frame;
-        r0 = (c % g.per_frame) * chb;
-        nr = min(chb, g.RH - r0);
-    };
-    auto chunk_n = [&](const TcBlock &g, int c) {   // the MMA width: keys rounded up to 16
+    // The chunks of block g in order: frame f, region rows [r0, r0 + nr);
+    // r0 steps by chb through the block's RH region rows, then the next frame.
+    struct ChunkPos {
         int f, r0, nr;
-        chunk_geom(g, c, f, r0, nr);
-        return (nr * rwb + 15) & ~15;
     };
-    // TMA copies of chunk c's K or V (both column blocks) into ring slot s
-    auto tma_chunk = [&](const TcBlock &g, int c, int s, bool v) {
-        int f, r0, nr;
-        chunk_geom(g, c, f, r0, nr);
+    auto chunk_start = [&](const TcBlock &g) { return ChunkPos{g.rt0, 0, min(chb, g.RH)}; };
+    auto chunk_advance = [&](const TcBlock &g, ChunkPos &cp) {
+        cp.r0 += chb;
+        if (cp.r0 >= g.RH) {
+            cp.r0 = 0;
+            ++cp.f;
+        }
+        cp.nr = min(chb, g.RH - cp.r0);
+    };
+    auto chunk_n = [&](const ChunkPos &cp) { return (cp.nr * rwb + 15) & ~15; };   // MMA width
+    // TMA copies of a chunk's K or V (both column blocks) into ring slot s
+    auto tma_chunk = [&](const TcBlock &g, const ChunkPos &cp, int s, bool v) {
+        const int f = cp.f, r0 = cp.r0;
         const int frame = g.b * p.T + f;
         const uint32_t full = bar(v ? vFull : kFull, s), dst = (v ? sV : sK) + s * kTcKvSlot;
         const CUtensorMap *map = v ? &tmV : &tmK;
@@ -1187,13 +1205,14 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             int gc = 0;   // chunks of the CTA so far
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
                 const TcBlock g = tc_block(p, shp, blk);
-                for (int c = 0; c < g.n_chunks; ++c, ++gc) {
+                ChunkPos cp = chunk_start(g);
+                for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
                     const int s = gc & 1;
                     const uint32_t use = uint32_t(gc >> 1);
                     if (gc >= 2) tc_wait(bar(kEmpty, s), (use - 1) & 1u, dead);
-                    tma_chunk(g, c, s, false);
+                    tma_chunk(g, cp, s, false);
                     if (gc >= 2) tc_wait(bar(vEmpty, s), (use - 1) & 1u, dead);
-                    tma_chunk(g, c, s, true);
+                    tma_chunk(g, cp, s, true);
                 }
             }
         }
@@ -1202,14 +1221,14 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         // block's last P V at its end
         if (lane == 0) {
             int gc = 0;
-            auto issue_pv = [&](const TcBlock &g, int c, int gg, uint32_t o_col) {
+            auto issue_pv = [&](int c, int n, int gg, uint32_t o_col) {
                 const int s = gg & 1;
                 const uint32_t use = uint32_t(gg >> 1);
                 tc_wait(bar(pFull, s), use & 1u, dead);
                 tc_wait(bar(vFull, s), use & 1u, dead);
                 tc_fence_after();
                 const uint32_t id = tc_idesc(kTcM, kHD, 1);
-                const int ngrp = chunk_n(g, c) >> 4;
+                const int ngrp = n >> 4;
                 const uint32_t pt = sP + s * kTcPSlot, vt = sV + s * kTcKvSlot;
                 for (int j = 0; j < ngrp; ++j)
                     tc_mma(o_col, tc_sdesc(pt + (j >> 2) * kTcQCb + (j & 3) * 32, 16, 1024),
@@ -1221,13 +1240,16 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 const TcBlock g = tc_block(p, shp, blk);
                 const uint32_t o_col = tmem + kTcColO + uint32_t(k & 1) * 128;
                 tc_wait(qReady, uint32_t(k) & 1u, dead);
-                for (int c = 0; c < g.n_chunks; ++c, ++gc) {
+                ChunkPos cp = chunk_start(g);
+                int n_prev = 0;   // the previous chunk's MMA width
+                for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
                     const int s = gc & 1;
                     const uint32_t use = uint32_t(gc >> 1);
                     tc_wait(bar(kMode == kRotQK ? kReady : kFull, s), use & 1u, dead);
                     if (gc >= 2) tc_wait(bar(sEmpty, s), (use - 1) & 1u, dead);
                     tc_fence_after();
-                    const uint32_t id = tc_idesc(kTcM, uint32_t(chunk_n(g, c)), 0);
+                    const int n = chunk_n(cp);
+                    const uint32_t id = tc_idesc(kTcM, uint32_t(n), 0);
                     const uint32_t kt = sK + s * kTcKvSlot;
 #pragma unroll
                     for (int ks = 0; ks < kHD / 16; ++ks) {
@@ -1238,9 +1260,10 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                     tc_commit(bar(kEmpty, s));
                     tc_commit(bar(sFull, s));
                     if (c == g.n_chunks - 1) tc_commit(qEmpty);
-                    if (c >= 1) issue_pv(g, c - 1, gc - 1, o_col);
+                    if (c >= 1) issue_pv(c - 1, n_prev, gc - 1, o_col);
+                    n_prev = n;
                 }
-                issue_pv(g, g.n_chunks - 1, gc - 1, o_col);
+                issue_pv(g.n_chunks - 1, n_prev, gc - 1, o_col);
             }
         }
     } else if (warp < kTcSoftWarp0) {
@@ -1290,11 +1313,11 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 fence_async_smem();
                 mbar_arrive(qReady);
                 if constexpr (kMode == kRotQK) {
-                    for (int c = 0; c < g.n_chunks; ++c, ++gc) {
+                    ChunkPos cp = chunk_start(g);
+                    for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
                         const int s = gc & 1;
                         const uint32_t use = uint32_t(gc >> 1);
-                        int f, r0, nr;
-                        chunk_geom(g, c, f, r0, nr);
+                        const int f = cp.f, r0 = cp.r0, nr = cp.nr;
                         tc_wait(bar(kFull, s), use & 1u, dead);
                         const int nvec = nr * rwb * 16;
                         for (int u = rt; u < nvec; u += kTcRotThreads) {
@@ -1317,6 +1340,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         const int lg = warp & 3, qq = (warp - kTcSoftWarp0) >> 2;
         const int row = 32 * lg + lane;
         const uint32_t lanes = uint32_t(32 * lg) << 16;
+        const uint32_t p_row = uint32_t(row) * 128u;   // this row in a P column block
         int gc = 0;
         for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
             const TcBlock g = tc_block(p, shp, blk);
@@ -1329,11 +1353,11 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             const uint32_t tO = tmem + kTcColO + uint32_t(k & 1) * 128 + lanes;
             float m_ref = -INFINITY, l_part = 0.f;   // running reference and this part's sum
 
-            for (int c = 0; c < g.n_chunks; ++c, ++gc) {
+            ChunkPos cp = chunk_start(g);
+            for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
                 const int s = gc & 1;
                 const uint32_t use = uint32_t(gc >> 1);
-                int f, r0, nr;
-                chunk_geom(g, c, f, r0, nr);
+                const int f = cp.f, r0 = cp.r0, nr = cp.nr;
                 const uint32_t tS = tmem + s * kTcColS + lanes;
                 // this thread's half of the chunk's columns, [cb0, cb0 + nhalf),
                 // loaded at once as 32 + 16 + 8 columns; columns past nhalf stay
@@ -1377,10 +1401,11 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 // S is in registers: the MMA may write S(c + 2) into this buffer
                 tc_fence_before();
                 mbar_arrive(bar(sEmpty, s));
-                // the masked maximum, as eight independent partial maxima
-                float pm[8];
+                // the masked maximum, as four independent partial maxima taken two
+                // values at a time
+                float pm[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) pm[e] = -INFINITY;
+                for (int e = 0; e < 4; ++e) pm[e] = -INFINITY;
 #pragma unroll
                 for (int k8 = 0; k8 < kTcHalf / 8; ++k8) {
                     if ((live >> k8) & 1u) {
@@ -1388,12 +1413,14 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                         for (int e = 0; e < 8; ++e) {
                             const int kk = 8 * k8 + e;
                             x[kk] = (win >> kk) & 1u ? x[kk] : -INFINITY;   // outside: weight 0
-                            pm[e] = fmaxf(pm[e], x[kk]);
                         }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            pm[e] = fmax3(pm[e], x[8 * k8 + 2 * e], x[8 * k8 + 2 * e + 1]);
                     }
                 }
-                float cmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+                float cmax = fmax3(pm[0], pm[1], fmaxf(pm[2], pm[3]));
+
                 cmax *= p.scale_log2;   // a positive scale: the maximum of the scaled scores
                 float *rm = red_max + (s * kTcParts) * kTcM;   // this chunk parity's [part][128]
                 rm[qq * kTcM + row] = cmax;
@@ -1434,7 +1461,8 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                                 w4[e >> 1] = pack_bf16(a0, a1);
                             }
                         }
-                        *reinterpret_cast<uint4 *>(pt + sw128(uint32_t(row), uint32_t((cb0 >> 3) + k8), kTcQCb)) =
+                        const uint32_t cc = uint32_t((cb0 >> 3) + k8);   // 16-byte chunk of the P row
+                        *reinterpret_cast<uint4 *>(pt + p_row + (cc >> 3) * kTcQCb + (((cc ^ uint32_t(row)) & 7u) << 4)) =
                             make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
                 }
@@ -1471,7 +1499,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             for (int i = 1; i < kTcParts; ++i) l += red_sum[i * kTcM + row];
             const float inv = l > 0.f ? 1.f / l : 0.f;
             constexpr int kOCols = 128 / kTcParts;   // channels of this thread
-#pragma unroll
+#pragma unroll 2   // (fully unrolled, registers spill)
             for (int h2 = 0; h2 < kOCols / 16; ++h2) {
                 float o[16];
                 tc_ld16(tO + uint32_t(kOCols * qq + 16 * h2), o);
