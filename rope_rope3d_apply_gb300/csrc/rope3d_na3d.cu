@@ -1359,14 +1359,14 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 const uint32_t use = uint32_t(gc >> 1);
                 const int f = cp.f, r0 = cp.r0, nr = cp.nr;
                 const uint32_t tS = tmem + s * kTcColS + lanes;
-                // this thread's half of the chunk's columns, [cb0, cb0 + nhalf),
-                // loaded at once as 32 + 16 + 8 columns; columns past nhalf stay
-                // inside this S buffer (cb0 + kTcHalf <= kTcN) and are masked.
+                // this thread's half of the chunk's columns, [cb0, cb0 + 56), loaded
+                // at once as 32 + 16 + 8 columns. Columns past the chunk's keys are
+                // masked (their S values are stale or zero-row products) and their
+                // weights, written as zeros, lie past the P V MMA's width.
                 // A warp's rows share their frame (lanes 0-63 of tensor memory are
                 // the block's first frame, 64-127 its second), so a frame outside
                 // the warp's time window is skipped by the whole warp: zero weights.
-                const int nhalf = ((nr * rwb + 15) & ~15) >> 1;   // a multiple of 8
-                const int cb0 = qq * nhalf;
+                const int cb0 = qq * kTcHalf;
                 const bool frame_ok = row_ok && unsigned(f - st_q) < unsigned(p.kt);
                 // window mask (geometry only, so made before S is waited for): bit
                 // k stands for column cb0 + k; each chunk row the half spans that
@@ -1374,25 +1374,21 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 uint64_t win = 0;
                 if (frame_ok) {
                     const int rr0 = int(fdiv(uint32_t(cb0), rwd));
-                    for (int rr = rr0, js = rr0 * rwb - cb0; js < nhalf && rr < nr; ++rr, js += rwb) {
+                    for (int rr = rr0, js = rr0 * rwb - cb0; js < kTcHalf && rr < nr; ++rr, js += rwb) {
                         if (unsigned(r0 + rr - ah) < unsigned(p.kh)) {
-                            const int a = max(js + clo, 0), b2 = min(js + chi, nhalf);
+                            const int a = max(js + clo, 0), b2 = min(js + chi, kTcHalf);
                             if (a < b2) win |= (~0ull >> (64 - (b2 - a))) << a;
                         }
                     }
                 }
-                // groups of 8 keys that no query of the warp has in its window are
-                // skipped by the whole warp (their weights are written as zeros);
-                // a warp with no live group does not read S at all
-                uint32_t need = 0;
-#pragma unroll
-                for (int k8 = 0; k8 < kTcHalf / 8; ++k8)
-                    need |= ((win >> (8 * k8)) & 0xFFull) != 0 ? 1u << k8 : 0u;
-                const uint32_t live = __reduce_or_sync(0xffffffffu, need);
+                // A warp none of whose rows has a key of its window here reads no
+                // S. The others treat every group alike: straight-line code (the
+                // groups' work interleaves) beats skipping groups by branches.
+                const bool any = __any_sync(0xffffffffu, win != 0);
                 tc_wait(bar(sFull, s), use & 1u, dead);
                 tc_fence_after();
                 float x[kTcHalf];
-                if (live != 0) {
+                if (any) {
                     tc_ld32_async(tS + uint32_t(cb0), x);
                     tc_ld16_async(tS + uint32_t(cb0 + 32), x + 32);
                     tc_ld8_async(tS + uint32_t(cb0 + 48), x + 48);
@@ -1403,12 +1399,13 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 mbar_arrive(bar(sEmpty, s));
                 // the masked maximum, as four independent partial maxima taken two
                 // values at a time
-                float pm[4];
+                float cmax = -INFINITY;
+                if (any) {
+                    float pm[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) pm[e] = -INFINITY;
+                    for (int e = 0; e < 4; ++e) pm[e] = -INFINITY;
 #pragma unroll
-                for (int k8 = 0; k8 < kTcHalf / 8; ++k8) {
-                    if ((live >> k8) & 1u) {
+                    for (int k8 = 0; k8 < kTcHalf / 8; ++k8) {
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const int kk = 8 * k8 + e;
@@ -1418,9 +1415,8 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                         for (int e = 0; e < 4; ++e)
                             pm[e] = fmax3(pm[e], x[8 * k8 + 2 * e], x[8 * k8 + 2 * e + 1]);
                     }
+                    cmax = fmax3(pm[0], pm[1], fmaxf(pm[2], pm[3]));
                 }
-                float cmax = fmax3(pm[0], pm[1], fmaxf(pm[2], pm[3]));
-
                 cmax *= p.scale_log2;   // a positive scale: the maximum of the scaled scores
                 float *rm = red_max + (s * kTcParts) * kTcM;   // this chunk parity's [part][128]
                 rm[qq * kTcM + row] = cmax;
@@ -1450,21 +1446,19 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int k8 = 0; k8 < kTcHalf / 8; ++k8) {
-                    if (8 * k8 < nhalf) {
-                        uint32_t w4[4] = {0u, 0u, 0u, 0u};
-                        if ((live >> k8) & 1u) {
+                    uint32_t w4[4] = {0u, 0u, 0u, 0u};
+                    if (any) {
 #pragma unroll
-                            for (int e = 0; e < 8; e += 2) {
-                                const float2 t = __ffma2_rn(make_float2(x[8 * k8 + e], x[8 * k8 + e + 1]), sc2, nm2);
-                                const float a0 = ex2(t.x), a1 = ex2(t.y);
-                                sum2[(e >> 1) & 1] = __fadd2_rn(sum2[(e >> 1) & 1], make_float2(a0, a1));
-                                w4[e >> 1] = pack_bf16(a0, a1);
-                            }
+                        for (int e = 0; e < 8; e += 2) {
+                            const float2 t = __ffma2_rn(make_float2(x[8 * k8 + e], x[8 * k8 + e + 1]), sc2, nm2);
+                            const float a0 = ex2(t.x), a1 = ex2(t.y);
+                            sum2[(e >> 1) & 1] = __fadd2_rn(sum2[(e >> 1) & 1], make_float2(a0, a1));
+                            w4[e >> 1] = pack_bf16(a0, a1);
                         }
-                        const uint32_t cc = uint32_t((cb0 >> 3) + k8);   // 16-byte chunk of the P row
-                        *reinterpret_cast<uint4 *>(pt + p_row + (cc >> 3) * kTcQCb + (((cc ^ uint32_t(row)) & 7u) << 4)) =
-                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
+                    const uint32_t cc = uint32_t((cb0 >> 3) + k8);   // 16-byte chunk of the P row
+                    *reinterpret_cast<uint4 *>(pt + p_row + (cc >> 3) * kTcQCb + (((cc ^ uint32_t(row)) & 7u) << 4)) =
+                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
                 l_part += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
                 // O rescaled after the weights are out (the row's S values are

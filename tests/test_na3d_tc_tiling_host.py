@@ -21,6 +21,8 @@ the field layout they implement. The attention's arithmetic is left to the
 GPU tests, which compare the outputs with the float64 oracle."""
 from __future__ import annotations
 
+import random
+
 import pytest
 
 TC_M = 128                 # queries per CTA
@@ -224,18 +226,21 @@ def check_block(cfg, T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
             assert vs_base <= va and va + 1024 + 1024 + KV_CB <= vs_base + KV_SLOT
         # S buffer `slot` holds columns [slot * COL_S, + N), clear of the other and of O
         assert slot * COL_S + N <= (slot + 1) * COL_S <= COL_O
-        # the softmax: thread part qq of a row reads columns [qq * npart, + 56)
-        # of its S buffer (npart = N / 2 used, the rest masked) and writes the
-        # weights of its npart columns 8 keys (16 bytes) at a time
-        npart = N // PARTS
-        assert PARTS == 2 and npart % 8 == 0 and npart <= 56
+        # the softmax: thread part qq of a row reads columns [qq * 56, + 56) of
+        # its S buffer (columns past the chunk's keys masked) and writes the
+        # weights of all 56, 8 keys (16 bytes) at a time; the parts' P columns
+        # are disjoint and cover the P V MMA's K = N columns
+        npart = 56
+        assert PARTS == 2 and PARTS * npart == TC_N
+        written = []
         for qq in range(PARTS):
             cb0 = qq * npart
-            assert cb0 + 56 <= COL_S                  # inside this S buffer
+            assert cb0 + npart <= COL_S                # inside this S buffer
             for k8 in range(7):
-                if 8 * k8 < npart:
-                    key = cb0 + 8 * k8
-                    assert key % 8 == 0 and (key >> 3) // 8 < P_BLOCKS
+                key = cb0 + 8 * k8
+                assert key % 8 == 0 and (key >> 3) // 8 < P_BLOCKS
+                written += range(key, key + 8)
+        assert sorted(written) == list(range(TC_N)) and N <= TC_N
         # the window masks of every query row: a 64-bit mask per thread part,
         # built from the chunk rows its part spans, each in the window
         # contributing columns [clo, chi)
@@ -261,6 +266,7 @@ def check_block(cfg, T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
                         rr += 1
                         js += rwb
                 assert win < (1 << npart)
+                assert win >> max(nr * rwb - cb0, 0) == 0     # only the chunk's keys
                 for k in range(npart):
                     if win >> k & 1:
                         key = rows[cb0 + k]
