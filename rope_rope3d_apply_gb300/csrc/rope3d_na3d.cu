@@ -810,7 +810,9 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 //   K  [2 slots][2 column blocks][kTcN rows][128 B]     57,344
 //   V  [2 slots][2 column blocks][kTcN rows][128 B]     57,344
 //   P  [2 slots][2 column blocks of 64 keys][128][128 B] 65,536
-//   row maxima and sums of the row's two threads, 20 mbarriers, the TMEM address.
+//   row maxima and sums of the row's two threads, the softmax threads' window
+//   masks (4 KB per chunk row offset, up to 4 offsets), 20 mbarriers, the TMEM
+//   address.
 // Tensor memory (512 columns): S buffers at columns 0 and 128, O of even and
 // odd blocks at 256 and 384 (the next block's P V starts while the epilogue
 // reads the previous O).
@@ -835,7 +837,11 @@ constexpr uint32_t kTcOffK = kTcOffQ + 2 * kTcQCb;
 constexpr uint32_t kTcOffV = kTcOffK + 2 * kTcKvSlot;
 constexpr uint32_t kTcOffP = kTcOffV + 2 * kTcKvSlot;
 constexpr uint32_t kTcOffRed = kTcOffP + 2 * kTcPSlot;      // float max [2][2][128], sum [2][128]
-constexpr uint32_t kTcOffBar = kTcOffRed + 6 * kTcM * 4;    // 20 mbarriers + TMEM address
+// the softmax threads' window masks of a block's chunk row offsets (frames
+// share them): [offset][part][128] 64-bit words, each thread its own
+constexpr int kTcMaxPF = 4;                                 // offsets kept; more: made per chunk
+constexpr uint32_t kTcOffMask = kTcOffRed + 6 * kTcM * 4;
+constexpr uint32_t kTcOffBar = kTcOffMask + kTcMaxPF * kTcSoftThreads * 8;   // 20 mbarriers + TMEM address
 constexpr uint32_t kTcSmem = kTcOffBar + 176 + 1024;        // + room to align to 1024
 constexpr uint32_t kTcColS = 128;                           // S buffer b at column b * 128
 constexpr uint32_t kTcColO = 256;                           // O of block k at 256 + 128 (k & 1)
@@ -1135,13 +1141,15 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     // The chunks of block g in order: frame f, region rows [r0, r0 + nr);
     // r0 steps by chb through the block's RH region rows, then the next frame.
     struct ChunkPos {
-        int f, r0, nr;
+        int f, r0, nr, pf;   // pf: the chunk's index within its frame
     };
-    auto chunk_start = [&](const TcBlock &g) { return ChunkPos{g.rt0, 0, min(chb, g.RH)}; };
+    auto chunk_start = [&](const TcBlock &g) { return ChunkPos{g.rt0, 0, min(chb, g.RH), 0}; };
     auto chunk_advance = [&](const TcBlock &g, ChunkPos &cp) {
         cp.r0 += chb;
+        ++cp.pf;
         if (cp.r0 >= g.RH) {
             cp.r0 = 0;
+            cp.pf = 0;
             ++cp.f;
         }
         cp.nr = min(chb, g.RH - cp.r0);
@@ -1352,6 +1360,28 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             const int clo = max(aw, 0), chi = min(aw + p.kw, g.RW);   // window columns of a region row
             const uint32_t tO = tmem + kTcColO + uint32_t(k & 1) * 128 + lanes;
             float m_ref = -INFINITY, l_part = 0.f;   // running reference and this part's sum
+            const int cb0 = qq * kTcHalf;   // this thread's columns of a chunk: [cb0, cb0 + 56)
+            // Window mask of the chunk at region rows [r0, r0 + nr): bit k stands
+            // for column cb0 + k; each chunk row the part spans that lies in the
+            // window contributes its columns [clo, chi). It depends on the row
+            // offset only (every frame's chunks share it).
+            auto window_mask = [&](int r0, int nr) {
+                uint64_t m = 0;
+                const int rr0 = int(fdiv(uint32_t(cb0), rwd));
+                for (int rr = rr0, js = rr0 * rwb - cb0; js < kTcHalf && rr < nr; ++rr, js += rwb) {
+                    if (unsigned(r0 + rr - ah) < unsigned(p.kh)) {
+                        const int a = max(js + clo, 0), b2 = min(js + chi, kTcHalf);
+                        if (a < b2) m |= (~0ull >> (64 - (b2 - a))) << a;
+                    }
+                }
+                return m;
+            };
+            uint64_t *wmask = reinterpret_cast<uint64_t *>(sm + kTcOffMask) + (qq * kTcM + row);
+            const bool kept = g.per_frame <= kTcMaxPF;
+            if (kept) {
+                for (int pf = 0, r0 = 0; pf < g.per_frame; ++pf, r0 += chb)
+                    wmask[pf * kTcSoftThreads] = window_mask(r0, min(chb, g.RH - r0));
+            }
 
             ChunkPos cp = chunk_start(g);
             for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
@@ -1366,21 +1396,10 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 // A warp's rows share their frame (lanes 0-63 of tensor memory are
                 // the block's first frame, 64-127 its second), so a frame outside
                 // the warp's time window is skipped by the whole warp: zero weights.
-                const int cb0 = qq * kTcHalf;
                 const bool frame_ok = row_ok && unsigned(f - st_q) < unsigned(p.kt);
-                // window mask (geometry only, so made before S is waited for): bit
-                // k stands for column cb0 + k; each chunk row the half spans that
-                // lies in the window contributes its columns [clo, chi)
+                // the window mask (geometry only, so read before S is waited for)
                 uint64_t win = 0;
-                if (frame_ok) {
-                    const int rr0 = int(fdiv(uint32_t(cb0), rwd));
-                    for (int rr = rr0, js = rr0 * rwb - cb0; js < kTcHalf && rr < nr; ++rr, js += rwb) {
-                        if (unsigned(r0 + rr - ah) < unsigned(p.kh)) {
-                            const int a = max(js + clo, 0), b2 = min(js + chi, kTcHalf);
-                            if (a < b2) win |= (~0ull >> (64 - (b2 - a))) << a;
-                        }
-                    }
-                }
+                if (frame_ok) win = kept ? wmask[cp.pf * kTcSoftThreads] : window_mask(r0, nr);
                 // A warp none of whose rows has a key of its window here reads no
                 // S. The others treat every group alike: straight-line code (the
                 // groups' work interleaves) beats skipping groups by branches.
