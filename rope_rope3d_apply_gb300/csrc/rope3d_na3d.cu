@@ -785,16 +785,19 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 // tensor cores, the copies and the softmax overlap, also across blocks:
 //   warp 0 (one thread): TMA copies of each chunk's K and V (two boxes each,
 //     one per 64 channels, with the 128-byte swizzle) into two-slot rings;
-//   warp 1 (one thread): the MMAs. S(c) = Q K(c)^T into one of two S buffers
-//     in tensor memory (eight k16 steps), then O += P(c-1) V(c-1) (V read as
-//     an MN-major operand); so S(c + 1) and P V of chunk c - 1 run while the
-//     softmax of chunk c does;
-//   warps 2-5: each query block's Q tile, read from global memory into
+//   warp 1 (one thread): the P V MMAs, O += P(c) V(c) (V read as an MN-major
+//     operand), once the softmax has written P(c);
+//   warp 2 (one thread): the S MMAs, S(c) = Q K(c)^T into one of two S
+//     buffers in tensor memory (eight k16 steps), as soon as K(c) has landed
+//     and the softmax has taken S(c - 2) out of that buffer. Two issuing
+//     threads keep either kind of product from waiting behind the other's
+//     inputs; S(c + 1) and S(c + 2) run while the softmax of chunk c does;
+//   warps 3-6: each query block's Q tile, read from global memory into
 //     registers (and rotated there in the rotating modes) while the previous
 //     block still uses the Q buffer, then written into it in the swizzled
 //     layout; in the mode that rotates K per CTA, each K tile too, in place
 //     once it lands;
-//   warps 6-13: the softmax. Each query row's S is read back from tensor
+//   warps 7-14: the softmax. Each query row's S is read back from tensor
 //     memory by two threads (half of the chunk's columns each, in one batch of
 //     loads: warps w and w + 4 share the 32 lanes of tensor memory that warp w
 //     reaches), masked to the query's window (a 64-bit mask from the region
@@ -818,9 +821,9 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 // reads the previous O).
 // Tensor memory (all 512 columns: one CTA per SM): S in [0, 128) and
 // [128, 256), O in [256, 384).
-constexpr int kTcThreads = 448;              // 14 warps: TMA, MMA, 4 rotation, 8 softmax
-constexpr int kTcSoftWarp0 = 6;              // first softmax warp
-constexpr int kTcRotThreads = 128;           // warps 2-5
+constexpr int kTcThreads = 480;              // 15 warps: TMA, P V MMA, S MMA, 4 Q, 8 softmax
+constexpr int kTcSoftWarp0 = 7;              // first softmax warp
+constexpr int kTcRotThreads = 128;           // warps 3-6
 constexpr int kTcSoftThreads = 256;          // 2 threads per query row
 constexpr int kTcParts = kTcSoftThreads / 128;
 constexpr int kTcM = 128;                    // queries per CTA: 2 x 8 x 8
@@ -1107,8 +1110,10 @@ __device__ __forceinline__ TcBlock tc_block(const NAParams &p, const TcShape &sh
     return g;
 }
 
+// (bounded as for 512 threads: 128 registers a thread, so that the four warps
+// a sub-partition holds fit its quarter of the register file)
 template <int kMode>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(512, 1)
 rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
     extern __shared__ unsigned char tc_raw[];
@@ -1225,39 +1230,49 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             }
         }
     } else if (warp == 1) {
-        // ---- MMA issuer: per block, S(c) then P V of chunk c - 1, and the
-        // block's last P V at its end
+        // ---- P V issuer: O += P(c) V(c) for every chunk once the softmax has
+        // written its weights (its own thread, so that these MMAs never wait
+        // behind an S product that waits for its K tile, nor the reverse)
         if (lane == 0) {
             int gc = 0;
-            auto issue_pv = [&](int c, int n, int gg, uint32_t o_col) {
-                const int s = gg & 1;
-                const uint32_t use = uint32_t(gg >> 1);
-                tc_wait(bar(pFull, s), use & 1u, dead);
-                tc_wait(bar(vFull, s), use & 1u, dead);
-                tc_fence_after();
-                const uint32_t id = tc_idesc(kTcM, kHD, 1);
-                const int ngrp = n >> 4;
-                const uint32_t pt = sP + s * kTcPSlot, vt = sV + s * kTcKvSlot;
-                for (int j = 0; j < ngrp; ++j)
-                    tc_mma(o_col, tc_sdesc(pt + (j >> 2) * kTcQCb + (j & 3) * 32, 16, 1024),
-                           tc_sdesc(vt + j * 2048, kTcKvCb, 1024), id, (j > 0 || c > 0) ? 1u : 0u);
-                tc_commit(bar(vEmpty, s));
-                tc_commit(bar(pEmpty, s));
-            };
+            const uint32_t id = tc_idesc(kTcM, kHD, 1);
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
                 const TcBlock g = tc_block(p, shp, blk);
                 const uint32_t o_col = tmem + kTcColO + uint32_t(k & 1) * 128;
+                ChunkPos cp = chunk_start(g);
+                for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
+                    const int s = gc & 1;
+                    const uint32_t use = uint32_t(gc >> 1);
+                    tc_wait(bar(pFull, s), use & 1u, dead);
+                    tc_wait(bar(vFull, s), use & 1u, dead);
+                    tc_fence_after();
+                    const int ngrp = chunk_n(cp) >> 4;
+                    const uint32_t pt = sP + s * kTcPSlot, vt = sV + s * kTcKvSlot;
+                    for (int j = 0; j < ngrp; ++j)
+                        tc_mma(o_col, tc_sdesc(pt + (j >> 2) * kTcQCb + (j & 3) * 32, 16, 1024),
+                               tc_sdesc(vt + j * 2048, kTcKvCb, 1024), id, (j > 0 || c > 0) ? 1u : 0u);
+                    tc_commit(bar(vEmpty, s));
+                    tc_commit(bar(pEmpty, s));
+                }
+            }
+        }
+    } else if (warp == 2) {
+        // ---- S issuer: S(c) = Q K(c)^T into S buffer c & 1 as soon as K(c)
+        // has landed (rotated, in the per-CTA mode) and the softmax has taken
+        // S(c - 2) out of that buffer: up to two chunks ahead of the softmax
+        if (lane == 0) {
+            int gc = 0;
+            for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
+                const TcBlock g = tc_block(p, shp, blk);
                 tc_wait(qReady, uint32_t(k) & 1u, dead);
                 ChunkPos cp = chunk_start(g);
-                int n_prev = 0;   // the previous chunk's MMA width
                 for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
                     const int s = gc & 1;
                     const uint32_t use = uint32_t(gc >> 1);
                     tc_wait(bar(kMode == kRotQK ? kReady : kFull, s), use & 1u, dead);
                     if (gc >= 2) tc_wait(bar(sEmpty, s), (use - 1) & 1u, dead);
                     tc_fence_after();
-                    const int n = chunk_n(cp);
-                    const uint32_t id = tc_idesc(kTcM, uint32_t(n), 0);
+                    const uint32_t id = tc_idesc(kTcM, uint32_t(chunk_n(cp)), 0);
                     const uint32_t kt = sK + s * kTcKvSlot;
 #pragma unroll
                     for (int ks = 0; ks < kHD / 16; ++ks) {
@@ -1268,10 +1283,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                     tc_commit(bar(kEmpty, s));
                     tc_commit(bar(sFull, s));
                     if (c == g.n_chunks - 1) tc_commit(qEmpty);
-                    if (c >= 1) issue_pv(c - 1, n_prev, gc - 1, o_col);
-                    n_prev = n;
                 }
-                issue_pv(g.n_chunks - 1, n_prev, gc - 1, o_col);
             }
         }
     } else if (warp < kTcSoftWarp0) {
@@ -1284,7 +1296,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         // rt / 16 + 8 i, i = 0 .. 15: a row is (t, h, w) = (i / 8, i % 8, rt / 16)
         // from the block's corner, so a warp reads two tokens' 256 bytes.
         {
-            const int rt = tid - 64;   // 0 .. kTcRotThreads - 1
+            const int rt = tid - 96;   // 0 .. kTcRotThreads - 1
             const int cv = rt & 15, qw_off = rt >> 4;
             [[maybe_unused]] const TabSlot tsg = tab_slot_global(p.pT, p.pH, p.pW, p.offH, p.offW, cv);
             [[maybe_unused]] int gc = 0;

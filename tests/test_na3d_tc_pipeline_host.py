@@ -1,6 +1,6 @@
 """A CPU model of the tensor-core attention kernel's hand-over protocol
 (rope_rope3d_apply_gb300/csrc/rope3d_na3d.cu, rope3d_na3d_tc_kernel): the TMA
-thread, the MMA thread, the Q warps (which write each block's Q tile and, in
+thread, the two MMA threads (S products; P V products), the Q warps (which write each block's Q tile and, in
 the mode that rotates K per CTA, rotate the K tiles) and the softmax threads
 of one persistent CTA walking several query blocks, each a sequence of the kernel's
 mbarrier waits, arrivals and buffer accesses, run in many random
@@ -97,8 +97,8 @@ def simulate(blocks, rot_q, rot_k, seed):
                 g += 1
                 yield None
 
-    def mma():
-        def issue_pv(k, c, g):
+    def pv_issuer():
+        for g, (k, c) in enumerate(seq):
             s, use = g & 1, g >> 1
             yield ("wait", B["pFull", s], use & 1, use)
             yield ("wait", B["vFull", s], use & 1, use)
@@ -106,21 +106,18 @@ def simulate(blocks, rot_q, rot_k, seed):
             if c == 0:   # the block's first P V overwrites O buffer k & 1: read out two blocks ago
                 assert state["Oread"][k & 1] == k - 2 or (k < 2 and state["Oread"][k & 1] == -1)
             inflight.append(("pv", (s, g, k, c)))
-        g = 0
-        for k, n in enumerate(blocks):
-            yield ("wait", B["qReady"], k & 1, k)
-            for c in range(n):
-                s, use = g & 1, g >> 1
-                yield ("wait", B["kReady" if rot_k else "kFull", s], use & 1, use)
-                if g >= 2:
-                    yield ("wait", B["sEmpty", s], (use - 1) & 1, use - 1)
-                assert state["K"][s] == (g, "rot" if rot_k else "raw"), "S reads K of its chunk"
-                assert state["Q"] == (k, "rot" if rot_q else "raw"), "S reads Q of its block"
-                inflight.append(("s", (s, g, k, c == n - 1)))
-                if c >= 1:
-                    yield from issue_pv(k, c - 1, g - 1)
-                g += 1
-            yield from issue_pv(k, n - 1, g - 1)
+
+    def s_issuer():
+        for g, (k, c) in enumerate(seq):
+            s, use = g & 1, g >> 1
+            if c == 0:
+                yield ("wait", B["qReady"], k & 1, k)
+            yield ("wait", B["kReady" if rot_k else "kFull", s], use & 1, use)
+            if g >= 2:
+                yield ("wait", B["sEmpty", s], (use - 1) & 1, use - 1)
+            assert state["K"][s] == (g, "rot" if rot_k else "raw"), "S reads K of its chunk"
+            assert state["Q"] == (k, "rot" if rot_q else "raw"), "S reads Q of its block"
+            inflight.append(("s", (s, g, k, c == blocks[k] - 1)))
 
     def q_warp(i):
         g = 0
@@ -178,7 +175,8 @@ def simulate(blocks, rot_q, rot_k, seed):
             if i == 0:
                 state["Oread"][k & 1] = k
 
-    roles = [producer(), mma()] + [softmax(i) for i in range(SOFT)] + [q_warp(i) for i in range(4)]
+    roles = [producer(), s_issuer(), pv_issuer()] + [softmax(i) for i in range(SOFT)] + \
+        [q_warp(i) for i in range(4)]
     waiting = [None] * len(roles)
     done = [False] * len(roles)
     steps = 0
@@ -193,8 +191,9 @@ def simulate(blocks, rot_q, rot_k, seed):
             if "tma" in kinds and (rng.random() < 0.5 or all(kd == "tma" for kd in kinds)):
                 tma_idx = [j for j, kd in enumerate(kinds) if kd == "tma"]
                 idx = rng.choice(tma_idx)
-            else:   # MMAs complete in issue order
-                idx = next(j for j, kd in enumerate(kinds) if kd in ("s", "pv"))
+            else:   # each issuer's MMAs complete in its issue order
+                first = [next((j for j, kd in enumerate(kinds) if kd == want), None) for want in ("s", "pv")]
+                idx = rng.choice([j for j in first if j is not None])
             kind, pl = inflight.pop(idx)
             if kind == "tma":
                 buf, s, x = pl
