@@ -839,13 +839,15 @@ constexpr uint32_t kTcOffQ = 0;
 constexpr uint32_t kTcOffK = kTcOffQ + 2 * kTcQCb;
 constexpr uint32_t kTcOffV = kTcOffK + 2 * kTcKvSlot;
 constexpr uint32_t kTcOffP = kTcOffV + 2 * kTcKvSlot;
-constexpr uint32_t kTcOffRed = kTcOffP + 2 * kTcPSlot;      // float max [2][2][128], sum [2][128]
+// float row maxima [chunk parity][part][128], row sums [block parity][part][128]
+constexpr uint32_t kTcOffRed = kTcOffP + 2 * kTcPSlot;
 // the softmax threads' window masks of a block's chunk row offsets (frames
 // share them): [offset][part][128] 64-bit words, each thread its own
 constexpr int kTcMaxPF = 4;                                 // offsets kept; more: made per chunk
-constexpr uint32_t kTcOffMask = kTcOffRed + 6 * kTcM * 4;
-constexpr uint32_t kTcOffBar = kTcOffMask + kTcMaxPF * kTcSoftThreads * 8;   // 20 mbarriers + TMEM address
-constexpr uint32_t kTcSmem = kTcOffBar + 176 + 1024;        // + room to align to 1024
+constexpr uint32_t kTcOffMask = kTcOffRed + 4 * kTcParts * kTcM * 4;
+constexpr int kTcBars = 26;                                 // mbarriers, then the TMEM address
+constexpr uint32_t kTcOffBar = kTcOffMask + kTcMaxPF * kTcSoftThreads * 8;
+constexpr uint32_t kTcSmem = kTcOffBar + kTcBars * 8 + 16 + 1024;   // + room to align to 1024
 constexpr uint32_t kTcColS = 128;                           // S buffer b at column b * 128
 constexpr uint32_t kTcColO = 256;                           // O of block k at 256 + 128 (k & 1)
 constexpr uint32_t kTcTmemCols = 512;
@@ -1121,9 +1123,9 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     const uint32_t sQ = smem_addr(sm + kTcOffQ), sK = smem_addr(sm + kTcOffK);
     const uint32_t sV = smem_addr(sm + kTcOffV), sP = smem_addr(sm + kTcOffP);
     float *red_max = reinterpret_cast<float *>(sm + kTcOffRed);   // [chunk parity][part][128]
-    float *red_sum = red_max + 2 * kTcParts * kTcM;                 // [part][128]
+    float *red_sum = red_max + 2 * kTcParts * kTcM;                 // [block parity][part][128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kTcOffBar);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kTcOffBar + 20 * 8);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kTcOffBar + kTcBars * 8);
     // mbarriers, two of each kind (one per ring slot s = chunk & 1), counted
     // over the CTA's whole sequence of chunks:
     //   kFull  K landed (TMA)          kReady  K rotated (kRotQK; 128 arrivals)
@@ -1136,6 +1138,12 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     auto bar = [&](int kind, int slot) { return smem_addr(&bars[2 * kind + slot]); };
     enum { kFull, kReady, kEmpty, vFull, vEmpty, sFull, sEmpty, pFull, pEmpty };
     const uint32_t qReady = smem_addr(&bars[18]), qEmpty = smem_addr(&bars[19]);
+    // per O buffer b (block parity): oReady[b] the block's last P V done
+    // (commit), oFull[b] its row sums written (softmax threads), oEmpty[b] O
+    // read out (Q warps), so that block k + 2's first P V may overwrite it
+    auto oReady = [&](int b) { return smem_addr(&bars[20 + b]); };
+    auto oFull = [&](int b) { return smem_addr(&bars[22 + b]); };
+    auto oEmpty = [&](int b) { return smem_addr(&bars[24 + b]); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long tok = (long long)p.heads * kHD;   // elements per token
@@ -1181,6 +1189,11 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(qReady), "r"(kTcRotThreads) : "memory");
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(qEmpty) : "memory");
+        for (int b = 0; b < 2; ++b) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(oReady(b)) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(oFull(b)), "r"(kTcSoftThreads) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(oEmpty(b)), "r"(kTcRotThreads) : "memory");
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
@@ -1239,6 +1252,8 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
                 const TcBlock g = tc_block(p, shp, blk);
                 const uint32_t o_col = tmem + kTcColO + uint32_t(k & 1) * 128;
+                // O buffer k & 1 once the Q warps have read block k - 2's result
+                if (k >= 2) tc_wait(oEmpty(k & 1), uint32_t((k - 2) >> 1) & 1u, dead);
                 ChunkPos cp = chunk_start(g);
                 for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
                     const int s = gc & 1;
@@ -1253,6 +1268,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                                tc_sdesc(vt + j * 2048, kTcKvCb, 1024), id, (j > 0 || c > 0) ? 1u : 0u);
                     tc_commit(bar(vEmpty, s));
                     tc_commit(bar(pEmpty, s));
+                    if (c == g.n_chunks - 1) tc_commit(oReady(k & 1));
                 }
             }
         }
@@ -1295,11 +1311,49 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         // Thread rt holds 16-byte vector cv = rt % 16 of query rows
         // rt / 16 + 8 i, i = 0 .. 15: a row is (t, h, w) = (i / 8, i % 8, rt / 16)
         // from the block's corner, so a warp reads two tokens' 256 bytes.
+        // They also write each block's result: once its last P V is done and
+        // the softmax threads have left their row sums, each thread takes the
+        // row of tensor memory lane 32 (warp % 4) + lane (the lanes its warp
+        // reaches), normalises its 128 channels and stores them, while the
+        // softmax threads already work on the next block.
         {
             const int rt = tid - 96;   // 0 .. kTcRotThreads - 1
             const int cv = rt & 15, qw_off = rt >> 4;
             [[maybe_unused]] const TabSlot tsg = tab_slot_global(p.pT, p.pH, p.pW, p.offH, p.offW, cv);
             [[maybe_unused]] int gc = 0;
+            const int orow = 32 * (warp & 3) + lane;   // the O row this thread stores
+            auto store_o = [&](const TcBlock &g, int k) {
+                const int b = k & 1;
+                const uint32_t ph = uint32_t(k >> 1) & 1u;
+                tc_wait(oReady(b), ph, dead);
+                tc_wait(oFull(b), ph, dead);
+                tc_fence_after();
+                float l = 0.f;
+#pragma unroll
+                for (int i = 0; i < kTcParts; ++i) l += red_sum[(b * kTcParts + i) * kTcM + orow];
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const int qt = g.t0 + (orow >> 6), qh = g.h0 + ((orow >> 3) & 7), qw = g.w0 + (orow & 7);
+                const bool ok = qt < p.T && qh < p.H && qw < p.W;
+                const long long base = ((((long long)g.b * p.T + qt) * p.H + qh) * p.W + qw) * tok +
+                                       (long long)g.head * kHD;
+                const uint32_t tO = tmem + kTcColO + uint32_t(b) * 128 + (uint32_t(32 * (warp & 3)) << 16);
+#pragma unroll 1
+                for (int h2 = 0; h2 < kHD / 16; ++h2) {
+                    float o[16];
+                    tc_ld16(tO + uint32_t(16 * h2), o);
+                    uint32_t packed[8];
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2) packed[i / 2] = pack_bf16(o[i] * inv, o[i + 1] * inv);
+                    if (ok && bound_ok(base + 16 * h2, 16, p.total)) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.out + base + 16 * h2);
+                        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                    }
+                }
+                tc_fence_before();   // the reads of O, before the buffer is handed back
+                mbar_arrive(oEmpty(b));
+            };
+            TcBlock g_prev{};
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
                 const TcBlock g = tc_block(p, shp, blk);
                 const int w = g.w0 + qw_off;
@@ -1353,7 +1407,12 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                         mbar_arrive(bar(kReady, s));
                     }
                 }
+                if (k >= 1) store_o(g_prev, k - 1);   // the previous block's result
+                g_prev = g;
             }
+            const int nblk = shp.total > int(blockIdx.x)
+                                 ? (shp.total - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x) : 0;
+            if (nblk >= 1) store_o(g_prev, nblk - 1);
         }
     } else {
         // ---- softmax warps: this thread's query row and column part
@@ -1514,37 +1573,10 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 mbar_arrive(bar(pFull, s));
             }
 
-            // ---- normalise and store this thread's part (64 channels) of its row
-            tc_wait(bar(pEmpty, (gc - 1) & 1), uint32_t((gc - 1) >> 1) & 1u, dead);
-            tc_fence_after();
-            red_sum[qq * kTcM + row] = l_part;
-            asm volatile("bar.sync %0, %1;" ::"r"(1 + lg), "n"(32 * kTcParts) : "memory");
-            float l = red_sum[row];
-#pragma unroll
-            for (int i = 1; i < kTcParts; ++i) l += red_sum[i * kTcM + row];
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            constexpr int kOCols = 128 / kTcParts;   // channels of this thread
-#pragma unroll 2   // (fully unrolled, registers spill)
-            for (int h2 = 0; h2 < kOCols / 16; ++h2) {
-                float o[16];
-                tc_ld16(tO + uint32_t(kOCols * qq + 16 * h2), o);
-                uint32_t packed[8];
-#pragma unroll
-                for (int i = 0; i < 16; i += 2) packed[i / 2] = pack_bf16(o[i] * inv, o[i + 1] * inv);
-                if (row_ok) {
-                    const long long off = (((long long)g.b * p.T + qt) * p.H + qh) * p.W * tok +
-                                          (long long)qw * tok + (long long)g.head * kHD + kOCols * qq + 16 * h2;
-                    if (bound_ok(off, 16, p.total)) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.out + off);
-                        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                    }
-                }
-            }
-            // the reads of O are complete before this block's O buffer is
-            // reused two blocks on (its first P V needs this thread's P first)
-            tc_fence_before();
-            asm volatile("bar.sync %0, %1;" ::"r"(1 + lg), "n"(32 * kTcParts) : "memory");   // red_sum read by all
+            // ---- this part's row sum for the Q warps, which normalise and store
+            // the block's O while this thread goes on to the next block
+            red_sum[((k & 1) * kTcParts + qq) * kTcM + row] = l_part;
+            mbar_arrive(oFull(k & 1));
         }
     }
     tc_fence_before();

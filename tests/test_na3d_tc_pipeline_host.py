@@ -70,11 +70,14 @@ def simulate(blocks, rot_q, rot_k, seed):
                           ("sFull", 1), ("sEmpty", 256), ("pFull", 256), ("pEmpty", 1)):
             B[kind, s] = Bar(cnt)
     B["qReady"], B["qEmpty"] = Bar(128), Bar(1)
+    for b in (0, 1):   # per O buffer: last P V done, row sums written, O read out
+        B["oReady", b], B["oFull", b], B["oEmpty", b] = Bar(1), Bar(256), Bar(128)
     state = {  # what each buffer holds
         "K": [None, None], "V": [None, None], "S": [None, None], "P": [None, None],
         "Q": None,                     # (block, "rot" or "raw") of the Q tile in place
         "O": [(-1, -1), (-1, -1)],     # O buffer k & 1: (block, last chunk added)
         "Oread": [-1, -1],             # O buffer: last block whose result was read out
+        "sums": [-1, -1],              # row-sum buffer (block parity): block whose sums it holds
     }
     inflight = []                      # asynchronous events: (kind, payload)
     SOFT = 4                           # softmax threads modelled (arrivals scaled)
@@ -100,6 +103,8 @@ def simulate(blocks, rot_q, rot_k, seed):
     def pv_issuer():
         for g, (k, c) in enumerate(seq):
             s, use = g & 1, g >> 1
+            if c == 0 and k >= 2:   # O buffer k & 1 read out by the Q warps (block k - 2)
+                yield ("wait", B["oEmpty", k & 1], ((k - 2) >> 1) & 1, (k - 2) >> 1)
             yield ("wait", B["pFull", s], use & 1, use)
             yield ("wait", B["vFull", s], use & 1, use)
             assert state["P"][s] == g and state["V"][s] == g, "P V reads P and V of its chunk"
@@ -141,6 +146,21 @@ def simulate(blocks, rot_q, rot_k, seed):
                         B["kReady", s].arrive()
                 g += 1
                 yield None
+            if k >= 1:
+                yield from store_o(i, k - 1)
+        yield from store_o(i, len(blocks) - 1)
+
+    def store_o(i, k):
+        b, ph = k & 1, k >> 1
+        yield ("wait", B["oReady", b], ph & 1, ph)
+        yield ("wait", B["oFull", b], ph & 1, ph)
+        assert state["O"][b] == (k, blocks[k] - 1), "the block's O is complete"
+        assert state["sums"][b] == k, "its row sums are written"
+        yield None                        # O read, normalised, stored
+        if i == 0:
+            state["Oread"][b] = k
+        for _ in range(32):
+            B["oEmpty", b].arrive()
 
     def softmax(i):
         g = 0
@@ -169,11 +189,13 @@ def simulate(blocks, rot_q, rot_k, seed):
                     B["pFull", s].arrive()
                 g += 1
                 yield None
-            last = g - 1
-            yield ("wait", B["pEmpty", last & 1], (last >> 1) & 1, last >> 1)
-            assert state["O"][k & 1] == (k, n - 1), "the block's O is complete"
+            # this part's row sums for the Q warps; on to the next block at once
             if i == 0:
-                state["Oread"][k & 1] = k
+                assert state["sums"][k & 1] in (-1, k - 2), "row sums of block k - 2 were read"
+                assert state["Oread"][k & 1] == k - 2 or (k < 2 and state["Oread"][k & 1] == -1)
+                state["sums"][k & 1] = k
+            for _ in range(256 // SOFT):
+                B["oFull", k & 1].arrive()
 
     roles = [producer(), s_issuer(), pv_issuer()] + [softmax(i) for i in range(SOFT)] + \
         [q_warp(i) for i in range(4)]
@@ -219,8 +241,10 @@ def simulate(blocks, rot_q, rot_k, seed):
                 ob = state["O"][k & 1]
                 assert (c == 0) or ob == (k, c - 1), "P V in chunk order within the block"
                 state["O"][k & 1] = (k, c)
-                B["vEmpty", s].arrive()      # the two commits after P V(g)
+                B["vEmpty", s].arrive()      # the commits after P V(g)
                 B["pEmpty", s].arrive()
+                if c == blocks[k] - 1:
+                    B["oReady", k & 1].arrive()
             continue
         assert runnable, "deadlock"
         i = rng.choice(runnable)

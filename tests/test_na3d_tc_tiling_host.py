@@ -145,9 +145,10 @@ def test_q_warps_write_every_q_tile_chunk_once():
 def test_shared_memory_layout(cfg):
     c = CONFIGS[cfg]
     assert all(o % 1024 == 0 for o in (c.OFF_K, c.OFF_V, c.OFF_P, c.OFF_RED, c.KV_CB, c.KV_SLOT))
-    # maxima [2][parts] and sums [parts] of 128 floats, window masks
-    # [4 offsets][parts][128] of 8 bytes, 20 mbarriers + the TMEM address
-    total = c.OFF_RED + 3 * c.PARTS * TC_M * 4 + 4 * c.THREADS * 8 + 176 + 1024
+    # maxima [chunk parity][parts] and sums [block parity][parts] of 128
+    # floats, window masks [4 offsets][parts][128] of 8 bytes, 26 mbarriers +
+    # the TMEM address
+    total = c.OFF_RED + 4 * c.PARTS * TC_M * 4 + 4 * c.THREADS * 8 + 26 * 8 + 16 + 1024
     assert c.CTAS * (total + 1024) <= 228 * 1024          # 1 KB reserved per CTA
     assert c.TC_N <= c.COL_S and c.COL_S + c.TC_N <= c.COL_O and c.COL_O + 128 <= c.TMEM_COLS
 
