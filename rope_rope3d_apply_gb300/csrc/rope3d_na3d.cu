@@ -783,8 +783,9 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 // ...; its warps have one job each and hand work over through mbarriers
 // (counted over the CTA's whole sequence of chunks and blocks), so that the
 // tensor cores, the copies and the softmax overlap, also across blocks:
-//   warp 0 (one thread): TMA copies of each chunk's K and V (two boxes each,
-//     one per 64 channels, with the 128-byte swizzle) into two-slot rings;
+//   warps 0 and 3 (one thread each): TMA copies of each chunk's K (warp 0)
+//     and V (warp 3), two boxes each, one per 64 channels, with the 128-byte
+//     swizzle, into two-slot rings;
 //   warp 1 (one thread): the P V MMAs, O += P(c) V(c) (V read as an MN-major
 //     operand), once the softmax has written P(c);
 //   warp 2 (one thread): the S MMAs, S(c) = Q K(c)^T into one of two S
@@ -792,12 +793,12 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 //     and the softmax has taken S(c - 2) out of that buffer. Two issuing
 //     threads keep either kind of product from waiting behind the other's
 //     inputs; S(c + 1) and S(c + 2) run while the softmax of chunk c does;
-//   warps 3-6: each query block's Q tile, read from global memory into
+//   warps 4-7: each query block's Q tile, read from global memory into
 //     registers (and rotated there in the rotating modes) while the previous
 //     block still uses the Q buffer, then written into it in the swizzled
 //     layout; in the mode that rotates K per CTA, each K tile too, in place
 //     once it lands;
-//   warps 7-14: the softmax. Each query row's S is read back from tensor
+//   warps 8-15: the softmax. Each query row's S is read back from tensor
 //     memory by two threads (half of the chunk's columns each, in one batch of
 //     loads: warps w and w + 4 share the 32 lanes of tensor memory that warp w
 //     reaches), masked to the query's window (a 64-bit mask from the region
@@ -821,9 +822,9 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 // reads the previous O).
 // Tensor memory (all 512 columns: one CTA per SM): S in [0, 128) and
 // [128, 256), O in [256, 384).
-constexpr int kTcThreads = 480;              // 15 warps: TMA, P V MMA, S MMA, 4 Q, 8 softmax
-constexpr int kTcSoftWarp0 = 7;              // first softmax warp
-constexpr int kTcRotThreads = 128;           // warps 3-6
+constexpr int kTcThreads = 512;              // 16 warps: K TMA, P V MMA, S MMA, V TMA, 4 Q, 8 softmax
+constexpr int kTcSoftWarp0 = 8;              // first softmax warp
+constexpr int kTcRotThreads = 128;           // warps 4-7
 constexpr int kTcSoftThreads = 256;          // 2 threads per query row
 constexpr int kTcParts = kTcSoftThreads / 128;
 constexpr int kTcM = 128;                    // queries per CTA: 2 x 8 x 8
@@ -1112,10 +1113,10 @@ __device__ __forceinline__ TcBlock tc_block(const NAParams &p, const TcShape &sh
     return g;
 }
 
-// (bounded as for 512 threads: 128 registers a thread, so that the four warps
-// a sub-partition holds fit its quarter of the register file)
+// 128 registers a thread: the four warps a sub-partition holds fill its
+// quarter of the register file
 template <int kMode>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(kTcThreads, 1)
 rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
     extern __shared__ unsigned char tc_raw[];
@@ -1222,12 +1223,16 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     const uint32_t tmem = *tmem_slot;
     bool dead = false;
 
-    if (warp == 0) {
-        // ---- TMA producer: each block's chunks' K and V into the rings
+    if (warp == 0 || warp == 3) {
+        // ---- TMA producers: each block's chunks' K (warp 0) or V (warp 3) into
+        // their ring, each slot once the MMAs of the chunk two before are done
+        // with it (two threads, so that K never waits for a V slot)
         if (lane == 0) {
+            const bool v = warp == 3;
             // K of the rotate-once form comes from the kernel before this one in
             // the stream (programmatic serialization): wait for it first
-            if constexpr (kMode == kRotQ) asm volatile("griddepcontrol.wait;" ::: "memory");
+            if constexpr (kMode == kRotQ)
+                if (!v) asm volatile("griddepcontrol.wait;" ::: "memory");
             int gc = 0;   // chunks of the CTA so far
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
                 const TcBlock g = tc_block(p, shp, blk);
@@ -1235,10 +1240,8 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
                     const int s = gc & 1;
                     const uint32_t use = uint32_t(gc >> 1);
-                    if (gc >= 2) tc_wait(bar(kEmpty, s), (use - 1) & 1u, dead);
-                    tma_chunk(g, cp, s, false);
-                    if (gc >= 2) tc_wait(bar(vEmpty, s), (use - 1) & 1u, dead);
-                    tma_chunk(g, cp, s, true);
+                    if (gc >= 2) tc_wait(bar(v ? vEmpty : kEmpty, s), (use - 1) & 1u, dead);
+                    tma_chunk(g, cp, s, v);
                 }
             }
         }
@@ -1302,7 +1305,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 }
             }
         }
-    } else if (warp < kTcSoftWarp0) {
+    } else if (warp < kTcSoftWarp0) {   // warps 4-7
         // ---- Q warps: each block's Q tile through registers (read from global
         // memory and, in the rotating modes, rotated before the previous block
         // is done with the Q buffer; then written into it in the layout of a
@@ -1317,7 +1320,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         // reaches), normalises its 128 channels and stores them, while the
         // softmax threads already work on the next block.
         {
-            const int rt = tid - 96;   // 0 .. kTcRotThreads - 1
+            const int rt = tid - 128;   // 0 .. kTcRotThreads - 1
             const int cv = rt & 15, qw_off = rt >> 4;
             [[maybe_unused]] const TabSlot tsg = tab_slot_global(p.pT, p.pH, p.pW, p.offH, p.offW, cv);
             [[maybe_unused]] int gc = 0;

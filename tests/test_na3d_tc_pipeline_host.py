@@ -1,6 +1,6 @@
 """A CPU model of the tensor-core attention kernel's hand-over protocol
-(rope_rope3d_apply_gb300/csrc/rope3d_na3d.cu, rope3d_na3d_tc_kernel): the TMA
-thread, the two MMA threads (S products; P V products), the Q warps (which write each block's Q tile and, in
+(rope_rope3d_apply_gb300/csrc/rope3d_na3d.cu, rope3d_na3d_tc_kernel): the two
+TMA threads (K; V), the two MMA threads (S products; P V products), the Q warps (which write each block's Q tile and, in
 the mode that rotates K per CTA, rotate the K tiles) and the softmax threads
 of one persistent CTA walking several query blocks, each a sequence of the kernel's
 mbarrier waits, arrivals and buffer accesses, run in many random
@@ -84,21 +84,14 @@ def simulate(blocks, rot_q, rot_k, seed):
     # global chunk g -> (block k, chunk c)
     seq = [(k, c) for k, n in enumerate(blocks) for c in range(n)]
 
-    def producer():
-        g = 0
-        for k, n in enumerate(blocks):
-            for c in range(n):
-                s, use = g & 1, g >> 1
-                if g >= 2:
-                    yield ("wait", B["kEmpty", s], (use - 1) & 1, use - 1)
-                B["kFull", s].expect_tx(2)
-                inflight.append(("tma", ("K", s, g)))
-                if g >= 2:
-                    yield ("wait", B["vEmpty", s], (use - 1) & 1, use - 1)
-                B["vFull", s].expect_tx(2)
-                inflight.append(("tma", ("V", s, g)))
-                g += 1
-                yield None
+    def producer(kind):   # the K thread and the V thread, each over its own ring
+        for g in range(len(seq)):
+            s, use = g & 1, g >> 1
+            if g >= 2:
+                yield ("wait", B[kind + "Empty", s], (use - 1) & 1, use - 1)
+            B[kind + "Full", s].expect_tx(2)
+            inflight.append(("tma", (kind.upper(), s, g)))
+            yield None
 
     def pv_issuer():
         for g, (k, c) in enumerate(seq):
@@ -197,7 +190,7 @@ def simulate(blocks, rot_q, rot_k, seed):
             for _ in range(256 // SOFT):
                 B["oFull", k & 1].arrive()
 
-    roles = [producer(), s_issuer(), pv_issuer()] + [softmax(i) for i in range(SOFT)] + \
+    roles = [producer("k"), producer("v"), s_issuer(), pv_issuer()] + [softmax(i) for i in range(SOFT)] + \
         [q_warp(i) for i in range(4)]
     waiting = [None] * len(roles)
     done = [False] * len(roles)
