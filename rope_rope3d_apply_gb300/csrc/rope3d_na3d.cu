@@ -807,19 +807,19 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 //     softmax as the
 //     warp-MMA kernel (the reference moves only when a row maximum passes it
 //     by more than 2^kLazy; O in tensor memory is rescaled then); the bf16
-//     weights go to one of two P tiles (K-major, swizzled).
+//     weights are written back into the S buffer they came from (over the S
+//     values, as bf16 pairs), where the P V MMA reads them as its A operand.
 // Q stays in shared memory for every chunk of its block.
 // Shared memory (bytes; every tile 1024-aligned, the swizzle's period):
 //   Q  [2 column blocks][128 rows][128 B]               32,768
 //   K  [2 slots][2 column blocks][kTcN rows][128 B]     57,344
 //   V  [2 slots][2 column blocks][kTcN rows][128 B]     57,344
-//   P  [2 slots][2 column blocks of 64 keys][128][128 B] 65,536
 //   row maxima and sums of the row's two threads, the softmax threads' window
 //   masks (4 KB per chunk row offset, up to 4 offsets), 20 mbarriers, the TMEM
 //   address.
-// Tensor memory (512 columns): S buffers at columns 0 and 128, O of even and
-// odd blocks at 256 and 384 (the next block's P V starts while the epilogue
-// reads the previous O).
+// Tensor memory (512 columns): S buffers at columns 0 and 128 (S, then P in
+// their first 56 columns), O of even and odd blocks at 256 and 384 (the next
+// block's P V starts while the Q warps read the previous O out).
 // Tensor memory (all 512 columns: one CTA per SM): S in [0, 128) and
 // [128, 256), O in [256, 384).
 constexpr int kTcThreads = 512;              // 16 warps: K TMA, P V MMA, S MMA, V TMA, 4 Q, 8 softmax
@@ -831,17 +831,14 @@ constexpr int kTcM = 128;                    // queries per CTA: 2 x 8 x 8
 constexpr int kTcQT = 2, kTcQH = 8, kTcQW = 8;
 constexpr int kTcN = 112;                    // keys per chunk at most
 constexpr int kTcHalf = kTcN / kTcParts;     // columns of S a softmax thread reads at most
-constexpr int kTcPBlocks = (kTcN + 63) / 64; // 64-key column blocks of a P tile
 constexpr uint32_t kTcQCb = kTcM * 128;      // bytes of a column block of Q or P
 constexpr uint32_t kTcKvCb = kTcN * 128;     // bytes of a column block of K or V
 constexpr uint32_t kTcKvSlot = 2 * kTcKvCb;  // bytes of a K or V slot
-constexpr uint32_t kTcPSlot = kTcPBlocks * kTcQCb;
 constexpr uint32_t kTcOffQ = 0;
 constexpr uint32_t kTcOffK = kTcOffQ + 2 * kTcQCb;
 constexpr uint32_t kTcOffV = kTcOffK + 2 * kTcKvSlot;
-constexpr uint32_t kTcOffP = kTcOffV + 2 * kTcKvSlot;
 // float row maxima [chunk parity][part][128], row sums [block parity][part][128]
-constexpr uint32_t kTcOffRed = kTcOffP + 2 * kTcPSlot;
+constexpr uint32_t kTcOffRed = kTcOffV + 2 * kTcKvSlot;
 // the softmax threads' window masks of a block's chunk row offsets (frames
 // share them): [offset][part][128] 64-bit words, each thread its own
 constexpr int kTcMaxPF = 4;                                 // offsets kept; more: made per chunk
@@ -854,7 +851,7 @@ constexpr uint32_t kTcColO = 256;                           // O of block k at 2
 constexpr uint32_t kTcTmemCols = 512;
 constexpr int kTcMaxRW = kTcN;                              // a region row must fit a chunk
 static_assert(kTcKvCb % 1024 == 0 && kTcOffK % 1024 == 0 && kTcOffV % 1024 == 0 &&
-              kTcOffP % 1024 == 0, "1024-aligned tiles");
+              kTcOffRed % 1024 == 0, "1024-aligned tiles");
 static_assert(kTcN % 16 == 0 && kTcN <= int(kTcColS), "an S buffer holds a chunk");
 static_assert(kTcColO + 128 <= kTcTmemCols, "O fits the allocation");
 static_assert(kTcSmem + 1024 <= 228 * 1024, "one CTA per SM");
@@ -886,6 +883,16 @@ __device__ __forceinline__ void tc_mma(uint32_t tmem, uint64_t a, uint64_t b, ui
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// The same with A (M x 16, K-major, two bf16 per 32-bit column) read from
+// tensor memory at a_tmem.
+__device__ __forceinline__ void tc_mma_ta(uint32_t tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
 }
 
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -1058,6 +1065,29 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
         : "memory");
 }
 
+// 16, 8 or 4 consecutive 32-bit columns of this warp's 32 lanes of tensor
+// memory (lane = thread), from registers; tcgen05.wait::st completes them.
+__device__ __forceinline__ void tc_st16w(uint32_t taddr, const uint32_t *w) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16};"
+        ::"r"(taddr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+          "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]),
+          "r"(w[15])
+        : "memory");
+}
+__device__ __forceinline__ void tc_st8w(uint32_t taddr, const uint32_t *w) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 ::"r"(taddr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                   "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+__device__ __forceinline__ void tc_st4w(uint32_t taddr, const uint32_t *w) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
+                 ::"r"(taddr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                 : "memory");
+}
+
 // Byte offset of 16-byte chunk c (0..15: 8 elements each) of row `row` in a
 // K-major tile with the 128-byte swizzle: chunk c lies in column block c / 8,
 // and inside a 128-byte row the chunk index is XORed with row mod 8.
@@ -1122,7 +1152,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     extern __shared__ unsigned char tc_raw[];
     unsigned char *sm = tc_raw + ((1024u - (smem_addr(tc_raw) & 1023u)) & 1023u);
     const uint32_t sQ = smem_addr(sm + kTcOffQ), sK = smem_addr(sm + kTcOffK);
-    const uint32_t sV = smem_addr(sm + kTcOffV), sP = smem_addr(sm + kTcOffP);
+    const uint32_t sV = smem_addr(sm + kTcOffV);
     float *red_max = reinterpret_cast<float *>(sm + kTcOffRed);   // [chunk parity][part][128]
     float *red_sum = red_max + 2 * kTcParts * kTcM;                 // [block parity][part][128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kTcOffBar);
@@ -1183,7 +1213,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     // ---- set-up: barriers, tensor memory, zeroed pad rows
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
-            const int counts[9] = {1, kTcRotThreads, 1, 1, 1, 1, kTcSoftThreads, kTcSoftThreads, 1};
+            const int counts[9] = {1, kTcRotThreads, 1, 1, 1, 1, 1, kTcSoftThreads, 1};
             for (int kind = 0; kind < 9; ++kind)
                 asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar(kind, s)),
                              "r"(counts[kind]) : "memory");
@@ -1265,12 +1295,14 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                     tc_wait(bar(vFull, s), use & 1u, dead);
                     tc_fence_after();
                     const int ngrp = chunk_n(cp) >> 4;
-                    const uint32_t pt = sP + s * kTcPSlot, vt = sV + s * kTcKvSlot;
+                    // P(c) is in S buffer s: 16 keys = 8 columns of bf16 pairs a step
+                    const uint32_t pa = tmem + s * kTcColS, vt = sV + s * kTcKvSlot;
                     for (int j = 0; j < ngrp; ++j)
-                        tc_mma(o_col, tc_sdesc(pt + (j >> 2) * kTcQCb + (j & 3) * 32, 16, 1024),
-                               tc_sdesc(vt + j * 2048, kTcKvCb, 1024), id, (j > 0 || c > 0) ? 1u : 0u);
+                        tc_mma_ta(o_col, pa + uint32_t(8 * j), tc_sdesc(vt + j * 2048, kTcKvCb, 1024), id,
+                                  (j > 0 || c > 0) ? 1u : 0u);
                     tc_commit(bar(vEmpty, s));
                     tc_commit(bar(pEmpty, s));
+                    tc_commit(bar(sEmpty, s));   // S buffer s (and P in it) free for S(c + 2)
                     if (c == g.n_chunks - 1) tc_commit(oReady(k & 1));
                 }
             }
@@ -1422,7 +1454,6 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         const int lg = warp & 3, qq = (warp - kTcSoftWarp0) >> 2;
         const int row = 32 * lg + lane;
         const uint32_t lanes = uint32_t(32 * lg) << 16;
-        const uint32_t p_row = uint32_t(row) * 128u;   // this row in a P column block
         int gc = 0;
         for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
             const TcBlock g = tc_block(p, shp, blk);
@@ -1487,9 +1518,6 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                     tc_ld8_async(tS + uint32_t(cb0 + 48), x + 48);
                     tc_ld_wait_hold<kTcHalf>(x);
                 }
-                // S is in registers: the MMA may write S(c + 2) into this buffer
-                tc_fence_before();
-                mbar_arrive(bar(sEmpty, s));
                 // the masked maximum, as four independent partial maxima taken two
                 // values at a time
                 float cmax = -INFINITY;
@@ -1530,30 +1558,34 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                     m_ref = mn;
                     l_part *= corr;
                 }
-                // weights into P tile s, once P V of chunk gc - 2 is done with it
-                if (gc >= 2) tc_wait(bar(pEmpty, s), (use - 1) & 1u, dead);
+                // The weights, as bf16 pairs, into this S buffer's first 56 columns
+                // (this part's 28 from column cb0 / 2) over the S values both
+                // threads of the row have read (the exchange above came after
+                // their loads); the P V MMA reads them from there.
                 const float ms = m_ref == -INFINITY ? 0.f : m_ref;
-                unsigned char *pt = sm + kTcOffP + s * kTcPSlot;
                 // exponent arguments and the row sum in packed pairs (two sums)
                 const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-ms, -ms);
                 float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                uint32_t pw[kTcHalf / 2];
 #pragma unroll
                 for (int k8 = 0; k8 < kTcHalf / 8; ++k8) {
-                    uint32_t w4[4] = {0u, 0u, 0u, 0u};
-                    if (any) {
 #pragma unroll
-                        for (int e = 0; e < 8; e += 2) {
+                    for (int e = 0; e < 8; e += 2) {
+                        uint32_t w = 0u;
+                        if (any) {
                             const float2 t = __ffma2_rn(make_float2(x[8 * k8 + e], x[8 * k8 + e + 1]), sc2, nm2);
                             const float a0 = ex2(t.x), a1 = ex2(t.y);
                             sum2[(e >> 1) & 1] = __fadd2_rn(sum2[(e >> 1) & 1], make_float2(a0, a1));
-                            w4[e >> 1] = pack_bf16(a0, a1);
+                            w = pack_bf16(a0, a1);
                         }
+                        pw[4 * k8 + (e >> 1)] = w;
                     }
-                    const uint32_t cc = uint32_t((cb0 >> 3) + k8);   // 16-byte chunk of the P row
-                    *reinterpret_cast<uint4 *>(pt + p_row + (cc >> 3) * kTcQCb + (((cc ^ uint32_t(row)) & 7u) << 4)) =
-                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
                 l_part += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
+                const uint32_t tP = tS + uint32_t(cb0 >> 1);
+                tc_st16w(tP, pw);
+                tc_st8w(tP + 16, pw + 16);
+                tc_st4w(tP + 24, pw + 24);
                 // O rescaled after the weights are out (the row's S values are
                 // no longer held), before P V of this chunk adds to it
                 if (__any_sync(0xffffffffu, rescale)) {
@@ -1569,10 +1601,9 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                         for (int i = 0; i < 16; ++i) o[i] *= corr;
                         tc_st16(ta, o);
                     }
-                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 }
-                fence_async_smem();   // P, for the MMA's reads
-                tc_fence_before();    // the accesses of O, before the hand-over
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");   // P (and O) written
+                tc_fence_before();    // the tensor-memory accesses, before the hand-over
                 mbar_arrive(bar(pFull, s));
             }
 

@@ -11,11 +11,12 @@ It asserts, in every interleaving, that:
   - every role runs to its end (no wait that can never be satisfied);
   - a wait on parity P is never made while the barrier is two or more phases
     past the phase it stands for (a parity wait cannot tell those apart);
-  - no ring slot, S buffer, P tile or O is written while a reader of the
-    previous contents may still be reading it, nor read before it is written:
-    K slot s is overwritten only after the S MMAs of its last chunk have
-    completed; V slot s only after that chunk's P V; S buffer s only after the
-    softmax read it; P tile s only after its P V; O is rescaled only after the
+  - no ring slot, S buffer or O is written while a reader of the previous
+    contents may still be reading it, nor read before it is written: K slot s
+    is overwritten only after the S MMAs of its last chunk have completed; V
+    slot s only after that chunk's P V; S buffer s (where the softmax writes
+    P over S) only after P V of the chunk two before has read its P; O is
+    rescaled only after the
     previous P V has completed, and P V of chunk c runs on P and V of chunk c;
     Q is rewritten only after the previous block's S MMAs, and a block's first
     P V overwrites an O buffer only after the block two earlier was read out.
@@ -67,17 +68,18 @@ def simulate(blocks, rot_q, rot_k, seed):
     B = {}
     for s in (0, 1):
         for kind, cnt in (("kFull", 1), ("kReady", 128), ("kEmpty", 1), ("vFull", 1), ("vEmpty", 1),
-                          ("sFull", 1), ("sEmpty", 256), ("pFull", 256), ("pEmpty", 1)):
+                          ("sFull", 1), ("sEmpty", 1), ("pFull", 256), ("pEmpty", 1)):
             B[kind, s] = Bar(cnt)
     B["qReady"], B["qEmpty"] = Bar(128), Bar(1)
     for b in (0, 1):   # per O buffer: last P V done, row sums written, O read out
         B["oReady", b], B["oFull", b], B["oEmpty", b] = Bar(1), Bar(256), Bar(128)
-    state = {  # what each buffer holds
-        "K": [None, None], "V": [None, None], "S": [None, None], "P": [None, None],
+    state = {  # what each buffer holds; S buffer s holds ("S", g) then ("P", g)
+        "K": [None, None], "V": [None, None], "S": [None, None],
         "Q": None,                     # (block, "rot" or "raw") of the Q tile in place
         "O": [(-1, -1), (-1, -1)],     # O buffer k & 1: (block, last chunk added)
         "Oread": [-1, -1],             # O buffer: last block whose result was read out
         "sums": [-1, -1],              # row-sum buffer (block parity): block whose sums it holds
+        "pv_done": -1,                 # last chunk whose P V completed
     }
     inflight = []                      # asynchronous events: (kind, payload)
     SOFT = 4                           # softmax threads modelled (arrivals scaled)
@@ -100,7 +102,7 @@ def simulate(blocks, rot_q, rot_k, seed):
                 yield ("wait", B["oEmpty", k & 1], ((k - 2) >> 1) & 1, (k - 2) >> 1)
             yield ("wait", B["pFull", s], use & 1, use)
             yield ("wait", B["vFull", s], use & 1, use)
-            assert state["P"][s] == g and state["V"][s] == g, "P V reads P and V of its chunk"
+            assert state["S"][s] == ("P", g) and state["V"][s] == g, "P V reads P and V of its chunk"
             if c == 0:   # the block's first P V overwrites O buffer k & 1: read out two blocks ago
                 assert state["Oread"][k & 1] == k - 2 or (k < 2 and state["Oread"][k & 1] == -1)
             inflight.append(("pv", (s, g, k, c)))
@@ -162,17 +164,14 @@ def simulate(blocks, rot_q, rot_k, seed):
             for c in range(n):
                 s, use = g & 1, g >> 1
                 yield ("wait", B["sFull", s], use & 1, use)
-                assert state["S"][s] == g, "the softmax reads S of its chunk"
-                for _ in range(256 // SOFT):   # S held in registers: released at once
-                    B["sEmpty", s].arrive()
+                assert state["S"][s] in (("S", g), ("P", g)), "the softmax reads S of its chunk"
                 yield None
                 rescale = m_valid and rng.random() < 0.3
                 m_valid = True
-                if g >= 2:
-                    yield ("wait", B["pEmpty", s], (use - 1) & 1, use - 1)
-                assert state["P"][s] in (None, g - 2, g), "P tile free"
+                # P(g) over S(g) in the same buffer (after the row's exchange)
+                assert state["S"][s] in (("S", g), ("P", g)), "S buffer still this chunk's"
                 if i == 0:
-                    state["P"][s] = g
+                    state["S"][s] = ("P", g)
                 yield None
                 if rescale:                    # after the weights are written
                     prev = g - 1
@@ -223,8 +222,9 @@ def simulate(blocks, rot_q, rot_k, seed):
             elif kind == "s":
                 s, g, k, last = pl
                 assert state["Q"][0] == k, "Q kept until the block's S MMAs complete"
-                assert state["S"][s] is None or state["S"][s] == g - 2
-                state["S"][s] = g
+                # S(g) overwrites buffer s only after P V(g - 2) has read P(g - 2)
+                assert state["S"][s] is None or (state["S"][s] == ("P", g - 2) and state["pv_done"] >= g - 2)
+                state["S"][s] = ("S", g)
                 B["kEmpty", s].arrive()      # the commits after S(g)
                 B["sFull", s].arrive()
                 if last:
@@ -234,8 +234,11 @@ def simulate(blocks, rot_q, rot_k, seed):
                 ob = state["O"][k & 1]
                 assert (c == 0) or ob == (k, c - 1), "P V in chunk order within the block"
                 state["O"][k & 1] = (k, c)
+                assert state["S"][s] == ("P", g), "P kept until its P V completes"
+                state["pv_done"] = g
                 B["vEmpty", s].arrive()      # the commits after P V(g)
                 B["pEmpty", s].arrive()
+                B["sEmpty", s].arrive()      # S buffer s free for S(g + 2)
                 if c == blocks[k] - 1:
                     B["oReady", k & 1].arrive()
             continue
@@ -250,6 +253,7 @@ def simulate(blocks, rot_q, rot_k, seed):
         except StopIteration:
             done[i] = True
     assert not inflight
+    assert state["pv_done"] == len(seq) - 1
 
 
 BLOCKS = [[1], [3], [8], [1, 1, 1], [3, 2, 4], [8, 8, 6, 8], [2, 5, 1, 7, 3]]

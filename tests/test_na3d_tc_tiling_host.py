@@ -40,14 +40,11 @@ class Config:
         self.THREADS = 256          # softmax threads
         self.CTAS = 1
         self.PARTS = self.THREADS // TC_M
-        self.P_BLOCKS = (self.TC_N + 63) // 64
         self.KV_CB = self.TC_N * 128
         self.KV_SLOT = 2 * self.KV_CB
-        self.P_SLOT = self.P_BLOCKS * Q_CB
         self.OFF_Q, self.OFF_K = 0, 2 * Q_CB
         self.OFF_V = self.OFF_K + 2 * self.KV_SLOT
-        self.OFF_P = self.OFF_V + 2 * self.KV_SLOT
-        self.OFF_RED = self.OFF_P + 2 * self.P_SLOT
+        self.OFF_RED = self.OFF_V + 2 * self.KV_SLOT
         self.COL_S = 128            # S buffer s at column s * 128
         self.COL_O = 256
         self.TMEM_COLS = 512
@@ -144,7 +141,7 @@ def test_q_warps_write_every_q_tile_chunk_once():
 @pytest.mark.parametrize("cfg", sorted(CONFIGS))
 def test_shared_memory_layout(cfg):
     c = CONFIGS[cfg]
-    assert all(o % 1024 == 0 for o in (c.OFF_K, c.OFF_V, c.OFF_P, c.OFF_RED, c.KV_CB, c.KV_SLOT))
+    assert all(o % 1024 == 0 for o in (c.OFF_K, c.OFF_V, c.OFF_RED, c.KV_CB, c.KV_SLOT))
     # maxima [chunk parity][parts] and sums [block parity][parts] of 128
     # floats, window masks [4 offsets][parts][128] of 8 bytes, 26 mbarriers +
     # the TMEM address
@@ -154,9 +151,9 @@ def test_shared_memory_layout(cfg):
 
 
 def check_block(cfg, T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
-    TC_N, THREADS, PARTS, P_BLOCKS = cfg.TC_N, cfg.THREADS, cfg.PARTS, cfg.P_BLOCKS
-    KV_CB, OFF_Q, OFF_K, OFF_V, OFF_P = cfg.KV_CB, cfg.OFF_Q, cfg.OFF_K, cfg.OFF_V, cfg.OFF_P
-    COL_O, COL_S, KV_SLOT, P_SLOT = cfg.COL_O, cfg.COL_S, cfg.KV_SLOT, cfg.P_SLOT
+    TC_N, THREADS, PARTS = cfg.TC_N, cfg.THREADS, cfg.PARTS
+    KV_CB, OFF_Q, OFF_K, OFF_V = cfg.KV_CB, cfg.OFF_Q, cfg.OFF_K, cfg.OFF_V
+    COL_O, COL_S, KV_SLOT = cfg.COL_O, cfg.COL_S, cfg.KV_SLOT
     t0, h0, w0 = bt * QT, bh * QH, bw * QW
     rt0 = na_start(t0, T, kt)
     rt1 = na_start(min(t0 + 1, T - 1), T, kt) + kt
@@ -209,8 +206,8 @@ def check_block(cfg, T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
         zeroed = set(range(box_rows, box_rows + pad))
         assert all(r < TC_N for r in zeroed) and not zeroed & set(range(box_rows))
         assert set(range(box_rows, N)) <= zeroed
-        slot = c & 1   # ring slot of the chunk's K, V and P tiles and S buffer
-        ks_base, vs_base, ps_base = OFF_K + slot * KV_SLOT, OFF_V + slot * KV_SLOT, OFF_P + slot * P_SLOT
+        slot = c & 1   # ring slot of the chunk's K and V tiles and S buffer
+        ks_base, vs_base = OFF_K + slot * KV_SLOT, OFF_V + slot * KV_SLOT
         # S = Q K^T: eight k16 steps; A reads 128 rows of 32 bytes at koff in
         # column block ks / 4, B reads N rows likewise
         for ks in range(8):
@@ -219,31 +216,34 @@ def check_block(cfg, T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
             b0 = ks_base + (ks >> 2) * KV_CB + koff
             assert OFF_Q <= a0 and a0 - koff + TC_M * 128 <= OFF_Q + 2 * Q_CB
             assert ks_base <= b0 and b0 - koff + N * 128 <= ks_base + KV_SLOT
-        # O += P V: N / 16 k16 steps; P in column block s / 4; V as an MN-major
-        # operand: 16 keys (2 groups of 8 rows, SBO = 1024) x 128 channels (2
-        # column blocks, LBO = KV_CB)
+        # O += P V: N / 16 k16 steps; A = P from tensor memory (the S buffer's
+        # columns 8 s .. 8 s + 7: keys 16 s .. 16 s + 15 as bf16 pairs); V as an
+        # MN-major operand: 16 keys (2 groups of 8 rows, SBO = 1024) x 128
+        # channels (2 column blocks, LBO = KV_CB)
         for s in range(N // 16):
-            pa = ps_base + (s >> 2) * Q_CB + (s & 3) * 32
-            assert ps_base <= pa and pa - (s & 3) * 32 + TC_M * 128 <= ps_base + P_SLOT
+            pcol = slot * COL_S + 8 * s
+            assert slot * COL_S <= pcol and pcol + 8 <= slot * COL_S + TC_N // 2
             va = vs_base + s * 2048
             assert vs_base <= va and va + 1024 + 1024 + KV_CB <= vs_base + KV_SLOT
         # S buffer `slot` holds columns [slot * COL_S, + N), clear of the other and of O
         assert slot * COL_S + N <= (slot + 1) * COL_S <= COL_O
         # the softmax: thread part qq of a row reads columns [qq * 56, + 56) of
         # its S buffer (columns past the chunk's keys masked) and writes the
-        # weights of all 56, 8 keys (16 bytes) at a time; the parts' P columns
-        # are disjoint and cover the P V MMA's K = N columns
+        # weights of all 56 as 28 bf16 pairs from column qq * 28 (16 + 8 + 4
+        # columns): the parts' P columns are disjoint, cover every column the
+        # P V MMA reads, and overwrite only S columns [0, 56), which both parts
+        # have read before either writes (the row's exchange lies between)
         npart = 56
         assert PARTS == 2 and PARTS * npart == TC_N
         written = []
         for qq in range(PARTS):
             cb0 = qq * npart
             assert cb0 + npart <= COL_S                # inside this S buffer
-            for k8 in range(7):
-                key = cb0 + 8 * k8
-                assert key % 8 == 0 and (key >> 3) // 8 < P_BLOCKS
-                written += range(key, key + 8)
-        assert sorted(written) == list(range(TC_N)) and N <= TC_N
+            col = cb0 // 2
+            for width in (16, 8, 4):
+                written += range(col, col + width)
+                col += width
+        assert sorted(written) == list(range(TC_N // 2)) and (N // 16) * 8 <= TC_N // 2
         # the window masks of every query row: a 64-bit mask per thread part,
         # built from the chunk rows its part spans, each in the window
         # contributing columns [clo, chi)
