@@ -817,9 +817,10 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 //   row maxima and sums of the row's two threads, the softmax threads' window
 //   masks (4 KB per chunk row offset, up to 4 offsets), 20 mbarriers, the TMEM
 //   address.
-// Tensor memory (512 columns): S buffers at columns 0 and 128 (S, then P in
-// their first 56 columns), O of even and odd blocks at 256 and 384 (the next
-// block's P V starts while the Q warps read the previous O out).
+// Tensor memory (512 columns): three S buffers at columns 0, 128 and 256 (S,
+// then P in their first 56 columns), so that the S products run up to two
+// chunks ahead of the softmax while P V reads the third; O at 384 (a block's
+// first P V waits for the Q warps to have read the previous block's O out).
 // Tensor memory (all 512 columns: one CTA per SM): S in [0, 128) and
 // [128, 256), O in [256, 384).
 constexpr int kTcThreads = 512;              // 16 warps: K TMA, P V MMA, S MMA, V TMA, 4 Q, 8 softmax
@@ -843,17 +844,22 @@ constexpr uint32_t kTcOffRed = kTcOffV + 2 * kTcKvSlot;
 // share them): [offset][part][128] 64-bit words, each thread its own
 constexpr int kTcMaxPF = 4;                                 // offsets kept; more: made per chunk
 constexpr uint32_t kTcOffMask = kTcOffRed + 4 * kTcParts * kTcM * 4;
-constexpr int kTcBars = 26;                                 // mbarriers, then the TMEM address
+constexpr int kTcBars = 28;                                 // mbarriers, then the TMEM address
 constexpr uint32_t kTcOffBar = kTcOffMask + kTcMaxPF * kTcSoftThreads * 8;
 constexpr uint32_t kTcSmem = kTcOffBar + kTcBars * 8 + 16 + 1024;   // + room to align to 1024
+#ifndef NA_TC_SBUFS   // S buffers in tensor memory: 3 (O single) or 2 (O double-buffered)
+#define NA_TC_SBUFS 3
+#endif
+constexpr int kTcSBufs = NA_TC_SBUFS;
+constexpr int kTcOBufs = kTcSBufs == 3 ? 1 : 2;             // O buffers
 constexpr uint32_t kTcColS = 128;                           // S buffer b at column b * 128
-constexpr uint32_t kTcColO = 256;                           // O of block k at 256 + 128 (k & 1)
+constexpr uint32_t kTcColO = kTcSBufs * kTcColS;            // O buffer b at kTcColO + 128 b
 constexpr uint32_t kTcTmemCols = 512;
 constexpr int kTcMaxRW = kTcN;                              // a region row must fit a chunk
 static_assert(kTcKvCb % 1024 == 0 && kTcOffK % 1024 == 0 && kTcOffV % 1024 == 0 &&
               kTcOffRed % 1024 == 0, "1024-aligned tiles");
 static_assert(kTcN % 16 == 0 && kTcN <= int(kTcColS), "an S buffer holds a chunk");
-static_assert(kTcColO + 128 <= kTcTmemCols, "O fits the allocation");
+static_assert(kTcColO + 128 * kTcOBufs <= kTcTmemCols, "S and O fit the allocation");
 static_assert(kTcSmem + 1024 <= 228 * 1024, "one CTA per SM");
 static_assert((128 / kTcParts) % 16 == 0, "O columns per thread");
 static_assert(kTcParts == 2 && kTcHalf == 56, "a half row: 32 + 16 + 8 columns, a 64-bit mask");
@@ -1157,24 +1163,29 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     float *red_sum = red_max + 2 * kTcParts * kTcM;                 // [block parity][part][128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kTcOffBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kTcOffBar + kTcBars * 8);
-    // mbarriers, two of each kind (one per ring slot s = chunk & 1), counted
-    // over the CTA's whole sequence of chunks:
+    // mbarriers, counted over the CTA's whole sequence of chunks. One per K or
+    // V ring slot (chunk & 1):
     //   kFull  K landed (TMA)          kReady  K rotated (kRotQK; 128 arrivals)
     //   kEmpty S MMAs done with K      vFull   V landed (TMA)
-    //   vEmpty P V MMAs done with V    sFull   S written (MMA)
-    //   sEmpty softmax done with S (256 arrivals)
-    //   pFull  P written (256 arrivals)  pEmpty P V MMAs done with P (and O updated)
-    // and one of each per query block: qReady (the Q tile written, rotated in
-    // the rotating modes; 128 arrivals), qEmpty (the block's S MMAs done with Q).
+    //   vEmpty P V MMAs done with V
+    // one per S buffer (chunk % kTcSBufs):
+    //   sFull  S written (MMA)         sEmpty  P V done with the P in it (commit)
+    //   pFull  P written (256 arrivals) pEmpty  P V done (O updated)
+    // one of each per query block: qReady (the Q tile written, rotated in the
+    // rotating modes; 128 arrivals), qEmpty (the block's S MMAs done with Q);
+    // per O buffer b: oReady[b] the block's last P V done (commit), oEmpty[b]
+    // O read out (Q warps), so the next block using b may overwrite it; and
+    // oFull[block parity] the block's row sums written (softmax threads).
+    enum { kFull, kReady, kEmpty, vFull, vEmpty };
+    enum { sFull, sEmpty, pFull, pEmpty };
     auto bar = [&](int kind, int slot) { return smem_addr(&bars[2 * kind + slot]); };
-    enum { kFull, kReady, kEmpty, vFull, vEmpty, sFull, sEmpty, pFull, pEmpty };
-    const uint32_t qReady = smem_addr(&bars[18]), qEmpty = smem_addr(&bars[19]);
-    // per O buffer b (block parity): oReady[b] the block's last P V done
-    // (commit), oFull[b] its row sums written (softmax threads), oEmpty[b] O
-    // read out (Q warps), so that block k + 2's first P V may overwrite it
-    auto oReady = [&](int b) { return smem_addr(&bars[20 + b]); };
-    auto oFull = [&](int b) { return smem_addr(&bars[22 + b]); };
-    auto oEmpty = [&](int b) { return smem_addr(&bars[24 + b]); };
+    auto sbar = [&](int kind, int b) { return smem_addr(&bars[10 + kTcSBufs * kind + b]); };
+    constexpr int kQb = 10 + 4 * kTcSBufs;
+    const uint32_t qReady = smem_addr(&bars[kQb]), qEmpty = smem_addr(&bars[kQb + 1]);
+    auto oReady = [&](int b) { return smem_addr(&bars[kQb + 2 + b]); };
+    auto oEmpty = [&](int b) { return smem_addr(&bars[kQb + 2 + kTcOBufs + b]); };
+    auto oFull = [&](int b) { return smem_addr(&bars[kQb + 2 + 2 * kTcOBufs + b]); };
+    static_assert(kQb + 2 + 2 * kTcOBufs + 2 <= kTcBars, "mbarriers");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long tok = (long long)p.heads * kHD;   // elements per token
@@ -1213,18 +1224,25 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     // ---- set-up: barriers, tensor memory, zeroed pad rows
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
-            const int counts[9] = {1, kTcRotThreads, 1, 1, 1, 1, 1, kTcSoftThreads, 1};
-            for (int kind = 0; kind < 9; ++kind)
+            const int counts[5] = {1, kTcRotThreads, 1, 1, 1};
+            for (int kind = 0; kind < 5; ++kind)
                 asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar(kind, s)),
+                             "r"(counts[kind]) : "memory");
+        }
+        for (int b = 0; b < kTcSBufs; ++b) {
+            const int counts[4] = {1, 1, kTcSoftThreads, 1};
+            for (int kind = 0; kind < 4; ++kind)
+                asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sbar(kind, b)),
                              "r"(counts[kind]) : "memory");
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(qReady), "r"(kTcRotThreads) : "memory");
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(qEmpty) : "memory");
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kTcOBufs; ++b) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(oReady(b)) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(oFull(b)), "r"(kTcSoftThreads) : "memory");
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(oEmpty(b)), "r"(kTcRotThreads) : "memory");
         }
+        for (int b = 0; b < 2; ++b)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(oFull(b)), "r"(kTcSoftThreads) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
@@ -1284,33 +1302,34 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             const uint32_t id = tc_idesc(kTcM, kHD, 1);
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
                 const TcBlock g = tc_block(p, shp, blk);
-                const uint32_t o_col = tmem + kTcColO + uint32_t(k & 1) * 128;
-                // O buffer k & 1 once the Q warps have read block k - 2's result
-                if (k >= 2) tc_wait(oEmpty(k & 1), uint32_t((k - 2) >> 1) & 1u, dead);
+                const int ob = k % kTcOBufs;
+                const uint32_t o_col = tmem + kTcColO + uint32_t(ob) * 128;
+                // O buffer ob once the Q warps have read the previous result in it
+                if (k >= kTcOBufs) tc_wait(oEmpty(ob), uint32_t(k / kTcOBufs - 1) & 1u, dead);
                 ChunkPos cp = chunk_start(g);
                 for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
-                    const int s = gc & 1;
-                    const uint32_t use = uint32_t(gc >> 1);
-                    tc_wait(bar(pFull, s), use & 1u, dead);
+                    const int s = gc & 1, sb = gc % kTcSBufs;   // V slot, S buffer
+                    const uint32_t use = uint32_t(gc >> 1), suse = uint32_t(gc / kTcSBufs);
+                    tc_wait(sbar(pFull, sb), suse & 1u, dead);
                     tc_wait(bar(vFull, s), use & 1u, dead);
                     tc_fence_after();
                     const int ngrp = chunk_n(cp) >> 4;
-                    // P(c) is in S buffer s: 16 keys = 8 columns of bf16 pairs a step
-                    const uint32_t pa = tmem + s * kTcColS, vt = sV + s * kTcKvSlot;
+                    // P(c) is in S buffer sb: 16 keys = 8 columns of bf16 pairs a step
+                    const uint32_t pa = tmem + sb * kTcColS, vt = sV + s * kTcKvSlot;
                     for (int j = 0; j < ngrp; ++j)
                         tc_mma_ta(o_col, pa + uint32_t(8 * j), tc_sdesc(vt + j * 2048, kTcKvCb, 1024), id,
                                   (j > 0 || c > 0) ? 1u : 0u);
                     tc_commit(bar(vEmpty, s));
-                    tc_commit(bar(pEmpty, s));
-                    tc_commit(bar(sEmpty, s));   // S buffer s (and P in it) free for S(c + 2)
-                    if (c == g.n_chunks - 1) tc_commit(oReady(k & 1));
+                    tc_commit(sbar(pEmpty, sb));
+                    tc_commit(sbar(sEmpty, sb));   // S buffer sb (and P in it) free again
+                    if (c == g.n_chunks - 1) tc_commit(oReady(ob));
                 }
             }
         }
     } else if (warp == 2) {
-        // ---- S issuer: S(c) = Q K(c)^T into S buffer c & 1 as soon as K(c)
-        // has landed (rotated, in the per-CTA mode) and the softmax has taken
-        // S(c - 2) out of that buffer: up to two chunks ahead of the softmax
+        // ---- S issuer: S(c) = Q K(c)^T into S buffer c % kTcSBufs as soon as
+        // K(c) has landed (rotated, in the per-CTA mode) and P V has read the
+        // P of the chunk kTcSBufs before from that buffer
         if (lane == 0) {
             int gc = 0;
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
@@ -1318,21 +1337,21 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 tc_wait(qReady, uint32_t(k) & 1u, dead);
                 ChunkPos cp = chunk_start(g);
                 for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
-                    const int s = gc & 1;
-                    const uint32_t use = uint32_t(gc >> 1);
+                    const int s = gc & 1, sb = gc % kTcSBufs;   // K slot, S buffer
+                    const uint32_t use = uint32_t(gc >> 1), suse = uint32_t(gc / kTcSBufs);
                     tc_wait(bar(kMode == kRotQK ? kReady : kFull, s), use & 1u, dead);
-                    if (gc >= 2) tc_wait(bar(sEmpty, s), (use - 1) & 1u, dead);
+                    if (gc >= kTcSBufs) tc_wait(sbar(sEmpty, sb), (suse - 1) & 1u, dead);
                     tc_fence_after();
                     const uint32_t id = tc_idesc(kTcM, uint32_t(chunk_n(cp)), 0);
                     const uint32_t kt = sK + s * kTcKvSlot;
 #pragma unroll
                     for (int ks = 0; ks < kHD / 16; ++ks) {
                         const uint32_t koff = (ks & 3) * 32;   // 16 channels = 32 bytes
-                        tc_mma(tmem + s * kTcColS, tc_sdesc(sQ + (ks >> 2) * kTcQCb + koff, 16, 1024),
+                        tc_mma(tmem + sb * kTcColS, tc_sdesc(sQ + (ks >> 2) * kTcQCb + koff, 16, 1024),
                                tc_sdesc(kt + (ks >> 2) * kTcKvCb + koff, 16, 1024), id, ks > 0);
                     }
                     tc_commit(bar(kEmpty, s));
-                    tc_commit(bar(sFull, s));
+                    tc_commit(sbar(sFull, sb));
                     if (c == g.n_chunks - 1) tc_commit(qEmpty);
                 }
             }
@@ -1358,10 +1377,9 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             [[maybe_unused]] int gc = 0;
             const int orow = 32 * (warp & 3) + lane;   // the O row this thread stores
             auto store_o = [&](const TcBlock &g, int k) {
-                const int b = k & 1;
-                const uint32_t ph = uint32_t(k >> 1) & 1u;
-                tc_wait(oReady(b), ph, dead);
-                tc_wait(oFull(b), ph, dead);
+                const int b = k & 1, ob = k % kTcOBufs;   // row-sum and O buffers
+                tc_wait(oReady(ob), uint32_t(k / kTcOBufs) & 1u, dead);
+                tc_wait(oFull(b), uint32_t(k >> 1) & 1u, dead);
                 tc_fence_after();
                 float l = 0.f;
 #pragma unroll
@@ -1371,7 +1389,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 const bool ok = qt < p.T && qh < p.H && qw < p.W;
                 const long long base = ((((long long)g.b * p.T + qt) * p.H + qh) * p.W + qw) * tok +
                                        (long long)g.head * kHD;
-                const uint32_t tO = tmem + kTcColO + uint32_t(b) * 128 + (uint32_t(32 * (warp & 3)) << 16);
+                const uint32_t tO = tmem + kTcColO + uint32_t(ob) * 128 + (uint32_t(32 * (warp & 3)) << 16);
 #pragma unroll 1
                 for (int h2 = 0; h2 < kHD / 16; ++h2) {
                     float o[16];
@@ -1386,7 +1404,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                     }
                 }
                 tc_fence_before();   // the reads of O, before the buffer is handed back
-                mbar_arrive(oEmpty(b));
+                mbar_arrive(oEmpty(ob));
             };
             TcBlock g_prev{};
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
@@ -1421,6 +1439,10 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                     *reinterpret_cast<uint4 *>(sm + kTcOffQ + sw128(uint32_t(qw_off + 8 * i), uint32_t(cv), kTcQCb)) = qv[i];
                 fence_async_smem();
                 mbar_arrive(qReady);
+                // the previous block's result: before this block's K tiles, whose
+                // S products may wait for the O buffer through P V
+                if (k >= 1) store_o(g_prev, k - 1);
+                g_prev = g;
                 if constexpr (kMode == kRotQK) {
                     ChunkPos cp = chunk_start(g);
                     for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
@@ -1442,8 +1464,6 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                         mbar_arrive(bar(kReady, s));
                     }
                 }
-                if (k >= 1) store_o(g_prev, k - 1);   // the previous block's result
-                g_prev = g;
             }
             const int nblk = shp.total > int(blockIdx.x)
                                  ? (shp.total - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x) : 0;
@@ -1463,7 +1483,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             const int ah = na_start(min(qh, p.H - 1), p.H, p.kh) - g.rh0;
             const int aw = na_start(min(qw, p.W - 1), p.W, p.kw) - g.rw0;
             const int clo = max(aw, 0), chi = min(aw + p.kw, g.RW);   // window columns of a region row
-            const uint32_t tO = tmem + kTcColO + uint32_t(k & 1) * 128 + lanes;
+            const uint32_t tO = tmem + kTcColO + uint32_t(k % kTcOBufs) * 128 + lanes;
             float m_ref = -INFINITY, l_part = 0.f;   // running reference and this part's sum
             const int cb0 = qq * kTcHalf;   // this thread's columns of a chunk: [cb0, cb0 + 56)
             // Window mask of the chunk at region rows [r0, r0 + nr): bit k stands
@@ -1490,10 +1510,11 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
 
             ChunkPos cp = chunk_start(g);
             for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
-                const int s = gc & 1;
-                const uint32_t use = uint32_t(gc >> 1);
+                const int s = gc & 1;   // parity of the row-maximum exchange buffer
                 const int f = cp.f, r0 = cp.r0, nr = cp.nr;
-                const uint32_t tS = tmem + s * kTcColS + lanes;
+                const int sb = gc % kTcSBufs;   // S buffer
+                const uint32_t suse = uint32_t(gc / kTcSBufs);
+                const uint32_t tS = tmem + sb * kTcColS + lanes;
                 // this thread's half of the chunk's columns, [cb0, cb0 + 56), loaded
                 // at once as 32 + 16 + 8 columns. Columns past the chunk's keys are
                 // masked (their S values are stale or zero-row products) and their
@@ -1509,7 +1530,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 // S. The others treat every group alike: straight-line code (the
                 // groups' work interleaves) beats skipping groups by branches.
                 const bool any = __any_sync(0xffffffffu, win != 0);
-                tc_wait(bar(sFull, s), use & 1u, dead);
+                tc_wait(sbar(sFull, sb), suse & 1u, dead);
                 tc_fence_after();
                 float x[kTcHalf];
                 if (any) {
@@ -1590,7 +1611,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 // no longer held), before P V of this chunk adds to it
                 if (__any_sync(0xffffffffu, rescale)) {
                     // O must hold chunk c - 1's P V first (the same block)
-                    tc_wait(bar(pEmpty, (gc - 1) & 1), uint32_t((gc - 1) >> 1) & 1u, dead);
+                    tc_wait(sbar(pEmpty, (gc - 1) % kTcSBufs), uint32_t((gc - 1) / kTcSBufs) & 1u, dead);
                     tc_fence_after();
                     float o[16];
 #pragma unroll 1   // (unrolled, the loads are hoisted and registers spill)
@@ -1604,7 +1625,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");   // P (and O) written
                 tc_fence_before();    // the tensor-memory accesses, before the hand-over
-                mbar_arrive(bar(pFull, s));
+                mbar_arrive(sbar(pFull, sb));
             }
 
             // ---- this part's row sum for the Q warps, which normalise and store

@@ -1,27 +1,35 @@
 """A CPU model of the tensor-core attention kernel's hand-over protocol
-(rope_rope3d_apply_gb300/csrc/rope3d_na3d.cu, rope3d_na3d_tc_kernel): the two
-TMA threads (K; V), the two MMA threads (S products; P V products), the Q warps (which write each block's Q tile and, in
-the mode that rotates K per CTA, rotate the K tiles) and the softmax threads
-of one persistent CTA walking several query blocks, each a sequence of the kernel's
-mbarrier waits, arrivals and buffer accesses, run in many random
-interleavings over model mbarriers (a phase counter, a pending arrival count
-and a transaction byte count each).
+(rope_rope3d_apply_gb300/csrc/rope3d_na3d.cu, rope3d_na3d_tc_kernel).
+
+The roles of one persistent CTA walking several query blocks are modelled:
+  - the two TMA threads (K; V);
+  - the two MMA threads (S products; P V products);
+  - the Q warps, which write each block's Q tile, store each block's O and,
+    in the mode that rotates K per CTA, rotate the K tiles;
+  - the softmax threads, which write P over S in the S buffer.
+Each role is a sequence of the kernel's mbarrier waits, arrivals and buffer
+accesses. They run in many random interleavings over model mbarriers (a phase
+counter, a pending arrival count and a transaction byte count each). The
+layouts built are the kernel's: three S buffers with one O buffer (the
+default), and two S buffers with two O buffers.
 
 It asserts, in every interleaving, that:
   - every role runs to its end (no wait that can never be satisfied);
   - a wait on parity P is never made while the barrier is two or more phases
     past the phase it stands for (a parity wait cannot tell those apart);
-  - no ring slot, S buffer or O is written while a reader of the previous
-    contents may still be reading it, nor read before it is written: K slot s
-    is overwritten only after the S MMAs of its last chunk have completed; V
-    slot s only after that chunk's P V; S buffer s (where the softmax writes
-    P over S) only after P V of the chunk two before has read its P; O is
-    rescaled only after the
-    previous P V has completed, and P V of chunk c runs on P and V of chunk c;
-    Q is rewritten only after the previous block's S MMAs, and a block's first
-    P V overwrites an O buffer only after the block two earlier was read out.
+  - no ring slot, S buffer or O buffer is written while a reader of the
+    previous contents may still be reading it, nor read before it is written:
+      - K slot s is overwritten only after the S MMAs of its last chunk;
+      - V slot s only after that chunk's P V;
+      - S buffer b (where the softmax writes P over S) only after the P V of
+        the chunk one ring turn before has read its P;
+      - O is rescaled only after the previous P V, and P V of chunk c runs on
+        P and V of chunk c;
+      - Q is rewritten only after the previous block's S MMAs;
+      - a block's first P V overwrites an O buffer only after its previous
+        block was read out of it, and row sums are read before rewritten.
 The MMAs' completions are modelled as separate asynchronous events (a commit
-arrives when the MMAs issued before it finish)."""
+arrives when the MMAs issued before it finish; each MMA thread's in order)."""
 from __future__ import annotations
 
 import random
@@ -62,23 +70,30 @@ class Bar:
         return self.phase >= want_phase + 1
 
 
-def simulate(blocks, rot_q, rot_k, seed):
-    """blocks: the chunk count of each query block the CTA walks in turn."""
+def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
+    """blocks: the chunk count of each query block the CTA walks in turn;
+    sbufs: S buffers (3 with one O buffer, 2 with two)."""
+    obufs = 1 if sbufs == 3 else 2
     rng = random.Random(seed)
     B = {}
-    for s in (0, 1):
-        for kind, cnt in (("kFull", 1), ("kReady", 128), ("kEmpty", 1), ("vFull", 1), ("vEmpty", 1),
-                          ("sFull", 1), ("sEmpty", 1), ("pFull", 256), ("pEmpty", 1)):
+    for s in (0, 1):   # K and V ring slots
+        for kind, cnt in (("kFull", 1), ("kReady", 128), ("kEmpty", 1), ("vFull", 1), ("vEmpty", 1)):
             B[kind, s] = Bar(cnt)
+    for b in range(sbufs):
+        for kind, cnt in (("sFull", 1), ("sEmpty", 1), ("pFull", 256), ("pEmpty", 1)):
+            B[kind, b] = Bar(cnt)
     B["qReady"], B["qEmpty"] = Bar(128), Bar(1)
-    for b in (0, 1):   # per O buffer: last P V done, row sums written, O read out
-        B["oReady", b], B["oFull", b], B["oEmpty", b] = Bar(1), Bar(256), Bar(128)
-    state = {  # what each buffer holds; S buffer s holds ("S", g) then ("P", g)
-        "K": [None, None], "V": [None, None], "S": [None, None],
+    for b in range(obufs):   # per O buffer: last P V done, O read out
+        B["oReady", b], B["oEmpty", b] = Bar(1), Bar(128)
+    for b in (0, 1):         # per block parity: row sums written
+        B["oFull", b] = Bar(256)
+    state = {  # what each buffer holds; S buffer b holds ("S", g) then ("P", g)
+        "K": [None, None], "V": [None, None], "S": [None] * sbufs,
         "Q": None,                     # (block, "rot" or "raw") of the Q tile in place
-        "O": [(-1, -1), (-1, -1)],     # O buffer k & 1: (block, last chunk added)
-        "Oread": [-1, -1],             # O buffer: last block whose result was read out
+        "O": [(-1, -1)] * obufs,       # O buffer: (block, last chunk added)
+        "Oread": [-1] * obufs,         # O buffer: last block whose result was read out
         "sums": [-1, -1],              # row-sum buffer (block parity): block whose sums it holds
+        "sums_read": [-1, -1],         # row-sum buffer: last block whose sums were read
         "pv_done": -1,                 # last chunk whose P V completed
     }
     inflight = []                      # asynchronous events: (kind, payload)
@@ -98,26 +113,30 @@ def simulate(blocks, rot_q, rot_k, seed):
     def pv_issuer():
         for g, (k, c) in enumerate(seq):
             s, use = g & 1, g >> 1
-            if c == 0 and k >= 2:   # O buffer k & 1 read out by the Q warps (block k - 2)
-                yield ("wait", B["oEmpty", k & 1], ((k - 2) >> 1) & 1, (k - 2) >> 1)
-            yield ("wait", B["pFull", s], use & 1, use)
+            sb, suse = g % sbufs, g // sbufs
+            ob = k % obufs
+            if c == 0 and k >= obufs:   # O buffer ob read out by the Q warps (block k - obufs)
+                u = k // obufs - 1
+                yield ("wait", B["oEmpty", ob], u & 1, u)
+            yield ("wait", B["pFull", sb], suse & 1, suse)
             yield ("wait", B["vFull", s], use & 1, use)
-            assert state["S"][s] == ("P", g) and state["V"][s] == g, "P V reads P and V of its chunk"
-            if c == 0:   # the block's first P V overwrites O buffer k & 1: read out two blocks ago
-                assert state["Oread"][k & 1] == k - 2 or (k < 2 and state["Oread"][k & 1] == -1)
-            inflight.append(("pv", (s, g, k, c)))
+            assert state["S"][sb] == ("P", g) and state["V"][s] == g, "P V reads P and V of its chunk"
+            if c == 0:   # the block's first P V overwrites O buffer ob
+                assert state["Oread"][ob] == k - obufs or (k < obufs and state["Oread"][ob] == -1)
+            inflight.append(("pv", (s, sb, g, k, c)))
 
     def s_issuer():
         for g, (k, c) in enumerate(seq):
             s, use = g & 1, g >> 1
+            sb, suse = g % sbufs, g // sbufs
             if c == 0:
                 yield ("wait", B["qReady"], k & 1, k)
             yield ("wait", B["kReady" if rot_k else "kFull", s], use & 1, use)
-            if g >= 2:
-                yield ("wait", B["sEmpty", s], (use - 1) & 1, use - 1)
+            if g >= sbufs:
+                yield ("wait", B["sEmpty", sb], (suse - 1) & 1, suse - 1)
             assert state["K"][s] == (g, "rot" if rot_k else "raw"), "S reads K of its chunk"
             assert state["Q"] == (k, "rot" if rot_q else "raw"), "S reads Q of its block"
-            inflight.append(("s", (s, g, k, c == blocks[k] - 1)))
+            inflight.append(("s", (s, sb, g, k, c == blocks[k] - 1)))
 
     def q_warp(i):
         g = 0
@@ -130,6 +149,8 @@ def simulate(blocks, rot_q, rot_k, seed):
                 state["Q"] = (k, "rot" if rot_q else "raw")
             for _ in range(32):
                 B["qReady"].arrive()
+            if k >= 1:                 # the previous block's result, before this block's K tiles
+                yield from store_o(i, k - 1)
             for c in range(n):
                 if rot_k:
                     s, use = g & 1, g >> 1
@@ -141,50 +162,52 @@ def simulate(blocks, rot_q, rot_k, seed):
                         B["kReady", s].arrive()
                 g += 1
                 yield None
-            if k >= 1:
-                yield from store_o(i, k - 1)
         yield from store_o(i, len(blocks) - 1)
 
     def store_o(i, k):
-        b, ph = k & 1, k >> 1
-        yield ("wait", B["oReady", b], ph & 1, ph)
-        yield ("wait", B["oFull", b], ph & 1, ph)
-        assert state["O"][b] == (k, blocks[k] - 1), "the block's O is complete"
+        b, ob = k & 1, k % obufs
+        u = k // obufs
+        yield ("wait", B["oReady", ob], u & 1, u)
+        yield ("wait", B["oFull", b], (k >> 1) & 1, k >> 1)
+        assert state["O"][ob] == (k, blocks[k] - 1), "the block's O is complete"
         assert state["sums"][b] == k, "its row sums are written"
         yield None                        # O read, normalised, stored
         if i == 0:
-            state["Oread"][b] = k
+            state["Oread"][ob] = k
+            state["sums_read"][b] = k
         for _ in range(32):
-            B["oEmpty", b].arrive()
+            B["oEmpty", ob].arrive()
 
     def softmax(i):
         g = 0
         for k, n in enumerate(blocks):
             m_valid = False
+            ob = k % obufs
             for c in range(n):
-                s, use = g & 1, g >> 1
-                yield ("wait", B["sFull", s], use & 1, use)
-                assert state["S"][s] in (("S", g), ("P", g)), "the softmax reads S of its chunk"
+                sb, suse = g % sbufs, g // sbufs
+                yield ("wait", B["sFull", sb], suse & 1, suse)
+                assert state["S"][sb] in (("S", g), ("P", g)), "the softmax reads S of its chunk"
                 yield None
                 rescale = m_valid and rng.random() < 0.3
                 m_valid = True
                 # P(g) over S(g) in the same buffer (after the row's exchange)
-                assert state["S"][s] in (("S", g), ("P", g)), "S buffer still this chunk's"
+                assert state["S"][sb] in (("S", g), ("P", g)), "S buffer still this chunk's"
                 if i == 0:
-                    state["S"][s] = ("P", g)
+                    state["S"][sb] = ("P", g)
                 yield None
                 if rescale:                    # after the weights are written
                     prev = g - 1
-                    yield ("wait", B["pEmpty", prev & 1], (prev >> 1) & 1, prev >> 1)
-                    assert state["O"][k & 1] == (k, c - 1), "O rescaled after the previous P V"
+                    pb, pu = prev % sbufs, prev // sbufs
+                    yield ("wait", B["pEmpty", pb], pu & 1, pu)
+                    assert state["O"][ob] == (k, c - 1), "O rescaled after the previous P V"
                 for _ in range(256 // SOFT):
-                    B["pFull", s].arrive()
+                    B["pFull", sb].arrive()
                 g += 1
                 yield None
             # this part's row sums for the Q warps; on to the next block at once
             if i == 0:
-                assert state["sums"][k & 1] in (-1, k - 2), "row sums of block k - 2 were read"
-                assert state["Oread"][k & 1] == k - 2 or (k < 2 and state["Oread"][k & 1] == -1)
+                assert state["sums_read"][k & 1] == k - 2 or (k < 2 and state["sums_read"][k & 1] == -1), \
+                    "row sums of block k - 2 were read"
                 state["sums"][k & 1] = k
             for _ in range(256 // SOFT):
                 B["oFull", k & 1].arrive()
@@ -220,27 +243,30 @@ def simulate(blocks, rot_q, rot_k, seed):
                     state["V"][s] = x
                     B["vFull", s].complete_tx(2)
             elif kind == "s":
-                s, g, k, last = pl
+                s, sb, g, k, last = pl
                 assert state["Q"][0] == k, "Q kept until the block's S MMAs complete"
-                # S(g) overwrites buffer s only after P V(g - 2) has read P(g - 2)
-                assert state["S"][s] is None or (state["S"][s] == ("P", g - 2) and state["pv_done"] >= g - 2)
-                state["S"][s] = ("S", g)
+                # S(g) overwrites buffer sb only after P V of the chunk one ring
+                # turn before has read the P in it
+                assert state["S"][sb] is None or (state["S"][sb] == ("P", g - sbufs)
+                                                  and state["pv_done"] >= g - sbufs)
+                state["S"][sb] = ("S", g)
                 B["kEmpty", s].arrive()      # the commits after S(g)
-                B["sFull", s].arrive()
+                B["sFull", sb].arrive()
                 if last:
                     B["qEmpty"].arrive()
             else:
-                s, g, k, c = pl
-                ob = state["O"][k & 1]
-                assert (c == 0) or ob == (k, c - 1), "P V in chunk order within the block"
-                state["O"][k & 1] = (k, c)
-                assert state["S"][s] == ("P", g), "P kept until its P V completes"
+                s, sb, g, k, c = pl
+                ob = k % obufs
+                prev = state["O"][ob]
+                assert (c == 0) or prev == (k, c - 1), "P V in chunk order within the block"
+                state["O"][ob] = (k, c)
+                assert state["S"][sb] == ("P", g), "P kept until its P V completes"
                 state["pv_done"] = g
                 B["vEmpty", s].arrive()      # the commits after P V(g)
-                B["pEmpty", s].arrive()
-                B["sEmpty", s].arrive()      # S buffer s free for S(g + 2)
+                B["pEmpty", sb].arrive()
+                B["sEmpty", sb].arrive()     # S buffer sb free again
                 if c == blocks[k] - 1:
-                    B["oReady", k & 1].arrive()
+                    B["oReady", ob].arrive()
             continue
         assert runnable, "deadlock"
         i = rng.choice(runnable)
@@ -256,11 +282,12 @@ def simulate(blocks, rot_q, rot_k, seed):
     assert state["pv_done"] == len(seq) - 1
 
 
-BLOCKS = [[1], [3], [8], [1, 1, 1], [3, 2, 4], [8, 8, 6, 8], [2, 5, 1, 7, 3]]
+BLOCKS = [[1], [3], [8], [1, 1, 1], [3, 2, 4], [8, 8, 6, 8], [2, 5, 1, 7, 3], [1, 2, 1, 2, 1]]
 
 
+@pytest.mark.parametrize("sbufs", [3, 2])
 @pytest.mark.parametrize("blocks", BLOCKS, ids=[str(b) for b in BLOCKS])
 @pytest.mark.parametrize("mode", ["none", "q", "qk"])
-def test_pipeline_protocol(blocks, mode):
+def test_pipeline_protocol(blocks, mode, sbufs):
     for seed in range(40):
-        simulate(blocks, mode != "none", mode == "qk", seed * 7919 + len(blocks))
+        simulate(blocks, mode != "none", mode == "qk", seed * 7919 + len(blocks), sbufs)

@@ -45,8 +45,10 @@ class Config:
         self.OFF_Q, self.OFF_K = 0, 2 * Q_CB
         self.OFF_V = self.OFF_K + 2 * self.KV_SLOT
         self.OFF_RED = self.OFF_V + 2 * self.KV_SLOT
-        self.COL_S = 128            # S buffer s at column s * 128
-        self.COL_O = 256
+        self.SBUFS = 3              # S buffers: b at column b * 128
+        self.COL_S = 128
+        self.COL_O = 384            # the O buffer
+        self.OBUFS = 1
         self.TMEM_COLS = 512
 
 
@@ -147,13 +149,14 @@ def test_shared_memory_layout(cfg):
     # the TMEM address
     total = c.OFF_RED + 4 * c.PARTS * TC_M * 4 + 4 * c.THREADS * 8 + 26 * 8 + 16 + 1024
     assert c.CTAS * (total + 1024) <= 228 * 1024          # 1 KB reserved per CTA
-    assert c.TC_N <= c.COL_S and c.COL_S + c.TC_N <= c.COL_O and c.COL_O + 128 <= c.TMEM_COLS
+    assert c.TC_N <= c.COL_S and (c.SBUFS - 1) * c.COL_S + c.TC_N <= c.COL_O
+    assert c.SBUFS * c.COL_S <= c.COL_O and c.COL_O + 128 * c.OBUFS <= c.TMEM_COLS
 
 
 def check_block(cfg, T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
     TC_N, THREADS, PARTS = cfg.TC_N, cfg.THREADS, cfg.PARTS
     KV_CB, OFF_Q, OFF_K, OFF_V = cfg.KV_CB, cfg.OFF_Q, cfg.OFF_K, cfg.OFF_V
-    COL_O, COL_S, KV_SLOT = cfg.COL_O, cfg.COL_S, cfg.KV_SLOT
+    COL_O, COL_S, KV_SLOT, SBUFS = cfg.COL_O, cfg.COL_S, cfg.KV_SLOT, cfg.SBUFS
     t0, h0, w0 = bt * QT, bh * QH, bw * QW
     rt0 = na_start(t0, T, kt)
     rt1 = na_start(min(t0 + 1, T - 1), T, kt) + kt
@@ -206,7 +209,8 @@ def check_block(cfg, T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
         zeroed = set(range(box_rows, box_rows + pad))
         assert all(r < TC_N for r in zeroed) and not zeroed & set(range(box_rows))
         assert set(range(box_rows, N)) <= zeroed
-        slot = c & 1   # ring slot of the chunk's K and V tiles and S buffer
+        slot = c & 1   # ring slot of the chunk's K and V tiles
+        sb = c % SBUFS  # its S buffer
         ks_base, vs_base = OFF_K + slot * KV_SLOT, OFF_V + slot * KV_SLOT
         # S = Q K^T: eight k16 steps; A reads 128 rows of 32 bytes at koff in
         # column block ks / 4, B reads N rows likewise
@@ -221,12 +225,12 @@ def check_block(cfg, T, H, W, kt, kh, kw, bt, bh, bw, heads=3):
         # MN-major operand: 16 keys (2 groups of 8 rows, SBO = 1024) x 128
         # channels (2 column blocks, LBO = KV_CB)
         for s in range(N // 16):
-            pcol = slot * COL_S + 8 * s
-            assert slot * COL_S <= pcol and pcol + 8 <= slot * COL_S + TC_N // 2
+            pcol = sb * COL_S + 8 * s
+            assert sb * COL_S <= pcol and pcol + 8 <= sb * COL_S + TC_N // 2
             va = vs_base + s * 2048
             assert vs_base <= va and va + 1024 + 1024 + KV_CB <= vs_base + KV_SLOT
-        # S buffer `slot` holds columns [slot * COL_S, + N), clear of the other and of O
-        assert slot * COL_S + N <= (slot + 1) * COL_S <= COL_O
+        # S buffer `sb` holds columns [sb * COL_S, + N), clear of the others and of O
+        assert sb * COL_S + N <= (sb + 1) * COL_S <= COL_O
         # the softmax: thread part qq of a row reads columns [qq * 56, + 56) of
         # its S buffer (columns past the chunk's keys masked) and writes the
         # weights of all 56 as 28 bf16 pairs from column qq * 28 (16 + 8 + 4
