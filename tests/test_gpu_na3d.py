@@ -230,6 +230,36 @@ def test_rotate_once_rejections():
     tabs.close()
 
 
+@pytest.mark.parametrize("W, kw, want", [(112, 105, 1), (130, 113, 2)], ids=["rows112-tc", "rows120-mma"])
+def test_default_kernel_by_region_row_width(W, kw, want):
+    """The default attention is the tensor-core kernel while a region row,
+    min(W, k_w + 7) keys, fits its 112-key chunk (here exactly: one region
+    row a chunk), and the warp-MMA kernel beyond; both within the bound of
+    the oracle, with the RoPE."""
+    r.rope3d_testing_na3d_kernel(0)
+    B, T, H, heads, split, kernel = 1, 2, 5, 1, (32, 48, 48), (1, 3, kw)
+    shape6 = (B, T, H, W, heads, 128)
+    n = int(np.prod(shape6))
+    q_np, k_np, v_np = (synthetic.normal(n, 1.0, 308, i, "bf16") for i in range(3))
+    shp = (B, T * H * W, heads, 128)
+    q, k, v = (bf16(a).reshape(shp).to(DEV) for a in (q_np, k_np, v_np))
+    tabs = r.rope3d_build_tables(T, H, W, split)
+    out = r.rope3d_na3d(q, k, v, tabs, kernel)
+    torch.cuda.synchronize()
+    assert r.rope3d_testing_na3d_last_kernel() == want
+    got = to_f64(out).reshape(shape6)
+    otabs = oracle.tables(T, H, W, split)
+    ref = oracle.rope_na3d(q_np, k_np, v_np, shape6, split, otabs, kernel)
+    to64 = lambda b: (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)  # noqa: E731
+    qr = oracle.rope3d(q_np, shape6, split, otabs)
+    kr = oracle.rope3d(k_np, shape6, split, otabs)
+    absv = oracle.na3d(to64(qr), to64(kr), np.abs(to64(v_np)), shape6, kernel)
+    bound = 2.0 ** -7 * absv + 2.0 ** -8 * np.abs(ref) + 1e-6
+    err = np.abs(got - ref)
+    assert np.all(err <= bound), (err.max(), (err / bound).max())
+    tabs.close()
+
+
 def test_single_key_window_returns_v():
     B, T, H, W, heads = 1, 2, 9, 10, 3
     shp = (B, T * H * W, heads, 128)
