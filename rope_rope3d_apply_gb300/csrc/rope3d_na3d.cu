@@ -809,9 +809,10 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 //     by more than 2^kLazy; O in tensor memory is rescaled then); the bf16
 //     weights are written back into the S buffer they came from (over the S
 //     values, as bf16 pairs), where the P V MMA reads them as its A operand.
-// Q stays in shared memory for every chunk of its block.
+// Q stays in shared memory for every chunk of its block; the next block's Q
+// is written into the other buffer meanwhile.
 // Shared memory (bytes; every tile 1024-aligned, the swizzle's period):
-//   Q  [2 column blocks][128 rows][128 B]               32,768
+//   Q  [2 buffers][2 column blocks][128 rows][128 B]    65,536
 //   K  [2 slots][2 column blocks][kTcN rows][128 B]     57,344
 //   V  [2 slots][2 column blocks][kTcN rows][128 B]     57,344
 //   row maxima and sums of the row's two threads, the softmax threads' window
@@ -823,20 +824,21 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 // first P V waits for the Q warps to have read the previous block's O out).
 // Tensor memory (all 512 columns: one CTA per SM): S in [0, 128) and
 // [128, 256), O in [256, 384).
-constexpr int kTcThreads = 512;              // 16 warps: K TMA, P V MMA, S MMA, V TMA, 4 Q, 8 softmax
+constexpr int kTcParts = 2;                  // softmax threads per query row
 constexpr int kTcSoftWarp0 = 8;              // first softmax warp
 constexpr int kTcRotThreads = 128;           // warps 4-7
-constexpr int kTcSoftThreads = 256;          // 2 threads per query row
-constexpr int kTcParts = kTcSoftThreads / 128;
+constexpr int kTcSoftThreads = 128 * kTcParts;
+// 16 warps: K TMA, P V MMA, S MMA, V TMA, 4 Q warps, 8 softmax warps
+constexpr int kTcThreads = 256 + kTcSoftThreads;
 constexpr int kTcM = 128;                    // queries per CTA: 2 x 8 x 8
 constexpr int kTcQT = 2, kTcQH = 8, kTcQW = 8;
 constexpr int kTcN = 112;                    // keys per chunk at most
-constexpr int kTcHalf = kTcN / kTcParts;     // columns of S a softmax thread reads at most
+constexpr int kTcHalf = kTcN / kTcParts;     // columns of a chunk a softmax thread takes
 constexpr uint32_t kTcQCb = kTcM * 128;      // bytes of a column block of Q or P
 constexpr uint32_t kTcKvCb = kTcN * 128;     // bytes of a column block of K or V
 constexpr uint32_t kTcKvSlot = 2 * kTcKvCb;  // bytes of a K or V slot
 constexpr uint32_t kTcOffQ = 0;
-constexpr uint32_t kTcOffK = kTcOffQ + 2 * kTcQCb;
+constexpr uint32_t kTcOffK = kTcOffQ + 4 * kTcQCb;        // two Q buffers (block parity)
 constexpr uint32_t kTcOffV = kTcOffK + 2 * kTcKvSlot;
 // float row maxima [chunk parity][part][128], row sums [block parity][part][128]
 constexpr uint32_t kTcOffRed = kTcOffV + 2 * kTcKvSlot;
@@ -844,7 +846,7 @@ constexpr uint32_t kTcOffRed = kTcOffV + 2 * kTcKvSlot;
 // share them): [offset][part][128] 64-bit words, each thread its own
 constexpr int kTcMaxPF = 4;                                 // offsets kept; more: made per chunk
 constexpr uint32_t kTcOffMask = kTcOffRed + 4 * kTcParts * kTcM * 4;
-constexpr int kTcBars = 28;                                 // mbarriers, then the TMEM address
+constexpr int kTcBars = 30;                                 // mbarriers, then the TMEM address
 constexpr uint32_t kTcOffBar = kTcOffMask + kTcMaxPF * kTcSoftThreads * 8;
 constexpr uint32_t kTcSmem = kTcOffBar + kTcBars * 8 + 16 + 1024;   // + room to align to 1024
 #ifndef NA_TC_SBUFS   // S buffers in tensor memory: 3 (O single) or 2 (O double-buffered)
@@ -1151,6 +1153,8 @@ __device__ __forceinline__ TcBlock tc_block(const NAParams &p, const TcShape &sh
 
 // 128 registers a thread: the four warps a sub-partition holds fill its
 // quarter of the register file
+// 128 registers a thread: the four warps a sub-partition holds fill its
+// quarter of the register file
 template <int kMode>
 __global__ void __launch_bounds__(kTcThreads, 1)
 rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant__ CUtensorMap tmK,
@@ -1171,7 +1175,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     // one per S buffer (chunk % kTcSBufs):
     //   sFull  S written (MMA)         sEmpty  P V done with the P in it (commit)
     //   pFull  P written (256 arrivals) pEmpty  P V done (O updated)
-    // one of each per query block: qReady (the Q tile written, rotated in the
+    // per Q buffer (block parity): qReady (the Q tile written, rotated in the
     // rotating modes; 128 arrivals), qEmpty (the block's S MMAs done with Q);
     // per O buffer b: oReady[b] the block's last P V done (commit), oEmpty[b]
     // O read out (Q warps), so the next block using b may overwrite it; and
@@ -1181,11 +1185,12 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     auto bar = [&](int kind, int slot) { return smem_addr(&bars[2 * kind + slot]); };
     auto sbar = [&](int kind, int b) { return smem_addr(&bars[10 + kTcSBufs * kind + b]); };
     constexpr int kQb = 10 + 4 * kTcSBufs;
-    const uint32_t qReady = smem_addr(&bars[kQb]), qEmpty = smem_addr(&bars[kQb + 1]);
-    auto oReady = [&](int b) { return smem_addr(&bars[kQb + 2 + b]); };
-    auto oEmpty = [&](int b) { return smem_addr(&bars[kQb + 2 + kTcOBufs + b]); };
-    auto oFull = [&](int b) { return smem_addr(&bars[kQb + 2 + 2 * kTcOBufs + b]); };
-    static_assert(kQb + 2 + 2 * kTcOBufs + 2 <= kTcBars, "mbarriers");
+    auto qReady = [&](int b) { return smem_addr(&bars[kQb + b]); };
+    auto qEmpty = [&](int b) { return smem_addr(&bars[kQb + 2 + b]); };
+    auto oReady = [&](int b) { return smem_addr(&bars[kQb + 4 + b]); };
+    auto oEmpty = [&](int b) { return smem_addr(&bars[kQb + 4 + kTcOBufs + b]); };
+    auto oFull = [&](int b) { return smem_addr(&bars[kQb + 4 + 2 * kTcOBufs + b]); };
+    static_assert(kQb + 4 + 2 * kTcOBufs + 2 <= kTcBars, "mbarriers");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long tok = (long long)p.heads * kHD;   // elements per token
@@ -1235,8 +1240,10 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sbar(kind, b)),
                              "r"(counts[kind]) : "memory");
         }
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(qReady), "r"(kTcRotThreads) : "memory");
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(qEmpty) : "memory");
+        for (int b = 0; b < 2; ++b) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(qReady(b)), "r"(kTcRotThreads) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(qEmpty(b)) : "memory");
+        }
         for (int b = 0; b < kTcOBufs; ++b) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(oReady(b)) : "memory");
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(oEmpty(b)), "r"(kTcRotThreads) : "memory");
@@ -1334,7 +1341,8 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             int gc = 0;
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
                 const TcBlock g = tc_block(p, shp, blk);
-                tc_wait(qReady, uint32_t(k) & 1u, dead);
+                tc_wait(qReady(k & 1), uint32_t(k >> 1) & 1u, dead);
+                const uint32_t sQk = sQ + uint32_t(k & 1) * 2 * kTcQCb;   // this block's Q buffer
                 ChunkPos cp = chunk_start(g);
                 for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
                     const int s = gc & 1, sb = gc % kTcSBufs;   // K slot, S buffer
@@ -1347,21 +1355,21 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
 #pragma unroll
                     for (int ks = 0; ks < kHD / 16; ++ks) {
                         const uint32_t koff = (ks & 3) * 32;   // 16 channels = 32 bytes
-                        tc_mma(tmem + sb * kTcColS, tc_sdesc(sQ + (ks >> 2) * kTcQCb + koff, 16, 1024),
+                        tc_mma(tmem + sb * kTcColS, tc_sdesc(sQk + (ks >> 2) * kTcQCb + koff, 16, 1024),
                                tc_sdesc(kt + (ks >> 2) * kTcKvCb + koff, 16, 1024), id, ks > 0);
                     }
                     tc_commit(bar(kEmpty, s));
                     tc_commit(sbar(sFull, sb));
-                    if (c == g.n_chunks - 1) tc_commit(qEmpty);
+                    if (c == g.n_chunks - 1) tc_commit(qEmpty(k & 1));
                 }
             }
         }
     } else if (warp < kTcSoftWarp0) {   // warps 4-7
-        // ---- Q warps: each block's Q tile through registers (read from global
-        // memory and, in the rotating modes, rotated before the previous block
-        // is done with the Q buffer; then written into it in the layout of a
-        // 128-byte-swizzled TMA box); in the mode that rotates K per CTA, each
-        // K tile too, in place once it lands.
+        // ---- Q warps: each block's Q tile, read from global memory (and, in
+        // the rotating modes, rotated) into Q buffer k & 1 in the layout of a
+        // 128-byte-swizzled TMA box, while the previous block still runs on the
+        // other buffer; in the mode that rotates K per CTA, each K tile too, in
+        // place once it lands.
         // Thread rt holds 16-byte vector cv = rt % 16 of query rows
         // rt / 16 + 8 i, i = 0 .. 15: a row is (t, h, w) = (i / 8, i % 8, rt / 16)
         // from the block's corner, so a warp reads two tokens' 256 bytes.
@@ -1410,35 +1418,38 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
                 const TcBlock g = tc_block(p, shp, blk);
                 const int w = g.w0 + qw_off;
-                uint4 qv[16];
+                // Q buffer k & 1, once block k - 2's S MMAs are done with it
+                if (k >= 2) tc_wait(qEmpty(k & 1), uint32_t((k - 2) >> 1) & 1u, dead);
+                unsigned char *qbuf = sm + kTcOffQ + (k & 1) * 2 * kTcQCb;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int t = g.t0 + (i >> 3), h = g.h0 + (i & 7);
-                    qv[i] = make_uint4(0u, 0u, 0u, 0u);   // outside the grid: zeros
-                    if (t < p.T && h < p.H && w < p.W) {
-                        const long long off = (((long long)g.b * p.T + t) * p.H + h) * p.W * tok +
-                                              (long long)w * tok + (long long)g.head * kHD + 8 * cv;
-                        if (bound_ok(off, 8, p.total))
-                            qv[i] = __ldg(reinterpret_cast<const uint4 *>(p.q + off));
-                    }
-                }
-                if constexpr (kMode != kRotNone) {
+                for (int i0 = 0; i0 < 16; i0 += 4) {   // four vectors a round
+                    uint4 qv[4];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = i0; i < i0 + 4; ++i) {
                         const int t = g.t0 + (i >> 3), h = g.h0 + (i & 7);
+                        qv[i - i0] = make_uint4(0u, 0u, 0u, 0u);   // outside the grid: zeros
                         if (t < p.T && h < p.H && w < p.W) {
-                            const int pos = tsg.axis == 0 ? t : (tsg.axis == 1 ? h : w);
-                            qv[i] = rot_vec_at<true>(qv[i], p.tab, tsg, uint32_t(pos), p.tab_len);
+                            const long long off = (((long long)g.b * p.T + t) * p.H + h) * p.W * tok +
+                                                  (long long)w * tok + (long long)g.head * kHD + 8 * cv;
+                            if (bound_ok(off, 8, p.total))
+                                qv[i - i0] = __ldg(reinterpret_cast<const uint4 *>(p.q + off));
                         }
                     }
-                }
-                // the previous block's S MMAs are done with the Q buffer
-                if (k >= 1) tc_wait(qEmpty, uint32_t(k - 1) & 1u, dead);
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    *reinterpret_cast<uint4 *>(sm + kTcOffQ + sw128(uint32_t(qw_off + 8 * i), uint32_t(cv), kTcQCb)) = qv[i];
+                    for (int i = i0; i < i0 + 4; ++i) {
+                        if constexpr (kMode != kRotNone) {
+                            const int t = g.t0 + (i >> 3), h = g.h0 + (i & 7);
+                            if (t < p.T && h < p.H && w < p.W) {
+                                const int pos = tsg.axis == 0 ? t : (tsg.axis == 1 ? h : w);
+                                qv[i - i0] = rot_vec_at<true>(qv[i - i0], p.tab, tsg, uint32_t(pos), p.tab_len);
+                            }
+                        }
+                        *reinterpret_cast<uint4 *>(qbuf + sw128(uint32_t(qw_off + 8 * i), uint32_t(cv), kTcQCb)) =
+                            qv[i - i0];
+                    }
+                }
                 fence_async_smem();
-                mbar_arrive(qReady);
+                mbar_arrive(qReady(k & 1));
                 // the previous block's result: before this block's K tiles, whose
                 // S products may wait for the O buffer through P V
                 if (k >= 1) store_o(g_prev, k - 1);

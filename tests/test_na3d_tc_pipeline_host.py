@@ -82,14 +82,15 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
     for b in range(sbufs):
         for kind, cnt in (("sFull", 1), ("sEmpty", 1), ("pFull", 256), ("pEmpty", 1)):
             B[kind, b] = Bar(cnt)
-    B["qReady"], B["qEmpty"] = Bar(128), Bar(1)
+    for b in (0, 1):         # per Q buffer (block parity): Q written, S MMAs done with it
+        B["qReady", b], B["qEmpty", b] = Bar(128), Bar(1)
     for b in range(obufs):   # per O buffer: last P V done, O read out
         B["oReady", b], B["oEmpty", b] = Bar(1), Bar(128)
     for b in (0, 1):         # per block parity: row sums written
         B["oFull", b] = Bar(256)
     state = {  # what each buffer holds; S buffer b holds ("S", g) then ("P", g)
         "K": [None, None], "V": [None, None], "S": [None] * sbufs,
-        "Q": None,                     # (block, "rot" or "raw") of the Q tile in place
+        "Q": [None, None],             # Q buffer: (block, "rot" or "raw") of the tile in it
         "O": [(-1, -1)] * obufs,       # O buffer: (block, last chunk added)
         "Oread": [-1] * obufs,         # O buffer: last block whose result was read out
         "sums": [-1, -1],              # row-sum buffer (block parity): block whose sums it holds
@@ -130,25 +131,25 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
             s, use = g & 1, g >> 1
             sb, suse = g % sbufs, g // sbufs
             if c == 0:
-                yield ("wait", B["qReady"], k & 1, k)
+                yield ("wait", B["qReady", k & 1], (k >> 1) & 1, k >> 1)
             yield ("wait", B["kReady" if rot_k else "kFull", s], use & 1, use)
             if g >= sbufs:
                 yield ("wait", B["sEmpty", sb], (suse - 1) & 1, suse - 1)
             assert state["K"][s] == (g, "rot" if rot_k else "raw"), "S reads K of its chunk"
-            assert state["Q"] == (k, "rot" if rot_q else "raw"), "S reads Q of its block"
+            assert state["Q"][k & 1] == (k, "rot" if rot_q else "raw"), "S reads Q of its block"
             inflight.append(("s", (s, sb, g, k, c == blocks[k] - 1)))
 
     def q_warp(i):
         g = 0
         for k, n in enumerate(blocks):
-            yield None                 # Q of block k read (and rotated) into registers
-            if k >= 1:                 # the previous block's S MMAs are done with Q
-                yield ("wait", B["qEmpty"], (k - 1) & 1, k - 1)
+            if k >= 2:                 # block k - 2's S MMAs are done with Q buffer k & 1
+                yield ("wait", B["qEmpty", k & 1], ((k - 2) >> 1) & 1, (k - 2) >> 1)
+            yield None                 # Q of block k read (and rotated) and written
             if i == 0:
-                assert state["Q"] is None or state["Q"][0] == k - 1
-                state["Q"] = (k, "rot" if rot_q else "raw")
+                assert state["Q"][k & 1] is None or state["Q"][k & 1][0] == k - 2
+                state["Q"][k & 1] = (k, "rot" if rot_q else "raw")
             for _ in range(32):
-                B["qReady"].arrive()
+                B["qReady", k & 1].arrive()
             if k >= 1:                 # the previous block's result, before this block's K tiles
                 yield from store_o(i, k - 1)
             for c in range(n):
@@ -244,7 +245,7 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
                     B["vFull", s].complete_tx(2)
             elif kind == "s":
                 s, sb, g, k, last = pl
-                assert state["Q"][0] == k, "Q kept until the block's S MMAs complete"
+                assert state["Q"][k & 1][0] == k, "Q kept until the block's S MMAs complete"
                 # S(g) overwrites buffer sb only after P V of the chunk one ring
                 # turn before has read the P in it
                 assert state["S"][sb] is None or (state["S"][sb] == ("P", g - sbufs)
@@ -253,7 +254,7 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
                 B["kEmpty", s].arrive()      # the commits after S(g)
                 B["sFull", sb].arrive()
                 if last:
-                    B["qEmpty"].arrive()
+                    B["qEmpty", k & 1].arrive()
             else:
                 s, sb, g, k, c = pl
                 ob = k % obufs

@@ -42,7 +42,7 @@ class Config:
         self.PARTS = self.THREADS // TC_M
         self.KV_CB = self.TC_N * 128
         self.KV_SLOT = 2 * self.KV_CB
-        self.OFF_Q, self.OFF_K = 0, 2 * Q_CB
+        self.OFF_Q, self.OFF_K = 0, 4 * Q_CB   # two Q buffers (block parity)
         self.OFF_V = self.OFF_K + 2 * self.KV_SLOT
         self.OFF_RED = self.OFF_V + 2 * self.KV_SLOT
         self.SBUFS = 3              # S buffers: b at column b * 128
