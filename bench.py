@@ -787,6 +787,31 @@ def run_neox(args):
 NA3D = dict(B=1, T=16, H=64, W=64, heads=16, split=(32, 48, 48), kernel=(3, 7, 7))
 
 
+def na3d_tc_mma_flops(B, T, H, W, heads, kernel, chunk_keys=112):
+    """The tensor-core attention's issued MMA work: per 2 x 8 x 8 query block,
+    S = Q K^T and O += P V over every chunk of its key region (whole region
+    rows of one frame, rwb = min(W, k_w + 7) keys each, chunk_keys // rwb rows
+    a chunk, the chunk's keys rounded up to 16), 4 * 128 * 128 * N flops a
+    chunk of N keys."""
+    kt, kh, kw = kernel
+
+    def start(i, L, k):
+        s0 = max(i - k // 2, 0)
+        return L - k if s0 + k > L else s0
+
+    rwb = min(W, kw + 7)
+    chb = chunk_keys // rwb
+    total = 0
+    for t0 in range(0, T, 2):
+        frames = start(min(t0 + 1, T - 1), T, kt) + kt - start(t0, T, kt)
+        for h0 in range(0, H, 8):
+            rh0 = start(h0, H, kh)
+            RH = start(min(h0 + 7, H - 1), H, kh) + kh - rh0
+            keys = sum(((min(chb, RH - r0) * rwb + 15) // 16) * 16 for r0 in range(0, RH, chb))
+            total += frames * keys * ((W + 7) // 8)
+    return 4.0 * 128 * 128 * total * B * heads
+
+
 def run_na3d(args):
     """The RoPE fused with the neighbourhood attention, each element of Q and
     K rotated once (rope3d_na3d_rotate_once: the step), against the per-CTA
@@ -859,6 +884,7 @@ def run_na3d(args):
     kt, kh, kw = c["kernel"]
     window = kt * kh * kw
     flops = 4.0 * 128 * window * N * c["heads"] * c["B"]           # q.k and p.v over each window
+    mma_flops = na3d_tc_mma_flops(c["B"], c["T"], c["H"], c["W"], c["heads"], c["kernel"])
     tflops = flops / (ms_once / 1e3) / 1e12
     peak = 1898.6
     try:
@@ -884,6 +910,10 @@ def run_na3d(args):
         "fused_ms": ms_fused, "fused_per_cta_ms": ms_per_cta,
         "attention_only_ms": ms_attention,
         "attention_only_tflops": flops / (ms_attention / 1e3) / 1e12,
+        # the tensor cores' issued work (the whole key region of each query
+        # block), against the same peak: how busy the MMAs are
+        "attention_only_mma_issued_tflops": mma_flops / (ms_attention / 1e3) / 1e12,
+        "attention_only_mma_issued_frac": mma_flops / (ms_attention / 1e3) / 1e12 / peak,
         "clocks": clocks.summary(t0, t1), "gpu_launches": 2 * args.steps,
     }
     print(json.dumps(line), flush=True)

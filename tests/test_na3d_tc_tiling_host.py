@@ -344,3 +344,33 @@ def test_tc_tiling_of_the_benchmark_geometry(cfg):
     picks = [0, 1, 4, 7]
     check_grid(CONFIGS[cfg], 16, 64, 64, 3, 7, 7,
                blocks=[(bt, bh, bw) for bt in (0, 4, 7) for bh in picks for bw in picks])
+
+
+def block_mma_widths(cfg, T, H, W, kt, kh, kw, bt, bh, bw):
+    """The MMA widths (keys rounded up to 16) of one query block's chunks, by
+    the same region and chunk arithmetic as check_block."""
+    t0, h0 = bt * QT, bh * QH
+    rt0 = na_start(t0, T, kt)
+    rt1 = na_start(min(t0 + 1, T - 1), T, kt) + kt
+    rh0 = na_start(h0, H, kh)
+    RH = na_start(min(h0 + QH - 1, H - 1), H, kh) + kh - rh0
+    rwb = min(W, kw + QW - 1)
+    chb = cfg.TC_N // rwb
+    per_frame = (RH + chb - 1) // chb
+    return [(min(chb, RH - (c % per_frame) * chb) * rwb + 15) & ~15 for c in range((rt1 - rt0) * per_frame)]
+
+
+@pytest.mark.parametrize("geom", [(16, 64, 64, 3, 7, 7), (5, 13, 27, 3, 5, 7), (3, 9, 40, 1, 3, 33)])
+def test_bench_mma_flops_match_the_tiling(geom):
+    """bench.py's count of the tensor-core attention's issued MMA work is the
+    sum over every query block's chunks of 4 * 128 * 128 * N."""
+    import bench
+
+    T, H, W, kt, kh, kw = geom
+    cfg = CONFIGS["tc"]
+    nbt, nbh, nbw = (T + QT - 1) // QT, (H + QH - 1) // QH, (W + QW - 1) // QW
+    want = sum(4 * 128 * 128 * n
+               for bt in range(nbt) for bh in range(nbh) for bw in range(nbw)
+               for n in block_mma_widths(cfg, T, H, W, kt, kh, kw, bt, bh, bw))
+    assert bench.na3d_tc_mma_flops(1, T, H, W, 1, (kt, kh, kw)) == want
+    assert bench.na3d_tc_mma_flops(2, T, H, W, 3, (kt, kh, kw)) == 6 * want
