@@ -111,6 +111,27 @@ def workload_config(w: synthetic.Workload) -> dict:
     }
 
 
+def host_link_gbs(torch, dev, h_in, h_out, d_in, d_out, reps=5):
+    """`reps` rounds of raw copies: the pinned host inputs to device buffers on
+    one stream while the device outputs go to pinned host buffers on another;
+    per round, bytes moved both ways over the round's time (GB/s)."""
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    nbytes = sum(t.numel() * t.element_size() for t in h_in) + sum(t.numel() * t.element_size() for t in h_out)
+    rounds = []
+    for _ in range(reps):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(s_in):
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for h, d in zip(h_out, d_out):
+                h.copy_(d, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        rounds.append(nbytes / (time.perf_counter() - t0) / 1e9)
+    return rounds
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -596,15 +617,29 @@ def run_ours(args, w):
         r.rope3d_apply_pair_host(hq, hk, hqo, hko, tabs)  # warm-up: staging allocation
         if dist:
             dist.barrier()
-        t0 = time.perf_counter()
+        stamps = [time.perf_counter()]
         for _ in range(args.e2e_steps):
             r.rope3d_apply_pair_host(hq, hk, hqo, hko, tabs)
-        e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
+            stamps.append(time.perf_counter())
+        e2e_s = max_over_ranks(stamps[-1] - stamps[0], dist, dev)
+        step_gbs = sorted(world * bytes_step / (b - a) / 1e9 for a, b in zip(stamps, stamps[1:]))
         e2e = {"value": world * args.e2e_steps * bytes_step / e2e_s / 1e9, "unit": UNIT,
                "h2d_bytes_per_step": 2 * w.numel * w.elem_bytes,
                "d2h_bytes_per_step": 2 * w.numel * w.elem_bytes,
-               "steps": args.e2e_steps, "api": "rope3d_apply_pair_host (pinned host buffers)"}
+               "steps": args.e2e_steps, "api": "rope3d_apply_pair_host (pinned host buffers)",
+               "step_values": {"min": step_gbs[0], "median": statistics.median(step_gbs),
+                               "max": step_gbs[-1]}}
         r.rope3d_release_scratch()
+        # The host link right after (it stalls at random moments on some boxes):
+        # raw concurrent copies of the same bytes, Q and K in, both outputs out.
+        dq, dk, dqo, dko = (t.view(torch.uint8).reshape(-1) for t in sets[0])
+        link = sorted(host_link_gbs(torch, dev, host[:2], host[2:], (dq, dk), (dqo, dko)))
+        copied = e2e["h2d_bytes_per_step"] + e2e["d2h_bytes_per_step"]
+        e2e["host_link_gbs"] = {"min": link[0], "median": statistics.median(link), "max": link[-1],
+                                "rounds": len(link)}
+        # copies of the median step against the link's median round
+        e2e["frac_of_host_link"] = (statistics.median(step_gbs) / world * copied / bytes_step
+                                    / statistics.median(link))
 
     if rank == 0:
         line = {

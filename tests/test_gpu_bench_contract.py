@@ -45,6 +45,12 @@ def test_gpu_arm_line_has_every_contract_field():
     e2e = d["e2e"]
     assert e2e["value"] > 0 and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+    sv, link = e2e["step_values"], e2e["host_link_gbs"]
+    assert 0 < sv["min"] <= sv["median"] <= sv["max"]
+    assert 0 < link["min"] <= link["median"] <= link["max"] and link["rounds"] >= 3
+    # the whole-run value lies within its steps' spread
+    assert sv["min"] * (1 - 1e-9) <= e2e["value"] <= sv["max"] * (1 + 1e-9)
+    assert e2e["frac_of_host_link"] > 0
     for key in ("sm_mhz", "sm_max_mhz", "reasons"):
         assert key in d["clocks"], key
     assert d["gpu_launches"] >= d["steps"]
