@@ -1133,13 +1133,27 @@ struct TcBlock {
     int per_frame, n_chunks;
 };
 
-__device__ __forceinline__ TcBlock tc_block(const NAParams &p, const TcShape &shp, int blk) {
+// The block index's divisors (blocks along W, H, T, heads) as multiply-high
+// constants, made once per thread: every role walks the blocks.
+struct TcDivs {
+    rope3d::FastDiv nbw, nbh, nbt, heads;
+};
+
+__device__ __forceinline__ TcBlock tc_block(const NAParams &p, const TcShape &shp, const TcDivs &dv,
+                                            int blk) {
     TcBlock g;
-    g.w0 = (blk % p.nbw) * kTcQW; blk /= p.nbw;
-    g.h0 = (blk % p.nbh) * kTcQH; blk /= p.nbh;
-    g.t0 = (blk % shp.nbt) * kTcQT; blk /= shp.nbt;
-    g.head = blk % p.heads;
-    g.b = blk / p.heads;
+    uint32_t b = uint32_t(blk), q = fdiv(b, dv.nbw);
+    g.w0 = int(b - q * dv.nbw.d) * kTcQW;
+    b = q;
+    q = fdiv(b, dv.nbh);
+    g.h0 = int(b - q * dv.nbh.d) * kTcQH;
+    b = q;
+    q = fdiv(b, dv.nbt);
+    g.t0 = int(b - q * dv.nbt.d) * kTcQT;
+    b = q;
+    q = fdiv(b, dv.heads);
+    g.head = int(b - q * dv.heads.d);
+    g.b = int(q);
     g.rt0 = na_start(g.t0, p.T, p.kt);
     const int rt1 = na_start(min(g.t0 + 1, p.T - 1), p.T, p.kt) + p.kt;
     g.rh0 = na_start(g.h0, p.H, p.kh);
@@ -1196,6 +1210,8 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     const long long tok = (long long)p.heads * kHD;   // elements per token
     const int rwb = shp.rwb, chb = shp.chb;          // RW <= rwb, chb * rwb <= kTcN
     const rope3d::FastDiv rwd = fastdiv_make_dev(uint32_t(rwb));
+    const TcDivs dv{fastdiv_make_dev(uint32_t(p.nbw)), fastdiv_make_dev(uint32_t(p.nbh)),
+                    fastdiv_make_dev(uint32_t(shp.nbt)), fastdiv_make_dev(uint32_t(p.heads))};
     const uint32_t box_bytes = uint32_t(2 * 128 * rwb * chb);   // both column blocks
 
     // The chunks of block g in order: frame f, region rows [r0, r0 + nr);
@@ -1290,7 +1306,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 if (!v) asm volatile("griddepcontrol.wait;" ::: "memory");
             int gc = 0;   // chunks of the CTA so far
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
-                const TcBlock g = tc_block(p, shp, blk);
+                const TcBlock g = tc_block(p, shp, dv, blk);
                 ChunkPos cp = chunk_start(g);
                 for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
                     const int s = gc & 1;
@@ -1308,7 +1324,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             int gc = 0;
             const uint32_t id = tc_idesc(kTcM, kHD, 1);
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
-                const TcBlock g = tc_block(p, shp, blk);
+                const TcBlock g = tc_block(p, shp, dv, blk);
                 const int ob = k % kTcOBufs;
                 const uint32_t o_col = tmem + kTcColO + uint32_t(ob) * 128;
                 // O buffer ob once the Q warps have read the previous result in it
@@ -1340,7 +1356,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         if (lane == 0) {
             int gc = 0;
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
-                const TcBlock g = tc_block(p, shp, blk);
+                const TcBlock g = tc_block(p, shp, dv, blk);
                 tc_wait(qReady(k & 1), uint32_t(k >> 1) & 1u, dead);
                 const uint32_t sQk = sQ + uint32_t(k & 1) * 2 * kTcQCb;   // this block's Q buffer
                 ChunkPos cp = chunk_start(g);
@@ -1416,7 +1432,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             };
             TcBlock g_prev{};
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
-                const TcBlock g = tc_block(p, shp, blk);
+                const TcBlock g = tc_block(p, shp, dv, blk);
                 const int w = g.w0 + qw_off;
                 // Q buffer k & 1, once block k - 2's S MMAs are done with it
                 if (k >= 2) tc_wait(qEmpty(k & 1), uint32_t((k - 2) >> 1) & 1u, dead);
@@ -1486,8 +1502,10 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         const int row = 32 * lg + lane;
         const uint32_t lanes = uint32_t(32 * lg) << 16;
         int gc = 0;
+        // the window geometry the masks in shared memory were made for
+        int mk_ah = -1, mk_clo = -1, mk_chi = -1, mk_rh = -1;
         for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
-            const TcBlock g = tc_block(p, shp, blk);
+            const TcBlock g = tc_block(p, shp, dv, blk);
             const int qt = g.t0 + (row >> 6), qh = g.h0 + ((row >> 3) & 7), qw = g.w0 + (row & 7);
             const bool row_ok = qt < p.T && qh < p.H && qw < p.W;
             const int st_q = na_start(min(qt, p.T - 1), p.T, p.kt);
@@ -1513,10 +1531,17 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 return m;
             };
             uint64_t *wmask = reinterpret_cast<uint64_t *>(sm + kTcOffMask) + (qq * kTcM + row);
+            // A mask depends on the row's window in the region and the region's
+            // height only, so blocks that share them (every interior block of
+            // the grid) keep the masks of the block before.
             const bool kept = g.per_frame <= kTcMaxPF;
-            if (kept) {
+            if (kept && (ah != mk_ah || clo != mk_clo || chi != mk_chi || g.RH != mk_rh)) {
                 for (int pf = 0, r0 = 0; pf < g.per_frame; ++pf, r0 += chb)
                     wmask[pf * kTcSoftThreads] = window_mask(r0, min(chb, g.RH - r0));
+                mk_ah = ah;
+                mk_clo = clo;
+                mk_chi = chi;
+                mk_rh = g.RH;
             }
 
             ChunkPos cp = chunk_start(g);
