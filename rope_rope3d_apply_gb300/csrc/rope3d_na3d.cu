@@ -825,6 +825,7 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 // Tensor memory (all 512 columns: one CTA per SM): S in [0, 128) and
 // [128, 256), O in [256, 384).
 constexpr int kTcParts = 2;                  // softmax threads per query row
+constexpr int kTcQBar = 5;                   // named barrier of the Q warps (1-4: softmax pairs)
 constexpr int kTcSoftWarp0 = 8;              // first softmax warp
 constexpr int kTcRotThreads = 128;           // warps 4-7
 constexpr int kTcSoftThreads = 128 * kTcParts;
@@ -950,6 +951,25 @@ __device__ __forceinline__ void tma_load5(uint32_t dst, const CUtensorMap *map, 
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
           "r"(c4), "r"(bar)
         : "memory");
+}
+
+// A 5-D tile store from shared memory (a bulk group of this thread), its
+// commit, and the waits for the group's shared-memory reads or its completion.
+__device__ __forceinline__ void tma_store5(const CUtensorMap *map, uint32_t src, int c0, int c1,
+                                           int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4, %5}], [%6];"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(src)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Wait for phase `parity` of an mbarrier for at most ~0.1 s of SM clocks.
@@ -1172,7 +1192,7 @@ __device__ __forceinline__ TcBlock tc_block(const NAParams &p, const TcShape &sh
 template <int kMode>
 __global__ void __launch_bounds__(kTcThreads, 1)
 rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV) {
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO) {
     extern __shared__ unsigned char tc_raw[];
     unsigned char *sm = tc_raw + ((1024u - (smem_addr(tc_raw) & 1023u)) & 1023u);
     const uint32_t sQ = smem_addr(sm + kTcOffQ), sK = smem_addr(sm + kTcOffK);
@@ -1269,6 +1289,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmO)) : "memory");
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -1392,14 +1413,20 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         // They also write each block's result: once its last P V is done and
         // the softmax threads have left their row sums, each thread takes the
         // row of tensor memory lane 32 (warp % 4) + lane (the lanes its warp
-        // reaches), normalises its 128 channels and stores them, while the
-        // softmax threads already work on the next block.
+        // reaches) and normalises its 128 channels, while the softmax threads
+        // already work on the next block. The rows go into the block's own Q
+        // buffer (its S products are done) in the TMA box layout, O is handed
+        // back, and two TMA stores write the tile; the buffer takes the block
+        // after next's Q once the stores have read it. A block whose frame pair
+        // passes the grid's last frame (odd T) is stored row by row instead:
+        // the tensor map's frame axis runs on into the next batch.
         {
             const int rt = tid - 128;   // 0 .. kTcRotThreads - 1
             const int cv = rt & 15, qw_off = rt >> 4;
             [[maybe_unused]] const TabSlot tsg = tab_slot_global(p.pT, p.pH, p.pW, p.offH, p.offW, cv);
             [[maybe_unused]] int gc = 0;
             const int orow = 32 * (warp & 3) + lane;   // the O row this thread stores
+            bool o_pending = false;   // a TMA store of O may still read a Q buffer
             auto store_o = [&](const TcBlock &g, int k) {
                 const int b = k & 1, ob = k % kTcOBufs;   // row-sum and O buffers
                 tc_wait(oReady(ob), uint32_t(k / kTcOBufs) & 1u, dead);
@@ -1414,6 +1441,8 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 const long long base = ((((long long)g.b * p.T + qt) * p.H + qh) * p.W + qw) * tok +
                                        (long long)g.head * kHD;
                 const uint32_t tO = tmem + kTcColO + uint32_t(ob) * 128 + (uint32_t(32 * (warp & 3)) << 16);
+                const bool tma_o = g.t0 + kTcQT <= p.T;
+                unsigned char *stg = sm + kTcOffQ + (k & 1) * 2 * kTcQCb;
 #pragma unroll 1
                 for (int h2 = 0; h2 < kHD / 16; ++h2) {
                     float o[16];
@@ -1421,7 +1450,12 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                     uint32_t packed[8];
 #pragma unroll
                     for (int i = 0; i < 16; i += 2) packed[i / 2] = pack_bf16(o[i] * inv, o[i + 1] * inv);
-                    if (ok && bound_ok(base + 16 * h2, 16, p.total)) {
+                    if (tma_o) {   // 16-byte vectors 2 h2 and 2 h2 + 1 of the row
+                        *reinterpret_cast<uint4 *>(stg + sw128(uint32_t(orow), uint32_t(2 * h2), kTcQCb)) =
+                            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        *reinterpret_cast<uint4 *>(stg + sw128(uint32_t(orow), uint32_t(2 * h2 + 1), kTcQCb)) =
+                            make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                    } else if (ok && bound_ok(base + 16 * h2, 16, p.total)) {
                         uint4 *dst = reinterpret_cast<uint4 *>(p.out + base + 16 * h2);
                         dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
                         dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
@@ -1429,13 +1463,35 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 }
                 tc_fence_before();   // the reads of O, before the buffer is handed back
                 mbar_arrive(oEmpty(ob));
+                if (tma_o) {
+                    fence_async_smem();   // the staged rows, to the tensor copies
+                    asm volatile("bar.sync %0, %1;" ::"n"(kTcQBar), "n"(kTcRotThreads) : "memory");
+                    if (rt == 0) {
+                        const uint32_t src = smem_addr(stg);
+                        const int frame = g.b * p.T + g.t0;
+                        tma_store5(&tmO, src, 0, g.head, g.w0, g.h0, frame);
+                        tma_store5(&tmO, src + kTcQCb, 64, g.head, g.w0, g.h0, frame);
+                        bulk_commit();
+                    }
+                    o_pending = true;
+                }
+            };
+            // before a Q buffer is written: the TMA stores that read it are done
+            auto o_reads_done = [&]() {
+                if (o_pending) {
+                    if (rt == 0) bulk_wait_read_all();
+                    asm volatile("bar.sync %0, %1;" ::"n"(kTcQBar), "n"(kTcRotThreads) : "memory");
+                    o_pending = false;
+                }
             };
             TcBlock g_prev{};
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
                 const TcBlock g = tc_block(p, shp, dv, blk);
                 const int w = g.w0 + qw_off;
                 // Q buffer k & 1, once block k - 2's S MMAs are done with it
+                // and the TMA stores of block k - 2's O have read it
                 if (k >= 2) tc_wait(qEmpty(k & 1), uint32_t((k - 2) >> 1) & 1u, dead);
+                o_reads_done();
                 unsigned char *qbuf = sm + kTcOffQ + (k & 1) * 2 * kTcQCb;
 #pragma unroll
                 for (int i0 = 0; i0 < 16; i0 += 4) {   // four vectors a round
@@ -1495,6 +1551,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             const int nblk = shp.total > int(blockIdx.x)
                                  ? (shp.total - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x) : 0;
             if (nblk >= 1) store_o(g_prev, nblk - 1);
+            if (rt == 0) bulk_wait_all();   // the last stores, before the CTA ends
         }
     } else {
         // ---- softmax warps: this thread's query row and column part
@@ -1977,9 +2034,10 @@ int na3d_launch_rotate_once(NAParams &p, const void *k, void *k_rot, const rope3
     const bool tc = na3d_use_tc(p);
     g_na3d_last_kernel = tc ? 1 : 2;
     const TcShape shp = na3d_tc_shape(p);
-    CUtensorMap mk{}, mv{};
+    CUtensorMap mk{}, mv{}, mo{};
     if (tc && (!na3d_tc_attribute<kRotQ>() || !na3d_tc_map(&mk, p.k, p, shp.rwb, shp.chb, 1) ||
-               !na3d_tc_map(&mv, p.v, p, shp.rwb, shp.chb, 1)))
+               !na3d_tc_map(&mv, p.v, p, shp.rwb, shp.chb, 1) ||
+               !na3d_tc_map(&mo, p.out, p, kTcQW, kTcQH, kTcQT)))
         return ROPE3D_ERR_CUDA;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(tc ? na3d_tc_grid(shp) : na3d_blocks(p));
@@ -1991,7 +2049,7 @@ int na3d_launch_rotate_once(NAParams &p, const void *k, void *k_rot, const rope3
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t le = tc ? cudaLaunchKernelEx(&cfg, rope3d_na3d_tc_kernel<kRotQ>, p, shp, mk, mv)
+    const cudaError_t le = tc ? cudaLaunchKernelEx(&cfg, rope3d_na3d_tc_kernel<kRotQ>, p, shp, mk, mv, mo)
                               : cudaLaunchKernelEx(&cfg, rope3d_na3d_kernel<kRotQ>, p);
     if (le != cudaSuccess) {
         cudaGetLastError();
@@ -2081,15 +2139,16 @@ extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *ou
     g_na3d_last_kernel = na3d_use_tc(p) ? 1 : 2;
     if (na3d_use_tc(p)) {
         const TcShape shp = na3d_tc_shape(p);
-        CUtensorMap mk, mv;
-        if (!na3d_tc_map(&mk, p.k, p, shp.rwb, shp.chb, 1) || !na3d_tc_map(&mv, p.v, p, shp.rwb, shp.chb, 1))
+        CUtensorMap mk, mv, mo;
+        if (!na3d_tc_map(&mk, p.k, p, shp.rwb, shp.chb, 1) || !na3d_tc_map(&mv, p.v, p, shp.rwb, shp.chb, 1) ||
+            !na3d_tc_map(&mo, p.out, p, kTcQW, kTcQH, kTcQT))
             return ROPE3D_ERR_CUDA;
         if (apply_rope) {
             if (!na3d_tc_attribute<kRotQK>()) return ROPE3D_ERR_CUDA;
-            rope3d_na3d_tc_kernel<kRotQK><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv);
+            rope3d_na3d_tc_kernel<kRotQK><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv, mo);
         } else {
             if (!na3d_tc_attribute<kRotNone>()) return ROPE3D_ERR_CUDA;
-            rope3d_na3d_tc_kernel<kRotNone><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv);
+            rope3d_na3d_tc_kernel<kRotNone><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv, mo);
         }
     } else {
         if (!na3d_attributes()) return ROPE3D_ERR_CUDA;

@@ -88,6 +88,9 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
         B["oReady", b], B["oEmpty", b] = Bar(1), Bar(128)
     for b in (0, 1):         # per block parity: row sums written
         B["oFull", b] = Bar(256)
+    for b in (0, 1):         # per Q buffer: the TMA store of O staged in it has read it
+        B["ostore", b] = Bar(1)
+    B["qbar"] = Bar(4)       # the Q warps' named barrier (one arrival per modelled warp)
     state = {  # what each buffer holds; S buffer b holds ("S", g) then ("P", g)
         "K": [None, None], "V": [None, None], "S": [None] * sbufs,
         "Q": [None, None],             # Q buffer: (block, "rot" or "raw") of the tile in it
@@ -96,11 +99,14 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
         "sums": [-1, -1],              # row-sum buffer (block parity): block whose sums it holds
         "sums_read": [-1, -1],         # row-sum buffer: last block whose sums were read
         "pv_done": -1,                 # last chunk whose P V completed
+        "s_done": -1,                  # last chunk whose S MMAs completed
+        "staged": [0, 0],              # Q buffer: warps that wrote their O rows into it
     }
     inflight = []                      # asynchronous events: (kind, payload)
     SOFT = 4                           # softmax threads modelled (arrivals scaled)
     # global chunk g -> (block k, chunk c)
     seq = [(k, c) for k, n in enumerate(blocks) for c in range(n)]
+    last_g = [sum(blocks[:k + 1]) - 1 for k in range(len(blocks))]
 
     def producer(kind):   # the K thread and the V thread, each over its own ring
         for g in range(len(seq)):
@@ -141,17 +147,20 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
 
     def q_warp(i):
         g = 0
+        ws = {"qb": 0, "ost": [0, 0], "pending": None}
         for k, n in enumerate(blocks):
             if k >= 2:                 # block k - 2's S MMAs are done with Q buffer k & 1
                 yield ("wait", B["qEmpty", k & 1], ((k - 2) >> 1) & 1, (k - 2) >> 1)
+            yield from o_reads_done(i, ws)   # and the TMA store of its O has read it
             yield None                 # Q of block k read (and rotated) and written
             if i == 0:
-                assert state["Q"][k & 1] is None or state["Q"][k & 1][0] == k - 2
+                assert state["Q"][k & 1] is None or state["Q"][k & 1] == (k - 2, "Oread"), \
+                    "a Q buffer is rewritten only after the O staged in it was stored"
                 state["Q"][k & 1] = (k, "rot" if rot_q else "raw")
             for _ in range(32):
                 B["qReady", k & 1].arrive()
             if k >= 1:                 # the previous block's result, before this block's K tiles
-                yield from store_o(i, k - 1)
+                yield from store_o(i, k - 1, ws)
             for c in range(n):
                 if rot_k:
                     s, use = g & 1, g >> 1
@@ -163,21 +172,52 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
                         B["kReady", s].arrive()
                 g += 1
                 yield None
-        yield from store_o(i, len(blocks) - 1)
+        yield from store_o(i, len(blocks) - 1, ws)
+        if i == 0:                     # the last store, before the CTA ends
+            b = ws["pending"] & 1
+            u = ws["ost"][b]
+            ws["ost"][b] += 1
+            yield ("wait", B["ostore", b], u & 1, u)
 
-    def store_o(i, k):
+    def qbar(ws):                      # bar.sync among the four Q warps
+        B["qbar"].arrive()
+        n = ws["qb"]
+        ws["qb"] += 1
+        yield ("wait", B["qbar"], n & 1, n)
+
+    def o_reads_done(i, ws):
+        if ws["pending"] is not None:
+            b = ws["pending"] & 1
+            if i == 0:                 # the thread that committed the store waits for its reads
+                u = ws["ost"][b]
+                ws["ost"][b] += 1
+                yield ("wait", B["ostore", b], u & 1, u)
+            yield from qbar(ws)
+            ws["pending"] = None
+
+    def store_o(i, k, ws):
         b, ob = k & 1, k % obufs
         u = k // obufs
         yield ("wait", B["oReady", ob], u & 1, u)
         yield ("wait", B["oFull", b], (k >> 1) & 1, k >> 1)
         assert state["O"][ob] == (k, blocks[k] - 1), "the block's O is complete"
         assert state["sums"][b] == k, "its row sums are written"
-        yield None                        # O read, normalised, stored
+        # this warp's rows of O, normalised, into the block's own Q buffer
+        assert state["s_done"] >= last_g[k], "the block's S MMAs no longer read its Q buffer"
+        assert state["Q"][b] in ((k, "rot"), (k, "raw"), (k, "O")), "the Q buffer still holds block k"
+        state["Q"][b] = (k, "O")
+        state["staged"][b] += 1
+        yield None
         if i == 0:
             state["Oread"][ob] = k
             state["sums_read"][b] = k
         for _ in range(32):
             B["oEmpty", ob].arrive()
+        yield from qbar(ws)            # every warp's rows staged
+        if i == 0:
+            assert state["staged"][b] == 4, "the store reads all rows"
+            inflight.append(("tmao", (k,)))
+        ws["pending"] = k
 
     def softmax(i):
         g = 0
@@ -226,14 +266,22 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
                     if waiting[i] is None or waiting[i][0].ready(waiting[i][1], waiting[i][2])]
         if inflight and (not runnable or rng.random() < 0.4):
             kinds = [kd for kd, _ in inflight]
-            if "tma" in kinds and (rng.random() < 0.5 or all(kd == "tma" for kd in kinds)):
-                tma_idx = [j for j, kd in enumerate(kinds) if kd == "tma"]
+            if any(kd in ("tma", "tmao") for kd in kinds) and (
+                    rng.random() < 0.5 or all(kd in ("tma", "tmao") for kd in kinds)):
+                tma_idx = [j for j, kd in enumerate(kinds) if kd in ("tma", "tmao")]
                 idx = rng.choice(tma_idx)
             else:   # each issuer's MMAs complete in its issue order
                 first = [next((j for j, kd in enumerate(kinds) if kd == want), None) for want in ("s", "pv")]
                 idx = rng.choice([j for j in first if j is not None])
             kind, pl = inflight.pop(idx)
-            if kind == "tma":
+            if kind == "tmao":
+                (kk,) = pl
+                assert state["Q"][kk & 1] == (kk, "O") and state["staged"][kk & 1] == 4, \
+                    "the store reads the staged O"
+                state["Q"][kk & 1] = (kk, "Oread")
+                state["staged"][kk & 1] = 0
+                B["ostore", kk & 1].arrive()
+            elif kind == "tma":
                 buf, s, x = pl
                 if buf == "K":
                     assert state["K"][s] is None or state["K"][s][0] <= x - 2
@@ -251,6 +299,7 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
                 assert state["S"][sb] is None or (state["S"][sb] == ("P", g - sbufs)
                                                   and state["pv_done"] >= g - sbufs)
                 state["S"][sb] = ("S", g)
+                state["s_done"] = g
                 B["kEmpty", s].arrive()      # the commits after S(g)
                 B["sFull", sb].arrive()
                 if last:
