@@ -740,6 +740,15 @@ __device__ __forceinline__ uint4 ld_v4(const uint4 *ptr) {
     return r;
 }
 
+// Read-only streaming load that leaves L1 to data read again (the tables).
+__device__ __forceinline__ uint4 ldg_stream_v4(const uint4 *ptr) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(ptr));
+    return r;
+}
+
 // Grid coordinate on `axis` of the token of vector vv.
 __device__ __forceinline__ uint32_t axis_pos(const RKParams &p, uint32_t vv, int axis) {
     const uint32_t gt = p.tok0 + fdiv(vv >> 4, p.heads);   // < 2^31
@@ -816,14 +825,12 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 //   K  [2 slots][2 column blocks][kTcN rows][128 B]     57,344
 //   V  [2 slots][2 column blocks][kTcN rows][128 B]     57,344
 //   row maxima and sums of the row's two threads, the softmax threads' window
-//   masks (4 KB per chunk row offset, up to 4 offsets), 20 mbarriers, the TMEM
-//   address.
+//   masks (3 sets of 4 KB per chunk row offset, up to 4 offsets), 30
+//   mbarriers, the TMEM address.
 // Tensor memory (512 columns): three S buffers at columns 0, 128 and 256 (S,
 // then P in their first 56 columns), so that the S products run up to two
 // chunks ahead of the softmax while P V reads the third; O at 384 (a block's
 // first P V waits for the Q warps to have read the previous block's O out).
-// Tensor memory (all 512 columns: one CTA per SM): S in [0, 128) and
-// [128, 256), O in [256, 384).
 constexpr int kTcParts = 2;                  // softmax threads per query row
 constexpr int kTcQBar = 5;                   // named barrier of the Q warps (1-4: softmax pairs)
 constexpr int kTcSoftWarp0 = 8;              // first softmax warp
@@ -844,11 +851,13 @@ constexpr uint32_t kTcOffV = kTcOffK + 2 * kTcKvSlot;
 // float row maxima [chunk parity][part][128], row sums [block parity][part][128]
 constexpr uint32_t kTcOffRed = kTcOffV + 2 * kTcKvSlot;
 // the softmax threads' window masks of a block's chunk row offsets (frames
-// share them): [offset][part][128] 64-bit words, each thread its own
+// share them): [set][offset][part][128] 64-bit words, each thread its own;
+// a set per window geometry the thread has met lately
 constexpr int kTcMaxPF = 4;                                 // offsets kept; more: made per chunk
+constexpr int kTcMaskSets = 3;
 constexpr uint32_t kTcOffMask = kTcOffRed + 4 * kTcParts * kTcM * 4;
 constexpr int kTcBars = 30;                                 // mbarriers, then the TMEM address
-constexpr uint32_t kTcOffBar = kTcOffMask + kTcMaxPF * kTcSoftThreads * 8;
+constexpr uint32_t kTcOffBar = kTcOffMask + kTcMaskSets * kTcMaxPF * kTcSoftThreads * 8;
 constexpr uint32_t kTcSmem = kTcOffBar + kTcBars * 8 + 16 + 1024;   // + room to align to 1024
 #ifndef NA_TC_SBUFS   // S buffers in tensor memory: 3 (O single) or 2 (O double-buffered)
 #define NA_TC_SBUFS 3
@@ -1504,7 +1513,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                             const long long off = (((long long)g.b * p.T + t) * p.H + h) * p.W * tok +
                                                   (long long)w * tok + (long long)g.head * kHD + 8 * cv;
                             if (bound_ok(off, 8, p.total))
-                                qv[i - i0] = __ldg(reinterpret_cast<const uint4 *>(p.q + off));
+                                qv[i - i0] = ldg_stream_v4(reinterpret_cast<const uint4 *>(p.q + off));
                         }
                     }
 #pragma unroll
@@ -1559,8 +1568,10 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         const int row = 32 * lg + lane;
         const uint32_t lanes = uint32_t(32 * lg) << 16;
         int gc = 0;
-        // the window geometry the masks in shared memory were made for
-        int mk_ah = -1, mk_clo = -1, mk_chi = -1, mk_rh = -1;
+        // the window geometries (packed) the mask sets were made for; the
+        // set made longest ago is replaced first
+        uint32_t mk0 = ~0u, mk1 = ~0u, mk2 = ~0u;
+        int mk_next = 0;
         for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
             const TcBlock g = tc_block(p, shp, dv, blk);
             const int qt = g.t0 + (row >> 6), qh = g.h0 + ((row >> 3) & 7), qw = g.w0 + (row & 7);
@@ -1587,19 +1598,27 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 }
                 return m;
             };
-            uint64_t *wmask = reinterpret_cast<uint64_t *>(sm + kTcOffMask) + (qq * kTcM + row);
             // A mask depends on the row's window in the region and the region's
-            // height only, so blocks that share them (every interior block of
-            // the grid) keep the masks of the block before.
+            // height only (every interior block of the grid has the same), so
+            // the sets made for recent blocks are kept and looked up.
             const bool kept = g.per_frame <= kTcMaxPF;
-            if (kept && (ah != mk_ah || clo != mk_clo || chi != mk_chi || g.RH != mk_rh)) {
+            const uint32_t key = g.RH < 256 ? uint32_t(ah) | uint32_t(clo) << 8 | uint32_t(chi) << 16 |
+                                                  uint32_t(g.RH) << 24
+                                            : ~0u;   // not kept across blocks
+            int set = key == ~0u ? -1 : key == mk0 ? 0 : key == mk1 ? 1 : key == mk2 ? 2 : -1;
+            if (kept && set < 0) {
+                set = mk_next;
+                mk_next = mk_next == kTcMaskSets - 1 ? 0 : mk_next + 1;
+                mk0 = set == 0 ? key : mk0;
+                mk1 = set == 1 ? key : mk1;
+                mk2 = set == 2 ? key : mk2;
+                uint64_t *wm = reinterpret_cast<uint64_t *>(sm + kTcOffMask) +
+                               (set * kTcMaxPF * kTcSoftThreads + qq * kTcM + row);
                 for (int pf = 0, r0 = 0; pf < g.per_frame; ++pf, r0 += chb)
-                    wmask[pf * kTcSoftThreads] = window_mask(r0, min(chb, g.RH - r0));
-                mk_ah = ah;
-                mk_clo = clo;
-                mk_chi = chi;
-                mk_rh = g.RH;
+                    wm[pf * kTcSoftThreads] = window_mask(r0, min(chb, g.RH - r0));
             }
+            const uint64_t *wmask = reinterpret_cast<const uint64_t *>(sm + kTcOffMask) +
+                                    (max(set, 0) * kTcMaxPF * kTcSoftThreads + qq * kTcM + row);
 
             ChunkPos cp = chunk_start(g);
             for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
