@@ -63,6 +63,24 @@ TRAFFIC_RECORD = {
 }
 
 
+# DRAM traffic of one launch of the tensor-core attention rotating its Q tiles
+# (rope3d_na3d_tc_kernel<2>, the larger of the two kernels of the rotate-once
+# step) on the NA3D workload, from one ncu capture (--set full, one launch,
+# 1.07 GB on the device):
+#   python bench.py --op na3d --steps 3 --warmup 3
+#   ncu --set full --clock-control none -k regex:rope3d_na3d_tc_kernel -s 9 -c 1 (the same command)
+# Valid while the attention source hashes to `kernel_source` and the workload
+# is the recorded one.
+NA3D_KERNEL_SOURCES = [os.path.join(ROOT, "rope_rope3d_apply_gb300", "csrc", "rope3d_na3d.cu")]
+NA3D_TRAFFIC_RECORD = {
+    "kernel_source": "c8712d7518d16612",
+    "kernel": "rope3d_na3d_tc_kernel<2>",
+    "workload": {"B": 1, "T": 16, "H": 64, "W": 64, "heads": 16, "kernel": (3, 7, 7)},
+    "dram_read_bytes": 805_637_632,
+    "dram_write_bytes": 244_956_160,
+}
+
+
 def parse_args():
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--gpus", type=int, default=1)
@@ -142,12 +160,23 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in sources or KERNEL_SOURCES:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def na3d_traffic_per_launch(c) -> int | None:
+    """DRAM bytes of one launch of the recorded attention kernel, while its
+    source and the workload are the captured ones; otherwise None."""
+    rec = NA3D_TRAFFIC_RECORD
+    w = rec["workload"]
+    same = all(c[key] == w[key] for key in ("B", "T", "H", "W", "heads")) and tuple(c["kernel"]) == w["kernel"]
+    if not same or kernel_source_hash(NA3D_KERNEL_SOURCES) != rec["kernel_source"]:
+        return None
+    return rec["dram_read_bytes"] + rec["dram_write_bytes"]
 
 
 def traffic_per_launch(w: synthetic.Workload):
@@ -936,7 +965,8 @@ def run_na3d(args):
         "config": {"workload": "na3d: B=%d, T=%d, H=%d, W=%d, heads=%d x 128, window %dx%dx%d" % (
             c["B"], c["T"], c["H"], c["W"], c["heads"], kt, kh, kw), "useful_flops": flops},
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": tflops / peak, "traffic": None,
+                     "frac": tflops / peak, "traffic": na3d_traffic_per_launch(c),
+                     "traffic_kernel": NA3D_TRAFFIC_RECORD["kernel"],
                      "peak_source": f"{kind} bf16_tflops (cuBLAS burst)", "kernel_ms": ms_once},
         "step": "rope3d_na3d_rotate_once (K pass + attention rotating its Q tiles)",
         "attention_kernel": {1: "tcgen05 (tensor memory)", 2: "warp-level mma.sync"}.get(

@@ -112,3 +112,19 @@ def test_reference_arm_other_ranks_exit_quietly():
                           "--steps", "1", "--warmup", "0", "--workload", "tiny"],
                          capture_output=True, text=True, timeout=120, env=env)
     assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+def test_na3d_traffic_only_for_the_captured_kernel_and_workload(monkeypatch):
+    """The attention line's traffic is the recorded capture's DRAM bytes only
+    while the kernel source and the workload are the captured ones."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    rec = bench.NA3D_TRAFFIC_RECORD
+    c = dict(bench.NA3D)
+    monkeypatch.setitem(rec, "kernel_source", bench.kernel_source_hash(bench.NA3D_KERNEL_SOURCES))
+    assert bench.na3d_traffic_per_launch(c) == rec["dram_read_bytes"] + rec["dram_write_bytes"]
+    assert bench.na3d_traffic_per_launch(dict(c, W=32)) is None
+    assert bench.na3d_traffic_per_launch(dict(c, kernel=(1, 7, 7))) is None
+    monkeypatch.setitem(rec, "kernel_source", "0" * 16)
+    assert bench.na3d_traffic_per_launch(c) is None

@@ -60,6 +60,8 @@ CASES = [
     ((1, 2, 6, 80, 1), (32, 48, 48), (1, 3, 67)),      # a region row of 74 keys: split in columns
     ((1, 2, 12, 40, 1), (32, 48, 48), (1, 9, 33)),     # region rows of 40 keys: three 16-key steps
     ((2, 4, 13, 11, 3), (16, 56, 56), (3, 5, 7)),      # two batches, three heads, odd grid, split
+    ((2, 3, 9, 10, 2), (32, 48, 48), (3, 5, 5)),       # two batches, odd T: the last frame pair of
+                                                        # batch 0 must not reach batch 1's first frame
 ]
 
 
