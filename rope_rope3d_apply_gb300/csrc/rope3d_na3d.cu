@@ -797,24 +797,25 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 //     swizzle, into two-slot rings;
 //   warp 1 (one thread): the P V MMAs, O += P(c) V(c) (V read as an MN-major
 //     operand), once the softmax has written P(c);
-//   warp 2 (one thread): the S MMAs, S(c) = Q K(c)^T into one of two S
+//   warp 2 (one thread): the S MMAs, S(c) = Q K(c)^T into one of three S
 //     buffers in tensor memory (eight k16 steps), as soon as K(c) has landed
-//     and the softmax has taken S(c - 2) out of that buffer. Two issuing
-//     threads keep either kind of product from waiting behind the other's
-//     inputs; S(c + 1) and S(c + 2) run while the softmax of chunk c does;
+//     and P V has read the weights of chunk c - 3 out of that buffer. Two
+//     issuing threads keep either kind of product from waiting behind the
+//     other's inputs; S(c + 1) and S(c + 2) run while the softmax of chunk c
+//     does;
 //   warps 4-7: each query block's Q tile, read from global memory into
 //     registers (and rotated there in the rotating modes) while the previous
-//     block still uses the Q buffer, then written into it in the swizzled
-//     layout; in the mode that rotates K per CTA, each K tile too, in place
-//     once it lands;
+//     block still uses the other Q buffer, then written into its own in the
+//     swizzled layout; each block's O, normalised, through its spent Q buffer
+//     and two TMA stores; in the mode that rotates K per CTA, each K tile
+//     too, in place once it lands;
 //   warps 8-15: the softmax. Each query row's S is read back from tensor
 //     memory by two threads (half of the chunk's columns each, in one batch of
 //     loads: warps w and w + 4 share the 32 lanes of tensor memory that warp w
 //     reaches), masked to the query's window (a 64-bit mask from the region
-//     rows the half spans; groups of 8 keys that no query of the warp needs
-//     are skipped), scaled, and turned into weights with the same online
-//     softmax as the
-//     warp-MMA kernel (the reference moves only when a row maximum passes it
+//     rows the half spans; a warp none of whose rows has a key in the chunk
+//     skips it), scaled, and turned into weights with the same online
+//     softmax as the warp-MMA kernel (the reference moves only when a row maximum passes it
 //     by more than 2^kLazy; O in tensor memory is rescaled then); the bf16
 //     weights are written back into the S buffer they came from (over the S
 //     values, as bf16 pairs), where the P V MMA reads them as its A operand.
