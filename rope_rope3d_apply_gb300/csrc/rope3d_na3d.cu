@@ -740,15 +740,6 @@ __device__ __forceinline__ uint4 ld_v4(const uint4 *ptr) {
     return r;
 }
 
-// Read-only streaming load that leaves L1 to data read again (the tables).
-__device__ __forceinline__ uint4 ldg_stream_v4(const uint4 *ptr) {
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(ptr));
-    return r;
-}
-
 // Grid coordinate on `axis` of the token of vector vv.
 __device__ __forceinline__ uint32_t axis_pos(const RKParams &p, uint32_t vv, int axis) {
     const uint32_t gt = p.tok0 + fdiv(vv >> 4, p.heads);   // < 2^31
@@ -826,7 +817,7 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 //   K  [2 slots][2 column blocks][kTcN rows][128 B]     57,344
 //   V  [2 slots][2 column blocks][kTcN rows][128 B]     57,344
 //   row maxima and sums of the row's two threads, the softmax threads' window
-//   masks (3 sets of 4 KB per chunk row offset, up to 4 offsets), 30
+//   masks (3 sets of 4 KB per chunk row offset, up to 4 offsets), 32
 //   mbarriers, the TMEM address.
 // Tensor memory (512 columns): three S buffers at columns 0, 128 and 256 (S,
 // then P in their first 56 columns), so that the S products run up to two
@@ -857,7 +848,7 @@ constexpr uint32_t kTcOffRed = kTcOffV + 2 * kTcKvSlot;
 constexpr int kTcMaxPF = 4;                                 // offsets kept; more: made per chunk
 constexpr int kTcMaskSets = 3;
 constexpr uint32_t kTcOffMask = kTcOffRed + 4 * kTcParts * kTcM * 4;
-constexpr int kTcBars = 30;                                 // mbarriers, then the TMEM address
+constexpr int kTcBars = 32;                                 // mbarriers, then the TMEM address
 constexpr uint32_t kTcOffBar = kTcOffMask + kTcMaskSets * kTcMaxPF * kTcSoftThreads * 8;
 constexpr uint32_t kTcSmem = kTcOffBar + kTcBars * 8 + 16 + 1024;   // + room to align to 1024
 #ifndef NA_TC_SBUFS   // S buffers in tensor memory: 3 (O single) or 2 (O double-buffered)
@@ -1202,7 +1193,8 @@ __device__ __forceinline__ TcBlock tc_block(const NAParams &p, const TcShape &sh
 template <int kMode>
 __global__ void __launch_bounds__(kTcThreads, 1)
 rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO) {
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                      const __grid_constant__ CUtensorMap tmQ) {
     extern __shared__ unsigned char tc_raw[];
     unsigned char *sm = tc_raw + ((1024u - (smem_addr(tc_raw) & 1023u)) & 1023u);
     const uint32_t sQ = smem_addr(sm + kTcOffQ), sK = smem_addr(sm + kTcOffK);
@@ -1219,8 +1211,9 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     // one per S buffer (chunk % kTcSBufs):
     //   sFull  S written (MMA)         sEmpty  P V done with the P in it (commit)
     //   pFull  P written (256 arrivals) pEmpty  P V done (O updated)
-    // per Q buffer (block parity): qReady (the Q tile written, rotated in the
-    // rotating modes; 128 arrivals), qEmpty (the block's S MMAs done with Q);
+    // per Q buffer (block parity): qFull (the Q tile landed, TMA), qReady (the
+    // tile rotated, in the rotating modes; 128 arrivals), qEmpty (the block's
+    // S MMAs done with Q);
     // per O buffer b: oReady[b] the block's last P V done (commit), oEmpty[b]
     // O read out (Q warps), so the next block using b may overwrite it; and
     // oFull[block parity] the block's row sums written (softmax threads).
@@ -1234,7 +1227,8 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     auto oReady = [&](int b) { return smem_addr(&bars[kQb + 4 + b]); };
     auto oEmpty = [&](int b) { return smem_addr(&bars[kQb + 4 + kTcOBufs + b]); };
     auto oFull = [&](int b) { return smem_addr(&bars[kQb + 4 + 2 * kTcOBufs + b]); };
-    static_assert(kQb + 4 + 2 * kTcOBufs + 2 <= kTcBars, "mbarriers");
+    auto qFull = [&](int b) { return smem_addr(&bars[kQb + 6 + 2 * kTcOBufs + b]); };
+    static_assert(kQb + 6 + 2 * kTcOBufs + 2 <= kTcBars, "mbarriers");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long tok = (long long)p.heads * kHD;   // elements per token
@@ -1294,12 +1288,15 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(oReady(b)) : "memory");
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(oEmpty(b)), "r"(kTcRotThreads) : "memory");
         }
-        for (int b = 0; b < 2; ++b)
+        for (int b = 0; b < 2; ++b) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(oFull(b)), "r"(kTcSoftThreads) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(qFull(b)) : "memory");
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmO)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmQ)) : "memory");
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -1388,7 +1385,8 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             int gc = 0;
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
                 const TcBlock g = tc_block(p, shp, dv, blk);
-                tc_wait(qReady(k & 1), uint32_t(k >> 1) & 1u, dead);
+                // this block's Q: landed (TMA), or landed and rotated
+                tc_wait(kMode == kRotNone ? qFull(k & 1) : qReady(k & 1), uint32_t(k >> 1) & 1u, dead);
                 const uint32_t sQk = sQ + uint32_t(k & 1) * 2 * kTcQCb;   // this block's Q buffer
                 ChunkPos cp = chunk_start(g);
                 for (int c = 0; c < g.n_chunks; ++c, ++gc, chunk_advance(g, cp)) {
@@ -1503,35 +1501,32 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 if (k >= 2) tc_wait(qEmpty(k & 1), uint32_t((k - 2) >> 1) & 1u, dead);
                 o_reads_done();
                 unsigned char *qbuf = sm + kTcOffQ + (k & 1) * 2 * kTcQCb;
-#pragma unroll
-                for (int i0 = 0; i0 < 16; i0 += 4) {   // four vectors a round
-                    uint4 qv[4];
-#pragma unroll
-                    for (int i = i0; i < i0 + 4; ++i) {
-                        const int t = g.t0 + (i >> 3), h = g.h0 + (i & 7);
-                        qv[i - i0] = make_uint4(0u, 0u, 0u, 0u);   // outside the grid: zeros
-                        if (t < p.T && h < p.H && w < p.W) {
-                            const long long off = (((long long)g.b * p.T + t) * p.H + h) * p.W * tok +
-                                                  (long long)w * tok + (long long)g.head * kHD + 8 * cv;
-                            if (bound_ok(off, 8, p.total))
-                                qv[i - i0] = ldg_stream_v4(reinterpret_cast<const uint4 *>(p.q + off));
-                        }
-                    }
-#pragma unroll
-                    for (int i = i0; i < i0 + 4; ++i) {
-                        if constexpr (kMode != kRotNone) {
-                            const int t = g.t0 + (i >> 3), h = g.h0 + (i & 7);
-                            if (t < p.T && h < p.H && w < p.W) {
-                                const int pos = tsg.axis == 0 ? t : (tsg.axis == 1 ? h : w);
-                                qv[i - i0] = rot_vec_at<true>(qv[i - i0], p.tab, tsg, uint32_t(pos), p.tab_len);
-                            }
-                        }
-                        *reinterpret_cast<uint4 *>(qbuf + sw128(uint32_t(qw_off + 8 * i), uint32_t(cv), kTcQCb)) =
-                            qv[i - i0];
-                    }
+                // the tile by two TMA box loads (64 channels each); rows past the
+                // grid read zeros (or, past an odd last frame, the next batch's
+                // first frame): their queries are masked
+                if (rt == 0) {
+                    const uint32_t dst = smem_addr(qbuf), full = qFull(k & 1);
+                    const int frame = g.b * p.T + g.t0;
+                    mbar_expect_tx(full, 2 * kTcQCb);
+                    tma_load5(dst, &tmQ, 0, g.head, g.w0, g.h0, frame, full);
+                    tma_load5(dst + kTcQCb, &tmQ, 64, g.head, g.w0, g.h0, frame, full);
                 }
-                fence_async_smem();
-                mbar_arrive(qReady(k & 1));
+                if constexpr (kMode != kRotNone) {
+                    // rotated in place, each thread its 16 vectors
+                    tc_wait(qFull(k & 1), uint32_t(k >> 1) & 1u, dead);
+#pragma unroll 4
+                    for (int i = 0; i < 16; ++i) {
+                        const int t = g.t0 + (i >> 3), h = g.h0 + (i & 7);
+                        if (t < p.T && h < p.H && w < p.W) {
+                            uint4 *ptr = reinterpret_cast<uint4 *>(
+                                qbuf + sw128(uint32_t(qw_off + 8 * i), uint32_t(cv), kTcQCb));
+                            const int pos = tsg.axis == 0 ? t : (tsg.axis == 1 ? h : w);
+                            *ptr = rot_vec_at<true>(*ptr, p.tab, tsg, uint32_t(pos), p.tab_len);
+                        }
+                    }
+                    fence_async_smem();
+                    mbar_arrive(qReady(k & 1));
+                }
                 // the previous block's result: before this block's K tiles, whose
                 // S products may wait for the O buffer through P V
                 if (k >= 1) store_o(g_prev, k - 1);
@@ -2054,10 +2049,11 @@ int na3d_launch_rotate_once(NAParams &p, const void *k, void *k_rot, const rope3
     const bool tc = na3d_use_tc(p);
     g_na3d_last_kernel = tc ? 1 : 2;
     const TcShape shp = na3d_tc_shape(p);
-    CUtensorMap mk{}, mv{}, mo{};
+    CUtensorMap mk{}, mv{}, mo{}, mq{};
     if (tc && (!na3d_tc_attribute<kRotQ>() || !na3d_tc_map(&mk, p.k, p, shp.rwb, shp.chb, 1) ||
                !na3d_tc_map(&mv, p.v, p, shp.rwb, shp.chb, 1) ||
-               !na3d_tc_map(&mo, p.out, p, kTcQW, kTcQH, kTcQT)))
+               !na3d_tc_map(&mo, p.out, p, kTcQW, kTcQH, kTcQT) ||
+               !na3d_tc_map(&mq, p.q, p, kTcQW, kTcQH, kTcQT)))
         return ROPE3D_ERR_CUDA;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(tc ? na3d_tc_grid(shp) : na3d_blocks(p));
@@ -2069,7 +2065,7 @@ int na3d_launch_rotate_once(NAParams &p, const void *k, void *k_rot, const rope3
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t le = tc ? cudaLaunchKernelEx(&cfg, rope3d_na3d_tc_kernel<kRotQ>, p, shp, mk, mv, mo)
+    const cudaError_t le = tc ? cudaLaunchKernelEx(&cfg, rope3d_na3d_tc_kernel<kRotQ>, p, shp, mk, mv, mo, mq)
                               : cudaLaunchKernelEx(&cfg, rope3d_na3d_kernel<kRotQ>, p);
     if (le != cudaSuccess) {
         cudaGetLastError();
@@ -2159,16 +2155,16 @@ extern "C" int rope3d_na3d(const void *q, const void *k, const void *v, void *ou
     g_na3d_last_kernel = na3d_use_tc(p) ? 1 : 2;
     if (na3d_use_tc(p)) {
         const TcShape shp = na3d_tc_shape(p);
-        CUtensorMap mk, mv, mo;
+        CUtensorMap mk, mv, mo, mq;
         if (!na3d_tc_map(&mk, p.k, p, shp.rwb, shp.chb, 1) || !na3d_tc_map(&mv, p.v, p, shp.rwb, shp.chb, 1) ||
-            !na3d_tc_map(&mo, p.out, p, kTcQW, kTcQH, kTcQT))
+            !na3d_tc_map(&mo, p.out, p, kTcQW, kTcQH, kTcQT) || !na3d_tc_map(&mq, p.q, p, kTcQW, kTcQH, kTcQT))
             return ROPE3D_ERR_CUDA;
         if (apply_rope) {
             if (!na3d_tc_attribute<kRotQK>()) return ROPE3D_ERR_CUDA;
-            rope3d_na3d_tc_kernel<kRotQK><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv, mo);
+            rope3d_na3d_tc_kernel<kRotQK><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv, mo, mq);
         } else {
             if (!na3d_tc_attribute<kRotNone>()) return ROPE3D_ERR_CUDA;
-            rope3d_na3d_tc_kernel<kRotNone><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv, mo);
+            rope3d_na3d_tc_kernel<kRotNone><<<na3d_tc_grid(shp), kTcThreads, kTcSmem, st>>>(p, shp, mk, mv, mo, mq);
         }
     } else {
         if (!na3d_attributes()) return ROPE3D_ERR_CUDA;

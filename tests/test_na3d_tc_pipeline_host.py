@@ -4,8 +4,10 @@
 The roles of one persistent CTA walking several query blocks are modelled:
   - the two TMA threads (K; V);
   - the two MMA threads (S products; P V products);
-  - the Q warps, which write each block's Q tile, store each block's O and,
-    in the mode that rotates K per CTA, rotate the K tiles;
+  - the Q warps, which have each block's Q tile copied by TMA (and rotate it
+    in place in the rotating modes), store each block's O through the block's
+    spent Q buffer and a TMA store and, in the mode that rotates K per CTA,
+    rotate the K tiles;
   - the softmax threads, which write P over S in the S buffer.
 Each role is a sequence of the kernel's mbarrier waits, arrivals and buffer
 accesses. They run in many random interleavings over model mbarriers (a phase
@@ -82,8 +84,8 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
     for b in range(sbufs):
         for kind, cnt in (("sFull", 1), ("sEmpty", 1), ("pFull", 256), ("pEmpty", 1)):
             B[kind, b] = Bar(cnt)
-    for b in (0, 1):         # per Q buffer (block parity): Q written, S MMAs done with it
-        B["qReady", b], B["qEmpty", b] = Bar(128), Bar(1)
+    for b in (0, 1):         # per Q buffer (block parity): Q landed (TMA), Q rotated, S MMAs done with it
+        B["qFull", b], B["qReady", b], B["qEmpty", b] = Bar(1), Bar(128), Bar(1)
     for b in range(obufs):   # per O buffer: last P V done, O read out
         B["oReady", b], B["oEmpty", b] = Bar(1), Bar(128)
     for b in (0, 1):         # per block parity: row sums written
@@ -137,7 +139,7 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
             s, use = g & 1, g >> 1
             sb, suse = g % sbufs, g // sbufs
             if c == 0:
-                yield ("wait", B["qReady", k & 1], (k >> 1) & 1, k >> 1)
+                yield ("wait", B["qReady" if rot_q else "qFull", k & 1], (k >> 1) & 1, k >> 1)
             yield ("wait", B["kReady" if rot_k else "kFull", s], use & 1, use)
             if g >= sbufs:
                 yield ("wait", B["sEmpty", sb], (suse - 1) & 1, suse - 1)
@@ -152,13 +154,18 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
             if k >= 2:                 # block k - 2's S MMAs are done with Q buffer k & 1
                 yield ("wait", B["qEmpty", k & 1], ((k - 2) >> 1) & 1, (k - 2) >> 1)
             yield from o_reads_done(i, ws)   # and the TMA store of its O has read it
-            yield None                 # Q of block k read (and rotated) and written
-            if i == 0:
-                assert state["Q"][k & 1] is None or state["Q"][k & 1] == (k - 2, "Oread"), \
-                    "a Q buffer is rewritten only after the O staged in it was stored"
-                state["Q"][k & 1] = (k, "rot" if rot_q else "raw")
-            for _ in range(32):
-                B["qReady", k & 1].arrive()
+            if i == 0:                 # the tile by TMA into Q buffer k & 1
+                B["qFull", k & 1].expect_tx(2)
+                inflight.append(("tmaq", (k,)))
+            yield None
+            if rot_q:                  # landed, then rotated in place by every Q thread
+                yield ("wait", B["qFull", k & 1], (k >> 1) & 1, k >> 1)
+                assert state["Q"][k & 1] in ((k, "raw"), (k, "rot")), "the Q warps rotate their block's tile"
+                yield None
+                if i == 0:
+                    state["Q"][k & 1] = (k, "rot")
+                for _ in range(32):
+                    B["qReady", k & 1].arrive()
             if k >= 1:                 # the previous block's result, before this block's K tiles
                 yield from store_o(i, k - 1, ws)
             for c in range(n):
@@ -266,15 +273,21 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
                     if waiting[i] is None or waiting[i][0].ready(waiting[i][1], waiting[i][2])]
         if inflight and (not runnable or rng.random() < 0.4):
             kinds = [kd for kd, _ in inflight]
-            if any(kd in ("tma", "tmao") for kd in kinds) and (
-                    rng.random() < 0.5 or all(kd in ("tma", "tmao") for kd in kinds)):
-                tma_idx = [j for j, kd in enumerate(kinds) if kd in ("tma", "tmao")]
+            if any(kd in ("tma", "tmao", "tmaq") for kd in kinds) and (
+                    rng.random() < 0.5 or all(kd in ("tma", "tmao", "tmaq") for kd in kinds)):
+                tma_idx = [j for j, kd in enumerate(kinds) if kd in ("tma", "tmao", "tmaq")]
                 idx = rng.choice(tma_idx)
             else:   # each issuer's MMAs complete in its issue order
                 first = [next((j for j, kd in enumerate(kinds) if kd == want), None) for want in ("s", "pv")]
                 idx = rng.choice([j for j in first if j is not None])
             kind, pl = inflight.pop(idx)
-            if kind == "tmao":
+            if kind == "tmaq":
+                (kk,) = pl
+                assert state["Q"][kk & 1] is None or state["Q"][kk & 1] == (kk - 2, "Oread"), \
+                    "a Q buffer is rewritten only after the O staged in it was stored"
+                state["Q"][kk & 1] = (kk, "raw")
+                B["qFull", kk & 1].complete_tx(2)
+            elif kind == "tmao":
                 (kk,) = pl
                 assert state["Q"][kk & 1] == (kk, "O") and state["staged"][kk & 1] == 4, \
                     "the store reads the staged O"
