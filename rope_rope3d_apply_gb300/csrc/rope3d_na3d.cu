@@ -817,8 +817,8 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 //   K  [2 slots][2 column blocks][kTcN rows][128 B]     57,344
 //   V  [2 slots][2 column blocks][kTcN rows][128 B]     57,344
 //   row maxima and sums of the row's two threads, the softmax threads' window
-//   masks (3 sets of 4 KB per chunk row offset, up to 4 offsets), 32
-//   mbarriers, the TMEM address.
+//   masks (3 sets of 4 KB per chunk row offset, up to 4 offsets), two block
+//   descriptors, 36 mbarriers, the TMEM address.
 // Tensor memory (512 columns): three S buffers at columns 0, 128 and 256 (S,
 // then P in their first 56 columns), so that the S products run up to two
 // chunks ahead of the softmax while P V reads the third; O at 384 (a block's
@@ -848,8 +848,14 @@ constexpr uint32_t kTcOffRed = kTcOffV + 2 * kTcKvSlot;
 constexpr int kTcMaxPF = 4;                                 // offsets kept; more: made per chunk
 constexpr int kTcMaskSets = 3;
 constexpr uint32_t kTcOffMask = kTcOffRed + 4 * kTcParts * kTcM * 4;
-constexpr int kTcBars = 32;                                 // mbarriers, then the TMEM address
-constexpr uint32_t kTcOffBar = kTcOffMask + kTcMaskSets * kTcMaxPF * kTcSoftThreads * 8;
+// block descriptors for the softmax threads, written by the Q warps a block
+// ahead: [block parity] {first region frame, region rows, chunks per frame,
+// chunks}, then per query row {in the grid, first window frame, window's first
+// region row, window columns [lo, hi) packed}
+constexpr uint32_t kTcDescSlot = 16 + kTcM * 16;
+constexpr uint32_t kTcOffDesc = kTcOffMask + kTcMaskSets * kTcMaxPF * kTcSoftThreads * 8;
+constexpr int kTcBars = 36;                                 // mbarriers, then the TMEM address
+constexpr uint32_t kTcOffBar = kTcOffDesc + 2 * kTcDescSlot;
 constexpr uint32_t kTcSmem = kTcOffBar + kTcBars * 8 + 16 + 1024;   // + room to align to 1024
 #ifndef NA_TC_SBUFS   // S buffers in tensor memory: 3 (O single) or 2 (O double-buffered)
 #define NA_TC_SBUFS 3
@@ -1216,7 +1222,9 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     // S MMAs done with Q);
     // per O buffer b: oReady[b] the block's last P V done (commit), oEmpty[b]
     // O read out (Q warps), so the next block using b may overwrite it; and
-    // oFull[block parity] the block's row sums written (softmax threads).
+    // oFull[block parity] the block's row sums written (softmax threads);
+    // per block descriptor (block parity): dFull (written, 128 arrivals of the
+    // Q warps), dEmpty (read, 256 arrivals of the softmax threads).
     enum { kFull, kReady, kEmpty, vFull, vEmpty };
     enum { sFull, sEmpty, pFull, pEmpty };
     auto bar = [&](int kind, int slot) { return smem_addr(&bars[2 * kind + slot]); };
@@ -1228,7 +1236,9 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
     auto oEmpty = [&](int b) { return smem_addr(&bars[kQb + 4 + kTcOBufs + b]); };
     auto oFull = [&](int b) { return smem_addr(&bars[kQb + 4 + 2 * kTcOBufs + b]); };
     auto qFull = [&](int b) { return smem_addr(&bars[kQb + 6 + 2 * kTcOBufs + b]); };
-    static_assert(kQb + 6 + 2 * kTcOBufs + 2 <= kTcBars, "mbarriers");
+    auto dFull = [&](int b) { return smem_addr(&bars[kQb + 8 + 2 * kTcOBufs + b]); };
+    auto dEmpty = [&](int b) { return smem_addr(&bars[kQb + 10 + 2 * kTcOBufs + b]); };
+    static_assert(kQb + 10 + 2 * kTcOBufs + 2 <= kTcBars, "mbarriers");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long tok = (long long)p.heads * kHD;   // elements per token
@@ -1291,6 +1301,8 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         for (int b = 0; b < 2; ++b) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(oFull(b)), "r"(kTcSoftThreads) : "memory");
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(qFull(b)) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(dFull(b)), "r"(kTcRotThreads) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(dEmpty(b)), "r"(kTcSoftThreads) : "memory");
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
@@ -1496,6 +1508,20 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
                 const TcBlock g = tc_block(p, shp, dv, blk);
                 const int w = g.w0 + qw_off;
+                // the softmax threads' descriptor of this block, into slot k & 1
+                // once they have read the one of block k - 2
+                if (k >= 2) tc_wait(dEmpty(k & 1), uint32_t((k - 2) >> 1) & 1u, dead);
+                {
+                    unsigned char *ds = sm + kTcOffDesc + (k & 1) * kTcDescSlot;
+                    if (rt == 0) *reinterpret_cast<int4 *>(ds) = make_int4(g.rt0, g.RH, g.per_frame, g.n_chunks);
+                    const int qt = g.t0 + (orow >> 6), qh = g.h0 + ((orow >> 3) & 7), qw = g.w0 + (orow & 7);
+                    const int aw = na_start(min(qw, p.W - 1), p.W, p.kw) - g.rw0;
+                    const int clo = max(aw, 0), chi = min(aw + p.kw, g.RW);   // window columns of a region row
+                    reinterpret_cast<int4 *>(ds + 16)[orow] =
+                        make_int4(qt < p.T && qh < p.H && qw < p.W, na_start(min(qt, p.T - 1), p.T, p.kt),
+                                  na_start(min(qh, p.H - 1), p.H, p.kh) - g.rh0, clo | chi << 16);
+                    mbar_arrive(dFull(k & 1));
+                }
                 // Q buffer k & 1, once block k - 2's S MMAs are done with it
                 // and the TMA stores of block k - 2's O have read it
                 if (k >= 2) tc_wait(qEmpty(k & 1), uint32_t((k - 2) >> 1) & 1u, dead);
@@ -1569,13 +1595,20 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         uint32_t mk0 = ~0u, mk1 = ~0u, mk2 = ~0u;
         int mk_next = 0;
         for (int blk = blockIdx.x, k = 0; blk < shp.total; blk += gridDim.x, ++k) {
-            const TcBlock g = tc_block(p, shp, dv, blk);
-            const int qt = g.t0 + (row >> 6), qh = g.h0 + ((row >> 3) & 7), qw = g.w0 + (row & 7);
-            const bool row_ok = qt < p.T && qh < p.H && qw < p.W;
-            const int st_q = na_start(min(qt, p.T - 1), p.T, p.kt);
-            const int ah = na_start(min(qh, p.H - 1), p.H, p.kh) - g.rh0;
-            const int aw = na_start(min(qw, p.W - 1), p.W, p.kw) - g.rw0;
-            const int clo = max(aw, 0), chi = min(aw + p.kw, g.RW);   // window columns of a region row
+            // the block's chunk geometry and this row's window, from the Q warps
+            tc_wait(dFull(k & 1), uint32_t(k >> 1) & 1u, dead);
+            const unsigned char *ds = sm + kTcOffDesc + (k & 1) * kTcDescSlot;
+            const int4 bd = *reinterpret_cast<const int4 *>(ds);
+            const int4 rd = reinterpret_cast<const int4 *>(ds + 16)[row];
+            mbar_arrive(dEmpty(k & 1));
+            TcBlock g{};
+            g.rt0 = bd.x;
+            g.RH = bd.y;
+            g.per_frame = bd.z;
+            g.n_chunks = bd.w;
+            const bool row_ok = rd.x != 0;
+            const int st_q = rd.y, ah = rd.z;
+            const int clo = rd.w & 0xffff, chi = rd.w >> 16;   // window columns of a region row
             const uint32_t tO = tmem + kTcColO + uint32_t(k % kTcOBufs) * 128 + lanes;
             float m_ref = -INFINITY, l_part = 0.f;   // running reference and this part's sum
             const int cb0 = qq * kTcHalf;   // this thread's columns of a chunk: [cb0, cb0 + 56)

@@ -92,6 +92,8 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
         B["oFull", b] = Bar(256)
     for b in (0, 1):         # per Q buffer: the TMA store of O staged in it has read it
         B["ostore", b] = Bar(1)
+    for b in (0, 1):         # per block descriptor (block parity): written, read
+        B["dFull", b], B["dEmpty", b] = Bar(128), Bar(256)
     B["qbar"] = Bar(4)       # the Q warps' named barrier (one arrival per modelled warp)
     state = {  # what each buffer holds; S buffer b holds ("S", g) then ("P", g)
         "K": [None, None], "V": [None, None], "S": [None] * sbufs,
@@ -103,6 +105,7 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
         "pv_done": -1,                 # last chunk whose P V completed
         "s_done": -1,                  # last chunk whose S MMAs completed
         "staged": [0, 0],              # Q buffer: warps that wrote their O rows into it
+        "desc": [None, None],          # descriptor slot: [block, softmax threads that read it]
     }
     inflight = []                      # asynchronous events: (kind, payload)
     SOFT = 4                           # softmax threads modelled (arrivals scaled)
@@ -151,6 +154,15 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
         g = 0
         ws = {"qb": 0, "ost": [0, 0], "pending": None}
         for k, n in enumerate(blocks):
+            if k >= 2:                 # the softmax threads have read block k - 2's descriptor
+                yield ("wait", B["dEmpty", k & 1], ((k - 2) >> 1) & 1, (k - 2) >> 1)
+            if i == 0:
+                d = state["desc"][k & 1]
+                assert d is None or d == [k - 2, SOFT], "a descriptor is rewritten only after it was read"
+                state["desc"][k & 1] = [k, 0]
+            yield None                 # this warp's rows of the descriptor written
+            for _ in range(32):
+                B["dFull", k & 1].arrive()
             if k >= 2:                 # block k - 2's S MMAs are done with Q buffer k & 1
                 yield ("wait", B["qEmpty", k & 1], ((k - 2) >> 1) & 1, (k - 2) >> 1)
             yield from o_reads_done(i, ws)   # and the TMA store of its O has read it
@@ -231,6 +243,11 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
         for k, n in enumerate(blocks):
             m_valid = False
             ob = k % obufs
+            yield ("wait", B["dFull", k & 1], (k >> 1) & 1, k >> 1)
+            assert state["desc"][k & 1][0] == k, "the softmax reads its block's descriptor"
+            state["desc"][k & 1][1] += 1
+            for _ in range(256 // SOFT):
+                B["dEmpty", k & 1].arrive()
             for c in range(n):
                 sb, suse = g % sbufs, g // sbufs
                 yield ("wait", B["sFull", sb], suse & 1, suse)

@@ -145,9 +145,11 @@ def test_shared_memory_layout(cfg):
     c = CONFIGS[cfg]
     assert all(o % 1024 == 0 for o in (c.OFF_K, c.OFF_V, c.OFF_RED, c.KV_CB, c.KV_SLOT))
     # maxima [chunk parity][parts] and sums [block parity][parts] of 128
-    # floats, window masks [3 sets][4 offsets][parts][128] of 8 bytes, 32
-    # mbarriers + the TMEM address
-    total = c.OFF_RED + 4 * c.PARTS * TC_M * 4 + 3 * 4 * c.THREADS * 8 + 32 * 8 + 16 + 1024
+    # floats, window masks [3 sets][4 offsets][parts][128] of 8 bytes, two
+    # block descriptors (16 bytes + 16 per query row), 36 mbarriers + the TMEM
+    # address
+    total = (c.OFF_RED + 4 * c.PARTS * TC_M * 4 + 3 * 4 * c.THREADS * 8 + 2 * (16 + TC_M * 16) + 36 * 8 +
+             16 + 1024)
     assert c.CTAS * (total + 1024) <= 228 * 1024          # 1 KB reserved per CTA
     assert c.TC_N <= c.COL_S and (c.SBUFS - 1) * c.COL_S + c.TC_N <= c.COL_O
     assert c.SBUFS * c.COL_S <= c.COL_O and c.COL_O + 128 * c.OBUFS <= c.TMEM_COLS
