@@ -1468,8 +1468,12 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                     float o[16];
                     tc_ld16(tO + uint32_t(16 * h2), o);
                     uint32_t packed[8];
+                    const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-                    for (int i = 0; i < 16; i += 2) packed[i / 2] = pack_bf16(o[i] * inv, o[i + 1] * inv);
+                    for (int i = 0; i < 16; i += 2) {   // packed multiplies: two channels each
+                        const float2 y = __fmul2_rn(make_float2(o[i], o[i + 1]), inv2);
+                        packed[i / 2] = pack_bf16(y.x, y.y);
+                    }
                     if (tma_o) {   // 16-byte vectors 2 h2 and 2 h2 + 1 of the row
                         *reinterpret_cast<uint4 *>(stg + sw128(uint32_t(orow), uint32_t(2 * h2), kTcQCb)) =
                             make_uint4(packed[0], packed[1], packed[2], packed[3]);
