@@ -1463,26 +1463,33 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 const uint32_t tO = tmem + kTcColO + uint32_t(ob) * 128 + (uint32_t(32 * (warp & 3)) << 16);
                 const bool tma_o = g.t0 + kTcQT <= p.T;
                 unsigned char *stg = sm + kTcOffQ + (k & 1) * 2 * kTcQCb;
+                // 64 columns per tensor-memory wait
 #pragma unroll 1
-                for (int h2 = 0; h2 < kHD / 16; ++h2) {
-                    float o[16];
-                    tc_ld16(tO + uint32_t(16 * h2), o);
-                    uint32_t packed[8];
-                    const float2 inv2 = make_float2(inv, inv);
+                for (int hh = 0; hh < kHD / 64; ++hh) {
+                    float o[64];
+                    tc_ld32_async(tO + uint32_t(64 * hh), o);
+                    tc_ld32_async(tO + uint32_t(64 * hh + 32), o + 32);
+                    tc_ld_wait_hold<64>(o);
 #pragma unroll
-                    for (int i = 0; i < 16; i += 2) {   // packed multiplies: two channels each
-                        const float2 y = __fmul2_rn(make_float2(o[i], o[i + 1]), inv2);
-                        packed[i / 2] = pack_bf16(y.x, y.y);
-                    }
-                    if (tma_o) {   // 16-byte vectors 2 h2 and 2 h2 + 1 of the row
-                        *reinterpret_cast<uint4 *>(stg + sw128(uint32_t(orow), uint32_t(2 * h2), kTcQCb)) =
-                            make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                        *reinterpret_cast<uint4 *>(stg + sw128(uint32_t(orow), uint32_t(2 * h2 + 1), kTcQCb)) =
-                            make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                    } else if (ok && bound_ok(base + 16 * h2, 16, p.total)) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.out + base + 16 * h2);
-                        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int h2 = 4 * hh + q4;   // 16 columns: vectors 2 h2 and 2 h2 + 1
+                        uint32_t packed[8];
+                        const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+                        for (int i = 0; i < 16; i += 2) {   // packed multiplies: two channels each
+                            const float2 y = __fmul2_rn(make_float2(o[16 * q4 + i], o[16 * q4 + i + 1]), inv2);
+                            packed[i / 2] = pack_bf16(y.x, y.y);
+                        }
+                        if (tma_o) {
+                            *reinterpret_cast<uint4 *>(stg + sw128(uint32_t(orow), uint32_t(2 * h2), kTcQCb)) =
+                                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                            *reinterpret_cast<uint4 *>(stg + sw128(uint32_t(orow), uint32_t(2 * h2 + 1), kTcQCb)) =
+                                make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                        } else if (ok && bound_ok(base + 16 * h2, 16, p.total)) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(p.out + base + 16 * h2);
+                            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                        }
                     }
                 }
                 tc_fence_before();   // the reads of O, before the buffer is handed back
