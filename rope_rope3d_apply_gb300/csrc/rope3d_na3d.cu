@@ -979,6 +979,16 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Whether phase `parity` of an mbarrier has completed (no waiting).
+__device__ __forceinline__ bool mbar_done(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    return done != 0;
+}
+
 // Wait for phase `parity` of an mbarrier for at most ~0.1 s of SM clocks.
 // Returns false (and counts) when it gave up; `dead` then skips every later
 // wait of this thread, so a CTA whose MMAs never complete still ends.
@@ -1601,6 +1611,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
         const int row = 32 * lg + lane;
         const uint32_t lanes = uint32_t(32 * lg) << 16;
         int gc = 0;
+        bool s_seen = false;   // the next chunk's S seen complete already (the whole warp)
         // the window geometries (packed) the mask sets were made for; the
         // set made longest ago is replaced first
         uint32_t mk0 = ~0u, mk1 = ~0u, mk2 = ~0u;
@@ -1682,7 +1693,7 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                 // S. The others treat every group alike: straight-line code (the
                 // groups' work interleaves) beats skipping groups by branches.
                 const bool any = __any_sync(0xffffffffu, win != 0);
-                tc_wait(sbar(sFull, sb), suse & 1u, dead);
+                if (!s_seen) tc_wait(sbar(sFull, sb), suse & 1u, dead);
                 tc_fence_after();
                 float x[kTcHalf];
                 if (any) {
@@ -1775,6 +1786,11 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
                         tc_st16(ta, o);
                     }
                 }
+                // the next chunk's S buffer, tested without waiting while this
+                // chunk's weights are handed over (a phase not yet complete is
+                // waited for at the next chunk as before)
+                s_seen = __all_sync(0xffffffffu, mbar_done(sbar(sFull, (gc + 1) % kTcSBufs),
+                                                           uint32_t((gc + 1) / kTcSBufs) & 1u));
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");   // P (and O) written
                 tc_fence_before();    // the tensor-memory accesses, before the hand-over
                 mbar_arrive(sbar(pFull, sb));
