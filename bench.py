@@ -73,7 +73,7 @@ TRAFFIC_RECORD = {
 # is the recorded one.
 NA3D_KERNEL_SOURCES = [os.path.join(ROOT, "rope_rope3d_apply_gb300", "csrc", "rope3d_na3d.cu")]
 NA3D_TRAFFIC_RECORD = {
-    "kernel_source": "955cdc7de1091d2f",
+    "kernel_source": "3beb48028a0ef549",
     "kernel": "rope3d_na3d_tc_kernel<2>",
     "workload": {"B": 1, "T": 16, "H": 64, "W": 64, "heads": 16, "kernel": (3, 7, 7)},
     "dram_read_bytes": 805_516_544,

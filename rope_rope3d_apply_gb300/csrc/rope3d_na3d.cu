@@ -794,12 +794,12 @@ __global__ void __launch_bounds__(kRotThreads, 3) rope3d_na3d_rotate_k_kernel(co
 //     issuing threads keep either kind of product from waiting behind the
 //     other's inputs; S(c + 1) and S(c + 2) run while the softmax of chunk c
 //     does;
-//   warps 4-7: each query block's Q tile, read from global memory into
-//     registers (and rotated there in the rotating modes) while the previous
-//     block still uses the other Q buffer, then written into its own in the
-//     swizzled layout; each block's O, normalised, through its spent Q buffer
-//     and two TMA stores; in the mode that rotates K per CTA, each K tile
-//     too, in place once it lands;
+//   warps 4-7: each query block's Q tile, copied by TMA into its Q buffer
+//     while the previous block still uses the other (and rotated in place in
+//     the rotating modes); each block's descriptor for the softmax, a block
+//     ahead; each block's O, normalised, through its spent Q buffer and two
+//     TMA stores; in the mode that rotates K per CTA, each K tile too, in
+//     place once it lands;
 //   warps 8-15: the softmax. Each query row's S is read back from tensor
 //     memory by two threads (half of the chunk's columns each, in one batch of
 //     loads: warps w and w + 4 share the 32 lanes of tensor memory that warp w
@@ -1432,14 +1432,14 @@ rope3d_na3d_tc_kernel(const NAParams p, const TcShape shp, const __grid_constant
             }
         }
     } else if (warp < kTcSoftWarp0) {   // warps 4-7
-        // ---- Q warps: each block's Q tile, read from global memory (and, in
-        // the rotating modes, rotated) into Q buffer k & 1 in the layout of a
-        // 128-byte-swizzled TMA box, while the previous block still runs on the
-        // other buffer; in the mode that rotates K per CTA, each K tile too, in
-        // place once it lands.
-        // Thread rt holds 16-byte vector cv = rt % 16 of query rows
-        // rt / 16 + 8 i, i = 0 .. 15: a row is (t, h, w) = (i / 8, i % 8, rt / 16)
-        // from the block's corner, so a warp reads two tokens' 256 bytes.
+        // ---- Q warps: each block's Q tile copied by TMA into Q buffer k & 1
+        // (128-byte-swizzled box layout) while the previous block still runs on
+        // the other buffer, and in the rotating modes rotated there in place;
+        // each block's descriptor for the softmax threads, a block ahead; in the
+        // mode that rotates K per CTA, each K tile too, in place once it lands.
+        // For the rotation, thread rt holds 16-byte vector cv = rt % 16 of query
+        // rows rt / 16 + 8 i, i = 0 .. 15: a row is (t, h, w) = (i / 8, i % 8,
+        // rt / 16) from the block's corner.
         // They also write each block's result: once its last P V is done and
         // the softmax threads have left their row sums, each thread takes the
         // row of tensor memory lane 32 (warp % 4) + lane (the lanes its warp
