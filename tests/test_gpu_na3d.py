@@ -62,6 +62,8 @@ CASES = [
     ((2, 4, 13, 11, 3), (16, 56, 56), (3, 5, 7)),      # two batches, three heads, odd grid, split
     ((2, 3, 9, 10, 2), (32, 48, 48), (3, 5, 5)),       # two batches, odd T: the last frame pair of
                                                         # batch 0 must not reach batch 1's first frame
+    ((1, 1, 8, 8, 608), (32, 48, 48), (1, 3, 3)),      # 608 one-chunk blocks: four per CTA in turn
+    ((1, 3, 8, 16, 96), (32, 48, 48), (3, 5, 5)),      # 384 blocks of one and two frames, several per CTA
 ]
 
 
