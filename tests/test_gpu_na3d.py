@@ -64,6 +64,8 @@ CASES = [
                                                         # batch 0 must not reach batch 1's first frame
     ((1, 1, 8, 8, 608), (32, 48, 48), (1, 3, 3)),      # 608 one-chunk blocks: four per CTA in turn
     ((1, 3, 8, 16, 96), (32, 48, 48), (3, 5, 5)),      # 384 blocks of one and two frames, several per CTA
+    ((1, 2, 40, 24, 80), (32, 48, 48), (1, 7, 7)),     # 1,200 blocks: each CTA meets more window
+                                                        # geometries than it keeps mask sets for
 ]
 
 
