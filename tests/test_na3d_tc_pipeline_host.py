@@ -72,7 +72,7 @@ class Bar:
         return self.phase >= want_phase + 1
 
 
-def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
+def simulate(blocks, rot_q, rot_k, seed, sbufs=3, drop_o_wait=False):
     """blocks: the chunk count of each query block the CTA walks in turn;
     sbufs: S buffers (3 with one O buffer, 2 with two)."""
     obufs = 1 if sbufs == 3 else 2
@@ -152,7 +152,7 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
 
     def q_warp(i):
         g = 0
-        ws = {"qb": 0, "ost": [0, 0], "pending": None}
+        ws = {"qb": 0, "ost": [0, 0], "ost_n": [0, 0], "pending": None}
         for k, n in enumerate(blocks):
             if k >= 2:                 # the softmax threads have read block k - 2's descriptor
                 yield ("wait", B["dEmpty", k & 1], ((k - 2) >> 1) & 1, (k - 2) >> 1)
@@ -180,7 +180,7 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
                     B["qReady", k & 1].arrive()
             if k >= 1:                 # the previous block's result, before this block's K tiles
                 yield from store_o(i, k - 1, ws)
-            for c in range(n):
+            for c in range(n):         # K tiles: only the per-CTA mode has work here
                 if rot_k:
                     s, use = g & 1, g >> 1
                     yield ("wait", B["kFull", s], use & 1, use)
@@ -189,14 +189,15 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
                         state["K"][s] = (g, "rot")
                     for _ in range(32):
                         B["kReady", s].arrive()
+                    yield None
                 g += 1
-                yield None
         yield from store_o(i, len(blocks) - 1, ws)
-        if i == 0:                     # the last store, before the CTA ends
-            b = ws["pending"] & 1
-            u = ws["ost"][b]
-            ws["ost"][b] += 1
-            yield ("wait", B["ostore", b], u & 1, u)
+        if i == 0:                     # every store still out (a bulk-group wait), before the CTA ends
+            for b in (0, 1):
+                while ws["ost"][b] < ws["ost_n"][b]:
+                    u = ws["ost"][b]
+                    ws["ost"][b] += 1
+                    yield ("wait", B["ostore", b], u & 1, u)
 
     def qbar(ws):                      # bar.sync among the four Q warps
         B["qbar"].arrive()
@@ -210,7 +211,8 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
             if i == 0:                 # the thread that committed the store waits for its reads
                 u = ws["ost"][b]
                 ws["ost"][b] += 1
-                yield ("wait", B["ostore", b], u & 1, u)
+                if not drop_o_wait:
+                    yield ("wait", B["ostore", b], u & 1, u)
             yield from qbar(ws)
             ws["pending"] = None
 
@@ -236,6 +238,7 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
         if i == 0:
             assert state["staged"][b] == 4, "the store reads all rows"
             inflight.append(("tmao", (k,)))
+            ws["ost_n"][b] += 1
         ws["pending"] = k
 
     def softmax(i):
@@ -297,6 +300,10 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3):
             else:   # each issuer's MMAs complete in its issue order
                 first = [next((j for j, kd in enumerate(kinds) if kd == want), None) for want in ("s", "pv")]
                 idx = rng.choice([j for j in first if j is not None])
+            # a TMA store of a whole O tile takes long next to the Q warps' own
+            # steps: it completes only now and then while anything else can move
+            if kinds[idx] == "tmao" and runnable and rng.random() < 0.9:
+                continue
             kind, pl = inflight.pop(idx)
             if kind == "tmaq":
                 (kk,) = pl
@@ -371,3 +378,17 @@ BLOCKS = [[1], [3], [8], [1, 1, 1], [3, 2, 4], [8, 8, 6, 8], [2, 5, 1, 7, 3], [1
 def test_pipeline_protocol(blocks, mode, sbufs):
     for seed in range(40):
         simulate(blocks, mode != "none", mode == "qk", seed * 7919 + len(blocks), sbufs)
+
+
+@pytest.mark.parametrize("blocks", [[3, 2, 4], [8, 8, 6, 8]], ids=str)
+def test_protocol_model_catches_a_dropped_wait(blocks):
+    """A planted mistake: the Q warps copy the next Q tile into a buffer
+    without waiting for the TMA store of the O staged there to have read it.
+    Some interleaving must then find the buffer overwritten under the store."""
+    messages = set()
+    for seed in range(40):
+        try:
+            simulate(blocks, True, False, seed, 3, drop_o_wait=True)
+        except AssertionError as e:
+            messages.add(str(e).split("\n")[0])
+    assert any("staged" in m_ for m_ in messages), messages
