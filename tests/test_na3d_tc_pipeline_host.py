@@ -72,7 +72,7 @@ class Bar:
         return self.phase >= want_phase + 1
 
 
-def simulate(blocks, rot_q, rot_k, seed, sbufs=3, drop_o_wait=False):
+def simulate(blocks, rot_q, rot_k, seed, sbufs=3, drop_o_wait=False, drop=(), slow_q=False):
     """blocks: the chunk count of each query block the CTA walks in turn;
     sbufs: S buffers (3 with one O buffer, 2 with two)."""
     obufs = 1 if sbufs == 3 else 2
@@ -95,6 +95,8 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3, drop_o_wait=False):
     for b in (0, 1):         # per block descriptor (block parity): written, read
         B["dFull", b], B["dEmpty", b] = Bar(128), Bar(256)
     B["qbar"] = Bar(4)       # the Q warps' named barrier (one arrival per modelled warp)
+    for key, bar_ in B.items():   # planted mistakes: waits on these barriers are skipped
+        bar_.dropped = (key[0] if isinstance(key, tuple) else key) in drop
     state = {  # what each buffer holds; S buffer b holds ("S", g) then ("P", g)
         "K": [None, None], "V": [None, None], "S": [None] * sbufs,
         "Q": [None, None],             # Q buffer: (block, "rot" or "raw") of the tile in it
@@ -247,7 +249,8 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3, drop_o_wait=False):
             m_valid = False
             ob = k % obufs
             yield ("wait", B["dFull", k & 1], (k >> 1) & 1, k >> 1)
-            assert state["desc"][k & 1][0] == k, "the softmax reads its block's descriptor"
+            assert state["desc"][k & 1] is not None and state["desc"][k & 1][0] == k, \
+                "the softmax reads its block's descriptor"
             state["desc"][k & 1][1] += 1
             for _ in range(256 // SOFT):
                 B["dEmpty", k & 1].arrive()
@@ -282,6 +285,7 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3, drop_o_wait=False):
 
     roles = [producer("k"), producer("v"), s_issuer(), pv_issuer()] + [softmax(i) for i in range(SOFT)] + \
         [q_warp(i) for i in range(4)]
+    n_fast = len(roles) - 4   # the roles before the Q warps
     waiting = [None] * len(roles)
     done = [False] * len(roles)
     steps = 0
@@ -357,12 +361,17 @@ def simulate(blocks, rot_q, rot_k, seed, sbufs=3, drop_o_wait=False):
             continue
         assert runnable, "deadlock"
         i = rng.choice(runnable)
+        if slow_q and i >= n_fast and rng.random() < 0.9:   # the Q warps run rarely
+            fast = [j for j in runnable if j < n_fast]
+            if fast:
+                i = rng.choice(fast)
         waiting[i] = None
         try:
             ev = next(roles[i])
             if ev is not None:
                 _, bar, parity, phase = ev
-                waiting[i] = (bar, parity, phase)
+                if not bar.dropped:
+                    waiting[i] = (bar, parity, phase)
         except StopIteration:
             done[i] = True
     assert not inflight
@@ -392,3 +401,28 @@ def test_protocol_model_catches_a_dropped_wait(blocks):
         except AssertionError as e:
             messages.add(str(e).split("\n")[0])
     assert any("staged" in m_ for m_ in messages), messages
+
+
+@pytest.mark.parametrize("wait", ["sEmpty", "oEmpty", "kEmpty", "vEmpty", "dFull", "sFull", "pFull", "oFull"])
+def test_protocol_model_catches_each_dropped_wait(wait):
+    """Planted mistakes: every wait on one kind of barrier skipped. Some
+    interleaving (the Q warps running slowly in half of them) must then fail
+    one of the model's assertions."""
+    failed = 0
+    for seed in range(40):
+        try:
+            simulate([3, 2, 4, 1, 2], True, False, seed, 3, drop=(wait,), slow_q=seed % 2 == 1)
+        except AssertionError:
+            failed += 1
+    assert failed > 0
+
+
+@pytest.mark.parametrize("wait", ["dEmpty", "qEmpty"])
+def test_protocol_waits_implied_by_the_o_hand_over(wait):
+    """Two waits of the Q warps are implied by an earlier one: before block
+    k's descriptor and Q tile go into slot and buffer k & 1, the Q warps have
+    stored block k - 2's O, which waited for its last P V (after all its S
+    products) and for all its softmax row sums (after every softmax thread read
+    its descriptor). Dropping either changes nothing, even with slow Q warps."""
+    for seed in range(40):
+        simulate([3, 2, 4, 1, 2], True, False, seed, 3, drop=(wait,), slow_q=seed % 2 == 1)
